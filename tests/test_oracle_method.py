@@ -1,0 +1,303 @@
+"""Pins for the oracle's rotation, quantizer, QJL estimator, packing and attention."""
+
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy import stats
+
+import oracle
+from oracle import turboquant as tq
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+D = 128
+
+
+@pytest.fixture(scope="module")
+def p3():
+    return oracle.make_params(d=D, m=128, k_bits=(3, 3), v_bits=(3, 3), seed=0)
+
+
+# --- rotation ---------------------------------------------------------------
+
+def test_rotation_is_orthogonal(p3):
+    Pi = p3.Pi
+    assert np.max(np.abs(Pi.T @ Pi - np.eye(D))) < 1e-12
+    assert np.max(np.abs(Pi @ Pi.T - np.eye(D))) < 1e-12
+
+
+def test_rotation_is_the_positive_diagonal_qr_factor(p3):
+    g = oracle.gaussian_stream(0, 1, D * D).reshape(D, D)
+    R = p3.Pi.T @ g
+    assert np.max(np.abs(np.tril(R, -1))) < 1e-11
+    assert np.all(np.diag(R) > 0)
+    assert np.allclose(p3.Pi[:, 0], g[:, 0] / np.linalg.norm(g[:, 0]), atol=1e-14)
+
+
+def test_rotation_spreads_coordinates_like_the_sphere():
+    """Over seeds, coordinates of Pi e_1 have std 1/sqrt(d) and kurtosis 3d/(d+2)."""
+    d = 32
+    vals = np.concatenate([oracle.rotation_matrix(d, s)[:, 0] for s in range(400)])
+    assert abs(vals.std() * math.sqrt(d) - 1.0) < 0.03
+    kurt = stats.kurtosis(vals, fisher=False)
+    assert abs(kurt - 3.0 * d / (d + 2)) < 0.12
+    # heavy outlier channels are flattened: kurtosis of a spiky vector before/after rotation
+    x = np.zeros(128)
+    x[:4] = 10.0
+    x[4:] = np.random.default_rng(0).standard_normal(124)
+    y = oracle.rotation_matrix(128, 1) @ x
+    assert stats.kurtosis(x, fisher=False) > 10 and stats.kurtosis(y, fisher=False) < 4.5
+
+
+# --- quantizer --------------------------------------------------------------
+
+def _unit_vectors(n, d, seed):
+    x = np.random.default_rng(seed).standard_normal((n, d))
+    return x / np.linalg.norm(x, axis=1, keepdims=True)
+
+
+def test_two_over_pi_shrinkage_one_bit():
+    """MSE-only 1-bit: E<q, x^>/<q, x> = sqrt(d) sqrt(2/pi) Gamma(d/2) / (sqrt(pi) Gamma((d+1)/2))."""
+    p = oracle.make_params(d=D, k_bits=(1, 1), v_bits=(1, 1), seed=3, k_qjl=False)
+    closed = math.sqrt(D) * math.sqrt(2 / math.pi) * math.exp(
+        math.lgamma(D / 2) - math.lgamma((D + 1) / 2)) / math.sqrt(math.pi)
+    assert abs(closed - 0.637864) < 1e-6 and abs(closed - 2 / math.pi) < 2e-3
+    X = _unit_vectors(100000, D, 5)
+    q = oracle.quantize_vectors(p, X, "v")
+    Xhat = tq.dequantize_values(p, {"codes": q["codes"], "n16": np.linalg.norm(X, axis=1)}) @ p.Pi
+    ratio = np.sum(X * Xhat, axis=1)          # <x, x^> / ||x||^2 with ||x|| = 1
+    se = ratio.std() / math.sqrt(ratio.size)
+    assert abs(ratio.mean() - closed) < 4 * se + 1e-12
+    # and with a general query: E<q, x^> = closed * <q, x> (linear in q)
+    qv = np.random.default_rng(6).standard_normal(D)
+    num = Xhat @ qv
+    den = X @ qv
+    slope = np.sum(num * den) / np.sum(den * den)
+    assert abs(slope - closed) < 0.01
+
+
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_distortion_per_bit(bits):
+    """||x - x^||^2 / ||x||^2 on random unit vectors tracks the Gaussian Lloyd-Max MSE."""
+    p = oracle.make_params(d=D, k_bits=(bits, bits), v_bits=(bits, bits), seed=2, k_qjl=False)
+    X = _unit_vectors(4000, D, bits)
+    q = oracle.quantize_vectors(p, X, "v")
+    Yhat = tq.dequantize_values(p, {"codes": q["codes"], "n16": np.ones(len(X))})
+    err = np.sum((q["y"] - Yhat) ** 2, axis=1).mean()
+    gauss = p.books[bits].mse()
+    assert abs(err / gauss - 1.0) < 0.03
+    assert 4.0 ** -bits <= err <= math.sqrt(3) * math.pi / 2 * 4.0 ** -bits
+
+
+def test_codes_follow_boundaries_and_tie_rounds_up(p3):
+    cb = p3.books[3]
+    # craft a vector whose rotated unit-variance coordinates are chosen exactly
+    u = np.linspace(-3, 3, D)
+    u[0] = cb.boundaries[2]         # exactly on a boundary -> upper cell
+    u[1] = np.nextafter(cb.boundaries[2], -np.inf)
+    y = u / np.linalg.norm(u)       # ||x|| = 1 -> u = sqrt(d) y exactly up to rounding
+    x = p3.Pi.T @ y
+    q = oracle.quantize_vectors(p3, x[None, :], "v")
+    uu = q["u"][0]
+    expect = np.searchsorted(cb.boundaries, uu, side="right")
+    assert np.array_equal(q["codes"][0], expect)
+    assert np.all((q["codes"] >= 0) & (q["codes"] < 8))
+
+
+def test_zero_vector(p3):
+    q = oracle.quantize_vectors(p3, np.zeros((1, D)), "k")
+    assert np.all(q["codes"] == 4)                      # u = 0 sits on the middle boundary -> upper
+    assert q["n16"][0] == 0 and q["rho16"][0] == 0
+    assert np.all(q["signs"] == 1)                      # S * 0 = 0 -> sign bit set
+
+
+def test_two_stage_estimator_is_unbiased():
+    """Mean over many Gaussian projections of the stage-2 estimate equals <q, x> exactly."""
+    rng = np.random.default_rng(11)
+    p = oracle.make_params(d=D, m=128, k_bits=(2, 2), v_bits=(2, 2), seed=4)
+    x = rng.standard_normal(D)
+    x[:4] *= 10
+    qv = rng.standard_normal(D)
+    q = oracle.quantize_vectors(p, x[None, :], "k")
+    r = q["r"][0]
+    rho = float(np.linalg.norm(r))
+    qt = p.Pi @ qv
+    exact = float(qv @ x)
+    n_draws = 2000
+    est = np.empty(n_draws)
+    mse_only = None
+    for i in range(n_draws):
+        S = rng.standard_normal((p.m, D))
+        pp = tq.TQParams(**{**p.__dict__, "S": S})
+        z = S @ r
+        rec = {"codes": q["codes"], "n16": q["n16"], "signs": (z >= 0).astype(np.uint8)[None, :],
+               "rho16": np.array([rho])}
+        est[i] = tq.estimate_scores(pp, qt, S @ qt, rec)[0]
+        if mse_only is None:
+            pq = tq.TQParams(**{**p.__dict__, "k_qjl": False})
+            mse_only = tq.estimate_scores(pq, qt, None, rec)[0]
+    var = ((math.pi / 2) * (qt @ qt) * rho ** 2 - (qt @ r) ** 2) / p.m
+    z = (est.mean() - exact) / math.sqrt(var / n_draws)
+    assert abs(z) < 4.5
+    assert abs(est.var() / var - 1) < 0.15
+    # stage 1 alone misses exactly the residual term <qt, r>
+    assert abs(mse_only + qt @ r - exact) < 1e-9
+
+
+# --- packing and the paged cache -------------------------------------------
+
+def test_pack_hand_example():
+    with open(os.path.join(GOLDEN, "pack_b3_codes_0to7.txt")) as f:
+        want = [int(t, 16) for ln in f if not ln.startswith("#") for t in ln.split()]
+    p = oracle.make_params(d=D, k_bits=(3, 3), v_bits=(3, 3), seed=0)
+    codes = np.zeros((1, D), dtype=np.int64)
+    codes[0, :8] = np.arange(8)
+    raw = tq._pack_codes(p, codes, "v")
+    assert raw[0, :3].tolist() == want and raw.shape == (1, 48)
+
+
+@pytest.mark.parametrize("kb,vb", [((3, 3), (3, 3)), ((4, 3), (4, 3)), ((3, 2), (3, 2)), ((1, 1), (2, 4))])
+def test_pack_is_little_endian_integer(kb, vb):
+    p = oracle.make_params(d=D, k_bits=kb, v_bits=vb, seed=0)
+    rng = np.random.default_rng(1)
+    for kind in ("k", "v"):
+        cb = p.channel_bits(kind)
+        codes = np.stack([rng.integers(0, 1 << int(b), size=5) for b in cb], axis=1)
+        raw = tq._pack_codes(p, codes, kind)
+        for row in range(5):
+            acc, off = 0, 0
+            for j in range(D):
+                acc |= int(codes[row, j]) << off
+                off += int(cb[j])
+            assert bytes(raw[row]) == acc.to_bytes(off // 8, "little")
+        assert np.array_equal(tq._unpack_codes(p, raw, kind), codes)
+
+
+def test_sign_bit_order(p3):
+    signs = np.zeros((1, 128), dtype=np.uint8)
+    signs[0, [0, 9, 127]] = 1
+    rec = oracle.pack_k_records(p3, {"codes": np.zeros((1, D), dtype=np.int64), "n16": np.ones(1),
+                                     "signs": signs, "rho16": np.ones(1)})
+    w = rec["signs"][0].view("<u4")
+    assert w.tolist() == [1 | (1 << 9), 0, 0, 1 << 31]
+
+
+@pytest.mark.parametrize("kb,vb,kbytes,vbytes", [((3, 3), (3, 3), 1088, 800), ((4, 3), (4, 3), 1216, 928),
+                                                  ((3, 2), (3, 2), 960, 672)])
+def test_block_sizes(kb, vb, kbytes, vbytes):
+    """Per token-head: 3-bit 68+50 B, 3.5-bit 76+58 B, 2.5-bit 60+42 B; 16 slots per block."""
+    p = oracle.make_params(d=D, k_bits=kb, v_bits=vb, seed=0)
+    assert oracle.cache_block_bytes(p, "k") == kbytes and oracle.cache_block_bytes(p, "v") == vbytes
+
+
+def test_paged_roundtrip_through_permuted_block_table(p3):
+    rng = np.random.default_rng(2)
+    B, H, T = 3, 2, 37
+    maxp = 4
+    perm = rng.permutation(B * maxp)
+    bt = perm.reshape(B, maxp).astype(np.int32)
+    X = rng.standard_normal((B, T, H, D))
+    q = oracle.quantize_vectors(p3, X.reshape(-1, D), "k")
+    rec = oracle.pack_k_records(p3, q)
+    bb = oracle.cache_block_bytes(p3, "k")
+    cache = np.zeros(B * maxp * H * bb, dtype=np.uint8)
+    bi, ti, hi = np.meshgrid(np.arange(B), np.arange(T), np.arange(H), indexing="ij")
+    pages = bt[bi.ravel(), ti.ravel() // 16]
+    slots = ti.ravel() % 16
+    oracle.write_paged(p3, "k", cache, rec, pages, slots, hi.ravel(), H)
+    back = oracle.read_paged(p3, "k", cache, pages, slots, hi.ravel(), H)
+    for k in rec:
+        assert np.array_equal(np.asarray(back[k]).view(np.uint8), np.asarray(rec[k]).view(np.uint8))
+    # the byte address of one field follows the block layout by hand
+    b, t, h = 2, 21, 1
+    page = bt[b, t // 16]
+    off = page * H * bb + h * bb + 16 * 48 + 16 * 16 + (t % 16) * 2
+    n16 = np.frombuffer(cache[off:off + 2].tobytes(), dtype=np.float16)[0]
+    assert n16 == np.float16(q["n16"][(b * T + t) * H + h])
+
+
+# --- attention ----------------------------------------------------------------
+
+def _records(p, K, V):
+    return (oracle.unpack_k_records(p, oracle.pack_k_records(p, oracle.quantize_vectors(p, K, "k"))),
+            oracle.unpack_v_records(p, oracle.pack_v_records(p, oracle.quantize_vectors(p, V, "v"))))
+
+
+def test_attention_single_token_returns_dequantized_value(p3):
+    rng = np.random.default_rng(3)
+    K, V, qv = rng.standard_normal((1, D)), rng.standard_normal((1, D)), rng.standard_normal(D)
+    kr, vr = _records(p3, K, V)
+    o = tq.attend_one(p3, qv, kr, vr, 1 / math.sqrt(D))
+    vq = oracle.quantize_vectors(p3, V, "v")
+    want = p3.Pi.T @ (vq["n16"][0] / math.sqrt(D) * p3.books[3].centroids[vq["codes"][0]])
+    assert np.allclose(o, want, atol=1e-14)
+
+
+def test_attention_identical_keys_average_values(p3):
+    rng = np.random.default_rng(4)
+    K = np.repeat(rng.standard_normal((1, D)), 17, axis=0)
+    V = rng.standard_normal((17, D))
+    kr, vr = _records(p3, K, V)
+    o = tq.attend_one(p3, rng.standard_normal(D), kr, vr, 1 / math.sqrt(D))
+    want = p3.Pi.T @ tq.dequantize_values(p3, vr).mean(axis=0)
+    assert np.allclose(o, want, atol=1e-13)
+
+
+def test_attention_token_order_does_not_matter(p3):
+    rng = np.random.default_rng(5)
+    K, V, qv = rng.standard_normal((17, D)), rng.standard_normal((17, D)), rng.standard_normal(D)
+    kr, vr = _records(p3, K, V)
+    perm = rng.permutation(17)
+    o1 = tq.attend_one(p3, qv, kr, vr, 0.1)
+    o2 = tq.attend_one(p3, qv, {k: v[perm] for k, v in kr.items()}, {k: v[perm] for k, v in vr.items()}, 0.1)
+    assert np.allclose(o1, o2, atol=1e-13)
+
+
+@pytest.mark.parametrize("qjl", [False, True])
+@pytest.mark.parametrize("n", [2, 3, 17, 64])
+def test_attention_approaches_exact_attention_with_more_bits(n, qjl):
+    """The quantized path converges to textbook fp64 attention as bits grow.
+
+    At 8 bits the per-coordinate error is about sqrt(2.7 * 4**-8) ~ 6e-3 of the
+    coordinate scale, so the output must agree to ~1% RMS; each extra pair of bits
+    must shrink the error, and 1-bit codes must be visibly worse.
+    """
+    rng = np.random.default_rng(n)
+    K, V, qv = rng.standard_normal((n, D)), rng.standard_normal((n, D)), rng.standard_normal(D)
+    ref = oracle.exact_attention(qv, K, V, 1 / math.sqrt(D))
+    errs = {}
+    for bits in (1, 2, 4, 8):
+        p = oracle.make_params(d=D, m=128, k_bits=(bits, bits), v_bits=(bits, bits), seed=6, k_qjl=qjl)
+        kr, vr = _records(p, K, V)
+        o = tq.attend_one(p, qv, kr, vr, 1 / math.sqrt(D))
+        errs[bits] = np.linalg.norm(o - ref) / np.linalg.norm(ref)
+    assert errs[8] < 1.5e-2
+    assert errs[8] < errs[4] < errs[2]
+    assert errs[1] > 0.1
+
+
+def test_decode_attention_gqa_and_paging(p3):
+    rng = np.random.default_rng(7)
+    B, Hq, Hk, maxp = 2, 4, 2, 3
+    lens = np.array([37, 5])
+    bt = rng.permutation(B * maxp).reshape(B, maxp).astype(np.int32)
+    kbb, vbb = oracle.cache_block_bytes(p3, "k"), oracle.cache_block_bytes(p3, "v")
+    kc = np.zeros(B * maxp * Hk * kbb, np.uint8)
+    vc = np.zeros(B * maxp * Hk * vbb, np.uint8)
+    Ks, Vs = {}, {}
+    for b in range(B):
+        for h in range(Hk):
+            K = rng.standard_normal((lens[b], D))
+            V = rng.standard_normal((lens[b], D))
+            Ks[b, h], Vs[b, h] = K, V
+            pages, slots = tq.token_locations(bt, b, np.arange(lens[b]))
+            heads = np.full(lens[b], h)
+            oracle.write_paged(p3, "k", kc, oracle.pack_k_records(p3, oracle.quantize_vectors(p3, K, "k")), pages, slots, heads, Hk)
+            oracle.write_paged(p3, "v", vc, oracle.pack_v_records(p3, oracle.quantize_vectors(p3, V, "v")), pages, slots, heads, Hk)
+    Q = rng.standard_normal((B, Hq, D))
+    out = oracle.decode_attention(p3, Q, lens, bt, kc, vc, Hk)
+    for b in range(B):
+        for h in range(Hq):
+            kr, vr = _records(p3, Ks[b, h // 2], Vs[b, h // 2])
+            assert np.allclose(out[b, h], tq.attend_one(p3, Q[b, h], kr, vr, 1 / math.sqrt(D)), atol=1e-13)
