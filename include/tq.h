@@ -1,0 +1,164 @@
+/*
+ * tq.h -- C ABI of the GB300 (sm_103a) TurboQuant-style online KV-cache
+ * quantizer and decode-attention library (libtq.so).
+ *
+ * Method sources (web pages, cited by title and section):
+ *   [P2] "생각정리 209 (TurboQuant)", uiyeonassociation.blogspot.com: the
+ *        two-stage method (rotation + codebook, then QJL on the residual).
+ *   [P4] "[LLM Serving] TurboQuant란 무엇이며, 어떻게 KV Cache 양자화로 메모리를
+ *        5배 줄일 수 있을까?", riverfrot.github.io: §2.2 attention, §2.4 KV
+ *        size, §3.1 paged blocks, §4.1 rotation, §4.2 Lloyd-Max, §4.3 QJL.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named "device" must be CUDA device pointers on the current
+ *     device; "host" pointers are ordinary CPU memory.  The library never
+ *     takes ownership of caller memory.
+ *   - Quantize and decode are stream-ordered on `stream` (0 = legacy default
+ *     stream), allocate nothing and never synchronise the host.
+ *   - Argument errors are reported synchronously (TQ_ERR_INVALID_ARG) and
+ *     launch nothing.  Launch failures return TQ_ERR_CUDA.
+ *   - Corrupt device-side inputs (a page id outside [0, num_pages), a position
+ *     beyond the block table, a sequence length beyond max_seq_len) are never
+ *     dereferenced: the affected token is skipped and a bit is set in the
+ *     context's device error word, read back by tq_check_device_status().
+ *   - Every entry point returns a tq_status; tq_status_string() names it.
+ *
+ * Data layout (little-endian):
+ *   K/V inputs    [batch][n_new][num_kv_heads][d], bf16 or fp32, dense.
+ *   queries       [batch][num_q_heads][d], bf16 or fp32, dense.
+ *   output        [batch][num_q_heads][d], fp32.
+ *   block table   int32 [batch][max_pages_per_seq]: physical page of each
+ *                 16-token block of a sequence ([P4] §3.1).
+ *   caches        bytes; page p, KV head h starts at
+ *                 p * page_bytes + h * (page_bytes / num_kv_heads).
+ *   One (page, head) block of the K cache holds, for its 16 token slots:
+ *     codes[16][code_bytes_k] | signs[16][m/8] | norm fp16[16] | rnorm fp16[16]
+ *   and of the V cache:  codes[16][code_bytes_v] | norm fp16[16].
+ *   Codes of one vector form a little-endian bit stream: channel j (in the
+ *   rotated basis) takes bits [off_j, off_j + b_j), b_j = bits_hi for
+ *   j < split else bits_lo, off_j = sum of b over earlier channels, least
+ *   significant code bit first.  Code values are 0-based, ascending with the
+ *   centroid.  QJL sign i is bit i%8 of byte i/8 (1 = projection >= 0).
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_ARG = 1,   /* bad pointer, size or configuration */
+  TQ_ERR_CUDA = 2,          /* a CUDA runtime call or launch failed */
+  TQ_ERR_OOM = 3,           /* tq_create could not allocate its tables */
+  TQ_ERR_UNSUPPORTED = 4,   /* valid but not implemented (e.g. d != 128) */
+  TQ_ERR_DEVICE_CHECK = 5,  /* a kernel skipped out-of-range device input */
+  TQ_ERR_WORKSPACE = 6      /* workspace too small for the requested call */
+} tq_status;
+
+typedef enum { TQ_BF16 = 0, TQ_F32 = 1 } tq_dtype;
+
+/* Method configuration.  d = 128 and page_size = 16 are the supported
+ * values.  Bits per channel in [1, 4]; channels [0, split) of the rotated
+ * vector use bits_hi, channels [split, d) bits_lo; split is a multiple of 32.
+ * m (QJL projections) is a multiple of 32 in [32, 128].  k_qjl = 0 gives
+ * MSE-only keys (no signs, no residual norm stored). */
+typedef struct {
+  int d, m, page_size;
+  int k_bits_hi, k_bits_lo, k_split;
+  int v_bits_hi, v_bits_lo, v_split;
+  int k_qjl;
+  uint64_t seed;
+} tq_config;
+
+typedef struct tq_ctx tq_ctx;   /* opaque; immutable after creation */
+
+/* Fill `cfg` with d = 128, page_size = 16, b bits on every channel for keys
+ * and values, QJL on keys with m projections, and `seed`. */
+tq_status tq_config_init(tq_config* cfg, int d, int b, int m, uint64_t seed);
+
+/* Build the context on the current device ([P4] §4.1-§4.3): the random
+ * rotation Pi (Householder QR of a d x d Gaussian, positive R diagonal), the
+ * QJL matrix S (m x d Gaussian) and the Gaussian Lloyd-Max codebooks, drawn
+ * from the SplitMix64/Box-Muller streams 1 and 2 of `seed`.  The only call
+ * that allocates device memory (about 0.5 MB) and the only one that copies
+ * host to device.  `*out` receives the context; free it with tq_destroy. */
+tq_status tq_create(int d, int b, int m, uint64_t seed, tq_ctx** out);
+tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out);
+tq_status tq_destroy(tq_ctx* ctx);
+tq_status tq_get_config(const tq_ctx* ctx, tq_config* cfg);
+
+/* Bytes of one cache page (16 tokens x num_kv_heads) for K and for V.  A
+ * cache of P pages is P * page_bytes; per-head blocks are page_bytes/H. */
+tq_status tq_cache_layout(const tq_ctx* ctx, int num_kv_heads,
+                          size_t* k_page_bytes, size_t* v_page_bytes);
+
+/* Host-only copies of the tables tq_create builds (no GPU needed).
+ * pi: d*d doubles, row-major (y = Pi x).  s: m*d doubles, row-major.
+ * centroids: 2^bits doubles ascending; boundaries: 2^bits - 1 doubles. */
+tq_status tq_host_rotation(int d, uint64_t seed, double* pi);
+tq_status tq_host_qjl(int m, int d, uint64_t seed, double* s);
+tq_status tq_host_codebook(int bits, double* centroids, double* boundaries);
+
+/* Online quantize-and-append ([P2] stages 1-2; [P4] §4.1-§4.3, §3.1).
+ * k, v (device): [batch][n_new][num_kv_heads][d] in `dtype`; either may be
+ * NULL to skip that cache.  Token t of sequence b is written at position
+ * start_pos[b] + t, i.e. page block_table[b*max_pages_per_seq + pos/16],
+ * slot pos%16.  start_pos, block_table: device int32.  num_pages bounds the
+ * page ids.  Per vector: y = Pi x; code_j = #{k : sqrt(d) y_j/||x|| >= t_k};
+ * norm = fp16(||x||); keys also get r = y - norm/sqrt(d) * c[code],
+ * sign bits of S r and fp16(||r||).  Codes and signs are decided exactly:
+ * a value the fp32 fast path finds close to a boundary is recomputed in
+ * fp64 before it is stored. */
+tq_status tq_quantize(const tq_ctx* ctx, const void* k, const void* v, tq_dtype dtype,
+                      int batch, int n_new, int num_kv_heads,
+                      const int32_t* start_pos, const int32_t* block_table,
+                      int max_pages_per_seq, int num_pages,
+                      void* k_cache, void* v_cache, void* stream);
+
+/* Workspace bytes tq_decode_attention needs for these sizes: the query
+ * projections and the split-K partials (max, sum, acc[d]) per chunk. */
+tq_status tq_workspace_size(const tq_ctx* ctx, int batch, int num_q_heads,
+                            int max_seq_len, int chunk_tokens, size_t* bytes);
+
+/* Decode attention over the compressed cache ([P4] §2.2, §4.3; [P2] stage 2).
+ * q (device): [batch][num_q_heads][d]; query head h reads KV head
+ * h / (num_q_heads / num_kv_heads).  seq_lens (device int32 [batch]) <=
+ * max_seq_len.  Score of cached key t: (norm_t/sqrt(d)) <Pi q, c[code_t]>
+ * + sqrt(pi/2)/m * rnorm_t * <S Pi q, +-1 signs_t>; weights are
+ * softmax(score * softmax_scale) (pass 1/sqrt(d) for the usual scale);
+ * out = Pi^T sum_t w_t (vnorm_t/sqrt(d)) c_v[code_t], fp32.  The context is
+ * split into chunks of chunk_tokens (a multiple of 16; 0 picks one) merged
+ * with a log-sum-exp reduction.  A sequence of length 0 yields zeros.
+ * workspace (device) of at least tq_workspace_size() bytes. */
+tq_status tq_decode_attention(const tq_ctx* ctx, const void* q, tq_dtype dtype,
+                              int batch, int num_q_heads, int num_kv_heads,
+                              const int32_t* seq_lens, int max_seq_len,
+                              const int32_t* block_table, int max_pages_per_seq, int num_pages,
+                              const void* k_cache, const void* v_cache,
+                              int chunk_tokens, float softmax_scale,
+                              float* out, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/* Synchronise the device and report (then clear) the context's device error
+ * word: TQ_OK, or TQ_ERR_DEVICE_CHECK with the bits in *flags (may be NULL):
+ * 1 = page id out of range, 2 = position beyond the block table,
+ * 4 = sequence length beyond max_seq_len or the block table. */
+tq_status tq_check_device_status(const tq_ctx* ctx, uint32_t* flags);
+
+/* Counters of near-boundary decisions the quantize kernels re-took in fp64
+ * since creation (or the last reset): out[0] codes, out[1] key vectors whose
+ * signs were re-taken.  Synchronises the device. */
+tq_status tq_refine_counters(const tq_ctx* ctx, unsigned long long out[2], int reset);
+
+const char* tq_status_string(tq_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H_ */

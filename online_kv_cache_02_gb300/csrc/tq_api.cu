@@ -1,0 +1,313 @@
+// C ABI entry points: context creation, argument checks, launches, status.
+#include "tq_internal.h"
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+using namespace tq;
+
+namespace {
+
+bool valid_bits(int b) { return b >= 1 && b <= 4; }
+
+tq_status check_config(const tq_config* c) {
+  if (!c) return TQ_ERR_INVALID_ARG;
+  if (c->d != kD || c->page_size != kPage) return TQ_ERR_UNSUPPORTED;
+  if (c->m < 32 || c->m > kMaxM || c->m % 32) return TQ_ERR_INVALID_ARG;
+  if (!valid_bits(c->k_bits_hi) || !valid_bits(c->k_bits_lo) || !valid_bits(c->v_bits_hi) ||
+      !valid_bits(c->v_bits_lo))
+    return TQ_ERR_INVALID_ARG;
+  if (c->k_split < 0 || c->k_split > c->d || c->k_split % 32) return TQ_ERR_INVALID_ARG;
+  if (c->v_split < 0 || c->v_split > c->d || c->v_split % 32) return TQ_ERR_INVALID_ARG;
+  if (c->k_qjl != 0 && c->k_qjl != 1) return TQ_ERR_INVALID_ARG;
+  return TQ_OK;
+}
+
+void fill_group(GroupBook& g, int bits) {
+  double c[256], t[256];
+  codebook_fill(bits, c, t);
+  g.bits = bits;
+  g.nb = (1 << bits) - 1;
+  for (int k = 0; k < 16; ++k) {
+    bool in_c = k < (1 << bits), in_t = k < g.nb;
+    g.c64[k] = in_c ? c[k] : 0.0;
+    g.c[k] = static_cast<float>(g.c64[k]);
+    g.t64[k] = in_t ? t[k] : INFINITY;
+    g.t[k] = in_t ? static_cast<float>(t[k]) : INFINITY;
+  }
+}
+
+void fill_layout(KindLayout& L, int bits_hi, int bits_lo, int split, int d, int m, bool key, bool qjl) {
+  fill_group(L.g[0], bits_hi);
+  fill_group(L.g[1], bits_lo);
+  L.split = split;
+  L.code_bytes = (split * bits_hi + (d - split) * bits_lo) / 8;
+  L.qjl = (key && qjl) ? 1 : 0;
+  int sign_bytes = L.qjl ? m / 8 : 0;
+  L.off_signs = kPage * L.code_bytes;
+  L.off_norm = L.off_signs + kPage * sign_bytes;
+  L.off_rnorm = L.off_norm + kPage * 2;
+  L.block_bytes = L.off_norm + kPage * 2 + (L.qjl ? kPage * 2 : 0);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int pick_chunk(int units, int max_seq_len) {
+  int sms = 152;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
+  }
+  long long target = 4LL * sms;
+  long long nch = (target + units - 1) / units;
+  if (nch < 1) nch = 1;
+  long long chunk = (max_seq_len + nch - 1) / nch;
+  chunk = ((chunk + 63) / 64) * 64;
+  if (chunk < 64) chunk = 64;
+  return static_cast<int>(chunk);
+}
+
+}  // namespace
+
+extern "C" tq_status tq_config_init(tq_config* cfg, int d, int b, int m, uint64_t seed) {
+  if (!cfg) return TQ_ERR_INVALID_ARG;
+  cfg->d = d;
+  cfg->m = m;
+  cfg->page_size = kPage;
+  cfg->k_bits_hi = cfg->k_bits_lo = b;
+  cfg->v_bits_hi = cfg->v_bits_lo = b;
+  cfg->k_split = cfg->v_split = d / 2;
+  cfg->k_qjl = 1;
+  cfg->seed = seed;
+  return check_config(cfg);
+}
+
+extern "C" tq_status tq_create(int d, int b, int m, uint64_t seed, tq_ctx** out) {
+  tq_config cfg;
+  tq_status st = tq_config_init(&cfg, d, b, m, seed);
+  if (st != TQ_OK) return st;
+  return tq_create_ex(&cfg, out);
+}
+
+extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
+  if (!out) return TQ_ERR_INVALID_ARG;
+  *out = nullptr;
+  tq_status st = check_config(cfg);
+  if (st != TQ_OK) return st;
+  const int d = cfg->d, m = cfg->m;
+  tq_ctx* ctx = new (std::nothrow) tq_ctx();
+  if (!ctx) return TQ_ERR_OOM;
+  ctx->cfg = *cfg;
+  if (cudaGetDevice(&ctx->device) != cudaSuccess) { delete ctx; return TQ_ERR_CUDA; }
+  fill_layout(ctx->kl, cfg->k_bits_hi, cfg->k_bits_lo, cfg->k_split, d, m, true, cfg->k_qjl != 0);
+  fill_layout(ctx->vl, cfg->v_bits_hi, cfg->v_bits_lo, cfg->v_split, d, m, false, false);
+
+  std::vector<double> pi(static_cast<size_t>(d) * d), s(static_cast<size_t>(m) * d);
+  rotation_fill(d, cfg->seed, pi.data());
+  qjl_fill(m, d, cfg->seed, s.data());
+  std::vector<float> pit(d * d), pif(d * d), st_(static_cast<size_t>(d) * m);
+  for (int i = 0; i < d; ++i)
+    for (int k = 0; k < d; ++k) {
+      pif[i * d + k] = static_cast<float>(pi[i * d + k]);
+      pit[k * d + i] = static_cast<float>(pi[i * d + k]);
+    }
+  for (int i = 0; i < m; ++i)
+    for (int j = 0; j < d; ++j) st_[static_cast<size_t>(j) * m + i] = static_cast<float>(s[i * d + j]);
+
+  size_t o_pit = 0;
+  size_t o_pi = align256(o_pit + sizeof(float) * d * d);
+  size_t o_pi64 = align256(o_pi + sizeof(float) * d * d);
+  size_t o_st = align256(o_pi64 + sizeof(double) * d * d);
+  size_t o_s64 = align256(o_st + sizeof(float) * d * m);
+  size_t o_err = align256(o_s64 + sizeof(double) * d * m);
+  size_t o_cnt = align256(o_err + sizeof(uint32_t));
+  size_t total = align256(o_cnt + 2 * sizeof(unsigned long long));
+  void* blk = nullptr;
+  if (cudaMalloc(&blk, total) != cudaSuccess) { delete ctx; cudaGetLastError(); return TQ_ERR_OOM; }
+  char* b = static_cast<char*>(blk);
+  ctx->dev_block = blk;
+  ctx->tab.pit = reinterpret_cast<float*>(b + o_pit);
+  ctx->tab.pi = reinterpret_cast<float*>(b + o_pi);
+  ctx->tab.pi64 = reinterpret_cast<double*>(b + o_pi64);
+  ctx->tab.st = reinterpret_cast<float*>(b + o_st);
+  ctx->tab.s64 = reinterpret_cast<double*>(b + o_s64);
+  ctx->tab.err = reinterpret_cast<uint32_t*>(b + o_err);
+  ctx->tab.counters = reinterpret_cast<unsigned long long*>(b + o_cnt);
+  bool ok = cudaMemcpy(ctx->tab.pit, pit.data(), sizeof(float) * d * d, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(ctx->tab.pi, pif.data(), sizeof(float) * d * d, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(ctx->tab.pi64, pi.data(), sizeof(double) * d * d, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(ctx->tab.st, st_.data(), sizeof(float) * d * m, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(ctx->tab.s64, s.data(), sizeof(double) * d * m, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemset(b + o_err, 0, total - o_err) == cudaSuccess;
+  if (!ok) { cudaFree(blk); delete ctx; cudaGetLastError(); return TQ_ERR_CUDA; }
+  *out = ctx;
+  return TQ_OK;
+}
+
+extern "C" tq_status tq_destroy(tq_ctx* ctx) {
+  if (!ctx) return TQ_ERR_INVALID_ARG;
+  cudaError_t e = cudaFree(ctx->dev_block);
+  delete ctx;
+  return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+extern "C" tq_status tq_get_config(const tq_ctx* ctx, tq_config* cfg) {
+  if (!ctx || !cfg) return TQ_ERR_INVALID_ARG;
+  *cfg = ctx->cfg;
+  return TQ_OK;
+}
+
+extern "C" tq_status tq_cache_layout(const tq_ctx* ctx, int num_kv_heads, size_t* kpb, size_t* vpb) {
+  if (!ctx || num_kv_heads < 1 || (!kpb && !vpb)) return TQ_ERR_INVALID_ARG;
+  if (kpb) *kpb = static_cast<size_t>(ctx->kl.block_bytes) * num_kv_heads;
+  if (vpb) *vpb = static_cast<size_t>(ctx->vl.block_bytes) * num_kv_heads;
+  return TQ_OK;
+}
+
+extern "C" tq_status tq_quantize(const tq_ctx* ctx, const void* k, const void* v, tq_dtype dtype,
+                                 int batch, int n_new, int H, const int32_t* start_pos,
+                                 const int32_t* block_table, int maxp, int num_pages, void* k_cache,
+                                 void* v_cache, void* stream) {
+  if (!ctx || (!k && !v) || batch < 0 || n_new < 0 || H < 1 || maxp < 1 || num_pages < 1)
+    return TQ_ERR_INVALID_ARG;
+  if (dtype != TQ_BF16 && dtype != TQ_F32) return TQ_ERR_INVALID_ARG;
+  if ((k && !k_cache) || (v && !v_cache)) return TQ_ERR_INVALID_ARG;
+  if (batch == 0 || n_new == 0) return TQ_OK;
+  if (!start_pos || !block_table) return TQ_ERR_INVALID_ARG;
+  if (static_cast<long long>(batch) * n_new * H > (1LL << 31) - 1) return TQ_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int kind = 0; kind < 2; ++kind) {
+    const void* x = kind == 0 ? k : v;
+    if (!x) continue;
+    QuantizeArgs a{};
+    a.x = x;
+    a.f32 = dtype == TQ_F32;
+    a.batch = batch;
+    a.n_new = n_new;
+    a.H = H;
+    a.start_pos = start_pos;
+    a.block_table = block_table;
+    a.maxp = maxp;
+    a.num_pages = num_pages;
+    a.cache = static_cast<uint8_t*>(kind == 0 ? k_cache : v_cache);
+    a.lay = kind == 0 ? ctx->kl : ctx->vl;
+    a.page_bytes = static_cast<long long>(a.lay.block_bytes) * H;
+    a.m = ctx->cfg.m;
+    a.tab = ctx->tab;
+    if (launch_quantize(a, s) != cudaSuccess) return TQ_ERR_CUDA;
+  }
+  return TQ_OK;
+}
+
+namespace {
+int nchunks_for(int max_seq_len, int chunk) { return max_seq_len <= 0 ? 1 : (max_seq_len + chunk - 1) / chunk; }
+
+size_t ws_bytes(int B, int Hq, int d, int m, int nch) {
+  return align256(sizeof(float) * static_cast<size_t>(B) * Hq * (d + m)) +
+         align256(sizeof(float) * static_cast<size_t>(B) * Hq * nch * (d + 2));
+}
+}  // namespace
+
+extern "C" tq_status tq_workspace_size(const tq_ctx* ctx, int batch, int Hq, int max_seq_len,
+                                       int chunk_tokens, size_t* bytes) {
+  if (!ctx || !bytes || batch < 0 || Hq < 1 || max_seq_len < 0 || chunk_tokens < 0 ||
+      chunk_tokens % kPage)
+    return TQ_ERR_INVALID_ARG;
+  int chunk = chunk_tokens ? chunk_tokens : 0;
+  if (!chunk) {
+    // the automatic chunk depends on the KV-head count, which is not known
+    // here; size for the smallest chunk the automatic choice can pick
+    chunk = 64;
+  }
+  *bytes = ws_bytes(batch, Hq, ctx->cfg.d, ctx->cfg.m, nchunks_for(max_seq_len, chunk));
+  return TQ_OK;
+}
+
+extern "C" tq_status tq_decode_attention(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batch,
+                                         int Hq, int H, const int32_t* seq_lens, int max_seq_len,
+                                         const int32_t* block_table, int maxp, int num_pages,
+                                         const void* k_cache, const void* v_cache, int chunk_tokens,
+                                         float softmax_scale, float* out, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  if (!ctx || batch < 0 || Hq < 1 || H < 1 || Hq % H || max_seq_len < 0 || maxp < 1 ||
+      num_pages < 1 || chunk_tokens < 0 || chunk_tokens % kPage)
+    return TQ_ERR_INVALID_ARG;
+  if (dtype != TQ_BF16 && dtype != TQ_F32) return TQ_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return TQ_ERR_INVALID_ARG;
+  if (Hq / H > kMaxGroup) return TQ_ERR_UNSUPPORTED;
+  if (batch == 0) return TQ_OK;
+  if (!q || !seq_lens || !block_table || !k_cache || !v_cache || !out || !workspace)
+    return TQ_ERR_INVALID_ARG;
+  int chunk = chunk_tokens ? chunk_tokens : pick_chunk(batch * H, max_seq_len);
+  int nch = nchunks_for(max_seq_len, chunk);
+  const int d = ctx->cfg.d, m = ctx->cfg.m;
+  size_t need = ws_bytes(batch, Hq, d, m, nch);
+  if (workspace_bytes < need) return TQ_ERR_WORKSPACE;
+  if (static_cast<long long>(nch) > 65535 || H > 65535 || batch > 65535) return TQ_ERR_UNSUPPORTED;
+  DecodeArgs a{};
+  a.q = q;
+  a.f32 = dtype == TQ_F32;
+  a.B = batch;
+  a.Hq = Hq;
+  a.H = H;
+  a.G = Hq / H;
+  a.seq_lens = seq_lens;
+  a.max_seq_len = max_seq_len;
+  a.block_table = block_table;
+  a.maxp = maxp;
+  a.num_pages = num_pages;
+  a.kc = static_cast<const uint8_t*>(k_cache);
+  a.vc = static_cast<const uint8_t*>(v_cache);
+  a.kl = ctx->kl;
+  a.vl = ctx->vl;
+  a.k_page_bytes = static_cast<long long>(ctx->kl.block_bytes) * H;
+  a.v_page_bytes = static_cast<long long>(ctx->vl.block_bytes) * H;
+  a.chunk = chunk;
+  a.nchunks = nch;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.m = m;
+  a.tab = ctx->tab;
+  char* w = static_cast<char*>(workspace);
+  a.qprep = reinterpret_cast<float*>(w);
+  a.part = reinterpret_cast<float*>(w + align256(sizeof(float) * static_cast<size_t>(batch) * Hq * (d + m)));
+  a.out = out;
+  return launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+extern "C" tq_status tq_check_device_status(const tq_ctx* ctx, uint32_t* flags) {
+  if (!ctx) return TQ_ERR_INVALID_ARG;
+  uint32_t h = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
+  if (cudaMemcpy(&h, ctx->tab.err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return TQ_ERR_CUDA;
+  if (cudaMemset(ctx->tab.err, 0, sizeof(h)) != cudaSuccess) return TQ_ERR_CUDA;
+  if (flags) *flags = h;
+  return h ? TQ_ERR_DEVICE_CHECK : TQ_OK;
+}
+
+extern "C" tq_status tq_refine_counters(const tq_ctx* ctx, unsigned long long out[2], int reset) {
+  if (!ctx || !out) return TQ_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
+  if (cudaMemcpy(out, ctx->tab.counters, 2 * sizeof(unsigned long long), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return TQ_ERR_CUDA;
+  if (reset && cudaMemset(ctx->tab.counters, 0, 2 * sizeof(unsigned long long)) != cudaSuccess) return TQ_ERR_CUDA;
+  return TQ_OK;
+}
+
+extern "C" const char* tq_status_string(tq_status s) {
+  switch (s) {
+    case TQ_OK: return "ok";
+    case TQ_ERR_INVALID_ARG: return "invalid argument";
+    case TQ_ERR_CUDA: return "CUDA error";
+    case TQ_ERR_OOM: return "out of device memory";
+    case TQ_ERR_UNSUPPORTED: return "unsupported configuration";
+    case TQ_ERR_DEVICE_CHECK: return "device-side range check failed (input skipped)";
+    case TQ_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}

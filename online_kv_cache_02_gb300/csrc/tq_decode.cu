@@ -1,0 +1,312 @@
+// Decode attention over the packed, paged cache.
+//
+// [P4] riverfrot.github.io "TurboQuant란 무엇이며…", §2.2-§2.3 (decode: the new
+// token's query against every cached key, softmax, weighted sum of values),
+// §4.3 (stage-1 reconstruction plus the QJL 1-bit correction gives an unbiased
+// inner product; softmax(Q K^T / sqrt(d))); [P2] "생각정리 209 (TurboQuant)",
+// stage 2 (the residual's 1-bit sketch makes the inner product unbiased).
+//
+// Three launches on one stream:
+//   qprep  : q~ = Pi q, u = S q~ (fp32) per query head
+//   chunk  : per (chunk, KV head, sequence): every cached key t of the chunk is
+//            scored as (n_t/sqrt(d)) <q~, c[code_t]> + sqrt(pi/2)/m rho_t
+//            <u, +-1_t>, an online (flash-style) softmax keeps (max, sum,
+//            acc[d]) per query head, acc += p_t (nv_t/sqrt(d)) c_v[code_t]
+//   merge  : log-sum-exp merge of the chunk partials, o = Pi^T (acc / sum)
+// The G query heads that share a KV head share every unpacked key and value.
+
+#include "tq_internal.h"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace tq {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kRecStride = 17;     // words per lane in the staged key-code records
+constexpr float kInvSqrtD = 0.08838834764831845f;
+constexpr float kSqrtHalfPi = 1.2533141373155003f;   // sqrt(pi/2)
+
+__device__ __forceinline__ float load_q(const void* q, bool f32, long long idx) {
+  if (f32) return static_cast<const float*>(q)[idx];
+  return __bfloat162float(static_cast<const __nv_bfloat16*>(q)[idx]);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__global__ void __launch_bounds__(kThreads) qprep_kernel(DecodeArgs a) {
+  __shared__ float qs[kD];
+  __shared__ float qt[kD];
+  const long long bh = blockIdx.x;
+  const int i = threadIdx.x;
+  qs[i] = load_q(a.q, a.f32, bh * kD + i);
+  __syncthreads();
+  float acc = 0.0f;
+#pragma unroll 8
+  for (int k = 0; k < kD; ++k) acc = fmaf(a.tab.pit[k * kD + i], qs[k], acc);
+  qt[i] = acc;
+  __syncthreads();
+  float* dst = a.qprep + bh * (kD + a.m);
+  dst[i] = acc;
+  for (int p = i; p < a.m; p += kThreads) {
+    float u = 0.0f;
+#pragma unroll 8
+    for (int j = 0; j < kD; ++j) u = fmaf(a.tab.st[j * a.m + p], qt[j], u);
+    dst[kD + p] = u;
+  }
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads) chunk_kernel(DecodeArgs a) {
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float qt_s[G][kD];
+  __shared__ float u_s[G][kMaxM];
+  __shared__ float ck_s[2][16];
+  __shared__ float cv_s[2][16];
+  __shared__ unsigned rec_s[4][32 * kRecStride];
+  __shared__ float red_m[4][G];
+  __shared__ float red_l[4][G];
+  __shared__ float red_acc[4][G][kD];
+
+  for (int idx = threadIdx.x; idx < G * kD; idx += kThreads) {
+    int g = idx / kD, j = idx % kD;
+    qt_s[g][j] = a.qprep[(static_cast<long long>(b) * a.Hq + h * G + g) * (kD + a.m) + j];
+  }
+  for (int idx = threadIdx.x; idx < G * a.m; idx += kThreads) {
+    int g = idx / a.m, p = idx % a.m;
+    u_s[g][p] = a.qprep[(static_cast<long long>(b) * a.Hq + h * G + g) * (kD + a.m) + kD + p];
+  }
+  if (threadIdx.x < 32) {
+    int gi = threadIdx.x >> 4, k = threadIdx.x & 15;
+    ck_s[gi][k] = a.kl.g[gi].c[k];
+    cv_s[gi][k] = a.vl.g[gi].c[k];
+  }
+  int L = a.seq_lens[b];
+  if (L < 0 || L > a.max_seq_len || L > a.maxp * kPage) {
+    if (threadIdx.x == 0 && chunk == 0 && h == 0) atomicOr(a.tab.err, kErrSeqLen);
+    L = L < 0 ? 0 : L;
+    L = L > a.max_seq_len ? a.max_seq_len : L;
+    L = L > a.maxp * kPage ? a.maxp * kPage : L;
+  }
+  __syncthreads();
+
+  const int t0 = chunk * a.chunk;
+  const int t1 = min(t0 + a.chunk, L);
+  const int kbh = a.kl.g[0].bits, kbl = a.kl.g[1].bits, ksplit = a.kl.split;
+  const int vbh = a.vl.g[0].bits, vbl = a.vl.g[1].bits, vsplit = a.vl.split;
+  const int kcw = a.kl.code_bytes / 4;
+  const int swords = a.kl.qjl ? a.m / 32 : 0;
+  const float qjl_scale = kSqrtHalfPi / static_cast<float>(a.m);
+  unsigned* rec = rec_s[warp] + lane * kRecStride;
+
+  float m_run[G], l_run[G], acc[G][4];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    m_run[g] = -INFINITY;
+    l_run[g] = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[g][q] = 0.0f;
+  }
+  // this lane's 4 value channels
+  const int vj0 = 4 * lane;
+  const int vgrp = vj0 < vsplit ? 1 : 0;   // 1 -> hi group
+  const int vbits = vgrp ? vbh : vbl;
+  const int voff = vj0 < vsplit ? vj0 * vbh : vsplit * vbh + (vj0 - vsplit) * vbl;
+  const float* cvt = cv_s[vgrp ? 0 : 1];
+
+  for (int base = t0 + warp * 32; base < t1; base += 4 * 32) {
+    const int t = base + lane;
+    bool valid = t < t1;
+    int page = 0;
+    if (valid) {
+      page = a.block_table[static_cast<long long>(b) * a.maxp + (t >> 4)];
+      if (page < 0 || page >= a.num_pages) {
+        atomicOr(a.tab.err, kErrPage);
+        valid = false;
+      }
+    }
+    const int slot = t & 15;
+    float logit[G];
+    if (valid) {
+      const unsigned char* kb = a.kc + static_cast<long long>(page) * a.k_page_bytes +
+                                static_cast<long long>(h) * a.kl.block_bytes;
+      const unsigned* cw = reinterpret_cast<const unsigned*>(kb + slot * a.kl.code_bytes);
+      for (int w = 0; w < kcw; ++w) rec[w] = cw[w];
+      rec[kcw] = 0;
+      float s1[G], s2[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) s1[g] = s2[g] = 0.0f;
+      int off = 0;
+      for (int j = 0; j < kD; ++j) {
+        const int bits = j < ksplit ? kbh : kbl;
+        const int w = off >> 5, sh = off & 31;
+        unsigned long long pair = (static_cast<unsigned long long>(rec[w + 1]) << 32) | rec[w];
+        const int code = static_cast<int>((pair >> sh) & ((1u << bits) - 1u));
+        const float c = ck_s[j < ksplit ? 0 : 1][code];
+#pragma unroll
+        for (int g = 0; g < G; ++g) s1[g] = fmaf(c, qt_s[g][j], s1[g]);
+        off += bits;
+      }
+      const unsigned* sw = reinterpret_cast<const unsigned*>(kb + a.kl.off_signs + slot * (a.m / 8));
+      for (int w = 0; w < swords; ++w) {
+        const unsigned bitsw = sw[w];
+#pragma unroll 4
+        for (int i = 0; i < 32; ++i) {
+          const bool pos = (bitsw >> i) & 1u;
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float u = u_s[g][32 * w + i];
+            s2[g] += pos ? u : -u;
+          }
+        }
+      }
+      const float nk = __half2float(reinterpret_cast<const __half*>(kb + a.kl.off_norm)[slot]);
+      const float rk = a.kl.qjl ? __half2float(reinterpret_cast<const __half*>(kb + a.kl.off_rnorm)[slot]) : 0.0f;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        logit[g] = (nk * kInvSqrtD * s1[g] + qjl_scale * rk * s2[g]) * a.scale_log2;
+    } else {
+#pragma unroll
+      for (int g = 0; g < G; ++g) logit[g] = -INFINITY;
+    }
+    float p[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float mx = warp_max(logit[g]);
+      const float m_new = fmaxf(m_run[g], mx);
+      const float alpha = m_run[g] == -INFINITY ? 0.0f : exp2f(m_run[g] - m_new);
+      p[g] = valid ? exp2f(logit[g] - m_new) : 0.0f;
+      l_run[g] = l_run[g] * alpha + warp_sum(p[g]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[g][q] *= alpha;
+      m_run[g] = m_new;
+    }
+    // value accumulation: every lane owns 4 channels, tokens go one by one
+    const int ntok = min(32, t1 - base);
+    for (int tt = 0; tt < ntok; ++tt) {
+      const int ok = __shfl_sync(0xffffffffu, valid ? 1 : 0, tt);
+      const int pg = __shfl_sync(0xffffffffu, page, tt);
+      float w[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) w[g] = __shfl_sync(0xffffffffu, p[g], tt);
+      if (!ok) continue;
+      const int ts = (base + tt) & 15;
+      const unsigned char* vb = a.vc + static_cast<long long>(pg) * a.v_page_bytes +
+                                static_cast<long long>(h) * a.vl.block_bytes;
+      const unsigned* vw = reinterpret_cast<const unsigned*>(vb + ts * a.vl.code_bytes);
+      const float nv = __half2float(reinterpret_cast<const __half*>(vb + a.vl.off_norm)[ts]) * kInvSqrtD;
+      const int wi = voff >> 5, sh = voff & 31;
+      const unsigned lo = vw[wi];
+      const unsigned hi = (wi + 1 < a.vl.code_bytes / 4) ? vw[wi + 1] : 0u;
+      const unsigned long long pair = (static_cast<unsigned long long>(hi) << 32) | lo;
+      const unsigned bitsv = static_cast<unsigned>(pair >> sh);
+      float cv[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) cv[q] = cvt[(bitsv >> (q * vbits)) & ((1u << vbits) - 1u)];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float wg = w[g] * nv;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[g][q] = fmaf(wg, cv[q], acc[g][q]);
+      }
+    }
+  }
+
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    if (lane == 0) {
+      red_m[warp][g] = m_run[g];
+      red_l[warp][g] = l_run[g];
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) red_acc[warp][g][4 * lane + q] = acc[g][q];
+  }
+  __syncthreads();
+  const int j = threadIdx.x;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, red_m[w][g]);
+    float lsum = 0.0f, A = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      if (red_m[w][g] == -INFINITY) continue;
+      const float sc = exp2f(red_m[w][g] - M);
+      lsum = fmaf(sc, red_l[w][g], lsum);
+      A = fmaf(sc, red_acc[w][g][j], A);
+    }
+    float* dst = a.part + ((static_cast<long long>(b) * a.Hq + h * G + g) * a.nchunks + chunk) * (kD + 2);
+    if (j == 0) {
+      dst[0] = M;
+      dst[1] = lsum;
+    }
+    dst[2 + j] = A;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) merge_kernel(DecodeArgs a) {
+  __shared__ float os[kD];
+  const long long bh = blockIdx.x;
+  const int j = threadIdx.x;
+  const float* P = a.part + bh * a.nchunks * (kD + 2);
+  float M = -INFINITY;
+  for (int c = 0; c < a.nchunks; ++c) M = fmaxf(M, P[c * (kD + 2)]);
+  float l = 0.0f, A = 0.0f;
+  for (int c = 0; c < a.nchunks; ++c) {
+    const float mc = P[c * (kD + 2)];
+    if (mc == -INFINITY) continue;
+    const float w = exp2f(mc - M);
+    l = fmaf(w, P[c * (kD + 2) + 1], l);
+    A = fmaf(w, P[c * (kD + 2) + 2 + j], A);
+  }
+  os[j] = l > 0.0f ? A / l : 0.0f;
+  __syncthreads();
+  float o = 0.0f;
+#pragma unroll 8
+  for (int i = 0; i < kD; ++i) o = fmaf(a.tab.pi[i * kD + j], os[i], o);
+  a.out[bh * kD + j] = o;
+}
+
+template <int G>
+cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
+  dim3 grid(a.nchunks, a.H, a.B);
+  chunk_kernel<G><<<grid, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
+  qprep_kernel<<<a.B * a.Hq, kThreads, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  switch (a.G) {
+    case 1: e = launch_g<1>(a, s); break;
+    case 2: e = launch_g<2>(a, s); break;
+    case 3: e = launch_g<3>(a, s); break;
+    case 4: e = launch_g<4>(a, s); break;
+    case 5: e = launch_g<5>(a, s); break;
+    case 6: e = launch_g<6>(a, s); break;
+    case 7: e = launch_g<7>(a, s); break;
+    case 8: e = launch_g<8>(a, s); break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
+  merge_kernel<<<a.B * a.Hq, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace tq

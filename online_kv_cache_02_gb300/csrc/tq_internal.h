@@ -1,0 +1,111 @@
+// Internal declarations shared by the library's translation units.
+#ifndef TQ_INTERNAL_H_
+#define TQ_INTERNAL_H_
+
+#include "../../include/tq.h"
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace tq {
+
+constexpr int kD = 128;          // supported head dimension
+constexpr int kPage = 16;        // tokens per cache page
+constexpr int kMaxM = 128;       // QJL projections, multiple of 32
+constexpr int kMaxGroup = 8;     // query heads per KV head handled by the decode kernels
+
+// Device error word bits.
+constexpr uint32_t kErrPage = 1u;      // page id outside [0, num_pages)
+constexpr uint32_t kErrBlock = 2u;     // position beyond the block table
+constexpr uint32_t kErrSeqLen = 4u;    // sequence length beyond max_seq_len / block table
+
+// One channel group's Lloyd-Max codebook in unit-variance units.
+struct GroupBook {
+  int bits;
+  int nb;                // 2^bits - 1 boundaries
+  float c[16];           // centroids, fp32
+  float t[16];           // boundaries, fp32 (entries >= nb are +inf)
+  double c64[16];
+  double t64[16];
+};
+
+// Codebooks and bit layout for one kind (K or V).
+struct KindLayout {
+  GroupBook g[2];        // g[0]: channels [0, split), g[1]: [split, d)
+  int split;
+  int code_bytes;        // per vector
+  int block_bytes;       // per (page, head) block
+  int off_signs;         // byte offsets inside a block
+  int off_norm;
+  int off_rnorm;
+  int qjl;               // keys with QJL signs + residual norm
+};
+
+// Host functions (tq_host.cpp).
+void gaussian_fill(uint64_t seed, uint64_t stream, size_t n, double* out);
+void rotation_fill(int d, uint64_t seed, double* pi);
+void qjl_fill(int m, int d, uint64_t seed, double* s);
+void codebook_fill(int bits, double* centroids, double* boundaries);
+
+// Device tables owned by a context.
+struct DeviceTables {
+  float* pit;            // Pi^T, fp32 [d][d]: pit[k*d + i] = Pi[i][k]
+  float* pi;             // Pi, fp32 [d][d] row-major
+  double* pi64;          // Pi, fp64 row-major
+  float* st;             // S^T, fp32 [d][m]: st[j*m + i] = S[i][j]
+  double* s64;           // S, fp64 row-major [m][d]
+  uint32_t* err;         // device error word
+  unsigned long long* counters;  // [0] codes re-taken in fp64, [1] key vectors with signs re-taken
+};
+
+struct QuantizeArgs {
+  const void* x;         // [batch][n_new][H][d]
+  int f32;               // 1: fp32 input, 0: bf16
+  int batch, n_new, H;
+  const int32_t* start_pos;
+  const int32_t* block_table;
+  int maxp, num_pages;
+  uint8_t* cache;
+  long long page_bytes;
+  int m;
+  KindLayout lay;
+  DeviceTables tab;
+};
+
+struct DecodeArgs {
+  const void* q;
+  int f32;
+  int B, Hq, H, G;
+  const int32_t* seq_lens;
+  int max_seq_len;
+  const int32_t* block_table;
+  int maxp, num_pages;
+  const uint8_t* kc;
+  const uint8_t* vc;
+  long long k_page_bytes, v_page_bytes;
+  int chunk, nchunks;
+  float scale_log2;      // softmax_scale * log2(e)
+  int m;
+  KindLayout kl, vl;
+  DeviceTables tab;
+  float* qprep;          // [B][Hq][d + m]
+  float* part;           // [B][Hq][nchunks][d + 2]
+  float* out;            // [B][Hq][d]
+};
+
+cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+}  // namespace tq
+
+struct tq_ctx {
+  tq_config cfg;
+  int device;
+  tq::KindLayout kl, vl;
+  tq::DeviceTables tab;
+  void* dev_block;       // single allocation holding every device table
+};
+
+#endif  // TQ_INTERNAL_H_

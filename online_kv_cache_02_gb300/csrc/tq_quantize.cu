@@ -1,0 +1,425 @@
+// Online quantize-and-append kernel.
+//
+// [P2] "생각정리 209 (TurboQuant)", stage 1 and stage 2; [P4] riverfrot.github.io
+// "TurboQuant란 무엇이며…", §4.1 (x~ = R x/||x||), §4.2 (per-coordinate
+// Lloyd-Max lookup), §4.3 (residual r = x - Q^-1(Q(x)), 1-bit sign sketch of a
+// random projection of r), §3.1 (fixed-size blocks addressed by a block table).
+//
+// Per tile of 32 vectors (one CTA, persistent over tiles, Pi^T and S^T resident
+// in shared memory):
+//   1. x tile -> shared (transposed), ||x||^2 as an exact double-float sum
+//   2. y = Pi x on the fp32 pipes (4x4 register tile per thread)
+//   3. u = sqrt(d) y / ||x||, code = #{k : u >= t_k}; a u within 2e-5 of a
+//      boundary is re-decided from y and ||x|| recomputed in fp64
+//   4. keys: r = y - fp16(||x||)/sqrt(d) c[code]; z = S r (fp32); sign = z >= 0;
+//      if any |z_i| < 5e-5 ||r|| the whole vector's r, z and ||r|| are redone
+//      in fp64 (the fp32 residual carries the cancellation error of y - y^)
+//   5. bit-pack codes / signs, fp16 norms, store at (page, slot, head).
+// fp32 error of the fast path is ~1e-7 in u units and ~1e-6 ||r|| for z, so
+// the guards sit 100x and 30x beyond it: the stored codes and signs are the
+// ones exact arithmetic gives, except for values within ~1e-13 of a boundary.
+
+#include "tq_internal.h"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace tq {
+namespace {
+
+constexpr int kTile = 32;
+constexpr int kThreads = 256;
+constexpr int kXS = 36;            // padded row stride (floats) of the transposed tiles
+constexpr float kCodeGuard = 2e-5f;
+constexpr float kSignGuard = 5e-5f;
+
+// ---- double-float helpers (error-free transformations) ----------------------
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+__device__ __forceinline__ void fast_two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  e = b - (s - a);
+}
+__device__ __forceinline__ void df_add(float& h, float& l, float bh, float bl) {
+  float s, e;
+  two_sum(h, bh, s, e);
+  e += l + bl;
+  fast_two_sum(s, e, h, l);
+}
+
+// fp16 round-to-nearest-even of the double-float value hi + lo (hi >= 0).
+__device__ __half df_to_half(float hi, float lo) {
+  __half h = __float2half_rn(hi);
+  float back = __half2float(h);
+  if (back == hi || lo == 0.0f || isinf(back)) return h;
+  unsigned short bits = __half_as_ushort(h);
+  __half nb = __ushort_as_half(hi > back ? static_cast<unsigned short>(bits + 1)
+                                         : static_cast<unsigned short>(bits - 1));
+  float nbf = __half2float(nb);
+  float mid = 0.5f * (back + nbf);
+  if (hi != mid) return h;                 // not on a tie: hi rounds like hi + lo
+  bool up = lo > 0.0f;                     // tie broken by the low part
+  bool nb_is_up = nbf > back;
+  return (up == nb_is_up) ? nb : h;
+}
+
+__device__ __forceinline__ float load_x(const void* x, bool f32, long long idx) {
+  if (f32) return static_cast<const float*>(x)[idx];
+  return __bfloat162float(static_cast<const __nv_bfloat16*>(x)[idx]);
+}
+
+struct Smem {
+  float* pit;     // [128][128]
+  float* st;      // [128][128]  (S^T, columns >= m unused)
+  float* xt;      // [128][kXS]
+  float* rt;      // [128][kXS]
+  unsigned char* codes;   // [32][128]
+  unsigned char* snib;    // [32][32]
+  double* r64;    // [8 warps][128]
+  float* npart;   // [8][32][2]
+  float* nhi;     // [32]
+  float* nlo;
+  float* scale;
+  float* n16f;
+  float* rho2;
+  unsigned* sflag;   // [32]
+  unsigned* sword;   // [32][4] refined sign words
+  unsigned short* n16;   // [32]
+  unsigned short* r16;   // [32]
+};
+
+template <bool KEY>
+size_t smem_bytes() {
+  size_t b = 0;
+  b += 128 * 128 * 4;                 // pit
+  if (KEY) b += 128 * 128 * 4;        // st
+  b += 128 * kXS * 4;                 // xt
+  if (KEY) b += 128 * kXS * 4;        // rt
+  b += 32 * 128;                      // codes
+  b += 32 * 32;                       // snib
+  if (KEY) b += 8 * 128 * 8;          // r64
+  b += 8 * 32 * 2 * 4;                // npart
+  b += 5 * 32 * 4;                    // nhi, nlo, scale, n16f, rho2
+  b += 32 * 4 + 32 * 4 * 4;           // sflag, sword
+  b += 2 * 32 * 2;                    // n16, r16
+  return b + 64;
+}
+
+template <bool KEY>
+__device__ Smem carve(unsigned char* p) {
+  Smem s;
+  auto take = [&](size_t n) { unsigned char* r = p; p += (n + 15) & ~size_t(15); return r; };
+  s.pit = reinterpret_cast<float*>(take(128 * 128 * 4));
+  s.st = KEY ? reinterpret_cast<float*>(take(128 * 128 * 4)) : nullptr;
+  s.xt = reinterpret_cast<float*>(take(128 * kXS * 4));
+  s.rt = KEY ? reinterpret_cast<float*>(take(128 * kXS * 4)) : nullptr;
+  s.r64 = KEY ? reinterpret_cast<double*>(take(8 * 128 * 8)) : nullptr;
+  s.codes = take(32 * 128);
+  s.snib = take(32 * 32);
+  s.npart = reinterpret_cast<float*>(take(8 * 32 * 2 * 4));
+  s.nhi = reinterpret_cast<float*>(take(32 * 4));
+  s.nlo = reinterpret_cast<float*>(take(32 * 4));
+  s.scale = reinterpret_cast<float*>(take(32 * 4));
+  s.n16f = reinterpret_cast<float*>(take(32 * 4));
+  s.rho2 = reinterpret_cast<float*>(take(32 * 4));
+  s.sflag = reinterpret_cast<unsigned*>(take(32 * 4));
+  s.sword = reinterpret_cast<unsigned*>(take(32 * 4 * 4));
+  s.n16 = reinterpret_cast<unsigned short*>(take(32 * 2));
+  s.r16 = reinterpret_cast<unsigned short*>(take(32 * 2));
+  return s;
+}
+
+__device__ __forceinline__ int channel_off(const KindLayout& L, int j) {
+  return j < L.split ? j * L.g[0].bits : L.split * L.g[0].bits + (j - L.split) * L.g[1].bits;
+}
+
+// 32-bit word w of a vector's code stream, from one byte per channel.
+__device__ unsigned pack_code_word(const KindLayout& L, const unsigned char* codes, int w) {
+  const int bh = L.g[0].bits, bl = L.g[1].bits;
+  const int lo = 32 * w, hi = lo + 32;
+  int j = lo < L.split * bh ? lo / bh : L.split + (lo - L.split * bh) / bl;
+  unsigned word = 0;
+  for (; j < kD; ++j) {
+    int off = channel_off(L, j);
+    if (off >= hi) break;
+    unsigned long long c = codes[j];
+    int sh = off - lo;
+    word |= sh >= 0 ? static_cast<unsigned>(c << sh) : static_cast<unsigned>(c >> (-sh));
+  }
+  return word;
+}
+
+template <bool KEY>
+__global__ void __launch_bounds__(kThreads, 1) quantize_kernel(QuantizeArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Smem sm = carve<KEY>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const KindLayout& L = a.lay;
+  const float inv_sqrt_d = 0.08838834764831845f;     // 1/sqrt(128)
+  const double inv_sqrt_d64 = 1.0 / sqrt(128.0);
+  const double sqrt_d64 = sqrt(128.0);
+
+  for (int i = tid; i < 128 * 128 / 4; i += kThreads)
+    reinterpret_cast<float4*>(sm.pit)[i] = reinterpret_cast<const float4*>(a.tab.pit)[i];
+  if (KEY) {
+    for (int i = tid; i < 128 * 128; i += kThreads) {
+      int j = i >> 7, c = i & 127;
+      sm.st[i] = c < a.m ? a.tab.st[j * a.m + c] : 0.0f;
+    }
+  }
+  __syncthreads();
+
+  const long long nvec = static_cast<long long>(a.batch) * a.n_new * a.H;
+  const long long ntiles = (nvec + kTile - 1) / kTile;
+  for (long long tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const long long v0 = tile * kTile;
+    // 1. x tile (transposed) and double-float partial norms
+    {
+      const int v = lane, kc = warp;
+      const long long gv = v0 + v;
+      float sh = 0.0f, sl = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        int k = kc * 16 + q;
+        float xv = gv < nvec ? load_x(a.x, a.f32, gv * kD + k) : 0.0f;
+        sm.xt[k * kXS + v] = xv;
+        float p = xv * xv;
+        float e = fmaf(xv, xv, -p);
+        float s, t;
+        two_sum(sh, p, s, t);
+        sh = s;
+        sl += t + e;
+      }
+      sm.npart[(kc * 32 + v) * 2 + 0] = sh;
+      sm.npart[(kc * 32 + v) * 2 + 1] = sl;
+      if (tid < 32) sm.sflag[tid] = 0;
+    }
+    __syncthreads();
+    if (tid < 32) {
+      float h = 0.0f, l = 0.0f;
+      for (int kc = 0; kc < 8; ++kc) df_add(h, l, sm.npart[(kc * 32 + tid) * 2], sm.npart[(kc * 32 + tid) * 2 + 1]);
+      float nh = 0.0f, nl = 0.0f;
+      if (h > 0.0f) {
+        float r = sqrtf(h);
+        float res = fmaf(-r, r, h) + l;
+        fast_two_sum(r, res / (2.0f * r), nh, nl);
+      }
+      sm.nhi[tid] = nh;
+      sm.nlo[tid] = nl;
+      sm.scale[tid] = nh > 0.0f ? 11.313708498984761f / nh : 0.0f;   // sqrt(128) / ||x||
+      __half n16 = df_to_half(nh, nl);
+      sm.n16[tid] = __half_as_ushort(n16);
+      sm.n16f[tid] = __half2float(n16);
+    }
+    __syncthreads();
+
+    // 2. y = Pi x: thread owns vectors 4*warp..+3, outputs 4*lane..+3
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+#pragma unroll 8
+    for (int k = 0; k < 128; ++k) {
+      float4 p = *reinterpret_cast<const float4*>(&sm.pit[k * 128 + 4 * lane]);
+      float4 xx = *reinterpret_cast<const float4*>(&sm.xt[k * kXS + 4 * warp]);
+      float xa[4] = {xx.x, xx.y, xx.z, xx.w};
+      float pa[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+      for (int vi = 0; vi < 4; ++vi)
+#pragma unroll
+        for (int oi = 0; oi < 4; ++oi) acc[vi][oi] = fmaf(pa[oi], xa[vi], acc[vi][oi]);
+    }
+
+    // 3. codes (+ fp64 re-decision near boundaries); keys: residual
+    float rpart[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int vi = 0; vi < 4; ++vi) {
+      const int v = 4 * warp + vi;
+      const bool valid = v0 + v < nvec;
+      const float sc = sm.scale[v];
+#pragma unroll
+      for (int oi = 0; oi < 4; ++oi) {
+        const int i = 4 * lane + oi;
+        const GroupBook& gb = L.g[i < L.split ? 0 : 1];
+        float u = acc[vi][oi] * sc;
+        int code = 0;
+        float mind = INFINITY;
+        for (int k = 0; k < gb.nb; ++k) {
+          code += u >= gb.t[k];
+          mind = fminf(mind, fabsf(u - gb.t[k]));
+        }
+        if (valid && mind < kCodeGuard) {
+          double y64 = 0.0;
+          for (int k = 0; k < 128; ++k) y64 = fma(a.tab.pi64[i * 128 + k], static_cast<double>(sm.xt[k * kXS + v]), y64);
+          double n64 = static_cast<double>(sm.nhi[v]) + static_cast<double>(sm.nlo[v]);
+          double u64 = n64 > 0.0 ? sqrt_d64 * y64 / n64 : 0.0;
+          code = 0;
+          for (int k = 0; k < gb.nb; ++k) code += u64 >= gb.t64[k];
+          atomicAdd(&a.tab.counters[0], 1ULL);
+        }
+        sm.codes[v * 128 + i] = static_cast<unsigned char>(code);
+        if (KEY) {
+          float r = fmaf(-sm.n16f[v] * inv_sqrt_d, gb.c[code], acc[vi][oi]);
+          sm.rt[i * kXS + v] = r;
+          rpart[vi] = fmaf(r, r, rpart[vi]);
+        }
+      }
+    }
+    if (KEY) {
+#pragma unroll
+      for (int vi = 0; vi < 4; ++vi) {
+        float s = rpart[vi];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) sm.rho2[4 * warp + vi] = s;
+      }
+      __syncthreads();
+      // 4. z = S r for projections 4*lane..+3
+      float z[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) z[i][j] = 0.0f;
+#pragma unroll 8
+      for (int j = 0; j < 128; ++j) {
+        float4 s4 = *reinterpret_cast<const float4*>(&sm.st[j * 128 + 4 * lane]);
+        float4 rr = *reinterpret_cast<const float4*>(&sm.rt[j * kXS + 4 * warp]);
+        float ra[4] = {rr.x, rr.y, rr.z, rr.w};
+        float sa[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+        for (int vi = 0; vi < 4; ++vi)
+#pragma unroll
+          for (int oi = 0; oi < 4; ++oi) z[vi][oi] = fmaf(sa[oi], ra[vi], z[vi][oi]);
+      }
+#pragma unroll
+      for (int vi = 0; vi < 4; ++vi) {
+        const int v = 4 * warp + vi;
+        const float guard = kSignGuard * sqrtf(sm.rho2[v]);
+        unsigned nib = 0;
+        bool near = false;
+#pragma unroll
+        for (int oi = 0; oi < 4; ++oi) {
+          nib |= (z[vi][oi] >= 0.0f ? 1u : 0u) << oi;
+          near |= (4 * lane + oi < a.m) && fabsf(z[vi][oi]) < guard;
+        }
+        sm.snib[v * 32 + lane] = static_cast<unsigned char>(nib);
+        unsigned any = __ballot_sync(0xffffffffu, near);
+        if (lane == 0 && any) sm.sflag[v] = 1u;
+      }
+    }
+    __syncthreads();
+
+    // 5. per-vector finalisation: warp handles vectors warp, warp+8, ...
+    for (int r = 0; r < 4; ++r) {
+      const int v = warp + 8 * r;
+      const long long gv = v0 + v;
+      if (gv >= nvec) continue;
+      const int h = static_cast<int>(gv % a.H);
+      const long long bt = gv / a.H;
+      const int t = static_cast<int>(bt % a.n_new);
+      const int b = static_cast<int>(bt / a.n_new);
+      bool refine = KEY && L.qjl && sm.sflag[v];
+      unsigned short r16 = 0;
+      if (KEY && L.qjl) {
+        if (refine) {
+          // fp64 residual, projections and residual norm for this vector
+          double* r64 = sm.r64 + warp * 128;
+          double n16d = static_cast<double>(sm.n16f[v]);
+          double rs = 0.0;
+          for (int q = 0; q < 4; ++q) {
+            const int i = lane + 32 * q;
+            double y64 = 0.0;
+            for (int k = 0; k < 128; ++k) y64 = fma(a.tab.pi64[i * 128 + k], static_cast<double>(sm.xt[k * kXS + v]), y64);
+            const GroupBook& gb = L.g[i < L.split ? 0 : 1];
+            double rr = y64 - (n16d * inv_sqrt_d64) * gb.c64[sm.codes[v * 128 + i]];
+            r64[i] = rr;
+            rs = fma(rr, rr, rs);
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
+          __syncwarp();
+          for (int q = 0; q < a.m / 32; ++q) {
+            const int p = lane + 32 * q;
+            double zz = 0.0;
+            for (int j = 0; j < 128; ++j) zz = fma(a.tab.s64[p * 128 + j], r64[j], zz);
+            unsigned w = __ballot_sync(0xffffffffu, zz >= 0.0);
+            if (lane == 0) sm.sword[v * 4 + q] = w;
+          }
+          r16 = __half_as_ushort(__double2half(sqrt(rs)));
+          if (lane == 0) atomicAdd(&a.tab.counters[1], 1ULL);
+          __syncwarp();
+        } else {
+          r16 = __half_as_ushort(__float2half_rn(sqrtf(sm.rho2[v])));
+        }
+      }
+      const int pos = a.start_pos[b] + t;
+      const int blk = pos >> 4;
+      if (pos < 0 || blk >= a.maxp) {
+        if (lane == 0) atomicOr(a.tab.err, kErrBlock);
+        continue;
+      }
+      const int page = a.block_table[static_cast<long long>(b) * a.maxp + blk];
+      if (page < 0 || page >= a.num_pages) {
+        if (lane == 0) atomicOr(a.tab.err, kErrPage);
+        continue;
+      }
+      const int slot = pos & 15;
+      unsigned char* base = a.cache + static_cast<long long>(page) * a.page_bytes +
+                            static_cast<long long>(h) * L.block_bytes;
+      const int nwords = L.code_bytes / 4;
+      for (int w = lane; w < nwords; w += 32) {
+        reinterpret_cast<unsigned*>(base + slot * L.code_bytes)[w] = pack_code_word(L, sm.codes + v * 128, w);
+      }
+      if (KEY && L.qjl) {
+        const int sw = a.m / 32;
+        if (lane < sw) {
+          unsigned word;
+          if (refine) {
+            word = sm.sword[v * 4 + lane];
+          } else {
+            word = 0;
+            for (int l = 0; l < 8; ++l) word |= static_cast<unsigned>(sm.snib[v * 32 + 8 * lane + l]) << (4 * l);
+          }
+          reinterpret_cast<unsigned*>(base + L.off_signs + slot * (a.m / 8))[lane] = word;
+        }
+        if (lane == 0) reinterpret_cast<unsigned short*>(base + L.off_rnorm)[slot] = r16;
+      }
+      if (lane == 0) reinterpret_cast<unsigned short*>(base + L.off_norm)[slot] = sm.n16[v];
+    }
+    __syncthreads();
+  }
+}
+
+template <bool KEY>
+cudaError_t launch_kind(const QuantizeArgs& a, cudaStream_t s) {
+  static bool configured[2] = {false, false};
+  const size_t smem = smem_bytes<KEY>();
+  if (!configured[KEY]) {
+    cudaError_t e = cudaFuncSetAttribute(quantize_kernel<KEY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured[KEY] = true;
+  }
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long nvec = static_cast<long long>(a.batch) * a.n_new * a.H;
+  const long long ntiles = (nvec + kTile - 1) / kTile;
+  const int grid = static_cast<int>(ntiles < sms ? ntiles : sms);
+  quantize_kernel<KEY><<<grid, kThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s) {
+  if (a.lay.qjl) return launch_kind<true>(a, s);
+  return launch_kind<false>(a, s);
+}
+
+}  // namespace tq

@@ -1,0 +1,149 @@
+"""GPU decode-attention parity against the oracle, through the C ABI.
+
+Both sides read the same cache bytes: the oracle quantizes and packs the
+synthetic K/V, the bytes go to the device unchanged, and the GPU's output is
+compared with the oracle's two-pass fp64 softmax over the same records.
+"""
+
+import numpy as np
+import pytest
+
+from .gpu_common import (alloc_caches, ctx_for, gpu_decode, oracle, oracle_cache_bytes, seq_locations, th, to_dev,
+                         tq, wl)
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_setup(w, lens, H, seed):
+    rng = np.random.default_rng(seed)
+    B = len(lens)
+    pps = max(1, (int(max(lens)) + 15) // 16)
+    num_pages = B * pps + 2
+    bt = rng.permutation(num_pages)[:B * pps].astype(np.int32).reshape(B, pps)
+    p = th.params_for(w)
+    kc = oracle_cache_bytes(p, H, num_pages, "k")
+    vc = oracle_cache_bytes(p, H, num_pages, "v")
+    for b in range(B):
+        L = int(lens[b])
+        if L == 0:
+            continue
+        K = rng.standard_normal((L, H, 128)).astype(np.float32)
+        K[..., :w.outlier_channels] *= w.outlier_scale
+        V = rng.standard_normal((L, H, 128)).astype(np.float32)
+        if w.dtype == "bf16":
+            K, V = wl.bf16_round(K), wl.bf16_round(V)
+        pages, slots, heads = seq_locations(bt, b, np.arange(L), H)
+        th.oracle_quantize_into(p, "k", kc, K.reshape(-1, 128), pages, slots, heads, H)
+        th.oracle_quantize_into(p, "v", vc, V.reshape(-1, 128), pages, slots, heads, H)
+    return p, bt, num_pages, kc, vc
+
+
+def _check(w, lens, Hq, H, chunk=0, scale=None, seed=0, qdtype=None):
+    lens = np.asarray(lens, dtype=np.int32)
+    p, bt, num_pages, kc, vc = _oracle_setup(w, lens, H, seed)
+    rng = np.random.default_rng(seed + 100)
+    Q = rng.standard_normal((len(lens), Hq, 128)).astype(np.float32)
+    qd = qdtype or w.dtype
+    if qd == "bf16":
+        Q = wl.bf16_round(Q)
+    scale = th.scale_for() if scale is None else scale
+    ctx = ctx_for(w)
+    try:
+        got = gpu_decode(ctx, Q, qd, H, lens, int(max(lens.max(), 1)), bt, num_pages, to_dev(kc), to_dev(vc),
+                         chunk=chunk, scale=scale)
+        assert tq.tq_check_device_status(ctx) == 0
+    finally:
+        tq.tq_destroy(ctx)
+    ref = oracle.decode_attention(p, Q.astype(np.float64), lens, bt, kc, vc, H, scale=scale)
+    err = th.rel_err(got, ref)
+    assert np.all(np.isfinite(got))
+    assert err.max() <= th.ATT_TOL, (err.max(), np.unravel_index(err.argmax(), err.shape))
+    return err.max()
+
+
+BASE = wl.Workload("t", "decode", 1, 8, 1, 0, seed=0)
+
+
+@pytest.mark.parametrize("kb,vb,qjl", [((3, 3), (3, 3), True), ((4, 3), (4, 3), True), ((3, 2), (3, 2), True),
+                                       ((2, 2), (4, 4), False), ((1, 1), (1, 1), True), ((4, 4), (2, 3), True)])
+def test_decode_bit_configs(kb, vb, qjl):
+    w = BASE.scaled(k_bits=kb, v_bits=vb, qjl=qjl, dtype="bf16")
+    _check(w, [300, 17, 129], Hq=8, H=2, chunk=64, seed=1)
+
+
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 7, 8])
+def test_decode_gqa_group_sizes(G):
+    w = BASE.scaled(dtype="bf16")
+    _check(w, [200, 45], Hq=2 * G, H=2, chunk=0, seed=G)
+
+
+@pytest.mark.parametrize("chunk", [16, 48, 1024, 0])
+def test_decode_chunking_is_invisible(chunk):
+    w = BASE.scaled(dtype="bf16")
+    _check(w, [1000, 1, 16, 33], Hq=4, H=1, chunk=chunk, seed=3)
+
+
+def test_decode_empty_and_single_token_sequences():
+    w = BASE.scaled(dtype="f32")
+    lens = [0, 1, 2, 0]
+    _check(w, lens, Hq=4, H=2, chunk=16, seed=4)
+
+
+def test_decode_fp32_queries_and_scale():
+    w = BASE.scaled(dtype="f32")
+    _check(w, [257, 90], Hq=4, H=2, chunk=32, scale=0.3, seed=5)
+    _check(w, [257, 90], Hq=4, H=2, chunk=32, scale=0.0, seed=5)    # uniform weights
+
+
+def test_decode_config_c1():
+    """Single head, N=1024 fp32 keys (channels 0-3 x10) and values, 8 fp32 queries, 3-bit + QJL."""
+    w = wl.WORKLOADS["c1"]
+    _check(w, [1024], Hq=8, H=1, chunk=0, seed=0)
+
+
+def test_decode_bad_page_is_skipped_and_flagged():
+    w = BASE.scaled(dtype="bf16")
+    lens = np.array([40], np.int32)
+    p, bt, num_pages, kc, vc = _oracle_setup(w, lens, 1, 9)
+    bt_bad = bt.copy()
+    bt_bad[0, 1] = num_pages + 5                 # tokens 16..31 point outside the cache
+    Q = wl.bf16_round(np.random.default_rng(9).standard_normal((1, 4, 128)).astype(np.float32))
+    ctx = ctx_for(w)
+    try:
+        got = gpu_decode(ctx, Q, "bf16", 1, lens, 40, bt_bad, num_pages, to_dev(kc), to_dev(vc), chunk=16)
+        assert tq.tq_check_device_status(ctx) & 1
+        # a length beyond max_seq_len is clamped and flagged
+        gpu_decode(ctx, Q, "bf16", 1, np.array([48], np.int32), 40, bt, num_pages, to_dev(kc), to_dev(vc))
+        assert tq.tq_check_device_status(ctx) & 4
+    finally:
+        tq.tq_destroy(ctx)
+    # the skipped block simply does not take part
+    keep = np.r_[0:16, 32:40]
+    pages, slots = bt[0, keep // 16], keep % 16
+    heads = np.zeros(len(keep), dtype=np.int64)
+    kr = oracle.unpack_k_records(p, oracle.read_paged(p, "k", kc, pages, slots, heads, 1))
+    vr = oracle.unpack_v_records(p, oracle.read_paged(p, "v", vc, pages, slots, heads, 1))
+    ref = np.stack([oracle.turboquant.attend_one(p, Q[0, h].astype(np.float64), kr, vr, th.scale_for())
+                    for h in range(4)])
+    assert th.rel_err(got[0], ref).max() <= th.ATT_TOL
+
+
+def test_workspace_too_small_is_rejected():
+    w = BASE.scaled(dtype="bf16")
+    ctx = ctx_for(w)
+    try:
+        kc, vc = alloc_caches(ctx, 1, 1)
+        n = tq.tq_workspace_size(ctx, 1, 4, 16, 16)
+        import torch
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        out = torch.empty(1, 4, 128, dtype=torch.float32, device="cuda")
+        q = torch.zeros(1, 4, 128, dtype=torch.bfloat16, device="cuda")
+        lens = to_dev(np.array([16], np.int32))
+        bt = to_dev(np.zeros((1, 1), np.int32))
+        with pytest.raises(tq.TQError) as e:
+            tq.tq_decode_attention(ctx, q, tq.TQ_BF16, 1, 4, 1, lens, 16, bt, 1, 1, kc, vc, 16, 0.1, out, ws, n - 1)
+        assert e.value.status == tq.TQ_ERR_WORKSPACE
+        with pytest.raises(tq.TQError):
+            tq.tq_decode_attention(ctx, q, tq.TQ_BF16, 1, 4, 3, lens, 16, bt, 1, 1, kc, vc, 16, 0.1, out, ws, n)
+    finally:
+        tq.tq_destroy(ctx)

@@ -1,0 +1,166 @@
+"""GPU quantize parity against the oracle, through the C ABI."""
+
+import numpy as np
+import pytest
+
+from .gpu_common import (alloc_caches, ctx_for, gpu_quantize, oracle, oracle_cache_bytes, seq_locations, th, tq,
+                         wl)
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = [
+    # k_bits, v_bits, qjl, m, dtype
+    ((3, 3), (3, 3), True, 128, "f32"),
+    ((3, 3), (3, 3), True, 128, "bf16"),
+    ((4, 3), (4, 3), True, 128, "bf16"),
+    ((3, 2), (3, 2), True, 128, "bf16"),
+    ((1, 1), (2, 2), True, 64, "f32"),
+    ((4, 4), (1, 4), False, 128, "bf16"),
+    ((2, 4), (4, 1), True, 96, "f32"),
+]
+
+
+def _run_case(kb, vb, qjl, m, dtype, B=3, T=37, H=2, starts=(0, 5, 19), seed=11):
+    w = wl.Workload("t", "quantize", B, H, H, T, k_bits=kb, v_bits=vb, qjl=qjl, m=m, dtype=dtype, seed=seed)
+    rng = np.random.default_rng(seed)
+    pps = (max(starts) + T + 15) // 16
+    num_pages = B * pps + 3
+    bt = rng.permutation(num_pages)[:B * pps].astype(np.int32).reshape(B, pps)
+    K = rng.standard_normal((B, T, H, 128)).astype(np.float32)
+    K[..., :4] *= 10
+    V = rng.standard_normal((B, T, H, 128)).astype(np.float32)
+    if dtype == "bf16":
+        K, V = wl.bf16_round(K), wl.bf16_round(V)
+    ctx = ctx_for(w)
+    try:
+        kc, vc = alloc_caches(ctx, H, num_pages)
+        gpu_quantize(ctx, K, V, dtype, starts, bt, num_pages, kc, vc)
+        assert tq.tq_check_device_status(ctx) == 0
+        got_k, got_v = kc.cpu().numpy(), vc.cpu().numpy()
+    finally:
+        tq.tq_destroy(ctx)
+    p = th.params_for(w)
+    for kind, X, got in (("k", K, got_k), ("v", V, got_v)):
+        pages, slots, heads = [], [], []
+        for b in range(B):
+            pg, sl, hd = seq_locations(bt, b, starts[b] + np.arange(T), H)
+            pages.append(pg), slots.append(sl), heads.append(hd)
+        pages, slots, heads = map(np.concatenate, (pages, slots, heads))
+        want = oracle_cache_bytes(p, H, num_pages, kind)
+        q, ex = th.oracle_quantize_into(p, kind, want, X.reshape(-1, 128), pages, slots, heads, H)
+        res = th.compare_records(p, kind, got, q, ex, pages, slots, heads, H)
+        th.assert_records_ok(res)
+        # addressing: bytes outside the written records are untouched
+        mask = th.touched_mask(p, kind, got.size, pages, slots, heads, H)
+        assert np.all(got[~mask] == 0xA5)
+        # and written bytes equal the oracle's except where a residual norm may differ by one ulp
+        diff = np.nonzero(got != want)[0]
+        if kind == "v" or not qjl:
+            assert diff.size == 0 or res["codes_mismatch_excluded"] > 0, res
+
+
+@pytest.mark.parametrize("kb,vb,qjl,m,dtype", VARIANTS)
+def test_quantize_matches_oracle(kb, vb, qjl, m, dtype):
+    _run_case(kb, vb, qjl, m, dtype)
+
+
+def test_quantize_many_tiles_ragged_tail():
+    # 1000 vectors per kind: 31 full tiles of 32 and a ragged tail of 8
+    _run_case((3, 3), (3, 3), True, 128, "bf16", B=5, T=25, H=8, starts=(0, 16, 3, 40, 7), seed=5)
+
+
+def test_append_one_token_at_a_time_equals_bulk():
+    w = wl.Workload("t", "quantize", 2, 4, 4, 21, seed=2)
+    rng = np.random.default_rng(2)
+    B, T, H = 2, 21, 4
+    pps = 2
+    bt = np.array([[3, 0], [1, 2]], dtype=np.int32)
+    K = wl.bf16_round(rng.standard_normal((B, T, H, 128)).astype(np.float32))
+    V = wl.bf16_round(rng.standard_normal((B, T, H, 128)).astype(np.float32))
+    ctx = ctx_for(w)
+    try:
+        kc1, vc1 = alloc_caches(ctx, H, 4)
+        gpu_quantize(ctx, K, V, "bf16", [0, 0], bt, 4, kc1, vc1)
+        kc2, vc2 = alloc_caches(ctx, H, 4)
+        for t in range(T):
+            gpu_quantize(ctx, K[:, t:t + 1], V[:, t:t + 1], "bf16", [t, t], bt, 4, kc2, vc2)
+        assert tq.tq_check_device_status(ctx) == 0
+        assert np.array_equal(kc1.cpu().numpy(), kc2.cpu().numpy())
+        assert np.array_equal(vc1.cpu().numpy(), vc2.cpu().numpy())
+    finally:
+        tq.tq_destroy(ctx)
+
+
+def test_zero_and_boundary_vectors():
+    """A zero vector and vectors placed exactly on codebook boundaries (fp64 re-decision path)."""
+    w = wl.Workload("t", "quantize", 1, 1, 1, 8, dtype="f32", seed=0)
+    p = th.params_for(w)
+    cb = p.books[3]
+    X = np.zeros((8, 128))
+    for r in range(1, 8):
+        u = np.random.default_rng(r).standard_normal(128)
+        u[:16] = cb.boundaries[np.arange(16) % 7]
+        y = u / np.linalg.norm(u) * 3.0
+        X[r] = p.Pi.T @ y
+    X = X.astype(np.float32)
+    K = X.reshape(1, 8, 1, 128)
+    bt = np.array([[0]], dtype=np.int32)
+    ctx = ctx_for(w)
+    try:
+        tq.tq_refine_counters(ctx, reset=True)
+        kc, vc = alloc_caches(ctx, 1, 1)
+        gpu_quantize(ctx, K, K, "f32", [0], bt, 1, kc, vc)
+        refined = tq.tq_refine_counters(ctx)
+        got_k, got_v = kc.cpu().numpy(), vc.cpu().numpy()
+    finally:
+        tq.tq_destroy(ctx)
+    assert refined[0] >= 7 * 16
+    pages, slots, heads = seq_locations(bt, 0, np.arange(8), 1)
+    for kind, got in (("k", got_k), ("v", got_v)):
+        q = oracle.quantize_vectors(p, X.astype(np.float64), kind)
+        res = th.compare_records(p, kind, got, q, oracle.quantize_exclusions(p, q, kind), pages, slots, heads, 1)
+        assert res["codes_mismatch"] == 0 and res["norm_mismatch"] == 0, res
+        # the values within 1e-6 of a boundary were re-decided in fp64: they agree too
+        assert res["codes_excluded"] >= 7 * 16 and res["codes_mismatch_excluded"] == 0, res
+        if kind == "k":
+            assert res["signs_mismatch"] == 0, res
+
+
+def test_out_of_range_pages_are_skipped_and_flagged():
+    w = wl.Workload("t", "quantize", 2, 1, 1, 20, seed=3)
+    rng = np.random.default_rng(3)
+    K = wl.bf16_round(rng.standard_normal((2, 20, 1, 128)).astype(np.float32))
+    bt = np.array([[0, 7], [1, 2]], dtype=np.int32)     # page 7 does not exist (3 pages)
+    ctx = ctx_for(w)
+    try:
+        kc, vc = alloc_caches(ctx, 1, 3)
+        gpu_quantize(ctx, K, K, "bf16", [0, 30], bt, 3, kc, vc)   # seq 1: positions 30.. exceed 2 pages
+        flags = tq.tq_check_device_status(ctx)
+        assert flags & 1 and flags & 2
+        assert tq.tq_check_device_status(ctx) == 0               # cleared by the read
+        got = kc.cpu().numpy()
+    finally:
+        tq.tq_destroy(ctx)
+    p = th.params_for(w)
+    # tokens 0..15 of seq 0 landed in page 0; nothing else was written
+    pages, slots, heads = seq_locations(bt, 0, np.arange(16), 1)
+    q = oracle.quantize_vectors(p, K[0, :16, 0].astype(np.float64), "k")
+    th.assert_records_ok(th.compare_records(p, "k", got, q, oracle.quantize_exclusions(p, q, "k"),
+                                            pages, slots, heads, 1))
+    mask = th.touched_mask(p, "k", got.size, pages, slots, heads, 1)
+    assert np.all(got[~mask] == 0xA5)
+
+
+def test_invalid_arguments_launch_nothing():
+    w = wl.Workload("t", "quantize", 1, 1, 1, 4, seed=0)
+    ctx = ctx_for(w)
+    try:
+        kc, vc = alloc_caches(ctx, 1, 1)
+        bt = np.zeros((1, 1), np.int32)
+        with pytest.raises(tq.TQError):
+            gpu_quantize(ctx, np.zeros((1, 4, 1, 128), np.float32), None, "f32", [0], bt, 0, kc, vc)
+        with pytest.raises(tq.TQError):
+            tq.tq_quantize(ctx, kc, None, 7, 1, 1, 1, kc, kc, 1, 1, kc, None)
+        assert np.all(kc.cpu().numpy() == 0xA5)
+    finally:
+        tq.tq_destroy(ctx)
