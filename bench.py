@@ -1,0 +1,459 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized-KV hot path on GB300: one JSON line on stdout.
+
+A step is one pass of the whole path over one batch: for the decode workloads
+(default c3, Llama-3.1-8B-shaped, 16 x 32768 tokens, 3.5-bit K + QJL / 3.5-bit
+V) it appends one new token per sequence (tq_quantize) and runs decode
+attention over the L+1 cached tokens (tq_decode_attention, three stages); the
+quantize workload c2 appends 2,097,152 K/V vectors.  Headline value: packed
+cache bytes read per decode step / step time (GB/s); the c2 quantize rate
+(vectors/s) rides along in "quantize".  Inputs are synthetic (seeded), resident
+in HBM; the packed caches are larger than L2, so no flush is needed between
+steps.  --impl reference times the fp64 CPU oracle on the same workload.
+"""
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from online_kv_cache_02_gb300 import workloads as wl  # noqa: E402
+
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="c3", choices=["c3", "c4", "c5"])
+    ap.add_argument("--no-quantize", action="store_true", help="skip the c2 quantize measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks (NVML through ctypes; read-only queries)
+# ---------------------------------------------------------------------------
+
+REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+           0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
+
+
+class ClockSampler:
+    def __init__(self, torch):
+        self.ok = False
+        self.samples = []
+        self.reasons = 0
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            props = torch.cuda.get_device_properties(torch.cuda.current_device())
+            bus = getattr(props, "pci_bus_id", None)
+            got = 1
+            if bus is not None:
+                busid = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), bus, getattr(props, "pci_device_id", 0))
+                got = self.nv.nvmlDeviceGetHandleByPciBusId_v2(busid.encode(), ctypes.byref(self.h))
+            if got != 0:
+                got = self.nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.h))
+            if got != 0:
+                return
+            mx = ctypes.c_uint()
+            self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+            self.max_mhz = mx.value
+            self.reason_fn = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(self.nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except OSError:
+            pass
+
+    def _run(self):
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) == 0:
+                self.samples.append(c.value)
+            if self.reason_fn(self.h, ctypes.byref(r)) == 0:
+                self.reasons |= r.value
+            time.sleep(0.005)
+
+    def __enter__(self):
+        if self.ok:
+            self.stop = threading.Event()
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self.stop.set()
+            self.t.join()
+
+    def result(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "samples": len(self.samples),
+                "reasons": [n for b, n in REASONS.items() if self.reasons & b and n != "gpu_idle"]}
+
+
+def traffic_for(kernel_file, kernel):
+    """dram bytes per launch from a committed ncu capture, if the kernel source is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    with open(os.path.join(ROOT, "online_kv_cache_02_gb300", "csrc", kernel_file), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    return rec.get("bytes_per_launch") if rec.get("source_sha") == sha else None
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+class DecodeBench:
+    def __init__(self, w, torch, tq):
+        self.w, self.torch, self.tq = w, torch, tq
+        dev = torch.device("cuda", torch.cuda.current_device())
+        self.dev = dev
+        cfg = tq.make_config(k_bits=w.k_bits, v_bits=w.v_bits, m=w.m, seed=w.seed, k_qjl=w.qjl)
+        self.ctx = tq.tq_create_ex(cfg)
+        B, H, Hq = w.batch, w.kv_heads, w.q_heads
+        self.lens = wl.seq_lens(w)
+        self.bt = wl.block_table(w)
+        self.pps = self.bt.shape[1]
+        self.num_pages = B * self.pps
+        kpb, vpb = tq.tq_cache_layout(self.ctx, H)
+        self.kc = torch.empty(self.num_pages * kpb, dtype=torch.uint8, device=dev)
+        self.vc = torch.empty(self.num_pages * vpb, dtype=torch.uint8, device=dev)
+        self.bt_d = torch.from_numpy(self.bt).to(dev)
+        zero = torch.zeros(1, dtype=torch.int32, device=dev)
+        # history: quantize every cached token once (untimed)
+        for b in range(B):
+            L = int(self.lens[b])
+            for s0 in range(0, L, 8192):
+                n = min(8192, L - s0)
+                K = torch.from_numpy(wl.kv_tokens(w, "k", b, s0, n)).to(dev).to(torch.bfloat16)
+                V = torch.from_numpy(wl.kv_tokens(w, "v", b, s0, n)).to(dev).to(torch.bfloat16)
+                zero.fill_(s0)
+                tq.tq_quantize(self.ctx, K, V, tq.TQ_BF16, 1, n, H, zero, self.bt_d[b], self.pps, self.num_pages,
+                               self.kc, self.vc)
+        torch.cuda.synchronize()
+        assert tq.tq_check_device_status(self.ctx) == 0
+        self.knew_h = torch.from_numpy(wl.new_tokens(w, "k")).to(torch.bfloat16).pin_memory()
+        self.vnew_h = torch.from_numpy(wl.new_tokens(w, "v")).to(torch.bfloat16).pin_memory()
+        self.q_h = torch.from_numpy(wl.queries(w)).to(torch.bfloat16).pin_memory()
+        self.knew = self.knew_h.to(dev)
+        self.vnew = self.vnew_h.to(dev)
+        self.q = self.q_h.to(dev)
+        self.start = torch.from_numpy(self.lens.astype(np.int32)).to(dev)
+        self.lens1 = torch.from_numpy((self.lens + 1).astype(np.int32)).to(dev)
+        self.max_len = int(self.lens.max()) + 1
+        self.ws_n = tq.tq_workspace_size(self.ctx, B, Hq, self.max_len, w.chunk)
+        self.ws = torch.empty(self.ws_n, dtype=torch.uint8, device=dev)
+        self.out = torch.empty(B, Hq, 128, dtype=torch.float32, device=dev)
+        self.out_h = torch.empty(B, Hq, 128, dtype=torch.float32).pin_memory()
+        self.tokens = int((self.lens + 1).sum())
+        self.bytes_step = self.tokens * H * wl.packed_bytes_per_token_head(w)
+        self.launches_per_step = 2 + 3
+
+    def decode(self, stream, stages):
+        w, tq = self.w, self.tq
+        tq.tq_decode_attention_ex(self.ctx, self.q, tq.TQ_BF16, w.batch, w.q_heads, w.kv_heads, self.lens1,
+                                  self.max_len, self.bt_d, self.pps, self.num_pages, self.kc, self.vc, w.chunk,
+                                  1.0 / math.sqrt(128), self.out, self.ws, self.ws_n, stages, stream)
+
+    def append(self, stream):
+        w, tq = self.w, self.tq
+        tq.tq_quantize(self.ctx, self.knew, self.vnew, tq.TQ_BF16, w.batch, 1, w.kv_heads, self.start, self.bt_d,
+                       self.pps, self.num_pages, self.kc, self.vc, stream)
+
+    def step(self, stream, ev=None):
+        tq = self.tq
+        self.append(stream)
+        self.decode(stream, tq.TQ_STAGE_QPREP)
+        if ev is not None:
+            ev[0].record(stream)
+        self.decode(stream, tq.TQ_STAGE_PARTIALS)
+        if ev is not None:
+            ev[1].record(stream)
+        self.decode(stream, tq.TQ_STAGE_MERGE)
+
+    def step_e2e(self, stream):
+        self.knew.copy_(self.knew_h, non_blocking=True)
+        self.vnew.copy_(self.vnew_h, non_blocking=True)
+        self.q.copy_(self.q_h, non_blocking=True)
+        self.append(stream)
+        self.decode(stream, self.tq.TQ_STAGE_ALL)
+        self.out_h.copy_(self.out, non_blocking=True)
+
+    def e2e_bytes(self):
+        return (self.knew.numel() + self.vnew.numel() + self.q.numel()) * 2, self.out.numel() * 4
+
+    def close(self):
+        self.tq.tq_destroy(self.ctx)
+
+
+class QuantizeBench:
+    def __init__(self, w, torch, tq):
+        self.w, self.torch, self.tq = w, torch, tq
+        dev = torch.device("cuda", torch.cuda.current_device())
+        cfg = tq.make_config(k_bits=w.k_bits, v_bits=w.v_bits, m=w.m, seed=w.seed, k_qjl=w.qjl)
+        self.ctx = tq.tq_create_ex(cfg)
+        B, H, T = w.batch, w.kv_heads, w.seq_len
+        self.bt = wl.block_table(w)
+        self.pps = self.bt.shape[1]
+        self.num_pages = B * self.pps
+        kpb, vpb = tq.tq_cache_layout(self.ctx, H)
+        self.kc = torch.empty(self.num_pages * kpb, dtype=torch.uint8, device=dev)
+        self.vc = torch.empty(self.num_pages * vpb, dtype=torch.uint8, device=dev)
+        self.K = torch.empty(B, T, H, 128, dtype=torch.bfloat16, device=dev)
+        self.V = torch.empty(B, T, H, 128, dtype=torch.bfloat16, device=dev)
+        for b in range(B):
+            self.K[b] = torch.from_numpy(wl.kv_tokens(w, "k", b)).to(dev).to(torch.bfloat16)
+            self.V[b] = torch.from_numpy(wl.kv_tokens(w, "v", b)).to(dev).to(torch.bfloat16)
+        self.bt_d = torch.from_numpy(self.bt).to(dev)
+        self.start = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.vectors = 2 * B * T * H
+        self.bytes_in = self.vectors * 128 * 2
+        self.bytes_out = B * T * H * (kpb + vpb) // (16 * H)
+
+    def step(self, stream):
+        w, tq = self.w, self.tq
+        tq.tq_quantize(self.ctx, self.K, self.V, tq.TQ_BF16, w.batch, w.seq_len, w.kv_heads, self.start, self.bt_d,
+                       self.pps, self.num_pages, self.kc, self.vc, stream)
+
+    def close(self):
+        self.tq.tq_destroy(self.ctx)
+
+
+def timed(torch, stream, fn, steps, warmup, dist=None, per_step_events=None):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        fn(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    return ms
+
+
+def run_ours(args):
+    import torch
+    from online_kv_cache_02_gb300 import tq
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl")
+        dist = tdist
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = peaks()
+
+    w = wl.WORKLOADS[args.config]
+    db = DecodeBench(w, torch, tq)
+    steps, warmup = args.steps, max(3, args.warmup)
+    ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(steps)]
+    for _ in range(warmup):
+        db.step(stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch)
+    with sampler:
+        ms = timed(torch, stream, lambda i=None: db.step(stream, ev[i] if i is not None else None), steps, 0, dist)
+    kern_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    ms_step = ms / steps
+    value = db.bytes_step * world / (ms_step * 1e-3) / 1e9
+    achieved = db.bytes_step / (kern_ms * 1e-3) / 1e9
+    # end to end through the C ABI with host buffers
+    ms_e2e = timed(torch, stream, lambda i=None: db.step_e2e(stream), steps, warmup, dist)
+    h2d, d2h = db.e2e_bytes()
+    e2e_value = db.bytes_step * world / (ms_e2e / steps * 1e-3) / 1e9
+    flags = tq.tq_check_device_status(db.ctx)
+    line = {
+        "metric": "quantized-KV decode attention GB/s (% of HBM peak); KV vectors quantized/s",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps, "warmup": warmup,
+        "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "packed 2-4 bit codes + QJL signs, fp32 accumulation", "data": "synthetic (seeded N(0,1), outlier channels)",
+        "config": {"workload": f"{w.name}: decode step = append 1 token + attention, batch {w.batch}, "
+                               f"{w.q_heads}/{w.kv_heads} heads, head_dim 128, context {int(db.lens.max())}+1, "
+                               f"K {w.k_bits} bits + QJL m={w.m}, V {w.v_bits} bits",
+                   "packed_bytes_per_step": db.bytes_step, "hbm_fraction": round(value / world / peak, 4),
+                   "l2": f"packed cache {db.bytes_step / 2**20:.0f} MiB > L2 129 MiB, no flush needed",
+                   "parallelism": f"replicas x{world}, no collective"},
+        "roofline": {"kernel": "decode partials (per-chunk scoring + online softmax + value sums)", "bound": "hbm",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": db.bytes_step, "avg_launch_ms": round(kern_ms, 5),
+                     "traffic": traffic_for("tq_decode.cu", "chunk_kernel")},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": steps * db.launches_per_step,
+        "clocks": sampler.result(),
+        "device_flags": flags,
+    }
+    db.close()
+    del db
+    torch.cuda.empty_cache()
+    if not args.no_quantize:
+        qb = QuantizeBench(wl.WORKLOADS["c2"], torch, tq)
+        qsteps = max(3, min(steps, 20))
+        qs = ClockSampler(torch)
+        with qs:
+            qms = timed(torch, stream, lambda i=None: qb.step(stream), qsteps, warmup, dist)
+        qstep = qms / qsteps
+        qbytes = qb.bytes_in + qb.bytes_out
+        line["quantize"] = {
+            "workload": "c2: quantize-append 32 seq x 8 KV heads x 4096 tokens bf16, 3-bit K + QJL m=128 / 3-bit V, "
+                        "random block-table permutation",
+            "value": round(qb.vectors * world / (qstep * 1e-3), 1), "unit": "KV vectors/s", "ms_per_step": round(qstep, 4),
+            "steps": qsteps,
+            "roofline": {"kernel": "quantize (K and V launches)", "bound": "hbm",
+                         "achieved": round(qbytes / (qstep * 1e-3) / 1e9, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(qbytes / (qstep * 1e-3) / 1e9 / peak, 4), "peak_source": peak_kind,
+                         "algorithmic_bytes_per_launch": qbytes // 2,
+                         "traffic": traffic_for("tq_quantize.cu", "quantize_kernel")},
+            "refined": tq.tq_refine_counters(qb.ctx),
+            "clocks": qs.result(),
+        }
+        line["gpu_launches"] += 2 * qsteps
+        qb.close()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_decode_sample(w, seconds=15.0)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+class OracleDecode:
+    """One (sequence, KV head) of the workload, quantized and decoded by the fp64 oracle."""
+
+    def __init__(self, w, b=0, h=0):
+        import oracle
+        from oracle import turboquant as otq
+        self.o, self.otq = oracle, otq
+        self.w, self.b, self.h = w, b, h
+        self.p = oracle.make_params(d=128, m=w.m, k_bits=w.k_bits, v_bits=w.v_bits, seed=w.seed, k_qjl=w.qjl)
+        L = int(wl.seq_lens(w)[b])
+        self.L = L
+        K = wl.kv_tokens(w, "k", b)[:, h].astype(np.float64)
+        V = wl.kv_tokens(w, "v", b)[:, h].astype(np.float64)
+        self.kraw = oracle.pack_k_records(self.p, oracle.quantize_vectors(self.p, K, "k"))
+        self.vraw = oracle.pack_v_records(self.p, oracle.quantize_vectors(self.p, V, "v"))
+        self.knew = wl.new_tokens(w, "k")[b, :, h].astype(np.float64)
+        self.vnew = wl.new_tokens(w, "v")[b, :, h].astype(np.float64)
+        G = w.q_heads // w.kv_heads
+        self.Q = wl.queries(w)[b, h * G:(h + 1) * G].astype(np.float64)
+        self.bytes = (L + 1) * wl.packed_bytes_per_token_head(w)
+
+    def step(self):
+        o, p = self.o, self.p
+        kn = o.pack_k_records(p, o.quantize_vectors(p, self.knew, "k"))
+        vn = o.pack_v_records(p, o.quantize_vectors(p, self.vnew, "v"))
+        kr = o.unpack_k_records(p, {k: np.concatenate([self.kraw[k], kn[k]]) for k in kn})
+        vr = o.unpack_v_records(p, {k: np.concatenate([self.vraw[k], vn[k]]) for k in vn})
+        return [self.otq.attend_one(p, q, kr, vr, 1.0 / math.sqrt(128)) for q in self.Q]
+
+
+def oracle_decode_sample(w, seconds):
+    od = OracleDecode(w)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        od.step()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or n >= 50:
+            break
+    return {"value": round(od.bytes * n / el / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} steps of sequence 0, KV head 0 ({w.q_heads // w.kv_heads} query heads): append 1 token "
+                      f"+ fp64 decode over {od.L + 1} tokens ({od.bytes} packed bytes per step), "
+                      f"numpy with 1 BLAS thread"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = wl.WORKLOADS[args.config]
+    od = OracleDecode(w)
+    for _ in range(args.warmup):
+        od.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        od.step()
+    el = time.perf_counter() - t0
+    value = od.bytes * args.steps / el / 1e9
+    line = {
+        "impl": "reference",
+        "metric": "quantized-KV decode attention GB/s (% of HBM peak); KV vectors quantized/s",
+        "value": round(value, 6), "unit": "GB/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: oracle sample, sequence 0 KV head 0 of the decode step"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: append 1 token + fp64 decode of sequence 0, KV head 0 "
+                                   f"({w.q_heads // w.kv_heads} query heads) over {od.L + 1} tokens"},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

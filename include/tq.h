@@ -144,6 +144,26 @@ tq_status tq_decode_attention(const tq_ctx* ctx, const void* q, tq_dtype dtype,
                               float* out, void* workspace, size_t workspace_bytes,
                               void* stream);
 
+/* Same as tq_decode_attention, restricted to a subset of its three
+ * stream-ordered stages (bit mask): TQ_STAGE_QPREP (q~ = Pi q, S q~ into the
+ * workspace), TQ_STAGE_PARTIALS (per-chunk scores, online softmax and value
+ * sums into the workspace), TQ_STAGE_MERGE (log-sum-exp merge, inverse
+ * rotation, out).  Running the stages in order in separate calls with the
+ * same arguments equals one tq_decode_attention call; a later stage reads
+ * what the earlier one left in the workspace. */
+#define TQ_STAGE_QPREP 1
+#define TQ_STAGE_PARTIALS 2
+#define TQ_STAGE_MERGE 4
+#define TQ_STAGE_ALL 7
+tq_status tq_decode_attention_ex(const tq_ctx* ctx, const void* q, tq_dtype dtype,
+                                 int batch, int num_q_heads, int num_kv_heads,
+                                 const int32_t* seq_lens, int max_seq_len,
+                                 const int32_t* block_table, int max_pages_per_seq, int num_pages,
+                                 const void* k_cache, const void* v_cache,
+                                 int chunk_tokens, float softmax_scale,
+                                 float* out, void* workspace, size_t workspace_bytes,
+                                 int stages, void* stream);
+
 /* Synchronise the device and report (then clear) the context's device error
  * word: TQ_OK, or TQ_ERR_DEVICE_CHECK with the bits in *flags (may be NULL):
  * 1 = page id out of range, 2 = position beyond the block table,

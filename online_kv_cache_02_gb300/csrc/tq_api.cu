@@ -235,6 +235,18 @@ extern "C" tq_status tq_decode_attention(const tq_ctx* ctx, const void* q, tq_dt
                                          const void* k_cache, const void* v_cache, int chunk_tokens,
                                          float softmax_scale, float* out, void* workspace,
                                          size_t workspace_bytes, void* stream) {
+  return tq_decode_attention_ex(ctx, q, dtype, batch, Hq, H, seq_lens, max_seq_len, block_table, maxp, num_pages,
+                                k_cache, v_cache, chunk_tokens, softmax_scale, out, workspace, workspace_bytes,
+                                TQ_STAGE_ALL, stream);
+}
+
+extern "C" tq_status tq_decode_attention_ex(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batch,
+                                            int Hq, int H, const int32_t* seq_lens, int max_seq_len,
+                                            const int32_t* block_table, int maxp, int num_pages,
+                                            const void* k_cache, const void* v_cache, int chunk_tokens,
+                                            float softmax_scale, float* out, void* workspace,
+                                            size_t workspace_bytes, int stages, void* stream) {
+  if (stages < 1 || stages > TQ_STAGE_ALL) return TQ_ERR_INVALID_ARG;
   if (!ctx || batch < 0 || Hq < 1 || H < 1 || Hq % H || max_seq_len < 0 || maxp < 1 ||
       num_pages < 1 || chunk_tokens < 0 || chunk_tokens % kPage)
     return TQ_ERR_INVALID_ARG;
@@ -277,7 +289,7 @@ extern "C" tq_status tq_decode_attention(const tq_ctx* ctx, const void* q, tq_dt
   a.qprep = reinterpret_cast<float*>(w);
   a.part = reinterpret_cast<float*>(w + align256(sizeof(float) * static_cast<size_t>(batch) * Hq * (d + m)));
   a.out = out;
-  return launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  return launch_decode(a, stages, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 extern "C" tq_status tq_check_device_status(const tq_ctx* ctx, uint32_t* flags) {

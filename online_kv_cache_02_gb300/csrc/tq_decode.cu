@@ -289,24 +289,32 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
-  qprep_kernel<<<a.B * a.Hq, kThreads, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  switch (a.G) {
-    case 1: e = launch_g<1>(a, s); break;
-    case 2: e = launch_g<2>(a, s); break;
-    case 3: e = launch_g<3>(a, s); break;
-    case 4: e = launch_g<4>(a, s); break;
-    case 5: e = launch_g<5>(a, s); break;
-    case 6: e = launch_g<6>(a, s); break;
-    case 7: e = launch_g<7>(a, s); break;
-    case 8: e = launch_g<8>(a, s); break;
-    default: return cudaErrorInvalidValue;
+cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  if (stages & TQ_STAGE_QPREP) {
+    qprep_kernel<<<a.B * a.Hq, kThreads, 0, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
-  if (e != cudaSuccess) return e;
-  merge_kernel<<<a.B * a.Hq, kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  if (stages & TQ_STAGE_PARTIALS) {
+    switch (a.G) {
+      case 1: e = launch_g<1>(a, s); break;
+      case 2: e = launch_g<2>(a, s); break;
+      case 3: e = launch_g<3>(a, s); break;
+      case 4: e = launch_g<4>(a, s); break;
+      case 5: e = launch_g<5>(a, s); break;
+      case 6: e = launch_g<6>(a, s); break;
+      case 7: e = launch_g<7>(a, s); break;
+      case 8: e = launch_g<8>(a, s); break;
+      default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
+  }
+  if (stages & TQ_STAGE_MERGE) {
+    merge_kernel<<<a.B * a.Hq, kThreads, 0, s>>>(a);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 }  // namespace tq

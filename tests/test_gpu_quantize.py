@@ -142,9 +142,12 @@ def test_out_of_range_pages_are_skipped_and_flagged():
     finally:
         tq.tq_destroy(ctx)
     p = th.params_for(w)
-    # tokens 0..15 of seq 0 landed in page 0; nothing else was written
-    pages, slots, heads = seq_locations(bt, 0, np.arange(16), 1)
-    q = oracle.quantize_vectors(p, K[0, :16, 0].astype(np.float64), "k")
+    # tokens 0..15 of seq 0 landed in page 0, positions 30-31 of seq 1 in page 2; nothing else was written
+    pg0, sl0, hd0 = seq_locations(bt, 0, np.arange(16), 1)
+    pg1, sl1, hd1 = seq_locations(bt, 1, np.array([30, 31]), 1)
+    pages, slots, heads = np.r_[pg0, pg1], np.r_[sl0, sl1], np.r_[hd0, hd1]
+    X = np.concatenate([K[0, :16, 0], K[1, :2, 0]]).astype(np.float64)
+    q = oracle.quantize_vectors(p, X, "k")
     th.assert_records_ok(th.compare_records(p, "k", got, q, oracle.quantize_exclusions(p, q, "k"),
                                             pages, slots, heads, 1))
     mask = th.touched_mask(p, "k", got.size, pages, slots, heads, 1)
