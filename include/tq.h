@@ -164,6 +164,31 @@ tq_status tq_decode_attention_ex(const tq_ctx* ctx, const void* q, tq_dtype dtyp
                                  float* out, void* workspace, size_t workspace_bytes,
                                  int stages, void* stream);
 
+/* Decode attention for callers that cannot allocate device memory.  The
+ * paper has no counterpart: this entry point exists for callers that have no
+ * way to call cudaMalloc when they run decode (code running inside a custom
+ * allocator or memory pool, runtimes whose arena already owns the whole
+ * device, embeddings that only pass pointers they already own).  Same
+ * arguments and result as tq_decode_attention, without the workspace: the
+ * query projections and split-K partials go to a fixed array of
+ * TQ_NOALLOC_SCRATCH_BYTES that the library image holds on every device that
+ * loads it, until the process exits.  Nothing is allocated, by this call or
+ * by the library.  Returns TQ_ERR_WORKSPACE, launching nothing, when the
+ * sizes need more than TQ_NOALLOC_SCRATCH_BYTES (tq_workspace_size gives the
+ * need).  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, once per device); make that first call before any
+ * stream capture.  Every call on a device shares the array and it keeps the
+ * last call's contents (decode writes every byte it reads, so nothing needs
+ * clearing); calls whose work overlaps on the GPU race on it. */
+#define TQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+tq_status tq_decode_attention_noalloc(const tq_ctx* ctx, const void* q, tq_dtype dtype,
+                                      int batch, int num_q_heads, int num_kv_heads,
+                                      const int32_t* seq_lens, int max_seq_len,
+                                      const int32_t* block_table, int max_pages_per_seq, int num_pages,
+                                      const void* k_cache, const void* v_cache,
+                                      int chunk_tokens, float softmax_scale,
+                                      float* out, void* stream);
+
 /* Synchronise the device and report (then clear) the context's device error
  * word: TQ_OK, or TQ_ERR_DEVICE_CHECK with the bits in *flags (may be NULL):
  * 1 = page id out of range, 2 = position beyond the block table,

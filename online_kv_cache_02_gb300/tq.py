@@ -68,6 +68,8 @@ EXPORTS = {
                              _P, _P, _SZ, _P], _S),
     "tq_decode_attention_ex": ([_P, _P, _I, _I, _I, _I, _P, _I, _P, _I, _I, _P, _P, _I, ctypes.c_float,
                                 _P, _P, _SZ, _I, _P], _S),
+    "tq_decode_attention_noalloc": ([_P, _P, _I, _I, _I, _I, _P, _I, _P, _I, _I, _P, _P, _I, ctypes.c_float,
+                                     _P, _P], _S),
     "tq_check_device_status": ([_P, ctypes.POINTER(ctypes.c_uint32)], _S),
     "tq_refine_counters": ([_P, ctypes.POINTER(ctypes.c_ulonglong), _I], _S),
     "tq_status_string": ([_S], ctypes.c_char_p),
@@ -197,6 +199,19 @@ def tq_decode_attention_ex(ctx, q, dtype, batch, num_q_heads, num_kv_heads, seq_
         ctx, _ptr(q), dtype, batch, num_q_heads, num_kv_heads, _ptr(seq_lens), max_seq_len, _ptr(block_table),
         max_pages_per_seq, num_pages, _ptr(k_cache), _ptr(v_cache), chunk_tokens, softmax_scale, _ptr(out),
         _ptr(workspace), workspace_bytes, stages, _stream(stream)))
+
+
+def tq_decode_attention_noalloc(ctx, q, dtype, batch, num_q_heads, num_kv_heads, seq_lens, max_seq_len,
+                                block_table, max_pages_per_seq, num_pages, k_cache, v_cache, chunk_tokens,
+                                softmax_scale, out, stream=None):
+    """Decode attention with the library's fixed device scratch instead of a caller workspace."""
+    _check("tq_decode_attention_noalloc", _lib.tq_decode_attention_noalloc(
+        ctx, _ptr(q), dtype, batch, num_q_heads, num_kv_heads, _ptr(seq_lens), max_seq_len, _ptr(block_table),
+        max_pages_per_seq, num_pages, _ptr(k_cache), _ptr(v_cache), chunk_tokens, softmax_scale, _ptr(out),
+        _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def tq_check_device_status(ctx):
