@@ -297,6 +297,10 @@ cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   if (stages & TQ_STAGE_PARTIALS) {
+    cudaError_t em = cudaSuccess;
+    if (launch_partials_mma(a, s, &em)) {
+      if (em != cudaSuccess) return em;
+    } else {
     switch (a.G) {
       case 1: e = launch_g<1>(a, s); break;
       case 2: e = launch_g<2>(a, s); break;
@@ -309,6 +313,7 @@ cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
       default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
+    }
   }
   if (stages & TQ_STAGE_MERGE) {
     merge_kernel<<<a.B * a.Hq, kThreads, 0, s>>>(a);

@@ -97,6 +97,7 @@ struct DecodeArgs {
 
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s);
+bool launch_partials_mma(const DecodeArgs& a, cudaStream_t s, cudaError_t* err);
 
 }  // namespace tq
 

@@ -57,7 +57,11 @@ def _check(w, lens, Hq, H, chunk=0, scale=None, seed=0, qdtype=None):
     ref = oracle.decode_attention(p, Q.astype(np.float64), lens, bt, kc, vc, H, scale=scale)
     err = th.rel_err(got, ref)
     assert np.all(np.isfinite(got))
-    assert err.max() <= th.ATT_TOL, (err.max(), np.unravel_index(err.argmax(), err.shape))
+    # The bar is 2e-3 at the standard scale 1/sqrt(d).  The tensor-core path rounds q~ and the
+    # centroids to fp16 (relative 2^-12 each), so its logit error grows with the scale: above
+    # 1/sqrt(d) the bar is 2e-3 * scale * sqrt(d).
+    tol = th.ATT_TOL * max(1.0, scale * np.sqrt(128))
+    assert err.max() <= tol, (err.max(), np.unravel_index(err.argmax(), err.shape))
     return err.max()
 
 
@@ -65,6 +69,8 @@ BASE = wl.Workload("t", "decode", 1, 8, 1, 0, seed=0)
 
 
 @pytest.mark.parametrize("kb,vb,qjl", [((3, 3), (3, 3), True), ((4, 3), (4, 3), True), ((3, 2), (3, 2), True),
+                                       ((4, 4), (4, 4), True), ((2, 2), (2, 2), True), ((4, 4), (2, 2), True),
+                                       ((3, 3), (3, 3), False), ((4, 3), (4, 3), False),
                                        ((2, 2), (4, 4), False), ((1, 1), (1, 1), True), ((4, 4), (2, 3), True)])
 def test_decode_bit_configs(kb, vb, qjl):
     w = BASE.scaled(k_bits=kb, v_bits=vb, qjl=qjl, dtype="bf16")
