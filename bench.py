@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="c3", choices=["c3", "c4", "c5"])
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     ap.add_argument("--no-quantize", action="store_true", help="skip the c2 quantize measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -188,16 +189,35 @@ class DecodeBench:
         self.bytes_step = self.tokens * H * wl.packed_bytes_per_token_head(w)
         self.launches_per_step = 2 + 3
 
-    def decode(self, stream, stages):
+    def _marshal(self, stream):
+        """ctypes argument tuples of the per-step C calls, built once per stream (pointers are fixed)."""
+        import ctypes
         w, tq = self.w, self.tq
-        tq.tq_decode_attention_ex(self.ctx, self.q, tq.TQ_BF16, w.batch, w.q_heads, w.kv_heads, self.lens1,
-                                  self.max_len, self.bt_d, self.pps, self.num_pages, self.kc, self.vc, w.chunk,
-                                  1.0 / math.sqrt(128), self.out, self.ws, self.ws_n, stages, stream)
+        sp = stream.cuda_stream
+        quant = (self.ctx, self.knew.data_ptr(), self.vnew.data_ptr(), tq.TQ_BF16, w.batch, 1, w.kv_heads,
+                 self.start.data_ptr(), self.bt_d.data_ptr(), self.pps, self.num_pages, self.kc.data_ptr(),
+                 self.vc.data_ptr(), sp)
+        dec = [self.ctx, self.q.data_ptr(), tq.TQ_BF16, w.batch, w.q_heads, w.kv_heads, self.lens1.data_ptr(),
+               self.max_len, self.bt_d.data_ptr(), self.pps, self.num_pages, self.kc.data_ptr(), self.vc.data_ptr(),
+               w.chunk, ctypes.c_float(1.0 / math.sqrt(128)), self.out.data_ptr(), self.ws.data_ptr(), self.ws_n]
+        stages = {st: tuple(dec + [st, sp]) for st in (tq.TQ_STAGE_QPREP, tq.TQ_STAGE_PARTIALS, tq.TQ_STAGE_MERGE,
+                                                       tq.TQ_STAGE_ALL)}
+        self._args = (stream, quant, stages)
+
+    def _call(self, name, args):
+        st = getattr(self.tq._lib, name)(*args)
+        if st != 0:
+            raise self.tq.TQError(name, st)
+
+    def decode(self, stream, stages):
+        if getattr(self, "_args", (None,))[0] is not stream:
+            self._marshal(stream)
+        self._call("tq_decode_attention_ex", self._args[2][stages])
 
     def append(self, stream):
-        w, tq = self.w, self.tq
-        tq.tq_quantize(self.ctx, self.knew, self.vnew, tq.TQ_BF16, w.batch, 1, w.kv_heads, self.start, self.bt_d,
-                       self.pps, self.num_pages, self.kc, self.vc, stream)
+        if getattr(self, "_args", (None,))[0] is not stream:
+            self._marshal(stream)
+        self._call("tq_quantize", self._args[1])
 
     def step(self, stream, ev=None):
         tq = self.tq
@@ -211,11 +231,14 @@ class DecodeBench:
         self.decode(stream, tq.TQ_STAGE_MERGE)
 
     def step_e2e(self, stream):
+        """One step through the public fused call, inputs from pinned host memory, output back to host."""
+        w, tq = self.w, self.tq
         self.knew.copy_(self.knew_h, non_blocking=True)
         self.vnew.copy_(self.vnew_h, non_blocking=True)
         self.q.copy_(self.q_h, non_blocking=True)
-        self.append(stream)
-        self.decode(stream, self.tq.TQ_STAGE_ALL)
+        tq.tq_append_decode(self.ctx, self.knew, self.vnew, self.q, tq.TQ_BF16, w.batch, w.q_heads, w.kv_heads,
+                            self.start, self.max_len, self.bt_d, self.pps, self.num_pages, self.kc, self.vc, w.chunk,
+                            1.0 / math.sqrt(128), self.out, self.ws, self.ws_n, stream)
         self.out_h.copy_(self.out, non_blocking=True)
 
     def e2e_bytes(self):
@@ -258,7 +281,7 @@ class QuantizeBench:
         self.tq.tq_destroy(self.ctx)
 
 
-def timed(torch, stream, fn, steps, warmup, dist=None, per_step_events=None):
+def timed(torch, stream, fn, steps, warmup, dist=None):
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
@@ -296,6 +319,8 @@ def run_ours(args):
     peak, peak_kind = peaks()
 
     w = wl.WORKLOADS[args.config]
+    if args.batch:
+        w = w.scaled(batch=args.batch)
     db = DecodeBench(w, torch, tq)
     steps, warmup = args.steps, max(3, args.warmup)
     ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(steps)]
@@ -309,7 +334,7 @@ def run_ours(args):
     ms_step = ms / steps
     value = db.bytes_step * world / (ms_step * 1e-3) / 1e9
     achieved = db.bytes_step / (kern_ms * 1e-3) / 1e9
-    # end to end through the C ABI with host buffers
+    # end to end through the fused C-ABI call with host buffers
     ms_e2e = timed(torch, stream, lambda i=None: db.step_e2e(stream), steps, warmup, dist)
     h2d, d2h = db.e2e_bytes()
     e2e_value = db.bytes_step * world / (ms_e2e / steps * 1e-3) / 1e9

@@ -34,11 +34,15 @@
  *   One (page, head) block of the K cache holds, for its 16 token slots:
  *     codes[16][code_bytes_k] | signs[16][m/8] | norm fp16[16] | rnorm fp16[16]
  *   and of the V cache:  codes[16][code_bytes_v] | norm fp16[16].
- *   Codes of one vector form a little-endian bit stream: channel j (in the
- *   rotated basis) takes bits [off_j, off_j + b_j), b_j = bits_hi for
- *   j < split else bits_lo, off_j = sum of b over earlier channels, least
- *   significant code bit first.  Code values are 0-based, ascending with the
- *   centroid.  QJL sign i is bit i%8 of byte i/8 (1 = projection >= 0).
+ *   Codes of one vector form one bit stream (byte k = stream bits 8k..8k+7,
+ *   LSB first): channels [0, split) of the rotated vector first (bits_hi
+ *   each), then [split, d) (bits_lo).  Within a group, channel c's stored value
+ *   sits at group bits [b*c, b*c+b) for b = 1, 2, 4; for b = 3 channels come in
+ *   octets of 8 (24 bits at group bit 24*o): octet channel i < 6 at bits
+ *   4i..4i+2, channel 6 at bits 3/11/19, channel 7 at bits 7/15/23.  Codes are
+ *   0-based, ascending with the centroid; the stored value is the code, except
+ *   b = 4 which stores sign-magnitude (code >= 8 -> code-8, else 15-code).
+ *   QJL sign i is bit i%8 of byte i/8 (1 = projection >= 0).
  */
 #ifndef TQ_H_
 #define TQ_H_
@@ -188,6 +192,20 @@ tq_status tq_decode_attention_noalloc(const tq_ctx* ctx, const void* q, tq_dtype
                                       const void* k_cache, const void* v_cache,
                                       int chunk_tokens, float softmax_scale,
                                       float* out, void* stream);
+
+/* One decode step in one call ([P4] §2.3: the new token's K/V join the cache,
+ * then its query attends over every cached token): quantize-and-append
+ * k_new/v_new ([batch][1][H][d]) at position seq_lens[b] (lengths before the
+ * append, device int32), then decode attention over seq_lens[b] + 1 tokens.
+ * max_seq_len bounds the lengths after the append.  Same layouts, workspace
+ * and errors as tq_quantize + tq_decode_attention; stream-ordered, no host
+ * synchronisation. */
+tq_status tq_append_decode(const tq_ctx* ctx, const void* k_new, const void* v_new, const void* q,
+                           tq_dtype dtype, int batch, int num_q_heads, int num_kv_heads,
+                           const int32_t* seq_lens, int max_seq_len,
+                           const int32_t* block_table, int max_pages_per_seq, int num_pages,
+                           void* k_cache, void* v_cache, int chunk_tokens, float softmax_scale,
+                           float* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Synchronise the device and report (then clear) the context's device error
  * word: TQ_OK, or TQ_ERR_DEVICE_CHECK with the bits in *flags (may be NULL):

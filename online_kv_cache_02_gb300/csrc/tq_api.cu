@@ -57,6 +57,9 @@ void fill_layout(KindLayout& L, int bits_hi, int bits_lo, int split, int d, int 
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Split-K chunk length: the partials kernel keeps 3 CTAs resident per SM, so
+// pick the chunk count whose CTA total fills whole waves of 3 x SMs best
+// (chunks of at least 512 tokens, in multiples of 64).
 int pick_chunk(int units, int max_seq_len) {
   int sms = 152;
   int dev = 0;
@@ -64,13 +67,25 @@ int pick_chunk(int units, int max_seq_len) {
     int v = 0;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
   }
-  long long target = 4LL * sms;
-  long long nch = (target + units - 1) / units;
-  if (nch < 1) nch = 1;
-  long long chunk = (max_seq_len + nch - 1) / nch;
-  chunk = ((chunk + 63) / 64) * 64;
-  if (chunk < 64) chunk = 64;
-  return static_cast<int>(chunk);
+  const long long slots = 3LL * sms;
+  int best_chunk = ((max_seq_len + 63) / 64) * 64;
+  if (best_chunk < 64) best_chunk = 64;
+  double best_eff = -1.0;
+  for (int nch = 1; nch <= 256; ++nch) {
+    long long chunk = (max_seq_len + nch - 1) / nch;
+    chunk = ((chunk + 63) / 64) * 64;
+    if (chunk < 64) chunk = 64;
+    if (chunk < 512 && nch > 1) break;
+    const long long real = (max_seq_len + chunk - 1) / chunk;
+    const long long ctas = real * units;
+    const long long waves = (ctas + slots - 1) / slots;
+    const double eff = static_cast<double>(ctas) / static_cast<double>(waves * slots);
+    if (eff > best_eff + 0.02) {
+      best_eff = eff;
+      best_chunk = static_cast<int>(chunk);
+    }
+  }
+  return best_chunk;
 }
 
 }  // namespace
@@ -240,12 +255,12 @@ extern "C" tq_status tq_decode_attention(const tq_ctx* ctx, const void* q, tq_dt
                                 TQ_STAGE_ALL, stream);
 }
 
-extern "C" tq_status tq_decode_attention_ex(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batch,
-                                            int Hq, int H, const int32_t* seq_lens, int max_seq_len,
-                                            const int32_t* block_table, int maxp, int num_pages,
-                                            const void* k_cache, const void* v_cache, int chunk_tokens,
-                                            float softmax_scale, float* out, void* workspace,
-                                            size_t workspace_bytes, int stages, void* stream) {
+namespace {
+tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batch, int Hq, int H,
+                      const int32_t* seq_lens, int len_add, int max_seq_len, const int32_t* block_table, int maxp,
+                      int num_pages, const void* k_cache, const void* v_cache, int chunk_tokens,
+                      float softmax_scale, float* out, void* workspace, size_t workspace_bytes, int stages,
+                      void* stream) {
   if (stages < 1 || stages > TQ_STAGE_ALL) return TQ_ERR_INVALID_ARG;
   if (!ctx || batch < 0 || Hq < 1 || H < 1 || Hq % H || max_seq_len < 0 || maxp < 1 ||
       num_pages < 1 || chunk_tokens < 0 || chunk_tokens % kPage)
@@ -270,6 +285,7 @@ extern "C" tq_status tq_decode_attention_ex(const tq_ctx* ctx, const void* q, tq
   a.H = H;
   a.G = Hq / H;
   a.seq_lens = seq_lens;
+  a.len_add = len_add;
   a.max_seq_len = max_seq_len;
   a.block_table = block_table;
   a.maxp = maxp;
@@ -290,6 +306,38 @@ extern "C" tq_status tq_decode_attention_ex(const tq_ctx* ctx, const void* q, tq
   a.part = reinterpret_cast<float*>(w + align256(sizeof(float) * static_cast<size_t>(batch) * Hq * (d + m)));
   a.out = out;
   return launch_decode(a, stages, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" tq_status tq_decode_attention_ex(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batch,
+                                            int Hq, int H, const int32_t* seq_lens, int max_seq_len,
+                                            const int32_t* block_table, int maxp, int num_pages,
+                                            const void* k_cache, const void* v_cache, int chunk_tokens,
+                                            float softmax_scale, float* out, void* workspace,
+                                            size_t workspace_bytes, int stages, void* stream) {
+  return decode_impl(ctx, q, dtype, batch, Hq, H, seq_lens, 0, max_seq_len, block_table, maxp, num_pages, k_cache,
+                     v_cache, chunk_tokens, softmax_scale, out, workspace, workspace_bytes, stages, stream);
+}
+
+extern "C" tq_status tq_append_decode(const tq_ctx* ctx, const void* k_new, const void* v_new, const void* q,
+                                      tq_dtype dtype, int batch, int Hq, int H, const int32_t* seq_lens,
+                                      int max_seq_len, const int32_t* block_table, int maxp, int num_pages,
+                                      void* k_cache, void* v_cache, int chunk_tokens, float softmax_scale,
+                                      float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!ctx || !k_new || !v_new || batch < 0 || H < 1 || Hq < 1 || Hq % H || max_seq_len < 1)
+    return TQ_ERR_INVALID_ARG;
+  if (batch == 0) return TQ_OK;
+  // check the decode arguments before anything is launched
+  size_t need = 0;
+  tq_status st = tq_workspace_size(ctx, batch, Hq, max_seq_len, chunk_tokens, &need);
+  if (st != TQ_OK) return st;
+  if (!q || !out || !workspace || !seq_lens || !block_table) return TQ_ERR_INVALID_ARG;
+  if (Hq / H > kMaxGroup) return TQ_ERR_UNSUPPORTED;
+  st = tq_quantize(ctx, k_new, v_new, dtype, batch, 1, H, seq_lens, block_table, maxp, num_pages, k_cache, v_cache,
+                   stream);
+  if (st != TQ_OK) return st;
+  return decode_impl(ctx, q, dtype, batch, Hq, H, seq_lens, 1, max_seq_len, block_table, maxp, num_pages, k_cache,
+                     v_cache, chunk_tokens, softmax_scale, out, workspace, workspace_bytes, TQ_STAGE_ALL, stream);
 }
 
 extern "C" tq_status tq_check_device_status(const tq_ctx* ctx, uint32_t* flags) {

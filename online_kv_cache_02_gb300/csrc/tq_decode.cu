@@ -45,26 +45,64 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// q~ = Pi q and u = S q~ for 16 query heads per block, Pi^T and S^T read once per block.
+constexpr int kQB = 16;
+
 __global__ void __launch_bounds__(kThreads) qprep_kernel(DecodeArgs a) {
-  __shared__ float qs[kD];
-  __shared__ float qt[kD];
-  const long long bh = blockIdx.x;
+  __shared__ float qs[kQB][kD];
+  __shared__ float qt[kQB][kD];
+  const long long r0 = static_cast<long long>(blockIdx.x) * kQB;
+  const long long nq = static_cast<long long>(a.B) * a.Hq;
   const int i = threadIdx.x;
-  qs[i] = load_q(a.q, a.f32, bh * kD + i);
+  for (int r = 0; r < kQB; ++r) qs[r][i] = r0 + r < nq ? load_q(a.q, a.f32, (r0 + r) * kD + i) : 0.0f;
   __syncthreads();
-  float acc = 0.0f;
-#pragma unroll 8
-  for (int k = 0; k < kD; ++k) acc = fmaf(a.tab.pit[k * kD + i], qs[k], acc);
-  qt[i] = acc;
-  __syncthreads();
-  float* dst = a.qprep + bh * (kD + a.m);
-  dst[i] = acc;
-  for (int p = i; p < a.m; p += kThreads) {
-    float u = 0.0f;
-#pragma unroll 8
-    for (int j = 0; j < kD; ++j) u = fmaf(a.tab.st[j * a.m + p], qt[j], u);
-    dst[kD + p] = u;
+  float acc[kQB];
+#pragma unroll
+  for (int r = 0; r < kQB; ++r) acc[r] = 0.0f;
+#pragma unroll 4
+  for (int k = 0; k < kD; ++k) {
+    const float p = a.tab.pit[k * kD + i];
+#pragma unroll
+    for (int r = 0; r < kQB; ++r) acc[r] = fmaf(p, qs[r][k], acc[r]);
   }
+#pragma unroll
+  for (int r = 0; r < kQB; ++r) qt[r][i] = acc[r];
+  __syncthreads();
+  for (int r = 0; r < kQB; ++r)
+    if (r0 + r < nq) a.qprep[(r0 + r) * (kD + a.m) + i] = qt[r][i];
+  for (int p = i; p < a.m; p += kThreads) {
+#pragma unroll
+    for (int r = 0; r < kQB; ++r) acc[r] = 0.0f;
+#pragma unroll 4
+    for (int j = 0; j < kD; ++j) {
+      const float sv = a.tab.st[j * a.m + p];
+#pragma unroll
+      for (int r = 0; r < kQB; ++r) acc[r] = fmaf(sv, qt[r][j], acc[r]);
+    }
+    for (int r = 0; r < kQB; ++r)
+      if (r0 + r < nq) a.qprep[(r0 + r) * (kD + a.m) + kD + p] = acc[r];
+  }
+}
+
+// Code of channel j from a vector's code words (the stored format of tq.h).
+__device__ __forceinline__ int code_at(const unsigned* rec, int bh, int bl, int split, int j) {
+  const int grp = j < split ? 0 : 1;
+  const int b = grp ? bl : bh;
+  const int c = grp ? j - split : j;
+  const int base = grp ? split * bh : 0;
+  auto bitsat = [&](int off, int n) {
+    const unsigned long long pair = (static_cast<unsigned long long>(rec[(off >> 5) + 1]) << 32) | rec[off >> 5];
+    return static_cast<int>((pair >> (off & 31)) & ((1u << n) - 1u));
+  };
+  if (b == 3) {
+    const int ob = base + 24 * (c >> 3), i = c & 7;
+    if (i < 6) return bitsat(ob + 4 * i, 3);
+    const int s = ob + 3 + 4 * (i - 6);
+    return bitsat(s, 1) | (bitsat(s + 8, 1) << 1) | (bitsat(s + 16, 1) << 2);
+  }
+  const int v = bitsat(base + b * c, b);
+  if (b == 4) return (v & 8) ? 7 - (v & 7) : 8 + v;
+  return v;
 }
 
 template <int G>
@@ -93,7 +131,7 @@ __global__ void __launch_bounds__(kThreads) chunk_kernel(DecodeArgs a) {
     ck_s[gi][k] = a.kl.g[gi].c[k];
     cv_s[gi][k] = a.vl.g[gi].c[k];
   }
-  int L = a.seq_lens[b];
+  int L = a.seq_lens[b] + a.len_add;
   if (L < 0 || L > a.max_seq_len || L > a.maxp * kPage) {
     if (threadIdx.x == 0 && chunk == 0 && h == 0) atomicOr(a.tab.err, kErrSeqLen);
     L = L < 0 ? 0 : L;
@@ -122,8 +160,6 @@ __global__ void __launch_bounds__(kThreads) chunk_kernel(DecodeArgs a) {
   // this lane's 4 value channels
   const int vj0 = 4 * lane;
   const int vgrp = vj0 < vsplit ? 1 : 0;   // 1 -> hi group
-  const int vbits = vgrp ? vbh : vbl;
-  const int voff = vj0 < vsplit ? vj0 * vbh : vsplit * vbh + (vj0 - vsplit) * vbl;
   const float* cvt = cv_s[vgrp ? 0 : 1];
 
   for (int base = t0 + warp * 32; base < t1; base += 4 * 32) {
@@ -148,16 +184,11 @@ __global__ void __launch_bounds__(kThreads) chunk_kernel(DecodeArgs a) {
       float s1[G], s2[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) s1[g] = s2[g] = 0.0f;
-      int off = 0;
       for (int j = 0; j < kD; ++j) {
-        const int bits = j < ksplit ? kbh : kbl;
-        const int w = off >> 5, sh = off & 31;
-        unsigned long long pair = (static_cast<unsigned long long>(rec[w + 1]) << 32) | rec[w];
-        const int code = static_cast<int>((pair >> sh) & ((1u << bits) - 1u));
+        const int code = code_at(rec, kbh, kbl, ksplit, j);
         const float c = ck_s[j < ksplit ? 0 : 1][code];
 #pragma unroll
         for (int g = 0; g < G; ++g) s1[g] = fmaf(c, qt_s[g][j], s1[g]);
-        off += bits;
       }
       const unsigned* sw = reinterpret_cast<const unsigned*>(kb + a.kl.off_signs + slot * (a.m / 8));
       for (int w = 0; w < swords; ++w) {
@@ -207,14 +238,9 @@ __global__ void __launch_bounds__(kThreads) chunk_kernel(DecodeArgs a) {
                                 static_cast<long long>(h) * a.vl.block_bytes;
       const unsigned* vw = reinterpret_cast<const unsigned*>(vb + ts * a.vl.code_bytes);
       const float nv = __half2float(reinterpret_cast<const __half*>(vb + a.vl.off_norm)[ts]) * kInvSqrtD;
-      const int wi = voff >> 5, sh = voff & 31;
-      const unsigned lo = vw[wi];
-      const unsigned hi = (wi + 1 < a.vl.code_bytes / 4) ? vw[wi + 1] : 0u;
-      const unsigned long long pair = (static_cast<unsigned long long>(hi) << 32) | lo;
-      const unsigned bitsv = static_cast<unsigned>(pair >> sh);
       float cv[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) cv[q] = cvt[(bitsv >> (q * vbits)) & ((1u << vbits) - 1u)];
+      for (int q = 0; q < 4; ++q) cv[q] = cvt[code_at(vw, vbh, vbl, vsplit, vj0 + q)];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const float wg = w[g] * nv;
@@ -257,27 +283,36 @@ __global__ void __launch_bounds__(kThreads) chunk_kernel(DecodeArgs a) {
   }
 }
 
+// Log-sum-exp merge of the chunk partials and o = Pi^T (acc / l): one block
+// per (sequence, KV head) for its G query heads, Pi read once per block.
 __global__ void __launch_bounds__(kThreads) merge_kernel(DecodeArgs a) {
-  __shared__ float os[kD];
-  const long long bh = blockIdx.x;
+  __shared__ float os[kMaxGroup][kD];
+  const long long r0 = static_cast<long long>(blockIdx.x) * a.G;   // first query head (b*Hq + h*G)
   const int j = threadIdx.x;
-  const float* P = a.part + bh * a.nchunks * (kD + 2);
-  float M = -INFINITY;
-  for (int c = 0; c < a.nchunks; ++c) M = fmaxf(M, P[c * (kD + 2)]);
-  float l = 0.0f, A = 0.0f;
-  for (int c = 0; c < a.nchunks; ++c) {
-    const float mc = P[c * (kD + 2)];
-    if (mc == -INFINITY) continue;
-    const float w = exp2f(mc - M);
-    l = fmaf(w, P[c * (kD + 2) + 1], l);
-    A = fmaf(w, P[c * (kD + 2) + 2 + j], A);
+  for (int r = 0; r < a.G; ++r) {
+    const float* P = a.part + (r0 + r) * a.nchunks * (kD + 2);
+    float M = -INFINITY;
+    for (int c = 0; c < a.nchunks; ++c) M = fmaxf(M, P[c * (kD + 2)]);
+    float l = 0.0f, A = 0.0f;
+#pragma unroll 4
+    for (int c = 0; c < a.nchunks; ++c) {
+      const float w = exp2f(P[c * (kD + 2)] - M);
+      l = fmaf(w, P[c * (kD + 2) + 1], l);
+      A = fmaf(w, P[c * (kD + 2) + 2 + j], A);
+    }
+    os[r][j] = l > 0.0f ? A / l : 0.0f;
   }
-  os[j] = l > 0.0f ? A / l : 0.0f;
   __syncthreads();
-  float o = 0.0f;
-#pragma unroll 8
-  for (int i = 0; i < kD; ++i) o = fmaf(a.tab.pi[i * kD + j], os[i], o);
-  a.out[bh * kD + j] = o;
+  float o[kMaxGroup];
+#pragma unroll
+  for (int r = 0; r < kMaxGroup; ++r) o[r] = 0.0f;
+#pragma unroll 4
+  for (int i = 0; i < kD; ++i) {
+    const float p = a.tab.pi[i * kD + j];
+#pragma unroll
+    for (int r = 0; r < kMaxGroup; ++r) o[r] = fmaf(p, os[r][i], o[r]);
+  }
+  for (int r = 0; r < a.G; ++r) a.out[(r0 + r) * kD + j] = o[r];
 }
 
 template <int G>
@@ -292,7 +327,7 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
 cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
   if (stages & TQ_STAGE_QPREP) {
-    qprep_kernel<<<a.B * a.Hq, kThreads, 0, s>>>(a);
+    qprep_kernel<<<(a.B * a.Hq + kQB - 1) / kQB, kThreads, 0, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -316,7 +351,7 @@ cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
     }
   }
   if (stages & TQ_STAGE_MERGE) {
-    merge_kernel<<<a.B * a.Hq, kThreads, 0, s>>>(a);
+    merge_kernel<<<a.B * a.H, kThreads, 0, s>>>(a);
     e = cudaGetLastError();
   }
   return e;

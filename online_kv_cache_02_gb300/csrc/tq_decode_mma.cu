@@ -45,6 +45,10 @@ constexpr float kInvSqrtD = 0.08838834764831845f;
 constexpr float kSqrtHalfPi = 1.2533141373155003f;
 constexpr uint32_t kErrTimeout = 8u;
 constexpr int kWaitLimit = 1 << 22;
+// Finite "minus infinity": exp2 of (sentinel - finite) is exactly 0, and an
+// all-empty chunk ends with max = sentinel, acc = 0, so its merge weight or
+// its value is 0 either way; no -inf tests are needed around exp2.
+constexpr float kNegBig = -1.0e30f;
 
 // ---------------------------------------------------------------------------
 // PTX helpers
@@ -156,10 +160,13 @@ __device__ __forceinline__ void deq8(uint32_t v, const Tab& t, uint32_t (&h)[4])
 
 template <>
 __device__ __forceinline__ void deq8<3>(uint32_t v, const Tab& t, uint32_t (&h)[4]) {
-  // spread the eight 3-bit fields to nibbles (bit 3 of every nibble zero)
-  uint32_t x = (v & 0xFFFu) | ((v << 4) & 0x0FFF0000u);
-  x = (x & 0x003F003Fu) | ((x << 2) & 0x3F003F00u);
-  x = (x & 0x07070707u) | ((x << 1) & 0x70707070u);
+  // stored octet: channels 0-5 already in nibbles; channels 6, 7 in the spare
+  // bit 3 of each nibble, gathered into nibbles 6, 7 by one multiply
+  // (bits 3/11/19 -> 24/25/26, 7/15/23 -> 28/29/30; the other partial
+  // products land on distinct bits below 24, so nothing carries)
+  const uint32_t xm = v & 0x00777777u;
+  const uint32_t sp = (v & 0x00888888u) * 0x00204080u;
+  const uint32_t x = xm | (sp & 0x77000000u);
   const uint32_t xh = x >> 16;
   const uint32_t rl0 = prmt(t.l0, t.l1, x), rh0 = prmt(t.h0, t.h1, x);
   const uint32_t rl1 = prmt(t.l0, t.l1, xh), rh1 = prmt(t.h0, t.h1, xh);
@@ -171,9 +178,9 @@ __device__ __forceinline__ void deq8<3>(uint32_t v, const Tab& t, uint32_t (&h)[
 
 template <>
 __device__ __forceinline__ void deq8<4>(uint32_t w, const Tab& t, uint32_t (&h)[4]) {
-  // ascending 4-bit codes: code >= 8 -> +M[code-8]; code < 8 -> -M[7-code]
-  const uint32_t neg = ~w & 0x88888888u;                       // bit 3 of a nibble: negative centroid
-  const uint32_t idx = (w ^ ((neg >> 3) * 7u)) & 0x77777777u;  // magnitude index
+  // stored sign-magnitude nibbles: bit 3 = negative half, bits 0-2 = rank of |centroid|
+  const uint32_t neg = w & 0x88888888u;
+  const uint32_t idx = w & 0x77777777u;
   const uint32_t a = prmt(idx, 0u, 0x0020u);                   // nibbles n0 n1 n4 n5
   const uint32_t b = prmt(idx, 0u, 0x0031u);                   // nibbles n2 n3 n6 n7
   const uint32_t rla = prmt(t.l0, t.l1, a), rha = prmt(t.h0, t.h1, a);
@@ -196,8 +203,11 @@ __device__ __forceinline__ void deq8<2>(uint32_t v, const Tab& t, uint32_t (&h)[
   h[3] = prmt(rly, rhy, 0x7362u);   // (c5, c7)
 }
 
-// Field of `nbits` (<= 32) bits at bit offset `off` of a word array in shared memory.
+// The 8*B-bit field at bit offset `off` of a word array in shared memory
+// (4-bit fields are word aligned and need no shift).
+template <int B>
 __device__ __forceinline__ uint32_t field(const uint32_t* row, int off) {
+  if (B == 4) return row[off >> 5];
   const int w = off >> 5, sh = off & 31;
   return __funnelshift_r(row[w], row[w + 1], sh);
 }
@@ -274,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_mma_kernel(DecodeArgs a) {
     uf[p] = (QJL && head_ok) ? pack_h2(qrow[kD + plo], qrow[kD + phi]) : 0u;
   }
 
-  int L = a.seq_lens[b];
+  int L = a.seq_lens[b] + a.len_add;
   if (L < 0 || L > a.max_seq_len || L > a.maxp * kPage) {
     if (threadIdx.x == 0 && chunk == 0 && h == 0) atomicOr(a.tab.err, kErrSeqLen);
     L = L < 0 ? 0 : L;
@@ -324,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_mma_kernel(DecodeArgs a) {
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
-  float m_run[2] = {-INFINITY, -INFINITY};
+  float m_run[2] = {kNegBig, kNegBig};
   float l_run[2] = {0.0f, 0.0f};
   const float k1 = kInvSqrtD * a.scale_log2;
   const float k2 = kSqrtHalfPi / 128.0f * a.scale_log2;
@@ -352,12 +362,12 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_mma_kernel(DecodeArgs a) {
         uint32_t ha[4], hb[4];
         if (u < 2) {
           const int off = 32 * u * KBH + 8 * t * KBH;
-          deq8<KBH>(field(rg, off), tk0, ha);
-          deq8<KBH>(field(rg8, off), tk0, hb);
+          deq8<KBH>(field<KBH>(rg, off), tk0, ha);
+          deq8<KBH>(field<KBH>(rg8, off), tk0, hb);
         } else {
           const int off = 64 * KBH + 32 * (u - 2) * KBL + 8 * t * KBL;
-          deq8<KBL>(field(rg, off), tk1, ha);
-          deq8<KBL>(field(rg8, off), tk1, hb);
+          deq8<KBL>(field<KBL>(rg, off), tk1, ha);
+          deq8<KBL>(field<KBL>(rg8, off), tk1, hb);
         }
         mma16816(s1, ha[0], hb[0], ha[1], hb[1], qf[4 * u + 0], qf[4 * u + 1]);
         mma16816(s1, ha[2], hb[2], ha[3], hb[3], qf[4 * u + 2], qf[4 * u + 3]);
@@ -381,10 +391,10 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_mma_kernel(DecodeArgs a) {
     {
       const float nkg = __half2float(nk[g]), nkg8 = __half2float(nk[g + 8]);
       const float rkg = QJL ? __half2float(rk[g]) : 0.f, rkg8 = QJL ? __half2float(rk[g + 8]) : 0.f;
-      lg[0] = vg ? fmaf(nkg * k1, s1[0], rkg * k2 * s2[0]) : -INFINITY;
-      lg[1] = vg ? fmaf(nkg * k1, s1[1], rkg * k2 * s2[1]) : -INFINITY;
-      lg[2] = vg8 ? fmaf(nkg8 * k1, s1[2], rkg8 * k2 * s2[2]) : -INFINITY;
-      lg[3] = vg8 ? fmaf(nkg8 * k1, s1[3], rkg8 * k2 * s2[3]) : -INFINITY;
+      lg[0] = vg ? fmaf(nkg * k1, s1[0], rkg * k2 * s2[0]) : kNegBig;
+      lg[1] = vg ? fmaf(nkg * k1, s1[1], rkg * k2 * s2[1]) : kNegBig;
+      lg[2] = vg8 ? fmaf(nkg8 * k1, s1[2], rkg8 * k2 * s2[2]) : kNegBig;
+      lg[3] = vg8 ? fmaf(nkg8 * k1, s1[3], rkg8 * k2 * s2[3]) : kNegBig;
     }
     // ---- online softmax over this page (heads 2t, 2t+1) -------------------
     float pr[4];
@@ -395,9 +405,9 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_mma_kernel(DecodeArgs a) {
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
       const float m_new = fmaxf(m_run[c], mx);
-      const float alpha = m_run[c] == -INFINITY ? 0.0f : exp2f(m_run[c] - m_new);
-      pr[c] = lg[c] == -INFINITY ? 0.0f : exp2f(lg[c] - m_new);
-      pr[c + 2] = lg[c + 2] == -INFINITY ? 0.0f : exp2f(lg[c + 2] - m_new);
+      const float alpha = exp2f(m_run[c] - m_new);
+      pr[c] = exp2f(lg[c] - m_new);
+      pr[c + 2] = exp2f(lg[c + 2] - m_new);
       l_run[c] = fmaf(l_run[c], alpha, pr[c] + pr[c + 2]);
       m_run[c] = m_new;
 #pragma unroll
@@ -428,8 +438,8 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_mma_kernel(DecodeArgs a) {
         const uint32_t* r1 = reinterpret_cast<const uint32_t*>(vb + (ta + 1) * CBV);
         uint32_t x0[4], x1[4];
         // chunk A: channels 8g..8g+7 (hi group)
-        deq8<VBH>(field(r0, 8 * g * VBH), tv0, x0);
-        deq8<VBH>(field(r1, 8 * g * VBH), tv0, x1);
+        deq8<VBH>(field<VBH>(r0, 8 * g * VBH), tv0, x0);
+        deq8<VBH>(field<VBH>(r1, 8 * g * VBH), tv0, x1);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           bool hi;
@@ -437,8 +447,8 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_mma_kernel(DecodeArgs a) {
           fa[c][tp] = prmt(x0[j], x1[j], hi ? 0x7632u : 0x5410u);
         }
         // chunk B: channels 64+8g..64+8g+7 (lo group)
-        deq8<VBL>(field(r0, 64 * VBH + 8 * g * VBL), tv1, x0);
-        deq8<VBL>(field(r1, 64 * VBH + 8 * g * VBL), tv1, x1);
+        deq8<VBL>(field<VBL>(r0, 64 * VBH + 8 * g * VBL), tv1, x0);
+        deq8<VBL>(field<VBL>(r1, 64 * VBH + 8 * g * VBL), tv1, x1);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           bool hi;
@@ -474,13 +484,12 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_mma_kernel(DecodeArgs a) {
   __syncthreads();
   const int j = threadIdx.x;
   for (int hh = 0; hh < a.G; ++hh) {
-    float M = -INFINITY;
+    float M = kNegBig;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][hh]);
     float lsum = 0.0f, A = 0.0f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      if (red_m[w][hh] == -INFINITY) continue;
       const float sc = exp2f(red_m[w][hh] - M);
       lsum = fmaf(sc, red_l[w][hh], lsum);
       A = fmaf(sc, red_acc[w][hh][j], A);

@@ -79,6 +79,7 @@ struct DecodeArgs {
   int f32;
   int B, Hq, H, G;
   const int32_t* seq_lens;
+  int len_add;           // tokens appended in the same call (added to seq_lens[b])
   int max_seq_len;
   const int32_t* block_table;
   int maxp, num_pages;

@@ -133,22 +133,49 @@ __device__ Smem carve(unsigned char* p) {
   return s;
 }
 
-__device__ __forceinline__ int channel_off(const KindLayout& L, int j) {
-  return j < L.split ? j * L.g[0].bits : L.split * L.g[0].bits + (j - L.split) * L.g[1].bits;
+// Stored 24-bit octet of eight 3-bit codes: channels 0-5 in nibbles (bits
+// 4i..4i+2), channel 6 in bits 3/11/19 and channel 7 in bits 7/15/23.
+__device__ __forceinline__ unsigned octet3(const unsigned char* c) {
+  unsigned v = 0;
+  for (int i = 0; i < 6; ++i) v |= static_cast<unsigned>(c[i]) << (4 * i);
+  for (int q = 0; q < 3; ++q) {
+    v |= ((c[6] >> q) & 1u) << (8 * q + 3);
+    v |= ((c[7] >> q) & 1u) << (8 * q + 7);
+  }
+  return v;
 }
 
-// 32-bit word w of a vector's code stream, from one byte per channel.
+// Stored 4-bit value: sign-magnitude (bit 3 = negative half, bits 0-2 = rank of |centroid|).
+__device__ __forceinline__ unsigned stored4(unsigned c) { return c >= 8 ? c - 8 : 15 - c; }
+
+// 32-bit word w of a vector's code area, from one byte per channel.
 __device__ unsigned pack_code_word(const KindLayout& L, const unsigned char* codes, int w) {
-  const int bh = L.g[0].bits, bl = L.g[1].bits;
   const int lo = 32 * w, hi = lo + 32;
-  int j = lo < L.split * bh ? lo / bh : L.split + (lo - L.split * bh) / bl;
   unsigned word = 0;
-  for (; j < kD; ++j) {
-    int off = channel_off(L, j);
-    if (off >= hi) break;
-    unsigned long long c = codes[j];
-    int sh = off - lo;
-    word |= sh >= 0 ? static_cast<unsigned>(c << sh) : static_cast<unsigned>(c >> (-sh));
+  for (int grp = 0; grp < 2; ++grp) {
+    const int b = L.g[grp].bits;
+    const int c0 = grp ? L.split : 0;
+    const int n = grp ? kD - L.split : L.split;
+    const int base = grp ? L.split * L.g[0].bits : 0;
+    if (n == 0 || base >= hi || base + n * b <= lo) continue;
+    if (b == 3) {
+      for (int o = 0; o < n / 8; ++o) {
+        const int off = base + 24 * o;
+        if (off >= hi || off + 24 <= lo) continue;
+        const unsigned long long v = octet3(codes + c0 + 8 * o);
+        const int sh = off - lo;
+        word |= sh >= 0 ? static_cast<unsigned>(v << sh) : static_cast<unsigned>(v >> (-sh));
+      }
+    } else {
+      const int cs = lo > base ? (lo - base) / b : 0;
+      const int ce = min(n, (hi - base + b - 1) / b);
+      for (int c = cs; c < ce; ++c) {
+        unsigned long long v = codes[c0 + c];
+        if (b == 4) v = stored4(static_cast<unsigned>(v));
+        const int sh = base + b * c - lo;
+        word |= sh >= 0 ? static_cast<unsigned>(v << sh) : static_cast<unsigned>(v >> (-sh));
+      }
+    }
   }
   return word;
 }

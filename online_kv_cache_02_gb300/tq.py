@@ -70,6 +70,8 @@ EXPORTS = {
                                 _P, _P, _SZ, _I, _P], _S),
     "tq_decode_attention_noalloc": ([_P, _P, _I, _I, _I, _I, _P, _I, _P, _I, _I, _P, _P, _I, ctypes.c_float,
                                      _P, _P], _S),
+    "tq_append_decode": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _I, _I, _P, _P, _I, ctypes.c_float, _P,
+                          _P, _SZ, _P], _S),
     "tq_check_device_status": ([_P, ctypes.POINTER(ctypes.c_uint32)], _S),
     "tq_refine_counters": ([_P, ctypes.POINTER(ctypes.c_ulonglong), _I], _S),
     "tq_status_string": ([_S], ctypes.c_char_p),
@@ -187,6 +189,15 @@ def tq_decode_attention(ctx, q, dtype, batch, num_q_heads, num_kv_heads, seq_len
         ctx, _ptr(q), dtype, batch, num_q_heads, num_kv_heads, _ptr(seq_lens), max_seq_len, _ptr(block_table),
         max_pages_per_seq, num_pages, _ptr(k_cache), _ptr(v_cache), chunk_tokens, softmax_scale, _ptr(out),
         _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def tq_append_decode(ctx, k_new, v_new, q, dtype, batch, num_q_heads, num_kv_heads, seq_lens, max_seq_len,
+                     block_table, max_pages_per_seq, num_pages, k_cache, v_cache, chunk_tokens, softmax_scale, out,
+                     workspace, workspace_bytes, stream=None):
+    _check("tq_append_decode", _lib.tq_append_decode(
+        ctx, _ptr(k_new), _ptr(v_new), _ptr(q), dtype, batch, num_q_heads, num_kv_heads, _ptr(seq_lens), max_seq_len,
+        _ptr(block_table), max_pages_per_seq, num_pages, _ptr(k_cache), _ptr(v_cache), chunk_tokens, softmax_scale,
+        _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 TQ_STAGE_QPREP, TQ_STAGE_PARTIALS, TQ_STAGE_MERGE, TQ_STAGE_ALL = 1, 2, 4, 7

@@ -248,9 +248,19 @@ def quantize_exclusions(params, q, kind, eps=1e-6):
 # ---------------------------------------------------------------------------
 # Record format (this project's spec; the pages fix only "b-bit codes, signs,
 # norms, 16-token blocks"):
-#   codes: one little-endian bit stream per vector; channel j's code occupies
-#          bits [off_j, off_j + b_j) with off_j = sum of b over channels < j,
-#          least significant code bit first; byte k holds stream bits 8k..8k+7.
+#   codes: one bit stream per vector (byte k holds stream bits 8k..8k+7, least
+#          significant first).  Channels [0, split) form the first group
+#          (b_hi bits each), channels [split, d) the second (b_lo bits); each
+#          group holds its channels' *stored values* in order:
+#            b = 1, 2: value of group channel c at group bits [b*c, b*c + b).
+#            b = 3:    channels in octets of 8 (24 bits, octet o at group bit
+#                      24*o); octet channel i < 6 at octet bits 4i..4i+2,
+#                      channel 6 at octet bits 3, 11, 19 and channel 7 at
+#                      bits 7, 15, 23 (value bits 0, 1, 2 in that order).
+#            b = 4:    value of group channel c at group bits [4c, 4c + 4).
+#          The stored value is the code itself for b <= 3; for b = 4 it is
+#          sign-magnitude: code >= 8 -> code - 8, code < 8 -> 8 + (7 - code)
+#          (bit 3 set for the negative half, bits 0-2 the rank of |centroid|).
 #   signs: m bits, projection i at byte i//8, bit i%8 (so 32 per uint32 word).
 #   norms: IEEE half.
 # Block (one page, one KV head), structure of arrays over the 16 slots:
@@ -270,28 +280,62 @@ def cache_block_bytes(params, kind):
     return PAGE * (code_bytes(params, "v") + 2)
 
 
+def code_bit_positions(params, kind):
+    """pos[j][q]: stream bit of bit q of channel j's stored value (format above)."""
+    bits, split = (params.k_bits, params.k_split) if kind == "k" else (params.v_bits, params.v_split)
+    pos = []
+    for j in range(params.d):
+        if j < split:
+            base, c, b = 0, j, bits[0]
+        else:
+            base, c, b = split * bits[0], j - split, bits[1]
+        if b == 3:
+            ob, i = base + 24 * (c // 8), c % 8
+            if i < 6:
+                pos.append([ob + 4 * i + q for q in range(3)])
+            else:
+                pos.append([ob + 4 * (2 * q + (i - 6)) + 3 for q in range(3)])
+        else:
+            pos.append([base + b * c + q for q in range(b)])
+    return pos
+
+
+def stored_value(code, b):
+    """The b-bit value written for a code (identity except sign-magnitude at b = 4)."""
+    code = np.asarray(code)
+    if b != 4:
+        return code
+    return np.where(code >= 8, code - 8, 8 + (7 - code))
+
+
+def code_from_stored(value, b):
+    value = np.asarray(value)
+    if b != 4:
+        return value
+    return np.where(value & 8, 7 - (value & 7), 8 + value)
+
+
 def _pack_codes(params, codes, kind):
     cb = params.channel_bits(kind)
-    n = codes.shape[0]
-    total = int(cb.sum())
-    bits = np.zeros((n, total), dtype=np.uint8)
-    off = 0
+    pos = code_bit_positions(params, kind)
+    bits = np.zeros((codes.shape[0], int(cb.sum())), dtype=np.uint8)
     for j in range(params.d):
-        for q in range(int(cb[j])):
-            bits[:, off + q] = (codes[:, j] >> q) & 1
-        off += int(cb[j])
+        v = stored_value(codes[:, j], int(cb[j]))
+        for q, p in enumerate(pos[j]):
+            bits[:, p] = (v >> q) & 1
     return np.packbits(bits, axis=1, bitorder="little")
 
 
 def _unpack_codes(params, raw, kind):
     cb = params.channel_bits(kind)
+    pos = code_bit_positions(params, kind)
     bits = np.unpackbits(raw, axis=1, bitorder="little").astype(np.int64)
     codes = np.zeros((raw.shape[0], params.d), dtype=np.int64)
-    off = 0
     for j in range(params.d):
-        for q in range(int(cb[j])):
-            codes[:, j] |= bits[:, off + q] << q
-        off += int(cb[j])
+        v = np.zeros(raw.shape[0], dtype=np.int64)
+        for q, p in enumerate(pos[j]):
+            v |= bits[:, p] << q
+        codes[:, j] = code_from_stored(v, int(cb[j]))
     return codes
 
 

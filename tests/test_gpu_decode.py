@@ -153,3 +153,49 @@ def test_workspace_too_small_is_rejected():
             tq.tq_decode_attention(ctx, q, tq.TQ_BF16, 1, 4, 3, lens, 16, bt, 1, 1, kc, vc, 16, 0.1, out, ws, n)
     finally:
         tq.tq_destroy(ctx)
+
+
+def test_append_decode_equals_separate_calls():
+    import torch
+    from .gpu_common import gpu_quantize
+    w = BASE.scaled(k_bits=(4, 3), v_bits=(4, 3), dtype="bf16")
+    rng = np.random.default_rng(21)
+    B, H, Hq = 3, 2, 8
+    lens = np.array([40, 17, 5], np.int32)
+    pps = 4
+    num_pages = B * pps
+    bt = rng.permutation(num_pages).astype(np.int32).reshape(B, pps)
+    K = wl.bf16_round(rng.standard_normal((B, 40, H, 128)).astype(np.float32))
+    V = wl.bf16_round(rng.standard_normal((B, 40, H, 128)).astype(np.float32))
+    kn = wl.bf16_round(rng.standard_normal((B, 1, H, 128)).astype(np.float32))
+    vn = wl.bf16_round(rng.standard_normal((B, 1, H, 128)).astype(np.float32))
+    Q = wl.bf16_round(rng.standard_normal((B, Hq, 128)).astype(np.float32))
+    ctx = ctx_for(w)
+    try:
+        outs, caches = [], []
+        for fused in (True, False):
+            kc, vc = alloc_caches(ctx, H, num_pages)
+            for b in range(B):
+                gpu_quantize(ctx, K[b:b + 1, :lens[b]], V[b:b + 1, :lens[b]], "bf16", [0], bt[b:b + 1], num_pages,
+                             kc, vc)
+            max_len = int(lens.max()) + 1
+            n = tq.tq_workspace_size(ctx, B, Hq, max_len, 16)
+            ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+            out = torch.zeros(B, Hq, 128, dtype=torch.float32, device="cuda")
+            qd = to_dev(Q).to(torch.bfloat16)
+            if fused:
+                tq.tq_append_decode(ctx, to_dev(kn).to(torch.bfloat16), to_dev(vn).to(torch.bfloat16), qd, tq.TQ_BF16,
+                                    B, Hq, H, to_dev(lens), max_len, to_dev(bt), pps, num_pages, kc, vc, 16,
+                                    th.scale_for(), out, ws, n)
+            else:
+                gpu_quantize(ctx, kn, vn, "bf16", lens, bt, num_pages, kc, vc)
+                tq.tq_decode_attention(ctx, qd, tq.TQ_BF16, B, Hq, H, to_dev(lens + 1), max_len, to_dev(bt), pps,
+                                       num_pages, kc, vc, 16, th.scale_for(), out, ws, n)
+            torch.cuda.synchronize()
+            outs.append(out.cpu().numpy())
+            caches.append((kc.cpu().numpy(), vc.cpu().numpy()))
+        assert tq.tq_check_device_status(ctx) == 0
+    finally:
+        tq.tq_destroy(ctx)
+    assert np.array_equal(caches[0][0], caches[1][0]) and np.array_equal(caches[0][1], caches[1][1])
+    assert np.array_equal(outs[0], outs[1])

@@ -147,18 +147,61 @@ def test_two_stage_estimator_is_unbiased():
 
 # --- packing and the paged cache -------------------------------------------
 
-def test_pack_hand_example():
-    with open(os.path.join(GOLDEN, "pack_b3_codes_0to7.txt")) as f:
-        want = [int(t, 16) for ln in f if not ln.startswith("#") for t in ln.split()]
+def _golden_bytes(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [int(t, 16) for ln in f if not ln.startswith("#") for t in ln.split()]
+
+
+def test_pack_hand_example_3bit():
     p = oracle.make_params(d=D, k_bits=(3, 3), v_bits=(3, 3), seed=0)
     codes = np.zeros((1, D), dtype=np.int64)
     codes[0, :8] = np.arange(8)
     raw = tq._pack_codes(p, codes, "v")
-    assert raw[0, :3].tolist() == want and raw.shape == (1, 48)
+    assert raw[0, :3].tolist() == _golden_bytes("pack_b3_codes_0to7.txt") and raw.shape == (1, 48)
 
 
-@pytest.mark.parametrize("kb,vb", [((3, 3), (3, 3)), ((4, 3), (4, 3)), ((3, 2), (3, 2)), ((1, 1), (2, 4))])
-def test_pack_is_little_endian_integer(kb, vb):
+def test_pack_hand_example_4bit():
+    p = oracle.make_params(d=D, k_bits=(4, 4), v_bits=(4, 4), seed=0)
+    codes = np.full((1, D), 8, dtype=np.int64)
+    codes[0, :4] = [0, 7, 8, 15]
+    raw = tq._pack_codes(p, codes, "v")
+    assert raw[0, :2].tolist() == _golden_bytes("pack_b4_sign_magnitude.txt") and raw.shape == (1, 64)
+
+
+def _format_integer(codes, bits_per_channel):
+    """The code area as one integer, from the format's definition written group by group."""
+    acc, base = 0, 0
+    groups = []
+    j = 0
+    while j < len(codes):           # consecutive channels of equal width form a group
+        b = int(bits_per_channel[j])
+        k = j
+        while k < len(codes) and int(bits_per_channel[k]) == b:
+            k += 1
+        groups.append((b, [int(c) for c in codes[j:k]]))
+        j = k
+    for b, cs in groups:
+        if b == 3:
+            for o in range(0, len(cs), 8):
+                c = cs[o:o + 8]
+                octet = sum(c[i] << (4 * i) for i in range(6))
+                for q in range(3):
+                    octet |= ((c[6] >> q) & 1) << (8 * q + 3)
+                    octet |= ((c[7] >> q) & 1) << (8 * q + 7)
+                acc |= octet << (base + 3 * o)
+        elif b == 4:
+            for i, c in enumerate(cs):
+                acc |= ((c - 8) if c >= 8 else (15 - c)) << (base + 4 * i)
+        else:
+            for i, c in enumerate(cs):
+                acc |= c << (base + b * i)
+        base += b * len(cs)
+    return acc, base
+
+
+@pytest.mark.parametrize("kb,vb", [((3, 3), (3, 3)), ((4, 3), (4, 3)), ((3, 2), (3, 2)), ((1, 1), (2, 4)),
+                                   ((4, 4), (2, 2))])
+def test_pack_matches_format_definition(kb, vb):
     p = oracle.make_params(d=D, k_bits=kb, v_bits=vb, seed=0)
     rng = np.random.default_rng(1)
     for kind in ("k", "v"):
@@ -166,11 +209,8 @@ def test_pack_is_little_endian_integer(kb, vb):
         codes = np.stack([rng.integers(0, 1 << int(b), size=5) for b in cb], axis=1)
         raw = tq._pack_codes(p, codes, kind)
         for row in range(5):
-            acc, off = 0, 0
-            for j in range(D):
-                acc |= int(codes[row, j]) << off
-                off += int(cb[j])
-            assert bytes(raw[row]) == acc.to_bytes(off // 8, "little")
+            acc, nbits = _format_integer(codes[row], cb)
+            assert bytes(raw[row]) == acc.to_bytes(nbits // 8, "little")
         assert np.array_equal(tq._unpack_codes(p, raw, kind), codes)
 
 
