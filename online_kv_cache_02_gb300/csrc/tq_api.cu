@@ -37,6 +37,7 @@ void fill_group(GroupBook& g, int bits) {
     bool in_c = k < (1 << bits), in_t = k < g.nb;
     g.c64[k] = in_c ? c[k] : 0.0;
     g.c[k] = static_cast<float>(g.c64[k]);
+    g.c_lo[k] = static_cast<float>(g.c64[k] - static_cast<double>(g.c[k]));
     g.t64[k] = in_t ? t[k] : INFINITY;
     g.t[k] = in_t ? static_cast<float>(t[k]) : INFINITY;
   }
@@ -56,6 +57,50 @@ void fill_layout(KindLayout& L, int bits_hi, int bits_lo, int split, int d, int 
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Element offset (in halves) of (row n, channel k) of a K-major operand tile of
+// `rows` rows x 128 channels in the 128-byte-swizzled layout.
+size_t swz(int n, int k, int rows) {
+  const int kb = k >> 6, kk = k & 63;
+  const int chunk = (kk >> 3) ^ (n & 7);
+  return static_cast<size_t>(kb) * rows * 64 + static_cast<size_t>(n) * 64 + chunk * 8 + (kk & 7);
+}
+
+uint16_t to_f16(float x) {
+  // round to nearest even fp16 (host); values here are |x| < 2^15 and far from subnormal issues
+  uint32_t b;
+  std::memcpy(&b, &x, 4);
+  const uint32_t sign = (b >> 16) & 0x8000u;
+  const int exp = static_cast<int>((b >> 23) & 0xFF) - 127;
+  uint32_t man = b & 0x7FFFFFu;
+  if (exp < -24) return static_cast<uint16_t>(sign);
+  if (exp < -14) {                       // subnormal fp16
+    man |= 0x800000u;
+    const int shift = -exp - 14 + 13;
+    uint32_t h = man >> shift;
+    const uint32_t rem = man & ((1u << shift) - 1u), half = 1u << (shift - 1);
+    if (rem > half || (rem == half && (h & 1u))) ++h;
+    return static_cast<uint16_t>(sign | h);
+  }
+  uint32_t h = (static_cast<uint32_t>(exp + 15) << 10) | (man >> 13);
+  const uint32_t rem = man & 0x1FFFu;
+  if (rem > 0x1000u || (rem == 0x1000u && (h & 1u))) ++h;
+  return static_cast<uint16_t>(sign | h);
+}
+
+float from_f16(uint16_t h) {
+  const uint32_t sign = (h & 0x8000u) << 16;
+  const int exp = (h >> 10) & 0x1F;
+  const uint32_t man = h & 0x3FFu;
+  float v;
+  if (exp == 0) v = std::ldexp(static_cast<float>(man), -24);
+  else v = std::ldexp(static_cast<float>(man | 0x400u), exp - 25);
+  uint32_t b;
+  std::memcpy(&b, &v, 4);
+  b |= sign;
+  std::memcpy(&v, &b, 4);
+  return v;
+}
 
 // Split-K chunk length: the partials kernel keeps 3 CTAs resident per SM, so
 // pick the chunk count whose CTA total fills whole waves of 3 x SMs best
@@ -135,12 +180,50 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
   for (int i = 0; i < m; ++i)
     for (int j = 0; j < d; ++j) st_[static_cast<size_t>(j) * m + i] = static_cast<float>(s[i * d + j]);
 
+  // tensor-core operand tiles and double-float refinement tables
+  std::vector<uint16_t> pih(d * d), pil(d * d), sh(static_cast<size_t>(m) * d), sl(static_cast<size_t>(m) * d);
+  std::vector<float> pidf(static_cast<size_t>(d) * d * 2);
+  for (int i = 0; i < d; ++i)
+    for (int k = 0; k < d; ++k) {
+      const double v = pi[i * d + k] * kPiScale;   // scaled so the low part stays a normal fp16
+      const uint16_t hi = to_f16(static_cast<float>(v));
+      pih[swz(i, k, d)] = hi;
+      pil[swz(i, k, d)] = to_f16(static_cast<float>(v - static_cast<double>(from_f16(hi))));
+      const float phi = static_cast<float>(pi[i * d + k]);
+      pidf[(i * d + k) * 2] = phi;
+      pidf[(i * d + k) * 2 + 1] = static_cast<float>(pi[i * d + k] - static_cast<double>(phi));
+    }
+  for (int p = 0; p < m; ++p)
+    for (int j = 0; j < d; ++j) {
+      const uint16_t hi = to_f16(static_cast<float>(s[p * d + j]));
+      sh[swz(p, j, m)] = hi;
+      sl[swz(p, j, m)] = to_f16(static_cast<float>(s[p * d + j] - static_cast<double>(from_f16(hi))));
+    }
+  std::vector<float> adf(static_cast<size_t>(m) * d * 2), sdf(static_cast<size_t>(m) * d * 2);
+  for (int p = 0; p < m; ++p)
+    for (int k = 0; k < d; ++k) {
+      double acc = 0.0;
+      for (int i = 0; i < d; ++i) acc += s[p * d + i] * pi[i * d + k];   // (S Pi)[p][k]
+      const float hi = static_cast<float>(acc);
+      adf[(p * d + k) * 2] = hi;
+      adf[(p * d + k) * 2 + 1] = static_cast<float>(acc - static_cast<double>(hi));
+      const float shi = static_cast<float>(s[p * d + k]);
+      sdf[(p * d + k) * 2] = shi;
+      sdf[(p * d + k) * 2 + 1] = static_cast<float>(s[p * d + k] - static_cast<double>(shi));
+    }
   size_t o_pit = 0;
   size_t o_pi = align256(o_pit + sizeof(float) * d * d);
   size_t o_pi64 = align256(o_pi + sizeof(float) * d * d);
   size_t o_st = align256(o_pi64 + sizeof(double) * d * d);
   size_t o_s64 = align256(o_st + sizeof(float) * d * m);
-  size_t o_err = align256(o_s64 + sizeof(double) * d * m);
+  size_t o_pih = align256(o_s64 + sizeof(double) * d * m);
+  size_t o_pil = align256(o_pih + sizeof(uint16_t) * d * d);
+  size_t o_sh = align256(o_pil + sizeof(uint16_t) * d * d);
+  size_t o_sl = align256(o_sh + sizeof(uint16_t) * d * m);
+  size_t o_adf = align256(o_sl + sizeof(uint16_t) * d * m);
+  size_t o_sdf = align256(o_adf + sizeof(float) * d * m * 2);
+  size_t o_pidf = align256(o_sdf + sizeof(float) * d * m * 2);
+  size_t o_err = align256(o_pidf + sizeof(float) * d * d * 2);
   size_t o_cnt = align256(o_err + sizeof(uint32_t));
   size_t total = align256(o_cnt + 2 * sizeof(unsigned long long));
   void* blk = nullptr;
@@ -152,6 +235,13 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
   ctx->tab.pi64 = reinterpret_cast<double*>(b + o_pi64);
   ctx->tab.st = reinterpret_cast<float*>(b + o_st);
   ctx->tab.s64 = reinterpret_cast<double*>(b + o_s64);
+  ctx->tab.pih_sw = reinterpret_cast<unsigned short*>(b + o_pih);
+  ctx->tab.pil_sw = reinterpret_cast<unsigned short*>(b + o_pil);
+  ctx->tab.sh_sw = reinterpret_cast<unsigned short*>(b + o_sh);
+  ctx->tab.sl_sw = reinterpret_cast<unsigned short*>(b + o_sl);
+  ctx->tab.a_df = reinterpret_cast<float*>(b + o_adf);
+  ctx->tab.s_df = reinterpret_cast<float*>(b + o_sdf);
+  ctx->tab.pi_df = reinterpret_cast<float*>(b + o_pidf);
   ctx->tab.err = reinterpret_cast<uint32_t*>(b + o_err);
   ctx->tab.counters = reinterpret_cast<unsigned long long*>(b + o_cnt);
   bool ok = cudaMemcpy(ctx->tab.pit, pit.data(), sizeof(float) * d * d, cudaMemcpyHostToDevice) == cudaSuccess &&
@@ -159,6 +249,13 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
             cudaMemcpy(ctx->tab.pi64, pi.data(), sizeof(double) * d * d, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemcpy(ctx->tab.st, st_.data(), sizeof(float) * d * m, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemcpy(ctx->tab.s64, s.data(), sizeof(double) * d * m, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(ctx->tab.pih_sw, pih.data(), 2 * d * d, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(ctx->tab.pil_sw, pil.data(), 2 * d * d, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(ctx->tab.sh_sw, sh.data(), 2 * d * m, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(ctx->tab.sl_sw, sl.data(), 2 * d * m, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(ctx->tab.pi_df, pidf.data(), sizeof(float) * d * d * 2, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(ctx->tab.a_df, adf.data(), sizeof(float) * d * m * 2, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(ctx->tab.s_df, sdf.data(), sizeof(float) * d * m * 2, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemset(b + o_err, 0, total - o_err) == cudaSuccess;
   if (!ok) { cudaFree(blk); delete ctx; cudaGetLastError(); return TQ_ERR_CUDA; }
   *out = ctx;
@@ -196,12 +293,12 @@ extern "C" tq_status tq_quantize(const tq_ctx* ctx, const void* k, const void* v
   if (batch == 0 || n_new == 0) return TQ_OK;
   if (!start_pos || !block_table) return TQ_ERR_INVALID_ARG;
   if (static_cast<long long>(batch) * n_new * H > (1LL << 31) - 1) return TQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15) return TQ_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  QuantizeArgs args[2]{};
   for (int kind = 0; kind < 2; ++kind) {
-    const void* x = kind == 0 ? k : v;
-    if (!x) continue;
-    QuantizeArgs a{};
-    a.x = x;
+    QuantizeArgs& a = args[kind];
+    a.x = kind == 0 ? k : v;
     a.f32 = dtype == TQ_F32;
     a.batch = batch;
     a.n_new = n_new;
@@ -215,7 +312,12 @@ extern "C" tq_status tq_quantize(const tq_ctx* ctx, const void* k, const void* v
     a.page_bytes = static_cast<long long>(a.lay.block_bytes) * H;
     a.m = ctx->cfg.m;
     a.tab = ctx->tab;
-    if (launch_quantize(a, s) != cudaSuccess) return TQ_ERR_CUDA;
+  }
+  cudaError_t e = cudaSuccess;
+  if (launch_quantize_tc(args[0], args[1], s, &e)) return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  for (int kind = 0; kind < 2; ++kind) {
+    if (!args[kind].x) continue;
+    if (launch_quantize(args[kind], s) != cudaSuccess) return TQ_ERR_CUDA;
   }
   return TQ_OK;
 }

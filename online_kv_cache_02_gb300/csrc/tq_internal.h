@@ -15,6 +15,7 @@ constexpr int kD = 128;          // supported head dimension
 constexpr int kPage = 16;        // tokens per cache page
 constexpr int kMaxM = 128;       // QJL projections, multiple of 32
 constexpr int kMaxGroup = 8;     // query heads per KV head handled by the decode kernels
+constexpr float kPiScale = 16.0f;  // Pi is split into fp16 hi + lo after scaling by this power of two
 
 // Device error word bits.
 constexpr uint32_t kErrPage = 1u;      // page id outside [0, num_pages)
@@ -26,6 +27,7 @@ struct GroupBook {
   int bits;
   int nb;                // 2^bits - 1 boundaries
   float c[16];           // centroids, fp32
+  float c_lo[16];        // c64 - c (double-float low parts)
   float t[16];           // boundaries, fp32 (entries >= nb are +inf)
   double c64[16];
   double t64[16];
@@ -57,7 +59,17 @@ struct DeviceTables {
   float* st;             // S^T, fp32 [d][m]: st[j*m + i] = S[i][j]
   double* s64;           // S, fp64 row-major [m][d]
   uint32_t* err;         // device error word
-  unsigned long long* counters;  // [0] codes re-taken in fp64, [1] key vectors with signs re-taken
+  unsigned long long* counters;  // [0] codes re-taken in fp64, [1] sign bits re-taken
+  // tensor-core quantize operands: fp16 bit patterns in the 128-byte-swizzled
+  // K-major layout (rows of 64 channels per 128 B, chunk index XOR row % 8,
+  // two 64-channel halves one after the other)
+  unsigned short* pih_sw;   // Pi rounded to fp16, [128 rows][128]
+  unsigned short* pil_sw;   // fp16(Pi - pih)
+  unsigned short* sh_sw;    // S rounded to fp16, [m rows][128]
+  unsigned short* sl_sw;    // fp16(S - sh)
+  float* a_df;              // (S Pi) as double-float pairs [m][128][2]
+  float* s_df;              // S as double-float pairs [m][128][2]
+  float* pi_df;             // Pi as double-float pairs [128][128][2]
 };
 
 struct QuantizeArgs {
@@ -97,6 +109,9 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
+// Tensor-core quantize of K and V in one launch (bf16 inputs, supported
+// bit-width combinations); returns false when the configuration is not covered.
+bool launch_quantize_tc(const QuantizeArgs& k, const QuantizeArgs& v, cudaStream_t s, cudaError_t* err);
 cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s);
 bool launch_partials_mma(const DecodeArgs& a, cudaStream_t s, cudaError_t* err);
 
