@@ -10,23 +10,27 @@
 // and lane r of tensor memory; warp w serves lanes 32*(w%4).. (the only lanes
 // it may read) and channel quarter w/4, so each vector has four threads and a
 // quarter's codes fill whole 32-bit words of the record.
-//   1. x quarter -> partial sum of squares and max (reduced over the four
-//      threads in shared memory) -> fp32 norm, fp16 norm (exact: values near
-//      an fp16 rounding midpoint are recomputed in double-float), fp16 x scaled
-//      by a power of two (exact for bf16) in a 128-byte-swizzled K-major tile.
+//   1. x quarter -> partial sums of squares (double-float, exact products)
+//      and max, reduced over the four threads in shared memory -> fp32 norm,
+//      exactly rounded fp16 norm, fp16 x scaled by a power of two (exact for
+//      bf16) in a 128-byte-swizzled K-major tile.
 //   2. y = x Pi^T: tcgen05.mma kind::f16, M=128 N=128, accumulator in tensor
 //      memory; Pi is applied as fp16 hi + lo parts (about 22 bits).
 //   3. epilogue (tcgen05.ld, 32 columns): u = sqrt(d) y/||x||; the code comes
 //      from a 256-cell table over u in [-8, 8) (one 16-byte shared load: the
 //      boundary of the cell, the code below it and both centroids); a u within
-//      4e-6 of the boundary is flagged and re-decided after the unrolled pass
-//      from a double-float y and norm.  Keys: r' = y sqrt(d)/fp16(||x||) -
+//      4e-6 of the boundary is flagged.  Keys: r' = y sqrt(d)/fp16(||x||) -
 //      c[code] (the residual in unit-variance units) -> fp16 hi + lo tiles.
+//      Flagged codes go through a shared queue; one warp per entry re-decides
+//      it from a double-float y and norm and patches the stored word, the
+//      residual tiles and the residual norm (rare: about 1e-5 of the codes).
 //   4. keys: z = r' S^T as hi*hi + lo*hi + hi*lo fp16 MMAs (about 1e-7 of ||r'||
-//      accurate); a |z_p| below 2e-5 ||r'|| is re-decided exactly as
-//      (S Pi)_p x - fp16(||x||)/sqrt(d) * S_p c[code] in double-float.
+//      accurate); a |z_p| below 2e-5 ||r'|| is re-decided the same way, one
+//      warp per entry: (S Pi)_p x - fp16(||x||)/sqrt(d) * S_p c[code] in
+//      double-float.
 //   5. the record (codes, signs, fp16 norms) is stored at its page slot.
-// Supported here: bf16 inputs, d = 128, split 64, m multiple of 32 (<= 128),
+// Supported here: bf16 or fp32 inputs (fp32 x is split into fp16 hi + lo and
+// takes a third MMA set), d = 128, split 64, m multiple of 32 (<= 128), the
 // bit-width combinations instantiated below; the rest runs tq_quantize.cu.
 
 #include "tq_internal.h"
@@ -238,12 +242,12 @@ __device__ __forceinline__ void clear_code_q(uint32_t (&w)[4], int c) {
   }
 }
 
-// Code of channel j of a stored record (rare paths; any bit width).
+// Code of channel j of a stored record (rare paths; any bit width).  Reads go
+// to L2: the words may have been patched by atomics of other warps.
 __device__ int record_code(const uint32_t* cw, int bh, int bl, int j) {
   const int grp = j < 64 ? 0 : 1, b = grp ? bl : bh, c = grp ? j - 64 : j, base = grp ? 64 * bh : 0;
   auto bitsat = [&](int off, int n) {
-    const unsigned long long pair = (static_cast<unsigned long long>(cw[(off >> 5) + 1]) << 32) | cw[off >> 5];
-    return static_cast<int>((pair >> (off & 31)) & ((1u << n) - 1u));
+    return static_cast<int>((__ldcg(cw + (off >> 5)) >> (off & 31)) & ((1u << n) - 1u));
   };
   if (b == 3) {
     const int ob = base + 24 * (c >> 3), i = c & 7;
@@ -256,35 +260,130 @@ __device__ int record_code(const uint32_t* cw, int bh, int bl, int j) {
   return v;
 }
 
-// Exact code of channel i: y_i = (Pi_i hi + lo) . x and ||x|| in double-float,
-// u = sqrt(d) y_i / ||x|| compared with the fp64 boundaries.
-__device__ __noinline__ int refine_code(const __nv_bfloat16* x, const float* prow, const double* t64, int nb) {
-  DF yd{0.f, 0.f}, n2{0.f, 0.f};
-  for (int k = 0; k < kD; ++k) {
-    const float xv = __bfloat162float(x[k]);
-    yd = df_fma_acc(yd, prow[2 * k], prow[2 * k + 1], xv);
-    n2 = df_add(n2, DF{xv * xv, 0.f});        // squares of bf16 values are exact in fp32
+// Replace the code of channel j (old -> nu) in a stored record; fields never
+// straddle a word, and XOR patches from several warps commute.
+__device__ void patch_code(uint32_t* cw, int bh, int bl, int j, int old, int nu) {
+  const int grp = j < 64 ? 0 : 1, b = grp ? bl : bh, c = grp ? j - 64 : j, base = grp ? 64 * bh : 0;
+  if (b == 3) {
+    const int ob = base + 24 * (c >> 3), i = c & 7;
+    const uint32_t dx = static_cast<uint32_t>(old ^ nu);
+    if (i < 6) {
+      const int pos = ob + 4 * i;
+      atomicXor(cw + (pos >> 5), dx << (pos & 31));
+    } else {
+      for (int k = 0; k < 3; ++k) {
+        const int pos = ob + 3 + 4 * (i - 6) + 8 * k;
+        if ((dx >> k) & 1u) atomicXor(cw + (pos >> 5), 1u << (pos & 31));
+      }
+    }
+    return;
   }
+  auto sv = [&](int code) { return b == 4 ? (code >= 8 ? code - 8 : 15 - code) : code; };
+  const int pos = base + b * c;
+  atomicXor(cw + (pos >> 5), static_cast<uint32_t>(sv(old) ^ sv(nu)) << (pos & 31));
+}
+
+// Sum of a double-float over the warp (every lane gets a sum; lane 0's is used).
+__device__ __forceinline__ DF warp_df_sum(DF v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    v = df_add(v, DF{__shfl_xor_sync(0xffffffffu, v.h, off), __shfl_xor_sync(0xffffffffu, v.l, off)});
+  return v;
+}
+
+// The four channels 4*lane.. of a row (bf16 or fp32 input).
+__device__ __forceinline__ void lane_x4(const void* xrow, bool f32, int lane, float (&xv)[4]) {
+  if (f32) {
+    const float4 r = reinterpret_cast<const float4*>(xrow)[lane];
+    xv[0] = r.x, xv[1] = r.y, xv[2] = r.z, xv[3] = r.w;
+    return;
+  }
+  const uint2 r = reinterpret_cast<const uint2*>(xrow)[lane];
+  xv[0] = __uint_as_float(r.x << 16);
+  xv[1] = __uint_as_float(r.x & 0xFFFF0000u);
+  xv[2] = __uint_as_float(r.y << 16);
+  xv[3] = __uint_as_float(r.y & 0xFFFF0000u);
+}
+// x^2 as a double-float (exact).
+__device__ __forceinline__ DF df_sq(float x) {
+  const float p = x * x;
+  return {p, fmaf(x, x, -p)};
+}
+
+// Exact code of channel ch (warp-cooperative): y = (Pi_ch hi + lo) . x and
+// ||x||^2 in double-float, u = sqrt(d) y/||x|| compared with the fp64
+// boundaries.  Lane 0 patches the stored code when it differs and, for keys,
+// the residual tiles and the residual norm partial.
+__device__ __noinline__ void refine_code_item(const void* xrow, bool f32, const float* pidf_row, uint32_t* cw, int bh,
+                                              int bl, int ch, const double* t64, int nb, const float* cent, bool key,
+                                              float n16f, unsigned char* smem, float* rho2_slot, int row, int lane,
+                                              unsigned long long* counter) {
+  float xv[4];
+  lane_x4(xrow, f32, lane, xv);
+  const float4* pr = reinterpret_cast<const float4*>(pidf_row) + 2 * lane;
+  const float4 p0 = pr[0], p1 = pr[1];
+  DF yd{0.f, 0.f}, n2{0.f, 0.f};
+  yd = df_fma_acc(yd, p0.x, p0.y, xv[0]);
+  yd = df_fma_acc(yd, p0.z, p0.w, xv[1]);
+  yd = df_fma_acc(yd, p1.x, p1.y, xv[2]);
+  yd = df_fma_acc(yd, p1.z, p1.w, xv[3]);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) n2 = df_add(n2, df_sq(xv[k]));
+  yd = warp_df_sum(yd);
+  n2 = warp_df_sum(n2);
+  if (lane != 0) return;
   const double n64 = sqrt(df_to_d(n2));
   const double u64 = n64 > 0.0 ? kSqrtD64 * df_to_d(yd) / n64 : 0.0;
   int code = 0;
   for (int k = 0; k < nb; ++k) code += u64 >= t64[k];
-  return code;
+  atomicAdd(counter, 1ULL);
+  const int old = record_code(cw, bh, bl, ch);
+  if (code == old) return;
+  patch_code(cw, bh, bl, ch, old, code);
+  if (key && n16f > 0.0f) {          // with a zero fp16 norm the residual does not use the code
+    const float r = (yd.h + yd.l) * (kSqrtD / n16f) - cent[code];
+    const uint32_t off = swz_chunk(row, ch >> 3, kRows) + (ch & 7) * 2;
+    __half* ph = reinterpret_cast<__half*>(smem + kOffRH + off);
+    __half* pl = reinterpret_cast<__half*>(smem + kOffX + off);
+    const float rold = __half2float(*ph) + __half2float(*pl);
+    const __half hh = __float2half_rn(r);
+    *ph = hh;
+    *pl = __float2half_rn(r - __half2float(hh));
+    atomicAdd(rho2_slot, r * r - rold * rold);
+  }
 }
 
-// Exact sign bit of projection p: (S Pi)_p x - fp16(||x||)/sqrt(d) * S_p c[code],
-// with the centroid of every channel given as double-float pairs in cdf.
-__device__ __noinline__ uint32_t refine_sign(const __nv_bfloat16* x, const float* arow, const float* srow,
-                                             const float* cdf, float n16f) {
+// Exact sign bit of projection p (warp-cooperative):
+// (S Pi)_p x - fp16(||x||)/sqrt(d) * S_p c[code] in double-float, with the
+// codes read back from the stored record.  Lane 0 patches the stored bit.
+__device__ __noinline__ void refine_sign_item(const void* xrow, bool f32, const float* arow, const float* srow,
+                                              const uint32_t* cw, int bh, int bl, const float* ch, const float* cl,
+                                              float n16f, uint32_t* sw, int bit, int lane,
+                                              unsigned long long* counter) {
+  float xv[4];
+  lane_x4(xrow, f32, lane, xv);
+  const float4* ar = reinterpret_cast<const float4*>(arow) + 2 * lane;
+  const float4* sr = reinterpret_cast<const float4*>(srow) + 2 * lane;
+  const float4 a0 = ar[0], a1 = ar[1], s0 = sr[0], s1 = sr[1];
+  const float ah[4] = {a0.x, a0.z, a1.x, a1.z}, al[4] = {a0.y, a0.w, a1.y, a1.w};
+  const float sh[4] = {s0.x, s0.z, s1.x, s1.z}, sl[4] = {s0.y, s0.w, s1.y, s1.w};
   DF d1{0.f, 0.f}, d2{0.f, 0.f};
-  for (int j = 0; j < kD; ++j) {
-    d1 = df_fma_acc(d1, arow[2 * j], arow[2 * j + 1], __bfloat162float(x[j]));
-    d2 = df_add(d2, df_mul(DF{srow[2 * j], srow[2 * j + 1]}, DF{cdf[2 * j], cdf[2 * j + 1]}));
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int j = 4 * lane + k;
+    const int cj = record_code(cw, bh, bl, j) + (j < 64 ? 0 : 16);
+    d1 = df_fma_acc(d1, ah[k], al[k], xv[k]);
+    d2 = df_add(d2, df_mul(DF{sh[k], sl[k]}, DF{ch[cj], cl[cj]}));
   }
+  d1 = warp_df_sum(d1);
+  d2 = warp_df_sum(d2);
+  if (lane != 0) return;
   const DF f = df_mul(DF{n16f, 0.f}, DF{kInvSqrtDHi, kInvSqrtDLo});
   const DF fz = df_mul(f, d2);
   const DF z = df_add(d1, DF{-fz.h, -fz.l});
-  return (z.h > 0.0f || (z.h == 0.0f && z.l >= 0.0f)) ? 1u : 0u;
+  const uint32_t nb = (z.h > 0.0f || (z.h == 0.0f && z.l >= 0.0f)) ? 1u : 0u;
+  atomicAdd(counter, 1ULL);
+  if (((__ldcg(sw) >> bit) & 1u) != nb) atomicXor(sw, 1u << bit);
 }
 
 // Code-assignment cells: per channel group 256 cells of width 1/16 over
@@ -327,12 +426,11 @@ __device__ void build_cells(Cell* cells, const GroupBook& gb, int idx) {
 // shared memory beyond the tiles
 constexpr int kOffCells = 196608;                 // 4 groups x 256 cells x 16 B
 constexpr int kOffMisc4 = kOffCells + 4 * kCells * 16;
-constexpr int kSmemBytes4 = kOffMisc4 + 8192 + 1024;
 
 // Epilogue of one quarter (32 channels of group width B) of one row.
 template <int B, bool KEY>
 __device__ __forceinline__ void quarter_epilogue(const float (&v)[32], const Cell* cells, float ku, float kr,
-                                                 uint32_t (&words)[4], uint32_t& near, float& rho2,
+                                                 float sub, uint32_t (&words)[4], uint32_t& near, float& rho2,
                                                  uint32_t (&rh)[16], uint32_t (&rl)[16]) {
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
@@ -344,7 +442,7 @@ __device__ __forceinline__ void quarter_epilogue(const float (&v)[32], const Cel
     near |= (fabsf(u - cell.x) < kCodeGuard ? 1u : 0u) << c;
     put_code_q<B>(words, c, static_cast<uint32_t>(code));
     if (KEY) {
-      const float r = fmaf(v[c], kr, -(ge ? cell.w : cell.z));
+      const float r = fmaf(v[c], kr, -sub * (ge ? cell.w : cell.z));
       rho2 = fmaf(r, r, rho2);
       const __half hh = __float2half_rn(r);
       const __half hl = __float2half_rn(r - __half2float(hh));
@@ -359,36 +457,26 @@ __device__ __forceinline__ void quarter_epilogue(const float (&v)[32], const Cel
   }
 }
 
-// Re-decide flagged codes of a quarter exactly and patch words / residual.
-template <int B, bool KEY>
-__device__ __noinline__ void quarter_refine(const float (&v)[32], uint32_t near, const __nv_bfloat16* xrow,
-                                            const float* pi_df, int ch0, const double* t64, int nb, const float* cent,
-                                            float kr, uint32_t (&words)[4], float& rho2, uint32_t (&rh)[16],
-                                            uint32_t (&rl)[16], unsigned long long* counter) {
-  while (near) {
-    const int c = __ffs(near) - 1;
-    near &= near - 1;
-    const int code = refine_code(xrow, pi_df + (ch0 + c) * kD * 2, t64, nb);
-    atomicAdd(counter, 1ULL);
-#pragma unroll
-    for (int c2 = 0; c2 < 32; ++c2) {
-      if (c2 != c) continue;
-      clear_code_q<B>(words, c2);
-      put_code_q<B>(words, c2, static_cast<uint32_t>(code));
-      if (KEY) {
-        const uint32_t sh = (c2 & 1) ? 16u : 0u;
-        const float rold = __half2float(__ushort_as_half(static_cast<unsigned short>(rh[c2 >> 1] >> sh))) +
-                           __half2float(__ushort_as_half(static_cast<unsigned short>(rl[c2 >> 1] >> sh)));
-        const float r = fmaf(v[c2], kr, -cent[code]);
-        rho2 += r * r - rold * rold;
-        const __half hh = __float2half_rn(r);
-        const __half hl = __float2half_rn(r - __half2float(hh));
-        rh[c2 >> 1] = (rh[c2 >> 1] & ~(0xFFFFu << sh)) | (static_cast<uint32_t>(__half_as_ushort(hh)) << sh);
-        rl[c2 >> 1] = (rl[c2 >> 1] & ~(0xFFFFu << sh)) | (static_cast<uint32_t>(__half_as_ushort(hl)) << sh);
-      }
-    }
+// Value k (0..31) of a thread's quarter row held as raw 16-byte chunks.
+__device__ __forceinline__ float quarter_value(const uint4 (&raw)[8], int k, bool f32) {
+  if (f32) {
+    const uint4 c = raw[k >> 2];
+    const uint32_t w = (k & 3) == 0 ? c.x : (k & 3) == 1 ? c.y : (k & 3) == 2 ? c.z : c.w;
+    return __uint_as_float(w);
   }
+  const uint4 c = raw[k >> 3];
+  const int j = (k >> 1) & 3;
+  const uint32_t w = j == 0 ? c.x : j == 1 ? c.y : j == 2 ? c.z : c.w;
+  return __uint_as_float((k & 1) ? (w & 0xFFFF0000u) : (w << 16));
 }
+
+// Misc shared area (after the cells).
+constexpr int kQueueCap = 128;
+constexpr int kMiscQn = 20, kMiscT64 = 64, kMiscCent = 576, kMiscCentLo = 832, kMiscRedSH = 1152,
+              kMiscRedSL = 3200, kMiscRedM = 5248, kMiscRedR = 7296, kMiscN16 = 9344, kMiscCodePtr = 9856,
+              kMiscSignPtr = 10880, kMiscQueue = 11904, kMiscBytes = 12544;
+constexpr int kSmemBytes4 = kOffMisc4 + kMiscBytes + 1024;   // + alignment slack
+static_assert(kSmemBytes4 <= 232448, "shared memory per block");
 
 // ---------------------------------------------------------------------------
 // the kernel: 16 warps; warp w reads tensor-memory lanes 32*(w%4).. (rows) and
@@ -401,16 +489,24 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   Cell* cells = reinterpret_cast<Cell*>(smem + kOffCells);
-  unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem + kOffMisc4);   // [0] tables, [1] mma
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc4 + 16);
-  double* t64s = reinterpret_cast<double*>(smem + kOffMisc4 + 64);                      // [4][16]
-  float* cents = reinterpret_cast<float*>(smem + kOffMisc4 + 64 + 512);                 // [4][16]
-  float* red_s = reinterpret_cast<float*>(smem + kOffMisc4 + 1024);                     // [4][128]
-  float* red_m = red_s + 512;
-  float* red_r = red_m + 512;
+  unsigned char* misc = smem + kOffMisc4;
+  unsigned long long* bars = reinterpret_cast<unsigned long long*>(misc);   // [0] tables, [1] mma
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 16);
+  int* qn = reinterpret_cast<int*>(misc + kMiscQn);
+  double* t64s = reinterpret_cast<double*>(misc + kMiscT64);                  // [4][16]
+  float* cents = reinterpret_cast<float*>(misc + kMiscCent);                  // [4][16]
+  float* centl = reinterpret_cast<float*>(misc + kMiscCentLo);                // [4][16]
+  float* red_sh = reinterpret_cast<float*>(misc + kMiscRedSH);                // [4][128] each
+  float* red_sl = reinterpret_cast<float*>(misc + kMiscRedSL);
+  float* red_m = reinterpret_cast<float*>(misc + kMiscRedM);
+  float* red_r = reinterpret_cast<float*>(misc + kMiscRedR);
+  float* rown16 = reinterpret_cast<float*>(misc + kMiscN16);                  // [128]
+  uint32_t** codeptr = reinterpret_cast<uint32_t**>(misc + kMiscCodePtr);     // [128], null: no record
+  uint32_t** signptr = reinterpret_cast<uint32_t**>(misc + kMiscSignPtr);     // [128]
+  uint32_t* queue = reinterpret_cast<uint32_t*>(misc + kMiscQueue);           // [kQueueCap]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int sp = warp & 3, q = warp >> 2;
-  const int row = 32 * sp + lane;
+  const int q = warp >> 2;
+  const int row = 32 * (warp & 3) + lane;
   const int m = ka.m;
   const bool have_k = nk_tiles > 0;
 
@@ -423,8 +519,10 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
     const int grp = tid >> 4, k = tid & 15;
     const GroupBook& gb = (grp < 2 ? ka.lay : va.lay).g[grp & 1];
     t64s[tid] = gb.t64[k];
-    cents[grp * 16 + k] = gb.c[k];
+    cents[tid] = gb.c[k];
+    centl[tid] = gb.c_lo[k];
   }
+  if (tid == 0) *qn = 0;
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   if (tid == 0) {
     mbar_init(smem_u32(&bars[0]), 1);
@@ -443,82 +541,111 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  bool failed = !mbar_wait(smem_u32(&bars[0]), 0);
+  // a wait that gives up sets the flag in every thread (uniform exit)
+  bool failed = __syncthreads_or(!mbar_wait(smem_u32(&bars[0]), 0)) != 0;
   uint32_t phase = 0;
-  const uint32_t trow = tmem + ((32u * sp) << 16);
+  const uint32_t trow = tmem + ((32u * (warp & 3)) << 16);
 
   const int ntiles = nk_tiles + nv_tiles;
   for (int tile = blockIdx.x; tile < ntiles && !failed; tile += gridDim.x) {
     const bool key = tile < nk_tiles;
     const QuantizeArgs& a = key ? ka : va;
     const long long nvec = static_cast<long long>(a.batch) * a.n_new * a.H;
-    const long long gv = static_cast<long long>(key ? tile : tile - nk_tiles) * kRows + row;
-    const bool valid = gv < nvec;
-    const __nv_bfloat16* xrow = static_cast<const __nv_bfloat16*>(a.x) + gv * kD;
+    const long long gv0 = static_cast<long long>(key ? tile : tile - nk_tiles) * kRows;
+    const bool valid = gv0 + row < nvec;
+    const bool f32 = a.f32 != 0;
+    const bool sk = key && a.lay.qjl;              // keys with residual signs
+    const size_t esz = f32 ? 4 : 2;
+    const unsigned char* xbase = static_cast<const unsigned char*>(a.x) + static_cast<size_t>(gv0) * kD * esz;
+    auto xrow_of = [&](int r) { return static_cast<const void*>(xbase + static_cast<size_t>(r) * kD * esz); };
 
     // ---- 1. x quarter -> row statistics -> scaled fp16 tile ---------------
-    uint4 raw[4];
+    // raw holds the quarter's 32 values: 4 x (8 bf16) or 8 x (4 fp32)
+    uint4 raw[8];
     {
-      const uint4* src = reinterpret_cast<const uint4*>(xrow + 32 * q);
+      const uint4* src = reinterpret_cast<const uint4*>(xbase + static_cast<size_t>(row) * kD * esz + 32 * q * esz);
+      const int nchunk = f32 ? 8 : 4;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) raw[c] = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-      float ss = 0.f, mx = 0.f;
+      for (int c = 0; c < 8; ++c) raw[c] = (valid && c < nchunk) ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+      float sh = 0.f, sl = 0.f, mx = 0.f;      // double-float sum of the squares
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t wv[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float lo = __uint_as_float(wv[k] << 16), hi = __uint_as_float(wv[k] & 0xFFFF0000u);
-          ss = fmaf(lo, lo, fmaf(hi, hi, ss));
-          mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
-        }
+      for (int k = 0; k < 32; ++k) {
+        const float xv = quarter_value(raw, k, f32);
+        const DF p = df_sq(xv);
+        const float t = sh + p.h, bb = t - sh;
+        sl += ((sh - (t - bb)) + (p.h - bb)) + p.l;
+        sh = t;
+        mx = fmaxf(mx, fabsf(xv));
       }
-      red_s[q * 128 + row] = ss;
+      red_sh[q * 128 + row] = sh;
+      red_sl[q * 128 + row] = sl;
       red_m[q * 128 + row] = mx;
     }
+    // record location (one thread per row)
+    unsigned char* rec = nullptr;
+    int slot = 0;
+    if (q == 0) {
+      if (valid) {
+        const long long gv = gv0 + row;
+        const int h = static_cast<int>(gv % a.H);
+        const long long bt = gv / a.H;
+        const int t = static_cast<int>(bt % a.n_new);
+        const int b = static_cast<int>(bt / a.n_new);
+        const int pos = a.start_pos[b] + t;
+        const int blk = pos >> 4;
+        if (pos < 0 || blk >= a.maxp) {
+          atomicOr(a.tab.err, kErrBlock);
+        } else {
+          const int page = a.block_table[static_cast<long long>(b) * a.maxp + blk];
+          if (page < 0 || page >= a.num_pages) {
+            atomicOr(a.tab.err, kErrPage);
+          } else {
+            rec = a.cache + static_cast<long long>(page) * a.page_bytes + static_cast<long long>(h) * a.lay.block_bytes;
+            slot = pos & 15;
+          }
+        }
+      }
+      codeptr[row] = rec ? reinterpret_cast<uint32_t*>(rec + slot * a.lay.code_bytes) : nullptr;
+      signptr[row] = rec ? reinterpret_cast<uint32_t*>(rec + a.lay.off_signs + slot * (m / 8)) : nullptr;
+    }
     __syncthreads();
-    float nf, xs_scale = 1.0f, n16f;
-    unsigned short n16;
+    float nf = 0.0f, xs_scale = 1.0f, n16f;
     {
-      const float ss = (red_s[row] + red_s[128 + row]) + (red_s[256 + row] + red_s[384 + row]);
+      const DF n2 = df_add(df_add(DF{red_sh[row], red_sl[row]}, DF{red_sh[128 + row], red_sl[128 + row]}),
+                           df_add(DF{red_sh[256 + row], red_sl[256 + row]}, DF{red_sh[384 + row], red_sl[384 + row]}));
       const float mx = fmaxf(fmaxf(red_m[row], red_m[128 + row]), fmaxf(red_m[256 + row], red_m[384 + row]));
-      nf = sqrtf(ss);
-      if (mx > 0.0f) {
+      __half h = __ushort_as_half(static_cast<unsigned short>(0));
+      if (n2.h > 0.0f) {
+        const float r = sqrtf(n2.h);
+        const float rl = (fmaf(-r, r, n2.h) + n2.l) / (2.0f * r);
+        nf = r + rl;
+        h = df_to_half(nf, rl - (nf - r));
         int e;
         frexpf(mx, &e);
         xs_scale = ldexpf(1.0f, 14 - e);
       }
-      __half h = __float2half_rn(nf);
-      const float hb = __half2float(h);
-      const unsigned short hbits = __half_as_ushort(h);
-      const float up = __half2float(__ushort_as_half(static_cast<unsigned short>(hbits + 1)));
-      const float dn = hbits ? __half2float(__ushort_as_half(static_cast<unsigned short>(hbits - 1))) : 0.0f;
-      const float tol = 4e-6f * nf;
-      if (valid && nf > 0.0f && (fabsf(nf - 0.5f * (hb + up)) < tol || fabsf(nf - 0.5f * (hb + dn)) < tol)) {
-        DF acc{0.f, 0.f};
-        for (int k = 0; k < kD; ++k) {
-          const float xv = __bfloat162float(xrow[k]);
-          acc = df_add(acc, DF{xv * xv, 0.f});
-        }
-        const float r = sqrtf(acc.h);
-        const float res = fmaf(-r, r, acc.h) + acc.l;
-        const float rl2 = res / (2.0f * r);
-        h = df_to_half(r + rl2, rl2 - ((r + rl2) - r));
-      }
-      n16 = __half_as_ushort(h);
       n16f = __half2float(h);
+      if (q == 0) {
+        rown16[row] = n16f;
+        if (rec) reinterpret_cast<unsigned short*>(rec + a.lay.off_norm)[slot] = __half_as_ushort(h);
+      }
+      // fp16 x * 2^k (exact for bf16); fp32 input also gets the remainder as a
+      // second fp16 tile (in the residual tile, free until the epilogue)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const uint32_t wv[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
-        uint32_t hv[4];
+        uint32_t hv[4], lv[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const __half2 p = __floats2half2_rn(__uint_as_float(wv[k] << 16) * xs_scale,
-                                              __uint_as_float(wv[k] & 0xFFFF0000u) * xs_scale);
-          hv[k] = *reinterpret_cast<const uint32_t*>(&p);
+          const float x0 = quarter_value(raw, 8 * c + 2 * k, f32) * xs_scale;
+          const float x1 = quarter_value(raw, 8 * c + 2 * k + 1, f32) * xs_scale;
+          const __half2 ph = __floats2half2_rn(x0, x1);
+          const __half2 pl = __floats2half2_rn(x0 - __low2float(ph), x1 - __high2float(ph));
+          hv[k] = *reinterpret_cast<const uint32_t*>(&ph);
+          lv[k] = *reinterpret_cast<const uint32_t*>(&pl);
         }
-        *reinterpret_cast<uint4*>(smem + kOffX + swz_chunk(row, 4 * q + c, kRows)) =
-            make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        const uint32_t off = swz_chunk(row, 4 * q + c, kRows);
+        *reinterpret_cast<uint4*>(smem + kOffX + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        if (f32) *reinterpret_cast<uint4*>(smem + kOffRH + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
       }
     }
     fence_proxy_async();
@@ -534,9 +661,14 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
 #pragma unroll
       for (int s = 0; s < 8; ++s)
         umma_f16(tmem, kdesc(sbase + kOffX, kRows, s), kdesc(sbase + kOffPIL, kRows, s), idesc_f16(128), 1u);
+      if (f32) {
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          umma_f16(tmem, kdesc(sbase + kOffRH, kRows, s), kdesc(sbase + kOffPIH, kRows, s), idesc_f16(128), 1u);
+      }
       umma_commit(smem_u32(&bars[1]));
     }
-    if (!mbar_wait(smem_u32(&bars[1]), phase)) {
+    if (__syncthreads_or(!mbar_wait(smem_u32(&bars[1]), phase))) {
       failed = true;
       if (tid == 0) atomicOr(a.tab.err, kErrTimeout);
     }
@@ -546,39 +678,34 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
     // ---- 3. codes and residual of this quarter -------------------------------
     const int grp = q < 2 ? 0 : 1;
     const int gslot = (key ? 0 : 2) + grp;
-    const float inv = 1.0f / (xs_scale * kPiScale);
-    const float ku = nf > 0.0f ? inv * (kSqrtD / nf) : 0.0f;
-    const float kr = n16f > 0.0f ? inv * (kSqrtD / n16f) : 0.0f;
-    uint32_t words[4] = {0u, 0u, 0u, 0u};
-    uint32_t rh[16], rl[16];
+    const int bh = key ? KBH : VBH, bl = key ? KBL : VBL;
+    uint32_t* const cp = codeptr[row];
     uint32_t near = 0;
-    float rho2 = 0.0f;
     {
+      const float inv = 1.0f / (xs_scale * kPiScale);
+      const float ku = nf > 0.0f ? inv * (kSqrtD / nf) : 0.0f;
+      // a zero fp16 norm leaves the residual equal to y (any positive scale
+      // gives the same signs), so it is formed without the centroids
+      const float kr = n16f > 0.0f ? inv * (kSqrtD / n16f) : ku;
+      const float sub = n16f > 0.0f ? 1.0f : 0.0f;
+      uint32_t words[4] = {0u, 0u, 0u, 0u};
+      uint32_t rh[16], rl[16];
+      float rho2 = 0.0f;
       float v[32];
       tmem_ld32(trow + 32 * q, v);
       const Cell* cg = cells + gslot * kCells;
-      const int bits = key ? (grp ? KBL : KBH) : (grp ? VBL : VBH);
-      const float* cent = cents + gslot * 16;
-      const double* t64 = t64s + gslot * 16;
-      const int nb = (1 << bits) - 1;
-      if (!valid) near = 0;
-#define TQ_QUARTER(B, K)                                                                                       \
-  do {                                                                                                         \
-    quarter_epilogue<B, K>(v, cg, ku, kr, words, near, rho2, rh, rl);                                          \
-    if (!valid) near = 0;                                                                                      \
-    if (near)                                                                                                  \
-      quarter_refine<B, K>(v, near, xrow, a.tab.pi_df, 32 * q, t64, nb, cent, kr, words, rho2, rh, rl,         \
-                           &a.tab.counters[0]);                                                                \
-  } while (0)
-      if (key) {
-        if (grp == 0) TQ_QUARTER(KBH, true);
-        else TQ_QUARTER(KBL, true);
+      if (sk) {
+        if (grp == 0) quarter_epilogue<KBH, true>(v, cg, ku, kr, sub, words, near, rho2, rh, rl);
+        else quarter_epilogue<KBL, true>(v, cg, ku, kr, sub, words, near, rho2, rh, rl);
+      } else if (key) {
+        if (grp == 0) quarter_epilogue<KBH, false>(v, cg, ku, kr, sub, words, near, rho2, rh, rl);
+        else quarter_epilogue<KBL, false>(v, cg, ku, kr, sub, words, near, rho2, rh, rl);
       } else {
-        if (grp == 0) TQ_QUARTER(VBH, false);
-        else TQ_QUARTER(VBL, false);
+        if (grp == 0) quarter_epilogue<VBH, false>(v, cg, ku, kr, sub, words, near, rho2, rh, rl);
+        else quarter_epilogue<VBL, false>(v, cg, ku, kr, sub, words, near, rho2, rh, rl);
       }
-#undef TQ_QUARTER
-      if (key) {
+      if (!valid || nf == 0.0f || !cp) near = 0;
+      if (sk) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const uint32_t off = swz_chunk(row, 4 * q + c, kRows);
@@ -587,43 +714,47 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
         }
         red_r[q * 128 + row] = rho2;
       }
-    }
-
-    // record location
-    unsigned char* rec = nullptr;
-    int slot = 0;
-    if (valid) {
-      const int h = static_cast<int>(gv % a.H);
-      const long long bt = gv / a.H;
-      const int t = static_cast<int>(bt % a.n_new);
-      const int b = static_cast<int>(bt / a.n_new);
-      const int pos = a.start_pos[b] + t;
-      const int blk = pos >> 4;
-      if (pos < 0 || blk >= a.maxp) {
-        if (q == 0) atomicOr(a.tab.err, kErrBlock);
-      } else {
-        const int page = a.block_table[static_cast<long long>(b) * a.maxp + blk];
-        if (page < 0 || page >= a.num_pages) {
-          if (q == 0) atomicOr(a.tab.err, kErrPage);
-        } else {
-          rec = a.cache + static_cast<long long>(page) * a.page_bytes + static_cast<long long>(h) * a.lay.block_bytes;
-          slot = pos & 15;
-        }
+      if (cp) {
+        const int woff = q < 2 ? q * bh : 2 * bh + (q - 2) * bl;
+        const int nw = grp ? bl : bh;
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+          if (w < nw) cp[woff + w] = words[w];
       }
     }
-    if (rec) {
-      const int bh = key ? KBH : VBH, bl = key ? KBL : VBL;
-      const int woff = q < 2 ? q * bh : 2 * bh + (q - 2) * bl;
-      const int nw = grp ? bl : bh;
-      uint32_t* cw = reinterpret_cast<uint32_t*>(rec + slot * a.lay.code_bytes) + woff;
-#pragma unroll
-      for (int w = 0; w < 4; ++w)
-        if (w < nw) cw[w] = words[w];
-      if (q == 0) reinterpret_cast<unsigned short*>(rec + a.lay.off_norm)[slot] = n16;
+
+    // ---- 3b. exact re-decision of flagged codes (rare; whole CTA) -----------
+    if (__syncthreads_or(near != 0)) {
+      __threadfence();           // stored words reach L2 before the patches
+      __syncthreads();
+      uint32_t mine = near;
+      for (;;) {
+        while (mine) {
+          const int idx = atomicAdd(qn, 1);
+          if (idx >= kQueueCap) break;
+          const int c = __ffs(mine) - 1;
+          mine &= mine - 1;
+          queue[idx] = static_cast<uint32_t>(row) | (static_cast<uint32_t>(32 * q + c) << 8);
+        }
+        __syncthreads();
+        const int n = min(*qn, kQueueCap);
+        for (int i = warp; i < n; i += kThreadsTC4 / 32) {
+          const int r = static_cast<int>(queue[i] & 255u), ch = static_cast<int>(queue[i] >> 8);
+          const int gs = (key ? 0 : 2) + (ch < 64 ? 0 : 1);
+          const int b = ch < 64 ? bh : bl;
+          refine_code_item(xrow_of(r), f32, a.tab.pi_df + ch * kD * 2, codeptr[r], bh, bl, ch,
+                           t64s + gs * 16, (1 << b) - 1, cents + gs * 16, sk, rown16[r], smem, &red_r[r], r, lane,
+                           &a.tab.counters[0]);
+        }
+        __syncthreads();
+        if (tid == 0) *qn = 0;
+        if (!__syncthreads_or(mine != 0)) break;
+      }
+      __threadfence();
     }
 
     // ---- 4. keys: z = r' S^T and the sign bits -------------------------------
-    if (key) {
+    if (sk) {
       fence_proxy_async();
       tc_fence_before();
       __syncthreads();
@@ -641,44 +772,54 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
           umma_f16(zt, kdesc(sbase + kOffRH, kRows, s), kdesc(sbase + kOffSL, m, s), idesc_f16(m), 1u);
         umma_commit(smem_u32(&bars[1]));
       }
-      if (!mbar_wait(smem_u32(&bars[1]), phase)) {
+      if (__syncthreads_or(!mbar_wait(smem_u32(&bars[1]), phase))) {
         failed = true;
         if (tid == 0) atomicOr(a.tab.err, kErrTimeout);
       }
       phase ^= 1;
       tc_fence_after();
       const float rho = sqrtf((red_r[row] + red_r[128 + row]) + (red_r[256 + row] + red_r[384 + row]));
+      uint32_t nearz = 0;
       if (32 * q < m) {
         float v[32];
         tmem_ld32(trow + 128 + 32 * q, v);
         const float guard = kSignGuard * rho;
-        uint32_t word = 0, nearz = 0;
+        uint32_t word = 0;
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           word |= ((~__float_as_uint(v[k])) >> 31) << k;
           nearz |= (fabsf(v[k]) < guard ? 1u : 0u) << k;
         }
-        if (!rec) nearz = 0;
-        while (nearz) {
-          const int k = __ffs(nearz) - 1;
-          nearz &= nearz - 1;
-          const int p = 32 * q + k;
-          const uint32_t* cwr = reinterpret_cast<const uint32_t*>(rec + slot * a.lay.code_bytes);
-          float cv[2 * kD];
-          for (int j = 0; j < kD; ++j) {
-            const int cj = record_code(cwr, KBH, KBL, j);
-            const GroupBook& gb = a.lay.g[j < 64 ? 0 : 1];
-            cv[2 * j] = gb.c[cj];
-            cv[2 * j + 1] = gb.c_lo[cj];
-          }
-          const uint32_t bitv = refine_sign(xrow, a.tab.a_df + static_cast<long long>(p) * kD * 2,
-                                            a.tab.s_df + static_cast<long long>(p) * kD * 2, cv, n16f);
-          word = (word & ~(1u << k)) | (bitv << k);
-          atomicAdd(&a.tab.counters[1], 1ULL);
-        }
-        if (rec) reinterpret_cast<uint32_t*>(rec + a.lay.off_signs + slot * (m / 8))[q] = word;
+        uint32_t* const sp = signptr[row];
+        if (!sp) nearz = 0;
+        if (sp) sp[q] = word;
       }
-      if (rec && q == 0)
+      if (__syncthreads_or(nearz != 0)) {
+        __threadfence();
+        __syncthreads();
+        uint32_t mine = nearz;
+        for (;;) {
+          while (mine) {
+            const int idx = atomicAdd(qn, 1);
+            if (idx >= kQueueCap) break;
+            const int k = __ffs(mine) - 1;
+            mine &= mine - 1;
+            queue[idx] = static_cast<uint32_t>(row) | (static_cast<uint32_t>(32 * q + k) << 8);
+          }
+          __syncthreads();
+          const int n = min(*qn, kQueueCap);
+          for (int i = warp; i < n; i += kThreadsTC4 / 32) {
+            const int r = static_cast<int>(queue[i] & 255u), p = static_cast<int>(queue[i] >> 8);
+            refine_sign_item(xrow_of(r), f32, a.tab.a_df + static_cast<long long>(p) * kD * 2,
+                             a.tab.s_df + static_cast<long long>(p) * kD * 2, codeptr[r], KBH, KBL, cents, centl,
+                             rown16[r], signptr[r] + (p >> 5), p & 31, lane, &a.tab.counters[1]);
+          }
+          __syncthreads();
+          if (tid == 0) *qn = 0;
+          if (!__syncthreads_or(mine != 0)) break;
+        }
+      }
+      if (rec)
         reinterpret_cast<unsigned short*>(rec + a.lay.off_rnorm)[slot] =
             __half_as_ushort(__float2half_rn(rho * n16f * kInvSqrtDHi));
     }
@@ -712,11 +853,7 @@ cudaError_t launch_tc(const QuantizeArgs& k, const QuantizeArgs& v, int nk, int 
 }  // namespace
 
 bool launch_quantize_tc(const QuantizeArgs& k, const QuantizeArgs& v, cudaStream_t s, cudaError_t* err) {
-  const QuantizeArgs& any = k.x ? k : v;
-  if (any.f32) return false;
-  if ((k.x && (k.f32 || k.lay.split != 64 || k.m % 32 || k.m > 128 || !k.lay.qjl)) ||
-      (v.x && (v.f32 || v.lay.split != 64)))
-    return false;
+  if ((k.x && (k.lay.split != 64 || k.m % 32 || k.m < 32 || k.m > 128)) || (v.x && v.lay.split != 64)) return false;
   if ((reinterpret_cast<uintptr_t>(k.x) | reinterpret_cast<uintptr_t>(v.x)) & 15) return false;
   const long long nk_vec = k.x ? static_cast<long long>(k.batch) * k.n_new * k.H : 0;
   const long long nv_vec = v.x ? static_cast<long long>(v.batch) * v.n_new * v.H : 0;

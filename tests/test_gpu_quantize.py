@@ -92,36 +92,44 @@ def test_append_one_token_at_a_time_equals_bulk():
 
 
 def test_zero_and_boundary_vectors():
-    """A zero vector and vectors placed exactly on codebook boundaries (fp64 re-decision path)."""
-    w = wl.Workload("t", "quantize", 1, 1, 1, 8, dtype="f32", seed=0)
+    """A zero vector, a vector whose fp16 norm is zero, and vectors placed exactly on codebook boundaries.
+
+    The 22 boundary vectors carry 16 boundary coordinates each: 352 exact
+    re-decisions in one tile, more than one pass of the re-decision queue holds.
+    """
+    T = 24
+    w = wl.Workload("t", "quantize", 1, 1, 1, T, dtype="f32", seed=0)
     p = th.params_for(w)
     cb = p.books[3]
-    X = np.zeros((8, 128))
-    for r in range(1, 8):
+    X = np.zeros((T, 128))
+    for r in range(1, T - 1):
         u = np.random.default_rng(r).standard_normal(128)
         u[:16] = cb.boundaries[np.arange(16) % 7]
-        y = u / np.linalg.norm(u) * 3.0
-        X[r] = p.Pi.T @ y
+        u[16:] *= np.sqrt((128 - np.sum(u[:16] ** 2)) / np.sum(u[16:] ** 2))    # ||u||^2 = d, so u is kept
+        X[r] = p.Pi.T @ (u * 3.0 / np.sqrt(128))                                # ||x|| = 3
+    X[T - 1] = np.random.default_rng(99).standard_normal(128) * 1e-9     # ||x|| ~ 1e-8: fp16 norm 0
     X = X.astype(np.float32)
-    K = X.reshape(1, 8, 1, 128)
-    bt = np.array([[0]], dtype=np.int32)
+    K = X.reshape(1, T, 1, 128)
+    bt = np.array([[0, 1]], dtype=np.int32)
     ctx = ctx_for(w)
     try:
         tq.tq_refine_counters(ctx, reset=True)
-        kc, vc = alloc_caches(ctx, 1, 1)
-        gpu_quantize(ctx, K, K, "f32", [0], bt, 1, kc, vc)
+        kc, vc = alloc_caches(ctx, 1, 2)
+        gpu_quantize(ctx, K, K, "f32", [0], bt, 2, kc, vc)
+        assert tq.tq_check_device_status(ctx) == 0
         refined = tq.tq_refine_counters(ctx)
         got_k, got_v = kc.cpu().numpy(), vc.cpu().numpy()
     finally:
         tq.tq_destroy(ctx)
-    assert refined[0] >= 7 * 16
-    pages, slots, heads = seq_locations(bt, 0, np.arange(8), 1)
+    assert refined[0] >= 2 * (T - 2) * 16
+    pages, slots, heads = seq_locations(bt, 0, np.arange(T), 1)
     for kind, got in (("k", got_k), ("v", got_v)):
         q = oracle.quantize_vectors(p, X.astype(np.float64), kind)
+        assert q["n16"][T - 1] == 0 and q["norm"][T - 1] > 0
         res = th.compare_records(p, kind, got, q, oracle.quantize_exclusions(p, q, kind), pages, slots, heads, 1)
         assert res["codes_mismatch"] == 0 and res["norm_mismatch"] == 0, res
         # the values within 1e-6 of a boundary were re-decided in fp64: they agree too
-        assert res["codes_excluded"] >= 7 * 16 and res["codes_mismatch_excluded"] == 0, res
+        assert res["codes_excluded"] >= (T - 2) * 16 and res["codes_mismatch_excluded"] == 0, res
         if kind == "k":
             assert res["signs_mismatch"] == 0, res
 
