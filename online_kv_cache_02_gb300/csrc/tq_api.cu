@@ -133,6 +133,29 @@ int pick_chunk(int units, int max_seq_len) {
   return best_chunk;
 }
 
+// Chunk for the persistent kernel (one warp per chunk, chunks taken from a
+// counter): the busiest warp handles ceil(items / slots) chunks; minimise that
+// times (chunk + a per-chunk cost of about 64 tokens), chunks of >= 256 tokens.
+int pick_chunk_warps(int units, int max_seq_len, int slots) {
+  long long best_cost = -1;
+  int best_chunk = ((max_seq_len + kPage - 1) / kPage) * kPage;
+  if (best_chunk < kPage) best_chunk = kPage;
+  for (int nch = 1; nch <= 4096; ++nch) {
+    long long chunk = (max_seq_len + nch - 1) / nch;
+    chunk = ((chunk + kPage - 1) / kPage) * kPage;
+    if (chunk < kPage) chunk = kPage;
+    if (chunk < 256 && nch > 1) break;
+    const long long real = (max_seq_len + chunk - 1) / chunk;
+    const long long items = real * units;
+    const long long cost = ((items + slots - 1) / slots) * (chunk + 64);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_chunk = static_cast<int>(chunk);
+    }
+  }
+  return best_chunk;
+}
+
 }  // namespace
 
 extern "C" tq_status tq_config_init(tq_config* cfg, int d, int b, int m, uint64_t seed) {
@@ -327,7 +350,7 @@ int nchunks_for(int max_seq_len, int chunk) { return max_seq_len <= 0 ? 1 : (max
 
 size_t ws_bytes(int B, int Hq, int d, int m, int nch) {
   return align256(sizeof(float) * static_cast<size_t>(B) * Hq * (d + m)) +
-         align256(sizeof(float) * static_cast<size_t>(B) * Hq * nch * (d + 2));
+         align256(sizeof(float) * static_cast<size_t>(B) * Hq * nch * (d + 2)) + 256;   // + work counters
 }
 }  // namespace
 
@@ -373,7 +396,10 @@ tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batc
   if (batch == 0) return TQ_OK;
   if (!q || !seq_lens || !block_table || !k_cache || !v_cache || !out || !workspace)
     return TQ_ERR_INVALID_ARG;
-  int chunk = chunk_tokens ? chunk_tokens : pick_chunk(batch * H, max_seq_len);
+  const int lut_slots = lut_decode_slots(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H);
+  int chunk = chunk_tokens              ? chunk_tokens
+              : lut_slots > 0           ? pick_chunk_warps(batch * H, max_seq_len, lut_slots)
+                                        : pick_chunk(batch * H, max_seq_len);
   int nch = nchunks_for(max_seq_len, chunk);
   const int d = ctx->cfg.d, m = ctx->cfg.m;
   size_t need = ws_bytes(batch, Hq, d, m, nch);
@@ -406,6 +432,8 @@ tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batc
   char* w = static_cast<char*>(workspace);
   a.qprep = reinterpret_cast<float*>(w);
   a.part = reinterpret_cast<float*>(w + align256(sizeof(float) * static_cast<size_t>(batch) * Hq * (d + m)));
+  a.sched = reinterpret_cast<int*>(w + align256(sizeof(float) * static_cast<size_t>(batch) * Hq * (d + m)) +
+                                   align256(sizeof(float) * static_cast<size_t>(batch) * Hq * nch * (d + 2)));
   a.out = out;
   return launch_decode(a, stages, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }

@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(kThreads) qprep_kernel(DecodeArgs a) {
   const long long r0 = static_cast<long long>(blockIdx.x) * kQB;
   const long long nq = static_cast<long long>(a.B) * a.Hq;
   const int i = threadIdx.x;
+  if (blockIdx.x == 0 && i < 2 && a.sched) a.sched[i] = 0;
   for (int r = 0; r < kQB; ++r) qs[r][i] = r0 + r < nq ? load_q(a.q, a.f32, (r0 + r) * kD + i) : 0.0f;
   __syncthreads();
   float acc[kQB];
@@ -289,13 +290,19 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(DecodeArgs a) {
   __shared__ float os[kMaxGroup][kD];
   const long long r0 = static_cast<long long>(blockIdx.x) * a.G;   // first query head (b*Hq + h*G)
   const int j = threadIdx.x;
+  // chunks that start at or past the sequence end hold no partial
+  int L = a.seq_lens[blockIdx.x / a.H] + a.len_add;
+  L = L < 0 ? 0 : L;
+  L = L > a.max_seq_len ? a.max_seq_len : L;
+  L = L > a.maxp * kPage ? a.maxp * kPage : L;
+  const int nc = min(a.nchunks, (L + a.chunk - 1) / a.chunk);
   for (int r = 0; r < a.G; ++r) {
     const float* P = a.part + (r0 + r) * a.nchunks * (kD + 2);
     float M = -INFINITY;
-    for (int c = 0; c < a.nchunks; ++c) M = fmaxf(M, P[c * (kD + 2)]);
+    for (int c = 0; c < nc; ++c) M = fmaxf(M, P[c * (kD + 2)]);
     float l = 0.0f, A = 0.0f;
 #pragma unroll 4
-    for (int c = 0; c < a.nchunks; ++c) {
+    for (int c = 0; c < nc; ++c) {
       const float w = exp2f(P[c * (kD + 2)] - M);
       l = fmaf(w, P[c * (kD + 2) + 1], l);
       A = fmaf(w, P[c * (kD + 2) + 2 + j], A);
@@ -333,7 +340,7 @@ cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
   }
   if (stages & TQ_STAGE_PARTIALS) {
     cudaError_t em = cudaSuccess;
-    if (launch_partials_mma(a, s, &em)) {
+    if (launch_partials_lut(a, s, &em) || launch_partials_mma(a, s, &em)) {
       if (em != cudaSuccess) return em;
     } else {
     switch (a.G) {

@@ -1,0 +1,599 @@
+// Decode attention, split-K partials stage: persistent tensor-core kernel with
+// shared-memory lookup-table dequantization.
+//
+// [P4] riverfrot.github.io "TurboQuant란 무엇이며…", §2.2 (decode: one query per
+// head against every cached key, softmax, weighted sum of values), §4.2 (the
+// codebook is only looked up at run time), §4.3 (stage-1 score plus the 1-bit
+// QJL correction; softmax(QK^T/sqrt(d))); [P2] "생각정리 209 (TurboQuant)", stage 2.
+//
+// One CTA of 16 warps per SM.  A work item is one (sequence, KV head, chunk);
+// each warp takes items from a global counter and streams their 16-token pages
+// through its own 3-stage ring (cp.async.bulk, mbarrier completion); the ring
+// runs on across item boundaries, so a warp never drains between items.
+//
+// Dequantization is a table lookup: one byte of packed codes (two codes) indexes
+// a table whose entry is the fp16 pair of their centroids.  Each entry is
+// replicated for the 32 lanes (entry e, lane l at byte 256 e + 4 l, K table at
+// +0, V table at +128), so a warp's 32 lookups hit 32 different banks, and one
+// prmt builds the address (the code byte as byte 1, the lane offset as byte 0).
+// Keys pair two channels of one token (the byte as stored); values pair one
+// channel of two consecutive tokens (two tokens' codes interleaved by lop3),
+// the layout the value MMA wants.  3-bit octets are first gathered into eight
+// nibbles (channels 6 and 7 sit in the spare bit of each nibble).
+//   * scores: S1 = K^ Q~^T and S2 = sign * U^T, m16n8k16 with the 16 tokens on
+//     M and the G <= 8 query heads of the KV head on N (K = channels);
+//   * logits = (n_k/sqrt(d) S1 + sqrt(pi/2)/m rho S2) * scale; online softmax
+//     on the accumulator fragments;
+//   * P' = p * n_v / sqrt(d) through a 256-byte shared tile into the B operand
+//     of O^T += V^^T P'^T (M = channels, K = tokens).
+// The channel order inside the fragments is a fixed permutation that makes each
+// thread's code bytes contiguous; Q~ and the output use the same permutation.
+//
+// Supported here: d = 128, m = 128, channel split 64, the bit-width
+// combinations instantiated below.  Other configurations run tq_decode_mma.cu
+// or the CUDA-core kernel in tq_decode.cu.
+
+#include "tq_internal.h"
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace tq {
+namespace {
+
+constexpr int kWarpsL = 16;
+constexpr int kThreadsL = 32 * kWarpsL;
+constexpr float kInvSqrtD = 0.08838834764831845f;
+constexpr float kSqrtHalfPi = 1.2533141373155003f;
+constexpr uint32_t kErrTimeout = 8u;
+constexpr int kWaitLimit = 1 << 22;
+constexpr float kNegBig = -1.0e30f;    // finite "minus infinity" (see tq_decode_mma.cu)
+constexpr int kSmemLimit = 232448;     // opt-in shared memory per block
+
+// ---------------------------------------------------------------------------
+// PTX helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(s));
+  return d;
+}
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Bounded wait for phase `parity`; false after kWaitLimit polls.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (int i = 0; i < kWaitLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t f16bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) { return f16bits(lo) | (f16bits(hi) << 16); }
+
+// ---------------------------------------------------------------------------
+// tables
+// ---------------------------------------------------------------------------
+// Entries used per bit width: 4-bit bytes 0..255; 3-bit gathered nibble pairs
+// 0x00..0x77; 2-bit nibbles (two 2-bit codes) 0..15.
+__host__ __device__ constexpr int lut_entries(int b) { return b == 4 ? 256 : b == 3 ? 120 : 16; }
+__host__ __device__ constexpr int region_bytes(int kb, int vb) {
+  return 256 * (lut_entries(kb) > lut_entries(vb) ? lut_entries(kb) : lut_entries(vb));
+}
+
+// Code of a stored field value (4-bit fields are sign-magnitude, see tq.h).
+__device__ __forceinline__ int stored_code(int b, int f) { return b == 4 ? (f < 8 ? f + 8 : 15 - f) : f; }
+
+// fp16 pair of the centroids of the two fields of index e.
+__device__ uint32_t lut_entry(const GroupBook& gb, int b, int e) {
+  const int w = b == 2 ? 2 : 4;
+  const int mask = b == 4 ? 15 : b == 3 ? 7 : 3;
+  return pack_h2(gb.c[stored_code(b, e & mask)], gb.c[stored_code(b, (e >> w) & mask)]);
+}
+
+// 3-bit octet (24 bits as stored) -> eight nibbles, nibble i = code of channel i.
+// Channels 0-5 sit in nibbles already; the spare bits 3/11/19 (channel 6) and
+// 7/15/23 (channel 7) are gathered to bits 24-26 and 28-30 by one multiply.
+__device__ __forceinline__ uint32_t gather_octet(uint32_t v) {
+  return (v & 0x00777777u) | (((v & 0x00888888u) * 0x00204080u) & 0x77000000u);
+}
+
+__device__ __forceinline__ uint32_t bits_at(const uint32_t* w, int off) {
+  return __funnelshift_r(w[off >> 5], w[(off >> 5) + 1], off & 31);
+}
+
+// The eight key pair indices of thread slice t (channels 16t..16t+15 of a
+// group): pair j is byte j&3 of x[j>>2].
+template <int B>
+__device__ __forceinline__ void k_slice(const uint32_t* grp, int t, uint32_t (&x)[2]) {
+  if (B == 4) {
+    const uint2 w = reinterpret_cast<const uint2*>(grp)[t];
+    x[0] = w.x;
+    x[1] = w.y;
+  } else if (B == 3) {
+    x[0] = gather_octet(bits_at(grp, 48 * t));
+    x[1] = gather_octet(bits_at(grp, 48 * t + 24));
+  } else {
+    const uint32_t w = grp[t];
+    x[0] = w & 0x0F0F0F0Fu;
+    x[1] = (w >> 4) & 0x0F0F0F0Fu;
+  }
+}
+// Channel (within the slice) of the low half of key pair j.
+__host__ __device__ constexpr int k_pair_channel(int b, int j) { return b == 2 ? (j < 4 ? 4 * j : 4 * (j - 4) + 2) : 2 * j; }
+
+// Codes of channels 8g..8g+7 of one value vector (group-relative words).
+template <int B>
+__device__ __forceinline__ uint32_t v_word(const uint32_t* grp, int g) {
+  if (B == 4) return grp[g];
+  if (B == 3) return gather_octet(bits_at(grp, 24 * g));
+  return (grp[g >> 1] >> (16 * (g & 1))) & 0xFFFFu;
+}
+// Token-pair indices of the eight channels from the words of tokens a and a+1:
+// m-tile mt uses byte mt&3 of (mt < 4 ? lo : hi).
+template <int B>
+__device__ __forceinline__ void v_pairs(uint32_t xa, uint32_t xb, uint32_t& lo, uint32_t& hi) {
+  if (B == 2) {
+    const uint32_t A = (xa & 0x3333u) | ((xb << 2) & 0xCCCCu);
+    const uint32_t Bm = ((xa >> 2) & 0x3333u) | (xb & 0xCCCCu);
+    const uint32_t C = A | (Bm << 16);
+    lo = C & 0x0F0F0F0Fu;
+    hi = (C >> 4) & 0x0F0F0F0Fu;
+  } else {
+    lo = (xa & 0x0F0F0F0Fu) | ((xb << 4) & 0xF0F0F0F0u);
+    hi = ((xa >> 4) & 0x0F0F0F0Fu) | (xb & 0xF0F0F0F0u);
+  }
+}
+// Channel (within the eight) that m-tile mt covers.
+__host__ __device__ constexpr int v_channel(int b, int mt) {
+  return b == 2 ? (mt == 0 ? 0 : mt == 1 ? 4 : mt == 2 ? 1 : mt == 3 ? 5 : mt == 4 ? 2 : mt == 5 ? 6 : mt == 6 ? 3 : 7)
+                : (mt < 4 ? 2 * mt : 2 * (mt - 4) + 1);
+}
+
+// QJL sign pair (projections k, k+16 of a 32-bit word): +1.0 if the bit is set, else -1.0.
+__device__ __forceinline__ uint32_t sign_pair(uint32_t notw, int k) {
+  return ((notw << (15 - k)) & 0x80008000u) | 0x3C003C00u;
+}
+
+struct Slot {
+  int item;    // -1: no more work
+  int page;    // page index within the item's chunk
+  int valid;   // 0: page id out of range (flagged), no data
+  int pad;
+};
+
+template <int KBH, int KBL, int VBH, int VBL, bool QJL>
+struct Geo {
+  static constexpr int CBK = (64 * KBH + 64 * KBL) / 8;
+  static constexpr int CBV = (64 * VBH + 64 * VBL) / 8;
+  static constexpr int KBB = 16 * (CBK + (QJL ? 16 + 2 : 0) + 2);
+  static constexpr int VBB = 16 * (CBV + 2);
+  static constexpr int STAGE = KBB + VBB;
+  static constexpr int K_SIGNS = 16 * CBK;
+  static constexpr int K_NORM = K_SIGNS + (QJL ? 16 * 16 : 0);
+  static constexpr int K_RNORM = K_NORM + 32;
+  static constexpr int V_NORM = 16 * CBV;
+  static constexpr int R0 = region_bytes(KBH, VBH);
+  static constexpr int R1 = region_bytes(KBL, VBL);
+  static constexpr int TABLES = R0 + R1;
+  static constexpr int EXTRA = kWarpsL * (8 * 16 * 2 + 16 * 3 + 16 * 3) + 256;   // ptile, bars, slots, align
+  static constexpr int STAGES = TABLES + kWarpsL * 3 * STAGE + EXTRA <= kSmemLimit ? 3 : 2;
+  static constexpr int RING = TABLES;                                              // offset of the rings
+  static constexpr int BARS = RING + kWarpsL * STAGES * STAGE;
+  static constexpr int SLOTS = BARS + kWarpsL * STAGES * 8;
+  static constexpr int PTILE = (SLOTS + kWarpsL * STAGES * 16 + 15) & ~15;
+  static constexpr int SMEM = PTILE + kWarpsL * 8 * 16 * 2;
+  static_assert(STAGE % 16 == 0 && RING % 128 == 0, "bulk copy alignment");
+  static_assert(SMEM <= kSmemLimit, "shared memory per block");
+};
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <int KBH, int KBL, int VBH, int VBL, bool QJL>
+__global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a, int total_items) {
+  using Gm = Geo<KBH, KBL, VBH, VBL, QJL>;
+  constexpr int S = Gm::STAGES;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+
+  // ---- tables (once per CTA) ------------------------------------------------
+  {
+    constexpr int E0 = Gm::R0 / 256, E1 = Gm::R1 / 256;
+    for (int i = threadIdx.x; i < (E0 + E1) * 16; i += kThreadsL) {
+      const int quad = i & 7, which = (i >> 3) & 1;
+      int e = i >> 4;
+      const int region = e < E0 ? 0 : 1;
+      if (region) e -= E0;
+      const int b = region ? (which ? VBL : KBL) : (which ? VBH : KBH);
+      const GroupBook& gb = (which ? a.vl : a.kl).g[region];
+      const uint32_t v = e < lut_entries(b) ? lut_entry(gb, b, e) : 0u;
+      *reinterpret_cast<uint4*>(smem + (region ? Gm::R0 : 0) + e * 256 + which * 128 + quad * 16) =
+          make_uint4(v, v, v, v);
+    }
+  }
+  unsigned char* ring = smem + Gm::RING + warp * S * Gm::STAGE;
+  unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem + Gm::BARS) + warp * S;
+  Slot* slots = reinterpret_cast<Slot*>(smem + Gm::SLOTS) + warp * S;
+  __half(*ptile)[16] = reinterpret_cast<__half(*)[16]>(smem + Gm::PTILE + warp * 8 * 16 * 2);
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  const int nch = a.nchunks, C = a.chunk;
+  auto seq_len = [&](int b) {
+    int L = a.seq_lens[b] + a.len_add;
+    if (L < 0 || L > a.max_seq_len || L > a.maxp * kPage) {
+      atomicOr(a.tab.err, kErrSeqLen);
+      L = L < 0 ? 0 : L;
+      L = L > a.max_seq_len ? a.max_seq_len : L;
+      L = L > a.maxp * kPage ? a.maxp * kPage : L;
+    }
+    return L;
+  };
+
+  // ---- producer state (meaningful in lane 0) --------------------------------
+  int p_item = 0, p_page = 0, p_npages = 0, p_b = 0, p_h = 0, p_chunk = 0;   // p_item -1: done
+  auto issue = [&](int s) {      // lane 0: fill slot s with the next page of this warp's stream
+    const uint32_t bar = smem_u32(&bars[s]);
+    while (p_item >= 0 && p_page >= p_npages) {
+      const int it = atomicAdd(a.sched, 1);
+      if (it >= total_items) {
+        p_item = -1;
+        break;
+      }
+      p_chunk = it % nch;
+      const int bh = it / nch;
+      p_h = bh % a.H;
+      p_b = bh / a.H;
+      const int L = seq_len(p_b);
+      const int t0 = p_chunk * C;
+      if (t0 >= L) continue;                  // chunk past the end: no partial (the merge skips it)
+      p_item = it;
+      p_page = 0;
+      p_npages = (min(t0 + C, L) - t0 + kPage - 1) / kPage;
+    }
+    Slot& sl = slots[s];
+    if (p_item < 0) {
+      sl.item = -1;
+      sl.valid = 0;
+      mbar_arrive(bar);
+      return;
+    }
+    sl.item = p_item;
+    sl.page = p_page;
+    const int page = a.block_table[static_cast<long long>(p_b) * a.maxp + p_chunk * (C / kPage) + p_page];
+    ++p_page;
+    if (page < 0 || page >= a.num_pages) {
+      atomicOr(a.tab.err, kErrPage);
+      sl.valid = 0;
+      mbar_arrive(bar);
+      return;
+    }
+    sl.valid = 1;
+    unsigned char* dst = ring + s * Gm::STAGE;
+    fence_proxy_async();
+    mbar_arrive_tx(bar, Gm::STAGE);
+    bulk_g2s(smem_u32(dst), a.kc + static_cast<long long>(page) * a.k_page_bytes + static_cast<long long>(p_h) * Gm::KBB,
+             Gm::KBB, bar);
+    bulk_g2s(smem_u32(dst + Gm::KBB),
+             a.vc + static_cast<long long>(page) * a.v_page_bytes + static_cast<long long>(p_h) * Gm::VBB, Gm::VBB, bar);
+  };
+  if (lane == 0)
+    for (int s = 0; s < S; ++s) issue(s);
+  __syncwarp();
+
+  // ---- consumer state ---------------------------------------------------------
+  const uint32_t lbk = static_cast<uint32_t>(lane) * 4u, lbv = lbk + 128u;
+  const float k1 = kInvSqrtD * a.scale_log2;
+  const float k2 = kSqrtHalfPi / 128.0f * a.scale_log2;
+  int cur = -1, c_b = 0, c_h = 0, c_chunk = 0, c_t0 = 0, c_t1 = 0;
+  uint32_t qf[16], uf[16];
+  float acc[8][4];
+  float m_run[2], l_run[2];
+  bool failed = false;
+
+  auto flush = [&]() {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float l = l_run[c];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      const int hh = 2 * t + c;
+      if (hh < a.G) {
+        float* dst = a.part + ((static_cast<long long>(c_b) * a.Hq + c_h * a.G + hh) * nch + c_chunk) * (kD + 2);
+        if (g == 0) {
+          dst[0] = m_run[c];
+          dst[1] = l;
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          dst[2 + 8 * g + v_channel(VBH, mt)] = acc[mt][c];
+          dst[2 + 64 + 8 * g + v_channel(VBL, mt)] = acc[mt][c + 2];
+        }
+      }
+    }
+  };
+  auto start = [&](int item) {
+    c_chunk = item % nch;
+    const int bh = item / nch;
+    c_h = bh % a.H;
+    c_b = bh / a.H;
+    c_t0 = c_chunk * C;
+    c_t1 = min(c_t0 + C, seq_len(c_b));
+    const bool head_ok = g < a.G;
+    const float* qrow = a.qprep + (static_cast<long long>(c_b) * a.Hq + c_h * a.G + (head_ok ? g : 0)) * (kD + a.m);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int grp = kk >> 2, j = 2 * (kk & 3) + e;
+        const int ch = 64 * grp + 16 * t + k_pair_channel(grp ? KBL : KBH, j);
+        qf[2 * kk + e] = head_ok ? pack_h2(qrow[ch], qrow[ch + 1]) : 0u;
+      }
+    }
+#pragma unroll
+    for (int p = 0; p < 16; ++p) uf[p] = (QJL && head_ok) ? pack_h2(qrow[kD + 32 * t + p], qrow[kD + 32 * t + p + 16]) : 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+    m_run[0] = m_run[1] = kNegBig;
+    l_run[0] = l_run[1] = 0.0f;
+  };
+
+  // a warp consumes at most one slot per page of the launch plus its end
+  // marker; more means a broken stream: flag it and stop
+  const long long max_slots = static_cast<long long>(total_items) * (C / kPage) + S;
+  int i = 0, drain_from = 1;
+  for (;; ++i) {
+    const int s = i % S;
+    if (i > max_slots) {
+      failed = true;
+      drain_from = 0;
+      if (lane == 0) atomicOr(a.tab.err, kErrTimeout);
+      break;
+    }
+    // every lane polls; the vote makes a give-up uniform across the warp
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars[s]), (i / S) & 1))) {
+      failed = true;
+      if (lane == 0) atomicOr(a.tab.err, kErrTimeout);
+      break;
+    }
+    const Slot sl = slots[s];
+    if (sl.item < 0) {                     // end of this warp's stream
+      if (cur >= 0) flush();
+      break;
+    }
+    if (sl.item != cur) {
+      if (cur >= 0) flush();
+      cur = sl.item;
+      start(cur);
+    }
+    if (sl.valid) {
+      const unsigned char* kb = ring + s * Gm::STAGE;
+      const unsigned char* vb = kb + Gm::KBB;
+      const int pbase = c_t0 + sl.page * kPage;
+      // ---- scores ---------------------------------------------------------
+      float s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const uint32_t* ra = reinterpret_cast<const uint32_t*>(kb + g * Gm::CBK);
+        const uint32_t* rb = reinterpret_cast<const uint32_t*>(kb + (g + 8) * Gm::CBK);
+        uint32_t xa0[2], xb0[2], xa1[2], xb1[2];
+        k_slice<KBH>(ra, t, xa0);
+        k_slice<KBH>(rb, t, xb0);
+        k_slice<KBL>(ra + 2 * KBH, t, xa1);
+        k_slice<KBL>(rb + 2 * KBH, t, xb1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int j0 = 2 * (kk & 3), j1 = j0 + 1;
+          const uint32_t* xa = kk < 4 ? xa0 : xa1;
+          const uint32_t* xb = kk < 4 ? xb0 : xb1;
+          const unsigned char* tb = smem + (kk < 4 ? 0 : Gm::R0);
+          const uint32_t s0 = 0x7604u | (static_cast<uint32_t>(j0 & 3) << 4);
+          const uint32_t s1x = 0x7604u | (static_cast<uint32_t>(j1 & 3) << 4);
+          const uint32_t a0 = *reinterpret_cast<const uint32_t*>(tb + prmt(xa[j0 >> 2], lbk, s0));
+          const uint32_t a1 = *reinterpret_cast<const uint32_t*>(tb + prmt(xb[j0 >> 2], lbk, s0));
+          const uint32_t a2 = *reinterpret_cast<const uint32_t*>(tb + prmt(xa[j1 >> 2], lbk, s1x));
+          const uint32_t a3 = *reinterpret_cast<const uint32_t*>(tb + prmt(xb[j1 >> 2], lbk, s1x));
+          mma16816(s1, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
+        }
+        if (QJL) {
+          const uint32_t* sg = reinterpret_cast<const uint32_t*>(kb + Gm::K_SIGNS);
+          const uint32_t na = ~sg[g * 4 + t], nb = ~sg[(g + 8) * 4 + t];
+#pragma unroll
+          for (int st = 0; st < 8; ++st)
+            mma16816(s2, sign_pair(na, 2 * st), sign_pair(nb, 2 * st), sign_pair(na, 2 * st + 1),
+                     sign_pair(nb, 2 * st + 1), uf[2 * st], uf[2 * st + 1]);
+        }
+      }
+      const __half* nk = reinterpret_cast<const __half*>(kb + Gm::K_NORM);
+      const __half* rk = reinterpret_cast<const __half*>(kb + Gm::K_RNORM);
+      const __half* nv = reinterpret_cast<const __half*>(vb + Gm::V_NORM);
+      const bool vg = pbase + g < c_t1;
+      const bool vg8 = pbase + g + 8 < c_t1;
+      float lg[4];
+      {
+        const float nkg = __half2float(nk[g]), nkg8 = __half2float(nk[g + 8]);
+        const float rkg = QJL ? __half2float(rk[g]) : 0.f, rkg8 = QJL ? __half2float(rk[g + 8]) : 0.f;
+        lg[0] = vg ? fmaf(nkg * k1, s1[0], rkg * k2 * s2[0]) : kNegBig;
+        lg[1] = vg ? fmaf(nkg * k1, s1[1], rkg * k2 * s2[1]) : kNegBig;
+        lg[2] = vg8 ? fmaf(nkg8 * k1, s1[2], rkg8 * k2 * s2[2]) : kNegBig;
+        lg[3] = vg8 ? fmaf(nkg8 * k1, s1[3], rkg8 * k2 * s2[3]) : kNegBig;
+      }
+      // ---- online softmax over this page (heads 2t, 2t+1) -------------------
+      float pr[4];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float mx = fmaxf(lg[c], lg[c + 2]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float m_new = fmaxf(m_run[c], mx);
+        const float alpha = exp2f(m_run[c] - m_new);
+        pr[c] = exp2f(lg[c] - m_new);
+        pr[c + 2] = exp2f(lg[c + 2] - m_new);
+        l_run[c] = fmaf(l_run[c], alpha, pr[c] + pr[c + 2]);
+        m_run[c] = m_new;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          acc[mt][c] *= alpha;
+          acc[mt][c + 2] *= alpha;
+        }
+      }
+      // ---- P' = p * nv / sqrt(d) into the transposed shared tile -------------
+      {
+        const float wg = vg ? __half2float(nv[g]) * kInvSqrtD : 0.0f;
+        const float wg8 = vg8 ? __half2float(nv[g + 8]) * kInvSqrtD : 0.0f;
+        ptile[2 * t][g] = __float2half_rn(pr[0] * wg);
+        ptile[2 * t + 1][g] = __float2half_rn(pr[1] * wg);
+        ptile[2 * t][g + 8] = __float2half_rn(pr[2] * wg8);
+        ptile[2 * t + 1][g + 8] = __float2half_rn(pr[3] * wg8);
+      }
+      __syncwarp();
+      const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(&ptile[g][2 * t]);
+      const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(&ptile[g][2 * t + 8]);
+      // ---- O^T += V^^T P'^T ---------------------------------------------------
+      {
+        const uint32_t* r0 = reinterpret_cast<const uint32_t*>(vb + (2 * t) * Gm::CBV);
+        const uint32_t* r1 = reinterpret_cast<const uint32_t*>(vb + (2 * t + 1) * Gm::CBV);
+        const uint32_t* r8 = reinterpret_cast<const uint32_t*>(vb + (2 * t + 8) * Gm::CBV);
+        const uint32_t* r9 = reinterpret_cast<const uint32_t*>(vb + (2 * t + 9) * Gm::CBV);
+        uint32_t hl0, hh0, hl1, hh1, ll0, lh0, ll1, lh1;   // [group][token pair]
+        v_pairs<VBH>(v_word<VBH>(r0, g), v_word<VBH>(r1, g), hl0, hh0);
+        v_pairs<VBH>(v_word<VBH>(r8, g), v_word<VBH>(r9, g), hl1, hh1);
+        v_pairs<VBL>(v_word<VBL>(r0 + 2 * VBH, g), v_word<VBL>(r1 + 2 * VBH, g), ll0, lh0);
+        v_pairs<VBL>(v_word<VBL>(r8 + 2 * VBH, g), v_word<VBL>(r9 + 2 * VBH, g), ll1, lh1);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const uint32_t sel = 0x7604u | (static_cast<uint32_t>(mt & 3) << 4);
+          const uint32_t a0 = *reinterpret_cast<const uint32_t*>(smem + prmt(mt < 4 ? hl0 : hh0, lbv, sel));
+          const uint32_t a1 = *reinterpret_cast<const uint32_t*>(smem + Gm::R0 + prmt(mt < 4 ? ll0 : lh0, lbv, sel));
+          const uint32_t a2 = *reinterpret_cast<const uint32_t*>(smem + prmt(mt < 4 ? hl1 : hh1, lbv, sel));
+          const uint32_t a3 = *reinterpret_cast<const uint32_t*>(smem + Gm::R0 + prmt(mt < 4 ? ll1 : lh1, lbv, sel));
+          mma16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) issue(s);
+    __syncwarp();
+  }
+
+  if (failed && lane == 0) {
+    // slots i .. i+S-1 hold fills not consumed yet (slot i already gave up
+    // after a timeout): let their copies land before the CTA can exit
+    for (int k = drain_from; k < S; ++k) (void)mbar_wait(smem_u32(&bars[(i + k) % S]), ((i + k) / S) & 1);
+  }
+  // the last warp to finish resets the work counter for the next launch
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    const int total_warps = gridDim.x * kWarpsL;
+    if (atomicAdd(a.sched + 1, 1) == total_warps - 1) {
+      a.sched[0] = 0;
+      a.sched[1] = 0;
+      __threadfence();
+    }
+  }
+}
+
+template <int KBH, int KBL, int VBH, int VBL, bool QJL>
+cudaError_t launch_lut(const DecodeArgs& a, int items, cudaStream_t s) {
+  using Gm = Geo<KBH, KBL, VBH, VBL, QJL>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(lut_partials_kernel<KBH, KBL, VBH, VBL, QJL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int need = (items + kWarpsL - 1) / kWarpsL;
+  const int grid = need < sms ? (need > 0 ? need : 1) : sms;
+  lut_partials_kernel<KBH, KBL, VBH, VBL, QJL><<<grid, kThreadsL, Gm::SMEM, s>>>(a, items);
+  return cudaGetLastError();
+}
+
+template <int KBH, int KBL, int VBH, int VBL>
+cudaError_t launch_lut_q(const DecodeArgs& a, int items, cudaStream_t s) {
+  return a.kl.qjl ? launch_lut<KBH, KBL, VBH, VBL, true>(a, items, s) : launch_lut<KBH, KBL, VBH, VBL, false>(a, items, s);
+}
+
+int combo_code(const KindLayout& kl, const KindLayout& vl) {
+  return kl.g[0].bits * 1000 + kl.g[1].bits * 100 + vl.g[0].bits * 10 + vl.g[1].bits;
+}
+
+}  // namespace
+
+int lut_decode_slots(const KindLayout& kl, const KindLayout& vl, int m, int G) {
+  if (m != 128 || kl.split != 64 || vl.split != 64 || G > 8) return 0;
+  switch (combo_code(kl, vl)) {
+    case 3333: case 4343: case 3232: case 4444: case 2222: case 4422: break;
+    default: return 0;
+  }
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms * kWarpsL;
+}
+
+bool launch_partials_lut(const DecodeArgs& a, cudaStream_t s, cudaError_t* err) {
+  if (!lut_decode_slots(a.kl, a.vl, a.m, a.G) || !a.sched) return false;
+  if ((reinterpret_cast<uintptr_t>(a.kc) | reinterpret_cast<uintptr_t>(a.vc)) & 15) return false;
+  if ((a.k_page_bytes | a.v_page_bytes) & 15) return false;
+  const long long items = static_cast<long long>(a.B) * a.H * a.nchunks;
+  if (items > (1LL << 30)) return false;
+  const int n = static_cast<int>(items);
+  switch (combo_code(a.kl, a.vl)) {
+    case 3333: *err = launch_lut_q<3, 3, 3, 3>(a, n, s); return true;
+    case 4343: *err = launch_lut_q<4, 3, 4, 3>(a, n, s); return true;
+    case 3232: *err = launch_lut_q<3, 2, 3, 2>(a, n, s); return true;
+    case 4444: *err = launch_lut_q<4, 4, 4, 4>(a, n, s); return true;
+    case 2222: *err = launch_lut_q<2, 2, 2, 2>(a, n, s); return true;
+    case 4422: *err = launch_lut_q<4, 4, 2, 2>(a, n, s); return true;
+    default: return false;
+  }
+}
+
+}  // namespace tq

@@ -106,6 +106,7 @@ struct DecodeArgs {
   float* qprep;          // [B][Hq][d + m]
   float* part;           // [B][Hq][nchunks][d + 2]
   float* out;            // [B][Hq][d]
+  int* sched;            // [2] work counter and finished-warp count of the persistent kernel (zeroed by qprep)
 };
 
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
@@ -114,6 +115,10 @@ cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
 bool launch_quantize_tc(const QuantizeArgs& k, const QuantizeArgs& v, cudaStream_t s, cudaError_t* err);
 cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s);
 bool launch_partials_mma(const DecodeArgs& a, cudaStream_t s, cudaError_t* err);
+// Persistent lookup-table kernel (tq_decode_lut.cu): warp slots it runs with
+// (0: configuration not supported), and its launch (false: not supported).
+int lut_decode_slots(const KindLayout& kl, const KindLayout& vl, int m, int G);
+bool launch_partials_lut(const DecodeArgs& a, cudaStream_t s, cudaError_t* err);
 
 }  // namespace tq
 
