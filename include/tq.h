@@ -210,7 +210,9 @@ tq_status tq_append_decode(const tq_ctx* ctx, const void* k_new, const void* v_n
 /* Synchronise the device and report (then clear) the context's device error
  * word: TQ_OK, or TQ_ERR_DEVICE_CHECK with the bits in *flags (may be NULL):
  * 1 = page id out of range, 2 = position beyond the block table,
- * 4 = sequence length beyond max_seq_len or the block table. */
+ * 4 = sequence length beyond max_seq_len or the block table, 8 = a bounded
+ * wait inside a kernel gave up (that launch's results are incomplete),
+ * 16 = a kernel's shared-memory layout did not fit (it did no work). */
 tq_status tq_check_device_status(const tq_ctx* ctx, uint32_t* flags);
 
 /* Counters of near-boundary decisions the quantize kernels re-took in fp64

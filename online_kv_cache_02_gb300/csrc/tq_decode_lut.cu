@@ -47,7 +47,6 @@ constexpr int kWarpsL = 16;
 constexpr int kThreadsL = 32 * kWarpsL;
 constexpr float kInvSqrtD = 0.08838834764831845f;
 constexpr float kSqrtHalfPi = 1.2533141373155003f;
-constexpr uint32_t kErrTimeout = 8u;
 constexpr int kWaitLimit = 1 << 22;
 constexpr float kNegBig = -1.0e30f;    // finite "minus infinity" (see tq_decode_mma.cu)
 constexpr int kSmemLimit = 232448;     // opt-in shared memory per block
@@ -211,16 +210,29 @@ struct Geo {
   static constexpr int R0 = region_bytes(KBH, VBH);
   static constexpr int R1 = region_bytes(KBL, VBL);
   static constexpr int TABLES = R0 + R1;
-  static constexpr int EXTRA = kWarpsL * (8 * 16 * 2 + 16 * 3 + 16 * 3) + 256;   // ptile, bars, slots, align
-  static constexpr int STAGES = TABLES + kWarpsL * 3 * STAGE + EXTRA <= kSmemLimit ? 3 : 2;
-  static constexpr int RING = TABLES;                                              // offset of the rings
-  static constexpr int BARS = RING + kWarpsL * STAGES * STAGE;
-  static constexpr int SLOTS = BARS + kWarpsL * STAGES * 8;
-  static constexpr int PTILE = (SLOTS + kWarpsL * STAGES * 16 + 15) & ~15;
-  static constexpr int SMEM = PTILE + kWarpsL * 8 * 16 * 2;
-  static_assert(STAGE % 16 == 0 && RING % 128 == 0, "bulk copy alignment");
+  // per warp: ring, then (in the extras block) S barriers, S slots, a 256-byte P tile
+  __host__ __device__ static constexpr int extras(int st) { return kWarpsL * (st * 8 + st * 16 + 256); }
+  // the tables start at a 64 KiB-aligned shared address; the gap below them
+  // takes whole warp rings, so at most one ring (or, when every ring fits in
+  // the gap, the rest of the gap) is lost to the alignment
+  __host__ __device__ static constexpr int rings_plus_gap(int st) {
+    return (kWarpsL + 1) * st * STAGE > 65536 ? (kWarpsL + 1) * st * STAGE : 65536;
+  }
+  __host__ __device__ static constexpr int need(int st) { return TABLES + rings_plus_gap(st) + extras(st) + 1024; }
+  static constexpr int STAGES = need(3) <= kSmemLimit ? 3 : 2;
+  static constexpr int RINGW = STAGES * STAGE;
+  static constexpr int SMEM = need(STAGES);
+  static_assert(STAGE % 16 == 0 && TABLES % 256 == 0, "bulk copy alignment");
   static_assert(SMEM <= kSmemLimit, "shared memory per block");
 };
+
+// Shared load at a full 32-bit shared address plus a constant offset.
+template <int OFF>
+__device__ __forceinline__ uint32_t lds_at(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1+%2];" : "=r"(v) : "r"(addr), "n"(OFF));
+  return v;
+}
 
 // ---------------------------------------------------------------------------
 // the kernel
@@ -233,6 +245,16 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
 
+  // ---- layout: tables at the first 64 KiB boundary, rings around them ------
+  const uint32_t base = smem_u32(smem);
+  const uint32_t tab = (base + 0xFFFFu) & ~0xFFFFu;
+  const int n_low = min(kWarpsL, static_cast<int>((tab - base) / Gm::RINGW));   // rings below the tables
+  const uint32_t ext = tab + Gm::TABLES + (kWarpsL - n_low) * Gm::RINGW;
+  if (ext + Gm::extras(S) > base + Gm::SMEM) {          // cannot happen with the sizes above
+    if (threadIdx.x == 0) atomicOr(a.tab.err, kErrLayout);
+    return;
+  }
+  auto at = [&](uint32_t addr) { return smem + (addr - base); };
   // ---- tables (once per CTA) ------------------------------------------------
   {
     constexpr int E0 = Gm::R0 / 256, E1 = Gm::R1 / 256;
@@ -244,14 +266,14 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
       const int b = region ? (which ? VBL : KBL) : (which ? VBH : KBH);
       const GroupBook& gb = (which ? a.vl : a.kl).g[region];
       const uint32_t v = e < lut_entries(b) ? lut_entry(gb, b, e) : 0u;
-      *reinterpret_cast<uint4*>(smem + (region ? Gm::R0 : 0) + e * 256 + which * 128 + quad * 16) =
+      *reinterpret_cast<uint4*>(at(tab + (region ? Gm::R0 : 0) + e * 256 + which * 128 + quad * 16)) =
           make_uint4(v, v, v, v);
     }
   }
-  unsigned char* ring = smem + Gm::RING + warp * S * Gm::STAGE;
-  unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem + Gm::BARS) + warp * S;
-  Slot* slots = reinterpret_cast<Slot*>(smem + Gm::SLOTS) + warp * S;
-  __half(*ptile)[16] = reinterpret_cast<__half(*)[16]>(smem + Gm::PTILE + warp * 8 * 16 * 2);
+  unsigned char* ring = at(warp < n_low ? base + warp * Gm::RINGW : tab + Gm::TABLES + (warp - n_low) * Gm::RINGW);
+  unsigned long long* bars = reinterpret_cast<unsigned long long*>(at(ext)) + warp * S;
+  Slot* slots = reinterpret_cast<Slot*>(at(ext + kWarpsL * S * 8)) + warp * S;
+  __half(*ptile)[16] = reinterpret_cast<__half(*)[16]>(at(ext + kWarpsL * S * 24 + warp * 256));
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(smem_u32(&bars[s]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -272,6 +294,8 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
 
   // ---- producer state (meaningful in lane 0) --------------------------------
   int p_item = 0, p_page = 0, p_npages = 0, p_b = 0, p_h = 0, p_chunk = 0;   // p_item -1: done
+  int p_pid = 0;                 // page id of (p_item, p_page), loaded one refill ahead
+  const int* p_row = a.block_table;
   auto issue = [&](int s) {      // lane 0: fill slot s with the next page of this warp's stream
     const uint32_t bar = smem_u32(&bars[s]);
     while (p_item >= 0 && p_page >= p_npages) {
@@ -290,6 +314,8 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
       p_item = it;
       p_page = 0;
       p_npages = (min(t0 + C, L) - t0 + kPage - 1) / kPage;
+      p_row = a.block_table + static_cast<long long>(p_b) * a.maxp + p_chunk * (C / kPage);
+      p_pid = p_row[0];
     }
     Slot& sl = slots[s];
     if (p_item < 0) {
@@ -300,8 +326,9 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
     }
     sl.item = p_item;
     sl.page = p_page;
-    const int page = a.block_table[static_cast<long long>(p_b) * a.maxp + p_chunk * (C / kPage) + p_page];
+    const int page = p_pid;
     ++p_page;
+    if (p_page < p_npages) p_pid = p_row[p_page];   // used by the next refill
     if (page < 0 || page >= a.num_pages) {
       atomicOr(a.tab.err, kErrPage);
       sl.valid = 0;
@@ -322,7 +349,11 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
   __syncwarp();
 
   // ---- consumer state ---------------------------------------------------------
-  const uint32_t lbk = static_cast<uint32_t>(lane) * 4u, lbv = lbk + 128u;
+  // prmt operand: byte 0 = lane offset (+128 for the V half), bytes 2-3 = the
+  // 64 KiB block of the table region; byte 1 comes from the code byte
+  constexpr int OFF1 = Gm::R0 & 0xFFFF;                      // region 1 offset inside its 64 KiB block
+  const uint32_t lbk0 = tab | (static_cast<uint32_t>(lane) * 4u), lbv0 = lbk0 + 128u;
+  const uint32_t lbk1 = lbk0 + (static_cast<uint32_t>(Gm::R0) & ~0xFFFFu), lbv1 = lbk1 + 128u;
   const float k1 = kInvSqrtD * a.scale_log2;
   const float k2 = kSqrtHalfPi / 128.0f * a.scale_log2;
   int cur = -1, c_b = 0, c_h = 0, c_chunk = 0, c_t0 = 0, c_t1 = 0;
@@ -428,13 +459,20 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
           const int j0 = 2 * (kk & 3), j1 = j0 + 1;
           const uint32_t* xa = kk < 4 ? xa0 : xa1;
           const uint32_t* xb = kk < 4 ? xb0 : xb1;
-          const unsigned char* tb = smem + (kk < 4 ? 0 : Gm::R0);
           const uint32_t s0 = 0x7604u | (static_cast<uint32_t>(j0 & 3) << 4);
           const uint32_t s1x = 0x7604u | (static_cast<uint32_t>(j1 & 3) << 4);
-          const uint32_t a0 = *reinterpret_cast<const uint32_t*>(tb + prmt(xa[j0 >> 2], lbk, s0));
-          const uint32_t a1 = *reinterpret_cast<const uint32_t*>(tb + prmt(xb[j0 >> 2], lbk, s0));
-          const uint32_t a2 = *reinterpret_cast<const uint32_t*>(tb + prmt(xa[j1 >> 2], lbk, s1x));
-          const uint32_t a3 = *reinterpret_cast<const uint32_t*>(tb + prmt(xb[j1 >> 2], lbk, s1x));
+          uint32_t a0, a1, a2, a3;
+          if (kk < 4) {
+            a0 = lds_at<0>(prmt(xa[j0 >> 2], lbk0, s0));
+            a1 = lds_at<0>(prmt(xb[j0 >> 2], lbk0, s0));
+            a2 = lds_at<0>(prmt(xa[j1 >> 2], lbk0, s1x));
+            a3 = lds_at<0>(prmt(xb[j1 >> 2], lbk0, s1x));
+          } else {
+            a0 = lds_at<OFF1>(prmt(xa[j0 >> 2], lbk1, s0));
+            a1 = lds_at<OFF1>(prmt(xb[j0 >> 2], lbk1, s0));
+            a2 = lds_at<OFF1>(prmt(xa[j1 >> 2], lbk1, s1x));
+            a3 = lds_at<OFF1>(prmt(xb[j1 >> 2], lbk1, s1x));
+          }
           mma16816(s1, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
         }
         if (QJL) {
@@ -461,7 +499,7 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
         lg[3] = vg8 ? fmaf(nkg8 * k1, s1[3], rkg8 * k2 * s2[3]) : kNegBig;
       }
       // ---- online softmax over this page (heads 2t, 2t+1) -------------------
-      float pr[4];
+      float pr[4], alpha[2];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         float mx = fmaxf(lg[c], lg[c + 2]);
@@ -469,15 +507,21 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
         const float m_new = fmaxf(m_run[c], mx);
-        const float alpha = exp2f(m_run[c] - m_new);
+        alpha[c] = exp2f(m_run[c] - m_new);
         pr[c] = exp2f(lg[c] - m_new);
         pr[c + 2] = exp2f(lg[c + 2] - m_new);
-        l_run[c] = fmaf(l_run[c], alpha, pr[c] + pr[c + 2]);
+        l_run[c] = fmaf(l_run[c], alpha[c], pr[c] + pr[c + 2]);
         m_run[c] = m_new;
+      }
+      // the running max rarely moves once a chunk is under way: rescale only
+      // when it moved for some head of the warp
+      if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-          acc[mt][c] *= alpha;
-          acc[mt][c + 2] *= alpha;
+          acc[mt][0] *= alpha[0];
+          acc[mt][2] *= alpha[0];
+          acc[mt][1] *= alpha[1];
+          acc[mt][3] *= alpha[1];
         }
       }
       // ---- P' = p * nv / sqrt(d) into the transposed shared tile -------------
@@ -506,10 +550,10 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
           const uint32_t sel = 0x7604u | (static_cast<uint32_t>(mt & 3) << 4);
-          const uint32_t a0 = *reinterpret_cast<const uint32_t*>(smem + prmt(mt < 4 ? hl0 : hh0, lbv, sel));
-          const uint32_t a1 = *reinterpret_cast<const uint32_t*>(smem + Gm::R0 + prmt(mt < 4 ? ll0 : lh0, lbv, sel));
-          const uint32_t a2 = *reinterpret_cast<const uint32_t*>(smem + prmt(mt < 4 ? hl1 : hh1, lbv, sel));
-          const uint32_t a3 = *reinterpret_cast<const uint32_t*>(smem + Gm::R0 + prmt(mt < 4 ? ll1 : lh1, lbv, sel));
+          const uint32_t a0 = lds_at<0>(prmt(mt < 4 ? hl0 : hh0, lbv0, sel));
+          const uint32_t a1 = lds_at<OFF1>(prmt(mt < 4 ? ll0 : lh0, lbv1, sel));
+          const uint32_t a2 = lds_at<0>(prmt(mt < 4 ? hl1 : hh1, lbv0, sel));
+          const uint32_t a3 = lds_at<OFF1>(prmt(mt < 4 ? ll1 : lh1, lbv1, sel));
           mma16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
         }
       }

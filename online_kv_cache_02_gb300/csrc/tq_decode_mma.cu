@@ -43,7 +43,6 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kStages = 3;
 constexpr float kInvSqrtD = 0.08838834764831845f;
 constexpr float kSqrtHalfPi = 1.2533141373155003f;
-constexpr uint32_t kErrTimeout = 8u;
 constexpr int kWaitLimit = 1 << 22;
 // Finite "minus infinity": exp2 of (sentinel - finite) is exactly 0, and an
 // all-empty chunk ends with max = sentinel, acc = 0, so its merge weight or

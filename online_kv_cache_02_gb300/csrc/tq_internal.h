@@ -21,6 +21,8 @@ constexpr float kPiScale = 16.0f;  // Pi is split into fp16 hi + lo after scalin
 constexpr uint32_t kErrPage = 1u;      // page id outside [0, num_pages)
 constexpr uint32_t kErrBlock = 2u;     // position beyond the block table
 constexpr uint32_t kErrSeqLen = 4u;    // sequence length beyond max_seq_len / block table
+constexpr uint32_t kErrTimeout = 8u;   // a bounded wait gave up
+constexpr uint32_t kErrLayout = 16u;   // shared-memory layout did not fit
 
 // One channel group's Lloyd-Max codebook in unit-variance units.
 struct GroupBook {

@@ -48,7 +48,6 @@ constexpr int kRows = 128;
 constexpr int kTmemCols = 256;            // y: columns 0..127, z: 128..255
 constexpr float kCodeGuard = 4e-6f;
 constexpr float kSignGuard = 2e-5f;
-constexpr uint32_t kErrTimeout = 8u;
 constexpr int kWaitLimit = 1 << 22;
 constexpr float kSqrtD = 11.313708498984761f;
 constexpr double kSqrtD64 = 11.313708498984760390;
