@@ -125,8 +125,9 @@ class ClockSampler:
                 "reasons": [n for b, n in REASONS.items() if self.reasons & b and n != "gpu_idle"]}
 
 
-def traffic_for(kernel_file, kernel):
-    """dram bytes per launch from a committed ncu capture, if the kernel source is unchanged since."""
+def traffic_for(kernel_file, kernel, workload):
+    """dram bytes per launch of `kernel` on `workload` from a committed ncu capture (profiles/ncu_traffic.json),
+    or None when there is none or the kernel source changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
@@ -136,7 +137,9 @@ def traffic_for(kernel_file, kernel):
         return None
     with open(os.path.join(ROOT, "online_kv_cache_02_gb300", "csrc", kernel_file), "rb") as f:
         sha = hashlib.sha256(f.read()).hexdigest()[:16]
-    return rec.get("bytes_per_launch") if rec.get("source_sha") == sha else None
+    if rec.get("source_sha") != sha:
+        return None
+    return rec.get("bytes_per_launch", {}).get(workload)
 
 
 # ---------------------------------------------------------------------------
@@ -187,7 +190,8 @@ class DecodeBench:
         self.out_h = torch.empty(B, Hq, 128, dtype=torch.float32).pin_memory()
         self.tokens = int((self.lens + 1).sum())
         self.bytes_step = self.tokens * H * wl.packed_bytes_per_token_head(w)
-        self.launches_per_step = 2 + 3
+        # append (one quantize launch for K and V) + qprep + partials + merge
+        self.launches_per_step = 4
 
     def _marshal(self, stream):
         """ctypes argument tuples of the per-step C calls, built once per stream (pointers are fixed)."""
@@ -350,11 +354,11 @@ def run_ours(args):
                    "packed_bytes_per_step": db.bytes_step, "hbm_fraction": round(value / world / peak, 4),
                    "l2": f"packed cache {db.bytes_step / 2**20:.0f} MiB > L2 129 MiB, no flush needed",
                    "parallelism": f"replicas x{world}, no collective"},
-        "roofline": {"kernel": "decode partials (per-chunk scoring + online softmax + value sums)", "bound": "hbm",
-                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+        "roofline": {"kernel": "lut_partials_kernel (split-K partials: scoring, online softmax, value sums)",
+                     "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": db.bytes_step, "avg_launch_ms": round(kern_ms, 5),
-                     "traffic": traffic_for("tq_decode.cu", "chunk_kernel")},
+                     "traffic": None if args.batch else traffic_for("tq_decode_lut.cu", "lut_partials_kernel", w.name)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": steps * db.launches_per_step,
         "clocks": sampler.result(),
@@ -376,15 +380,15 @@ def run_ours(args):
                         "random block-table permutation",
             "value": round(qb.vectors * world / (qstep * 1e-3), 1), "unit": "KV vectors/s", "ms_per_step": round(qstep, 4),
             "steps": qsteps,
-            "roofline": {"kernel": "quantize (K and V launches)", "bound": "hbm",
+            "roofline": {"kernel": "quantize_tc_kernel (K and V tiles in one launch)", "bound": "hbm",
                          "achieved": round(qbytes / (qstep * 1e-3) / 1e9, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(qbytes / (qstep * 1e-3) / 1e9 / peak, 4), "peak_source": peak_kind,
-                         "algorithmic_bytes_per_launch": qbytes // 2,
-                         "traffic": traffic_for("tq_quantize.cu", "quantize_kernel")},
+                         "algorithmic_bytes_per_launch": qbytes,
+                         "traffic": traffic_for("tq_quantize_tc.cu", "quantize_tc_kernel", "c2")},
             "refined": tq.tq_refine_counters(qb.ctx),
             "clocks": qs.result(),
         }
-        line["gpu_launches"] += 2 * qsteps
+        line["gpu_launches"] += qsteps
         qb.close()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_decode_sample(w, seconds=15.0)

@@ -223,10 +223,14 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
       sl[swz(p, j, m)] = to_f16(static_cast<float>(s[p * d + j] - static_cast<double>(from_f16(hi))));
     }
   std::vector<float> adf(static_cast<size_t>(m) * d * 2), sdf(static_cast<size_t>(m) * d * 2);
+  std::vector<float> wt(static_cast<size_t>(d) * (d + m));   // W = [Pi; S Pi], stored transposed
+  for (int r = 0; r < d; ++r)
+    for (int k = 0; k < d; ++k) wt[static_cast<size_t>(k) * (d + m) + r] = static_cast<float>(pi[r * d + k]);
   for (int p = 0; p < m; ++p)
     for (int k = 0; k < d; ++k) {
       double acc = 0.0;
       for (int i = 0; i < d; ++i) acc += s[p * d + i] * pi[i * d + k];   // (S Pi)[p][k]
+      wt[static_cast<size_t>(k) * (d + m) + d + p] = static_cast<float>(acc);
       const float hi = static_cast<float>(acc);
       adf[(p * d + k) * 2] = hi;
       adf[(p * d + k) * 2 + 1] = static_cast<float>(acc - static_cast<double>(hi));
@@ -246,7 +250,8 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
   size_t o_adf = align256(o_sl + sizeof(uint16_t) * d * m);
   size_t o_sdf = align256(o_adf + sizeof(float) * d * m * 2);
   size_t o_pidf = align256(o_sdf + sizeof(float) * d * m * 2);
-  size_t o_err = align256(o_pidf + sizeof(float) * d * d * 2);
+  size_t o_wt = align256(o_pidf + sizeof(float) * d * d * 2);
+  size_t o_err = align256(o_wt + sizeof(float) * d * (d + m));
   size_t o_cnt = align256(o_err + sizeof(uint32_t));
   size_t total = align256(o_cnt + 2 * sizeof(unsigned long long));
   void* blk = nullptr;
@@ -265,6 +270,7 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
   ctx->tab.a_df = reinterpret_cast<float*>(b + o_adf);
   ctx->tab.s_df = reinterpret_cast<float*>(b + o_sdf);
   ctx->tab.pi_df = reinterpret_cast<float*>(b + o_pidf);
+  ctx->tab.wt = reinterpret_cast<float*>(b + o_wt);
   ctx->tab.err = reinterpret_cast<uint32_t*>(b + o_err);
   ctx->tab.counters = reinterpret_cast<unsigned long long*>(b + o_cnt);
   bool ok = cudaMemcpy(ctx->tab.pit, pit.data(), sizeof(float) * d * d, cudaMemcpyHostToDevice) == cudaSuccess &&
@@ -279,6 +285,7 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
             cudaMemcpy(ctx->tab.pi_df, pidf.data(), sizeof(float) * d * d * 2, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemcpy(ctx->tab.a_df, adf.data(), sizeof(float) * d * m * 2, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemcpy(ctx->tab.s_df, sdf.data(), sizeof(float) * d * m * 2, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(ctx->tab.wt, wt.data(), sizeof(float) * d * (d + m), cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemset(b + o_err, 0, total - o_err) == cudaSuccess;
   if (!ok) { cudaFree(blk); delete ctx; cudaGetLastError(); return TQ_ERR_CUDA; }
   *out = ctx;

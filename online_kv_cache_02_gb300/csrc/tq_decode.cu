@@ -7,7 +7,7 @@
 // stage 2 (the residual's 1-bit sketch makes the inner product unbiased).
 //
 // Three launches on one stream:
-//   qprep  : q~ = Pi q, u = S q~ (fp32) per query head
+//   qprep  : q~ = Pi q, u = S q~ = (S Pi) q (fp32) per query head
 //   chunk  : per (chunk, KV head, sequence): every cached key t of the chunk is
 //            scored as (n_t/sqrt(d)) <q~, c[code_t]> + sqrt(pi/2)/m rho_t
 //            <u, +-1_t>, an online (flash-style) softmax keeps (max, sum,
@@ -45,43 +45,46 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// q~ = Pi q and u = S q~ for 16 query heads per block, Pi^T and S^T read once per block.
-constexpr int kQB = 16;
+// [q~; u] = W q with W = [Pi; S Pi] (fp32, built once at create time): a
+// block takes 16 query heads x 64 outputs; its 32 KB slice of W^T arrives in
+// one round of independent 16-byte loads, then thread t computes output t%64
+// for heads 4(t/64) .. 4(t/64)+3 from shared memory.
+constexpr int kQP = 16;
+constexpr int kQO = 64;
+constexpr int kQThreads = 256;
 
-__global__ void __launch_bounds__(kThreads) qprep_kernel(DecodeArgs a) {
-  __shared__ float qs[kQB][kD];
-  __shared__ float qt[kQB][kD];
-  const long long r0 = static_cast<long long>(blockIdx.x) * kQB;
+__global__ void __launch_bounds__(kQThreads) qprep_kernel(DecodeArgs a) {
+  __shared__ __align__(16) float ws[kD][kQO];
+  __shared__ float qs[kQP][kD];
+  const int nout = kD + a.m;
+  const long long r0 = static_cast<long long>(blockIdx.x) * kQP;
+  const int c0 = blockIdx.y * kQO;
   const long long nq = static_cast<long long>(a.B) * a.Hq;
-  const int i = threadIdx.x;
-  if (blockIdx.x == 0 && i < 2 && a.sched) a.sched[i] = 0;
-  for (int r = 0; r < kQB; ++r) qs[r][i] = r0 + r < nq ? load_q(a.q, a.f32, (r0 + r) * kD + i) : 0.0f;
-  __syncthreads();
-  float acc[kQB];
+  const int tid = threadIdx.x, o = tid & (kQO - 1), h0 = 4 * (tid >> 6);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && tid < 2 && a.sched) a.sched[tid] = 0;   // partials work counters
 #pragma unroll
-  for (int r = 0; r < kQB; ++r) acc[r] = 0.0f;
-#pragma unroll 4
-  for (int k = 0; k < kD; ++k) {
-    const float p = a.tab.pit[k * kD + i];
-#pragma unroll
-    for (int r = 0; r < kQB; ++r) acc[r] = fmaf(p, qs[r][k], acc[r]);
+  for (int it = 0; it < kD * kQO / 4 / kQThreads; ++it) {
+    const int v = tid + it * kQThreads, k = v / (kQO / 4), c = 4 * (v % (kQO / 4));
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c0 + c < nout) x = *reinterpret_cast<const float4*>(a.tab.wt + static_cast<long long>(k) * nout + c0 + c);
+    *reinterpret_cast<float4*>(&ws[k][c]) = x;
   }
-#pragma unroll
-  for (int r = 0; r < kQB; ++r) qt[r][i] = acc[r];
+  for (int idx = tid; idx < kQP * kD; idx += kQThreads) {
+    const int r = idx / kD, c = idx % kD;
+    qs[r][c] = r0 + r < nq ? load_q(a.q, a.f32, (r0 + r) * kD + c) : 0.0f;
+  }
   __syncthreads();
-  for (int r = 0; r < kQB; ++r)
-    if (r0 + r < nq) a.qprep[(r0 + r) * (kD + a.m) + i] = qt[r][i];
-  for (int p = i; p < a.m; p += kThreads) {
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+  for (int k = 0; k < kD; ++k) {
+    const float w = ws[k][o];
 #pragma unroll
-    for (int r = 0; r < kQB; ++r) acc[r] = 0.0f;
-#pragma unroll 4
-    for (int j = 0; j < kD; ++j) {
-      const float sv = a.tab.st[j * a.m + p];
+    for (int r = 0; r < 4; ++r) acc[r] = fmaf(w, qs[h0 + r][k], acc[r]);
+  }
+  if (c0 + o < nout) {
 #pragma unroll
-      for (int r = 0; r < kQB; ++r) acc[r] = fmaf(sv, qt[r][j], acc[r]);
-    }
-    for (int r = 0; r < kQB; ++r)
-      if (r0 + r < nq) a.qprep[(r0 + r) * (kD + a.m) + kD + p] = acc[r];
+    for (int r = 0; r < 4; ++r)
+      if (r0 + h0 + r < nq) a.qprep[(r0 + h0 + r) * nout + c0 + o] = acc[r];
   }
 }
 
@@ -286,40 +289,77 @@ __global__ void __launch_bounds__(kThreads) chunk_kernel(DecodeArgs a) {
 
 // Log-sum-exp merge of the chunk partials and o = Pi^T (acc / l): one block
 // per (sequence, KV head) for its G query heads, Pi read once per block.
-__global__ void __launch_bounds__(kThreads) merge_kernel(DecodeArgs a) {
-  __shared__ float os[kMaxGroup][kD];
-  const long long r0 = static_cast<long long>(blockIdx.x) * a.G;   // first query head (b*Hq + h*G)
-  const int j = threadIdx.x;
-  // chunks that start at or past the sequence end hold no partial
-  int L = a.seq_lens[blockIdx.x / a.H] + a.len_add;
+// One block per query head: log-sum-exp merge of its chunk partials, then
+// o = Pi^T (acc / sum).  Four groups of 128 threads split the chunks (two
+// accumulation chains each) and then the rows of Pi.  Chunks that start at or
+// past the sequence end hold no partial and are skipped.
+template <int NT>
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
+  v = is_max ? warp_max(v) : warp_sum(v);
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int k = 1; k < NT / 32; ++k) r = is_max ? fmaxf(r, red[k]) : r + red[k];
+  return r;
+}
+
+constexpr int kMGroups = 4;
+constexpr int kMThreads = kMGroups * kD;
+
+__global__ void __launch_bounds__(kMThreads) merge_kernel(DecodeArgs a) {
+  __shared__ float wsh[kMThreads];
+  __shared__ float part[kMGroups][kD];
+  __shared__ float os[kD];
+  __shared__ float red[kMThreads / 32];
+  const long long row = blockIdx.x;                 // b * Hq + query head
+  const int tid = threadIdx.x, j = tid & (kD - 1), grp = tid >> 7;
+  int L = a.seq_lens[row / a.Hq] + a.len_add;
   L = L < 0 ? 0 : L;
   L = L > a.max_seq_len ? a.max_seq_len : L;
   L = L > a.maxp * kPage ? a.maxp * kPage : L;
   const int nc = min(a.nchunks, (L + a.chunk - 1) / a.chunk);
-  for (int r = 0; r < a.G; ++r) {
-    const float* P = a.part + (r0 + r) * a.nchunks * (kD + 2);
-    float M = -INFINITY;
-    for (int c = 0; c < nc; ++c) M = fmaxf(M, P[c * (kD + 2)]);
-    float l = 0.0f, A = 0.0f;
-#pragma unroll 4
-    for (int c = 0; c < nc; ++c) {
-      const float w = exp2f(P[c * (kD + 2)] - M);
-      l = fmaf(w, P[c * (kD + 2) + 1], l);
-      A = fmaf(w, P[c * (kD + 2) + 2 + j], A);
+  const float* P = a.part + row * a.nchunks * (kD + 2);
+  float M = -INFINITY;
+  for (int c = tid; c < nc; c += kMThreads) M = fmaxf(M, P[static_cast<long long>(c) * (kD + 2)]);
+  M = block_reduce<kMThreads>(M, true, red);
+  float lpart = 0.0f, A0 = 0.0f, A1 = 0.0f;
+  for (int c0 = 0; c0 < nc; c0 += kMThreads) {
+    const int c = c0 + tid;
+    float w = 0.0f;
+    if (c < nc) {
+      const float* pc = P + static_cast<long long>(c) * (kD + 2);
+      w = exp2f(pc[0] - M);
+      lpart = fmaf(w, pc[1], lpart);
     }
-    os[r][j] = l > 0.0f ? A / l : 0.0f;
+    __syncthreads();
+    wsh[tid] = w;
+    __syncthreads();
+    const int n = min(kMThreads, nc - c0);
+    int cc = grp;
+    for (; cc + kMGroups < n; cc += 2 * kMGroups) {
+      A0 = fmaf(wsh[cc], P[static_cast<long long>(c0 + cc) * (kD + 2) + 2 + j], A0);
+      A1 = fmaf(wsh[cc + kMGroups], P[static_cast<long long>(c0 + cc + kMGroups) * (kD + 2) + 2 + j], A1);
+    }
+    if (cc < n) A0 = fmaf(wsh[cc], P[static_cast<long long>(c0 + cc) * (kD + 2) + 2 + j], A0);
   }
+  const float l = block_reduce<kMThreads>(lpart, false, red);
+  part[grp][j] = A0 + A1;
   __syncthreads();
-  float o[kMaxGroup];
-#pragma unroll
-  for (int r = 0; r < kMaxGroup; ++r) o[r] = 0.0f;
-#pragma unroll 4
-  for (int i = 0; i < kD; ++i) {
-    const float p = a.tab.pi[i * kD + j];
-#pragma unroll
-    for (int r = 0; r < kMaxGroup; ++r) o[r] = fmaf(p, os[r][i], o[r]);
+  if (grp == 0) os[j] = l > 0.0f ? ((part[0][j] + part[1][j]) + (part[2][j] + part[3][j])) / l : 0.0f;
+  __syncthreads();
+  float o0 = 0.f, o1 = 0.f;                         // rows grp*32 .. grp*32+31 of Pi
+  const int i0 = grp * (kD / kMGroups);
+#pragma unroll 8
+  for (int i = 0; i < kD / kMGroups; i += 2) {
+    o0 = fmaf(a.tab.pi[(i0 + i) * kD + j], os[i0 + i], o0);
+    o1 = fmaf(a.tab.pi[(i0 + i + 1) * kD + j], os[i0 + i + 1], o1);
   }
-  for (int r = 0; r < a.G; ++r) a.out[(r0 + r) * kD + j] = o[r];
+  part[grp][j] = o0 + o1;
+  __syncthreads();
+  if (grp == 0) a.out[row * kD + j] = (part[0][j] + part[1][j]) + (part[2][j] + part[3][j]);
 }
 
 template <int G>
@@ -334,7 +374,9 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
 cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
   if (stages & TQ_STAGE_QPREP) {
-    qprep_kernel<<<(a.B * a.Hq + kQB - 1) / kQB, kThreads, 0, s>>>(a);
+    const dim3 grid(static_cast<unsigned>((static_cast<long long>(a.B) * a.Hq + kQP - 1) / kQP),
+                    static_cast<unsigned>((kD + a.m + kQO - 1) / kQO));
+    qprep_kernel<<<grid, kQThreads, 0, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -358,7 +400,7 @@ cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
     }
   }
   if (stages & TQ_STAGE_MERGE) {
-    merge_kernel<<<a.B * a.H, kThreads, 0, s>>>(a);
+    merge_kernel<<<static_cast<unsigned>(static_cast<long long>(a.B) * a.Hq), kMThreads, 0, s>>>(a);
     e = cudaGetLastError();
   }
   return e;

@@ -72,6 +72,7 @@ struct DeviceTables {
   float* a_df;              // (S Pi) as double-float pairs [m][128][2]
   float* s_df;              // S as double-float pairs [m][128][2]
   float* pi_df;             // Pi as double-float pairs [128][128][2]
+  float* wt;                // W^T, fp32 [d][d + m]: W = [Pi; S Pi], wt[k*(d+m) + r] = W[r][k]
 };
 
 struct QuantizeArgs {
