@@ -45,6 +45,8 @@ def parse(argv=None):
     ap.add_argument("--config", default="c3", choices=["c3", "c4", "c5"])
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     ap.add_argument("--no-quantize", action="store_true", help="skip the c2 quantize measurement")
+    ap.add_argument("--only", default="", choices=["", "quantize"],
+                    help="quantize: run the c2 quantize measurement alone (profiling; --batch scales it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args(argv)
 
@@ -339,6 +341,33 @@ def l2_flusher(torch, bytes_step):
                                    f"each step timed alone")
 
 
+def quantize_measure(torch, tq, qw, stream, qsteps, warmup, dist, peak, peak_kind, world):
+    """The quantize-append workload (c2 shape): one launch per step quantizes every K and V vector."""
+    qb = QuantizeBench(qw, torch, tq)
+    qs = ClockSampler(torch)
+    with qs:
+        qms = timed(torch, stream, lambda i=None: qb.step(stream), qsteps, warmup, dist)
+    qstep = qms / qsteps
+    qbytes = qb.bytes_in + qb.bytes_out
+    full = qw == wl.WORKLOADS["c2"]
+    rec = {
+        "workload": f"{qw.name}: quantize-append {qw.batch} seq x {qw.kv_heads} KV heads x {qw.seq_len} tokens bf16, "
+                    f"K {qw.k_bits} bits + QJL m={qw.m} / V {qw.v_bits} bits, random block-table permutation",
+        "value": round(qb.vectors * world / (qstep * 1e-3), 1), "unit": "KV vectors/s", "ms_per_step": round(qstep, 4),
+        "steps": qsteps,
+        "l2": f"{qb.bytes_in / 2**20:.0f} MiB of bf16 input per step > 2x L2: no flush",
+        "roofline": {"kernel": "quantize_tc_kernel (K and V tiles in one launch)", "bound": "hbm",
+                     "achieved": round(qbytes / (qstep * 1e-3) / 1e9, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(qbytes / (qstep * 1e-3) / 1e9 / peak, 4), "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": qbytes,
+                     "traffic": traffic_for("tq_quantize_tc.cu", "quantize_tc_kernel", "c2") if full else None},
+        "refined": tq.tq_refine_counters(qb.ctx),
+        "clocks": qs.result(),
+    }
+    qb.close()
+    return rec
+
+
 def run_ours(args):
     import torch
     from online_kv_cache_02_gb300 import tq
@@ -355,6 +384,16 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     peak, peak_kind = peaks()
 
+    if args.only == "quantize":
+        qw = wl.WORKLOADS["c2"].scaled(batch=args.batch) if args.batch else wl.WORKLOADS["c2"]
+        line = {"metric": "KV vectors quantized/s (quantize only)"}
+        line.update(quantize_measure(torch, tq, qw, stream, args.steps, max(3, args.warmup), dist, peak, peak_kind,
+                                     world))
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
     w = wl.WORKLOADS[args.config]
     if args.batch:
         w = w.scaled(batch=args.batch)
@@ -403,28 +442,9 @@ def run_ours(args):
     del db
     torch.cuda.empty_cache()
     if not args.no_quantize:
-        qb = QuantizeBench(wl.WORKLOADS["c2"], torch, tq)
-        qsteps = max(3, min(steps, 20))
-        qs = ClockSampler(torch)
-        with qs:
-            qms = timed(torch, stream, lambda i=None: qb.step(stream), qsteps, warmup, dist)
-        qstep = qms / qsteps
-        qbytes = qb.bytes_in + qb.bytes_out
-        line["quantize"] = {
-            "workload": "c2: quantize-append 32 seq x 8 KV heads x 4096 tokens bf16, 3-bit K + QJL m=128 / 3-bit V, "
-                        "random block-table permutation",
-            "value": round(qb.vectors * world / (qstep * 1e-3), 1), "unit": "KV vectors/s", "ms_per_step": round(qstep, 4),
-            "steps": qsteps,
-            "roofline": {"kernel": "quantize_tc_kernel (K and V tiles in one launch)", "bound": "hbm",
-                         "achieved": round(qbytes / (qstep * 1e-3) / 1e9, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(qbytes / (qstep * 1e-3) / 1e9 / peak, 4), "peak_source": peak_kind,
-                         "algorithmic_bytes_per_launch": qbytes,
-                         "traffic": traffic_for("tq_quantize_tc.cu", "quantize_tc_kernel", "c2")},
-            "refined": tq.tq_refine_counters(qb.ctx),
-            "clocks": qs.result(),
-        }
-        line["gpu_launches"] += qsteps
-        qb.close()
+        line["quantize"] = quantize_measure(torch, tq, wl.WORKLOADS["c2"], stream, max(3, min(steps, 20)), warmup,
+                                            dist, peak, peak_kind, world)
+        line["gpu_launches"] += line["quantize"]["steps"]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_decode_sample(w, seconds=15.0)
     if rank == 0:

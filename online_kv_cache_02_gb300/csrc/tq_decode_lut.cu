@@ -594,8 +594,9 @@ cudaError_t launch_lut(const DecodeArgs& a, int items, cudaStream_t s) {
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int need = (items + kWarpsL - 1) / kWarpsL;
-  const int grid = need < sms ? (need > 0 ? need : 1) : sms;
+  // one CTA per SM (fewer only when there are fewer chunks than SMs): a warp
+  // without a chunk exits at once, and every SM's copy engines are in use
+  const int grid = items < sms ? (items > 0 ? items : 1) : sms;
   lut_partials_kernel<KBH, KBL, VBH, VBL, QJL><<<grid, kThreadsL, Gm::SMEM, s>>>(a, items);
   return cudaGetLastError();
 }
