@@ -45,6 +45,7 @@ namespace {
 
 constexpr int kWarpsL = 16;
 constexpr int kThreadsL = 32 * kWarpsL;
+constexpr int kMaxStagesL = 4;         // ring depth per warp: the largest <= this that fits
 constexpr float kInvSqrtD = 0.08838834764831845f;
 constexpr float kSqrtHalfPi = 1.2533141373155003f;
 constexpr int kWaitLimit = 1 << 22;
@@ -101,6 +102,13 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 2^x (ex2.approx.ftz: about 2 ulp; the finite -1e30 sentinel gives exactly 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ uint32_t f16bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) { return f16bits(lo) | (f16bits(hi) << 16); }
@@ -219,7 +227,9 @@ struct Geo {
     return (kWarpsL + 1) * st * STAGE > 65536 ? (kWarpsL + 1) * st * STAGE : 65536;
   }
   __host__ __device__ static constexpr int need(int st) { return TABLES + rings_plus_gap(st) + extras(st) + 1024; }
-  static constexpr int STAGES = need(3) <= kSmemLimit ? 3 : 2;
+  static constexpr int STAGES = need(kMaxStagesL) <= kSmemLimit ? kMaxStagesL
+                                : need(kMaxStagesL - 1) <= kSmemLimit ? kMaxStagesL - 1
+                                : need(3) <= kSmemLimit ? 3 : 2;
   static constexpr int RINGW = STAGES * STAGE;
   static constexpr int SMEM = need(STAGES);
   static_assert(STAGE % 16 == 0 && TABLES % 256 == 0, "bulk copy alignment");
@@ -328,21 +338,25 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
     sl.page = p_page;
     const int page = p_pid;
     ++p_page;
-    if (p_page < p_npages) p_pid = p_row[p_page];   // used by the next refill
     if (page < 0 || page >= a.num_pages) {
       atomicOr(a.tab.err, kErrPage);
       sl.valid = 0;
       mbar_arrive(bar);
-      return;
+    } else {
+      sl.valid = 1;
+      unsigned char* dst = ring + s * Gm::STAGE;
+      fence_proxy_async();
+      mbar_arrive_tx(bar, Gm::STAGE);
+      bulk_g2s(smem_u32(dst),
+               a.kc + static_cast<long long>(page) * a.k_page_bytes + static_cast<long long>(p_h) * Gm::KBB, Gm::KBB,
+               bar);
+      bulk_g2s(smem_u32(dst + Gm::KBB),
+               a.vc + static_cast<long long>(page) * a.v_page_bytes + static_cast<long long>(p_h) * Gm::VBB, Gm::VBB,
+               bar);
     }
-    sl.valid = 1;
-    unsigned char* dst = ring + s * Gm::STAGE;
-    fence_proxy_async();
-    mbar_arrive_tx(bar, Gm::STAGE);
-    bulk_g2s(smem_u32(dst), a.kc + static_cast<long long>(page) * a.k_page_bytes + static_cast<long long>(p_h) * Gm::KBB,
-             Gm::KBB, bar);
-    bulk_g2s(smem_u32(dst + Gm::KBB),
-             a.vc + static_cast<long long>(page) * a.v_page_bytes + static_cast<long long>(p_h) * Gm::VBB, Gm::VBB, bar);
+    // the next page id, loaded after the fence and arrive above (which wait for
+    // this thread's outstanding memory operations) and used one refill later
+    if (p_page < p_npages) p_pid = p_row[p_page];
   };
   if (lane == 0)
     for (int s = 0; s < S; ++s) issue(s);
@@ -507,9 +521,9 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
         const float m_new = fmaxf(m_run[c], mx);
-        alpha[c] = exp2f(m_run[c] - m_new);
-        pr[c] = exp2f(lg[c] - m_new);
-        pr[c + 2] = exp2f(lg[c + 2] - m_new);
+        alpha[c] = fast_exp2(m_run[c] - m_new);
+        pr[c] = fast_exp2(lg[c] - m_new);
+        pr[c + 2] = fast_exp2(lg[c + 2] - m_new);
         l_run[c] = fmaf(l_run[c], alpha[c], pr[c] + pr[c + 2]);
         m_run[c] = m_new;
       }
