@@ -357,7 +357,8 @@ int nchunks_for(int max_seq_len, int chunk) { return max_seq_len <= 0 ? 1 : (max
 
 size_t ws_bytes(int B, int Hq, int d, int m, int nch) {
   return align256(sizeof(float) * static_cast<size_t>(B) * Hq * (d + m)) +
-         align256(sizeof(float) * static_cast<size_t>(B) * Hq * nch * (d + 2)) + 256;   // + work counters
+         align256(sizeof(float) * static_cast<size_t>(B) * Hq * nch * (d + 2)) +
+         align256(sizeof(uint32_t) * static_cast<size_t>(B) * Hq * 128) + 256;   // + query fragments, work counters
 }
 }  // namespace
 
@@ -439,8 +440,10 @@ tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batc
   char* w = static_cast<char*>(workspace);
   a.qprep = reinterpret_cast<float*>(w);
   a.part = reinterpret_cast<float*>(w + align256(sizeof(float) * static_cast<size_t>(batch) * Hq * (d + m)));
-  a.sched = reinterpret_cast<int*>(w + align256(sizeof(float) * static_cast<size_t>(batch) * Hq * (d + m)) +
-                                   align256(sizeof(float) * static_cast<size_t>(batch) * Hq * nch * (d + 2)));
+  const size_t o_frag = align256(sizeof(float) * static_cast<size_t>(batch) * Hq * (d + m)) +
+                        align256(sizeof(float) * static_cast<size_t>(batch) * Hq * nch * (d + 2));
+  a.qfrag = reinterpret_cast<uint32_t*>(w + o_frag);
+  a.sched = reinterpret_cast<int*>(w + o_frag + align256(sizeof(uint32_t) * static_cast<size_t>(batch) * Hq * 128));
   a.out = out;
   return launch_decode(a, stages, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }

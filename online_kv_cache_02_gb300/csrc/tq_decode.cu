@@ -86,6 +86,33 @@ __global__ void __launch_bounds__(kQThreads) qprep_kernel(DecodeArgs a) {
     for (int r = 0; r < 4; ++r)
       if (r0 + h0 + r < nq) a.qprep[(r0 + h0 + r) * nout + c0 + o] = acc[r];
   }
+  if (!a.qfrag || a.m != kD) return;
+  // fp16 fragments of the persistent partials kernel: this block's 64 outputs
+  // hold, per head, 32 of its 128 words (slice 0/1: key pairs of channel group
+  // 0/1 for every lane t; slice 2/3: u pairs of lanes t = 0,1 / 2,3)
+  __shared__ __half hs[kQP][kQO];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) hs[h0 + r][o] = __float2half_rn(acc[r]);
+  __syncthreads();
+  const int y = blockIdx.y;
+  for (int idx = tid; idx < kQP * 32; idx += kQThreads) {
+    const int h = idx >> 5, k = idx & 31;
+    if (r0 + h >= nq) continue;
+    int word, lo, hi;                        // word index in the head's 128, local offsets of its halves
+    if (y < 2) {
+      const int t = k >> 3, kk = 4 * y + ((k >> 1) & 3), e = k & 1;
+      word = 32 * t + 2 * kk + e;
+      lo = 16 * t + k_pair_channel(a.kl.g[y].bits, 2 * (kk & 3) + e);
+      hi = lo + 1;
+    } else {
+      const int t = 2 * (y - 2) + (k >> 4), p = k & 15;
+      word = 32 * t + 16 + p;
+      lo = 32 * t + p - 64 * (y - 2);
+      hi = lo + 16;
+    }
+    a.qfrag[(r0 + h) * 128 + word] = static_cast<uint32_t>(__half_as_ushort(hs[h][lo])) |
+                                     (static_cast<uint32_t>(__half_as_ushort(hs[h][hi])) << 16);
+  }
 }
 
 // Code of channel j from a vector's code words (the stored format of tq.h).

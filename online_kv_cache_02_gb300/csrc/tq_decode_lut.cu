@@ -161,8 +161,7 @@ __device__ __forceinline__ void k_slice(const uint32_t* grp, int t, uint32_t (&x
     x[1] = (w >> 4) & 0x0F0F0F0Fu;
   }
 }
-// Channel (within the slice) of the low half of key pair j.
-__host__ __device__ constexpr int k_pair_channel(int b, int j) { return b == 2 ? (j < 4 ? 4 * j : 4 * (j - 4) + 2) : 2 * j; }
+// (k_pair_channel in tq_internal.h gives the channel of the low half of pair j.)
 
 // Codes of channels 8g..8g+7 of one value vector (group-relative words).
 template <int B>
@@ -405,19 +404,21 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
     c_b = bh / a.H;
     c_t0 = c_chunk * C;
     c_t1 = min(c_t0 + C, seq_len(c_b));
-    const bool head_ok = g < a.G;
-    const float* qrow = a.qprep + (static_cast<long long>(c_b) * a.Hq + c_h * a.G + (head_ok ? g : 0)) * (kD + a.m);
+    // the query fragments, packed by qprep in this thread's order: 8 x 16 B
+    if (g < a.G) {
+      const uint4* fp = reinterpret_cast<const uint4*>(
+          a.qfrag + ((static_cast<long long>(c_b) * a.Hq + c_h * a.G + g) * 4 + t) * 32);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int grp = kk >> 2, j = 2 * (kk & 3) + e;
-        const int ch = 64 * grp + 16 * t + k_pair_channel(grp ? KBL : KBH, j);
-        qf[2 * kk + e] = head_ok ? pack_h2(qrow[ch], qrow[ch + 1]) : 0u;
+      for (int v = 0; v < 4; ++v) {
+        const uint4 x = fp[v], y = fp[4 + v];
+        qf[4 * v] = x.x, qf[4 * v + 1] = x.y, qf[4 * v + 2] = x.z, qf[4 * v + 3] = x.w;
+        uf[4 * v] = QJL ? y.x : 0u, uf[4 * v + 1] = QJL ? y.y : 0u;
+        uf[4 * v + 2] = QJL ? y.z : 0u, uf[4 * v + 3] = QJL ? y.w : 0u;
       }
-    }
+    } else {
 #pragma unroll
-    for (int p = 0; p < 16; ++p) uf[p] = (QJL && head_ok) ? pack_h2(qrow[kD + 32 * t + p], qrow[kD + 32 * t + p + 16]) : 0u;
+      for (int v = 0; v < 16; ++v) qf[v] = uf[v] = 0u;
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
@@ -638,7 +639,7 @@ int lut_decode_slots(const KindLayout& kl, const KindLayout& vl, int m, int G) {
 }
 
 bool launch_partials_lut(const DecodeArgs& a, cudaStream_t s, cudaError_t* err) {
-  if (!lut_decode_slots(a.kl, a.vl, a.m, a.G) || !a.sched) return false;
+  if (!lut_decode_slots(a.kl, a.vl, a.m, a.G) || !a.sched || !a.qfrag) return false;
   if ((reinterpret_cast<uintptr_t>(a.kc) | reinterpret_cast<uintptr_t>(a.vc)) & 15) return false;
   if ((a.k_page_bytes | a.v_page_bytes) & 15) return false;
   const long long items = static_cast<long long>(a.B) * a.H * a.nchunks;

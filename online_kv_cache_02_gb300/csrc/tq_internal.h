@@ -47,6 +47,14 @@ struct KindLayout {
   int qjl;               // keys with QJL signs + residual norm
 };
 
+// Key channel pairing of the persistent decode kernel: thread slice t covers
+// channels 16t..16t+15 of a channel group; pair j (0..7) holds the channel
+// below plus the next one (see tq_decode_lut.cu).  Shared with qprep, which
+// writes the query fragments in this order.
+__host__ __device__ constexpr int k_pair_channel(int b, int j) {
+  return b == 2 ? (j < 4 ? 4 * j : 4 * (j - 4) + 2) : 2 * j;
+}
+
 // Host functions (tq_host.cpp).
 void gaussian_fill(uint64_t seed, uint64_t stream, size_t n, double* out);
 void rotation_fill(int d, uint64_t seed, double* pi);
@@ -110,6 +118,8 @@ struct DecodeArgs {
   float* part;           // [B][Hq][nchunks][d + 2]
   float* out;            // [B][Hq][d]
   int* sched;            // [2] work counter and finished-warp count of the persistent kernel (zeroed by qprep)
+  uint32_t* qfrag;       // [B][Hq][4][32] fp16 pairs in the persistent kernel's fragment order (m = 128 only):
+                         // for lane t%4 of a KV-head warp, 16 words of q~ (key pairs) then 16 of u
 };
 
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
