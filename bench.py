@@ -186,7 +186,9 @@ class DecodeBench:
         self.start = torch.from_numpy(self.lens.astype(np.int32)).to(dev)
         self.lens1 = torch.from_numpy((self.lens + 1).astype(np.int32)).to(dev)
         self.max_len = int(self.lens.max()) + 1
-        self.ws_n = tq.tq_workspace_size(self.ctx, B, Hq, self.max_len, w.chunk)
+        # split-K chunk: the workload's own, else the library's choice for the actual total length
+        self.chunk = w.chunk or tq.tq_decode_chunk(self.ctx, B, Hq, H, int((self.lens + 1).sum()), self.max_len)
+        self.ws_n = tq.tq_workspace_size(self.ctx, B, Hq, self.max_len, self.chunk)
         self.ws = torch.empty(self.ws_n, dtype=torch.uint8, device=dev)
         self.out = torch.empty(B, Hq, 128, dtype=torch.float32, device=dev)
         self.out_h = torch.empty(B, Hq, 128, dtype=torch.float32).pin_memory()
@@ -205,7 +207,7 @@ class DecodeBench:
                  self.vc.data_ptr(), sp)
         dec = [self.ctx, self.q.data_ptr(), tq.TQ_BF16, w.batch, w.q_heads, w.kv_heads, self.lens1.data_ptr(),
                self.max_len, self.bt_d.data_ptr(), self.pps, self.num_pages, self.kc.data_ptr(), self.vc.data_ptr(),
-               w.chunk, ctypes.c_float(1.0 / math.sqrt(128)), self.out.data_ptr(), self.ws.data_ptr(), self.ws_n]
+               self.chunk, ctypes.c_float(1.0 / math.sqrt(128)), self.out.data_ptr(), self.ws.data_ptr(), self.ws_n]
         stages = {st: tuple(dec + [st, sp]) for st in (tq.TQ_STAGE_QPREP, tq.TQ_STAGE_PARTIALS, tq.TQ_STAGE_MERGE,
                                                        tq.TQ_STAGE_ALL)}
         self._args = (stream, quant, stages)
@@ -243,7 +245,7 @@ class DecodeBench:
         self.vnew.copy_(self.vnew_h, non_blocking=True)
         self.q.copy_(self.q_h, non_blocking=True)
         tq.tq_append_decode(self.ctx, self.knew, self.vnew, self.q, tq.TQ_BF16, w.batch, w.q_heads, w.kv_heads,
-                            self.start, self.max_len, self.bt_d, self.pps, self.num_pages, self.kc, self.vc, w.chunk,
+                            self.start, self.max_len, self.bt_d, self.pps, self.num_pages, self.kc, self.vc, self.chunk,
                             1.0 / math.sqrt(128), self.out, self.ws, self.ws_n, stream)
         self.out_h.copy_(self.out, non_blocking=True)
 
@@ -425,6 +427,7 @@ def run_ours(args):
         "config": {"workload": f"{w.name}: decode step = append 1 token + attention, batch {w.batch}, "
                                f"{w.q_heads}/{w.kv_heads} heads, head_dim 128, context {int(db.lens.max())}+1, "
                                f"K {w.k_bits} bits + QJL m={w.m}, V {w.v_bits} bits",
+                   "split_k_chunk_tokens": db.chunk,
                    "packed_bytes_per_step": db.bytes_step, "hbm_fraction": round(value / world / peak, 4),
                    "l2": l2_note,
                    "parallelism": f"replicas x{world}, no collective"},

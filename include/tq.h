@@ -129,6 +129,17 @@ tq_status tq_quantize(const tq_ctx* ctx, const void* k, const void* v, tq_dtype 
 tq_status tq_workspace_size(const tq_ctx* ctx, int batch, int num_q_heads,
                             int max_seq_len, int chunk_tokens, size_t* bytes);
 
+/* Split-K chunk for a decode over sequences totalling total_tokens (host
+ * value, e.g. the scheduler's sum of the lengths; <= batch * max_seq_len)
+ * with lengths <= max_seq_len: the chunk (multiple of 16, >= 256 unless the
+ * sequences are shorter) that balances the work of the partials kernel over
+ * the GPU.  Passing 0 as chunk_tokens to the decode calls assumes every
+ * sequence has max_seq_len tokens; with very unequal lengths this call gives
+ * a better split.  No counterpart in the pages (an implementation detail of
+ * the split-K decode).  Host only, no CUDA work. */
+tq_status tq_decode_chunk(const tq_ctx* ctx, int batch, int num_q_heads, int num_kv_heads,
+                          long long total_tokens, int max_seq_len, int* chunk_tokens);
+
 /* Decode attention over the compressed cache ([P4] §2.2, §4.3; [P2] stage 2).
  * q (device): [batch][num_q_heads][d]; query head h reads KV head
  * h / (num_q_heads / num_kv_heads).  seq_lens (device int32 [batch]) <=

@@ -135,7 +135,32 @@ int pick_chunk(int units, int max_seq_len) {
 
 // Chunk for the persistent kernel (one warp per chunk, chunks taken from a
 // counter): the busiest warp handles ceil(items / slots) chunks; minimise that
-// times (chunk + a per-chunk cost of about 64 tokens), chunks of >= 256 tokens.
+// times (chunk + a per-chunk cost of about 32 tokens), chunks of >= 256
+// tokens.  items = H * sum_b ceil(L_b / chunk), estimated from the total length
+// (each sequence adds half a chunk of rounding), at most every sequence full.
+int pick_chunk_total(int batch, int H, long long total_tokens, int max_seq_len, int slots) {
+  long long best_cost = -1;
+  int best_chunk = ((max_seq_len + kPage - 1) / kPage) * kPage;
+  if (best_chunk < kPage) best_chunk = kPage;
+  for (int nch = 1; nch <= 4096; ++nch) {
+    long long chunk = (max_seq_len + nch - 1) / nch;
+    chunk = ((chunk + kPage - 1) / kPage) * kPage;
+    if (chunk < kPage) chunk = kPage;
+    if (chunk < 256 && nch > 1) break;
+    const long long full = static_cast<long long>(batch) * ((max_seq_len + chunk - 1) / chunk);
+    const long long est = (total_tokens + chunk - 1) / chunk + batch / 2;
+    const long long items = static_cast<long long>(H) * (est < full ? est : full);
+    const long long cost = ((items + slots - 1) / slots) * (chunk + 32);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_chunk = static_cast<int>(chunk);
+    }
+  }
+  return best_chunk;
+}
+
+// Chunk for the persistent kernel when only max_seq_len is known: every
+// sequence assumed full (see pick_chunk_total, per-chunk cost 64 tokens).
 int pick_chunk_warps(int units, int max_seq_len, int slots) {
   long long best_cost = -1;
   int best_chunk = ((max_seq_len + kPage - 1) / kPage) * kPage;
@@ -374,6 +399,19 @@ extern "C" tq_status tq_workspace_size(const tq_ctx* ctx, int batch, int Hq, int
     chunk = 64;
   }
   *bytes = ws_bytes(batch, Hq, ctx->cfg.d, ctx->cfg.m, nchunks_for(max_seq_len, chunk));
+  return TQ_OK;
+}
+
+extern "C" tq_status tq_decode_chunk(const tq_ctx* ctx, int batch, int Hq, int H, long long total_tokens,
+                                     int max_seq_len, int* chunk_tokens) {
+  if (!ctx || !chunk_tokens || batch < 1 || Hq < 1 || H < 1 || Hq % H || max_seq_len < 0 || total_tokens < 0 ||
+      total_tokens > static_cast<long long>(batch) * max_seq_len)
+    return TQ_ERR_INVALID_ARG;
+  const int slots = lut_decode_slots(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H);
+  if (slots > 0)
+    *chunk_tokens = pick_chunk_total(batch, H, total_tokens, max_seq_len, slots);
+  else
+    *chunk_tokens = pick_chunk(batch * H, max_seq_len);
   return TQ_OK;
 }
 

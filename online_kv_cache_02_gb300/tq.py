@@ -64,6 +64,7 @@ EXPORTS = {
     "tq_host_codebook": ([_I, _P, _P], _S),
     "tq_quantize": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P], _S),
     "tq_workspace_size": ([_P, _I, _I, _I, _I, ctypes.POINTER(_SZ)], _S),
+    "tq_decode_chunk": ([_P, _I, _I, _I, ctypes.c_longlong, _I, ctypes.POINTER(_I)], _S),
     "tq_decode_attention": ([_P, _P, _I, _I, _I, _I, _P, _I, _P, _I, _I, _P, _P, _I, ctypes.c_float,
                              _P, _P, _SZ, _P], _S),
     "tq_decode_attention_ex": ([_P, _P, _I, _I, _I, _I, _P, _I, _P, _I, _I, _P, _P, _I, ctypes.c_float,
@@ -173,6 +174,13 @@ def tq_quantize(ctx, k, v, dtype, batch, n_new, num_kv_heads, start_pos, block_t
     _check("tq_quantize", _lib.tq_quantize(ctx, _ptr(k), _ptr(v), dtype, batch, n_new, num_kv_heads,
                                            _ptr(start_pos), _ptr(block_table), max_pages_per_seq, num_pages,
                                            _ptr(k_cache), _ptr(v_cache), _stream(stream)))
+
+
+def tq_decode_chunk(ctx, batch, num_q_heads, num_kv_heads, total_tokens, max_seq_len):
+    out = _I(0)
+    _check("tq_decode_chunk", _lib.tq_decode_chunk(ctx, batch, num_q_heads, num_kv_heads, int(total_tokens),
+                                                   max_seq_len, ctypes.byref(out)))
+    return out.value
 
 
 def tq_workspace_size(ctx, batch, num_q_heads, max_seq_len, chunk_tokens=0):

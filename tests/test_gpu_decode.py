@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 from .gpu_common import (alloc_caches, ctx_for, gpu_decode, oracle, oracle_cache_bytes, seq_locations, th, to_dev,
-                         tq, wl)
+                         torch, tq, wl)
 
 pytestmark = pytest.mark.gpu
 
@@ -199,3 +199,22 @@ def test_append_decode_equals_separate_calls():
         tq.tq_destroy(ctx)
     assert np.array_equal(caches[0][0], caches[1][0]) and np.array_equal(caches[0][1], caches[1][1])
     assert np.array_equal(outs[0], outs[1])
+
+
+def test_decode_chunk_choice():
+    """tq_decode_chunk: a multiple of 16; full equal-length batches fill whole waves of warps; a batch of much
+    shorter sequences (same max_seq_len) gets chunks no longer than the full batch's; decoding with it is
+    what any other chunk gives (the chunking tests above)."""
+    w = BASE.scaled(dtype="bf16", k_bits=(4, 3), v_bits=(4, 3))
+    ctx = ctx_for(w)
+    try:
+        full = tq.tq_decode_chunk(ctx, 16, 32, 8, 16 * 32769, 32769)
+        short = tq.tq_decode_chunk(ctx, 16, 32, 8, 16 * 6000, 32769)
+        assert full % 16 == 0 and short % 16 == 0 and 256 <= short <= full
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        items = 16 * 8 * (-(-32769 // full))
+        assert items % sms == 0 or items > 4 * sms
+        with pytest.raises(tq.TQError):
+            tq.tq_decode_chunk(ctx, 16, 32, 8, 16 * 32769 + 1, 32769)
+    finally:
+        tq.tq_destroy(ctx)
