@@ -10,10 +10,12 @@
 // and lane r of tensor memory; warp w serves lanes 32*(w%4).. (the only lanes
 // it may read) and channel quarter w/4, so each vector has four threads and a
 // quarter's codes fill whole 32-bit words of the record.
-//   1. x quarter -> partial sums of squares (double-float, exact products)
-//      and max, reduced over the four threads in shared memory -> fp32 norm,
-//      exactly rounded fp16 norm, fp16 x scaled by a power of two (exact for
-//      bf16) in a 128-byte-swizzled K-major tile.
+//   1. x rows, 16 lanes per row (8 channels each; bf16 tiles arrive in the
+//      residual tile by a bulk copy issued while the previous tile was in its
+//      epilogue) -> fp32 sum of squares and max by shuffles -> fp32 norm,
+//      exactly rounded fp16 norm (a norm near an fp16 rounding midpoint is
+//      recomputed from double-float sums of the exact squares), fp16 x scaled
+//      by a power of two (exact for bf16) in a 128-byte-swizzled K-major tile.
 //   2. y = x Pi^T: tcgen05.mma kind::f16, M=128 N=128, accumulator in tensor
 //      memory; Pi is applied as fp16 hi + lo parts (about 22 bits).
 //   3. epilogue (tcgen05.ld, 32 columns): u = sqrt(d) y/||x||; the code comes
@@ -456,19 +458,6 @@ __device__ __forceinline__ void quarter_epilogue(const float (&v)[32], const Cel
   }
 }
 
-// Value k (0..31) of a thread's quarter row held as raw 16-byte chunks.
-__device__ __forceinline__ float quarter_value(const uint4 (&raw)[8], int k, bool f32) {
-  if (f32) {
-    const uint4 c = raw[k >> 2];
-    const uint32_t w = (k & 3) == 0 ? c.x : (k & 3) == 1 ? c.y : (k & 3) == 2 ? c.z : c.w;
-    return __uint_as_float(w);
-  }
-  const uint4 c = raw[k >> 3];
-  const int j = (k >> 1) & 3;
-  const uint32_t w = j == 0 ? c.x : j == 1 ? c.y : j == 2 ? c.z : c.w;
-  return __uint_as_float((k & 1) ? (w & 0xFFFF0000u) : (w << 16));
-}
-
 // Misc shared area (after the cells).
 constexpr int kQueueCap = 128;
 constexpr int kMiscQn = 20, kMiscT64 = 64, kMiscCent = 576, kMiscCentLo = 832, kMiscRedSH = 1152,
@@ -490,14 +479,16 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
   Cell* cells = reinterpret_cast<Cell*>(smem + kOffCells);
   unsigned char* misc = smem + kOffMisc4;
   unsigned long long* bars = reinterpret_cast<unsigned long long*>(misc);   // [0] tables, [1] mma
+  unsigned long long* xbar = reinterpret_cast<unsigned long long*>(misc + 24);   // x prefetch
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 16);
   int* qn = reinterpret_cast<int*>(misc + kMiscQn);
   double* t64s = reinterpret_cast<double*>(misc + kMiscT64);                  // [4][16]
   float* cents = reinterpret_cast<float*>(misc + kMiscCent);                  // [4][16]
   float* centl = reinterpret_cast<float*>(misc + kMiscCentLo);                // [4][16]
-  float* red_sh = reinterpret_cast<float*>(misc + kMiscRedSH);                // [4][128] each
-  float* red_sl = reinterpret_cast<float*>(misc + kMiscRedSL);
-  float* red_m = reinterpret_cast<float*>(misc + kMiscRedM);
+  float* rownf = reinterpret_cast<float*>(misc + kMiscRedSH);                 // [128] fp32 norm
+  float* rowscale = reinterpret_cast<float*>(misc + kMiscRedSL);              // [128] power-of-two x scale
+  unsigned short** rnormptr = reinterpret_cast<unsigned short**>(misc + kMiscRedM);   // [128] rnorm slot or null
+  unsigned short** normptr = rnormptr + kRows;                                       // [128] norm slot or null
   float* red_r = reinterpret_cast<float*>(misc + kMiscRedR);
   float* rown16 = reinterpret_cast<float*>(misc + kMiscN16);                  // [128]
   uint32_t** codeptr = reinterpret_cast<uint32_t**>(misc + kMiscCodePtr);     // [128], null: no record
@@ -526,6 +517,7 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
   if (tid == 0) {
     mbar_init(smem_u32(&bars[0]), 1);
     mbar_init(smem_u32(&bars[1]), 1);
+    mbar_init(smem_u32(xbar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     const uint32_t bytes = 2 * 32768 + (have_k ? 2 * m * 256 : 0);
     mbar_arrive_tx(smem_u32(&bars[0]), bytes);
@@ -542,10 +534,27 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
   const uint32_t tmem = *tmem_slot;
   // a wait that gives up sets the flag in every thread (uniform exit)
   bool failed = __syncthreads_or(!mbar_wait(smem_u32(&bars[0]), 0)) != 0;
-  uint32_t phase = 0;
+  uint32_t phase = 0, xphase = 0;
   const uint32_t trow = tmem + ((32u * (warp & 3)) << 16);
 
   const int ntiles = nk_tiles + nv_tiles;
+  // bf16 tiles are contiguous (128 rows x 256 B): the next one is bulk-copied
+  // into the residual tile once that is free, so a tile starts from shared
+  // memory.  Returns whether a copy was issued (same answer in every thread).
+  auto prefetch_x = [&](int nt) {
+    if (nt >= ntiles) return false;
+    const QuantizeArgs& an = nt < nk_tiles ? ka : va;
+    if (an.f32) return false;
+    const long long nvec_n = static_cast<long long>(an.batch) * an.n_new * an.H;
+    const long long g0 = static_cast<long long>(nt < nk_tiles ? nt : nt - nk_tiles) * kRows;
+    const uint32_t rows = static_cast<uint32_t>(nvec_n - g0 < kRows ? nvec_n - g0 : kRows);
+    if (tid == 0) {
+      mbar_arrive_tx(smem_u32(xbar), rows * kD * 2);
+      bulk_g2s(sbase + kOffRH, static_cast<const unsigned char*>(an.x) + g0 * kD * 2, rows * kD * 2, smem_u32(xbar));
+    }
+    return true;
+  };
+  bool xpref = !failed && prefetch_x(blockIdx.x);
   for (int tile = blockIdx.x; tile < ntiles && !failed; tile += gridDim.x) {
     const bool key = tile < nk_tiles;
     const QuantizeArgs& a = key ? ka : va;
@@ -558,38 +567,127 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
     const unsigned char* xbase = static_cast<const unsigned char*>(a.x) + static_cast<size_t>(gv0) * kD * esz;
     auto xrow_of = [&](int r) { return static_cast<const void*>(xbase + static_cast<size_t>(r) * kD * esz); };
 
-    // ---- 1. x quarter -> row statistics -> scaled fp16 tile ---------------
-    // raw holds the quarter's 32 values: 4 x (8 bf16) or 8 x (4 fp32)
-    uint4 raw[8];
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(xbase + static_cast<size_t>(row) * kD * esz + 32 * q * esz);
-      const int nchunk = f32 ? 8 : 4;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) raw[c] = (valid && c < nchunk) ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-      float sh = 0.f, sl = 0.f, mx = 0.f;      // double-float sum of the squares
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float xv = quarter_value(raw, k, f32);
-        const DF p = df_sq(xv);
-        const float t = sh + p.h, bb = t - sh;
-        sl += ((sh - (t - bb)) + (p.h - bb)) + p.l;
-        sh = t;
-        mx = fmaxf(mx, fabsf(xv));
+    // ---- 1. rows -> statistics -> scaled fp16 tile (16 lanes per row) ------
+    const bool xsm = xpref;                  // this tile's x is in the residual tile
+    if (xsm) {
+      if (__syncthreads_or(!mbar_wait(smem_u32(xbar), xphase))) {
+        failed = true;
+        if (tid == 0) atomicOr(a.tab.err, kErrTimeout);
       }
-      red_sh[q * 128 + row] = sh;
-      red_sl[q * 128 + row] = sl;
-      red_m[q * 128 + row] = mx;
+      xphase ^= 1;
+      xpref = false;
     }
-    // record location (one thread per row)
-    unsigned char* rec = nullptr;
-    int slot = 0;
-    if (q == 0) {
-      if (valid) {
-        const long long gv = gv0 + row;
-        const int h = static_cast<int>(gv % a.H);
-        const long long bt = gv / a.H;
-        const int t = static_cast<int>(bt % a.n_new);
-        const int b = static_cast<int>(bt / a.n_new);
+#pragma unroll 1
+    for (int pass = 0; pass < kRows / 32; ++pass) {
+      const int r = 32 * pass + 2 * warp + (lane >> 4), c = lane & 15;   // row, channels 8c..8c+7
+      const bool rv = gv0 + r < nvec;
+      float xv[8];
+      if (f32) {
+        const float4* src = reinterpret_cast<const float4*>(xbase + static_cast<size_t>(r) * kD * 4) + 2 * c;
+        const float4 u0 = rv ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 u1 = rv ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+        xv[0] = u0.x, xv[1] = u0.y, xv[2] = u0.z, xv[3] = u0.w, xv[4] = u1.x, xv[5] = u1.y, xv[6] = u1.z, xv[7] = u1.w;
+      } else {
+        uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
+        if (rv)
+          w4 = xsm ? *reinterpret_cast<const uint4*>(smem + kOffRH + r * kD * 2 + 16 * c)
+                   : *reinterpret_cast<const uint4*>(xbase + static_cast<size_t>(r) * kD * 2 + 16 * c);
+        const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          xv[2 * k] = __uint_as_float(ww[k] << 16);
+          xv[2 * k + 1] = __uint_as_float(ww[k] & 0xFFFF0000u);
+        }
+      }
+      float s0 = 0.f, s1 = 0.f, mx = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; k += 2) {
+        s0 = fmaf(xv[k], xv[k], s0);
+        s1 = fmaf(xv[k + 1], xv[k + 1], s1);
+        mx = fmaxf(mx, fmaxf(fabsf(xv[k]), fabsf(xv[k + 1])));
+      }
+      float ss = s0 + s1;
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) {      // the row's 16 lanes
+        ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      }
+      // fp32 norm (relative error < 4e-6); the fp16 norm must round the exact
+      // value, so a norm within 1e-5 of an fp16 midpoint is recomputed from a
+      // double-float sum of the exact squares
+      float nf = ss > 0.0f ? sqrtf(ss) : 0.0f;
+      __half h = __float2half_rn(nf);
+      bool near_mid = false;
+      if (nf > 0.0f) {
+        const float hb = __half2float(h);
+        const unsigned short hbits = __half_as_ushort(h);
+        const float up = __half2float(__ushort_as_half(static_cast<unsigned short>(hbits + 1)));
+        const float dn = hbits ? __half2float(__ushort_as_half(static_cast<unsigned short>(hbits - 1))) : 0.0f;
+        const float tol = 1e-5f * nf;
+        near_mid = fabsf(nf - 0.5f * (hb + up)) < tol || fabsf(nf - 0.5f * (hb + dn)) < tol;
+      }
+      if (__any_sync(0xffffffffu, near_mid)) {
+        DF n2{0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) n2 = df_add(n2, df_sq(xv[k]));
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1)
+          n2 = df_add(n2, DF{__shfl_xor_sync(0xffffffffu, n2.h, off), __shfl_xor_sync(0xffffffffu, n2.l, off)});
+        if (near_mid) {
+          const float rr = sqrtf(n2.h);
+          const float rl = (fmaf(-rr, rr, n2.h) + n2.l) / (2.0f * rr);
+          nf = rr + rl;
+          h = df_to_half(nf, rl - (nf - rr));
+        }
+      }
+      float xs = 1.0f;
+      if (mx > 0.0f) {
+        int e;
+        frexpf(mx, &e);
+        xs = ldexpf(1.0f, 14 - e);
+      }
+      // fp16 x * 2^k (exact for bf16); fp32 input also gets the remainder as a
+      // second fp16 tile (in the residual tile, free until the epilogue)
+      uint32_t hv[4], lv[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float x0 = xv[2 * k] * xs, x1 = xv[2 * k + 1] * xs;
+        const __half2 ph = __floats2half2_rn(x0, x1);
+        hv[k] = *reinterpret_cast<const uint32_t*>(&ph);
+        if (f32) {
+          const __half2 pl = __floats2half2_rn(x0 - __low2float(ph), x1 - __high2float(ph));
+          lv[k] = *reinterpret_cast<const uint32_t*>(&pl);
+        }
+      }
+      const uint32_t off = swz_chunk(r, c, kRows);
+      *reinterpret_cast<uint4*>(smem + kOffX + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      if (f32) *reinterpret_cast<uint4*>(smem + kOffRH + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+      if (c == 0) {
+        rownf[r] = nf;
+        rown16[r] = __half2float(h);
+        rowscale[r] = xs;
+      }
+    }
+    // record location of every row: one thread per row
+    if (tid < kRows) {
+      const int r = tid;
+      unsigned char* rec = nullptr;
+      int slot = 0;
+      if (gv0 + r < nvec) {
+        int hh, t, b;
+        const long long gv = gv0 + r;
+        if (nvec < (1LL << 31)) {          // 32-bit division when it fits
+          const uint32_t g32 = static_cast<uint32_t>(gv), H32 = static_cast<uint32_t>(a.H);
+          const uint32_t bt = g32 / H32;
+          hh = static_cast<int>(g32 - bt * H32);
+          b = static_cast<int>(bt / static_cast<uint32_t>(a.n_new));
+          t = static_cast<int>(bt - static_cast<uint32_t>(b) * static_cast<uint32_t>(a.n_new));
+        } else {
+          const long long bt = gv / a.H;
+          hh = static_cast<int>(gv % a.H);
+          t = static_cast<int>(bt % a.n_new);
+          b = static_cast<int>(bt / a.n_new);
+        }
         const int pos = a.start_pos[b] + t;
         const int blk = pos >> 4;
         if (pos < 0 || blk >= a.maxp) {
@@ -599,53 +697,15 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
           if (page < 0 || page >= a.num_pages) {
             atomicOr(a.tab.err, kErrPage);
           } else {
-            rec = a.cache + static_cast<long long>(page) * a.page_bytes + static_cast<long long>(h) * a.lay.block_bytes;
+            rec = a.cache + static_cast<long long>(page) * a.page_bytes + static_cast<long long>(hh) * a.lay.block_bytes;
             slot = pos & 15;
           }
         }
       }
-      codeptr[row] = rec ? reinterpret_cast<uint32_t*>(rec + slot * a.lay.code_bytes) : nullptr;
-      signptr[row] = rec ? reinterpret_cast<uint32_t*>(rec + a.lay.off_signs + slot * (m / 8)) : nullptr;
-    }
-    __syncthreads();
-    float nf = 0.0f, xs_scale = 1.0f, n16f;
-    {
-      const DF n2 = df_add(df_add(DF{red_sh[row], red_sl[row]}, DF{red_sh[128 + row], red_sl[128 + row]}),
-                           df_add(DF{red_sh[256 + row], red_sl[256 + row]}, DF{red_sh[384 + row], red_sl[384 + row]}));
-      const float mx = fmaxf(fmaxf(red_m[row], red_m[128 + row]), fmaxf(red_m[256 + row], red_m[384 + row]));
-      __half h = __ushort_as_half(static_cast<unsigned short>(0));
-      if (n2.h > 0.0f) {
-        const float r = sqrtf(n2.h);
-        const float rl = (fmaf(-r, r, n2.h) + n2.l) / (2.0f * r);
-        nf = r + rl;
-        h = df_to_half(nf, rl - (nf - r));
-        int e;
-        frexpf(mx, &e);
-        xs_scale = ldexpf(1.0f, 14 - e);
-      }
-      n16f = __half2float(h);
-      if (q == 0) {
-        rown16[row] = n16f;
-        if (rec) reinterpret_cast<unsigned short*>(rec + a.lay.off_norm)[slot] = __half_as_ushort(h);
-      }
-      // fp16 x * 2^k (exact for bf16); fp32 input also gets the remainder as a
-      // second fp16 tile (in the residual tile, free until the epilogue)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t hv[4], lv[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float x0 = quarter_value(raw, 8 * c + 2 * k, f32) * xs_scale;
-          const float x1 = quarter_value(raw, 8 * c + 2 * k + 1, f32) * xs_scale;
-          const __half2 ph = __floats2half2_rn(x0, x1);
-          const __half2 pl = __floats2half2_rn(x0 - __low2float(ph), x1 - __high2float(ph));
-          hv[k] = *reinterpret_cast<const uint32_t*>(&ph);
-          lv[k] = *reinterpret_cast<const uint32_t*>(&pl);
-        }
-        const uint32_t off = swz_chunk(row, 4 * q + c, kRows);
-        *reinterpret_cast<uint4*>(smem + kOffX + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-        if (f32) *reinterpret_cast<uint4*>(smem + kOffRH + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-      }
+      codeptr[r] = rec ? reinterpret_cast<uint32_t*>(rec + slot * a.lay.code_bytes) : nullptr;
+      signptr[r] = rec ? reinterpret_cast<uint32_t*>(rec + a.lay.off_signs + slot * (m / 8)) : nullptr;
+      rnormptr[r] = (rec && sk) ? reinterpret_cast<unsigned short*>(rec + a.lay.off_rnorm) + slot : nullptr;
+      normptr[r] = rec ? reinterpret_cast<unsigned short*>(rec + a.lay.off_norm) + slot : nullptr;
     }
     fence_proxy_async();
     tc_fence_before();
@@ -673,6 +733,10 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
     }
     phase ^= 1;
     tc_fence_after();
+    // the residual tile is free now unless this tile still needs it for r'
+    if (!sk) xpref = prefetch_x(tile + gridDim.x);
+    const float nf = rownf[row], n16f = rown16[row], xs_scale = rowscale[row];
+    if (q == 0 && normptr[row]) *normptr[row] = __half_as_ushort(__float2half_rn(n16f));   // exact: n16f is fp16
 
     // ---- 3. codes and residual of this quarter -------------------------------
     const int grp = q < 2 ? 0 : 1;
@@ -777,6 +841,7 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
       }
       phase ^= 1;
       tc_fence_after();
+      xpref = prefetch_x(tile + gridDim.x);      // the z MMA has read the residual tile
       const float rho = sqrtf((red_r[row] + red_r[128 + row]) + (red_r[256 + row] + red_r[384 + row]));
       uint32_t nearz = 0;
       if (32 * q < m) {
@@ -818,15 +883,16 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
           if (!__syncthreads_or(mine != 0)) break;
         }
       }
-      if (rec)
-        reinterpret_cast<unsigned short*>(rec + a.lay.off_rnorm)[slot] =
-            __half_as_ushort(__float2half_rn(rho * n16f * kInvSqrtDHi));
+      if (q == 0 && rnormptr[row]) *rnormptr[row] = __half_as_ushort(__float2half_rn(rho * n16f * kInvSqrtDHi));
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
   }
 
+  // a prefetch issued for a tile this CTA no longer runs (after a failure)
+  // lands before the CTA can exit (bounded wait)
+  if (xpref) (void)mbar_wait(smem_u32(xbar), xphase);
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
