@@ -187,7 +187,8 @@ class DecodeBench:
         self.lens1 = torch.from_numpy((self.lens + 1).astype(np.int32)).to(dev)
         self.max_len = int(self.lens.max()) + 1
         # split-K chunk: the workload's own, else the library's choice for the actual total length
-        self.chunk = w.chunk or tq.tq_decode_chunk(self.ctx, B, Hq, H, int((self.lens + 1).sum()), self.max_len)
+        self.chunk = w.chunk or tq.tq_decode_chunk(self.ctx, B, Hq, H, int((self.lens + 1).sum()), self.max_len,
+                                                   fused_append=True)
         self.ws_n = tq.tq_workspace_size(self.ctx, B, Hq, self.max_len, self.chunk)
         self.ws = torch.empty(self.ws_n, dtype=torch.uint8, device=dev)
         self.out = torch.empty(B, Hq, 128, dtype=torch.float32, device=dev)
@@ -198,45 +199,27 @@ class DecodeBench:
         self.launches_per_step = 4
 
     def _marshal(self, stream):
-        """ctypes argument tuples of the per-step C calls, built once per stream (pointers are fixed)."""
+        """ctypes arguments of the fused per-step call, built once per stream (pointers are fixed)."""
         import ctypes
         w, tq = self.w, self.tq
         sp = stream.cuda_stream
-        quant = (self.ctx, self.knew.data_ptr(), self.vnew.data_ptr(), tq.TQ_BF16, w.batch, 1, w.kv_heads,
-                 self.start.data_ptr(), self.bt_d.data_ptr(), self.pps, self.num_pages, self.kc.data_ptr(),
-                 self.vc.data_ptr(), sp)
-        dec = [self.ctx, self.q.data_ptr(), tq.TQ_BF16, w.batch, w.q_heads, w.kv_heads, self.lens1.data_ptr(),
-               self.max_len, self.bt_d.data_ptr(), self.pps, self.num_pages, self.kc.data_ptr(), self.vc.data_ptr(),
-               self.chunk, ctypes.c_float(1.0 / math.sqrt(128)), self.out.data_ptr(), self.ws.data_ptr(), self.ws_n]
-        stages = {st: tuple(dec + [st, sp]) for st in (tq.TQ_STAGE_QPREP, tq.TQ_STAGE_PARTIALS, tq.TQ_STAGE_MERGE,
-                                                       tq.TQ_STAGE_ALL)}
-        self._args = (stream, quant, stages)
-
-    def _call(self, name, args):
-        st = getattr(self.tq._lib, name)(*args)
-        if st != 0:
-            raise self.tq.TQError(name, st)
-
-    def decode(self, stream, stages):
-        if getattr(self, "_args", (None,))[0] is not stream:
-            self._marshal(stream)
-        self._call("tq_decode_attention_ex", self._args[2][stages])
-
-    def append(self, stream):
-        if getattr(self, "_args", (None,))[0] is not stream:
-            self._marshal(stream)
-        self._call("tq_quantize", self._args[1])
+        self._args = (stream, [self.ctx, self.knew.data_ptr(), self.vnew.data_ptr(), self.q.data_ptr(), tq.TQ_BF16,
+                               w.batch, w.q_heads, w.kv_heads, self.start.data_ptr(), self.max_len,
+                               self.bt_d.data_ptr(), self.pps, self.num_pages, self.kc.data_ptr(), self.vc.data_ptr(),
+                               self.chunk, ctypes.c_float(1.0 / math.sqrt(128)), self.out.data_ptr(),
+                               self.ws.data_ptr(), self.ws_n, sp])
 
     def step(self, stream, ev=None):
-        tq = self.tq
-        self.append(stream)
-        self.decode(stream, tq.TQ_STAGE_QPREP)
+        """One decode step through the fused C call: quantize-append the new token at position L, decode over L+1;
+        `ev` (begin, end) events are recorded by the library around the partials kernel."""
+        if getattr(self, "_args", (None,))[0] is not stream:
+            self._marshal(stream)
+        handles = [None, None]
         if ev is not None:
-            ev[0].record(stream)
-        self.decode(stream, tq.TQ_STAGE_PARTIALS)
-        if ev is not None:
-            ev[1].record(stream)
-        self.decode(stream, tq.TQ_STAGE_MERGE)
+            handles = [e.cuda_event for e in ev]
+        st = self.tq._lib.tq_append_decode_ex(*self._args[1], *handles)
+        if st != 0:
+            raise self.tq.TQError("tq_append_decode_ex", st)
 
     def step_e2e(self, stream):
         """One step through the public fused call, inputs from pinned host memory, output back to host."""
@@ -402,6 +385,9 @@ def run_ours(args):
     db = DecodeBench(w, torch, tq)
     steps, warmup = args.steps, max(3, args.warmup)
     ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(steps)]
+    for pair in ev:                      # create the CUDA events (the library records them inside the step)
+        for e in pair:
+            e.record(stream)
     for _ in range(warmup):
         db.step(stream)
     torch.cuda.synchronize()

@@ -135,10 +135,12 @@ tq_status tq_workspace_size(const tq_ctx* ctx, int batch, int num_q_heads,
  * sequences are shorter) that balances the work of the partials kernel over
  * the GPU.  Passing 0 as chunk_tokens to the decode calls assumes every
  * sequence has max_seq_len tokens; with very unequal lengths this call gives
- * a better split.  No counterpart in the pages (an implementation detail of
- * the split-K decode).  Host only, no CUDA work. */
+ * a better split.  fused_append = 1 sizes it for tq_append_decode, whose
+ * partials kernel leaves a few SMs to the new token's quantize-append.  No
+ * counterpart in the pages (an implementation detail of the split-K decode).
+ * Host only, no CUDA work. */
 tq_status tq_decode_chunk(const tq_ctx* ctx, int batch, int num_q_heads, int num_kv_heads,
-                          long long total_tokens, int max_seq_len, int* chunk_tokens);
+                          long long total_tokens, int max_seq_len, int fused_append, int* chunk_tokens);
 
 /* Decode attention over the compressed cache ([P4] §2.2, §4.3; [P2] stage 2).
  * q (device): [batch][num_q_heads][d]; query head h reads KV head
@@ -217,6 +219,24 @@ tq_status tq_append_decode(const tq_ctx* ctx, const void* k_new, const void* v_n
                            const int32_t* block_table, int max_pages_per_seq, int num_pages,
                            void* k_cache, void* v_cache, int chunk_tokens, float softmax_scale,
                            float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* tq_append_decode with two optional CUDA events (cudaEvent_t, may be NULL)
+ * recorded on `stream` just before and just after the split-K partials kernel,
+ * for timing it inside the fused step.  Execution: the new token's
+ * quantize-append runs on a second stream created with the context on first
+ * use (joined with events; calls sharing a context serialise their host-side
+ * enqueue) next to the query prep and the partials kernel, which covers the
+ * seq_lens[b] cached tokens and leaves a few SMs to the append; the merge then
+ * scores the new token from its stored record and adds it to the log-sum-exp
+ * merge.  Results equal tq_quantize + tq_decode_attention over L+1 tokens up
+ * to fp32 rounding of the new token's term. */
+tq_status tq_append_decode_ex(const tq_ctx* ctx, const void* k_new, const void* v_new, const void* q,
+                              tq_dtype dtype, int batch, int num_q_heads, int num_kv_heads,
+                              const int32_t* seq_lens, int max_seq_len,
+                              const int32_t* block_table, int max_pages_per_seq, int num_pages,
+                              void* k_cache, void* v_cache, int chunk_tokens, float softmax_scale,
+                              float* out, void* workspace, size_t workspace_bytes, void* stream,
+                              void* partials_begin_event, void* partials_end_event);
 
 /* Synchronise the device and report (then clear) the context's device error
  * word: TQ_OK, or TQ_ERR_DEVICE_CHECK with the bits in *flags (may be NULL):

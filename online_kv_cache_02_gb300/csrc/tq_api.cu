@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -211,6 +212,8 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
   const int d = cfg->d, m = cfg->m;
   tq_ctx* ctx = new (std::nothrow) tq_ctx();
   if (!ctx) return TQ_ERR_OOM;
+  ctx->fused_mu = new (std::nothrow) std::mutex();
+  if (!ctx->fused_mu) { delete ctx; return TQ_ERR_OOM; }
   ctx->cfg = *cfg;
   if (cudaGetDevice(&ctx->device) != cudaSuccess) { delete ctx; return TQ_ERR_CUDA; }
   fill_layout(ctx->kl, cfg->k_bits_hi, cfg->k_bits_lo, cfg->k_split, d, m, true, cfg->k_qjl != 0);
@@ -319,6 +322,13 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
 
 extern "C" tq_status tq_destroy(tq_ctx* ctx) {
   if (!ctx) return TQ_ERR_INVALID_ARG;
+  if (ctx->aux_stream) {
+    cudaStreamSynchronize(ctx->aux_stream);
+    cudaStreamDestroy(ctx->aux_stream);
+    cudaEventDestroy(ctx->ev_fork);
+    cudaEventDestroy(ctx->ev_join);
+  }
+  delete static_cast<std::mutex*>(ctx->fused_mu);
   cudaError_t e = cudaFree(ctx->dev_block);
   delete ctx;
   return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
@@ -337,10 +347,24 @@ extern "C" tq_status tq_cache_layout(const tq_ctx* ctx, int num_kv_heads, size_t
   return TQ_OK;
 }
 
+namespace {
+tq_status quantize_impl(const tq_ctx* ctx, const void* k, const void* v, tq_dtype dtype, int batch, int n_new, int H,
+                        const int32_t* start_pos, const int32_t* block_table, int maxp, int num_pages, void* k_cache,
+                        void* v_cache, void* stream, int max_ctas);
+}  // namespace
+
 extern "C" tq_status tq_quantize(const tq_ctx* ctx, const void* k, const void* v, tq_dtype dtype,
                                  int batch, int n_new, int H, const int32_t* start_pos,
                                  const int32_t* block_table, int maxp, int num_pages, void* k_cache,
                                  void* v_cache, void* stream) {
+  return quantize_impl(ctx, k, v, dtype, batch, n_new, H, start_pos, block_table, maxp, num_pages, k_cache, v_cache,
+                       stream, 0);
+}
+
+namespace {
+tq_status quantize_impl(const tq_ctx* ctx, const void* k, const void* v, tq_dtype dtype, int batch, int n_new, int H,
+                        const int32_t* start_pos, const int32_t* block_table, int maxp, int num_pages, void* k_cache,
+                        void* v_cache, void* stream, int max_ctas) {
   if (!ctx || (!k && !v) || batch < 0 || n_new < 0 || H < 1 || maxp < 1 || num_pages < 1)
     return TQ_ERR_INVALID_ARG;
   if (dtype != TQ_BF16 && dtype != TQ_F32) return TQ_ERR_INVALID_ARG;
@@ -367,6 +391,7 @@ extern "C" tq_status tq_quantize(const tq_ctx* ctx, const void* k, const void* v
     a.page_bytes = static_cast<long long>(a.lay.block_bytes) * H;
     a.m = ctx->cfg.m;
     a.tab = ctx->tab;
+    a.max_ctas = max_ctas;
   }
   cudaError_t e = cudaSuccess;
   if (launch_quantize_tc(args[0], args[1], s, &e)) return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
@@ -376,6 +401,7 @@ extern "C" tq_status tq_quantize(const tq_ctx* ctx, const void* k, const void* v
   }
   return TQ_OK;
 }
+}  // namespace
 
 namespace {
 int nchunks_for(int max_seq_len, int chunk) { return max_seq_len <= 0 ? 1 : (max_seq_len + chunk - 1) / chunk; }
@@ -402,12 +428,29 @@ extern "C" tq_status tq_workspace_size(const tq_ctx* ctx, int batch, int Hq, int
   return TQ_OK;
 }
 
+namespace {
+int sm_count() {
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
+
+// SMs left to the one-token append of a fused step: one per 128-vector tile of
+// K and of V (the append's CTAs), at most 8.
+int append_reserve(int batch, int H) {
+  const long long tiles = 2 * ((static_cast<long long>(batch) * H + 127) / 128);
+  return static_cast<int>(tiles < 8 ? tiles : 8);
+}
+
+}  // namespace
+
 extern "C" tq_status tq_decode_chunk(const tq_ctx* ctx, int batch, int Hq, int H, long long total_tokens,
-                                     int max_seq_len, int* chunk_tokens) {
+                                     int max_seq_len, int fused_append, int* chunk_tokens) {
   if (!ctx || !chunk_tokens || batch < 1 || Hq < 1 || H < 1 || Hq % H || max_seq_len < 0 || total_tokens < 0 ||
       total_tokens > static_cast<long long>(batch) * max_seq_len)
     return TQ_ERR_INVALID_ARG;
-  const int slots = lut_decode_slots(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H);
+  int slots = lut_decode_slots(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H);
+  if (fused_append && slots > 0) slots = slots / sm_count() * (sm_count() - append_reserve(batch, H));
   if (slots > 0)
     *chunk_tokens = pick_chunk_total(batch, H, total_tokens, max_seq_len, slots);
   else
@@ -427,11 +470,21 @@ extern "C" tq_status tq_decode_attention(const tq_ctx* ctx, const void* q, tq_dt
 }
 
 namespace {
+// The fused decode step (tq_append_decode): the partials kernel covers the
+// cached tokens and leaves `reserve` SMs to the new token's quantize-append on
+// the context's second stream; the merge waits for it (join) and adds the new
+// token itself.  Optional events bracket the partials launch.
+struct FusedStep {
+  int reserve;
+  cudaEvent_t join;
+  cudaEvent_t partials_begin, partials_end;
+};
+
 tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batch, int Hq, int H,
                       const int32_t* seq_lens, int len_add, int max_seq_len, const int32_t* block_table, int maxp,
                       int num_pages, const void* k_cache, const void* v_cache, int chunk_tokens,
                       float softmax_scale, float* out, void* workspace, size_t workspace_bytes, int stages,
-                      void* stream) {
+                      void* stream, const FusedStep* fused = nullptr) {
   if (stages < 1 || stages > TQ_STAGE_ALL) return TQ_ERR_INVALID_ARG;
   if (!ctx || batch < 0 || Hq < 1 || H < 1 || Hq % H || max_seq_len < 0 || maxp < 1 ||
       num_pages < 1 || chunk_tokens < 0 || chunk_tokens % kPage)
@@ -442,7 +495,8 @@ tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batc
   if (batch == 0) return TQ_OK;
   if (!q || !seq_lens || !block_table || !k_cache || !v_cache || !out || !workspace)
     return TQ_ERR_INVALID_ARG;
-  const int lut_slots = lut_decode_slots(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H);
+  int lut_slots = lut_decode_slots(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H);
+  if (fused && lut_slots > 0) lut_slots = lut_slots / sm_count() * (sm_count() - fused->reserve);
   int chunk = chunk_tokens              ? chunk_tokens
               : lut_slots > 0           ? pick_chunk_warps(batch * H, max_seq_len, lut_slots)
                                         : pick_chunk(batch * H, max_seq_len);
@@ -483,7 +537,17 @@ tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batc
   a.qfrag = reinterpret_cast<uint32_t*>(w + o_frag);
   a.sched = reinterpret_cast<int*>(w + o_frag + align256(sizeof(uint32_t) * static_cast<size_t>(batch) * Hq * 128));
   a.out = out;
-  return launch_decode(a, stages, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!fused) return launch_decode(a, stages, st) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  a.new_token = 1;                       // len_add is 0 here: the partials cover [0, seq_lens[b])
+  a.max_ctas = sm_count() - fused->reserve;
+  bool ok = launch_decode(a, TQ_STAGE_QPREP, st) == cudaSuccess;
+  if (ok && fused->partials_begin) ok = cudaEventRecord(fused->partials_begin, st) == cudaSuccess;
+  ok = ok && launch_decode(a, TQ_STAGE_PARTIALS, st) == cudaSuccess;
+  if (ok && fused->partials_end) ok = cudaEventRecord(fused->partials_end, st) == cudaSuccess;
+  ok = ok && cudaStreamWaitEvent(st, fused->join, 0) == cudaSuccess;
+  ok = ok && launch_decode(a, TQ_STAGE_MERGE, st) == cudaSuccess;
+  return ok ? TQ_OK : TQ_ERR_CUDA;
 }
 }  // namespace
 
@@ -502,6 +566,17 @@ extern "C" tq_status tq_append_decode(const tq_ctx* ctx, const void* k_new, cons
                                       int max_seq_len, const int32_t* block_table, int maxp, int num_pages,
                                       void* k_cache, void* v_cache, int chunk_tokens, float softmax_scale,
                                       float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return tq_append_decode_ex(ctx, k_new, v_new, q, dtype, batch, Hq, H, seq_lens, max_seq_len, block_table, maxp,
+                             num_pages, k_cache, v_cache, chunk_tokens, softmax_scale, out, workspace,
+                             workspace_bytes, stream, nullptr, nullptr);
+}
+
+extern "C" tq_status tq_append_decode_ex(const tq_ctx* ctx, const void* k_new, const void* v_new, const void* q,
+                                         tq_dtype dtype, int batch, int Hq, int H, const int32_t* seq_lens,
+                                         int max_seq_len, const int32_t* block_table, int maxp, int num_pages,
+                                         void* k_cache, void* v_cache, int chunk_tokens, float softmax_scale,
+                                         float* out, void* workspace, size_t workspace_bytes, void* stream,
+                                         void* partials_begin, void* partials_end) {
   if (!ctx || !k_new || !v_new || batch < 0 || H < 1 || Hq < 1 || Hq % H || max_seq_len < 1)
     return TQ_ERR_INVALID_ARG;
   if (batch == 0) return TQ_OK;
@@ -511,11 +586,33 @@ extern "C" tq_status tq_append_decode(const tq_ctx* ctx, const void* k_new, cons
   if (st != TQ_OK) return st;
   if (!q || !out || !workspace || !seq_lens || !block_table) return TQ_ERR_INVALID_ARG;
   if (Hq / H > kMaxGroup) return TQ_ERR_UNSUPPORTED;
-  st = tq_quantize(ctx, k_new, v_new, dtype, batch, 1, H, seq_lens, block_table, maxp, num_pages, k_cache, v_cache,
-                   stream);
+  if (dtype != TQ_BF16 && dtype != TQ_F32) return TQ_ERR_INVALID_ARG;
+  if (!k_cache || !v_cache || maxp < 1 || num_pages < 1) return TQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15) return TQ_ERR_INVALID_ARG;
+  if (static_cast<long long>(batch) * H > (1LL << 31) - 1) return TQ_ERR_INVALID_ARG;
+  tq_ctx* c = const_cast<tq_ctx*>(ctx);
+  std::lock_guard<std::mutex> lock(*static_cast<std::mutex*>(c->fused_mu));
+  if (!c->aux_stream) {
+    if (cudaStreamCreateWithFlags(&c->aux_stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return TQ_ERR_CUDA;
+    }
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  FusedStep f{append_reserve(batch, H), c->ev_join, static_cast<cudaEvent_t>(partials_begin),
+              static_cast<cudaEvent_t>(partials_end)};
+  // fork: the quantize-append of the new token runs on the second stream
+  if (cudaEventRecord(c->ev_fork, s) != cudaSuccess || cudaStreamWaitEvent(c->aux_stream, c->ev_fork, 0) != cudaSuccess)
+    return TQ_ERR_CUDA;
+  st = quantize_impl(ctx, k_new, v_new, dtype, batch, 1, H, seq_lens, block_table, maxp, num_pages, k_cache, v_cache,
+                     c->aux_stream, f.reserve);
   if (st != TQ_OK) return st;
-  return decode_impl(ctx, q, dtype, batch, Hq, H, seq_lens, 1, max_seq_len, block_table, maxp, num_pages, k_cache,
-                     v_cache, chunk_tokens, softmax_scale, out, workspace, workspace_bytes, TQ_STAGE_ALL, stream);
+  if (cudaEventRecord(c->ev_join, c->aux_stream) != cudaSuccess) return TQ_ERR_CUDA;
+  // qprep and the partials over the cached tokens, then (joined) the merge
+  return decode_impl(ctx, q, dtype, batch, Hq, H, seq_lens, 0, max_seq_len, block_table, maxp, num_pages, k_cache,
+                     v_cache, chunk_tokens, softmax_scale, out, workspace, workspace_bytes, TQ_STAGE_ALL, stream, &f);
 }
 
 extern "C" tq_status tq_check_device_status(const tq_ctx* ctx, uint32_t* flags) {

@@ -336,10 +336,66 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) 
 constexpr int kMGroups = 4;
 constexpr int kMThreads = kMGroups * kD;
 
+// The token at position seq_lens[b] of a fused decode step, scored here from its
+// stored record (the quantize-append ran on another stream, next to the
+// partials kernel, which covered positions [0, seq_lens[b])): logit (log2
+// units) and, in vnew, its dequantized value scaled by n_v/sqrt(d).
+// Returns -inf when there is no such token (flags a bad page id or length).
+__device__ float new_token_logit(const DecodeArgs& a, long long row, float* vnew, float* red) {
+  const int tid = threadIdx.x, j = tid & (kD - 1), grp = tid >> 7;
+  const int b = static_cast<int>(row / a.Hq), hkv = static_cast<int>(row % a.Hq) / a.G;
+  const int L0 = a.seq_lens[b];
+  if (L0 < 0 || L0 >= a.maxp * kPage || L0 + 1 > a.max_seq_len) {
+    if (tid == 0 && (row % a.Hq) == 0) atomicOr(a.tab.err, kErrSeqLen);
+    return -INFINITY;
+  }
+  const int page = a.block_table[static_cast<long long>(b) * a.maxp + (L0 >> 4)], slot = L0 & 15;
+  if (page < 0 || page >= a.num_pages) {
+    if (tid == 0 && (row % a.Hq) == 0) atomicOr(a.tab.err, kErrPage);
+    return -INFINITY;
+  }
+  const uint8_t* krec = a.kc + static_cast<long long>(page) * a.k_page_bytes + static_cast<long long>(hkv) * a.kl.block_bytes;
+  const uint8_t* vrec = a.vc + static_cast<long long>(page) * a.v_page_bytes + static_cast<long long>(hkv) * a.vl.block_bytes;
+  const float* qr = a.qprep + row * (kD + a.m);
+  float part = 0.0f;
+  if (grp == 0) {                      // <q~, c_K[code]>
+    const unsigned* kw = reinterpret_cast<const unsigned*>(krec + slot * a.kl.code_bytes);
+    const int code = code_at(kw, a.kl.g[0].bits, a.kl.g[1].bits, a.kl.split, j);
+    part = qr[j] * a.kl.g[j < a.kl.split ? 0 : 1].c[code];
+  } else if (grp == 1 && a.kl.qjl && j < a.m) {   // <u, +-1 signs>
+    const uint8_t sb = krec[a.kl.off_signs + slot * (a.m / 8) + (j >> 3)];
+    part = ((sb >> (j & 7)) & 1u) ? qr[kD + j] : -qr[kD + j];
+  } else if (grp == 2) {               // value
+    const unsigned* vw = reinterpret_cast<const unsigned*>(vrec + slot * a.vl.code_bytes);
+    const int code = code_at(vw, a.vl.g[0].bits, a.vl.g[1].bits, a.vl.split, j);
+    const float nv = __half2float(reinterpret_cast<const __half*>(vrec + a.vl.off_norm)[slot]);
+    vnew[j] = nv * kInvSqrtD * a.vl.g[j < a.vl.split ? 0 : 1].c[code];
+  }
+  part = warp_sum(part);
+  __syncthreads();
+  if ((tid & 31) == 0) red[tid >> 5] = part;
+  __syncthreads();
+  float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    s1 += red[w];
+    s2 += red[4 + w];
+  }
+  const float nk = __half2float(reinterpret_cast<const __half*>(krec + a.kl.off_norm)[slot]);
+  float lg = nk * kInvSqrtD * s1;
+  if (a.kl.qjl) {
+    const float rk = __half2float(reinterpret_cast<const __half*>(krec + a.kl.off_rnorm)[slot]);
+    lg = fmaf(kSqrtHalfPi / static_cast<float>(a.m) * rk, s2, lg);
+  }
+  __syncthreads();                     // red is reused by the caller
+  return lg * a.scale_log2;
+}
+
 __global__ void __launch_bounds__(kMThreads) merge_kernel(DecodeArgs a) {
   __shared__ float wsh[kMThreads];
   __shared__ float part[kMGroups][kD];
   __shared__ float os[kD];
+  __shared__ float vnew[kD];
   __shared__ float red[kMThreads / 32];
   const long long row = blockIdx.x;                 // b * Hq + query head
   const int tid = threadIdx.x, j = tid & (kD - 1), grp = tid >> 7;
@@ -349,9 +405,11 @@ __global__ void __launch_bounds__(kMThreads) merge_kernel(DecodeArgs a) {
   L = L > a.maxp * kPage ? a.maxp * kPage : L;
   const int nc = min(a.nchunks, (L + a.chunk - 1) / a.chunk);
   const float* P = a.part + row * a.nchunks * (kD + 2);
+  const float lg_new = a.new_token ? new_token_logit(a, row, vnew, red) : -INFINITY;
   float M = -INFINITY;
   for (int c = tid; c < nc; c += kMThreads) M = fmaxf(M, P[static_cast<long long>(c) * (kD + 2)]);
-  M = block_reduce<kMThreads>(M, true, red);
+  M = fmaxf(block_reduce<kMThreads>(M, true, red), lg_new);
+  const float w_new = lg_new > -INFINITY ? exp2f(lg_new - M) : 0.0f;
   float lpart = 0.0f, A0 = 0.0f, A1 = 0.0f;
   for (int c0 = 0; c0 < nc; c0 += kMThreads) {
     const int c = c0 + tid;
@@ -372,6 +430,8 @@ __global__ void __launch_bounds__(kMThreads) merge_kernel(DecodeArgs a) {
     }
     if (cc < n) A0 = fmaf(wsh[cc], P[static_cast<long long>(c0 + cc) * (kD + 2) + 2 + j], A0);
   }
+  if (tid == 0) lpart += w_new;
+  if (grp == 0 && w_new > 0.0f) A0 = fmaf(w_new, vnew[j], A0);
   const float l = block_reduce<kMThreads>(lpart, false, red);
   part[grp][j] = A0 + A1;
   __syncthreads();

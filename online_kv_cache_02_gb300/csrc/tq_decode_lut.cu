@@ -609,9 +609,11 @@ cudaError_t launch_lut(const DecodeArgs& a, int items, cudaStream_t s) {
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  // one CTA per SM (fewer only when there are fewer chunks than SMs): a warp
+  // one CTA per SM (fewer when there are fewer chunks than SMs, or when the
+  // fused decode step leaves SMs to the new token's quantize-append): a warp
   // without a chunk exits at once, and every SM's copy engines are in use
-  const int grid = items < sms ? (items > 0 ? items : 1) : sms;
+  const int cap = a.max_ctas > 0 && a.max_ctas < sms ? a.max_ctas : sms;
+  const int grid = items < cap ? (items > 0 ? items : 1) : cap;
   lut_partials_kernel<KBH, KBL, VBH, VBL, QJL><<<grid, kThreadsL, Gm::SMEM, s>>>(a, items);
   return cudaGetLastError();
 }

@@ -95,6 +95,7 @@ struct QuantizeArgs {
   int m;
   KindLayout lay;
   DeviceTables tab;
+  int max_ctas;          // 0: up to one CTA per SM; else at most this many (fused decode step)
 };
 
 struct DecodeArgs {
@@ -118,6 +119,8 @@ struct DecodeArgs {
   float* part;           // [B][Hq][nchunks][d + 2]
   float* out;            // [B][Hq][d]
   int* sched;            // [2] work counter and finished-warp count of the persistent kernel (zeroed by qprep)
+  int new_token;         // 1: merge adds the token at position seq_lens[b] itself (fused decode step)
+  int max_ctas;          // partials kernel: 0 = one CTA per SM, else at most this many
   uint32_t* qfrag;       // [B][Hq][4][32] fp16 pairs in the persistent kernel's fragment order (m = 128 only):
                          // for lane t%4 of a KV-head warp, 16 words of q~ (key pairs) then 16 of u
 };
@@ -141,6 +144,11 @@ struct tq_ctx {
   tq::KindLayout kl, vl;
   tq::DeviceTables tab;
   void* dev_block;       // single allocation holding every device table
+  // fused decode step: the new token's quantize-append runs on this stream
+  // next to the partials kernel (created on first use, guarded by fused_mu)
+  void* fused_mu;        // std::mutex*
+  cudaStream_t aux_stream;
+  cudaEvent_t ev_fork, ev_join;
 };
 
 #endif  // TQ_INTERNAL_H_

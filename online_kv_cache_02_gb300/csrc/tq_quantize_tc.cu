@@ -910,7 +910,8 @@ cudaError_t launch_tc(const QuantizeArgs& k, const QuantizeArgs& v, int nk, int 
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int tiles = nk + nv;
-  const int grid = tiles < sms ? tiles : sms;
+  const int cap = k.max_ctas > 0 && k.max_ctas < sms ? k.max_ctas : sms;
+  const int grid = tiles < cap ? tiles : cap;
   quantize_tc_kernel<KBH, KBL, VBH, VBL><<<grid, kThreadsTC4, kSmemBytes4, s>>>(k, v, nk, nv);
   return cudaGetLastError();
 }

@@ -64,7 +64,7 @@ EXPORTS = {
     "tq_host_codebook": ([_I, _P, _P], _S),
     "tq_quantize": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P], _S),
     "tq_workspace_size": ([_P, _I, _I, _I, _I, ctypes.POINTER(_SZ)], _S),
-    "tq_decode_chunk": ([_P, _I, _I, _I, ctypes.c_longlong, _I, ctypes.POINTER(_I)], _S),
+    "tq_decode_chunk": ([_P, _I, _I, _I, ctypes.c_longlong, _I, _I, ctypes.POINTER(_I)], _S),
     "tq_decode_attention": ([_P, _P, _I, _I, _I, _I, _P, _I, _P, _I, _I, _P, _P, _I, ctypes.c_float,
                              _P, _P, _SZ, _P], _S),
     "tq_decode_attention_ex": ([_P, _P, _I, _I, _I, _I, _P, _I, _P, _I, _I, _P, _P, _I, ctypes.c_float,
@@ -73,6 +73,8 @@ EXPORTS = {
                                      _P, _P], _S),
     "tq_append_decode": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _I, _I, _P, _P, _I, ctypes.c_float, _P,
                           _P, _SZ, _P], _S),
+    "tq_append_decode_ex": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _I, _I, _P, _P, _I, ctypes.c_float, _P,
+                             _P, _SZ, _P, _P, _P], _S),
     "tq_check_device_status": ([_P, ctypes.POINTER(ctypes.c_uint32)], _S),
     "tq_refine_counters": ([_P, ctypes.POINTER(ctypes.c_ulonglong), _I], _S),
     "tq_status_string": ([_S], ctypes.c_char_p),
@@ -176,10 +178,10 @@ def tq_quantize(ctx, k, v, dtype, batch, n_new, num_kv_heads, start_pos, block_t
                                            _ptr(k_cache), _ptr(v_cache), _stream(stream)))
 
 
-def tq_decode_chunk(ctx, batch, num_q_heads, num_kv_heads, total_tokens, max_seq_len):
+def tq_decode_chunk(ctx, batch, num_q_heads, num_kv_heads, total_tokens, max_seq_len, fused_append=False):
     out = _I(0)
     _check("tq_decode_chunk", _lib.tq_decode_chunk(ctx, batch, num_q_heads, num_kv_heads, int(total_tokens),
-                                                   max_seq_len, ctypes.byref(out)))
+                                                   max_seq_len, int(bool(fused_append)), ctypes.byref(out)))
     return out.value
 
 
@@ -201,11 +203,13 @@ def tq_decode_attention(ctx, q, dtype, batch, num_q_heads, num_kv_heads, seq_len
 
 def tq_append_decode(ctx, k_new, v_new, q, dtype, batch, num_q_heads, num_kv_heads, seq_lens, max_seq_len,
                      block_table, max_pages_per_seq, num_pages, k_cache, v_cache, chunk_tokens, softmax_scale, out,
-                     workspace, workspace_bytes, stream=None):
-    _check("tq_append_decode", _lib.tq_append_decode(
+                     workspace, workspace_bytes, stream=None, partials_events=None):
+    """partials_events: optional (begin, end) CUDA event handles (ints) recorded around the partials kernel."""
+    ev0, ev1 = partials_events if partials_events else (None, None)
+    _check("tq_append_decode_ex", _lib.tq_append_decode_ex(
         ctx, _ptr(k_new), _ptr(v_new), _ptr(q), dtype, batch, num_q_heads, num_kv_heads, _ptr(seq_lens), max_seq_len,
         _ptr(block_table), max_pages_per_seq, num_pages, _ptr(k_cache), _ptr(v_cache), chunk_tokens, softmax_scale,
-        _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)))
+        _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream), ev0, ev1))
 
 
 TQ_STAGE_QPREP, TQ_STAGE_PARTIALS, TQ_STAGE_MERGE, TQ_STAGE_ALL = 1, 2, 4, 7

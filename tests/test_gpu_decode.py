@@ -198,7 +198,9 @@ def test_append_decode_equals_separate_calls():
     finally:
         tq.tq_destroy(ctx)
     assert np.array_equal(caches[0][0], caches[1][0]) and np.array_equal(caches[0][1], caches[1][1])
-    assert np.array_equal(outs[0], outs[1])
+    # the fused step scores the new token in the merge (fp32) rather than in the partials kernel (fp16 operands)
+    assert np.all(np.isfinite(outs[0]))
+    assert th.rel_err(outs[0], outs[1]).max() <= th.ATT_TOL
 
 
 def test_decode_chunk_choice():

@@ -93,4 +93,4 @@ def test_null_context_is_rejected(tq):
     assert st("tq_check_device_status", None, None) == tq.TQ_ERR_INVALID_ARG
     assert st("tq_cache_layout", None, 8, ctypes.byref(n), None) == tq.TQ_ERR_INVALID_ARG
     c = ctypes.c_int()
-    assert st("tq_decode_chunk", None, 16, 32, 8, 16 * 1000, 1000, ctypes.byref(c)) == tq.TQ_ERR_INVALID_ARG
+    assert st("tq_decode_chunk", None, 16, 32, 8, 16 * 1000, 1000, 0, ctypes.byref(c)) == tq.TQ_ERR_INVALID_ARG
