@@ -135,11 +135,12 @@ int pick_chunk(int units, int max_seq_len) {
 }
 
 // Chunk for the persistent kernel (one warp per chunk, chunks taken from a
-// counter): the busiest warp handles ceil(items / slots) chunks; minimise that
-// times (chunk + a per-chunk cost of about 32 tokens), chunks of >= 256
-// tokens.  items = H * sum_b ceil(L_b / chunk), estimated from the total length
+// counter, ctas x 12 or 16 warp slots): the busiest warp handles
+// ceil(items / slots) chunks; minimise lut_cost, that times (chunk + a
+// per-chunk cost of about 32 tokens) times the warps per CTA (a warp's speed
+// scales as their inverse), over both warp counts, chunks of >= 256 tokens.  items = H * sum_b ceil(L_b / chunk), estimated from the total length
 // (each sequence adds half a chunk of rounding), at most every sequence full.
-int pick_chunk_total(int batch, int H, long long total_tokens, int max_seq_len, int slots) {
+int pick_chunk_total(int batch, int H, long long total_tokens, int max_seq_len, int ctas) {
   long long best_cost = -1;
   int best_chunk = ((max_seq_len + kPage - 1) / kPage) * kPage;
   if (best_chunk < kPage) best_chunk = kPage;
@@ -151,7 +152,7 @@ int pick_chunk_total(int batch, int H, long long total_tokens, int max_seq_len, 
     const long long full = static_cast<long long>(batch) * ((max_seq_len + chunk - 1) / chunk);
     const long long est = (total_tokens + chunk - 1) / chunk + batch / 2;
     const long long items = static_cast<long long>(H) * (est < full ? est : full);
-    const long long cost = ((items + slots - 1) / slots) * (chunk + 32);
+    const long long cost = std::min(lut_cost(items, ctas, 12, chunk + 32), lut_cost(items, ctas, 16, chunk + 32));
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best_chunk = static_cast<int>(chunk);
@@ -162,7 +163,7 @@ int pick_chunk_total(int batch, int H, long long total_tokens, int max_seq_len, 
 
 // Chunk for the persistent kernel when only max_seq_len is known: every
 // sequence assumed full (see pick_chunk_total, per-chunk cost 64 tokens).
-int pick_chunk_warps(int units, int max_seq_len, int slots) {
+int pick_chunk_warps(int units, int max_seq_len, int ctas) {
   long long best_cost = -1;
   int best_chunk = ((max_seq_len + kPage - 1) / kPage) * kPage;
   if (best_chunk < kPage) best_chunk = kPage;
@@ -173,7 +174,7 @@ int pick_chunk_warps(int units, int max_seq_len, int slots) {
     if (chunk < 256 && nch > 1) break;
     const long long real = (max_seq_len + chunk - 1) / chunk;
     const long long items = real * units;
-    const long long cost = ((items + slots - 1) / slots) * (chunk + 64);
+    const long long cost = std::min(lut_cost(items, ctas, 12, chunk + 64), lut_cost(items, ctas, 16, chunk + 64));
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best_chunk = static_cast<int>(chunk);
@@ -449,10 +450,10 @@ extern "C" tq_status tq_decode_chunk(const tq_ctx* ctx, int batch, int Hq, int H
   if (!ctx || !chunk_tokens || batch < 1 || Hq < 1 || H < 1 || Hq % H || max_seq_len < 0 || total_tokens < 0 ||
       total_tokens > static_cast<long long>(batch) * max_seq_len)
     return TQ_ERR_INVALID_ARG;
-  int slots = lut_decode_slots(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H);
-  if (fused_append && slots > 0) slots = slots / sm_count() * (sm_count() - append_reserve(batch, H));
-  if (slots > 0)
-    *chunk_tokens = pick_chunk_total(batch, H, total_tokens, max_seq_len, slots);
+  int ctas = lut_decode_ctas(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H);
+  if (fused_append && ctas > 0) ctas -= append_reserve(batch, H);
+  if (ctas > 0)
+    *chunk_tokens = pick_chunk_total(batch, H, total_tokens, max_seq_len, ctas);
   else
     *chunk_tokens = pick_chunk(batch * H, max_seq_len);
   return TQ_OK;
@@ -495,10 +496,10 @@ tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batc
   if (batch == 0) return TQ_OK;
   if (!q || !seq_lens || !block_table || !k_cache || !v_cache || !out || !workspace)
     return TQ_ERR_INVALID_ARG;
-  int lut_slots = lut_decode_slots(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H);
-  if (fused && lut_slots > 0) lut_slots = lut_slots / sm_count() * (sm_count() - fused->reserve);
+  int lut_ctas = lut_decode_ctas(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H);
+  if (fused && lut_ctas > 0) lut_ctas -= fused->reserve;
   int chunk = chunk_tokens              ? chunk_tokens
-              : lut_slots > 0           ? pick_chunk_warps(batch * H, max_seq_len, lut_slots)
+              : lut_ctas > 0            ? pick_chunk_warps(batch * H, max_seq_len, lut_ctas)
                                         : pick_chunk(batch * H, max_seq_len);
   int nch = nchunks_for(max_seq_len, chunk);
   const int d = ctx->cfg.d, m = ctx->cfg.m;

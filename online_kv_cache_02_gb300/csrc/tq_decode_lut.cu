@@ -43,13 +43,16 @@
 namespace tq {
 namespace {
 
-constexpr int kWarpsL = 16;
-constexpr int kThreadsL = 32 * kWarpsL;
+// Warps per CTA: 16, or 12 with deeper rings and up to 168 registers per
+// thread; lut_warps_for picks per launch (tq_internal.h).
 constexpr int kMaxStagesL = 4;         // ring depth per warp: the largest <= this that fits
 constexpr float kInvSqrtD = 0.08838834764831845f;
 constexpr float kSqrtHalfPi = 1.2533141373155003f;
 constexpr int kWaitLimit = 1 << 22;
 constexpr float kNegBig = -1.0e30f;    // finite "minus infinity" (see tq_decode_mma.cu)
+// Slack of the running softmax max (log2 units): p <= 8, and 8 * 65504 / sqrt(128)
+// is below the fp16 maximum, so no fp16 value norm can overflow P'.
+constexpr float kLazyMax = 3.0f;
 constexpr int kSmemLimit = 232448;     // opt-in shared memory per block
 
 // ---------------------------------------------------------------------------
@@ -63,7 +66,7 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -203,7 +206,7 @@ struct Slot {
   int pad;
 };
 
-template <int KBH, int KBL, int VBH, int VBL, bool QJL>
+template <int W, int KBH, int KBL, int VBH, int VBL, bool QJL>
 struct Geo {
   static constexpr int CBK = (64 * KBH + 64 * KBL) / 8;
   static constexpr int CBV = (64 * VBH + 64 * VBL) / 8;
@@ -218,12 +221,12 @@ struct Geo {
   static constexpr int R1 = region_bytes(KBL, VBL);
   static constexpr int TABLES = R0 + R1;
   // per warp: ring, then (in the extras block) S barriers, S slots, a 256-byte P tile
-  __host__ __device__ static constexpr int extras(int st) { return kWarpsL * (st * 8 + st * 16 + 256); }
+  __host__ __device__ static constexpr int extras(int st) { return W * (st * 8 + st * 16 + 256); }
   // the tables start at a 64 KiB-aligned shared address; the gap below them
   // takes whole warp rings, so at most one ring (or, when every ring fits in
   // the gap, the rest of the gap) is lost to the alignment
   __host__ __device__ static constexpr int rings_plus_gap(int st) {
-    return (kWarpsL + 1) * st * STAGE > 65536 ? (kWarpsL + 1) * st * STAGE : 65536;
+    return (W + 1) * st * STAGE > 65536 ? (W + 1) * st * STAGE : 65536;
   }
   __host__ __device__ static constexpr int need(int st) { return TABLES + rings_plus_gap(st) + extras(st) + 1024; }
   static constexpr int STAGES = need(kMaxStagesL) <= kSmemLimit ? kMaxStagesL
@@ -246,9 +249,9 @@ __device__ __forceinline__ uint32_t lds_at(uint32_t addr) {
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int KBH, int KBL, int VBH, int VBL, bool QJL>
-__global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a, int total_items) {
-  using Gm = Geo<KBH, KBL, VBH, VBL, QJL>;
+template <int W, int KBH, int KBL, int VBH, int VBL, bool QJL>
+__global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, int total_items) {
+  using Gm = Geo<W, KBH, KBL, VBH, VBL, QJL>;
   constexpr int S = Gm::STAGES;
   extern __shared__ __align__(1024) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -257,8 +260,8 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
   // ---- layout: tables at the first 64 KiB boundary, rings around them ------
   const uint32_t base = smem_u32(smem);
   const uint32_t tab = (base + 0xFFFFu) & ~0xFFFFu;
-  const int n_low = min(kWarpsL, static_cast<int>((tab - base) / Gm::RINGW));   // rings below the tables
-  const uint32_t ext = tab + Gm::TABLES + (kWarpsL - n_low) * Gm::RINGW;
+  const int n_low = min(W, static_cast<int>((tab - base) / Gm::RINGW));   // rings below the tables
+  const uint32_t ext = tab + Gm::TABLES + (W - n_low) * Gm::RINGW;
   if (ext + Gm::extras(S) > base + Gm::SMEM) {          // cannot happen with the sizes above
     if (threadIdx.x == 0) atomicOr(a.tab.err, kErrLayout);
     return;
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
   // ---- tables (once per CTA) ------------------------------------------------
   {
     constexpr int E0 = Gm::R0 / 256, E1 = Gm::R1 / 256;
-    for (int i = threadIdx.x; i < (E0 + E1) * 16; i += kThreadsL) {
+    for (int i = threadIdx.x; i < (E0 + E1) * 16; i += 32 * W) {
       const int quad = i & 7, which = (i >> 3) & 1;
       int e = i >> 4;
       const int region = e < E0 ? 0 : 1;
@@ -281,8 +284,8 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
   }
   unsigned char* ring = at(warp < n_low ? base + warp * Gm::RINGW : tab + Gm::TABLES + (warp - n_low) * Gm::RINGW);
   unsigned long long* bars = reinterpret_cast<unsigned long long*>(at(ext)) + warp * S;
-  Slot* slots = reinterpret_cast<Slot*>(at(ext + kWarpsL * S * 8)) + warp * S;
-  __half(*ptile)[16] = reinterpret_cast<__half(*)[16]>(at(ext + kWarpsL * S * 24 + warp * 256));
+  Slot* slots = reinterpret_cast<Slot*>(at(ext + W * S * 8)) + warp * S;
+  __half(*ptile)[16] = reinterpret_cast<__half(*)[16]>(at(ext + W * S * 24 + warp * 256));
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(smem_u32(&bars[s]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -460,7 +463,10 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
       const unsigned char* vb = kb + Gm::KBB;
       const int pbase = c_t0 + sl.page * kPage;
       // ---- scores ---------------------------------------------------------
+      // two accumulators per score (channel group / even-odd projection
+      // steps) halve the dependent HMMA chains
       float s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+      float s1b[4] = {0.f, 0.f, 0.f, 0.f}, s2b[4] = {0.f, 0.f, 0.f, 0.f};
       {
         const uint32_t* ra = reinterpret_cast<const uint32_t*>(kb + g * Gm::CBK);
         const uint32_t* rb = reinterpret_cast<const uint32_t*>(kb + (g + 8) * Gm::CBK);
@@ -470,7 +476,8 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
         k_slice<KBL>(ra + 2 * KBH, t, xa1);
         k_slice<KBL>(rb + 2 * KBH, t, xb1);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int q = 0; q < 8; ++q) {
+          const int kk = (q >> 1) + 4 * (q & 1);   // alternate the two channel groups
           const int j0 = 2 * (kk & 3), j1 = j0 + 1;
           const uint32_t* xa = kk < 4 ? xa0 : xa1;
           const uint32_t* xb = kk < 4 ? xb0 : xb1;
@@ -488,15 +495,20 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
             a2 = lds_at<OFF1>(prmt(xa[j1 >> 2], lbk1, s1x));
             a3 = lds_at<OFF1>(prmt(xb[j1 >> 2], lbk1, s1x));
           }
-          mma16816(s1, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
+          mma16816(kk < 4 ? s1 : s1b, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
         }
         if (QJL) {
           const uint32_t* sg = reinterpret_cast<const uint32_t*>(kb + Gm::K_SIGNS);
           const uint32_t na = ~sg[g * 4 + t], nb = ~sg[(g + 8) * 4 + t];
 #pragma unroll
           for (int st = 0; st < 8; ++st)
-            mma16816(s2, sign_pair(na, 2 * st), sign_pair(nb, 2 * st), sign_pair(na, 2 * st + 1),
+            mma16816((st & 1) ? s2b : s2, sign_pair(na, 2 * st), sign_pair(nb, 2 * st), sign_pair(na, 2 * st + 1),
                      sign_pair(nb, 2 * st + 1), uf[2 * st], uf[2 * st + 1]);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          s1[r] += s1b[r];
+          s2[r] += s2b[r];
         }
       }
       const __half* nk = reinterpret_cast<const __half*>(kb + Gm::K_NORM);
@@ -514,23 +526,24 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
         lg[3] = vg8 ? fmaf(nkg8 * k1, s1[3], rkg8 * k2 * s2[3]) : kNegBig;
       }
       // ---- online softmax over this page (heads 2t, 2t+1) -------------------
-      float pr[4], alpha[2];
+      // The running max m only has to bound the logits: it moves (a warp-wide
+      // max and a rescale of l and acc) only when some logit of the warp lies
+      // more than kLazyMax above it, so p = 2^(lg - m) <= 2^kLazyMax and
+      // P' = p n_v / sqrt(d) stays finite in fp16 for every fp16 norm n_v.
+      if (__any_sync(0xffffffffu, fmaxf(lg[0], lg[2]) > m_run[0] + kLazyMax ||
+                                      fmaxf(lg[1], lg[3]) > m_run[1] + kLazyMax)) {
+        float alpha[2];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float mx = fmaxf(lg[c], lg[c + 2]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float m_new = fmaxf(m_run[c], mx);
-        alpha[c] = fast_exp2(m_run[c] - m_new);
-        pr[c] = fast_exp2(lg[c] - m_new);
-        pr[c + 2] = fast_exp2(lg[c + 2] - m_new);
-        l_run[c] = fmaf(l_run[c], alpha[c], pr[c] + pr[c + 2]);
-        m_run[c] = m_new;
-      }
-      // the running max rarely moves once a chunk is under way: rescale only
-      // when it moved for some head of the warp
-      if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+        for (int c = 0; c < 2; ++c) {
+          float mx = fmaxf(lg[c], lg[c + 2]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float m_new = fmaxf(m_run[c], mx);
+          alpha[c] = fast_exp2(m_run[c] - m_new);
+          l_run[c] *= alpha[c];
+          m_run[c] = m_new;
+        }
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
           acc[mt][0] *= alpha[0];
@@ -538,6 +551,13 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
           acc[mt][1] *= alpha[1];
           acc[mt][3] *= alpha[1];
         }
+      }
+      float pr[4];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        pr[c] = fast_exp2(lg[c] - m_run[c]);
+        pr[c + 2] = fast_exp2(lg[c + 2] - m_run[c]);
+        l_run[c] += pr[c] + pr[c + 2];
       }
       // ---- P' = p * nv / sqrt(d) into the transposed shared tile -------------
       {
@@ -587,7 +607,7 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
   __syncwarp();
   if (lane == 0) {
     __threadfence();
-    const int total_warps = gridDim.x * kWarpsL;
+    const int total_warps = gridDim.x * W;
     if (atomicAdd(a.sched + 1, 1) == total_warps - 1) {
       a.sched[0] = 0;
       a.sched[1] = 0;
@@ -596,16 +616,22 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_partials_kernel(DecodeArgs a
   }
 }
 
-template <int KBH, int KBL, int VBH, int VBL, bool QJL>
-cudaError_t launch_lut(const DecodeArgs& a, int items, cudaStream_t s) {
-  using Gm = Geo<KBH, KBL, VBH, VBL, QJL>;
+template <int W, int KBH, int KBL, int VBH, int VBL, bool QJL>
+cudaError_t launch_lut(const DecodeArgs& a, int items, int grid, cudaStream_t s) {
+  using Gm = Geo<W, KBH, KBL, VBH, VBL, QJL>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(lut_partials_kernel<KBH, KBL, VBH, VBL, QJL>,
+    cudaError_t e = cudaFuncSetAttribute(lut_partials_kernel<W, KBH, KBL, VBH, VBL, QJL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  lut_partials_kernel<W, KBH, KBL, VBH, VBL, QJL><<<grid, 32 * W, Gm::SMEM, s>>>(a, items);
+  return cudaGetLastError();
+}
+
+template <int KBH, int KBL, int VBH, int VBL>
+cudaError_t launch_lut_q(const DecodeArgs& a, int items, cudaStream_t s) {
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -614,13 +640,11 @@ cudaError_t launch_lut(const DecodeArgs& a, int items, cudaStream_t s) {
   // without a chunk exits at once, and every SM's copy engines are in use
   const int cap = a.max_ctas > 0 && a.max_ctas < sms ? a.max_ctas : sms;
   const int grid = items < cap ? (items > 0 ? items : 1) : cap;
-  lut_partials_kernel<KBH, KBL, VBH, VBL, QJL><<<grid, kThreadsL, Gm::SMEM, s>>>(a, items);
-  return cudaGetLastError();
-}
-
-template <int KBH, int KBL, int VBH, int VBL>
-cudaError_t launch_lut_q(const DecodeArgs& a, int items, cudaStream_t s) {
-  return a.kl.qjl ? launch_lut<KBH, KBL, VBH, VBL, true>(a, items, s) : launch_lut<KBH, KBL, VBH, VBL, false>(a, items, s);
+  if (lut_warps_for(items, cap) == 12)
+    return a.kl.qjl ? launch_lut<12, KBH, KBL, VBH, VBL, true>(a, items, grid, s)
+                    : launch_lut<12, KBH, KBL, VBH, VBL, false>(a, items, grid, s);
+  return a.kl.qjl ? launch_lut<16, KBH, KBL, VBH, VBL, true>(a, items, grid, s)
+                  : launch_lut<16, KBH, KBL, VBH, VBL, false>(a, items, grid, s);
 }
 
 int combo_code(const KindLayout& kl, const KindLayout& vl) {
@@ -629,7 +653,7 @@ int combo_code(const KindLayout& kl, const KindLayout& vl) {
 
 }  // namespace
 
-int lut_decode_slots(const KindLayout& kl, const KindLayout& vl, int m, int G) {
+int lut_decode_ctas(const KindLayout& kl, const KindLayout& vl, int m, int G) {
   if (m != 128 || kl.split != 64 || vl.split != 64 || G > 8) return 0;
   switch (combo_code(kl, vl)) {
     case 3333: case 4343: case 3232: case 4444: case 2222: case 4422: break;
@@ -637,11 +661,20 @@ int lut_decode_slots(const KindLayout& kl, const KindLayout& vl, int m, int G) {
   }
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  return sms * kWarpsL;
+  return sms;
+}
+
+long long lut_cost(long long items, int ctas, int warps, long long chunk_cost) {
+  const long long slots = static_cast<long long>(ctas > 0 ? ctas : 1) * warps;
+  return (items + slots - 1) / slots * chunk_cost * warps;
+}
+
+int lut_warps_for(long long items, int ctas) {
+  return lut_cost(items, ctas, 12, 1) < lut_cost(items, ctas, 16, 1) ? 12 : 16;
 }
 
 bool launch_partials_lut(const DecodeArgs& a, cudaStream_t s, cudaError_t* err) {
-  if (!lut_decode_slots(a.kl, a.vl, a.m, a.G) || !a.sched || !a.qfrag) return false;
+  if (!lut_decode_ctas(a.kl, a.vl, a.m, a.G) || !a.sched || !a.qfrag) return false;
   if ((reinterpret_cast<uintptr_t>(a.kc) | reinterpret_cast<uintptr_t>(a.vc)) & 15) return false;
   if ((a.k_page_bytes | a.v_page_bytes) & 15) return false;
   const long long items = static_cast<long long>(a.B) * a.H * a.nchunks;

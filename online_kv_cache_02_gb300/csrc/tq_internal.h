@@ -131,9 +131,16 @@ cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
 bool launch_quantize_tc(const QuantizeArgs& k, const QuantizeArgs& v, cudaStream_t s, cudaError_t* err);
 cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s);
 bool launch_partials_mma(const DecodeArgs& a, cudaStream_t s, cudaError_t* err);
-// Persistent lookup-table kernel (tq_decode_lut.cu): warp slots it runs with
-// (0: configuration not supported), and its launch (false: not supported).
-int lut_decode_slots(const KindLayout& kl, const KindLayout& vl, int m, int G);
+// Persistent lookup-table kernel (tq_decode_lut.cu): CTAs it runs with at
+// most, one per SM (0: configuration not supported), and its launch (false:
+// not supported).  A launch runs 12 or 16 warps per CTA: every warp takes
+// whole split-K items (chunks of one KV head) from a shared counter, a warp's
+// speed scales as 1/warps per CTA, so lut_cost (waves of items over the warp
+// slots x per-item cost x warps) estimates the time and lut_warps_for picks
+// the cheaper count.
+int lut_decode_ctas(const KindLayout& kl, const KindLayout& vl, int m, int G);
+long long lut_cost(long long items, int ctas, int warps, long long chunk_cost);
+int lut_warps_for(long long items, int ctas);
 bool launch_partials_lut(const DecodeArgs& a, cudaStream_t s, cudaError_t* err);
 
 }  // namespace tq

@@ -89,6 +89,15 @@ def test_decode_chunking_is_invisible(chunk):
     _check(w, [1000, 1, 16, 33], Hq=4, H=1, chunk=chunk, seed=3)
 
 
+@pytest.mark.parametrize("chunk", [16, 64])
+def test_decode_both_warp_counts(chunk):
+    """The persistent kernel runs 16 warps per CTA when the items (chunks x KV heads x sequences) fill more
+    than one wave of 12-warp CTAs but one of 16-warp CTAs (chunk 16: 2000 items), else 12 (chunk 64: 500
+    items); both agree with the oracle on the same 3.5-bit inputs."""
+    w = BASE.scaled(dtype="bf16", k_bits=(4, 3), v_bits=(4, 3))
+    _check(w, [8000, 7990], Hq=8, H=2, chunk=chunk, seed=6)
+
+
 def test_decode_empty_and_single_token_sequences():
     w = BASE.scaled(dtype="f32")
     lens = [0, 1, 2, 0]
