@@ -105,10 +105,12 @@ __global__ void __launch_bounds__(kQThreads) qprep_kernel(DecodeArgs a) {
       lo = 16 * t + k_pair_channel(a.kl.g[y].bits, 2 * (kk & 3) + e);
       hi = lo + 1;
     } else {
+      // u pair p = 2 st + h: projections 16h + st and 16h + 8 + st of word t,
+      // the sign bits the kernel's prmt places in the pair at step st
       const int t = 2 * (y - 2) + (k >> 4), p = k & 15;
       word = 32 * t + 16 + p;
-      lo = 32 * t + p - 64 * (y - 2);
-      hi = lo + 16;
+      lo = 32 * t + 16 * (p & 1) + (p >> 1) - 64 * (y - 2);
+      hi = lo + 8;
     }
     a.qfrag[(r0 + h) * 128 + word] = static_cast<uint32_t>(__half_as_ushort(hs[h][lo])) |
                                      (static_cast<uint32_t>(__half_as_ushort(hs[h][hi])) << 16);

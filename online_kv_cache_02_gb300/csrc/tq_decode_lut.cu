@@ -20,8 +20,10 @@
 // channel of two consecutive tokens (two tokens' codes interleaved by lop3),
 // the layout the value MMA wants.  3-bit octets are first gathered into eight
 // nibbles (channels 6 and 7 sit in the spare bit of each nibble).
-//   * scores: S1 = K^ Q~^T and S2 = sign * U^T, m16n8k16 with the 16 tokens on
-//     M and the G <= 8 query heads of the KV head on N (K = channels);
+//   * scores: S1 = K^ Q~^T and S2 = (1 + c b) U^T, m16n8k16 with the 16 tokens on
+//     M and the G <= 8 query heads of the KV head on N (K = channels, or the m
+//     projections); the sign bits b become fp16 1 or 1 + c (c = 255/1024) by one
+//     prmt per pair, and <u, 2b - 1> = (2/c) S2 - (2/c + 1) sum(u);
 //   * logits = (n_k/sqrt(d) S1 + sqrt(pi/2)/m rho S2) * scale; online softmax
 //     on the accumulator fragments;
 //   * P' = p * n_v / sqrt(d) through a 256-byte shared tile into the B operand
@@ -194,9 +196,13 @@ __host__ __device__ constexpr int v_channel(int b, int mt) {
                 : (mt < 4 ? 2 * mt : 2 * (mt - 4) + 1);
 }
 
-// QJL sign pair (projections k, k+16 of a 32-bit word): +1.0 if the bit is set, else -1.0.
-__device__ __forceinline__ uint32_t sign_pair(uint32_t notw, int k) {
-  return ((notw << (15 - k)) & 0x80008000u) | 0x3C003C00u;
+// QJL sign pair for the MMA from xs = w << (7 - s): bits s + 16h and s + 8 + 16h
+// of the sign word w as the fp16 pair (1 + kQjlC b, 1 + kQjlC b'), b = bit:
+// prmt's sign-replicate selectors copy a byte's top bit into the low byte of
+// each half (0xFF or 0), the high byte is 0x3C (1.0).
+constexpr float kQjlC = 255.0f / 1024.0f;
+__device__ __forceinline__ uint32_t qjl_pair(uint32_t xs, int h) {
+  return prmt(xs, 0x3C3C3C3Cu, h ? 0x4B4Au : 0x4948u);
 }
 
 struct Slot {
@@ -374,6 +380,7 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
   const float k2 = kSqrtHalfPi / 128.0f * a.scale_log2;
   int cur = -1, c_b = 0, c_h = 0, c_chunk = 0, c_t0 = 0, c_t1 = 0;
   uint32_t qf[16], uf[16];
+  float kqa, kqb[2];       // QJL logit terms: <u, +-1> = (2/c) raw - (2/c + 1) sum(u), times k2
   float acc[8][4];
   float m_run[2], l_run[2];
   bool failed = false;
@@ -421,6 +428,25 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
     } else {
 #pragma unroll
       for (int v = 0; v < 16; ++v) qf[v] = uf[v] = 0u;
+    }
+    if (QJL) {
+      // sum of head g's u (the fp16 values the MMA multiplies), then the sums
+      // of heads 2t, 2t+1 for this thread's accumulator columns
+      float su = 0.0f;
+#pragma unroll
+      for (int v = 0; v < 16; ++v) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&uf[v]));
+        su += f.x + f.y;
+      }
+      su += __shfl_xor_sync(0xffffffffu, su, 1);
+      su += __shfl_xor_sync(0xffffffffu, su, 2);
+      const float su0 = __shfl_sync(0xffffffffu, su, (2 * t) << 2);
+      const float su1 = __shfl_sync(0xffffffffu, su, (2 * t + 1) << 2);
+      kqa = k2 * (2.0f / kQjlC);
+      kqb[0] = -k2 * (2.0f / kQjlC + 1.0f) * su0;
+      kqb[1] = -k2 * (2.0f / kQjlC + 1.0f) * su1;
+    } else {
+      kqa = kqb[0] = kqb[1] = 0.0f;
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -499,11 +525,13 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
         }
         if (QJL) {
           const uint32_t* sg = reinterpret_cast<const uint32_t*>(kb + Gm::K_SIGNS);
-          const uint32_t na = ~sg[g * 4 + t], nb = ~sg[(g + 8) * 4 + t];
+          const uint32_t wa = sg[g * 4 + t], wb = sg[(g + 8) * 4 + t];
 #pragma unroll
-          for (int st = 0; st < 8; ++st)
-            mma16816((st & 1) ? s2b : s2, sign_pair(na, 2 * st), sign_pair(nb, 2 * st), sign_pair(na, 2 * st + 1),
-                     sign_pair(nb, 2 * st + 1), uf[2 * st], uf[2 * st + 1]);
+          for (int st = 0; st < 8; ++st) {
+            const uint32_t xa = wa << (7 - st), xb = wb << (7 - st);
+            mma16816((st & 1) ? s2b : s2, qjl_pair(xa, 0), qjl_pair(xb, 0), qjl_pair(xa, 1), qjl_pair(xb, 1),
+                     uf[2 * st], uf[2 * st + 1]);
+          }
         }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
@@ -520,10 +548,10 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
       {
         const float nkg = __half2float(nk[g]), nkg8 = __half2float(nk[g + 8]);
         const float rkg = QJL ? __half2float(rk[g]) : 0.f, rkg8 = QJL ? __half2float(rk[g + 8]) : 0.f;
-        lg[0] = vg ? fmaf(nkg * k1, s1[0], rkg * k2 * s2[0]) : kNegBig;
-        lg[1] = vg ? fmaf(nkg * k1, s1[1], rkg * k2 * s2[1]) : kNegBig;
-        lg[2] = vg8 ? fmaf(nkg8 * k1, s1[2], rkg8 * k2 * s2[2]) : kNegBig;
-        lg[3] = vg8 ? fmaf(nkg8 * k1, s1[3], rkg8 * k2 * s2[3]) : kNegBig;
+        lg[0] = vg ? fmaf(nkg * k1, s1[0], rkg * fmaf(kqa, s2[0], kqb[0])) : kNegBig;
+        lg[1] = vg ? fmaf(nkg * k1, s1[1], rkg * fmaf(kqa, s2[1], kqb[1])) : kNegBig;
+        lg[2] = vg8 ? fmaf(nkg8 * k1, s1[2], rkg8 * fmaf(kqa, s2[2], kqb[0])) : kNegBig;
+        lg[3] = vg8 ? fmaf(nkg8 * k1, s1[3], rkg8 * fmaf(kqa, s2[3], kqb[1])) : kNegBig;
       }
       // ---- online softmax over this page (heads 2t, 2t+1) -------------------
       // The running max m only has to bound the logits: it moves (a warp-wide

@@ -474,7 +474,9 @@ template <int KBH, int KBL, int VBH, int VBL>
 __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArgs ka, QuantizeArgs va, int nk_tiles,
                                                                      int nv_tiles) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // aligned by an offset on the shared array itself, so that every access
+  // through smem stays a shared-memory access (not a generic one)
+  unsigned char* smem = smem_raw + ((0u - smem_u32(smem_raw)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   Cell* cells = reinterpret_cast<Cell*>(smem + kOffCells);
   unsigned char* misc = smem + kOffMisc4;
