@@ -243,6 +243,20 @@ __device__ __forceinline__ void clear_code_q(uint32_t (&w)[4], int c) {
   }
 }
 
+// Code of channel c of a quarter from its words (rare paths; any bit width).
+__device__ int quarter_code(const uint32_t (&w)[4], int b, int c) {
+  auto bitsat = [&](int pos, int n) { return static_cast<int>((w[pos >> 5] >> (pos & 31)) & ((1u << n) - 1u)); };
+  if (b == 3) {
+    const int o = c >> 3, j = c & 7;
+    if (j < 6) return bitsat(24 * o + 4 * j, 3);
+    const int s0 = 24 * o + 3 + 4 * (j - 6);
+    return bitsat(s0, 1) | (bitsat(s0 + 8, 1) << 1) | (bitsat(s0 + 16, 1) << 2);
+  }
+  const int v = bitsat(b * c, b);
+  if (b == 4) return (v & 8) ? 7 - (v & 7) : 8 + v;
+  return v;
+}
+
 // Code of channel j of a stored record (rare paths; any bit width).  Reads go
 // to L2: the words may have been patched by atomics of other warps.
 __device__ int record_code(const uint32_t* cw, int bh, int bl, int j) {
@@ -313,10 +327,12 @@ __device__ __forceinline__ DF df_sq(float x) {
 
 // Exact code of channel ch (warp-cooperative): y = (Pi_ch hi + lo) . x and
 // ||x||^2 in double-float, u = sqrt(d) y/||x|| compared with the fp64
-// boundaries.  Lane 0 patches the stored code when it differs and, for keys,
+// boundaries.  Lane 0 patches the stored code (the fast path's code `old`,
+// stored before a block barrier) when it differs and, for keys,
 // the residual tiles and the residual norm partial.
 __device__ __noinline__ void refine_code_item(const void* xrow, bool f32, const float* pidf_row, uint32_t* cw, int bh,
-                                              int bl, int ch, const double* t64, int nb, const float* cent, bool key,
+                                              int bl, int ch, int old, const double* t64, int nb, const float* cent,
+                                              bool key,
                                               float n16f, unsigned char* smem, float* rho2_slot, int row, int lane,
                                               unsigned long long* counter) {
   float xv[4];
@@ -338,7 +354,6 @@ __device__ __noinline__ void refine_code_item(const void* xrow, bool f32, const 
   int code = 0;
   for (int k = 0; k < nb; ++k) code += u64 >= t64[k];
   atomicAdd(counter, 1ULL);
-  const int old = record_code(cw, bh, bl, ch);
   if (code == old) return;
   patch_code(cw, bh, bl, ch, old, code);
   if (key && n16f > 0.0f) {          // with a zero fp16 norm the residual does not use the code
@@ -746,6 +761,7 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
     const int bh = key ? KBH : VBH, bl = key ? KBL : VBL;
     uint32_t* const cp = codeptr[row];
     uint32_t near = 0;
+    uint32_t words[4] = {0u, 0u, 0u, 0u};   // this quarter's codes as stored
     {
       const float inv = 1.0f / (xs_scale * kPiScale);
       const float ku = nf > 0.0f ? inv * (kSqrtD / nf) : 0.0f;
@@ -753,7 +769,6 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
       // gives the same signs), so it is formed without the centroids
       const float kr = n16f > 0.0f ? inv * (kSqrtD / n16f) : ku;
       const float sub = n16f > 0.0f ? 1.0f : 0.0f;
-      uint32_t words[4] = {0u, 0u, 0u, 0u};
       uint32_t rh[16], rl[16];
       float rho2 = 0.0f;
       float v[32];
@@ -789,9 +804,8 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
     }
 
     // ---- 3b. exact re-decision of flagged codes (rare; whole CTA) -----------
+    // (the block barrier orders the stored words before the patches: no fence)
     if (__syncthreads_or(near != 0)) {
-      __threadfence();           // stored words reach L2 before the patches
-      __syncthreads();
       uint32_t mine = near;
       for (;;) {
         while (mine) {
@@ -799,15 +813,17 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
           if (idx >= kQueueCap) break;
           const int c = __ffs(mine) - 1;
           mine &= mine - 1;
-          queue[idx] = static_cast<uint32_t>(row) | (static_cast<uint32_t>(32 * q + c) << 8);
+          const uint32_t old = static_cast<uint32_t>(quarter_code(words, grp ? bl : bh, c));
+          queue[idx] = static_cast<uint32_t>(row) | (static_cast<uint32_t>(32 * q + c) << 8) | (old << 16);
         }
         __syncthreads();
         const int n = min(*qn, kQueueCap);
         for (int i = warp; i < n; i += kThreadsTC4 / 32) {
-          const int r = static_cast<int>(queue[i] & 255u), ch = static_cast<int>(queue[i] >> 8);
+          const int r = static_cast<int>(queue[i] & 255u), ch = static_cast<int>((queue[i] >> 8) & 255u);
+          const int old = static_cast<int>(queue[i] >> 16);
           const int gs = (key ? 0 : 2) + (ch < 64 ? 0 : 1);
           const int b = ch < 64 ? bh : bl;
-          refine_code_item(xrow_of(r), f32, a.tab.pi_df + ch * kD * 2, codeptr[r], bh, bl, ch,
+          refine_code_item(xrow_of(r), f32, a.tab.pi_df + ch * kD * 2, codeptr[r], bh, bl, ch, old,
                            t64s + gs * 16, (1 << b) - 1, cents + gs * 16, sk, rown16[r], smem, &red_r[r], r, lane,
                            &a.tab.counters[0]);
         }
@@ -815,7 +831,6 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
         if (tid == 0) *qn = 0;
         if (!__syncthreads_or(mine != 0)) break;
       }
-      __threadfence();
     }
 
     // ---- 4. keys: z = r' S^T and the sign bits -------------------------------
@@ -861,8 +876,6 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
         if (sp) sp[q] = word;
       }
       if (__syncthreads_or(nearz != 0)) {
-        __threadfence();
-        __syncthreads();
         uint32_t mine = nearz;
         for (;;) {
           while (mine) {
