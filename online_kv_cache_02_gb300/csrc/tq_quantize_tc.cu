@@ -245,7 +245,11 @@ __device__ __forceinline__ void clear_code_q(uint32_t (&w)[4], int c) {
 
 // Code of channel c of a quarter from its words (rare paths; any bit width).
 __device__ int quarter_code(const uint32_t (&w)[4], int b, int c) {
-  auto bitsat = [&](int pos, int n) { return static_cast<int>((w[pos >> 5] >> (pos & 31)) & ((1u << n) - 1u)); };
+  auto bitsat = [&](int pos, int n) {     // word by selects: no runtime index into w (kept in registers)
+    const int k = pos >> 5;
+    const uint32_t x = k == 0 ? w[0] : k == 1 ? w[1] : k == 2 ? w[2] : w[3];
+    return static_cast<int>((x >> (pos & 31)) & ((1u << n) - 1u));
+  };
   if (b == 3) {
     const int o = c >> 3, j = c & 7;
     if (j < 6) return bitsat(24 * o + 4 * j, 3);
@@ -443,11 +447,14 @@ __device__ void build_cells(Cell* cells, const GroupBook& gb, int idx) {
 constexpr int kOffCells = 196608;                 // 4 groups x 256 cells x 16 B
 constexpr int kOffMisc4 = kOffCells + 4 * kCells * 16;
 
-// Epilogue of one quarter (32 channels of group width B) of one row.
+// Epilogue of one quarter (32 channels of group width B) of one row: codes,
+// the smallest |u - t| (the caller builds the near-boundary mask when it is
+// under the guard, rarely) and, for keys, the residual as fp16 hi + lo pairs.
 template <int B, bool KEY>
 __device__ __forceinline__ void quarter_epilogue(const float (&v)[32], const Cell* cells, float ku, float kr,
-                                                 float sub, uint32_t (&words)[4], uint32_t& near, float& rho2,
+                                                 float sub, uint32_t (&words)[4], float& dmin, float& rho2,
                                                  uint32_t (&rh)[16], uint32_t (&rl)[16]) {
+  float r_even = 0.0f;
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
     const float u = v[c] * ku;
@@ -455,20 +462,20 @@ __device__ __forceinline__ void quarter_epilogue(const float (&v)[32], const Cel
     const float4 cell = reinterpret_cast<const float4*>(cells)[g];
     const bool ge = u >= cell.x;
     const int code = __float_as_int(cell.y) + (ge ? 1 : 0);
-    near |= (fabsf(u - cell.x) < kCodeGuard ? 1u : 0u) << c;
+    dmin = fminf(dmin, fabsf(u - cell.x));
     put_code_q<B>(words, c, static_cast<uint32_t>(code));
     if (KEY) {
       const float r = fmaf(v[c], kr, -sub * (ge ? cell.w : cell.z));
       rho2 = fmaf(r, r, rho2);
-      const __half hh = __float2half_rn(r);
-      const __half hl = __float2half_rn(r - __half2float(hh));
-      const uint32_t sh = (c & 1) ? 16u : 0u;
-      if (!(c & 1)) {
-        rh[c >> 1] = 0u;
-        rl[c >> 1] = 0u;
+      if (c & 1) {
+        const __half2 h = __floats2half2_rn(r_even, r);
+        const float2 hf = __half22float2(h);
+        const __half2 l = __floats2half2_rn(r_even - hf.x, r - hf.y);
+        rh[c >> 1] = *reinterpret_cast<const uint32_t*>(&h);
+        rl[c >> 1] = *reinterpret_cast<const uint32_t*>(&l);
+      } else {
+        r_even = r;
       }
-      rh[c >> 1] |= static_cast<uint32_t>(__half_as_ushort(hh)) << sh;
-      rl[c >> 1] |= static_cast<uint32_t>(__half_as_ushort(hl)) << sh;
     }
   }
 }
@@ -761,6 +768,7 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
     const int bh = key ? KBH : VBH, bl = key ? KBL : VBL;
     uint32_t* const cp = codeptr[row];
     uint32_t near = 0;
+    float dmin = INFINITY;
     uint32_t words[4] = {0u, 0u, 0u, 0u};   // this quarter's codes as stored
     {
       const float inv = 1.0f / (xs_scale * kPiScale);
@@ -775,14 +783,26 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
       tmem_ld32(trow + 32 * q, v);
       const Cell* cg = cells + gslot * kCells;
       if (sk) {
-        if (grp == 0) quarter_epilogue<KBH, true>(v, cg, ku, kr, sub, words, near, rho2, rh, rl);
-        else quarter_epilogue<KBL, true>(v, cg, ku, kr, sub, words, near, rho2, rh, rl);
+        if (grp == 0) quarter_epilogue<KBH, true>(v, cg, ku, kr, sub, words, dmin, rho2, rh, rl);
+        else quarter_epilogue<KBL, true>(v, cg, ku, kr, sub, words, dmin, rho2, rh, rl);
       } else if (key) {
-        if (grp == 0) quarter_epilogue<KBH, false>(v, cg, ku, kr, sub, words, near, rho2, rh, rl);
-        else quarter_epilogue<KBL, false>(v, cg, ku, kr, sub, words, near, rho2, rh, rl);
+        if (grp == 0) quarter_epilogue<KBH, false>(v, cg, ku, kr, sub, words, dmin, rho2, rh, rl);
+        else quarter_epilogue<KBL, false>(v, cg, ku, kr, sub, words, dmin, rho2, rh, rl);
       } else {
-        if (grp == 0) quarter_epilogue<VBH, false>(v, cg, ku, kr, sub, words, near, rho2, rh, rl);
-        else quarter_epilogue<VBL, false>(v, cg, ku, kr, sub, words, near, rho2, rh, rl);
+        if (grp == 0) quarter_epilogue<VBH, false>(v, cg, ku, kr, sub, words, dmin, rho2, rh, rl);
+        else quarter_epilogue<VBL, false>(v, cg, ku, kr, sub, words, dmin, rho2, rh, rl);
+      }
+      // near-boundary mask from the tensor-memory values again (warp-uniform:
+      // the load is collective; a row whose dmin passed gets no bits)
+      if (__any_sync(0xffffffffu, dmin < kCodeGuard)) {
+        float w2[32];
+        tmem_ld32(trow + 32 * q, w2);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float u = w2[c] * ku;
+          const int g = min(max(__float2int_rd(fmaf(u, 16.0f, 128.0f)), 0), kCells - 1);
+          near |= (fabsf(u - cg[g].t) < kCodeGuard ? 1u : 0u) << c;
+        }
       }
       if (!valid || nf == 0.0f || !cp) near = 0;
       if (sk) {
