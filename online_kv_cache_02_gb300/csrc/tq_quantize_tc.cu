@@ -886,10 +886,15 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
         tmem_ld32(trow + 128 + 32 * q, v);
         const float guard = kSignGuard * rho;
         uint32_t word = 0;
+        float amin = INFINITY;
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           word |= ((~__float_as_uint(v[k])) >> 31) << k;
-          nearz |= (fabsf(v[k]) < guard ? 1u : 0u) << k;
+          amin = fminf(amin, fabsf(v[k]));
+        }
+        if (__any_sync(0xffffffffu, amin < guard)) {     // rare: the near-zero mask
+#pragma unroll
+          for (int k = 0; k < 32; ++k) nearz |= (fabsf(v[k]) < guard ? 1u : 0u) << k;
         }
         uint32_t* const sp = signptr[row];
         if (!sp) nearz = 0;
