@@ -14,7 +14,9 @@ from .gpu_common import (alloc_caches, ctx_for, gpu_decode, oracle, oracle_cache
 pytestmark = pytest.mark.gpu
 
 
-def _oracle_setup(w, lens, H, seed):
+def _oracle_setup(w, lens, H, seed, kv=None):
+    """Oracle-quantized caches for sequences of the given lengths; kv = (K, V) [B, L, H, 128] fp32 replaces
+    the seeded N(0,1) draws."""
     rng = np.random.default_rng(seed)
     B = len(lens)
     pps = max(1, (int(max(lens)) + 15) // 16)
@@ -27,9 +29,12 @@ def _oracle_setup(w, lens, H, seed):
         L = int(lens[b])
         if L == 0:
             continue
-        K = rng.standard_normal((L, H, 128)).astype(np.float32)
-        K[..., :w.outlier_channels] *= w.outlier_scale
-        V = rng.standard_normal((L, H, 128)).astype(np.float32)
+        if kv is None:
+            K = rng.standard_normal((L, H, 128)).astype(np.float32)
+            K[..., :w.outlier_channels] *= w.outlier_scale
+            V = rng.standard_normal((L, H, 128)).astype(np.float32)
+        else:
+            K, V = kv[0][b, :L].astype(np.float32), kv[1][b, :L].astype(np.float32)
         if w.dtype == "bf16":
             K, V = wl.bf16_round(K), wl.bf16_round(V)
         pages, slots, heads = seq_locations(bt, b, np.arange(L), H)
@@ -38,11 +43,12 @@ def _oracle_setup(w, lens, H, seed):
     return p, bt, num_pages, kc, vc
 
 
-def _check(w, lens, Hq, H, chunk=0, scale=None, seed=0, qdtype=None):
+def _check(w, lens, Hq, H, chunk=0, scale=None, seed=0, qdtype=None, kv=None, Q=None, tol=None):
     lens = np.asarray(lens, dtype=np.int32)
-    p, bt, num_pages, kc, vc = _oracle_setup(w, lens, H, seed)
+    p, bt, num_pages, kc, vc = _oracle_setup(w, lens, H, seed, kv)
     rng = np.random.default_rng(seed + 100)
-    Q = rng.standard_normal((len(lens), Hq, 128)).astype(np.float32)
+    if Q is None:
+        Q = rng.standard_normal((len(lens), Hq, 128)).astype(np.float32)
     qd = qdtype or w.dtype
     if qd == "bf16":
         Q = wl.bf16_round(Q)
@@ -60,7 +66,8 @@ def _check(w, lens, Hq, H, chunk=0, scale=None, seed=0, qdtype=None):
     # The bar is 2e-3 at the standard scale 1/sqrt(d).  The tensor-core path rounds q~ and the
     # centroids to fp16 (relative 2^-12 each), so its logit error grows with the scale: above
     # 1/sqrt(d) the bar is 2e-3 * scale * sqrt(d).
-    tol = th.ATT_TOL * max(1.0, scale * np.sqrt(128))
+    if tol is None:
+        tol = th.ATT_TOL * max(1.0, scale * np.sqrt(128))
     assert err.max() <= tol, (err.max(), np.unravel_index(err.argmax(), err.shape))
     return err.max()
 
@@ -90,12 +97,40 @@ def test_decode_chunking_is_invisible(chunk):
 
 
 @pytest.mark.parametrize("chunk", [16, 64])
-def test_decode_both_warp_counts(chunk):
+@pytest.mark.parametrize("qjl", [True, False])
+def test_decode_both_warp_counts(chunk, qjl):
     """The persistent kernel runs 16 warps per CTA when the items (chunks x KV heads x sequences) fill more
     than one wave of 12-warp CTAs but one of 16-warp CTAs (chunk 16: 2000 items), else 12 (chunk 64: 500
-    items); both agree with the oracle on the same 3.5-bit inputs."""
-    w = BASE.scaled(dtype="bf16", k_bits=(4, 3), v_bits=(4, 3))
+    items); both agree with the oracle on the same 3.5-bit inputs, with and without the QJL term."""
+    w = BASE.scaled(dtype="bf16", k_bits=(4, 3), v_bits=(4, 3), qjl=qjl)
     _check(w, [8000, 7990], Hq=8, H=2, chunk=chunk, seed=6)
+
+
+def test_decode_running_max_moves_within_chunks():
+    """Logits that climb along the sequence (keys = noise + a ramp along query head 0's direction, 0 -> ~9 nats
+    over each 1024-token chunk for that head, ramps of random sign and size for the other heads) and a late spike
+    13 nats above everything before it: the running softmax max moves many times inside every chunk, several
+    times by more than the kernel's 2^3 slack.  Bar: the standard 2e-3 (a missed or wrong rescale changes
+    weights by 8x or more)."""
+    w = BASE.scaled(dtype="bf16", k_bits=(4, 3), v_bits=(4, 3))
+    rng = np.random.default_rng(77)
+    B, H, Hq, L = 2, 2, 8, 3072
+    Q = wl.bf16_round(rng.standard_normal((B, Hq, 128)).astype(np.float32))
+    K = 0.3 * rng.standard_normal((B, L, H, 128)).astype(np.float32)
+    V = rng.standard_normal((B, L, H, 128)).astype(np.float32)
+    G = Hq // H
+    t = np.arange(L)
+    ramp = 9.0 * (t % 1024) / 1024.0                       # nats, restarting at each chunk
+    for b in range(B):
+        for h in range(H):
+            qd = Q[b, h * G] / np.linalg.norm(Q[b, h * G])
+            amp = ramp * np.sqrt(128) / np.linalg.norm(Q[b, h * G])     # key length giving `ramp` nats
+            amp[L - 40] = 22.0 * np.sqrt(128) / np.linalg.norm(Q[b, h * G])
+            K[b, :, h, :] += amp[:, None] * qd[None, :]
+    K, V = wl.bf16_round(K), wl.bf16_round(V)
+    logits = np.einsum("bhd,blhd->bhl", Q.reshape(B, H, G, 128)[:, :, 0], K) / np.sqrt(128)
+    assert logits.max() > 20.0 and np.ptp(logits[:, :, :1024]) > 8.0     # the intended shape
+    _check(w, [L, L - 7], Hq=Hq, H=H, chunk=1024, seed=7, kv=(K, V), Q=Q, tol=th.ATT_TOL)
 
 
 def test_decode_empty_and_single_token_sequences():
