@@ -96,14 +96,15 @@ def test_decode_chunking_is_invisible(chunk):
     _check(w, [1000, 1, 16, 33], Hq=4, H=1, chunk=chunk, seed=3)
 
 
-@pytest.mark.parametrize("chunk", [16, 64])
+@pytest.mark.parametrize("lens,chunk", [([8000, 7990], 64), ([8000, 7990], 16)])
 @pytest.mark.parametrize("qjl", [True, False])
-def test_decode_both_warp_counts(chunk, qjl):
-    """The persistent kernel runs 16 warps per CTA when the items (chunks x KV heads x sequences) fill more
-    than one wave of 12-warp CTAs but one of 16-warp CTAs (chunk 16: 2000 items), else 12 (chunk 64: 500
-    items); both agree with the oracle on the same 3.5-bit inputs, with and without the QJL term."""
+def test_decode_warp_counts(lens, chunk, qjl):
+    """The persistent kernel runs 12 or 16 warps per CTA, whichever costs least for the launch's items
+    (chunks x KV heads x sequences; on 152 SMs: 500 items -> 12, 2000 -> 16, which fill one wave of 16-warp
+    CTAs but not of 12-warp ones); both agree with the oracle on the same 3.5-bit inputs, with and without the
+    QJL term."""
     w = BASE.scaled(dtype="bf16", k_bits=(4, 3), v_bits=(4, 3), qjl=qjl)
-    _check(w, [8000, 7990], Hq=8, H=2, chunk=chunk, seed=6)
+    _check(w, lens, Hq=8, H=2, chunk=chunk, seed=6)
 
 
 def test_decode_running_max_moves_within_chunks():
