@@ -46,21 +46,25 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // [q~; u] = W q with W = [Pi; S Pi] (fp32, built once at create time): a
-// block takes 16 query heads x 64 outputs; its 32 KB slice of W^T arrives in
-// one round of independent 16-byte loads, then thread t computes output t%64
-// for heads 4(t/64) .. 4(t/64)+3 from shared memory.
-constexpr int kQP = 16;
+// block takes 32 query heads x 64 outputs; its 32 KB slice of W^T arrives in
+// one round of independent 16-byte loads (dynamic shared memory), then each
+// of the 128 threads computes a 4 heads x 4 outputs tile (one 16-byte W load
+// and four broadcast q loads per 16 FMAs), every output summed over k in order.
+constexpr int kQP = 32;
 constexpr int kQO = 64;
-constexpr int kQThreads = 256;
+constexpr int kQThreads = 128;
+constexpr int kQPad = kD + 4;                   // q rows, padded
+constexpr int kQprepSmem = (kD * kQO + kQP * kQPad) * 4;
 
 __global__ void __launch_bounds__(kQThreads) qprep_kernel(DecodeArgs a) {
-  __shared__ __align__(16) float ws[kD][kQO];
-  __shared__ float qs[kQP][kD];
+  extern __shared__ __align__(16) float qsm[];
+  float(*ws)[kQO] = reinterpret_cast<float(*)[kQO]>(qsm);
+  float(*qs)[kQPad] = reinterpret_cast<float(*)[kQPad]>(qsm + kD * kQO);
   const int nout = kD + a.m;
   const long long r0 = static_cast<long long>(blockIdx.x) * kQP;
   const int c0 = blockIdx.y * kQO;
   const long long nq = static_cast<long long>(a.B) * a.Hq;
-  const int tid = threadIdx.x, o = tid & (kQO - 1), h0 = 4 * (tid >> 6);
+  const int tid = threadIdx.x, oq = 4 * (tid & 15), h0 = 4 * (tid >> 4);
   if (blockIdx.x == 0 && blockIdx.y == 0 && tid < 2 && a.sched) a.sched[tid] = 0;   // partials work counters
 #pragma unroll
   for (int it = 0; it < kD * kQO / 4 / kQThreads; ++it) {
@@ -74,17 +78,29 @@ __global__ void __launch_bounds__(kQThreads) qprep_kernel(DecodeArgs a) {
     qs[r][c] = r0 + r < nq ? load_q(a.q, a.f32, (r0 + r) * kD + c) : 0.0f;
   }
   __syncthreads();
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-  for (int k = 0; k < kD; ++k) {
-    const float w = ws[k][o];
+  float acc[4][4];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) acc[r] = fmaf(w, qs[h0 + r][k], acc[r]);
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.0f;
+#pragma unroll 4
+  for (int k = 0; k < kD; ++k) {
+    const float4 w = *reinterpret_cast<const float4*>(&ws[k][oq]);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float qv = qs[h0 + r][k];
+      acc[r][0] = fmaf(w.x, qv, acc[r][0]);
+      acc[r][1] = fmaf(w.y, qv, acc[r][1]);
+      acc[r][2] = fmaf(w.z, qv, acc[r][2]);
+      acc[r][3] = fmaf(w.w, qv, acc[r][3]);
+    }
   }
-  if (c0 + o < nout) {
+  if (c0 + oq < nout) {
 #pragma unroll
     for (int r = 0; r < 4; ++r)
-      if (r0 + h0 + r < nq) a.qprep[(r0 + h0 + r) * nout + c0 + o] = acc[r];
+      if (r0 + h0 + r < nq)
+        *reinterpret_cast<float4*>(a.qprep + (r0 + h0 + r) * nout + c0 + oq) =
+            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
   }
   if (!a.qfrag || a.m != kD) return;
   // fp16 fragments of the persistent partials kernel: this block's 64 outputs
@@ -92,7 +108,9 @@ __global__ void __launch_bounds__(kQThreads) qprep_kernel(DecodeArgs a) {
   // 0/1 for every lane t; slice 2/3: u pairs of lanes t = 0,1 / 2,3)
   __shared__ __half hs[kQP][kQO];
 #pragma unroll
-  for (int r = 0; r < 4; ++r) hs[h0 + r][o] = __float2half_rn(acc[r]);
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) hs[h0 + r][oq + c] = __float2half_rn(acc[r][c]);
   __syncthreads();
   const int y = blockIdx.y;
   for (int idx = tid; idx < kQP * 32; idx += kQThreads) {
@@ -465,7 +483,13 @@ cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
   if (stages & TQ_STAGE_QPREP) {
     const dim3 grid(static_cast<unsigned>((static_cast<long long>(a.B) * a.Hq + kQP - 1) / kQP),
                     static_cast<unsigned>((kD + a.m + kQO - 1) / kQO));
-    qprep_kernel<<<grid, kQThreads, 0, s>>>(a);
+    static bool configured = false;      // the W slice and q rows take 49 KB of dynamic shared memory
+    if (!configured) {
+      e = cudaFuncSetAttribute(qprep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQprepSmem);
+      if (e != cudaSuccess) return e;
+      configured = true;
+    }
+    qprep_kernel<<<grid, kQThreads, kQprepSmem, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
