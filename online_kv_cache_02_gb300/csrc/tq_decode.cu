@@ -425,9 +425,10 @@ __global__ void __launch_bounds__(kMThreads) merge_kernel(DecodeArgs a) {
   L = L > a.maxp * kPage ? a.maxp * kPage : L;
   const int nc = min(a.nchunks, (L + a.chunk - 1) / a.chunk);
   const float* P = a.part + row * a.nchunks * (kD + 2);
-  const float lg_new = a.new_token ? new_token_logit(a, row, vnew, red) : -INFINITY;
+  // the chunk maxima are requested before the new token is scored
   float M = -INFINITY;
   for (int c = tid; c < nc; c += kMThreads) M = fmaxf(M, P[static_cast<long long>(c) * (kD + 2)]);
+  const float lg_new = a.new_token ? new_token_logit(a, row, vnew, red) : -INFINITY;
   M = fmaxf(block_reduce<kMThreads>(M, true, red), lg_new);
   const float w_new = lg_new > -INFINITY ? exp2f(lg_new - M) : 0.0f;
   float lpart = 0.0f, A0 = 0.0f, A1 = 0.0f;
