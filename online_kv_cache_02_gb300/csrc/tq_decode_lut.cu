@@ -6,10 +6,11 @@
 // codebook is only looked up at run time), §4.3 (stage-1 score plus the 1-bit
 // QJL correction; softmax(QK^T/sqrt(d))); [P2] "생각정리 209 (TurboQuant)", stage 2.
 //
-// One CTA of 16 warps per SM.  A work item is one (sequence, KV head, chunk);
-// each warp takes items from a global counter and streams their 16-token pages
-// through its own 3-stage ring (cp.async.bulk, mbarrier completion); the ring
-// runs on across item boundaries, so a warp never drains between items.
+// One CTA of 12 or 16 warps per SM (chosen per launch).  A work item is one
+// (sequence, KV head, chunk); each warp takes items from a global counter and
+// streams their 16-token pages through its own ring of 3-4 stages
+// (cp.async.bulk, mbarrier completion); the ring runs on across item
+// boundaries, so a warp never drains between items.
 //
 // Dequantization is a table lookup: one byte of packed codes (two codes) indexes
 // a table whose entry is the fp16 pair of their centroids.  Each entry is
