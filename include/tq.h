@@ -66,17 +66,26 @@ typedef enum {
 
 typedef enum { TQ_BF16 = 0, TQ_F32 = 1 } tq_dtype;
 
+/* Density the Lloyd-Max codebooks are fitted to, in unit-variance units
+ * u = sqrt(d) y / ||x||: N(0,1) (the high-d limit), or the exact density of a
+ * coordinate of a uniformly rotated vector, f(u) ~ (1 - u^2/d)^((d-3)/2) on
+ * |u| < sqrt(d) ([P4] §4.2: a Beta distribution, close to Gaussian at high d). */
+#define TQ_CODEBOOK_GAUSSIAN 0
+#define TQ_CODEBOOK_SPHERE 1
+
 /* Method configuration.  d = 128 and page_size = 16 are the supported
  * values.  Bits per channel in [1, 4]; channels [0, split) of the rotated
  * vector use bits_hi, channels [split, d) bits_lo; split is a multiple of 32.
  * m (QJL projections) is a multiple of 32 in [32, 128].  k_qjl = 0 gives
- * MSE-only keys (no signs, no residual norm stored). */
+ * MSE-only keys (no signs, no residual norm stored).  codebook: one of the
+ * TQ_CODEBOOK_* densities (tq_config_init: TQ_CODEBOOK_GAUSSIAN). */
 typedef struct {
   int d, m, page_size;
   int k_bits_hi, k_bits_lo, k_split;
   int v_bits_hi, v_bits_lo, v_split;
   int k_qjl;
   uint64_t seed;
+  int codebook;
 } tq_config;
 
 typedef struct tq_ctx tq_ctx;   /* opaque; immutable after creation */
@@ -107,6 +116,9 @@ tq_status tq_cache_layout(const tq_ctx* ctx, int num_kv_heads,
 tq_status tq_host_rotation(int d, uint64_t seed, double* pi);
 tq_status tq_host_qjl(int m, int d, uint64_t seed, double* s);
 tq_status tq_host_codebook(int bits, double* centroids, double* boundaries);
+/* The codebook for `density` (TQ_CODEBOOK_*) at dimension d (d >= 4; d is
+ * ignored for the Gaussian density). */
+tq_status tq_host_codebook_ex(int bits, int d, int density, double* centroids, double* boundaries);
 
 /* Online quantize-and-append ([P2] stages 1-2; [P4] §4.1-§4.3, §3.1).
  * k, v (device): [batch][n_new][num_kv_heads][d] in `dtype`; either may be

@@ -26,12 +26,16 @@ tq_status check_config(const tq_config* c) {
   if (c->k_split < 0 || c->k_split > c->d || c->k_split % 32) return TQ_ERR_INVALID_ARG;
   if (c->v_split < 0 || c->v_split > c->d || c->v_split % 32) return TQ_ERR_INVALID_ARG;
   if (c->k_qjl != 0 && c->k_qjl != 1) return TQ_ERR_INVALID_ARG;
+  if (c->codebook != TQ_CODEBOOK_GAUSSIAN && c->codebook != TQ_CODEBOOK_SPHERE) return TQ_ERR_INVALID_ARG;
   return TQ_OK;
 }
 
-void fill_group(GroupBook& g, int bits) {
+void fill_group(GroupBook& g, int bits, int density, int d) {
   double c[256], t[256];
-  codebook_fill(bits, c, t);
+  if (density == TQ_CODEBOOK_SPHERE)
+    codebook_fill_sphere(bits, d, c, t);
+  else
+    codebook_fill(bits, c, t);
   g.bits = bits;
   g.nb = (1 << bits) - 1;
   for (int k = 0; k < 16; ++k) {
@@ -44,9 +48,10 @@ void fill_group(GroupBook& g, int bits) {
   }
 }
 
-void fill_layout(KindLayout& L, int bits_hi, int bits_lo, int split, int d, int m, bool key, bool qjl) {
-  fill_group(L.g[0], bits_hi);
-  fill_group(L.g[1], bits_lo);
+void fill_layout(KindLayout& L, int bits_hi, int bits_lo, int split, int d, int m, bool key, bool qjl,
+                 int density) {
+  fill_group(L.g[0], bits_hi, density, d);
+  fill_group(L.g[1], bits_lo, density, d);
   L.split = split;
   L.code_bytes = (split * bits_hi + (d - split) * bits_lo) / 8;
   L.qjl = (key && qjl) ? 1 : 0;
@@ -195,6 +200,7 @@ extern "C" tq_status tq_config_init(tq_config* cfg, int d, int b, int m, uint64_
   cfg->k_split = cfg->v_split = d / 2;
   cfg->k_qjl = 1;
   cfg->seed = seed;
+  cfg->codebook = TQ_CODEBOOK_GAUSSIAN;
   return check_config(cfg);
 }
 
@@ -217,8 +223,8 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
   if (!ctx->fused_mu) { delete ctx; return TQ_ERR_OOM; }
   ctx->cfg = *cfg;
   if (cudaGetDevice(&ctx->device) != cudaSuccess) { delete ctx; return TQ_ERR_CUDA; }
-  fill_layout(ctx->kl, cfg->k_bits_hi, cfg->k_bits_lo, cfg->k_split, d, m, true, cfg->k_qjl != 0);
-  fill_layout(ctx->vl, cfg->v_bits_hi, cfg->v_bits_lo, cfg->v_split, d, m, false, false);
+  fill_layout(ctx->kl, cfg->k_bits_hi, cfg->k_bits_lo, cfg->k_split, d, m, true, cfg->k_qjl != 0, cfg->codebook);
+  fill_layout(ctx->vl, cfg->v_bits_hi, cfg->v_bits_lo, cfg->v_split, d, m, false, false, cfg->codebook);
 
   std::vector<double> pi(static_cast<size_t>(d) * d), s(static_cast<size_t>(m) * d);
   rotation_fill(d, cfg->seed, pi.data());

@@ -1,5 +1,6 @@
 // Host-side construction of the method's fixed tables: the random rotation
-// Pi, the QJL projection S and the Gaussian Lloyd-Max codebooks.
+// Pi, the QJL projection S and the Lloyd-Max codebooks (for N(0,1), or for the
+// exact density of a rotated coordinate, [P4] §4.2's Beta distribution).
 //
 // [P4] riverfrot.github.io "TurboQuant란 무엇이며…", §4.1: multiply every KV
 // vector by one data-oblivious random orthogonal matrix; §4.2: a Lloyd-Max
@@ -130,6 +131,97 @@ void codebook_fill(int bits, double* centroids, double* boundaries) {
   }
 }
 
+// Regularized incomplete beta I_x(a, b): the continued fraction of
+// Abramowitz & Stegun 26.5.8 evaluated by the modified Lentz method, used
+// directly below x = (a+1)/(a+b+2) and through I_x(a,b) = 1 - I_{1-x}(b,a)
+// above it (where the fraction converges fast).
+static double beta_cf(double a, double b, double x) {
+  const double tiny = 1e-300;
+  double c = 1.0, dd = 1.0 - (a + b) * x / (a + 1.0);
+  if (std::fabs(dd) < tiny) dd = tiny;
+  dd = 1.0 / dd;
+  double f = dd;
+  for (int m = 1; m <= 100000; ++m) {
+    const double m2 = 2.0 * m;
+    double num = m * (b - m) * x / ((a + m2 - 1.0) * (a + m2));      // d_{2m}
+    dd = 1.0 + num * dd;
+    if (std::fabs(dd) < tiny) dd = tiny;
+    dd = 1.0 / dd;
+    c = 1.0 + num / c;
+    if (std::fabs(c) < tiny) c = tiny;
+    f *= dd * c;
+    num = -(a + m) * (a + b + m) * x / ((a + m2) * (a + m2 + 1.0));   // d_{2m+1}
+    dd = 1.0 + num * dd;
+    if (std::fabs(dd) < tiny) dd = tiny;
+    dd = 1.0 / dd;
+    c = 1.0 + num / c;
+    if (std::fabs(c) < tiny) c = tiny;
+    const double del = dd * c;
+    f *= del;
+    if (std::fabs(del - 1.0) < 4e-16) break;             // a couple of ulps of 1
+  }
+  return f;
+}
+static double reg_inc_beta(double a, double b, double x) {
+  if (x <= 0.0) return 0.0;
+  if (x >= 1.0) return 1.0;
+  const double front =
+      std::exp(std::lgamma(a + b) - std::lgamma(a) - std::lgamma(b) + a * std::log(x) + b * std::log1p(-x));
+  if (x < (a + 1.0) / (a + b + 2.0)) return front * beta_cf(a, b, x) / a;
+  return 1.0 - front * beta_cf(b, a, 1.0 - x) / b;
+}
+
+// Lloyd-Max for the density of u = sqrt(d) x_1, x uniform on the unit sphere
+// of R^d (the coordinate of a randomly rotated vector in unit-variance units):
+// f(u) proportional to (1 - u^2/d)^((d-3)/2) on |u| < sqrt(d).  Same sweep as
+// the Gaussian case on the positive half: with z = u/sqrt(d), the upper tail
+// P(Z >= z) = I_{1-z^2}((d-1)/2, 1/2) / 2 and the partial first moment
+// E[Z; Z >= z] = C (1 - z^2)^((d-1)/2) / (d-1), C = Gamma(d/2) /
+// (sqrt(pi) Gamma((d-1)/2)), so a cell's conditional mean is closed form.
+void codebook_fill_sphere(int bits, int d, double* centroids, double* boundaries) {
+  const int h = 1 << (bits - 1);
+  const double rd = std::sqrt(static_cast<double>(d));
+  const double ca = 0.5 * (d - 1), cb = 0.5;
+  const double cmom = std::exp(std::lgamma(0.5 * d) - std::lgamma(0.5 * (d - 1))) / std::sqrt(M_PI) / (d - 1);
+  auto tail = [&](double u) {                 // P(U >= u), u >= 0
+    const double z = u / rd;
+    return z >= 1.0 ? 0.0 : 0.5 * reg_inc_beta(ca, cb, 1.0 - z * z);
+  };
+  auto moment = [&](double u) {               // E[Z; Z >= z], z = u/sqrt(d) (times sqrt(d): E[U; U >= u])
+    const double z = u / rd;
+    return z >= 1.0 ? 0.0 : cmom * std::pow(1.0 - z * z, 0.5 * (d - 1));
+  };
+  std::vector<double> a(h), lo(h), nx(h);
+  for (int k = 0; k < h; ++k) a[k] = (k + 0.5) * 3.0 / h;
+  for (int it = 0; it < 200000; ++it) {
+    lo[0] = 0.0;
+    for (int k = 1; k < h; ++k) lo[k] = 0.5 * (a[k - 1] + a[k]);
+    double delta = 0.0;
+    for (int k = 0; k < h; ++k) {
+      const bool open = (k == h - 1);
+      const double l = lo[k], hi = open ? rd : lo[k + 1];
+      const double num = rd * (moment(l) - (open ? 0.0 : moment(hi)));
+      const double den = tail(l) - (open ? 0.0 : tail(hi));
+      nx[k] = num / den;
+      delta = std::fmax(delta, std::fabs(nx[k] - a[k]));
+    }
+    a.swap(nx);
+    // the incomplete beta's rounding (about 1e-13 near its slow region) keeps
+    // the sweep from settling below ~1e-12 at 4 bits: accept that after 2000
+    if (delta <= 4e-15 || (it >= 2000 && delta < 1e-12)) break;
+  }
+  for (int k = 0; k < h; ++k) {
+    centroids[h + k] = a[k];
+    centroids[h - 1 - k] = -a[k];
+  }
+  boundaries[h - 1] = 0.0;
+  for (int k = 1; k < h; ++k) {
+    const double t = 0.5 * (a[k - 1] + a[k]);
+    boundaries[h - 1 + k] = t;
+    boundaries[h - 1 - k] = -t;
+  }
+}
+
 }  // namespace tq
 
 extern "C" tq_status tq_host_rotation(int d, uint64_t seed, double* pi) {
@@ -147,5 +239,16 @@ extern "C" tq_status tq_host_qjl(int m, int d, uint64_t seed, double* s) {
 extern "C" tq_status tq_host_codebook(int bits, double* centroids, double* boundaries) {
   if (!centroids || !boundaries || bits < 1 || bits > 8) return TQ_ERR_INVALID_ARG;
   tq::codebook_fill(bits, centroids, boundaries);
+  return TQ_OK;
+}
+
+extern "C" tq_status tq_host_codebook_ex(int bits, int d, int density, double* centroids, double* boundaries) {
+  if (!centroids || !boundaries || bits < 1 || bits > 8) return TQ_ERR_INVALID_ARG;
+  if (density == TQ_CODEBOOK_GAUSSIAN) {
+    tq::codebook_fill(bits, centroids, boundaries);
+    return TQ_OK;
+  }
+  if (density != TQ_CODEBOOK_SPHERE || d < 4) return TQ_ERR_INVALID_ARG;
+  tq::codebook_fill_sphere(bits, d, centroids, boundaries);
   return TQ_OK;
 }

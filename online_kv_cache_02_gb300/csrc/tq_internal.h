@@ -60,6 +60,7 @@ void gaussian_fill(uint64_t seed, uint64_t stream, size_t n, double* out);
 void rotation_fill(int d, uint64_t seed, double* pi);
 void qjl_fill(int m, int d, uint64_t seed, double* s);
 void codebook_fill(int bits, double* centroids, double* boundaries);
+void codebook_fill_sphere(int bits, int d, double* centroids, double* boundaries);
 
 // Device tables owned by a context.
 struct DeviceTables {

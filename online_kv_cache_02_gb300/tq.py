@@ -36,7 +36,7 @@ class TQConfig(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int), ("m", ctypes.c_int), ("page_size", ctypes.c_int),
                 ("k_bits_hi", ctypes.c_int), ("k_bits_lo", ctypes.c_int), ("k_split", ctypes.c_int),
                 ("v_bits_hi", ctypes.c_int), ("v_bits_lo", ctypes.c_int), ("v_split", ctypes.c_int),
-                ("k_qjl", ctypes.c_int), ("seed", ctypes.c_uint64)]
+                ("k_qjl", ctypes.c_int), ("seed", ctypes.c_uint64), ("codebook", ctypes.c_int)]
 
 
 def _load():
@@ -62,6 +62,7 @@ EXPORTS = {
     "tq_host_rotation": ([_I, _U64, _P], _S),
     "tq_host_qjl": ([_I, _I, _U64, _P], _S),
     "tq_host_codebook": ([_I, _P, _P], _S),
+    "tq_host_codebook_ex": ([_I, _I, _I, _P, _P], _S),
     "tq_quantize": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P], _S),
     "tq_workspace_size": ([_P, _I, _I, _I, _I, ctypes.POINTER(_SZ)], _S),
     "tq_decode_chunk": ([_P, _I, _I, _I, ctypes.c_longlong, _I, _I, ctypes.POINTER(_I)], _S),
@@ -120,8 +121,13 @@ def tq_config_init(d, b, m, seed):
     return cfg
 
 
-def make_config(k_bits=(3, 3), v_bits=(3, 3), m=128, seed=0, k_split=64, v_split=64, k_qjl=True, d=128):
-    return TQConfig(d, m, 16, k_bits[0], k_bits[1], k_split, v_bits[0], v_bits[1], v_split, int(k_qjl), seed)
+TQ_CODEBOOK_GAUSSIAN, TQ_CODEBOOK_SPHERE = 0, 1
+
+
+def make_config(k_bits=(3, 3), v_bits=(3, 3), m=128, seed=0, k_split=64, v_split=64, k_qjl=True, d=128,
+                codebook=TQ_CODEBOOK_GAUSSIAN):
+    return TQConfig(d, m, 16, k_bits[0], k_bits[1], k_split, v_bits[0], v_bits[1], v_split, int(k_qjl), seed,
+                    codebook)
 
 
 def tq_create(d, b, m, seed):
@@ -168,6 +174,13 @@ def tq_host_codebook(bits):
     c = np.empty(1 << bits, dtype=np.float64)
     t = np.empty((1 << bits) - 1 if bits > 0 else 1, dtype=np.float64)
     _check("tq_host_codebook", _lib.tq_host_codebook(bits, c.ctypes.data, t.ctypes.data))
+    return c, t
+
+
+def tq_host_codebook_ex(bits, d, density):
+    c = np.empty(1 << bits, dtype=np.float64)
+    t = np.empty((1 << bits) - 1 if bits > 0 else 1, dtype=np.float64)
+    _check("tq_host_codebook_ex", _lib.tq_host_codebook_ex(bits, d, density, c.ctypes.data, t.ctypes.data))
     return c, t
 
 

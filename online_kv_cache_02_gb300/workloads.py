@@ -48,6 +48,7 @@ class Workload:
     seed: int = 0
     chunk: int = 0            # split-K chunk tokens (0: library picks)
     append: bool = True       # decode step appends one new token per sequence first
+    codebook: str = "gaussian"   # density the codebooks are fitted to: "gaussian" or "sphere"
 
     def scaled(self, **kw):
         return replace(self, **kw)

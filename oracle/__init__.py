@@ -25,7 +25,7 @@ real model KV and are not reproducible here ("parity unpinned" for those only).
 
 from .rng import splitmix64_stream, uniform_stream, gaussian_stream
 from .turboquant import (
-    Codebook, lloyd_max_gaussian, rotation_matrix, qjl_matrix,
+    Codebook, lloyd_max_gaussian, lloyd_max_sphere, rotation_matrix, qjl_matrix,
     TQParams, make_params, quantize_vectors, estimate_scores,
     pack_k_records, pack_v_records, unpack_k_records, unpack_v_records,
     cache_block_bytes, write_paged, read_paged, decode_attention,
@@ -34,7 +34,7 @@ from .turboquant import (
 
 __all__ = [
     "splitmix64_stream", "uniform_stream", "gaussian_stream",
-    "Codebook", "lloyd_max_gaussian", "rotation_matrix", "qjl_matrix",
+    "Codebook", "lloyd_max_gaussian", "lloyd_max_sphere", "rotation_matrix", "qjl_matrix",
     "TQParams", "make_params", "quantize_vectors", "estimate_scores",
     "pack_k_records", "pack_v_records", "unpack_k_records", "unpack_v_records",
     "cache_block_bytes", "write_paged", "read_paged", "decode_attention",

@@ -138,6 +138,52 @@ def lloyd_max_gaussian(bits, tol=1e-15, max_iter=200000):
 _BOOKS = {}
 
 
+def lloyd_max_sphere(bits, d, tol=1e-15, max_iter=200000):
+    """Lloyd-Max 2**b-level quantizer for the exact density of one coordinate of
+    a randomly rotated vector in unit-variance units ([P4] §4.2: the rotated
+    coordinate follows a Beta distribution, close to N(0,1) at high d).
+
+    u = sqrt(d) z with z a coordinate of a uniform point on the unit sphere of
+    R^d, so z^2 ~ Beta(1/2, (d-1)/2).  For u >= 0:
+      P(U >= u)   = I_{1 - u^2/d}((d-1)/2, 1/2) / 2   (regularized incomplete beta),
+      E[U; U >= u] = sqrt(d) Gamma(d/2) / (sqrt(pi) Gamma((d-1)/2) (d-1)) (1 - u^2/d)^((d-1)/2).
+    The same two Lloyd conditions and positive-half iteration as
+    lloyd_max_gaussian; the last cell ends at sqrt(d).
+    """
+    if bits < 1 or d < 4:
+        raise ValueError("bits >= 1, d >= 4")
+    key = ("sphere", bits, d, tol, max_iter)
+    if key in _BOOKS:
+        return _BOOKS[key]
+    rd = math.sqrt(d)
+    cmom = rd * math.exp(special.gammaln(d / 2.0) - special.gammaln((d - 1) / 2.0)) / math.sqrt(math.pi) / (d - 1)
+
+    def tail(u):
+        z2 = np.minimum(u / rd, 1.0) ** 2
+        return 0.5 * special.betainc((d - 1) / 2.0, 0.5, 1.0 - z2)
+
+    def moment(u):
+        z2 = np.minimum(u / rd, 1.0) ** 2
+        return cmom * (1.0 - z2) ** ((d - 1) / 2.0)
+
+    h = 1 << (bits - 1)
+    a = (np.arange(h) + 0.5) * 3.0 / h
+    it = 0
+    for it in range(1, max_iter + 1):
+        lo = np.concatenate([[0.0], 0.5 * (a[:-1] + a[1:])])
+        hi = np.concatenate([lo[1:], [rd]])
+        new = (moment(lo) - moment(hi)) / (tail(lo) - tail(hi))
+        delta = np.max(np.abs(new - a))
+        a = new
+        if delta <= tol:
+            break
+    pos_t = 0.5 * (a[:-1] + a[1:])
+    centroids = np.concatenate([-a[::-1], a])
+    boundaries = np.concatenate([-pos_t[::-1], [0.0], pos_t])
+    _BOOKS[key] = Codebook(bits, centroids, boundaries, it)
+    return _BOOKS[key]
+
+
 # ---------------------------------------------------------------------------
 # Parameters
 # ---------------------------------------------------------------------------
@@ -165,11 +211,18 @@ class TQParams:
 
 
 def make_params(d=128, m=128, k_bits=(3, 3), k_split=64, v_bits=(3, 3), v_split=64,
-                seed=0, k_qjl=True):
-    """Everything the method draws or precomputes once: Pi, S and the codebooks."""
+                seed=0, k_qjl=True, codebook="gaussian"):
+    """Everything the method draws or precomputes once: Pi, S and the codebooks
+    (codebook "gaussian": N(0,1) Lloyd-Max; "sphere": the exact rotated-coordinate
+    density, lloyd_max_sphere)."""
     Pi = rotation_matrix(d, seed)
     S = qjl_matrix(m, d, seed)
-    books = {b: lloyd_max_gaussian(b) for b in set(k_bits) | set(v_bits)}
+    if codebook == "sphere":
+        books = {b: lloyd_max_sphere(b, d) for b in set(k_bits) | set(v_bits)}
+    elif codebook == "gaussian":
+        books = {b: lloyd_max_gaussian(b) for b in set(k_bits) | set(v_bits)}
+    else:
+        raise ValueError(codebook)
     return TQParams(d, m, tuple(k_bits), k_split, tuple(v_bits), v_split, bool(k_qjl),
                     int(seed), Pi, S, books)
 

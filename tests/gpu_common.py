@@ -17,7 +17,8 @@ SENTINEL = 0xA5
 
 def ctx_for(w, seed=None):
     cfg = tq.make_config(k_bits=w.k_bits, v_bits=w.v_bits, m=w.m, seed=w.seed if seed is None else seed,
-                         k_qjl=w.qjl)
+                         k_qjl=w.qjl,
+                         codebook=tq.TQ_CODEBOOK_SPHERE if w.codebook == "sphere" else tq.TQ_CODEBOOK_GAUSSIAN)
     return tq.tq_create_ex(cfg)
 
 

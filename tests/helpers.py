@@ -24,7 +24,7 @@ ATT_TOL = 2e-3
 
 def params_for(w, seed=None):
     return oracle.make_params(d=128, m=w.m, k_bits=w.k_bits, v_bits=w.v_bits, seed=w.seed if seed is None else seed,
-                              k_qjl=w.qjl)
+                              k_qjl=w.qjl, codebook=w.codebook)
 
 
 def locations(block_table, b_idx, pos, h_idx):

@@ -134,6 +134,14 @@ def test_decode_running_max_moves_within_chunks():
     _check(w, [L, L - 7], Hq=Hq, H=H, chunk=1024, seed=7, kv=(K, V), Q=Q, tol=th.ATT_TOL)
 
 
+@pytest.mark.parametrize("kb,vb", [((3, 3), (3, 3)), ((4, 3), (4, 3)), ((3, 2), (3, 2))])
+def test_decode_sphere_codebook(kb, vb):
+    """Codebooks fitted to the exact rotated-coordinate density: the decode tables take the context's
+    centroids, so the parity bar is the standard one."""
+    w = BASE.scaled(dtype="bf16", k_bits=kb, v_bits=vb, codebook="sphere")
+    _check(w, [700, 33, 1], Hq=8, H=2, chunk=0, seed=8)
+
+
 def test_decode_empty_and_single_token_sequences():
     w = BASE.scaled(dtype="f32")
     lens = [0, 1, 2, 0]

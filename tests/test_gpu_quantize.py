@@ -20,8 +20,9 @@ VARIANTS = [
 ]
 
 
-def _run_case(kb, vb, qjl, m, dtype, B=3, T=37, H=2, starts=(0, 5, 19), seed=11):
-    w = wl.Workload("t", "quantize", B, H, H, T, k_bits=kb, v_bits=vb, qjl=qjl, m=m, dtype=dtype, seed=seed)
+def _run_case(kb, vb, qjl, m, dtype, B=3, T=37, H=2, starts=(0, 5, 19), seed=11, codebook="gaussian"):
+    w = wl.Workload("t", "quantize", B, H, H, T, k_bits=kb, v_bits=vb, qjl=qjl, m=m, dtype=dtype, seed=seed,
+                    codebook=codebook)
     rng = np.random.default_rng(seed)
     pps = (max(starts) + T + 15) // 16
     num_pages = B * pps + 3
@@ -62,6 +63,13 @@ def _run_case(kb, vb, qjl, m, dtype, B=3, T=37, H=2, starts=(0, 5, 19), seed=11)
 @pytest.mark.parametrize("kb,vb,qjl,m,dtype", VARIANTS)
 def test_quantize_matches_oracle(kb, vb, qjl, m, dtype):
     _run_case(kb, vb, qjl, m, dtype)
+
+
+@pytest.mark.parametrize("kb,vb", [((3, 3), (3, 3)), ((4, 3), (4, 3)), ((4, 4), (2, 2)), ((1, 1), (1, 1))])
+def test_quantize_sphere_codebook(kb, vb):
+    """Codebooks fitted to the exact rotated-coordinate density: the same bit-exact record parity on the
+    tensor-core path (and the SIMT path for 1 bit)."""
+    _run_case(kb, vb, True, 128, "bf16", T=150, codebook="sphere")
 
 
 def test_quantize_many_tiles_ragged_tail():

@@ -59,6 +59,18 @@ def test_codebook_matches_oracle(tq, bits):
     assert t[(1 << bits) // 2 - 1] == 0.0
 
 
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_sphere_codebook_matches_oracle(tq, bits):
+    """The library's rotated-coordinate codebook (incomplete beta by a continued fraction) against the
+    oracle's (scipy's incomplete beta): equal to well inside the 1e-6 boundary band."""
+    c, t = tq.tq_host_codebook_ex(bits, 128, tq.TQ_CODEBOOK_SPHERE)
+    cb = oracle.lloyd_max_sphere(bits, 128)
+    assert np.max(np.abs(c - cb.centroids)) < 1e-11
+    assert np.max(np.abs(t - cb.boundaries)) < 1e-11
+    g, _ = tq.tq_host_codebook_ex(bits, 128, tq.TQ_CODEBOOK_GAUSSIAN)
+    assert np.array_equal(g, tq.tq_host_codebook(bits)[0])
+
+
 def test_status_strings(tq):
     for s in range(7):
         assert tq.tq_status_string(s)
@@ -78,6 +90,9 @@ def test_config_validation_without_gpu(tq):
     assert st("tq_create_ex", ctypes.byref(bad), ctypes.byref(out)) == tq.TQ_ERR_INVALID_ARG
     bad = tq.make_config(k_bits=(0, 3))
     assert st("tq_create_ex", ctypes.byref(bad), ctypes.byref(out)) == tq.TQ_ERR_INVALID_ARG
+    bad = tq.make_config(codebook=2)                  # not a TQ_CODEBOOK_* density
+    assert st("tq_create_ex", ctypes.byref(bad), ctypes.byref(out)) == tq.TQ_ERR_INVALID_ARG
+    assert cfg.codebook == tq.TQ_CODEBOOK_GAUSSIAN    # tq_config_init's default
     assert st("tq_create_ex", None, ctypes.byref(out)) == tq.TQ_ERR_INVALID_ARG
     assert out.value is None
 
