@@ -265,6 +265,29 @@ tq_status tq_refine_counters(const tq_ctx* ctx, unsigned long long out[2], int r
 
 const char* tq_status_string(tq_status status);
 
+/* Inner-product search over a quantized key database ([P2] "생각정리 209
+ * (TurboQuant)": the vector-search use; [P4] §4.3: the two-stage estimate is
+ * unbiased).  For every query i and database vector t the score is the
+ * decode's estimate of <q_i, x_t> without any softmax or scale,
+ *   (n16_t/sqrt(d)) <Pi q_i, c[code_t]> + sqrt(pi/2)/m rho16_t <S Pi q_i, +-1_t>,
+ * then the k_top largest per query, best first (equal scores: lower t first).
+ * The database is a K cache of ONE KV head written by tq_quantize (batch 1,
+ * num_kv_heads 1, start_pos 0, n_new = n_db): vector t is in page
+ * block_table[t / 16], slot t % 16 (device int32 [ceil(n_db/16)]); num_pages
+ * bounds the page ids (an id outside [0, num_pages) is skipped, its score is
+ * -inf and the device error word is set).  q: device [nq][d] in `dtype`.
+ * top_scores (fp32) and top_index (int32): device [nq][k_top].  Requires
+ * 1 <= k_top <= min(n_db, 1024); workspace (device, 16-byte aligned) of
+ * tq_search_workspace_size bytes holds the q~/u rows and the [nq][n_db]
+ * scores (fp32, in the workspace after them).  Stream-ordered; no allocation.
+ * Errors: null pointers, k_top out of range, n_db > 16 num_pages, misaligned
+ * buffers -> TQ_ERR_INVALID_ARG; a small workspace -> TQ_ERR_WORKSPACE. */
+tq_status tq_search_workspace_size(const tq_ctx* ctx, int nq, int n_db, size_t* bytes);
+tq_status tq_search(const tq_ctx* ctx, const void* q, tq_dtype dtype, int nq, const void* k_cache,
+                    const int32_t* block_table, int num_pages, int n_db, int k_top,
+                    float* top_scores, int32_t* top_index, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -653,3 +653,43 @@ extern "C" const char* tq_status_string(tq_status s) {
   }
   return "unknown status";
 }
+
+// ---------------------------------------------------------------------------
+// inner-product search
+// ---------------------------------------------------------------------------
+extern "C" tq_status tq_search_workspace_size(const tq_ctx* ctx, int nq, int n_db, size_t* bytes) {
+  if (!ctx || !bytes || nq < 1 || n_db < 1) return TQ_ERR_INVALID_ARG;
+  *bytes = search_ws_bytes(nq, n_db, ctx->cfg.m);
+  return TQ_OK;
+}
+
+extern "C" tq_status tq_search(const tq_ctx* ctx, const void* q, tq_dtype dtype, int nq, const void* k_cache,
+                               const int32_t* block_table, int num_pages, int n_db, int k_top,
+                               float* top_scores, int32_t* top_index, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  if (!ctx || !q || !k_cache || !block_table || !top_scores || !top_index || !workspace) return TQ_ERR_INVALID_ARG;
+  if (dtype != TQ_BF16 && dtype != TQ_F32) return TQ_ERR_INVALID_ARG;
+  if (nq < 1 || n_db < 1 || num_pages < 1 || k_top < 1 || k_top > n_db || k_top > search_max_k())
+    return TQ_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_pages) * kPage < n_db) return TQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 15) || (reinterpret_cast<uintptr_t>(k_cache) & 15))
+    return TQ_ERR_INVALID_ARG;
+  if (workspace_bytes < search_ws_bytes(nq, n_db, ctx->cfg.m)) return TQ_ERR_WORKSPACE;
+  DecodeArgs a{};
+  a.q = q;
+  a.f32 = dtype == TQ_F32 ? 1 : 0;
+  a.B = 1;
+  a.Hq = nq;
+  a.H = 1;
+  a.G = nq;
+  a.m = ctx->cfg.m;
+  a.kl = ctx->kl;
+  a.vl = ctx->vl;
+  a.tab = ctx->tab;
+  a.qprep = static_cast<float*>(workspace);
+  a.qfrag = nullptr;
+  a.sched = nullptr;
+  const cudaError_t e = launch_search(a, static_cast<const uint8_t*>(k_cache), block_table, num_pages, n_db, k_top,
+                                      top_scores, top_index, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}

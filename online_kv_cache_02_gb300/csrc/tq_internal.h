@@ -142,6 +142,13 @@ bool launch_partials_mma(const DecodeArgs& a, cudaStream_t s, cudaError_t* err);
 int lut_decode_ctas(const KindLayout& kl, const KindLayout& vl, int m, int G);
 long long lut_cost(long long items, int ctas, int warps, long long chunk_cost);
 int lut_warps_for(long long items, int ctas);
+// Inner-product search (tq_search.cu): workspace bytes (q~/u rows, then the
+// [nq][n_db] scores), the launches (qprep of qa, scores, top k) and the
+// largest k supported.
+size_t search_ws_bytes(int nq, int n_db, int m);
+cudaError_t launch_search(const DecodeArgs& qa, const uint8_t* kc, const int32_t* bt, int num_pages, int n_db,
+                          int k, float* top_s, int32_t* top_i, cudaStream_t st);
+int search_max_k();
 bool launch_partials_lut(const DecodeArgs& a, cudaStream_t s, cudaError_t* err);
 
 }  // namespace tq

@@ -63,6 +63,8 @@ EXPORTS = {
     "tq_host_qjl": ([_I, _I, _U64, _P], _S),
     "tq_host_codebook": ([_I, _P, _P], _S),
     "tq_host_codebook_ex": ([_I, _I, _I, _P, _P], _S),
+    "tq_search_workspace_size": ([_P, _I, _I, ctypes.POINTER(ctypes.c_size_t)], _S),
+    "tq_search": ([_P, _P, _I, _I, _P, _P, _I, _I, _I, _P, _P, _P, ctypes.c_size_t, _P], _S),
     "tq_quantize": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P], _S),
     "tq_workspace_size": ([_P, _I, _I, _I, _I, ctypes.POINTER(_SZ)], _S),
     "tq_decode_chunk": ([_P, _I, _I, _I, ctypes.c_longlong, _I, _I, ctypes.POINTER(_I)], _S),
@@ -268,3 +270,17 @@ def tq_refine_counters(ctx, reset=False):
 def raw_status(fn_name, *args):
     """Call an export with already-marshalled arguments and return its status (for argument-check tests)."""
     return getattr(_lib, fn_name)(*args)
+
+
+def tq_search_workspace_size(ctx, nq, n_db):
+    n = ctypes.c_size_t()
+    _check("tq_search_workspace_size", _lib.tq_search_workspace_size(ctx, nq, n_db, ctypes.byref(n)))
+    return n.value
+
+
+def tq_search(ctx, q, dtype, nq, k_cache, block_table, num_pages, n_db, k_top, top_scores, top_index,
+              workspace, workspace_bytes, stream=None):
+    """Inner-product search: the k_top best database vectors per query (see tq.h)."""
+    _check("tq_search", _lib.tq_search(ctx, _ptr(q), dtype, nq, _ptr(k_cache), _ptr(block_table), num_pages, n_db,
+                                       k_top, _ptr(top_scores), _ptr(top_index), _ptr(workspace), workspace_bytes,
+                                       _stream(stream)))

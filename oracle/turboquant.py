@@ -554,6 +554,26 @@ def decode_attention(params, q, seq_lens, block_table, k_cache, v_cache, num_kv_
     return out
 
 
+def search(params, q, block_table_row, k_cache, n_db, k_top):
+    """Inner-product search over a quantized key database ([P2] "생각정리 209
+    (TurboQuant)": the vector-search use; [P4] §4.3: the two-stage estimate).
+
+    The database is one KV head's K cache: vector t at page block_table_row[t // 16],
+    slot t % 16.  Returns the [nq, n_db] estimated inner products and the k_top
+    best per query, best first, equal scores by lower index.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    pages = np.asarray(block_table_row, dtype=np.int64)[np.arange(n_db) // PAGE]
+    slots = np.arange(n_db) % PAGE
+    krec = unpack_k_records(params, read_paged(params, "k", k_cache, pages, slots, np.zeros(n_db, dtype=np.int64), 1))
+    scores = np.empty((q.shape[0], n_db))
+    for i in range(q.shape[0]):
+        qt = params.Pi @ q[i]
+        scores[i] = estimate_scores(params, qt, params.S @ qt, krec)
+    order = np.argsort(-scores, axis=1, kind="stable")[:, :k_top]
+    return scores, order, np.take_along_axis(scores, order, axis=1)
+
+
 def exact_attention(q, K, V, scale):
     """Textbook softmax(q K^T * scale) V in fp64, for pins only."""
     logits = scale * (K @ q)

@@ -1,0 +1,125 @@
+"""Inner-product search (the decode's two-stage estimate without softmax, then the k best per query)
+against the oracle, through the C ABI.
+
+Both sides read the same database bytes: the oracle quantizes and packs the vectors into one KV head's
+K cache, the bytes go to the device unchanged.  Checked: every score (left in the workspace after the
+q rows, as tq.h states) against the oracle's fp64 estimate; the returned top k as the exact stable
+ranking of the GPU's own scores (index work: bit-exact); and the returned vectors against the oracle's
+ranking up to the score tolerance.
+"""
+
+import numpy as np
+import pytest
+
+from .gpu_common import DEV, ctx_for, input_tensor, oracle, th, to_dev, torch, tq, wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _database(w, n, seed, perm_pages=True, X=None):
+    rng = np.random.default_rng(seed)
+    if X is None:
+        X = rng.standard_normal((n, 128)).astype(np.float32)
+        X[:, :w.outlier_channels] *= w.outlier_scale
+    npg = (n + 15) // 16
+    num_pages = npg + 3
+    row = (rng.permutation(num_pages)[:npg] if perm_pages else np.arange(npg)).astype(np.int32)
+    p = th.params_for(w)
+    cache = np.zeros(num_pages * oracle.cache_block_bytes(p, "k"), dtype=np.uint8)
+    th.oracle_quantize_into(p, "k", cache, X, row[np.arange(n) // 16].astype(np.int64), np.arange(n) % 16,
+                            np.zeros(n, dtype=np.int64), 1)
+    return p, X, row, num_pages, cache
+
+
+def _search(ctx, Q, dtype, row, num_pages, cache, n, k):
+    nq = Q.shape[0]
+    qd, code = input_tensor(Q, dtype)
+    ws_n = tq.tq_search_workspace_size(ctx, nq, n)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=DEV)
+    ts = torch.full((nq, k), float("nan"), dtype=torch.float32, device=DEV)
+    ti = torch.full((nq, k), -1, dtype=torch.int32, device=DEV)
+    tq.tq_search(ctx, qd, code, nq, to_dev(cache), to_dev(row), num_pages, n, k, ts, ti, ws, ws_n)
+    torch.cuda.synchronize()
+    off = ((4 * nq * (128 + 128)) + 255) // 256 * 256
+    scores = ws[off:off + 4 * nq * n].view(torch.float32).reshape(nq, n).cpu().numpy()
+    return ts.cpu().numpy(), ti.cpu().numpy(), scores
+
+
+def _check(w, n, nq, k, dtype="bf16", seed=0, X=None, Q=None):
+    p, X, row, num_pages, cache = _database(w, n, seed, X=X)
+    if Q is None:
+        Q = np.random.default_rng(seed + 1).standard_normal((nq, 128)).astype(np.float32)
+    if dtype == "bf16":
+        Q = wl.bf16_round(Q)
+    ctx = ctx_for(w)
+    try:
+        ts, ti, scores = _search(ctx, Q, dtype, row, num_pages, cache, n, k)
+        assert tq.tq_check_device_status(ctx) == 0
+    finally:
+        tq.tq_destroy(ctx)
+    want, wtop, wvals = oracle.search(p, Q.astype(np.float64), row, cache, n, k)
+    scale = np.abs(want).max(axis=1, keepdims=True)
+    tol = 1e-4 * scale
+    # every score
+    assert np.all(np.abs(scores - want) <= tol), float(np.max(np.abs(scores - want) / scale))
+    # the returned k: the exact stable ranking of the GPU's own scores
+    mine = np.argsort(-scores, axis=1, kind="stable")[:, :k]
+    assert np.array_equal(ti, mine)
+    assert np.array_equal(ts, np.take_along_axis(scores, ti, axis=1))
+    # against the oracle: each returned vector scores within tol of the oracle's k-th best or above
+    got_true = np.take_along_axis(want, ti.astype(np.int64), axis=1)
+    assert np.all(got_true >= wvals[:, -1:] - 2 * tol)
+    return ti, wtop
+
+
+@pytest.mark.parametrize("kb,qjl", [((3, 3), True), ((4, 3), True), ((3, 2), True), ((2, 2), False)])
+def test_search_matches_oracle(kb, qjl):
+    w = wl.Workload("s", "search", 1, 1, 1, 0, k_bits=kb, qjl=qjl, seed=4)
+    _check(w, 1000, 13, 10)
+
+
+def test_search_ragged_sizes_and_full_k():
+    """One query, a database of 37 vectors (a partial page), every vector returned; fp32 queries; 2049
+    vectors (two scoring blocks, the second with one vector) and 9 queries (two query groups)."""
+    w = wl.Workload("s", "search", 1, 1, 1, 0, k_bits=(3, 3), seed=5)
+    _check(w, 37, 1, 37, dtype="f32", seed=1)
+    _check(w, 2049, 9, 5, seed=2)
+
+
+def test_search_finds_scaled_copies():
+    """Each query's scaled copy in the database ranks first on the GPU as in the oracle."""
+    w = wl.Workload("s", "search", 1, 1, 1, 0, k_bits=(3, 3), seed=6)
+    rng = np.random.default_rng(11)
+    Q = rng.standard_normal((5, 128)).astype(np.float32)
+    X = rng.standard_normal((700, 128)).astype(np.float32)
+    where = rng.choice(700, 5, replace=False)
+    X[where] = 4.0 * Q
+    ti, wtop = _check(w, 700, 5, 3, dtype="f32", seed=3, X=X, Q=Q)
+    assert np.array_equal(ti[:, 0], where) and np.array_equal(wtop[:, 0], where)
+
+
+def test_search_bad_page_and_arguments():
+    """A page id out of range: its vectors score -inf (never ranked above a real one) and the device
+    error word is set; bad arguments and a short workspace are rejected before any launch."""
+    w = wl.Workload("s", "search", 1, 1, 1, 0, k_bits=(3, 3), seed=7)
+    p, X, row, num_pages, cache = _database(w, 64, 3)
+    row = row.copy()
+    row[1] = num_pages + 5                          # vectors 16..31
+    Q = wl.bf16_round(np.random.default_rng(4).standard_normal((3, 128)).astype(np.float32))
+    ctx = ctx_for(w)
+    try:
+        ts, ti, scores = _search(ctx, Q, "bf16", row, num_pages, cache, 64, 48)
+        assert tq.tq_check_device_status(ctx) != 0
+        assert np.all(np.isneginf(scores[:, 16:32]))
+        assert not np.any((ti >= 16) & (ti < 32))
+        qd, code = input_tensor(Q, "bf16")
+        ws = torch.empty(tq.tq_search_workspace_size(ctx, 3, 64), dtype=torch.uint8, device=DEV)
+        out_s = torch.empty(3, 8, device=DEV)
+        out_i = torch.empty(3, 8, dtype=torch.int32, device=DEV)
+        kc, bt = to_dev(cache), to_dev(row)
+        for k_top, n_db, ws_n in ((0, 64, ws.numel()), (65, 64, ws.numel()), (1025, 2000, ws.numel()),
+                                  (8, 64, ws.numel() - 1), (8, num_pages * 16 + 1, ws.numel())):
+            with pytest.raises(tq.TQError):
+                tq.tq_search(ctx, qd, code, 3, kc, bt, num_pages, n_db, k_top, out_s, out_i, ws, ws_n)
+    finally:
+        tq.tq_destroy(ctx)

@@ -341,3 +341,53 @@ def test_decode_attention_gqa_and_paging(p3):
         for h in range(Hq):
             kr, vr = _records(p3, Ks[b, h // 2], Vs[b, h // 2])
             assert np.allclose(out[b, h], tq.attend_one(p3, Q[b, h], kr, vr, 1 / math.sqrt(D)), atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# inner-product search (the vector-search use of the same estimate)
+# ---------------------------------------------------------------------------
+
+def _search_db(p, X, perm=None):
+    n = X.shape[0]
+    npg = (n + 15) // 16
+    row = np.arange(npg) if perm is None else np.asarray(perm)[:npg]
+    cache = np.zeros((int(row.max()) + 1) * oracle.cache_block_bytes(p, "k"), dtype=np.uint8)
+    q = oracle.quantize_vectors(p, X, "k")
+    pages, slots = row[np.arange(n) // 16], np.arange(n) % 16
+    oracle.write_paged(p, "k", cache, oracle.pack_k_records(p, q), pages, slots, np.zeros(n, dtype=np.int64), 1)
+    return row, cache
+
+
+def test_search_ranks_scaled_copies_first():
+    """A database holding 4x each query among random vectors: the estimate <q, 4q> = 4||q||^2 dwarfs every
+    other score, so each query's best hit is its own copy."""
+    p = oracle.make_params(k_bits=(3, 3), seed=3)
+    rng = np.random.default_rng(5)
+    Q = rng.standard_normal((6, 128))
+    X = rng.standard_normal((300, 128))
+    where = rng.choice(300, 6, replace=False)
+    X[where] = 4.0 * Q
+    row, cache = _search_db(p, X)
+    scores, top, vals = oracle.search(p, Q, row, cache, 300, 3)
+    assert np.array_equal(top[:, 0], where)
+    assert np.all(np.diff(vals, axis=1) <= 0)
+    # the estimate of <q, 4q> is within the quantization error of the exact value
+    exact = 4.0 * np.sum(Q * Q, axis=1)
+    assert np.all(np.abs(vals[:, 0] - exact) < 0.1 * exact)
+
+
+def test_search_ties_by_index_and_block_table_indirection():
+    """Duplicate vectors have equal estimates and rank by lower index; a permuted block table reads back
+    the same database."""
+    p = oracle.make_params(k_bits=(4, 3), seed=2)
+    rng = np.random.default_rng(8)
+    X = rng.standard_normal((100, 128))
+    X[[10, 40, 70]] = 3.0 * X[5]
+    Q = X[5:6] / np.linalg.norm(X[5])
+    row, cache = _search_db(p, X)
+    s1, top, _ = oracle.search(p, Q, row, cache, 100, 4)
+    assert list(top[0, :3]) == [10, 40, 70] and s1[0, 10] == s1[0, 40] == s1[0, 70]
+    perm = np.random.default_rng(9).permutation(20)
+    row2, cache2 = _search_db(p, X, perm)
+    s2, top2, _ = oracle.search(p, Q, row2, cache2, 100, 4)
+    assert np.array_equal(s1, s2) and np.array_equal(top, top2)
