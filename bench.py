@@ -45,7 +45,7 @@ def parse(argv=None):
     ap.add_argument("--config", default="c3", choices=["c3", "c4", "c5"])
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     ap.add_argument("--no-quantize", action="store_true", help="skip the c2 quantize measurement")
-    ap.add_argument("--only", default="", choices=["", "quantize"],
+    ap.add_argument("--only", default="", choices=["", "quantize", "search"],
                     help="quantize: run the c2 quantize measurement alone (profiling; --batch scales it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args(argv)
@@ -353,6 +353,92 @@ def quantize_measure(torch, tq, qw, stream, qsteps, warmup, dist, peak, peak_kin
     return rec
 
 
+SEARCH_N, SEARCH_NQ, SEARCH_K = 1 << 20, 64, 10
+
+
+def search_measure(torch, tq, stream, steps, warmup, peak, peak_kind):
+    """Inner-product search: 2^20 database vectors (one KV head's K cache, 3-bit + QJL, N(0,1) bf16 with
+    channels 0-3 x10, quantized by tq_quantize), 64 bf16 queries, the 10 best each; value = database bytes
+    read per search / time."""
+    dev = torch.device("cuda")
+    ctx = tq.tq_create_ex(tq.make_config(k_bits=(3, 3), v_bits=(3, 3), seed=4))
+    kpb, _ = tq.tq_cache_layout(ctx, 1)
+    npg = SEARCH_N // 16
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4)
+    kc = torch.zeros(npg * kpb, dtype=torch.uint8, device=dev)
+    bt = torch.randperm(npg, device=dev, generator=gen).to(torch.int32)
+    X = torch.randn(1, SEARCH_N, 1, 128, device=dev, generator=gen)
+    X[..., :4] *= 10
+    X = X.to(torch.bfloat16)
+    tq.tq_quantize(ctx, X, None, tq.TQ_BF16, 1, SEARCH_N, 1, torch.zeros(1, dtype=torch.int32, device=dev),
+                   bt.view(1, -1), npg, npg, kc, None, stream)
+    del X
+    q_h = torch.randn(SEARCH_NQ, 128, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).pin_memory()
+    q = q_h.to(dev)
+    ws_n = tq.tq_search_workspace_size(ctx, SEARCH_NQ, SEARCH_N)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=dev)
+    ts = torch.empty(SEARCH_NQ, SEARCH_K, device=dev)
+    ti = torch.empty(SEARCH_NQ, SEARCH_K, dtype=torch.int32, device=dev)
+    ts_h, ti_h = torch.empty_like(ts, device="cpu").pin_memory(), torch.empty_like(ti, device="cpu").pin_memory()
+    run = lambda: tq.tq_search(ctx, q, tq.TQ_BF16, SEARCH_NQ, kc, bt, npg, SEARCH_N, SEARCH_K, ts, ti, ws, ws_n,
+                               stream)
+
+    def run_e2e():
+        q.copy_(q_h, non_blocking=True)
+        run()
+        ts_h.copy_(ts, non_blocking=True)
+        ti_h.copy_(ti, non_blocking=True)
+
+    flush, l2_note = l2_flusher(torch, npg * kpb)
+    sampler = ClockSampler(torch)
+    with sampler:
+        ms = timed(torch, stream, lambda i=None: run(), steps, warmup, None, flush) / steps
+    ms_e2e = timed(torch, stream, lambda i=None: run_e2e(), steps, warmup, None, flush) / steps
+    db_bytes = npg * kpb
+    value = db_bytes / (ms * 1e-3) / 1e9
+    flags = tq.tq_check_device_status(ctx)
+    tq.tq_destroy(ctx)
+    return {
+        "metric": "inner-product search: quantized database GB/s per query batch",
+        "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms, 4), "steps": steps, "warmup": warmup,
+        "higher_is_better": True, "dtype": "packed 3-bit codes + QJL signs, fp32 scores",
+        "data": "synthetic (seeded N(0,1), channels 0-3 x10)",
+        "config": {"workload": f"search: {SEARCH_N} database vectors (one KV head, K 3-bit + QJL m=128), "
+                               f"{SEARCH_NQ} bf16 queries, top {SEARCH_K}",
+                   "database_bytes": db_bytes, "scores_per_s": round(SEARCH_NQ * SEARCH_N / (ms * 1e-3), 1),
+                   "l2": l2_note},
+        "roofline": {"kernel": "tq_search (qprep, CUDA-core scores, top k)", "bound": "hbm",
+                     "achieved": round(value, 2), "peak": peak, "unit": "GB/s", "frac": round(value / peak, 5),
+                     "peak_source": peak_kind, "algorithmic_bytes_per_launch": db_bytes, "traffic": None},
+        "e2e": {"value": round(db_bytes / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": q_h.numel() * 2, "d2h_bytes_per_step": ts.numel() * 4 + ti.numel() * 4},
+        "gpu_launches": 3 * steps, "clocks": sampler.result(), "device_flags": flags,
+    }
+
+
+def oracle_search_sample(seconds=10.0):
+    """The oracle's search (fp64) on a database sample: database bytes per second on one core."""
+    import oracle
+    p = oracle.make_params(k_bits=(3, 3), v_bits=(3, 3), seed=4)
+    rng = np.random.default_rng(4)
+    n = 4096
+    X = rng.standard_normal((n, 128))
+    X[:, :4] *= 10
+    Q = rng.standard_normal((SEARCH_NQ, 128))
+    row = np.arange(n // 16)
+    cache = np.zeros((n // 16) * oracle.cache_block_bytes(p, "k"), dtype=np.uint8)
+    rec = oracle.pack_k_records(p, oracle.quantize_vectors(p, X, "k"))
+    oracle.write_paged(p, "k", cache, rec, row[np.arange(n) // 16], np.arange(n) % 16, np.zeros(n, dtype=np.int64), 1)
+    reps, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds or reps == 0:
+        oracle.search(p, Q, row, cache, n, SEARCH_K)
+        reps += 1
+    el = time.perf_counter() - t0
+    return {"value": round(cache.size * reps / el / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} fp64 searches of {SEARCH_NQ} queries over {n} database vectors (3-bit + QJL)"}
+
+
 def run_ours(args):
     import torch
     from online_kv_cache_02_gb300 import tq
@@ -369,6 +455,16 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     peak, peak_kind = peaks()
 
+    if args.only == "search":
+        line = search_measure(torch, tq, stream, args.steps, max(3, args.warmup), peak, peak_kind)
+        line.update({"n_gpus": world, "scaling": "weak", "vs_baseline": None})
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = oracle_search_sample()
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
     if args.only == "quantize":
         qw = wl.WORKLOADS["c2"].scaled(batch=args.batch) if args.batch else wl.WORKLOADS["c2"]
         line = {"metric": "KV vectors quantized/s (quantize only)"}
