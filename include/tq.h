@@ -95,9 +95,10 @@ typedef struct tq_ctx tq_ctx;   /* opaque; immutable after creation */
 tq_status tq_config_init(tq_config* cfg, int d, int b, int m, uint64_t seed);
 
 /* Build the context on the current device ([P4] §4.1-§4.3): the random
- * rotation Pi (Householder QR of a d x d Gaussian, positive R diagonal), the
- * QJL matrix S (m x d Gaussian) and the Gaussian Lloyd-Max codebooks, drawn
- * from the SplitMix64/Box-Muller streams 1 and 2 of `seed`.  The only call
+ * rotation Pi (Householder QR of a d x d Gaussian, positive R diagonal) and
+ * the QJL matrix S (m x d Gaussian), drawn from the SplitMix64/Box-Muller
+ * streams 1 and 2 of `seed`, and the Lloyd-Max codebooks for cfg->codebook's
+ * density (tq_create: Gaussian).  The only call
  * that allocates device memory (about 0.5 MB) and the only one that copies
  * host to device.  `*out` receives the context; free it with tq_destroy. */
 tq_status tq_create(int d, int b, int m, uint64_t seed, tq_ctx** out);
