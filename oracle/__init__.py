@@ -29,7 +29,7 @@ from .turboquant import (
     TQParams, make_params, quantize_vectors, estimate_scores,
     pack_k_records, pack_v_records, unpack_k_records, unpack_v_records,
     cache_block_bytes, write_paged, read_paged, decode_attention,
-    exact_attention, quantize_exclusions, search,
+    exact_attention, quantize_exclusions, search, causal_attention,
 )
 
 __all__ = [
@@ -38,5 +38,5 @@ __all__ = [
     "TQParams", "make_params", "quantize_vectors", "estimate_scores",
     "pack_k_records", "pack_v_records", "unpack_k_records", "unpack_v_records",
     "cache_block_bytes", "write_paged", "read_paged", "decode_attention",
-    "exact_attention", "search", "quantize_exclusions",
+    "exact_attention", "search", "causal_attention", "quantize_exclusions",
 ]

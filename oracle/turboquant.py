@@ -554,6 +554,35 @@ def decode_attention(params, q, seq_lens, block_table, k_cache, v_cache, num_kv_
     return out
 
 
+def causal_attention(params, q, start_pos, block_table, k_cache, v_cache, num_kv_heads, scale=None):
+    """Multi-query causal attention over the compressed cache ([P4] §2.3: a new
+    token's query attends over every cached token, the new tokens' K/V having
+    been appended first).  q [B, T, Hq, d] holds the queries of T new tokens at
+    positions start_pos[b] + t; token t attends over positions 0 .. start_pos[b] + t
+    of sequence b (the cache already holds all of them).  Decode is T = 1.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, T, Hq, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    group = Hq // num_kv_heads
+    out = np.zeros((B, T, Hq, d))
+    for b in range(B):
+        last = int(start_pos[b]) + T                     # positions 0 .. last - 1 are needed
+        pages, slots = token_locations(block_table, b, np.arange(last))
+        for hk in range(num_kv_heads):
+            heads = np.full(last, hk)
+            kr = unpack_k_records(params, read_paged(params, "k", k_cache, pages, slots, heads, num_kv_heads))
+            vr = unpack_v_records(params, read_paged(params, "v", v_cache, pages, slots, heads, num_kv_heads))
+            for t in range(T):
+                n = int(start_pos[b]) + t + 1
+                kt = {key: val[:n] for key, val in kr.items()}
+                vt = {key: val[:n] for key, val in vr.items()}
+                for h in range(hk * group, (hk + 1) * group):
+                    out[b, t, h] = attend_one(params, q[b, t, h], kt, vt, scale)
+    return out
+
+
 def search(params, q, block_table_row, k_cache, n_db, k_top):
     """Inner-product search over a quantized key database ([P2] "생각정리 209
     (TurboQuant)": the vector-search use; [P4] §4.3: the two-stage estimate).

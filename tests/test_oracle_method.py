@@ -391,3 +391,76 @@ def test_search_ties_by_index_and_block_table_indirection():
     row2, cache2 = _search_db(p, X, perm)
     s2, top2, _ = oracle.search(p, Q, row2, cache2, 100, 4)
     assert np.array_equal(s1, s2) and np.array_equal(top, top2)
+
+
+# ---------------------------------------------------------------------------
+# multi-query causal attention over the compressed cache (many new tokens)
+# ---------------------------------------------------------------------------
+
+def _causal_setup(p, K, V, perm=None):
+    """K, V [B, L, H, d] written through a block table (identity or permuted pages)."""
+    B, L, H, _ = K.shape
+    pps = (L + 15) // 16
+    npages = B * pps
+    order = np.arange(npages) if perm is None else np.asarray(perm)
+    bt = order.reshape(B, pps)
+    kc = np.zeros(npages * H * oracle.cache_block_bytes(p, "k"), dtype=np.uint8)
+    vc = np.zeros(npages * H * oracle.cache_block_bytes(p, "v"), dtype=np.uint8)
+    for b in range(B):
+        pos = np.repeat(np.arange(L), H)
+        heads = np.tile(np.arange(H), L)
+        pages, slots = bt[b, pos // 16].astype(np.int64), pos % 16
+        for kind, X, cache in (("k", K, kc), ("v", V, vc)):
+            q = oracle.quantize_vectors(p, X[b].reshape(-1, 128), kind)
+            rec = oracle.pack_k_records(p, q) if kind == "k" else oracle.pack_v_records(p, q)
+            oracle.write_paged(p, kind, cache, rec, pages, slots, heads, H)
+    return bt, kc, vc
+
+
+def test_causal_attention_masks_the_future():
+    """A query at position s+t sees positions <= s+t only: changing a later key or value leaves it unchanged,
+    changing an earlier one does not; a permuted block table reads back the same result."""
+    p = oracle.make_params(k_bits=(3, 3), v_bits=(3, 3), seed=1)
+    rng = np.random.default_rng(12)
+    B, L, H, Hq, T = 2, 40, 2, 4, 6
+    K, V = rng.standard_normal((B, L, H, 128)), rng.standard_normal((B, L, H, 128))
+    start = np.array([30, 34])                       # new tokens at start .. start + T - 1 (< L)
+    Q = rng.standard_normal((B, T, Hq, 128))
+    bt, kc, vc = _causal_setup(p, K, V)
+    base = oracle.causal_attention(p, Q, start, bt, kc, vc, H)
+    K2, V2 = K.copy(), V.copy()
+    K2[0, 33] += 5.0                                 # position 33 of sequence 0: seen by t >= 3 only
+    V2[0, 33] -= 5.0
+    bt2, kc2, vc2 = _causal_setup(p, K2, V2)
+    other = oracle.causal_attention(p, Q, start, bt2, kc2, vc2, H)
+    assert np.array_equal(other[0, :3], base[0, :3]) and np.array_equal(other[1], base[1])
+    assert np.all(np.abs(other[0, 3:] - base[0, 3:]).max(axis=-1) > 1e-6)
+    perm = np.random.default_rng(3).permutation(B * ((L + 15) // 16))
+    bt3, kc3, vc3 = _causal_setup(p, K, V, perm)
+    assert np.array_equal(oracle.causal_attention(p, Q, start, bt3, kc3, vc3, H), base)
+
+
+def test_causal_attention_approaches_exact_at_four_bits():
+    """Against textbook causal softmax attention over the unquantized keys and values (each query against its
+    own prefix), the error of the compressed result about halves per bit (the reconstruction error of a
+    Lloyd-Max code falls about 2x per bit in norm); measured 0.79 / 0.40 / 0.20 at 2 / 3 / 4 bits here, where
+    averaging over 64 random values makes the exact output small."""
+    rng = np.random.default_rng(13)
+    B, L, H, Hq, T = 1, 64, 1, 2, 4
+    K, V = rng.standard_normal((B, L, H, 128)), rng.standard_normal((B, L, H, 128))
+    start = np.array([L - T])
+    Q = rng.standard_normal((B, T, Hq, 128))
+    errs = {}
+    for bits in (2, 3, 4):
+        p = oracle.make_params(k_bits=(bits, bits), v_bits=(bits, bits), seed=2)
+        bt, kc, vc = _causal_setup(p, K, V)
+        got = oracle.causal_attention(p, Q, start, bt, kc, vc, H)
+        e = 0.0
+        for t in range(T):
+            n = int(start[0]) + t + 1
+            for h in range(Hq):
+                want = oracle.exact_attention(Q[0, t, h], K[0, :n, 0], V[0, :n, 0], 1.0 / math.sqrt(128))
+                e = max(e, np.max(np.abs(got[0, t, h] - want)) / np.max(np.abs(want)))
+        errs[bits] = e
+    assert errs[2] > errs[3] > errs[4] and errs[4] < 0.25
+    assert 1.6 < errs[2] / errs[3] < 2.5 and 1.6 < errs[3] / errs[4] < 2.5
