@@ -109,3 +109,14 @@ def test_null_context_is_rejected(tq):
     assert st("tq_cache_layout", None, 8, ctypes.byref(n), None) == tq.TQ_ERR_INVALID_ARG
     c = ctypes.c_int()
     assert st("tq_decode_chunk", None, 16, 32, 8, 16 * 1000, 1000, 0, ctypes.byref(c)) == tq.TQ_ERR_INVALID_ARG
+    assert st("tq_search_workspace_size", None, 4, 100, ctypes.byref(n)) == tq.TQ_ERR_INVALID_ARG
+    assert st("tq_search", None, 1, 0, 4, 1, 1, 8, 100, 10, 1, 1, 1, 1 << 20, None) == tq.TQ_ERR_INVALID_ARG
+
+
+def test_codebook_ex_arguments(tq):
+    c, t = np.empty(16), np.empty(15)
+    st = tq.raw_status
+    assert st("tq_host_codebook_ex", 3, 128, 7, c.ctypes.data, t.ctypes.data) == tq.TQ_ERR_INVALID_ARG
+    assert st("tq_host_codebook_ex", 3, 3, tq.TQ_CODEBOOK_SPHERE, c.ctypes.data, t.ctypes.data) == tq.TQ_ERR_INVALID_ARG
+    assert st("tq_host_codebook_ex", 0, 128, tq.TQ_CODEBOOK_SPHERE, c.ctypes.data, t.ctypes.data) == tq.TQ_ERR_INVALID_ARG
+    assert st("tq_host_codebook_ex", 3, 128, tq.TQ_CODEBOOK_SPHERE, None, t.ctypes.data) == tq.TQ_ERR_INVALID_ARG
