@@ -100,7 +100,9 @@ tq_status tq_config_init(tq_config* cfg, int d, int b, int m, uint64_t seed);
  * streams 1 and 2 of `seed`, and the Lloyd-Max codebooks for cfg->codebook's
  * density (tq_create: Gaussian).  The only call
  * that allocates device memory (about 0.5 MB) and the only one that copies
- * host to device.  `*out` receives the context; free it with tq_destroy. */
+ * host to device; it also creates the second stream and the two events of the
+ * fused decode step (tq_append_decode), so no later call creates anything.
+ * `*out` receives the context; free it with tq_destroy. */
 tq_status tq_create(int d, int b, int m, uint64_t seed, tq_ctx** out);
 tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out);
 tq_status tq_destroy(tq_ctx* ctx);
@@ -236,9 +238,9 @@ tq_status tq_append_decode(const tq_ctx* ctx, const void* k_new, const void* v_n
 /* tq_append_decode with two optional CUDA events (cudaEvent_t, may be NULL)
  * recorded on `stream` just before and just after the split-K partials kernel,
  * for timing it inside the fused step.  Execution: the new token's
- * quantize-append runs on a second stream created with the context on first
- * use (joined with events; calls sharing a context serialise their host-side
- * enqueue) next to the query prep and the partials kernel, which covers the
+ * quantize-append runs on a second stream that tq_create made with the
+ * context (joined with events; calls sharing a context serialise their
+ * host-side enqueue) next to the query prep and the partials kernel, which covers the
  * seq_lens[b] cached tokens and leaves a few SMs to the append; the merge then
  * scores the new token from its stored record and adds it to the log-sum-exp
  * merge.  Results equal tq_quantize + tq_decode_attention over L+1 tokens up
@@ -282,7 +284,8 @@ const char* tq_status_string(tq_status status);
  * tq_search_workspace_size bytes holds the q~/u rows and the [nq][n_db]
  * scores (fp32, in the workspace after them).  Stream-ordered; no allocation.
  * Errors: null pointers, k_top out of range, n_db > 16 num_pages, misaligned
- * buffers -> TQ_ERR_INVALID_ARG; a small workspace -> TQ_ERR_WORKSPACE. */
+ * buffers -> TQ_ERR_INVALID_ARG; a small workspace -> TQ_ERR_WORKSPACE;
+ * nq > 524280 (65535 x 8) -> TQ_ERR_UNSUPPORTED.  All checked before any launch. */
 tq_status tq_search_workspace_size(const tq_ctx* ctx, int nq, int n_db, size_t* bytes);
 tq_status tq_search(const tq_ctx* ctx, const void* q, tq_dtype dtype, int nq, const void* k_cache,
                     const int32_t* block_table, int num_pages, int n_db, int k_top,

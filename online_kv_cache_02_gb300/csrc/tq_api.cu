@@ -222,7 +222,11 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
   ctx->fused_mu = new (std::nothrow) std::mutex();
   if (!ctx->fused_mu) { delete ctx; return TQ_ERR_OOM; }
   ctx->cfg = *cfg;
-  if (cudaGetDevice(&ctx->device) != cudaSuccess) { delete ctx; return TQ_ERR_CUDA; }
+  if (cudaGetDevice(&ctx->device) != cudaSuccess) {
+    delete static_cast<std::mutex*>(ctx->fused_mu);
+    delete ctx;
+    return TQ_ERR_CUDA;
+  }
   fill_layout(ctx->kl, cfg->k_bits_hi, cfg->k_bits_lo, cfg->k_split, d, m, true, cfg->k_qjl != 0, cfg->codebook);
   fill_layout(ctx->vl, cfg->v_bits_hi, cfg->v_bits_lo, cfg->v_split, d, m, false, false, cfg->codebook);
 
@@ -290,7 +294,12 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
   size_t o_cnt = align256(o_err + sizeof(uint32_t));
   size_t total = align256(o_cnt + 2 * sizeof(unsigned long long));
   void* blk = nullptr;
-  if (cudaMalloc(&blk, total) != cudaSuccess) { delete ctx; cudaGetLastError(); return TQ_ERR_OOM; }
+  if (cudaMalloc(&blk, total) != cudaSuccess) {
+    delete static_cast<std::mutex*>(ctx->fused_mu);
+    delete ctx;
+    cudaGetLastError();
+    return TQ_ERR_OOM;
+  }
   char* b = static_cast<char*>(blk);
   ctx->dev_block = blk;
   ctx->tab.pit = reinterpret_cast<float*>(b + o_pit);
@@ -322,7 +331,21 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
             cudaMemcpy(ctx->tab.s_df, sdf.data(), sizeof(float) * d * m * 2, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemcpy(ctx->tab.wt, wt.data(), sizeof(float) * d * (d + m), cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemset(b + o_err, 0, total - o_err) == cudaSuccess;
-  if (!ok) { cudaFree(blk); delete ctx; cudaGetLastError(); return TQ_ERR_CUDA; }
+  if (!ok) { cudaFree(blk); delete static_cast<std::mutex*>(ctx->fused_mu); delete ctx; cudaGetLastError(); return TQ_ERR_CUDA; }
+  // the fused decode step's second stream and its fork/join events: made here,
+  // so tq_append_decode creates nothing
+  if (cudaStreamCreateWithFlags(&ctx->aux_stream, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ctx->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ctx->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    if (ctx->aux_stream) cudaStreamDestroy(ctx->aux_stream);
+    if (ctx->ev_fork) cudaEventDestroy(ctx->ev_fork);
+    if (ctx->ev_join) cudaEventDestroy(ctx->ev_join);
+    cudaFree(blk);
+    delete static_cast<std::mutex*>(ctx->fused_mu);
+    delete ctx;
+    return TQ_ERR_CUDA;
+  }
   *out = ctx;
   return TQ_OK;
 }
@@ -598,15 +621,9 @@ extern "C" tq_status tq_append_decode_ex(const tq_ctx* ctx, const void* k_new, c
   if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15) return TQ_ERR_INVALID_ARG;
   if (static_cast<long long>(batch) * H > (1LL << 31) - 1) return TQ_ERR_INVALID_ARG;
   tq_ctx* c = const_cast<tq_ctx*>(ctx);
+  // the fork/join events are shared by every call on this context: one host
+  // thread at a time records and waits on them
   std::lock_guard<std::mutex> lock(*static_cast<std::mutex*>(c->fused_mu));
-  if (!c->aux_stream) {
-    if (cudaStreamCreateWithFlags(&c->aux_stream, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming) != cudaSuccess) {
-      cudaGetLastError();
-      return TQ_ERR_CUDA;
-    }
-  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   FusedStep f{append_reserve(batch, H), c->ev_join, static_cast<cudaEvent_t>(partials_begin),
               static_cast<cudaEvent_t>(partials_end)};
@@ -672,6 +689,7 @@ extern "C" tq_status tq_search(const tq_ctx* ctx, const void* q, tq_dtype dtype,
   if (nq < 1 || n_db < 1 || num_pages < 1 || k_top < 1 || k_top > n_db || k_top > search_max_k())
     return TQ_ERR_INVALID_ARG;
   if (static_cast<long long>(num_pages) * kPage < n_db) return TQ_ERR_INVALID_ARG;
+  if (nq > search_max_queries()) return TQ_ERR_UNSUPPORTED;   // checked before anything is launched
   if ((reinterpret_cast<uintptr_t>(workspace) & 15) || (reinterpret_cast<uintptr_t>(k_cache) & 15))
     return TQ_ERR_INVALID_ARG;
   if (workspace_bytes < search_ws_bytes(nq, n_db, ctx->cfg.m)) return TQ_ERR_WORKSPACE;

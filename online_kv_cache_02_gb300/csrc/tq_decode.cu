@@ -484,19 +484,16 @@ cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
   if (stages & TQ_STAGE_QPREP) {
     const dim3 grid(static_cast<unsigned>((static_cast<long long>(a.B) * a.Hq + kQP - 1) / kQP),
                     static_cast<unsigned>((kD + a.m + kQO - 1) / kQO));
-    static bool configured = false;      // the W slice and q rows take 49 KB of dynamic shared memory
-    if (!configured) {
-      e = cudaFuncSetAttribute(qprep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQprepSmem);
-      if (e != cudaSuccess) return e;
-      configured = true;
-    }
+    static std::atomic<unsigned long long> configured{0};   // the W slice and q rows take 49 KB
+    e = smem_attr_once(qprep_kernel, kQprepSmem, configured);
+    if (e != cudaSuccess) return e;
     qprep_kernel<<<grid, kQThreads, kQprepSmem, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (stages & TQ_STAGE_PARTIALS) {
     cudaError_t em = cudaSuccess;
-    if (launch_partials_lut(a, s, &em) || launch_partials_mma(a, s, &em)) {
+    if (launch_partials_lut(a, s, &em)) {
       if (em != cudaSuccess) return em;
     } else {
     switch (a.G) {

@@ -33,8 +33,8 @@
 // thread's code bytes contiguous; Q~ and the output use the same permutation.
 //
 // Supported here: d = 128, m = 128, channel split 64, the bit-width
-// combinations instantiated below.  Other configurations run tq_decode_mma.cu
-// or the CUDA-core kernel in tq_decode.cu.
+// combinations instantiated below.  Other configurations run the CUDA-core
+// kernel in tq_decode.cu.
 
 #include "tq_internal.h"
 
@@ -52,7 +52,7 @@ constexpr int kMaxStagesL = 4;         // ring depth per warp: the largest <= th
 constexpr float kInvSqrtD = 0.08838834764831845f;
 constexpr float kSqrtHalfPi = 1.2533141373155003f;
 constexpr int kWaitLimit = 1 << 22;
-constexpr float kNegBig = -1.0e30f;    // finite "minus infinity" (see tq_decode_mma.cu)
+constexpr float kNegBig = -1.0e30f;    // finite "minus infinity": 2^(kNegBig - m) is exactly 0, never NaN
 // Slack of the running softmax max (log2 units): p <= 8, and 8 * 65504 / sqrt(128)
 // is below the fp16 maximum, so no fp16 value norm can overflow P'.
 constexpr float kLazyMax = 3.0f;
@@ -648,13 +648,9 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
 template <int W, int KBH, int KBL, int VBH, int VBL, bool QJL>
 cudaError_t launch_lut(const DecodeArgs& a, int items, int grid, cudaStream_t s) {
   using Gm = Geo<W, KBH, KBL, VBH, VBL, QJL>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(lut_partials_kernel<W, KBH, KBL, VBH, VBL, QJL>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> configured{0};
+  const cudaError_t e = smem_attr_once(lut_partials_kernel<W, KBH, KBL, VBH, VBL, QJL>, Gm::SMEM, configured);
+  if (e != cudaSuccess) return e;
   lut_partials_kernel<W, KBH, KBL, VBH, VBL, QJL><<<grid, 32 * W, Gm::SMEM, s>>>(a, items);
   return cudaGetLastError();
 }

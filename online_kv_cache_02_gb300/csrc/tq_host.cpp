@@ -192,7 +192,9 @@ void codebook_fill_sphere(int bits, int d, double* centroids, double* boundaries
     return z >= 1.0 ? 0.0 : cmom * std::pow(1.0 - z * z, 0.5 * (d - 1));
   };
   std::vector<double> a(h), lo(h), nx(h);
-  for (int k = 0; k < h; ++k) a[k] = (k + 0.5) * 3.0 / h;
+  // start inside (0, sqrt(d)): a centroid at or beyond the support's end
+  // would leave its cell empty (0/0)
+  for (int k = 0; k < h; ++k) a[k] = (k + 0.5) * std::fmin(3.0, rd) / h;
   for (int it = 0; it < 200000; ++it) {
     lo[0] = 0.0;
     for (int k = 1; k < h; ++k) lo[k] = 0.5 * (a[k - 1] + a[k]);

@@ -4,6 +4,7 @@
 
 #include "../../include/tq.h"
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -126,12 +127,27 @@ struct DecodeArgs {
                          // for lane t%4 of a KV-head warp, 16 words of q~ (key pairs) then 16 of u
 };
 
+// Opt kernel `fn` into `bytes` of dynamic shared memory on the current device,
+// once per device: `done` (one static per launch site) keeps a bit per device
+// ordinal below 64 (higher ordinals set the attribute on every call).  Safe to
+// call from several host threads: setting the attribute twice is harmless.
+template <typename Kernel>
+cudaError_t smem_attr_once(Kernel* fn, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
 // Tensor-core quantize of K and V in one launch (bf16 inputs, supported
 // bit-width combinations); returns false when the configuration is not covered.
 bool launch_quantize_tc(const QuantizeArgs& k, const QuantizeArgs& v, cudaStream_t s, cudaError_t* err);
 cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s);
-bool launch_partials_mma(const DecodeArgs& a, cudaStream_t s, cudaError_t* err);
 // Persistent lookup-table kernel (tq_decode_lut.cu): CTAs it runs with at
 // most, one per SM (0: configuration not supported), and its launch (false:
 // not supported).  A launch runs 12 or 16 warps per CTA: every warp takes
@@ -149,6 +165,7 @@ size_t search_ws_bytes(int nq, int n_db, int m);
 cudaError_t launch_search(const DecodeArgs& qa, const uint8_t* kc, const int32_t* bt, int num_pages, int n_db,
                           int k, float* top_s, int32_t* top_i, cudaStream_t st);
 int search_max_k();
+int search_max_queries();
 bool launch_partials_lut(const DecodeArgs& a, cudaStream_t s, cudaError_t* err);
 
 }  // namespace tq
@@ -160,7 +177,8 @@ struct tq_ctx {
   tq::DeviceTables tab;
   void* dev_block;       // single allocation holding every device table
   // fused decode step: the new token's quantize-append runs on this stream
-  // next to the partials kernel (created on first use, guarded by fused_mu)
+  // next to the partials kernel (stream and events made by tq_create_ex;
+  // fused_mu serialises the host-side enqueue that records the shared events)
   void* fused_mu;        // std::mutex*
   cudaStream_t aux_stream;
   cudaEvent_t ev_fork, ev_join;

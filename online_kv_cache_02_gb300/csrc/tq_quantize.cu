@@ -424,14 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(QuantizeArgs a) {
 
 template <bool KEY>
 cudaError_t launch_kind(const QuantizeArgs& a, cudaStream_t s) {
-  static bool configured[2] = {false, false};
+  static std::atomic<unsigned long long> configured{0};
   const size_t smem = smem_bytes<KEY>();
-  if (!configured[KEY]) {
-    cudaError_t e = cudaFuncSetAttribute(quantize_kernel<KEY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured[KEY] = true;
-  }
+  const cudaError_t e = smem_attr_once(quantize_kernel<KEY>, static_cast<int>(smem), configured);
+  if (e != cudaSuccess) return e;
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -939,13 +939,9 @@ __global__ void __launch_bounds__(kThreadsTC4, 1) quantize_tc_kernel(QuantizeArg
 
 template <int KBH, int KBL, int VBH, int VBL>
 cudaError_t launch_tc(const QuantizeArgs& k, const QuantizeArgs& v, int nk, int nv, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(quantize_tc_kernel<KBH, KBL, VBH, VBL>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes4);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> configured{0};
+  const cudaError_t e = smem_attr_once(quantize_tc_kernel<KBH, KBL, VBH, VBL>, kSmemBytes4, configured);
+  if (e != cudaSuccess) return e;
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -288,4 +288,6 @@ cudaError_t launch_search(const DecodeArgs& qa, const uint8_t* kc, const int32_t
 
 int search_max_k() { return kTMax; }
 
+int search_max_queries() { return 65535 * kSG; }   // the scoring grid's y extent
+
 }  // namespace tq

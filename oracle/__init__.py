@@ -26,7 +26,7 @@ real model KV and are not reproducible here ("parity unpinned" for those only).
 from .rng import splitmix64_stream, uniform_stream, gaussian_stream
 from .turboquant import (
     Codebook, lloyd_max_gaussian, lloyd_max_sphere, rotation_matrix, qjl_matrix,
-    TQParams, make_params, quantize_vectors, estimate_scores,
+    TQParams, make_params, assign_codes, quantize_vectors, estimate_scores,
     pack_k_records, pack_v_records, unpack_k_records, unpack_v_records,
     cache_block_bytes, write_paged, read_paged, decode_attention,
     exact_attention, quantize_exclusions, search, causal_attention,
@@ -35,7 +35,7 @@ from .turboquant import (
 __all__ = [
     "splitmix64_stream", "uniform_stream", "gaussian_stream",
     "Codebook", "lloyd_max_gaussian", "lloyd_max_sphere", "rotation_matrix", "qjl_matrix",
-    "TQParams", "make_params", "quantize_vectors", "estimate_scores",
+    "TQParams", "make_params", "assign_codes", "quantize_vectors", "estimate_scores",
     "pack_k_records", "pack_v_records", "unpack_k_records", "unpack_v_records",
     "cache_block_bytes", "write_paged", "read_paged", "decode_attention",
     "exact_attention", "search", "causal_attention", "quantize_exclusions",

@@ -167,7 +167,7 @@ def lloyd_max_sphere(bits, d, tol=1e-15, max_iter=200000):
         return cmom * (1.0 - z2) ** ((d - 1) / 2.0)
 
     h = 1 << (bits - 1)
-    a = (np.arange(h) + 0.5) * 3.0 / h
+    a = (np.arange(h) + 0.5) * min(3.0, rd) / h     # every starting cell inside the support (0, sqrt(d))
     it = 0
     for it in range(1, max_iter + 1):
         lo = np.concatenate([[0.0], 0.5 * (a[:-1] + a[1:])])
@@ -242,6 +242,15 @@ def fp16_round(x):
     return np.asarray(x, dtype=np.float64).astype(np.float16).astype(np.float64)
 
 
+def assign_codes(u, boundaries):
+    """Code of each unit-variance coordinate u: the number of boundaries t_k with u >= t_k
+    ([P4] §4.2: a value falls in the cell between two boundaries; a value exactly on a
+    boundary goes to the upper cell)."""
+    u = np.asarray(u, dtype=np.float64)
+    t = np.asarray(boundaries, dtype=np.float64)
+    return np.sum(u[..., None] >= t, axis=-1).astype(np.int64)
+
+
 def quantize_vectors(params, X, kind):
     """Quantize rows of X (n x d, any float dtype, taken exactly into fp64).
 
@@ -261,7 +270,7 @@ def quantize_vectors(params, X, kind):
     chat = np.empty(U.shape)
     for j in range(d):
         bk = books[j]
-        codes[:, j] = np.searchsorted(bk.boundaries, U[:, j], side="right")
+        codes[:, j] = assign_codes(U[:, j], bk.boundaries)
         chat[:, j] = bk.centroids[codes[:, j]]
     n16 = fp16_round(norm)
     out = {"codes": codes, "norm": norm, "n16": n16, "u": U, "y": Y}

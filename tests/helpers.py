@@ -1,6 +1,6 @@
 """Shared helpers for the GPU parity tests: oracle-built caches and field-wise comparison.
 
-Parity bars (spec reading):
+Parity bars (the readings of the target tolerances these tests apply):
   * codes and sign bits bit-exact, except codes whose unit-variance value is
     within 1e-6 of a boundary and the signs of such vectors (and signs with
     |S r| < 1e-6 ||r||); the excluded count must stay <= 1e-4 of all codes

@@ -120,3 +120,14 @@ def test_codebook_ex_arguments(tq):
     assert st("tq_host_codebook_ex", 3, 3, tq.TQ_CODEBOOK_SPHERE, c.ctypes.data, t.ctypes.data) == tq.TQ_ERR_INVALID_ARG
     assert st("tq_host_codebook_ex", 0, 128, tq.TQ_CODEBOOK_SPHERE, c.ctypes.data, t.ctypes.data) == tq.TQ_ERR_INVALID_ARG
     assert st("tq_host_codebook_ex", 3, 128, tq.TQ_CODEBOOK_SPHERE, None, t.ctypes.data) == tq.TQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bits,d", [(3, 4), (4, 5), (3, 128)])
+def test_sphere_codebook_small_d_matches_oracle(tq, bits, d):
+    """The exact-density codebook at small d (support shorter than the Gaussian bulk) is finite and equals the
+    oracle's."""
+    c, t = tq.tq_host_codebook_ex(bits, d, tq.TQ_CODEBOOK_SPHERE)
+    cb = oracle.lloyd_max_sphere(bits, d)
+    assert np.all(np.isfinite(c)) and np.all(np.isfinite(t))
+    assert np.max(np.abs(c - cb.centroids)) < 1e-10
+    assert np.max(np.abs(t - cb.boundaries)) < 1e-10

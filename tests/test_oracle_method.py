@@ -90,19 +90,72 @@ def test_distortion_per_bit(bits):
     assert 4.0 ** -bits <= err <= math.sqrt(3) * math.pi / 2 * 4.0 ** -bits
 
 
-def test_codes_follow_boundaries_and_tie_rounds_up(p3):
-    cb = p3.books[3]
-    # craft a vector whose rotated unit-variance coordinates are chosen exactly
-    u = np.linspace(-3, 3, D)
-    u[0] = cb.boundaries[2]         # exactly on a boundary -> upper cell
-    u[1] = np.nextafter(cb.boundaries[2], -np.inf)
-    y = u / np.linalg.norm(u)       # ||x|| = 1 -> u = sqrt(d) y exactly up to rounding
-    x = p3.Pi.T @ y
-    q = oracle.quantize_vectors(p3, x[None, :], "v")
-    uu = q["u"][0]
-    expect = np.searchsorted(cb.boundaries, uu, side="right")
-    assert np.array_equal(q["codes"][0], expect)
-    assert np.all((q["codes"] >= 0) & (q["codes"] < 8))
+# The 3-bit Gaussian Lloyd-Max boundaries (Max 1960, tests/golden/max1960_gaussian.txt), to 4 decimals:
+# 0, +-0.5006, +-1.0500, +-1.7480.  Codes below are counted by hand from those values.
+def test_codes_on_between_and_just_below_boundaries(p3):
+    """code = #{k : u >= t_k}: on a boundary -> the upper cell, one ulp below -> the lower cell."""
+    t = p3.books[3].boundaries
+    assert np.allclose(t, [-1.7480, -1.0500, -0.5006, 0.0, 0.5006, 1.0500, 1.7480], atol=1e-4)
+    on = oracle.assign_codes(t, t)
+    below = oracle.assign_codes(np.nextafter(t, -np.inf), t)
+    above = oracle.assign_codes(np.nextafter(t, np.inf), t)
+    assert on.tolist() == [1, 2, 3, 4, 5, 6, 7]
+    assert below.tolist() == [0, 1, 2, 3, 4, 5, 6]
+    assert above.tolist() == [1, 2, 3, 4, 5, 6, 7]
+    between = [-9.0, -2.0, -1.5, -0.8, -0.3, 0.3, 0.8, 1.5, 2.0, 9.0, -0.0]
+    assert oracle.assign_codes(between, t).tolist() == [0, 0, 1, 2, 3, 4, 5, 6, 7, 7, 4]
+    # 1 bit: the single boundary 0 -> negative 0, non-negative 1; 2 bits: 0, +-0.9816 (Max 1960)
+    t1, t2 = p3.books.get(1) or oracle.lloyd_max_gaussian(1), oracle.lloyd_max_gaussian(2)
+    assert oracle.assign_codes([-1e-300, 0.0, 1e-300], t1.boundaries).tolist() == [0, 1, 1]
+    assert oracle.assign_codes([-1.0, -0.9, -1e-9, 0.0, 0.9, 1.0], t2.boundaries).tolist() == [0, 1, 1, 2, 2, 3]
+
+
+def test_quantize_assigns_exact_u_end_to_end():
+    """Identity rotation, d = 64, x with sixteen entries +-2 and the rest 0: ||x|| = 8 and u = sqrt(64) x / 8 = x
+    exactly, so the codes through quantize_vectors are known by hand (3 bits: u = -2 -> 0, u = 0 -> 4 (tie up),
+    u = 2 -> 7); keys: n16 = 8 and r~ = y - c[code] exactly representable."""
+    import dataclasses
+    p = oracle.make_params(d=64, m=32, k_bits=(3, 3), k_split=32, v_bits=(3, 3), v_split=32, seed=0)
+    p = dataclasses.replace(p, Pi=np.eye(64))
+    x = np.zeros(64)
+    x[:8] = 2.0
+    x[8:16] = -2.0
+    q = oracle.quantize_vectors(p, x[None, :], "k")
+    assert q["norm"][0] == 8.0 and q["n16"][0] == 8.0
+    assert np.array_equal(q["u"][0], x)
+    assert q["codes"][0].tolist() == [7] * 8 + [0] * 8 + [4] * 48
+    c = p.books[3].centroids
+    want_r = x - np.array([c[7]] * 8 + [c[0]] * 8 + [c[4]] * 48)     # y - (n16/sqrt(d)) c[code] with y = x, n16/sqrt(d) = 1
+    assert np.array_equal(q["r"][0], want_r)
+
+
+def test_quantize_exclusions_by_hand():
+    """Codes within eps = 1e-6 of a boundary and signs with |z| < eps rho are excluded; one excluded code
+    excludes every sign bit of its vector."""
+    p = oracle.make_params(d=D, m=128, k_bits=(3, 3), v_bits=(3, 3), seed=0)
+    t = p.books[3].boundaries
+    U = np.full((3, D), 0.25)                   # 0.25: more than 0.25 from every 3-bit boundary
+    U[0, 5] = t[4] + 5e-7                        # inside the band
+    U[0, 70] = t[1] - 9.9e-7                     # inside
+    U[1, 9] = t[6] + 2e-6                        # outside
+    U[1, 100] = t[3] - 1.01e-6                   # outside (boundary 0)
+    rho = np.array([2.0, 4.0, 1.0])
+    Z = np.full((3, 128), 0.5)
+    Z[1, 3] = 3.9e-6                             # |z| < 1e-6 * 4
+    Z[1, 77] = -4.1e-6                           # not
+    Z[2, 0] = -0.0                               # |z| = 0 < 1e-6
+    Z[2, 127] = 1.1e-6                           # not (rho = 1)
+    ex = oracle.quantize_exclusions(p, {"u": U, "z": Z, "rho": rho}, "k")
+    want_codes = np.zeros((3, D), dtype=bool)
+    want_codes[0, [5, 70]] = True
+    assert np.array_equal(ex["codes"], want_codes)
+    want_signs = np.zeros((3, 128), dtype=bool)
+    want_signs[0, :] = True                      # vector 0 has excluded codes
+    want_signs[1, 3] = True
+    want_signs[2, 0] = True
+    assert np.array_equal(ex["signs"], want_signs)
+    ex_v = oracle.quantize_exclusions(p, {"u": U}, "v")
+    assert "signs" not in ex_v and np.array_equal(ex_v["codes"], want_codes)
 
 
 def test_zero_vector(p3):

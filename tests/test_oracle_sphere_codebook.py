@@ -46,11 +46,12 @@ def test_one_bit_closed_form(d):
     assert book.centroids[0] == -book.centroids[1]
 
 
-@pytest.mark.parametrize("bits", [2, 3, 4])
-def test_lloyd_conditions_by_quadrature(bits):
-    """Each centroid is the conditional mean of its cell under f, each boundary the midpoint of its neighbours."""
-    d = 128
+@pytest.mark.parametrize("bits,d", [(2, 128), (3, 128), (4, 128), (3, 4), (4, 5), (4, 9)])
+def test_lloyd_conditions_by_quadrature(bits, d):
+    """Each centroid is the conditional mean of its cell under f, each boundary the midpoint of its neighbours.
+    Small d (support |u| < sqrt(d) shorter than the Gaussian's bulk) included: every cell must keep mass."""
     book, f = lloyd_max_sphere(bits, d), _density(d)
+    assert np.all(np.isfinite(book.centroids)) and np.all(np.abs(book.centroids) < math.sqrt(d))
     for (a, b), c in zip(_cells(book, d), book.centroids):
         p0 = integrate.quad(f, a, b, epsabs=1e-15, epsrel=1e-13)[0]
         m1 = integrate.quad(lambda u: u * f(u), a, b, epsabs=1e-15, epsrel=1e-13)[0]
