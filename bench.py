@@ -3,13 +3,16 @@
 
 A step is one pass of the whole path over one batch: for the decode workloads
 (default c3, Llama-3.1-8B-shaped, 16 x 32768 tokens, 3.5-bit K + QJL / 3.5-bit
-V) it appends one new token per sequence (tq_quantize) and runs decode
-attention over the L+1 cached tokens (tq_decode_attention, three stages); the
-quantize workload c2 appends 2,097,152 K/V vectors.  Headline value: packed
-cache bytes read per decode step / step time (GB/s); the c2 quantize rate
-(vectors/s) rides along in "quantize".  Inputs are synthetic (seeded), resident
-in HBM; the packed caches are larger than L2, so no flush is needed between
-steps.  --impl reference times the fp64 CPU oracle on the same workload.
+V) it appends one new token per sequence and runs decode attention over the
+L+1 cached tokens (tq_append_decode: quantize-append, query prep, split-K
+partials, merge); c1 (one head, 1024 fp32 tokens) decodes without an append.
+Headline value: packed cache bytes read per decode step / step time (GB/s) on
+c3; the c4, c5 and c1 decode workloads ride along under their own keys, and
+the c2 quantize rate (vectors/s) under "quantize".  Inputs are synthetic
+(seeded) and resident in HBM; caches under twice the L2 size get an L2 flush
+before every timed step.  cpu_baseline: the fp64 oracle on the host cores
+(every core, and one core alone).  --impl reference times the oracle alone on
+the same workload.
 """
 
 import argparse
@@ -42,12 +45,14 @@ def parse(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="c3", choices=["c3", "c4", "c5"])
+    ap.add_argument("--config", default="c3", choices=["c1", "c3", "c4", "c5"])
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     ap.add_argument("--no-quantize", action="store_true", help="skip the c2 quantize measurement")
     ap.add_argument("--only", default="", choices=["", "quantize", "search"],
                     help="quantize: run the c2 quantize measurement alone (profiling; --batch scales it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-others", action="store_true", help="time the headline decode workload only")
+    ap.add_argument("--cpu-workers", type=int, default=0, help="oracle worker processes (0: every host core)")
     return ap.parse_args(argv)
 
 
@@ -105,7 +110,7 @@ class ClockSampler:
                 self.samples.append(c.value)
             if self.reason_fn(self.h, ctypes.byref(r)) == 0:
                 self.reasons |= r.value
-            time.sleep(0.005)
+            time.sleep(0.001)
 
     def __enter__(self):
         if self.ok:
@@ -149,6 +154,10 @@ def traffic_for(kernel_file, kernel, workload):
 # ---------------------------------------------------------------------------
 
 class DecodeBench:
+    """One decode workload resident on the GPU.  A step with append (c3-c5) is one tq_append_decode_ex call:
+    quantize-append the new token at position L, decode over L+1; without append (c1) it is the three stages of
+    tq_decode_attention_ex over the cached tokens."""
+
     def __init__(self, w, torch, tq):
         self.w, self.torch, self.tq = w, torch, tq
         dev = torch.device("cuda", torch.cuda.current_device())
@@ -156,6 +165,9 @@ class DecodeBench:
         cfg = tq.make_config(k_bits=w.k_bits, v_bits=w.v_bits, m=w.m, seed=w.seed, k_qjl=w.qjl)
         self.ctx = tq.tq_create_ex(cfg)
         B, H, Hq = w.batch, w.kv_heads, w.q_heads
+        self.f32 = w.dtype == "f32"
+        self.tdt = torch.float32 if self.f32 else torch.bfloat16
+        self.dt = tq.TQ_F32 if self.f32 else tq.TQ_BF16
         self.lens = wl.seq_lens(w)
         self.bt = wl.block_table(w)
         self.pps = self.bt.shape[1]
@@ -170,70 +182,95 @@ class DecodeBench:
             L = int(self.lens[b])
             for s0 in range(0, L, 8192):
                 n = min(8192, L - s0)
-                K = torch.from_numpy(wl.kv_tokens(w, "k", b, s0, n)).to(dev).to(torch.bfloat16)
-                V = torch.from_numpy(wl.kv_tokens(w, "v", b, s0, n)).to(dev).to(torch.bfloat16)
+                K = torch.from_numpy(wl.kv_tokens(w, "k", b, s0, n)).to(dev).to(self.tdt)
+                V = torch.from_numpy(wl.kv_tokens(w, "v", b, s0, n)).to(dev).to(self.tdt)
                 zero.fill_(s0)
-                tq.tq_quantize(self.ctx, K, V, tq.TQ_BF16, 1, n, H, zero, self.bt_d[b], self.pps, self.num_pages,
+                tq.tq_quantize(self.ctx, K, V, self.dt, 1, n, H, zero, self.bt_d[b], self.pps, self.num_pages,
                                self.kc, self.vc)
         torch.cuda.synchronize()
         assert tq.tq_check_device_status(self.ctx) == 0
-        self.knew_h = torch.from_numpy(wl.new_tokens(w, "k")).to(torch.bfloat16).pin_memory()
-        self.vnew_h = torch.from_numpy(wl.new_tokens(w, "v")).to(torch.bfloat16).pin_memory()
-        self.q_h = torch.from_numpy(wl.queries(w)).to(torch.bfloat16).pin_memory()
-        self.knew = self.knew_h.to(dev)
-        self.vnew = self.vnew_h.to(dev)
+        self.q_h = torch.from_numpy(wl.queries(w)).to(self.tdt).pin_memory()
         self.q = self.q_h.to(dev)
+        self.append = w.append
+        extra = 1 if w.append else 0
+        if w.append:
+            self.knew_h = torch.from_numpy(wl.new_tokens(w, "k")).to(self.tdt).pin_memory()
+            self.vnew_h = torch.from_numpy(wl.new_tokens(w, "v")).to(self.tdt).pin_memory()
+            self.knew = self.knew_h.to(dev)
+            self.vnew = self.vnew_h.to(dev)
         self.start = torch.from_numpy(self.lens.astype(np.int32)).to(dev)
-        self.lens1 = torch.from_numpy((self.lens + 1).astype(np.int32)).to(dev)
-        self.max_len = int(self.lens.max()) + 1
+        self.max_len = int(self.lens.max()) + extra
         # split-K chunk: the workload's own, else the library's choice for the actual total length
-        self.chunk = w.chunk or tq.tq_decode_chunk(self.ctx, B, Hq, H, int((self.lens + 1).sum()), self.max_len,
-                                                   fused_append=True)
+        self.chunk = w.chunk or tq.tq_decode_chunk(self.ctx, B, Hq, H, int((self.lens + extra).sum()), self.max_len,
+                                                   fused_append=w.append)
         self.ws_n = tq.tq_workspace_size(self.ctx, B, Hq, self.max_len, self.chunk)
         self.ws = torch.empty(self.ws_n, dtype=torch.uint8, device=dev)
         self.out = torch.empty(B, Hq, 128, dtype=torch.float32, device=dev)
         self.out_h = torch.empty(B, Hq, 128, dtype=torch.float32).pin_memory()
-        self.tokens = int((self.lens + 1).sum())
+        self.tokens = int((self.lens + extra).sum())
         self.bytes_step = self.tokens * H * wl.packed_bytes_per_token_head(w)
         # append (one quantize launch for K and V) + qprep + partials + merge
-        self.launches_per_step = 4
+        self.launches_per_step = 4 if w.append else 3
 
     def _marshal(self, stream):
-        """ctypes arguments of the fused per-step call, built once per stream (pointers are fixed)."""
+        """ctypes arguments of the per-step call, built once per stream (pointers are fixed)."""
         import ctypes
         w, tq = self.w, self.tq
         sp = stream.cuda_stream
-        self._args = (stream, [self.ctx, self.knew.data_ptr(), self.vnew.data_ptr(), self.q.data_ptr(), tq.TQ_BF16,
-                               w.batch, w.q_heads, w.kv_heads, self.start.data_ptr(), self.max_len,
-                               self.bt_d.data_ptr(), self.pps, self.num_pages, self.kc.data_ptr(), self.vc.data_ptr(),
-                               self.chunk, ctypes.c_float(1.0 / math.sqrt(128)), self.out.data_ptr(),
-                               self.ws.data_ptr(), self.ws_n, sp])
+        scale = ctypes.c_float(1.0 / math.sqrt(128))
+        if self.append:
+            args = [self.ctx, self.knew.data_ptr(), self.vnew.data_ptr(), self.q.data_ptr(), self.dt,
+                    w.batch, w.q_heads, w.kv_heads, self.start.data_ptr(), self.max_len,
+                    self.bt_d.data_ptr(), self.pps, self.num_pages, self.kc.data_ptr(), self.vc.data_ptr(),
+                    self.chunk, scale, self.out.data_ptr(), self.ws.data_ptr(), self.ws_n, sp]
+        else:
+            args = [self.ctx, self.q.data_ptr(), self.dt, w.batch, w.q_heads, w.kv_heads, self.start.data_ptr(),
+                    self.max_len, self.bt_d.data_ptr(), self.pps, self.num_pages, self.kc.data_ptr(),
+                    self.vc.data_ptr(), self.chunk, scale, self.out.data_ptr(), self.ws.data_ptr(), self.ws_n]
+        self._args = (stream, args, sp)
 
     def step(self, stream, ev=None):
-        """One decode step through the fused C call: quantize-append the new token at position L, decode over L+1;
-        `ev` (begin, end) events are recorded by the library around the partials kernel."""
+        """One decode step through the C ABI; `ev` (begin, end) events bracket the partials kernel."""
         if getattr(self, "_args", (None,))[0] is not stream:
             self._marshal(stream)
-        handles = [None, None]
-        if ev is not None:
-            handles = [e.cuda_event for e in ev]
-        st = self.tq._lib.tq_append_decode_ex(*self._args[1], *handles)
-        if st != 0:
-            raise self.tq.TQError("tq_append_decode_ex", st)
+        lib = self.tq._lib
+        if self.append:
+            handles = [None, None] if ev is None else [e.cuda_event for e in ev]
+            st = lib.tq_append_decode_ex(*self._args[1], *handles)
+            if st != 0:
+                raise self.tq.TQError("tq_append_decode_ex", st)
+            return
+        args, sp = self._args[1], self._args[2]
+        for stage in (self.tq.TQ_STAGE_QPREP, self.tq.TQ_STAGE_PARTIALS, self.tq.TQ_STAGE_MERGE):
+            if ev is not None and stage == self.tq.TQ_STAGE_PARTIALS:
+                ev[0].record(stream)
+            st = lib.tq_decode_attention_ex(*args, stage, sp)
+            if st != 0:
+                raise self.tq.TQError("tq_decode_attention_ex", st)
+            if ev is not None and stage == self.tq.TQ_STAGE_PARTIALS:
+                ev[1].record(stream)
 
     def step_e2e(self, stream):
-        """One step through the public fused call, inputs from pinned host memory, output back to host."""
+        """One step through the public call, inputs from pinned host memory, output back to host."""
         w, tq = self.w, self.tq
-        self.knew.copy_(self.knew_h, non_blocking=True)
-        self.vnew.copy_(self.vnew_h, non_blocking=True)
         self.q.copy_(self.q_h, non_blocking=True)
-        tq.tq_append_decode(self.ctx, self.knew, self.vnew, self.q, tq.TQ_BF16, w.batch, w.q_heads, w.kv_heads,
-                            self.start, self.max_len, self.bt_d, self.pps, self.num_pages, self.kc, self.vc, self.chunk,
-                            1.0 / math.sqrt(128), self.out, self.ws, self.ws_n, stream)
+        if self.append:
+            self.knew.copy_(self.knew_h, non_blocking=True)
+            self.vnew.copy_(self.vnew_h, non_blocking=True)
+            tq.tq_append_decode(self.ctx, self.knew, self.vnew, self.q, self.dt, w.batch, w.q_heads, w.kv_heads,
+                                self.start, self.max_len, self.bt_d, self.pps, self.num_pages, self.kc, self.vc,
+                                self.chunk, 1.0 / math.sqrt(128), self.out, self.ws, self.ws_n, stream)
+        else:
+            tq.tq_decode_attention(self.ctx, self.q, self.dt, w.batch, w.q_heads, w.kv_heads, self.start,
+                                   self.max_len, self.bt_d, self.pps, self.num_pages, self.kc, self.vc, self.chunk,
+                                   1.0 / math.sqrt(128), self.out, self.ws, self.ws_n, stream)
         self.out_h.copy_(self.out, non_blocking=True)
 
     def e2e_bytes(self):
-        return (self.knew.numel() + self.vnew.numel() + self.q.numel()) * 2, self.out.numel() * 4
+        h2d = self.q.numel() * self.q.element_size()
+        if self.append:
+            h2d += (self.knew.numel() + self.vnew.numel()) * self.knew.element_size()
+        return h2d, self.out.numel() * 4
 
     def close(self):
         self.tq.tq_destroy(self.ctx)
@@ -324,6 +361,57 @@ def l2_flusher(torch, bytes_step):
     return (lambda: buf.zero_()), (f"packed cache {bytes_step / 2**20:.0f} MiB < 2x L2 ({l2 / 2**20:.0f} MiB): "
                                    f"a {4 * l2 / 2**20:.0f} MiB buffer is written before every timed step, "
                                    f"each step timed alone")
+
+
+def decode_measure(torch, tq, w, stream, steps, warmup, dist, peak, peak_kind, world, profile=False):
+    """One decode workload: `steps` timed steps after `warmup` (CUDA events on the launch stream), the partials
+    kernel timed by events recorded inside every step, then the same steps end to end from pinned host memory."""
+    db = DecodeBench(w, torch, tq)
+    ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(steps)]
+    for pair in ev:                      # create the CUDA events (the library records them inside the step)
+        for e in pair:
+            e.record(stream)
+    for _ in range(warmup):
+        db.step(stream)
+    torch.cuda.synchronize()
+    flush, l2_note = l2_flusher(torch, db.bytes_step)
+    sampler = ClockSampler(torch)
+    with sampler:                        # clocks over the timed steps and the end-to-end steps
+        ms = timed(torch, stream, lambda i=None: db.step(stream, ev[i] if i is not None else None), steps, 0, dist,
+                   flush)
+        ms_e2e = timed(torch, stream, lambda i=None: db.step_e2e(stream), steps, warmup, dist, flush)
+    kern_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    ms_step = ms / steps
+    value = db.bytes_step * world / (ms_step * 1e-3) / 1e9
+    achieved = db.bytes_step / (kern_ms * 1e-3) / 1e9
+    h2d, d2h = db.e2e_bytes()
+    e2e_value = db.bytes_step * world / (ms_e2e / steps * 1e-3) / 1e9
+    flags = tq.tq_check_device_status(db.ctx)
+    ctx_desc = f"context {int(db.lens.max())}" if w.len_range is None else \
+        f"context uniform in [{w.len_range[0]}, {w.len_range[1]}] (sum {int(db.lens.sum())})"
+    step_desc = "append 1 token + attention" if w.append else "attention over the cached tokens (no append)"
+    rec = {
+        "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms_step, 5), "steps": steps,
+        "warmup": warmup, "hbm_fraction": round(value / world / peak, 4),
+        "config": {"workload": f"{w.name}: decode step = {step_desc}, batch {w.batch}, {w.q_heads}/{w.kv_heads} "
+                               f"heads, head_dim 128, {ctx_desc}{'+1' if w.append else ''}, "
+                               f"K {w.k_bits} bits{' + QJL m=%d' % w.m if w.qjl else ''}, V {w.v_bits} bits, "
+                               f"{'fp32' if w.dtype == 'f32' else 'bf16'} inputs",
+                   "split_k_chunk_tokens": db.chunk, "packed_bytes_per_step": db.bytes_step, "l2": l2_note},
+        "roofline": {"kernel": "lut_partials_kernel (split-K partials: scoring, online softmax, value sums)",
+                     "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": db.bytes_step, "avg_launch_ms": round(kern_ms, 5),
+                     "traffic": None if profile else traffic_for("tq_decode_lut.cu", "lut_partials_kernel", w.name)},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": steps * db.launches_per_step,
+        "clocks": sampler.result(),
+        "device_flags": flags,
+    }
+    db.close()
+    del db
+    torch.cuda.empty_cache()
+    return rec
 
 
 def quantize_measure(torch, tq, qw, stream, qsteps, warmup, dist, peak, peak_kind, world):
@@ -446,6 +534,10 @@ def run_ours(args):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    # the oracle's worker processes start before the first GPU call (spawn)
+    pool = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.only:
+        pool = OraclePool(wl.WORKLOADS[args.config], cpu_workers(args.cpu_workers))
     torch.cuda.set_device(local)
     dist = None
     if world > 1:
@@ -454,9 +546,10 @@ def run_ours(args):
         dist = tdist
     stream = torch.cuda.current_stream()
     peak, peak_kind = peaks()
+    warmup = max(3, args.warmup)
 
     if args.only == "search":
-        line = search_measure(torch, tq, stream, args.steps, max(3, args.warmup), peak, peak_kind)
+        line = search_measure(torch, tq, stream, args.steps, warmup, peak, peak_kind)
         line.update({"n_gpus": world, "scaling": "weak", "vs_baseline": None})
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = oracle_search_sample()
@@ -468,8 +561,7 @@ def run_ours(args):
     if args.only == "quantize":
         qw = wl.WORKLOADS["c2"].scaled(batch=args.batch) if args.batch else wl.WORKLOADS["c2"]
         line = {"metric": "KV vectors quantized/s (quantize only)"}
-        line.update(quantize_measure(torch, tq, qw, stream, args.steps, max(3, args.warmup), dist, peak, peak_kind,
-                                     world))
+        line.update(quantize_measure(torch, tq, qw, stream, args.steps, warmup, dist, peak, peak_kind, world))
         if rank == 0:
             print(json.dumps(line), flush=True)
         if dist is not None:
@@ -478,60 +570,35 @@ def run_ours(args):
     w = wl.WORKLOADS[args.config]
     if args.batch:
         w = w.scaled(batch=args.batch)
-    db = DecodeBench(w, torch, tq)
-    steps, warmup = args.steps, max(3, args.warmup)
-    ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(steps)]
-    for pair in ev:                      # create the CUDA events (the library records them inside the step)
-        for e in pair:
-            e.record(stream)
-    for _ in range(warmup):
-        db.step(stream)
-    torch.cuda.synchronize()
-    flush, l2_note = l2_flusher(torch, db.bytes_step)
-    sampler = ClockSampler(torch)
-    with sampler:
-        ms = timed(torch, stream, lambda i=None: db.step(stream, ev[i] if i is not None else None), steps, 0, dist,
-                   flush)
-    kern_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    ms_step = ms / steps
-    value = db.bytes_step * world / (ms_step * 1e-3) / 1e9
-    achieved = db.bytes_step / (kern_ms * 1e-3) / 1e9
-    # end to end through the fused C-ABI call with host buffers
-    ms_e2e = timed(torch, stream, lambda i=None: db.step_e2e(stream), steps, warmup, dist, flush)
-    h2d, d2h = db.e2e_bytes()
-    e2e_value = db.bytes_step * world / (ms_e2e / steps * 1e-3) / 1e9
-    flags = tq.tq_check_device_status(db.ctx)
+    head = decode_measure(torch, tq, w, stream, args.steps, warmup, dist, peak, peak_kind, world,
+                          profile=bool(args.batch))
     line = {
         "metric": "quantized-KV decode attention GB/s (% of HBM peak); KV vectors quantized/s",
-        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps, "warmup": warmup,
-        "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "packed 2-4 bit codes + QJL signs, fp32 accumulation", "data": "synthetic (seeded N(0,1), outlier channels)",
-        "config": {"workload": f"{w.name}: decode step = append 1 token + attention, batch {w.batch}, "
-                               f"{w.q_heads}/{w.kv_heads} heads, head_dim 128, context {int(db.lens.max())}+1, "
-                               f"K {w.k_bits} bits + QJL m={w.m}, V {w.v_bits} bits",
-                   "split_k_chunk_tokens": db.chunk,
-                   "packed_bytes_per_step": db.bytes_step, "hbm_fraction": round(value / world / peak, 4),
-                   "l2": l2_note,
-                   "parallelism": f"replicas x{world}, no collective"},
-        "roofline": {"kernel": "lut_partials_kernel (split-K partials: scoring, online softmax, value sums)",
-                     "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                     "algorithmic_bytes_per_launch": db.bytes_step, "avg_launch_ms": round(kern_ms, 5),
-                     "traffic": None if args.batch else traffic_for("tq_decode_lut.cu", "lut_partials_kernel", w.name)},
-        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": steps * db.launches_per_step,
-        "clocks": sampler.result(),
-        "device_flags": flags,
+        "value": head["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": warmup,
+        "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "packed 2-4 bit codes + QJL signs, fp32 accumulation",
+        "data": "synthetic (seeded N(0,1), outlier channels)",
+        "config": dict(head["config"], hbm_fraction=head["hbm_fraction"],
+                       parallelism=f"replicas x{world}, no collective"),
+        "roofline": head["roofline"], "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"], "device_flags": head["device_flags"],
     }
-    db.close()
-    del db
-    torch.cuda.empty_cache()
+    if not args.no_others and not args.batch:
+        for name in ("c4", "c5", "c1"):
+            if name == args.config:
+                continue
+            rec = decode_measure(torch, tq, wl.WORKLOADS[name], stream, args.steps, warmup, dist, peak, peak_kind,
+                                 world)
+            line[name] = rec
+            line["gpu_launches"] += rec["gpu_launches"]
     if not args.no_quantize:
-        line["quantize"] = quantize_measure(torch, tq, wl.WORKLOADS["c2"], stream, max(3, min(steps, 20)), warmup,
-                                            dist, peak, peak_kind, world)
+        line["quantize"] = quantize_measure(torch, tq, wl.WORKLOADS["c2"], stream, max(3, min(args.steps, 20)),
+                                            warmup, dist, peak, peak_kind, world)
         line["gpu_launches"] += line["quantize"]["steps"]
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_decode_sample(w, seconds=15.0)
+    if pool is not None:
+        line["cpu_baseline"] = cpu_baseline(pool, w)
+        line["quantize"]["cpu_baseline"] = pool.quantize_rates() if "quantize" in line else None
+        pool.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -541,6 +608,39 @@ def run_ours(args):
 # ---------------------------------------------------------------------------
 # the oracle on the host cores (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
+
+def cpu_workers(requested=0):
+    """Host cores this process may run on (or `requested`, if smaller and positive)."""
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:
+        n = os.cpu_count() or 1
+    return min(n, requested) if requested > 0 else n
+
+
+def cpu_model():
+    """lscpu's model name (with the vendor where lscpu gives one), else /proc/cpuinfo's, else the machine."""
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        f = {k.strip(): v.strip() for k, _, v in (ln.partition(":") for ln in out.splitlines())}
+        name = f.get("Model name", "")
+        if name:
+            vendor = f.get("Vendor ID", "")
+            return f"{vendor} {name}".strip() if vendor and vendor not in name else name
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for ln in fh:
+                k, _, v = ln.partition(":")
+                if k.strip().lower() in ("model name", "cpu model"):
+                    return v.strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
 
 class OracleDecode:
     """One (sequence, KV head) of the workload, quantized and decoded by the fp64 oracle."""
@@ -557,35 +657,160 @@ class OracleDecode:
         V = wl.kv_tokens(w, "v", b)[:, h].astype(np.float64)
         self.kraw = oracle.pack_k_records(self.p, oracle.quantize_vectors(self.p, K, "k"))
         self.vraw = oracle.pack_v_records(self.p, oracle.quantize_vectors(self.p, V, "v"))
-        self.knew = wl.new_tokens(w, "k")[b, :, h].astype(np.float64)
-        self.vnew = wl.new_tokens(w, "v")[b, :, h].astype(np.float64)
+        self.append = w.append
+        if w.append:
+            self.knew = wl.new_tokens(w, "k")[b, :, h].astype(np.float64)
+            self.vnew = wl.new_tokens(w, "v")[b, :, h].astype(np.float64)
         G = w.q_heads // w.kv_heads
         self.Q = wl.queries(w)[b, h * G:(h + 1) * G].astype(np.float64)
-        self.bytes = (L + 1) * wl.packed_bytes_per_token_head(w)
+        self.bytes = (L + (1 if w.append else 0)) * wl.packed_bytes_per_token_head(w)
 
     def step(self):
         o, p = self.o, self.p
-        kn = o.pack_k_records(p, o.quantize_vectors(p, self.knew, "k"))
-        vn = o.pack_v_records(p, o.quantize_vectors(p, self.vnew, "v"))
-        kr = o.unpack_k_records(p, {k: np.concatenate([self.kraw[k], kn[k]]) for k in kn})
-        vr = o.unpack_v_records(p, {k: np.concatenate([self.vraw[k], vn[k]]) for k in vn})
+        kraw, vraw = self.kraw, self.vraw
+        if self.append:
+            kn = o.pack_k_records(p, o.quantize_vectors(p, self.knew, "k"))
+            vn = o.pack_v_records(p, o.quantize_vectors(p, self.vnew, "v"))
+            kraw = {k: np.concatenate([kraw[k], kn[k]]) for k in kn}
+            vraw = {k: np.concatenate([vraw[k], vn[k]]) for k in vn}
+        kr = o.unpack_k_records(p, kraw)
+        vr = o.unpack_v_records(p, vraw)
         return [self.otq.attend_one(p, q, kr, vr, 1.0 / math.sqrt(128)) for q in self.Q]
 
 
-def oracle_decode_sample(w, seconds):
-    od = OracleDecode(w)
+def _oracle_quantize_slice(w, b):
+    """The oracle's quantize of sequence b of a quantize workload (every KV head, K and V): (vectors, seconds)."""
+    import oracle
+    p = oracle.make_params(d=128, m=w.m, k_bits=w.k_bits, v_bits=w.v_bits, seed=w.seed, k_qjl=w.qjl)
+    K = wl.kv_tokens(w, "k", b).reshape(-1, 128).astype(np.float64)
+    V = wl.kv_tokens(w, "v", b).reshape(-1, 128).astype(np.float64)
+    bt = wl.block_table(w)
+    H, T = w.kv_heads, w.seq_len
+    kc = np.zeros(bt.size * oracle.cache_block_bytes(p, "k") * H, np.uint8)
+    vc = np.zeros(bt.size * oracle.cache_block_bytes(p, "v") * H, np.uint8)
+    ti, hi = np.meshgrid(np.arange(T), np.arange(H), indexing="ij")
+    pages, slots = bt[b, ti.ravel() // 16], ti.ravel() % 16
     t0 = time.perf_counter()
-    n = 0
+    oracle.write_paged(p, "k", kc, oracle.pack_k_records(p, oracle.quantize_vectors(p, K, "k")), pages, slots,
+                       hi.ravel(), H)
+    oracle.write_paged(p, "v", vc, oracle.pack_v_records(p, oracle.quantize_vectors(p, V, "v")), pages, slots,
+                       hi.ravel(), H)
+    return len(K) + len(V), time.perf_counter() - t0
+
+
+def _oracle_worker(conn, w, b, h):
+    """Worker process: holds one (sequence, KV head) of the decode workload; runs oracle steps on request.
+    It builds its oracle cache only when asked (so it stays idle while the GPU is being timed)."""
+    if conn.recv()[0] != "init":
+        return
+    od = OracleDecode(w, b, h)
+    conn.send(("ready", od.bytes, od.L))
     while True:
-        od.step()
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or n >= 50:
+        cmd = conn.recv()
+        if cmd[0] == "step":
+            t0 = time.perf_counter()
+            for _ in range(cmd[1]):
+                od.step()
+            conn.send(("done", time.perf_counter() - t0))
+        elif cmd[0] == "quantize":
+            conn.send(("done",) + _oracle_quantize_slice(wl.WORKLOADS["c2"], cmd[1]))
+        else:
             break
-    return {"value": round(od.bytes * n / el / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} steps of sequence 0, KV head 0 ({w.q_heads // w.kv_heads} query heads): append 1 token "
-                      f"+ fp64 decode over {od.L + 1} tokens ({od.bytes} packed bytes per step), "
-                      f"numpy with 1 BLAS thread"}
+
+
+class OraclePool:
+    """One spawn-started process per host core, each holding its own (sequence, KV head) of the decode workload
+    (the first `n` of its units).  Started before the first GPU call; each worker runs numpy with one BLAS
+    thread."""
+
+    def __init__(self, w, n):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        units = [(b, h) for b in range(w.batch) for h in range(w.kv_heads)]
+        self.n = max(1, min(n, len(units)))
+        self.w = w
+        self.conns, self.procs = [], []
+        for b, h in units[:self.n]:
+            a, bconn = ctx.Pipe()
+            pr = ctx.Process(target=_oracle_worker, args=(bconn, w, b, h), daemon=True)
+            pr.start()
+            self.conns.append(a)
+            self.procs.append(pr)
+        self._ready = None
+
+    def ready(self):
+        if self._ready is None:
+            for c in self.conns:
+                c.send(("init",))
+            self._ready = [c.recv() for c in self.conns]
+        return self._ready
+
+    def step(self, workers, reps=1):
+        """`reps` oracle steps on each of the first `workers` workers at once: (bytes, wall seconds)."""
+        info = self.ready()
+        t0 = time.perf_counter()
+        for c in self.conns[:workers]:
+            c.send(("step", reps))
+        for c in self.conns[:workers]:
+            c.recv()
+        return sum(i[1] for i in info[:workers]) * reps, time.perf_counter() - t0
+
+    def quantize_rates(self):
+        """The oracle's quantize of c2 slices (one sequence = 1/32 of the workload each): one core, then every
+        worker on its own sequence at once; vectors/s, extrapolated from the slices to the whole workload."""
+        self.ready()
+        qw = wl.WORKLOADS["c2"]
+        self.conns[0].send(("quantize", 0))
+        _, nv1, s1 = self.conns[0].recv()
+        k = min(self.n, qw.batch)
+        t0 = time.perf_counter()
+        for i, c in enumerate(self.conns[:k]):
+            c.send(("quantize", i))
+        nv = sum(c.recv()[1] for c in self.conns[:k])
+        wall = time.perf_counter() - t0
+        total = 2 * qw.batch * qw.seq_len * qw.kv_heads
+        return {"value": round(nv / wall, 1), "unit": "KV vectors/s", "cores": k, "kind": "oracle",
+                "sample": f"{k} of the 32 sequences of c2 (each 1/32 of the workload: {nv1} K+V vectors) quantized, "
+                          f"packed and written through the block table at once; extrapolated to the "
+                          f"{total}-vector workload: {total / (nv / wall):.1f} s",
+                "single_core": {"value": round(nv1 / s1, 1), "unit": "KV vectors/s", "cores": 1,
+                                "sample": f"sequence 0 of c2 (1/32 of the workload, {nv1} vectors) in {s1:.2f} s; "
+                                          f"extrapolated to the workload: {total / (nv1 / s1):.1f} s"},
+                "cpu_model": cpu_model()}
+
+    def close(self):
+        for c in self.conns:
+            try:
+                c.send(("quit",))
+            except (BrokenPipeError, OSError):
+                pass
+        for pr in self.procs:
+            pr.join(timeout=30)
+            if pr.is_alive():
+                pr.kill()
+
+
+def cpu_baseline(pool, w, seconds=8.0):
+    """The oracle on the host cores: every pool worker stepping its own (sequence, KV head) at once, and one
+    worker alone; decode GB/s of packed cache read (the GPU metric's bytes)."""
+    info = pool.ready()
+    b1, s1 = pool.step(1)
+    reps1 = max(1, int(seconds / max(s1, 1e-3)) - 1)
+    b1r, s1r = pool.step(1, reps1)
+    b1, s1 = b1 + b1r, s1 + s1r
+    bn, sn = pool.step(pool.n)
+    repsn = max(1, int(seconds / max(sn, 1e-3)) - 1)
+    bnr, snr = pool.step(pool.n, repsn)
+    bn, sn = bn + bnr, sn + snr
+    L = info[0][2]
+    G = w.q_heads // w.kv_heads
+    return {"value": round(bn / sn / 1e9, 6), "unit": "GB/s", "cores": pool.n, "kind": "oracle",
+            "sample": f"{pool.n} worker processes, each its own (sequence, KV head) of {w.name} ({G} query heads, "
+                      f"{L}{'+1' if w.append else ''} tokens: append + fp64 decode per step), all stepping at once; "
+                      f"{1 + repsn} steps each; numpy with 1 BLAS thread per worker",
+            "single_core": {"value": round(b1 / s1 / 1e9, 6), "unit": "GB/s", "cores": 1,
+                            "sample": f"one worker alone, {1 + reps1} steps"},
+            "cpu_model": cpu_model(), "host_cores": cpu_workers()}
 
 
 def run_reference(args):
@@ -593,24 +818,32 @@ def run_reference(args):
     if rank != 0:
         return
     w = wl.WORKLOADS[args.config]
-    od = OracleDecode(w)
-    for _ in range(args.warmup):
-        od.step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        od.step()
-    el = time.perf_counter() - t0
-    value = od.bytes * args.steps / el / 1e9
+    pool = OraclePool(w, cpu_workers(args.cpu_workers))
+    try:
+        pool.ready()
+        for _ in range(args.warmup):
+            pool.step(pool.n)
+        tot_b, tot_s = 0, 0.0
+        for _ in range(args.steps):
+            b, s = pool.step(pool.n)
+            tot_b += b
+            tot_s += s
+    finally:
+        pool.close()
+    value = tot_b / tot_s / 1e9
+    G = w.q_heads // w.kv_heads
+    sample = (f"each step: {pool.n} worker processes, each its own (sequence, KV head) of {w.name} ({G} query heads),"
+              f" append 1 token + fp64 decode over {pool.ready()[0][2] + 1} tokens, all at once; 1 BLAS thread each")
     line = {
         "impl": "reference",
         "metric": "quantized-KV decode attention GB/s (% of HBM peak); KV vectors quantized/s",
         "value": round(value, 6), "unit": "GB/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s / max(args.steps, 1) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{w.name}: oracle sample, sequence 0 KV head 0 of the decode step"},
-        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"each step: append 1 token + fp64 decode of sequence 0, KV head 0 "
-                                   f"({w.q_heads // w.kv_heads} query heads) over {od.L + 1} tokens"},
+        "config": {"workload": f"{w.name}: oracle sample of the decode step ({pool.n} of its "
+                               f"{w.batch * w.kv_heads} (sequence, KV head) units per step)"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": pool.n, "kind": "oracle",
+                         "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

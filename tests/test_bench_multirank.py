@@ -84,7 +84,8 @@ def test_reference_line_is_one_json_object(monkeypatch, capsys):
     import bench
     monkeypatch.setenv("RANK", "0")
     monkeypatch.setenv("WORLD_SIZE", "1")
-    bench.run_reference(bench.parse(["--impl", "reference", "--steps", "1", "--warmup", "0", "--config", "c3"]))
+    bench.run_reference(bench.parse(["--impl", "reference", "--steps", "1", "--warmup", "0", "--config", "c3",
+                                     "--cpu-workers", "2"]))
     lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
     assert len(lines) == 1
     rec = json.loads(lines[0])
@@ -92,3 +93,23 @@ def test_reference_line_is_one_json_object(monkeypatch, capsys):
                 "cpu_baseline", "e2e", "config"):
         assert key in rec
     assert rec["impl"] == "reference" and rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["value"] > 0
+
+
+def test_cpu_baseline_pool_reports_cores_and_rates():
+    """The oracle pool behind cpu_baseline: spawn-started workers, every worker at once and one alone, and the
+    quantize rate on c2 slices (extrapolated and labelled so)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from online_kv_cache_02_gb300 import workloads as wl
+    w = wl.WORKLOADS["c3"].scaled(batch=1, seq_len=512)
+    pool = bench.OraclePool(w, 2)
+    try:
+        rec = bench.cpu_baseline(pool, w, seconds=0.5)
+        assert rec["cores"] == 2 and rec["kind"] == "oracle" and rec["value"] > 0
+        assert rec["single_core"]["cores"] == 1 and rec["single_core"]["value"] > 0
+        assert rec["cpu_model"] and rec["host_cores"] >= 1
+        q = pool.quantize_rates()
+        assert q["cores"] == 2 and q["value"] > 0 and q["single_core"]["value"] > 0
+        assert "extrapolated" in q["sample"] and "extrapolated" in q["single_core"]["sample"]
+    finally:
+        pool.close()

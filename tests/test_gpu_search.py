@@ -123,3 +123,16 @@ def test_search_bad_page_and_arguments():
                 tq.tq_search(ctx, qd, code, 3, kc, bt, num_pages, n_db, k_top, out_s, out_i, ws, ws_n)
     finally:
         tq.tq_destroy(ctx)
+
+
+def test_query_count_beyond_the_grid_is_rejected_before_launch():
+    """nq above 65535 x 8 queries returns TQ_ERR_UNSUPPORTED before anything runs (the pointers are never read)."""
+    ctx = ctx_for(wl.WORKLOADS["c2"])
+    try:
+        st = tq.raw_status("tq_search", ctx, 256, tq.TQ_BF16, 65535 * 8 + 1, 256, 256, 1, 16, 1, 256, 256, 256,
+                           1 << 40, None)
+        assert st == tq.TQ_ERR_UNSUPPORTED
+        st = tq.raw_status("tq_search", ctx, 256, tq.TQ_BF16, 65535 * 8, 256, 256, 1, 16, 1, 256, 256, 256, 0, None)
+        assert st == tq.TQ_ERR_WORKSPACE          # at the limit: the next check (workspace) answers
+    finally:
+        tq.tq_destroy(ctx)
