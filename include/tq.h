@@ -268,6 +268,11 @@ tq_status tq_refine_counters(const tq_ctx* ctx, unsigned long long out[2], int r
 
 const char* tq_status_string(tq_status status);
 
+/* Name and message of the last CUDA error behind a TQ_ERR_CUDA returned to the
+ * calling host thread ("none" before any); the string stays valid until that
+ * thread's next failing call.  No counterpart in the pages (a diagnostic). */
+const char* tq_last_cuda_error(void);
+
 /* Inner-product search over a quantized key database ([P2] "생각정리 209
  * (TurboQuant)": the vector-search use; [P4] §4.3: the two-stage estimate is
  * unbiased).  For every query i and database vector t the score is the

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -13,6 +14,16 @@
 using namespace tq;
 
 namespace {
+
+// The last CUDA error a call on this host thread met (name and message).
+thread_local char g_last_cuda_error[160] = "none";
+
+tq_status cuda_fail(cudaError_t e) {
+  std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  return TQ_ERR_CUDA;
+}
+
+tq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TQ_OK : cuda_fail(e); }
 
 bool valid_bits(int b) { return b >= 1 && b <= 4; }
 
@@ -92,6 +103,24 @@ uint16_t to_f16(float x) {
   const uint32_t rem = man & 0x1FFFu;
   if (rem > 0x1000u || (rem == 0x1000u && (h & 1u))) ++h;
   return static_cast<uint16_t>(sign | h);
+}
+
+// bf16 of a double, round to nearest even (host; |x| well inside the normal range or 0)
+uint16_t to_bf16(double xd) {
+  const float x = static_cast<float>(xd);
+  uint32_t b;
+  std::memcpy(&b, &x, 4);
+  const uint32_t rem = b & 0xFFFFu;
+  uint32_t h = b >> 16;
+  if (rem > 0x8000u || (rem == 0x8000u && (h & 1u))) ++h;
+  return static_cast<uint16_t>(h);
+}
+
+double from_bf16(uint16_t h) {
+  const uint32_t b = static_cast<uint32_t>(h) << 16;
+  float x;
+  std::memcpy(&x, &b, 4);
+  return static_cast<double>(x);
 }
 
 float from_f16(uint16_t h) {
@@ -261,6 +290,17 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
       sh[swz(p, j, m)] = hi;
       sl[swz(p, j, m)] = to_f16(static_cast<float>(s[p * d + j] - static_cast<double>(from_f16(hi))));
     }
+  // bf16 hi + lo (swizzled operand tiles) + third term (row-major) of Pi
+  std::vector<uint16_t> pbh(d * d), pbl(d * d), pb3(d * d);
+  for (int i = 0; i < d; ++i)
+    for (int k = 0; k < d; ++k) {
+      const double v = pi[i * d + k];
+      const uint16_t h1 = to_bf16(v);
+      const uint16_t h2 = to_bf16(v - from_bf16(h1));
+      pbh[swz(i, k, d)] = h1;
+      pbl[swz(i, k, d)] = h2;
+      pb3[i * d + k] = to_bf16(v - from_bf16(h1) - from_bf16(h2));
+    }
   std::vector<float> adf(static_cast<size_t>(m) * d * 2), sdf(static_cast<size_t>(m) * d * 2);
   std::vector<float> wt(static_cast<size_t>(d) * (d + m));   // W = [Pi; S Pi], stored transposed
   for (int r = 0; r < d; ++r)
@@ -290,7 +330,10 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
   size_t o_sdf = align256(o_adf + sizeof(float) * d * m * 2);
   size_t o_pidf = align256(o_sdf + sizeof(float) * d * m * 2);
   size_t o_wt = align256(o_pidf + sizeof(float) * d * d * 2);
-  size_t o_err = align256(o_wt + sizeof(float) * d * (d + m));
+  size_t o_pbh = align256(o_wt + sizeof(float) * d * (d + m));
+  size_t o_pbl = align256(o_pbh + sizeof(uint16_t) * d * d);
+  size_t o_pb3 = align256(o_pbl + sizeof(uint16_t) * d * d);
+  size_t o_err = align256(o_pb3 + sizeof(uint16_t) * d * d);
   size_t o_cnt = align256(o_err + sizeof(uint32_t));
   size_t total = align256(o_cnt + 2 * sizeof(unsigned long long));
   void* blk = nullptr;
@@ -315,6 +358,9 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
   ctx->tab.s_df = reinterpret_cast<float*>(b + o_sdf);
   ctx->tab.pi_df = reinterpret_cast<float*>(b + o_pidf);
   ctx->tab.wt = reinterpret_cast<float*>(b + o_wt);
+  ctx->tab.pibh_sw = reinterpret_cast<unsigned short*>(b + o_pbh);
+  ctx->tab.pibl_sw = reinterpret_cast<unsigned short*>(b + o_pbl);
+  ctx->tab.pi3 = reinterpret_cast<unsigned short*>(b + o_pb3);
   ctx->tab.err = reinterpret_cast<uint32_t*>(b + o_err);
   ctx->tab.counters = reinterpret_cast<unsigned long long*>(b + o_cnt);
   bool ok = cudaMemcpy(ctx->tab.pit, pit.data(), sizeof(float) * d * d, cudaMemcpyHostToDevice) == cudaSuccess &&
@@ -330,6 +376,9 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
             cudaMemcpy(ctx->tab.a_df, adf.data(), sizeof(float) * d * m * 2, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemcpy(ctx->tab.s_df, sdf.data(), sizeof(float) * d * m * 2, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemcpy(ctx->tab.wt, wt.data(), sizeof(float) * d * (d + m), cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(ctx->tab.pibh_sw, pbh.data(), 2 * d * d, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(ctx->tab.pibl_sw, pbl.data(), 2 * d * d, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(ctx->tab.pi3, pb3.data(), 2 * d * d, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemset(b + o_err, 0, total - o_err) == cudaSuccess;
   if (!ok) { cudaFree(blk); delete static_cast<std::mutex*>(ctx->fused_mu); delete ctx; cudaGetLastError(); return TQ_ERR_CUDA; }
   // the fused decode step's second stream and its fork/join events: made here,
@@ -424,10 +473,12 @@ tq_status quantize_impl(const tq_ctx* ctx, const void* k, const void* v, tq_dtyp
     a.max_ctas = max_ctas;
   }
   cudaError_t e = cudaSuccess;
-  if (launch_quantize_tc(args[0], args[1], s, &e)) return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  if (launch_quantize_pipe(args[0], args[1], s, &e)) return cuda_status(e);
+  if (launch_quantize_tc(args[0], args[1], s, &e)) return cuda_status(e);
   for (int kind = 0; kind < 2; ++kind) {
     if (!args[kind].x) continue;
-    if (launch_quantize(args[kind], s) != cudaSuccess) return TQ_ERR_CUDA;
+    const cudaError_t ek = launch_quantize(args[kind], s);
+    if (ek != cudaSuccess) return cuda_fail(ek);
   }
   return TQ_OK;
 }
@@ -568,7 +619,7 @@ tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batc
   a.sched = reinterpret_cast<int*>(w + o_frag + align256(sizeof(uint32_t) * static_cast<size_t>(batch) * Hq * 128));
   a.out = out;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (!fused) return launch_decode(a, stages, st) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  if (!fused) return cuda_status(launch_decode(a, stages, st));
   a.new_token = 1;                       // len_add is 0 here: the partials cover [0, seq_lens[b])
   a.max_ctas = sm_count() - fused->reserve;
   bool ok = launch_decode(a, TQ_STAGE_QPREP, st) == cudaSuccess;
@@ -577,7 +628,7 @@ tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batc
   if (ok && fused->partials_end) ok = cudaEventRecord(fused->partials_end, st) == cudaSuccess;
   ok = ok && cudaStreamWaitEvent(st, fused->join, 0) == cudaSuccess;
   ok = ok && launch_decode(a, TQ_STAGE_MERGE, st) == cudaSuccess;
-  return ok ? TQ_OK : TQ_ERR_CUDA;
+  return ok ? TQ_OK : cuda_fail(cudaGetLastError());
 }
 }  // namespace
 
@@ -658,6 +709,8 @@ extern "C" tq_status tq_refine_counters(const tq_ctx* ctx, unsigned long long ou
   return TQ_OK;
 }
 
+extern "C" const char* tq_last_cuda_error(void) { return g_last_cuda_error; }
+
 extern "C" const char* tq_status_string(tq_status s) {
   switch (s) {
     case TQ_OK: return "ok";
@@ -707,7 +760,6 @@ extern "C" tq_status tq_search(const tq_ctx* ctx, const void* q, tq_dtype dtype,
   a.qprep = static_cast<float*>(workspace);
   a.qfrag = nullptr;
   a.sched = nullptr;
-  const cudaError_t e = launch_search(a, static_cast<const uint8_t*>(k_cache), block_table, num_pages, n_db, k_top,
-                                      top_scores, top_index, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  return cuda_status(launch_search(a, static_cast<const uint8_t*>(k_cache), block_table, num_pages, n_db, k_top,
+                                   top_scores, top_index, static_cast<cudaStream_t>(stream)));
 }

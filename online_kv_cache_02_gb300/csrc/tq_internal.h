@@ -83,6 +83,12 @@ struct DeviceTables {
   float* s_df;              // S as double-float pairs [m][128][2]
   float* pi_df;             // Pi as double-float pairs [128][128][2]
   float* wt;                // W^T, fp32 [d][d + m]: W = [Pi; S Pi], wt[k*(d+m) + r] = W[r][k]
+  // bf16 split of Pi for the bf16-input quantize kernel: Pi = hi + lo + third
+  // (each bf16, rounded in turn); hi and lo in the 128-byte-swizzled K-major
+  // layout above, the third term row-major [128][128]
+  unsigned short* pibh_sw;
+  unsigned short* pibl_sw;
+  unsigned short* pi3;
 };
 
 struct QuantizeArgs {
@@ -147,6 +153,11 @@ cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
 // Tensor-core quantize of K and V in one launch (bf16 inputs, supported
 // bit-width combinations); returns false when the configuration is not covered.
 bool launch_quantize_tc(const QuantizeArgs& k, const QuantizeArgs& v, cudaStream_t s, cudaError_t* err);
+// Pipelined tensor-core quantize of bf16 K and V (tq_quantize_pipe.cu): TMA
+// x tiles, bf16 MMAs, warp-specialized epilogue; any bit widths 1-4 and
+// splits that are multiples of 32.  Returns false when the inputs are not
+// covered (fp32 inputs, a codebook too fine for its cell tables).
+bool launch_quantize_pipe(const QuantizeArgs& k, const QuantizeArgs& v, cudaStream_t s, cudaError_t* err);
 cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s);
 // Persistent lookup-table kernel (tq_decode_lut.cu): CTAs it runs with at
 // most, one per SM (0: configuration not supported), and its launch (false:

@@ -29,7 +29,8 @@ TQ_F32 = 1
 class TQError(RuntimeError):
     def __init__(self, fn, status):
         self.status = status
-        super().__init__(f"{fn}: {tq_status_string(status)} (status {status})")
+        extra = f" [{tq_last_cuda_error()}]" if status == TQ_ERR_CUDA else ""
+        super().__init__(f"{fn}: {tq_status_string(status)} (status {status}){extra}")
 
 
 class TQConfig(ctypes.Structure):
@@ -81,6 +82,7 @@ EXPORTS = {
     "tq_check_device_status": ([_P, ctypes.POINTER(ctypes.c_uint32)], _S),
     "tq_refine_counters": ([_P, ctypes.POINTER(ctypes.c_ulonglong), _I], _S),
     "tq_status_string": ([_S], ctypes.c_char_p),
+    "tq_last_cuda_error": ([], ctypes.c_char_p),
 }
 for _name, (_args, _res) in EXPORTS.items():
     _f = getattr(_lib, _name)
@@ -115,6 +117,10 @@ def _check(fn, st):
 
 def tq_status_string(status):
     return _lib.tq_status_string(status).decode()
+
+
+def tq_last_cuda_error():
+    return _lib.tq_last_cuda_error().decode()
 
 
 def tq_config_init(d, b, m, seed):
