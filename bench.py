@@ -48,7 +48,7 @@ def parse(argv=None):
     ap.add_argument("--config", default="c3", choices=["c1", "c3", "c4", "c5"])
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     ap.add_argument("--no-quantize", action="store_true", help="skip the c2 quantize measurement")
-    ap.add_argument("--only", default="", choices=["", "quantize", "search"],
+    ap.add_argument("--only", default="", choices=["", "quantize", "search", "causal"],
                     help="quantize: run the c2 quantize measurement alone (profiling; --batch scales it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-others", action="store_true", help="time the headline decode workload only")
@@ -414,6 +414,65 @@ def decode_measure(torch, tq, w, stream, steps, warmup, dist, peak, peak_kind, w
     return rec
 
 
+CAUSAL_B, CAUSAL_L, CAUSAL_T = 4, 8192, 64
+
+
+def causal_measure(torch, tq, stream, steps, warmup, dist, peak, peak_kind, world):
+    """Multi-query causal attention (a prefill chunk): c3's shapes (32/8 heads, 3.5-bit K + QJL, 3.5-bit V) with
+    4 sequences of 8192 cached tokens and 64 new tokens each; a step quantize-appends the new tokens' K/V and runs
+    tq_causal_attention (token t attends over its prefix).  value = packed bytes of the attended cache / step time."""
+    w = wl.WORKLOADS["c3"].scaled(batch=CAUSAL_B, seq_len=CAUSAL_L)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ctx = tq.tq_create_ex(tq.make_config(k_bits=w.k_bits, v_bits=w.v_bits, m=w.m, seed=w.seed, k_qjl=w.qjl))
+    B, H, Hq, T, L = CAUSAL_B, w.kv_heads, w.q_heads, CAUSAL_T, CAUSAL_L
+    pps = (L + T + 15) // 16
+    bt = torch.randperm(B * pps, generator=torch.Generator().manual_seed(w.seed)).to(torch.int32).view(B, pps).to(dev)
+    kpb, vpb = tq.tq_cache_layout(ctx, H)
+    kc = torch.empty(B * pps * kpb, dtype=torch.uint8, device=dev)
+    vc = torch.empty(B * pps * vpb, dtype=torch.uint8, device=dev)
+    zero = torch.zeros(1, dtype=torch.int32, device=dev)
+    for b in range(B):
+        for s0 in range(0, L, 8192):
+            n = min(8192, L - s0)
+            K = torch.from_numpy(wl.kv_tokens(w, "k", b, s0, n)).to(dev).to(torch.bfloat16)
+            V = torch.from_numpy(wl.kv_tokens(w, "v", b, s0, n)).to(dev).to(torch.bfloat16)
+            zero.fill_(s0)
+            tq.tq_quantize(ctx, K, V, tq.TQ_BF16, 1, n, H, zero, bt[b], pps, B * pps, kc, vc)
+    g = torch.Generator(device=dev).manual_seed(w.seed + 1)
+    knew = torch.randn(B, T, H, 128, device=dev, generator=g).to(torch.bfloat16)
+    vnew = torch.randn(B, T, H, 128, device=dev, generator=g).to(torch.bfloat16)
+    q = torch.randn(B, T, Hq, 128, device=dev, generator=g).to(torch.bfloat16)
+    start = torch.full((B,), L, dtype=torch.int32, device=dev)
+    ws_n = tq.tq_causal_workspace_size(ctx, B, T, Hq, L + T, 0)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=dev)
+    out = torch.empty(B, T, Hq, 128, dtype=torch.float32, device=dev)
+
+    def step(i=None):
+        tq.tq_quantize(ctx, knew, vnew, tq.TQ_BF16, B, T, H, start, bt, pps, B * pps, kc, vc, stream)
+        tq.tq_causal_attention(ctx, q, tq.TQ_BF16, B, T, Hq, H, start, L + T, bt, pps, B * pps, kc, vc, 0,
+                               1.0 / math.sqrt(128), out, ws, ws_n, stream)
+
+    step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch)
+    with sampler:
+        ms = timed(torch, stream, step, steps, warmup, dist) / steps
+    bytes_step = B * H * (L + T) * wl.packed_bytes_per_token_head(w)     # every token up to the last new one
+    flags = tq.tq_check_device_status(ctx)
+    tq.tq_destroy(ctx)
+    value = bytes_step * world / (ms * 1e-3) / 1e9
+    return {"workload": f"causal: {B} seq x ({L} cached + {T} new tokens), {Hq}/{H} heads, K {w.k_bits} bits + QJL "
+                        f"m={w.m}, V {w.v_bits} bits; step = quantize-append the {T} new tokens + causal attention "
+                        f"(token t over its prefix)",
+            "value": round(value, 2), "unit": "GB/s of attended packed cache", "ms_per_step": round(ms, 5),
+            "queries_per_s": round(B * T * Hq * world / (ms * 1e-3), 1), "steps": steps,
+            "l2": f"packed cache {bytes_step / 2**20:.0f} MiB > 2x L2: no flush",
+            "roofline": {"kernel": "whole step (quantize-append + qprep + causal partials + merge)", "bound": "hbm",
+                         "achieved": round(value, 2), "peak": peak, "unit": "GB/s", "frac": round(value / peak, 4),
+                         "peak_source": peak_kind, "algorithmic_bytes_per_launch": bytes_step, "traffic": None},
+            "gpu_launches": 4 * steps, "clocks": sampler.result(), "device_flags": flags}
+
+
 def quantize_measure(torch, tq, qw, stream, qsteps, warmup, dist, peak, peak_kind, world):
     """The quantize-append workload (c2 shape): one launch per step quantizes every K and V vector."""
     qb = QuantizeBench(qw, torch, tq)
@@ -558,6 +617,14 @@ def run_ours(args):
         if dist is not None:
             dist.destroy_process_group()
         return
+    if args.only == "causal":
+        line = {"metric": "causal attention over the compressed cache: GB/s of attended packed cache"}
+        line.update(causal_measure(torch, tq, stream, args.steps, warmup, dist, peak, peak_kind, world))
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
     if args.only == "quantize":
         qw = wl.WORKLOADS["c2"].scaled(batch=args.batch) if args.batch else wl.WORKLOADS["c2"]
         line = {"metric": "KV vectors quantized/s (quantize only)"}
@@ -591,6 +658,9 @@ def run_ours(args):
                                  world)
             line[name] = rec
             line["gpu_launches"] += rec["gpu_launches"]
+    if not args.no_others and not args.batch:
+        line["causal"] = causal_measure(torch, tq, stream, args.steps, warmup, dist, peak, peak_kind, world)
+        line["gpu_launches"] += line["causal"]["gpu_launches"]
     if not args.no_quantize:
         line["quantize"] = quantize_measure(torch, tq, wl.WORKLOADS["c2"], stream, max(3, min(args.steps, 20)),
                                             warmup, dist, peak, peak_kind, world)

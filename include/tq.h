@@ -253,6 +253,29 @@ tq_status tq_append_decode_ex(const tq_ctx* ctx, const void* k_new, const void* 
                               float* out, void* workspace, size_t workspace_bytes, void* stream,
                               void* partials_begin_event, void* partials_end_event);
 
+/* Multi-query causal attention over the compressed cache ([P4] §2.3: a new
+ * token's query attends over every cached token; with T new tokens of one
+ * sequence, the t-th attends over its prefix).  q (device): [batch][n_new][Hq][d]
+ * in `dtype`, the queries of the tokens at positions start_pos[b] + t
+ * (start_pos: device int32 [batch]); the caches must already hold positions
+ * 0 .. start_pos[b] + n_new - 1 (append the new tokens' K/V with tq_quantize
+ * first).  Query t of sequence b attends over positions 0 .. start_pos[b] + t
+ * with the scores, softmax and value sums of tq_decode_attention; out (device,
+ * fp32): [batch][n_new][Hq][d].  start_pos[b] + n_new <= max_seq_len.  The
+ * context is split into chunks of chunk_tokens (0 picks one) merged per query.
+ * Runs the bit-width combinations of the persistent decode kernel (d = 128,
+ * m = 128, split 64; K/V bits 3/3, 4-3/4-3, 3-2/3-2, 4/4, 2/2, 4/2), else
+ * TQ_ERR_UNSUPPORTED; query heads per KV head <= 8.  workspace (device) of
+ * tq_causal_workspace_size bytes; stream-ordered, no allocation.  Errors as
+ * tq_decode_attention. */
+tq_status tq_causal_workspace_size(const tq_ctx* ctx, int batch, int n_new, int num_q_heads, int max_seq_len,
+                                   int chunk_tokens, size_t* bytes);
+tq_status tq_causal_attention(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batch, int n_new,
+                              int num_q_heads, int num_kv_heads, const int32_t* start_pos, int max_seq_len,
+                              const int32_t* block_table, int max_pages_per_seq, int num_pages,
+                              const void* k_cache, const void* v_cache, int chunk_tokens, float softmax_scale,
+                              float* out, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronise the device and report (then clear) the context's device error
  * word: TQ_OK, or TQ_ERR_DEVICE_CHECK with the bits in *flags (may be NULL):
  * 1 = page id out of range, 2 = position beyond the block table,

@@ -490,7 +490,7 @@ int nchunks_for(int max_seq_len, int chunk) { return max_seq_len <= 0 ? 1 : (max
 size_t ws_bytes(int B, int Hq, int d, int m, int nch) {
   return align256(sizeof(float) * static_cast<size_t>(B) * Hq * (d + m)) +
          align256(sizeof(float) * static_cast<size_t>(B) * Hq * nch * (d + 2)) +
-         align256(sizeof(uint32_t) * static_cast<size_t>(B) * Hq * 128) + 256;   // + query fragments, work counters
+         align256(sizeof(uint32_t) * static_cast<size_t>(B) * Hq * kQFragWords) + 256;   // + query fragments, work counters
 }
 }  // namespace
 
@@ -616,7 +616,7 @@ tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batc
   const size_t o_frag = align256(sizeof(float) * static_cast<size_t>(batch) * Hq * (d + m)) +
                         align256(sizeof(float) * static_cast<size_t>(batch) * Hq * nch * (d + 2));
   a.qfrag = reinterpret_cast<uint32_t*>(w + o_frag);
-  a.sched = reinterpret_cast<int*>(w + o_frag + align256(sizeof(uint32_t) * static_cast<size_t>(batch) * Hq * 128));
+  a.sched = reinterpret_cast<int*>(w + o_frag + align256(sizeof(uint32_t) * static_cast<size_t>(batch) * Hq * kQFragWords));
   a.out = out;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (!fused) return cuda_status(launch_decode(a, stages, st));
@@ -688,6 +688,88 @@ extern "C" tq_status tq_append_decode_ex(const tq_ctx* ctx, const void* k_new, c
   // qprep and the partials over the cached tokens, then (joined) the merge
   return decode_impl(ctx, q, dtype, batch, Hq, H, seq_lens, 0, max_seq_len, block_table, maxp, num_pages, k_cache,
                      v_cache, chunk_tokens, softmax_scale, out, workspace, workspace_bytes, TQ_STAGE_ALL, stream, &f);
+}
+
+// ---------------------------------------------------------------------------
+// multi-query causal attention (many new tokens per sequence)
+// ---------------------------------------------------------------------------
+namespace {
+int causal_qblocks(int T, int G) { return (T * G + 7) / 8; }
+}  // namespace
+
+extern "C" tq_status tq_causal_workspace_size(const tq_ctx* ctx, int batch, int n_new, int Hq, int max_seq_len,
+                                              int chunk_tokens, size_t* bytes) {
+  if (!ctx || !bytes || batch < 0 || n_new < 1 || Hq < 1 || max_seq_len < n_new || chunk_tokens < 0 ||
+      chunk_tokens % kPage)
+    return TQ_ERR_INVALID_ARG;
+  const int chunk = chunk_tokens ? chunk_tokens : 64;   // the smallest automatic chunk
+  *bytes = ws_bytes(static_cast<int>(static_cast<long long>(batch) * n_new), Hq, ctx->cfg.d, ctx->cfg.m,
+                    nchunks_for(max_seq_len, chunk));
+  return TQ_OK;
+}
+
+extern "C" tq_status tq_causal_attention(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batch, int n_new,
+                                         int Hq, int H, const int32_t* start_pos, int max_seq_len,
+                                         const int32_t* block_table, int maxp, int num_pages, const void* k_cache,
+                                         const void* v_cache, int chunk_tokens, float softmax_scale, float* out,
+                                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (!ctx || batch < 0 || n_new < 1 || Hq < 1 || H < 1 || Hq % H || max_seq_len < n_new || maxp < 1 ||
+      num_pages < 1 || chunk_tokens < 0 || chunk_tokens % kPage)
+    return TQ_ERR_INVALID_ARG;
+  if (dtype != TQ_BF16 && dtype != TQ_F32) return TQ_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return TQ_ERR_INVALID_ARG;
+  if (Hq / H > kMaxGroup) return TQ_ERR_UNSUPPORTED;
+  const int lut_ctas = lut_decode_ctas(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H);
+  if (lut_ctas <= 0) return TQ_ERR_UNSUPPORTED;        // the bit widths the persistent kernel takes
+  if (batch == 0) return TQ_OK;
+  if (!q || !start_pos || !block_table || !k_cache || !v_cache || !out || !workspace) return TQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15) return TQ_ERR_INVALID_ARG;
+  const long long rows = static_cast<long long>(batch) * n_new;
+  if (rows * Hq > (1LL << 31) - 1 || rows > 65535LL * 65535LL) return TQ_ERR_UNSUPPORTED;
+  const int G = Hq / H, nqb = causal_qblocks(n_new, G);
+  const int chunk = chunk_tokens ? chunk_tokens
+                                 : pick_chunk_warps(static_cast<int>(std::min<long long>(
+                                                        static_cast<long long>(batch) * H * nqb, 1 << 30)),
+                                                    max_seq_len, lut_ctas);
+  const int nch = nchunks_for(max_seq_len, chunk);
+  const int d = ctx->cfg.d, m = ctx->cfg.m;
+  if (workspace_bytes < ws_bytes(static_cast<int>(rows), Hq, d, m, nch)) return TQ_ERR_WORKSPACE;
+  if (static_cast<long long>(batch) * H * nqb * nch > (1LL << 30) || nch > 65535) return TQ_ERR_UNSUPPORTED;
+  DecodeArgs a{};
+  a.q = q;
+  a.f32 = dtype == TQ_F32;
+  a.B = batch;
+  a.Hq = Hq;
+  a.H = H;
+  a.G = G;
+  a.seq_lens = start_pos;
+  a.len_add = n_new;
+  a.max_seq_len = max_seq_len;
+  a.block_table = block_table;
+  a.maxp = maxp;
+  a.num_pages = num_pages;
+  a.kc = static_cast<const uint8_t*>(k_cache);
+  a.vc = static_cast<const uint8_t*>(v_cache);
+  a.kl = ctx->kl;
+  a.vl = ctx->vl;
+  a.k_page_bytes = static_cast<long long>(ctx->kl.block_bytes) * H;
+  a.v_page_bytes = static_cast<long long>(ctx->vl.block_bytes) * H;
+  a.chunk = chunk;
+  a.nchunks = nch;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.m = m;
+  a.tab = ctx->tab;
+  a.T = n_new;
+  a.nqb = nqb;
+  char* w = static_cast<char*>(workspace);
+  const size_t o_part = align256(sizeof(float) * static_cast<size_t>(rows) * Hq * (d + m));
+  const size_t o_frag = o_part + align256(sizeof(float) * static_cast<size_t>(rows) * Hq * nch * (d + 2));
+  a.qprep = reinterpret_cast<float*>(w);
+  a.part = reinterpret_cast<float*>(w + o_part);
+  a.qfrag = reinterpret_cast<uint32_t*>(w + o_frag);
+  a.sched = reinterpret_cast<int*>(w + o_frag + align256(sizeof(uint32_t) * static_cast<size_t>(rows) * Hq * kQFragWords));
+  a.out = out;
+  return cuda_status(launch_decode(a, TQ_STAGE_ALL, static_cast<cudaStream_t>(stream)));
 }
 
 extern "C" tq_status tq_check_device_status(const tq_ctx* ctx, uint32_t* flags) {

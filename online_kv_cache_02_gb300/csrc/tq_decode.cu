@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(kQThreads) qprep_kernel(DecodeArgs a) {
   const int nout = kD + a.m;
   const long long r0 = static_cast<long long>(blockIdx.x) * kQP;
   const int c0 = blockIdx.y * kQO;
-  const long long nq = static_cast<long long>(a.B) * a.Hq;
+  const long long nq = static_cast<long long>(a.B) * (a.T > 0 ? a.T : 1) * a.Hq;   // query rows
   const int tid = threadIdx.x, oq = 4 * (tid & 15), h0 = 4 * (tid >> 4);
   if (blockIdx.x == 0 && blockIdx.y == 0 && tid < 2 && a.sched) a.sched[tid] = 0;   // partials work counters
 #pragma unroll
@@ -107,10 +107,15 @@ __global__ void __launch_bounds__(kQThreads) qprep_kernel(DecodeArgs a) {
   // hold, per head, 32 of its 128 words (slice 0/1: key pairs of channel group
   // 0/1 for every lane t; slice 2/3: u pairs of lanes t = 0,1 / 2,3)
   __shared__ __half hs[kQP][kQO];
+  __shared__ __half hl[kQP][kQO];          // fp16 of the rounding remainder (q~ low parts)
 #pragma unroll
   for (int r = 0; r < 4; ++r)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) hs[h0 + r][oq + c] = __float2half_rn(acc[r][c]);
+    for (int c = 0; c < 4; ++c) {
+      const __half h = __float2half_rn(acc[r][c]);
+      hs[h0 + r][oq + c] = h;
+      hl[h0 + r][oq + c] = __float2half_rn(acc[r][c] - __half2float(h));
+    }
   __syncthreads();
   const int y = blockIdx.y;
   for (int idx = tid; idx < kQP * 32; idx += kQThreads) {
@@ -130,8 +135,14 @@ __global__ void __launch_bounds__(kQThreads) qprep_kernel(DecodeArgs a) {
       lo = 32 * t + 16 * (p & 1) + (p >> 1) - 64 * (y - 2);
       hi = lo + 8;
     }
-    a.qfrag[(r0 + h) * 128 + word] = static_cast<uint32_t>(__half_as_ushort(hs[h][lo])) |
-                                     (static_cast<uint32_t>(__half_as_ushort(hs[h][hi])) << 16);
+    a.qfrag[(r0 + h) * kQFragWords + word] = static_cast<uint32_t>(__half_as_ushort(hs[h][lo])) |
+                                             (static_cast<uint32_t>(__half_as_ushort(hs[h][hi])) << 16);
+    // q~ low parts of the key pairs: word 128 + 16 t + (2 kk + e), the same order
+    if (y < 2) {
+      const int t = k >> 3;
+      a.qfrag[(r0 + h) * kQFragWords + 128 + 16 * t + (word - 32 * t)] =
+          static_cast<uint32_t>(__half_as_ushort(hl[h][lo])) | (static_cast<uint32_t>(__half_as_ushort(hl[h][hi])) << 16);
+    }
   }
 }
 
@@ -417,9 +428,11 @@ __global__ void __launch_bounds__(kMThreads) merge_kernel(DecodeArgs a) {
   __shared__ float os[kD];
   __shared__ float vnew[kD];
   __shared__ float red[kMThreads / 32];
-  const long long row = blockIdx.x;                 // b * Hq + query head
+  const long long row = blockIdx.x;                 // b * Hq + query head (causal: (b T + t) Hq + query head)
   const int tid = threadIdx.x, j = tid & (kD - 1), grp = tid >> 7;
-  int L = a.seq_lens[row / a.Hq] + a.len_add;
+  // causal: row (b, t, h) attends positions [0, seq_lens[b] + t]
+  int L = a.T > 0 ? a.seq_lens[row / a.Hq / a.T] + static_cast<int>((row / a.Hq) % a.T) + 1
+                  : a.seq_lens[row / a.Hq] + a.len_add;
   L = L < 0 ? 0 : L;
   L = L > a.max_seq_len ? a.max_seq_len : L;
   L = L > a.maxp * kPage ? a.maxp * kPage : L;
@@ -482,7 +495,7 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
 cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
   if (stages & TQ_STAGE_QPREP) {
-    const dim3 grid(static_cast<unsigned>((static_cast<long long>(a.B) * a.Hq + kQP - 1) / kQP),
+    const dim3 grid(static_cast<unsigned>((static_cast<long long>(a.B) * (a.T > 0 ? a.T : 1) * a.Hq + kQP - 1) / kQP),
                     static_cast<unsigned>((kD + a.m + kQO - 1) / kQO));
     static std::atomic<unsigned long long> configured{0};   // the W slice and q rows take 49 KB
     e = smem_attr_once(qprep_kernel, kQprepSmem, configured);
@@ -511,7 +524,7 @@ cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
     }
   }
   if (stages & TQ_STAGE_MERGE) {
-    merge_kernel<<<static_cast<unsigned>(static_cast<long long>(a.B) * a.Hq), kMThreads, 0, s>>>(a);
+    merge_kernel<<<static_cast<unsigned>(static_cast<long long>(a.B) * (a.T > 0 ? a.T : 1) * a.Hq), kMThreads, 0, s>>>(a);
     e = cudaGetLastError();
   }
   return e;

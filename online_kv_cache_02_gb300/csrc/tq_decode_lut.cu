@@ -256,7 +256,7 @@ __device__ __forceinline__ uint32_t lds_at(uint32_t addr) {
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int W, int KBH, int KBL, int VBH, int VBL, bool QJL>
+template <int W, int KBH, int KBL, int VBH, int VBL, bool QJL, bool CAUSAL = false>
 __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, int total_items) {
   using Gm = Geo<W, KBH, KBL, VBH, VBL, QJL>;
   constexpr int S = Gm::STAGES;
@@ -311,6 +311,20 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
     return L;
   };
 
+  // causal: query rows of a (sequence, KV head) are r = t G + g (new token t,
+  // query head g of the group), eight per block; row r attends positions
+  // [0, seq_lens[b] + t] (seq_lens holds the first new position, len_add = T).
+  // block_len: the positions any row of block qb needs; row_len: one row's.
+  auto row_len = [&](int b, int r) {
+    if (r >= a.T * a.G) return 0;
+    const int L = a.seq_lens[b] + r / a.G + 1;
+    return min(L, seq_len(b));
+  };
+  auto block_len = [&](int b, int qb) {
+    const int last = min(a.T * a.G - 1, 8 * qb + 7);
+    return row_len(b, last);
+  };
+
   // ---- producer state (meaningful in lane 0) --------------------------------
   int p_item = 0, p_page = 0, p_npages = 0, p_b = 0, p_h = 0, p_chunk = 0;   // p_item -1: done
   int p_pid = 0;                 // page id of (p_item, p_page), loaded one refill ahead
@@ -324,10 +338,11 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
         break;
       }
       p_chunk = it % nch;
-      const int bh = it / nch;
+      const int rest = it / nch;
+      const int bh = CAUSAL ? rest / a.nqb : rest;
       p_h = bh % a.H;
       p_b = bh / a.H;
-      const int L = seq_len(p_b);
+      const int L = CAUSAL ? block_len(p_b, rest % a.nqb) : seq_len(p_b);
       const int t0 = p_chunk * C;
       if (t0 >= L) continue;                  // chunk past the end: no partial (the merge skips it)
       p_item = it;
@@ -379,7 +394,9 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
   const uint32_t lbk1 = lbk0 + (static_cast<uint32_t>(Gm::R0) & ~0xFFFFu), lbv1 = lbk1 + 128u;
   const float k1 = kInvSqrtD * a.scale_log2;
   const float k2 = kSqrtHalfPi / 128.0f * a.scale_log2;
-  int cur = -1, c_b = 0, c_h = 0, c_chunk = 0, c_t0 = 0, c_t1 = 0;
+  int cur = -1, c_b = 0, c_h = 0, c_chunk = 0, c_t0 = 0, c_t1 = 0, c_qb = 0;
+  int c_end[2] = {0, 0};   // causal: end of the valid positions of this thread's columns 2t, 2t + 1
+  const uint4* c_qlo = nullptr;   // fp16 low parts of this lane's q~ fragments (read per page, from L1)
   uint32_t qf[16], uf[16];
   float kqa, kqb[2];       // QJL logit terms: <u, +-1> = (2/c) raw - (2/c + 1) sum(u), times k2
   float acc[8][4];
@@ -394,8 +411,11 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
       l += __shfl_xor_sync(0xffffffffu, l, 8);
       l += __shfl_xor_sync(0xffffffffu, l, 16);
       const int hh = 2 * t + c;
-      if (hh < a.G) {
-        float* dst = a.part + ((static_cast<long long>(c_b) * a.Hq + c_h * a.G + hh) * nch + c_chunk) * (kD + 2);
+      const int r = 8 * c_qb + hh;
+      if (CAUSAL ? r < a.T * a.G : hh < a.G) {
+        const long long qrow = CAUSAL ? (static_cast<long long>(c_b) * a.T + r / a.G) * a.Hq + c_h * a.G + r % a.G
+                                      : static_cast<long long>(c_b) * a.Hq + c_h * a.G + hh;
+        float* dst = a.part + (qrow * nch + c_chunk) * (kD + 2);
         if (g == 0) {
           dst[0] = m_run[c];
           dst[1] = l;
@@ -410,15 +430,24 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
   };
   auto start = [&](int item) {
     c_chunk = item % nch;
-    const int bh = item / nch;
+    const int rest = item / nch;
+    const int bh = CAUSAL ? rest / a.nqb : rest;
+    c_qb = CAUSAL ? rest % a.nqb : 0;
     c_h = bh % a.H;
     c_b = bh / a.H;
     c_t0 = c_chunk * C;
-    c_t1 = min(c_t0 + C, seq_len(c_b));
+    c_t1 = min(c_t0 + C, CAUSAL ? block_len(c_b, c_qb) : seq_len(c_b));
+    if (CAUSAL) {
+      c_end[0] = min(c_t1, row_len(c_b, 8 * c_qb + 2 * t));
+      c_end[1] = min(c_t1, row_len(c_b, 8 * c_qb + 2 * t + 1));
+    }
     // the query fragments, packed by qprep in this thread's order: 8 x 16 B
-    if (g < a.G) {
-      const uint4* fp = reinterpret_cast<const uint4*>(
-          a.qfrag + ((static_cast<long long>(c_b) * a.Hq + c_h * a.G + g) * 4 + t) * 32);
+    const int qr = 8 * c_qb + g;
+    if (CAUSAL ? qr < a.T * a.G : g < a.G) {
+      const long long qrow = CAUSAL ? (static_cast<long long>(c_b) * a.T + qr / a.G) * a.Hq + c_h * a.G + qr % a.G
+                                    : static_cast<long long>(c_b) * a.Hq + c_h * a.G + g;
+      const uint4* fp = reinterpret_cast<const uint4*>(a.qfrag + qrow * kQFragWords + 32 * t);
+      c_qlo = reinterpret_cast<const uint4*>(a.qfrag + qrow * kQFragWords + 128 + 16 * t);
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         const uint4 x = fp[v], y = fp[4 + v];
@@ -429,6 +458,7 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
     } else {
 #pragma unroll
       for (int v = 0; v < 16; ++v) qf[v] = uf[v] = 0u;
+      c_qlo = nullptr;
     }
     if (QJL) {
       // sum of head g's u (the fp16 values the MMA multiplies), then the sums
@@ -502,6 +532,11 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
         k_slice<KBH>(rb, t, xb0);
         k_slice<KBL>(ra + 2 * KBH, t, xa1);
         k_slice<KBL>(rb + 2 * KBH, t, xb1);
+        // causal attention (many queries per page, a heavier contraction): q~ =
+        // hi + lo, the low parts (about 2^-11 of q~) through the same key
+        // fragments into the other accumulator chain, halving the logit's
+        // rounding error; decode keeps q~ in fp16 alone
+        uint4 ql = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const int kk = (q >> 1) + 4 * (q & 1);   // alternate the two channel groups
@@ -523,6 +558,10 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
             a3 = lds_at<OFF1>(prmt(xb[j1 >> 2], lbk1, s1x));
           }
           mma16816(kk < 4 ? s1 : s1b, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
+          if (CAUSAL) {
+            if ((kk & 1) == 0) ql = c_qlo ? __ldg(c_qlo + (kk >> 1)) : make_uint4(0u, 0u, 0u, 0u);
+            mma16816(kk < 4 ? s1b : s1, a0, a1, a2, a3, (kk & 1) ? ql.z : ql.x, (kk & 1) ? ql.w : ql.y);
+          }
         }
         if (QJL) {
           const uint32_t* sg = reinterpret_cast<const uint32_t*>(kb + Gm::K_SIGNS);
@@ -549,10 +588,13 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
       {
         const float nkg = __half2float(nk[g]), nkg8 = __half2float(nk[g + 8]);
         const float rkg = QJL ? __half2float(rk[g]) : 0.f, rkg8 = QJL ? __half2float(rk[g + 8]) : 0.f;
-        lg[0] = vg ? fmaf(nkg * k1, s1[0], rkg * fmaf(kqa, s2[0], kqb[0])) : kNegBig;
-        lg[1] = vg ? fmaf(nkg * k1, s1[1], rkg * fmaf(kqa, s2[1], kqb[1])) : kNegBig;
-        lg[2] = vg8 ? fmaf(nkg8 * k1, s1[2], rkg8 * fmaf(kqa, s2[2], kqb[0])) : kNegBig;
-        lg[3] = vg8 ? fmaf(nkg8 * k1, s1[3], rkg8 * fmaf(kqa, s2[3], kqb[1])) : kNegBig;
+        // causal: token p of column c is valid below that column's end
+        const bool v0 = CAUSAL ? pbase + g < c_end[0] : vg, v1 = CAUSAL ? pbase + g < c_end[1] : vg;
+        const bool v2 = CAUSAL ? pbase + g + 8 < c_end[0] : vg8, v3 = CAUSAL ? pbase + g + 8 < c_end[1] : vg8;
+        lg[0] = v0 ? fmaf(nkg * k1, s1[0], rkg * fmaf(kqa, s2[0], kqb[0])) : kNegBig;
+        lg[1] = v1 ? fmaf(nkg * k1, s1[1], rkg * fmaf(kqa, s2[1], kqb[1])) : kNegBig;
+        lg[2] = v2 ? fmaf(nkg8 * k1, s1[2], rkg8 * fmaf(kqa, s2[2], kqb[0])) : kNegBig;
+        lg[3] = v3 ? fmaf(nkg8 * k1, s1[3], rkg8 * fmaf(kqa, s2[3], kqb[1])) : kNegBig;
       }
       // ---- online softmax over this page (heads 2t, 2t+1) -------------------
       // The running max m only has to bound the logits: it moves (a warp-wide
@@ -645,13 +687,14 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
   }
 }
 
-template <int W, int KBH, int KBL, int VBH, int VBL, bool QJL>
+template <int W, int KBH, int KBL, int VBH, int VBL, bool QJL, bool CAUSAL = false>
 cudaError_t launch_lut(const DecodeArgs& a, int items, int grid, cudaStream_t s) {
   using Gm = Geo<W, KBH, KBL, VBH, VBL, QJL>;
   static std::atomic<unsigned long long> configured{0};
-  const cudaError_t e = smem_attr_once(lut_partials_kernel<W, KBH, KBL, VBH, VBL, QJL>, Gm::SMEM, configured);
+  const cudaError_t e =
+      smem_attr_once(lut_partials_kernel<W, KBH, KBL, VBH, VBL, QJL, CAUSAL>, Gm::SMEM, configured);
   if (e != cudaSuccess) return e;
-  lut_partials_kernel<W, KBH, KBL, VBH, VBL, QJL><<<grid, 32 * W, Gm::SMEM, s>>>(a, items);
+  lut_partials_kernel<W, KBH, KBL, VBH, VBL, QJL, CAUSAL><<<grid, 32 * W, Gm::SMEM, s>>>(a, items);
   return cudaGetLastError();
 }
 
@@ -665,6 +708,9 @@ cudaError_t launch_lut_q(const DecodeArgs& a, int items, cudaStream_t s) {
   // without a chunk exits at once, and every SM's copy engines are in use
   const int cap = a.max_ctas > 0 && a.max_ctas < sms ? a.max_ctas : sms;
   const int grid = items < cap ? (items > 0 ? items : 1) : cap;
+  if (a.T > 0)                         // causal (many new tokens): 16 warps
+    return a.kl.qjl ? launch_lut<16, KBH, KBL, VBH, VBL, true, true>(a, items, grid, s)
+                    : launch_lut<16, KBH, KBL, VBH, VBL, false, true>(a, items, grid, s);
   if (lut_warps_for(items, cap) == 12)
     return a.kl.qjl ? launch_lut<12, KBH, KBL, VBH, VBL, true>(a, items, grid, s)
                     : launch_lut<12, KBH, KBL, VBH, VBL, false>(a, items, grid, s);
@@ -702,7 +748,7 @@ bool launch_partials_lut(const DecodeArgs& a, cudaStream_t s, cudaError_t* err) 
   if (!lut_decode_ctas(a.kl, a.vl, a.m, a.G) || !a.sched || !a.qfrag) return false;
   if ((reinterpret_cast<uintptr_t>(a.kc) | reinterpret_cast<uintptr_t>(a.vc)) & 15) return false;
   if ((a.k_page_bytes | a.v_page_bytes) & 15) return false;
-  const long long items = static_cast<long long>(a.B) * a.H * a.nchunks;
+  const long long items = static_cast<long long>(a.B) * a.H * a.nchunks * (a.T > 0 ? a.nqb : 1);
   if (items > (1LL << 30)) return false;
   const int n = static_cast<int>(items);
   switch (combo_code(a.kl, a.vl)) {

@@ -17,6 +17,7 @@ constexpr int kPage = 16;        // tokens per cache page
 constexpr int kMaxM = 128;       // QJL projections, multiple of 32
 constexpr int kMaxGroup = 8;     // query heads per KV head handled by the decode kernels
 constexpr float kPiScale = 16.0f;  // Pi is split into fp16 hi + lo after scaling by this power of two
+constexpr int kQFragWords = 192;   // query fragment words per query row (see DecodeArgs::qfrag)
 
 // Device error word bits.
 constexpr uint32_t kErrPage = 1u;      // page id outside [0, num_pages)
@@ -129,8 +130,15 @@ struct DecodeArgs {
   int* sched;            // [2] work counter and finished-warp count of the persistent kernel (zeroed by qprep)
   int new_token;         // 1: merge adds the token at position seq_lens[b] itself (fused decode step)
   int max_ctas;          // partials kernel: 0 = one CTA per SM, else at most this many
-  uint32_t* qfrag;       // [B][Hq][4][32] fp16 pairs in the persistent kernel's fragment order (m = 128 only):
-                         // for lane t%4 of a KV-head warp, 16 words of q~ (key pairs) then 16 of u
+  uint32_t* qfrag;       // [B][Hq][kQFragWords] fp16 pairs in the persistent kernel's fragment order (m = 128
+                         // only): words 32 t .. 32 t + 31 for lane t%4 of a KV-head warp (16 of q~ key pairs, 16
+                         // of u), then 128 + 16 t .. : the fp16 low parts of lane t's q~ pairs
+  // causal attention of T > 0 new tokens per sequence (0: decode): the query
+  // rows are [B][T][Hq] (qprep, partials and out use B * T rows), seq_lens
+  // holds each sequence's first new position, len_add = T, and the partials
+  // kernel takes query rows eight at a time (nqb blocks per sequence and KV head)
+  int T;
+  int nqb;
 };
 
 // Opt kernel `fn` into `bytes` of dynamic shared memory on the current device,

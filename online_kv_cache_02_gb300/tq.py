@@ -79,6 +79,9 @@ EXPORTS = {
                           _P, _SZ, _P], _S),
     "tq_append_decode_ex": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _I, _I, _P, _P, _I, ctypes.c_float, _P,
                              _P, _SZ, _P, _P, _P], _S),
+    "tq_causal_workspace_size": ([_P, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)], _S),
+    "tq_causal_attention": ([_P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _I, _I, _P, _P, _I, ctypes.c_float, _P, _P, _SZ,
+                             _P], _S),
     "tq_check_device_status": ([_P, ctypes.POINTER(ctypes.c_uint32)], _S),
     "tq_refine_counters": ([_P, ctypes.POINTER(ctypes.c_ulonglong), _I], _S),
     "tq_status_string": ([_S], ctypes.c_char_p),
@@ -276,6 +279,22 @@ def tq_refine_counters(ctx, reset=False):
 def raw_status(fn_name, *args):
     """Call an export with already-marshalled arguments and return its status (for argument-check tests)."""
     return getattr(_lib, fn_name)(*args)
+
+
+def tq_causal_workspace_size(ctx, batch, n_new, num_q_heads, max_seq_len, chunk_tokens=0):
+    n = ctypes.c_size_t()
+    _check("tq_causal_workspace_size", _lib.tq_causal_workspace_size(ctx, batch, n_new, num_q_heads, max_seq_len,
+                                                                     chunk_tokens, ctypes.byref(n)))
+    return n.value
+
+
+def tq_causal_attention(ctx, q, dtype, batch, n_new, num_q_heads, num_kv_heads, start_pos, max_seq_len, block_table,
+                        max_pages_per_seq, num_pages, k_cache, v_cache, chunk_tokens, softmax_scale, out, workspace,
+                        workspace_bytes, stream=None):
+    _check("tq_causal_attention", _lib.tq_causal_attention(
+        ctx, _ptr(q), dtype, batch, n_new, num_q_heads, num_kv_heads, _ptr(start_pos), max_seq_len,
+        _ptr(block_table), max_pages_per_seq, num_pages, _ptr(k_cache), _ptr(v_cache), chunk_tokens,
+        ctypes.c_float(softmax_scale), _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def tq_search_workspace_size(ctx, nq, n_db):
