@@ -488,11 +488,11 @@ def quantize_measure(torch, tq, qw, stream, qsteps, warmup, dist, peak, peak_kin
         "value": round(qb.vectors * world / (qstep * 1e-3), 1), "unit": "KV vectors/s", "ms_per_step": round(qstep, 4),
         "steps": qsteps,
         "l2": f"{qb.bytes_in / 2**20:.0f} MiB of bf16 input per step > 2x L2: no flush",
-        "roofline": {"kernel": "quantize_tc_kernel (K and V tiles in one launch)", "bound": "hbm",
+        "roofline": {"kernel": "quantize_pipe_kernel (K and V tiles in one launch)", "bound": "hbm",
                      "achieved": round(qbytes / (qstep * 1e-3) / 1e9, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(qbytes / (qstep * 1e-3) / 1e9 / peak, 4), "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": qbytes,
-                     "traffic": traffic_for("tq_quantize_tc.cu", "quantize_tc_kernel", "c2") if full else None},
+                     "traffic": traffic_for("tq_quantize_pipe.cu", "quantize_pipe_kernel", "c2") if full else None},
         "refined": tq.tq_refine_counters(qb.ctx),
         "clocks": qs.result(),
     }

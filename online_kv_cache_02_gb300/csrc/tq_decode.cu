@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kQThreads) qprep_kernel(DecodeArgs a) {
   const int c0 = blockIdx.y * kQO;
   const long long nq = static_cast<long long>(a.B) * (a.T > 0 ? a.T : 1) * a.Hq;   // query rows
   const int tid = threadIdx.x, oq = 4 * (tid & 15), h0 = 4 * (tid >> 4);
+  pdl_trigger();                       // the partials kernel may launch now (it waits for this grid's results)
   if (blockIdx.x == 0 && blockIdx.y == 0 && tid < 2 && a.sched) a.sched[tid] = 0;   // partials work counters
 #pragma unroll
   for (int it = 0; it < kD * kQO / 4 / kQThreads; ++it) {
@@ -423,6 +424,7 @@ __device__ float new_token_logit(const DecodeArgs& a, long long row, float* vnew
 }
 
 __global__ void __launch_bounds__(kMThreads) merge_kernel(DecodeArgs a) {
+  pdl_wait();                          // the partials kernel before it has completed
   __shared__ float wsh[kMThreads];
   __shared__ float part[kMGroups][kD];
   __shared__ float os[kD];
@@ -524,8 +526,8 @@ cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
     }
   }
   if (stages & TQ_STAGE_MERGE) {
-    merge_kernel<<<static_cast<unsigned>(static_cast<long long>(a.B) * (a.T > 0 ? a.T : 1) * a.Hq), kMThreads, 0, s>>>(a);
-    e = cudaGetLastError();
+    e = launch_pdl(merge_kernel, dim3(static_cast<unsigned>(static_cast<long long>(a.B) * (a.T > 0 ? a.T : 1) * a.Hq)),
+                   dim3(kMThreads), 0, s, a);
   }
   return e;
 }

@@ -382,6 +382,9 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
     // this thread's outstanding memory operations) and used one refill later
     if (p_page < p_npages) p_pid = p_row[p_page];
   };
+  // the query prep (the kernel before this one) zeroes the work counter and
+  // writes the query fragments: everything above ran while it finished
+  pdl_wait();
   if (lane == 0)
     for (int s = 0; s < S; ++s) issue(s);
   __syncwarp();
@@ -694,8 +697,8 @@ cudaError_t launch_lut(const DecodeArgs& a, int items, int grid, cudaStream_t s)
   const cudaError_t e =
       smem_attr_once(lut_partials_kernel<W, KBH, KBL, VBH, VBL, QJL, CAUSAL>, Gm::SMEM, configured);
   if (e != cudaSuccess) return e;
-  lut_partials_kernel<W, KBH, KBL, VBH, VBL, QJL, CAUSAL><<<grid, 32 * W, Gm::SMEM, s>>>(a, items);
-  return cudaGetLastError();
+  return launch_pdl(lut_partials_kernel<W, KBH, KBL, VBH, VBL, QJL, CAUSAL>, dim3(grid), dim3(32 * W),
+                    static_cast<size_t>(Gm::SMEM), s, a, items);
 }
 
 template <int KBH, int KBL, int VBH, int VBL>
