@@ -59,7 +59,7 @@ typedef enum {
   TQ_ERR_INVALID_ARG = 1,   /* bad pointer, size or configuration */
   TQ_ERR_CUDA = 2,          /* a CUDA runtime call or launch failed */
   TQ_ERR_OOM = 3,           /* tq_create could not allocate its tables */
-  TQ_ERR_UNSUPPORTED = 4,   /* valid but not implemented (e.g. d != 128) */
+  TQ_ERR_UNSUPPORTED = 4,   /* valid but not implemented (e.g. d = 48) */
   TQ_ERR_DEVICE_CHECK = 5,  /* a kernel skipped out-of-range device input */
   TQ_ERR_WORKSPACE = 6      /* workspace too small for the requested call */
 } tq_status;
@@ -73,8 +73,11 @@ typedef enum { TQ_BF16 = 0, TQ_F32 = 1 } tq_dtype;
 #define TQ_CODEBOOK_GAUSSIAN 0
 #define TQ_CODEBOOK_SPHERE 1
 
-/* Method configuration.  d = 128 and page_size = 16 are the supported
- * values.  Bits per channel in [1, 4]; channels [0, split) of the rotated
+/* Method configuration.  d is a multiple of 32 in [32, 256]; page_size = 16.
+ * d = 128 runs on the tensor-core kernels (tcgen05 quantize, mma.sync LUT
+ * decode); every other d on generic CUDA-core kernels that compute the same
+ * records and the same attention (tq_causal_attention and tq_search: d = 128
+ * only).  Bits per channel in [1, 4]; channels [0, split) of the rotated
  * vector use bits_hi, channels [split, d) bits_lo; split is a multiple of 32.
  * m (QJL projections) is a multiple of 32 in [32, 128].  k_qjl = 0 gives
  * MSE-only keys (no signs, no residual norm stored).  codebook: one of the
@@ -90,8 +93,9 @@ typedef struct {
 
 typedef struct tq_ctx tq_ctx;   /* opaque; immutable after creation */
 
-/* Fill `cfg` with d = 128, page_size = 16, b bits on every channel for keys
- * and values, QJL on keys with m projections, and `seed`. */
+/* Fill `cfg` with head dimension d, page_size = 16, b bits on every channel
+ * for keys and values (split = d/2 rounded down to a multiple of 32), QJL on
+ * keys with m projections, the Gaussian codebook and `seed`. */
 tq_status tq_config_init(tq_config* cfg, int d, int b, int m, uint64_t seed);
 
 /* Build the context on the current device ([P4] §4.1-§4.3): the random

@@ -29,7 +29,7 @@ bool valid_bits(int b) { return b >= 1 && b <= 4; }
 
 tq_status check_config(const tq_config* c) {
   if (!c) return TQ_ERR_INVALID_ARG;
-  if (c->d != kD || c->page_size != kPage) return TQ_ERR_UNSUPPORTED;
+  if (c->d < 32 || c->d > kDMax || c->d % 32 || c->page_size != kPage) return TQ_ERR_UNSUPPORTED;
   if (c->m < 32 || c->m > kMaxM || c->m % 32) return TQ_ERR_INVALID_ARG;
   if (!valid_bits(c->k_bits_hi) || !valid_bits(c->k_bits_lo) || !valid_bits(c->v_bits_hi) ||
       !valid_bits(c->v_bits_lo))
@@ -103,24 +103,6 @@ uint16_t to_f16(float x) {
   const uint32_t rem = man & 0x1FFFu;
   if (rem > 0x1000u || (rem == 0x1000u && (h & 1u))) ++h;
   return static_cast<uint16_t>(sign | h);
-}
-
-// bf16 of a double, round to nearest even (host; |x| well inside the normal range or 0)
-uint16_t to_bf16(double xd) {
-  const float x = static_cast<float>(xd);
-  uint32_t b;
-  std::memcpy(&b, &x, 4);
-  const uint32_t rem = b & 0xFFFFu;
-  uint32_t h = b >> 16;
-  if (rem > 0x8000u || (rem == 0x8000u && (h & 1u))) ++h;
-  return static_cast<uint16_t>(h);
-}
-
-double from_bf16(uint16_t h) {
-  const uint32_t b = static_cast<uint32_t>(h) << 16;
-  float x;
-  std::memcpy(&x, &b, 4);
-  return static_cast<double>(x);
 }
 
 float from_f16(uint16_t h) {
@@ -226,7 +208,7 @@ extern "C" tq_status tq_config_init(tq_config* cfg, int d, int b, int m, uint64_
   cfg->page_size = kPage;
   cfg->k_bits_hi = cfg->k_bits_lo = b;
   cfg->v_bits_hi = cfg->v_bits_lo = b;
-  cfg->k_split = cfg->v_split = d / 2;
+  cfg->k_split = cfg->v_split = d / 64 * 32;          // half the channels, rounded down to a multiple of 32
   cfg->k_qjl = 1;
   cfg->seed = seed;
   cfg->codebook = TQ_CODEBOOK_GAUSSIAN;
@@ -271,36 +253,29 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
   for (int i = 0; i < m; ++i)
     for (int j = 0; j < d; ++j) st_[static_cast<size_t>(j) * m + i] = static_cast<float>(s[i * d + j]);
 
-  // tensor-core operand tiles and double-float refinement tables
+  // tensor-core operand tiles (d = 128 only: the swizzled layout holds 64-channel
+  // blocks) and double-float refinement tables
   std::vector<uint16_t> pih(d * d), pil(d * d), sh(static_cast<size_t>(m) * d), sl(static_cast<size_t>(m) * d);
   std::vector<float> pidf(static_cast<size_t>(d) * d * 2);
   for (int i = 0; i < d; ++i)
     for (int k = 0; k < d; ++k) {
-      const double v = pi[i * d + k] * kPiScale;   // scaled so the low part stays a normal fp16
-      const uint16_t hi = to_f16(static_cast<float>(v));
-      pih[swz(i, k, d)] = hi;
-      pil[swz(i, k, d)] = to_f16(static_cast<float>(v - static_cast<double>(from_f16(hi))));
+      if (d == kD) {
+        const double v = pi[i * d + k] * kPiScale;   // scaled so the low part stays a normal fp16
+        const uint16_t hi = to_f16(static_cast<float>(v));
+        pih[swz(i, k, d)] = hi;
+        pil[swz(i, k, d)] = to_f16(static_cast<float>(v - static_cast<double>(from_f16(hi))));
+      }
       const float phi = static_cast<float>(pi[i * d + k]);
       pidf[(i * d + k) * 2] = phi;
       pidf[(i * d + k) * 2 + 1] = static_cast<float>(pi[i * d + k] - static_cast<double>(phi));
     }
-  for (int p = 0; p < m; ++p)
-    for (int j = 0; j < d; ++j) {
-      const uint16_t hi = to_f16(static_cast<float>(s[p * d + j]));
-      sh[swz(p, j, m)] = hi;
-      sl[swz(p, j, m)] = to_f16(static_cast<float>(s[p * d + j] - static_cast<double>(from_f16(hi))));
-    }
-  // bf16 hi + lo (swizzled operand tiles) + third term (row-major) of Pi
-  std::vector<uint16_t> pbh(d * d), pbl(d * d), pb3(d * d);
-  for (int i = 0; i < d; ++i)
-    for (int k = 0; k < d; ++k) {
-      const double v = pi[i * d + k];
-      const uint16_t h1 = to_bf16(v);
-      const uint16_t h2 = to_bf16(v - from_bf16(h1));
-      pbh[swz(i, k, d)] = h1;
-      pbl[swz(i, k, d)] = h2;
-      pb3[i * d + k] = to_bf16(v - from_bf16(h1) - from_bf16(h2));
-    }
+  if (d == kD)
+    for (int p = 0; p < m; ++p)
+      for (int j = 0; j < d; ++j) {
+        const uint16_t hi = to_f16(static_cast<float>(s[p * d + j]));
+        sh[swz(p, j, m)] = hi;
+        sl[swz(p, j, m)] = to_f16(static_cast<float>(s[p * d + j] - static_cast<double>(from_f16(hi))));
+      }
   std::vector<float> adf(static_cast<size_t>(m) * d * 2), sdf(static_cast<size_t>(m) * d * 2);
   std::vector<float> wt(static_cast<size_t>(d) * (d + m));   // W = [Pi; S Pi], stored transposed
   for (int r = 0; r < d; ++r)
@@ -330,10 +305,7 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
   size_t o_sdf = align256(o_adf + sizeof(float) * d * m * 2);
   size_t o_pidf = align256(o_sdf + sizeof(float) * d * m * 2);
   size_t o_wt = align256(o_pidf + sizeof(float) * d * d * 2);
-  size_t o_pbh = align256(o_wt + sizeof(float) * d * (d + m));
-  size_t o_pbl = align256(o_pbh + sizeof(uint16_t) * d * d);
-  size_t o_pb3 = align256(o_pbl + sizeof(uint16_t) * d * d);
-  size_t o_err = align256(o_pb3 + sizeof(uint16_t) * d * d);
+  size_t o_err = align256(o_wt + sizeof(float) * d * (d + m));
   size_t o_cnt = align256(o_err + sizeof(uint32_t));
   size_t total = align256(o_cnt + 2 * sizeof(unsigned long long));
   void* blk = nullptr;
@@ -358,9 +330,6 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
   ctx->tab.s_df = reinterpret_cast<float*>(b + o_sdf);
   ctx->tab.pi_df = reinterpret_cast<float*>(b + o_pidf);
   ctx->tab.wt = reinterpret_cast<float*>(b + o_wt);
-  ctx->tab.pibh_sw = reinterpret_cast<unsigned short*>(b + o_pbh);
-  ctx->tab.pibl_sw = reinterpret_cast<unsigned short*>(b + o_pbl);
-  ctx->tab.pi3 = reinterpret_cast<unsigned short*>(b + o_pb3);
   ctx->tab.err = reinterpret_cast<uint32_t*>(b + o_err);
   ctx->tab.counters = reinterpret_cast<unsigned long long*>(b + o_cnt);
   bool ok = cudaMemcpy(ctx->tab.pit, pit.data(), sizeof(float) * d * d, cudaMemcpyHostToDevice) == cudaSuccess &&
@@ -376,9 +345,6 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
             cudaMemcpy(ctx->tab.a_df, adf.data(), sizeof(float) * d * m * 2, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemcpy(ctx->tab.s_df, sdf.data(), sizeof(float) * d * m * 2, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemcpy(ctx->tab.wt, wt.data(), sizeof(float) * d * (d + m), cudaMemcpyHostToDevice) == cudaSuccess &&
-            cudaMemcpy(ctx->tab.pibh_sw, pbh.data(), 2 * d * d, cudaMemcpyHostToDevice) == cudaSuccess &&
-            cudaMemcpy(ctx->tab.pibl_sw, pbl.data(), 2 * d * d, cudaMemcpyHostToDevice) == cudaSuccess &&
-            cudaMemcpy(ctx->tab.pi3, pb3.data(), 2 * d * d, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemset(b + o_err, 0, total - o_err) == cudaSuccess;
   if (!ok) { cudaFree(blk); delete static_cast<std::mutex*>(ctx->fused_mu); delete ctx; cudaGetLastError(); return TQ_ERR_CUDA; }
   // the fused decode step's second stream and its fork/join events: made here,
@@ -473,6 +439,14 @@ tq_status quantize_impl(const tq_ctx* ctx, const void* k, const void* v, tq_dtyp
     a.max_ctas = max_ctas;
   }
   cudaError_t e = cudaSuccess;
+  if (ctx->cfg.d != kD) {                 // head dimensions other than 128: CUDA-core kernel
+    for (int kind = 0; kind < 2; ++kind) {
+      if (!args[kind].x) continue;
+      const cudaError_t eg = launch_quantize_generic(args[kind], ctx->cfg.d, s);
+      if (eg != cudaSuccess) return cuda_fail(eg);
+    }
+    return TQ_OK;
+  }
   if (launch_quantize_pipe(args[0], args[1], s, &e)) return cuda_status(e);
   if (launch_quantize_tc(args[0], args[1], s, &e)) return cuda_status(e);
   for (int kind = 0; kind < 2; ++kind) {
@@ -530,7 +504,7 @@ extern "C" tq_status tq_decode_chunk(const tq_ctx* ctx, int batch, int Hq, int H
   if (!ctx || !chunk_tokens || batch < 1 || Hq < 1 || H < 1 || Hq % H || max_seq_len < 0 || total_tokens < 0 ||
       total_tokens > static_cast<long long>(batch) * max_seq_len)
     return TQ_ERR_INVALID_ARG;
-  int ctas = lut_decode_ctas(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H);
+  int ctas = ctx->cfg.d == kD ? lut_decode_ctas(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H) : 0;
   if (fused_append && ctas > 0) ctas -= append_reserve(batch, H);
   if (ctas > 0)
     *chunk_tokens = pick_chunk_total(batch, H, total_tokens, max_seq_len, ctas);
@@ -576,7 +550,7 @@ tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batc
   if (batch == 0) return TQ_OK;
   if (!q || !seq_lens || !block_table || !k_cache || !v_cache || !out || !workspace)
     return TQ_ERR_INVALID_ARG;
-  int lut_ctas = lut_decode_ctas(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H);
+  int lut_ctas = ctx->cfg.d == kD ? lut_decode_ctas(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H) : 0;
   if (fused && lut_ctas > 0) lut_ctas -= fused->reserve;
   int chunk = chunk_tokens              ? chunk_tokens
               : lut_ctas > 0            ? pick_chunk_warps(batch * H, max_seq_len, lut_ctas)
@@ -619,6 +593,7 @@ tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batc
   a.sched = reinterpret_cast<int*>(w + o_frag + align256(sizeof(uint32_t) * static_cast<size_t>(batch) * Hq * kQFragWords));
   a.out = out;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (d != kD) return cuda_status(launch_decode_generic(a, d, stages, st));
   if (!fused) return cuda_status(launch_decode(a, stages, st));
   a.new_token = 1;                       // len_add is 0 here: the partials cover [0, seq_lens[b])
   a.max_ctas = sm_count() - fused->reserve;
@@ -671,6 +646,19 @@ extern "C" tq_status tq_append_decode_ex(const tq_ctx* ctx, const void* k_new, c
   if (!k_cache || !v_cache || maxp < 1 || num_pages < 1) return TQ_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15) return TQ_ERR_INVALID_ARG;
   if (static_cast<long long>(batch) * H > (1LL << 31) - 1) return TQ_ERR_INVALID_ARG;
+  if (ctx->cfg.d != kD) {                 // other head dimensions: append, then decode over L + 1
+    st = quantize_impl(ctx, k_new, v_new, dtype, batch, 1, H, seq_lens, block_table, maxp, num_pages, k_cache, v_cache,
+                       stream, 0);
+    if (st != TQ_OK) return st;
+    if (partials_begin && cudaEventRecord(static_cast<cudaEvent_t>(partials_begin), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return cuda_fail(cudaGetLastError());
+    st = decode_impl(ctx, q, dtype, batch, Hq, H, seq_lens, 1, max_seq_len, block_table, maxp, num_pages, k_cache,
+                     v_cache, chunk_tokens, softmax_scale, out, workspace, workspace_bytes, TQ_STAGE_ALL, stream);
+    if (st == TQ_OK && partials_end &&
+        cudaEventRecord(static_cast<cudaEvent_t>(partials_end), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return cuda_fail(cudaGetLastError());
+    return st;
+  }
   tq_ctx* c = const_cast<tq_ctx*>(ctx);
   // the fork/join events are shared by every call on this context: one host
   // thread at a time records and waits on them
@@ -718,7 +706,7 @@ extern "C" tq_status tq_causal_attention(const tq_ctx* ctx, const void* q, tq_dt
     return TQ_ERR_INVALID_ARG;
   if (dtype != TQ_BF16 && dtype != TQ_F32) return TQ_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return TQ_ERR_INVALID_ARG;
-  if (Hq / H > kMaxGroup) return TQ_ERR_UNSUPPORTED;
+  if (Hq / H > kMaxGroup || ctx->cfg.d != kD) return TQ_ERR_UNSUPPORTED;
   const int lut_ctas = lut_decode_ctas(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H);
   if (lut_ctas <= 0) return TQ_ERR_UNSUPPORTED;        // the bit widths the persistent kernel takes
   if (batch == 0) return TQ_OK;
@@ -824,7 +812,7 @@ extern "C" tq_status tq_search(const tq_ctx* ctx, const void* q, tq_dtype dtype,
   if (nq < 1 || n_db < 1 || num_pages < 1 || k_top < 1 || k_top > n_db || k_top > search_max_k())
     return TQ_ERR_INVALID_ARG;
   if (static_cast<long long>(num_pages) * kPage < n_db) return TQ_ERR_INVALID_ARG;
-  if (nq > search_max_queries()) return TQ_ERR_UNSUPPORTED;   // checked before anything is launched
+  if (nq > search_max_queries() || ctx->cfg.d != kD) return TQ_ERR_UNSUPPORTED;   // checked before any launch
   if ((reinterpret_cast<uintptr_t>(workspace) & 15) || (reinterpret_cast<uintptr_t>(k_cache) & 15))
     return TQ_ERR_INVALID_ARG;
   if (workspace_bytes < search_ws_bytes(nq, n_db, ctx->cfg.m)) return TQ_ERR_WORKSPACE;

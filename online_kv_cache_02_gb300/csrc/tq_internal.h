@@ -85,12 +85,6 @@ struct DeviceTables {
   float* s_df;              // S as double-float pairs [m][128][2]
   float* pi_df;             // Pi as double-float pairs [128][128][2]
   float* wt;                // W^T, fp32 [d][d + m]: W = [Pi; S Pi], wt[k*(d+m) + r] = W[r][k]
-  // bf16 split of Pi for the bf16-input quantize kernel: Pi = hi + lo + third
-  // (each bf16, rounded in turn); hi and lo in the 128-byte-swizzled K-major
-  // layout above, the third term row-major [128][128]
-  unsigned short* pibh_sw;
-  unsigned short* pibl_sw;
-  unsigned short* pi3;
 };
 
 struct QuantizeArgs {
@@ -191,6 +185,11 @@ bool launch_quantize_tc(const QuantizeArgs& k, const QuantizeArgs& v, cudaStream
 // covered (fp32 inputs, a codebook too fine for its cell tables).
 bool launch_quantize_pipe(const QuantizeArgs& k, const QuantizeArgs& v, cudaStream_t s, cudaError_t* err);
 cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s);
+// Head dimensions other than 128 (tq_generic.cu): CUDA-core quantize and
+// decode for d a multiple of 32 up to 256.
+constexpr int kDMax = 256;
+cudaError_t launch_quantize_generic(const QuantizeArgs& a, int d, cudaStream_t s);
+cudaError_t launch_decode_generic(const DecodeArgs& a, int d, int stages, cudaStream_t s);
 // Persistent lookup-table kernel (tq_decode_lut.cu): CTAs it runs with at
 // most, one per SM (0: configuration not supported), and its launch (false:
 // not supported).  A launch runs 12 or 16 warps per CTA: every warp takes

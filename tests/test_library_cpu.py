@@ -84,7 +84,11 @@ def test_config_validation_without_gpu(tq):
     assert (cfg.k_bits_hi, cfg.k_split, cfg.page_size, cfg.k_qjl) == (3, 64, 16, 1)
     assert st("tq_config_init", ctypes.byref(cfg), 128, 5, 128, 0) == tq.TQ_ERR_INVALID_ARG
     assert st("tq_config_init", ctypes.byref(cfg), 128, 3, 100, 0) == tq.TQ_ERR_INVALID_ARG
-    assert st("tq_config_init", ctypes.byref(cfg), 64, 3, 128, 0) == tq.TQ_ERR_UNSUPPORTED
+    for d in (48, 16, 288, 512):                      # head dims off the multiple-of-32 grid or above 256
+        assert st("tq_config_init", ctypes.byref(cfg), d, 3, 128, 0) == tq.TQ_ERR_UNSUPPORTED
+    for d, split in ((32, 0), (64, 32), (96, 32), (256, 128)):
+        assert st("tq_config_init", ctypes.byref(cfg), d, 3, 128, 0) == tq.TQ_OK
+        assert (cfg.d, cfg.k_split, cfg.v_split) == (d, split, split)
     out = ctypes.c_void_p()
     bad = tq.make_config(k_bits=(3, 3), v_bits=(3, 3), k_split=40)
     assert st("tq_create_ex", ctypes.byref(bad), ctypes.byref(out)) == tq.TQ_ERR_INVALID_ARG

@@ -21,18 +21,22 @@ def p3():
 
 # --- rotation ---------------------------------------------------------------
 
-def test_rotation_is_orthogonal(p3):
-    Pi = p3.Pi
-    assert np.max(np.abs(Pi.T @ Pi - np.eye(D))) < 1e-12
-    assert np.max(np.abs(Pi @ Pi.T - np.eye(D))) < 1e-12
+@pytest.mark.parametrize("d", [32, 64, 128, 256])
+def test_rotation_is_orthogonal(d):
+    Pi = oracle.rotation_matrix(d, 0)
+    assert Pi.shape == (d, d)
+    assert np.max(np.abs(Pi.T @ Pi - np.eye(d))) < 1e-12
+    assert np.max(np.abs(Pi @ Pi.T - np.eye(d))) < 1e-12
 
 
-def test_rotation_is_the_positive_diagonal_qr_factor(p3):
-    g = oracle.gaussian_stream(0, 1, D * D).reshape(D, D)
-    R = p3.Pi.T @ g
+@pytest.mark.parametrize("d", [32, 128, 256])
+def test_rotation_is_the_positive_diagonal_qr_factor(d):
+    Pi = oracle.rotation_matrix(d, 0)
+    g = oracle.gaussian_stream(0, 1, d * d).reshape(d, d)
+    R = Pi.T @ g
     assert np.max(np.abs(np.tril(R, -1))) < 1e-11
     assert np.all(np.diag(R) > 0)
-    assert np.allclose(p3.Pi[:, 0], g[:, 0] / np.linalg.norm(g[:, 0]), atol=1e-14)
+    assert np.allclose(Pi[:, 0], g[:, 0] / np.linalg.norm(g[:, 0]), atol=1e-14)
 
 
 def test_rotation_spreads_coordinates_like_the_sphere():
@@ -57,20 +61,22 @@ def _unit_vectors(n, d, seed):
     return x / np.linalg.norm(x, axis=1, keepdims=True)
 
 
-def test_two_over_pi_shrinkage_one_bit():
-    """MSE-only 1-bit: E<q, x^>/<q, x> = sqrt(d) sqrt(2/pi) Gamma(d/2) / (sqrt(pi) Gamma((d+1)/2))."""
-    p = oracle.make_params(d=D, k_bits=(1, 1), v_bits=(1, 1), seed=3, k_qjl=False)
-    closed = math.sqrt(D) * math.sqrt(2 / math.pi) * math.exp(
-        math.lgamma(D / 2) - math.lgamma((D + 1) / 2)) / math.sqrt(math.pi)
-    assert abs(closed - 0.637864) < 1e-6 and abs(closed - 2 / math.pi) < 2e-3
-    X = _unit_vectors(100000, D, 5)
+@pytest.mark.parametrize("d,n,closed_6dp", [(64, 100000, 0.639111), (128, 100000, 0.637864), (256, 50000, 0.637242)])
+def test_two_over_pi_shrinkage_one_bit(d, n, closed_6dp):
+    """MSE-only 1-bit: E<q, x^>/<q, x> = sqrt(d) sqrt(2/pi) Gamma(d/2) / (sqrt(pi) Gamma((d+1)/2)), which falls
+    to 2/pi = 0.63662 as d grows."""
+    p = oracle.make_params(d=d, k_bits=(1, 1), v_bits=(1, 1), seed=3, k_qjl=False)
+    closed = math.sqrt(d) * math.sqrt(2 / math.pi) * math.exp(
+        math.lgamma(d / 2) - math.lgamma((d + 1) / 2)) / math.sqrt(math.pi)
+    assert abs(closed - closed_6dp) < 1e-6 and 2 / math.pi < closed < 2 / math.pi * (1 + 1 / d)
+    X = _unit_vectors(n, d, 5)
     q = oracle.quantize_vectors(p, X, "v")
     Xhat = tq.dequantize_values(p, {"codes": q["codes"], "n16": np.linalg.norm(X, axis=1)}) @ p.Pi
     ratio = np.sum(X * Xhat, axis=1)          # <x, x^> / ||x||^2 with ||x|| = 1
     se = ratio.std() / math.sqrt(ratio.size)
     assert abs(ratio.mean() - closed) < 4 * se + 1e-12
     # and with a general query: E<q, x^> = closed * <q, x> (linear in q)
-    qv = np.random.default_rng(6).standard_normal(D)
+    qv = np.random.default_rng(6).standard_normal(d)
     num = Xhat @ qv
     den = X @ qv
     slope = np.sum(num * den) / np.sum(den * den)
@@ -78,10 +84,11 @@ def test_two_over_pi_shrinkage_one_bit():
 
 
 @pytest.mark.parametrize("bits", [1, 2, 3, 4])
-def test_distortion_per_bit(bits):
+@pytest.mark.parametrize("d", [128, 256])
+def test_distortion_per_bit(bits, d):
     """||x - x^||^2 / ||x||^2 on random unit vectors tracks the Gaussian Lloyd-Max MSE."""
-    p = oracle.make_params(d=D, k_bits=(bits, bits), v_bits=(bits, bits), seed=2, k_qjl=False)
-    X = _unit_vectors(4000, D, bits)
+    p = oracle.make_params(d=d, k_bits=(bits, bits), v_bits=(bits, bits), seed=2, k_qjl=False)
+    X = _unit_vectors(4000, d, bits)
     q = oracle.quantize_vectors(p, X, "v")
     Yhat = tq.dequantize_values(p, {"codes": q["codes"], "n16": np.ones(len(X))})
     err = np.sum((q["y"] - Yhat) ** 2, axis=1).mean()
@@ -165,13 +172,14 @@ def test_zero_vector(p3):
     assert np.all(q["signs"] == 1)                      # S * 0 = 0 -> sign bit set
 
 
-def test_two_stage_estimator_is_unbiased():
+@pytest.mark.parametrize("d,m", [(128, 128), (256, 96)])
+def test_two_stage_estimator_is_unbiased(d, m):
     """Mean over many Gaussian projections of the stage-2 estimate equals <q, x> exactly."""
     rng = np.random.default_rng(11)
-    p = oracle.make_params(d=D, m=128, k_bits=(2, 2), v_bits=(2, 2), seed=4)
-    x = rng.standard_normal(D)
+    p = oracle.make_params(d=d, m=m, k_bits=(2, 2), k_split=d // 2, v_bits=(2, 2), v_split=d // 2, seed=4)
+    x = rng.standard_normal(d)
     x[:4] *= 10
-    qv = rng.standard_normal(D)
+    qv = rng.standard_normal(d)
     q = oracle.quantize_vectors(p, x[None, :], "k")
     r = q["r"][0]
     rho = float(np.linalg.norm(r))
@@ -181,7 +189,7 @@ def test_two_stage_estimator_is_unbiased():
     est = np.empty(n_draws)
     mse_only = None
     for i in range(n_draws):
-        S = rng.standard_normal((p.m, D))
+        S = rng.standard_normal((p.m, d))
         pp = tq.TQParams(**{**p.__dict__, "S": S})
         z = S @ r
         rec = {"codes": q["codes"], "n16": q["n16"], "signs": (z >= 0).astype(np.uint8)[None, :],
