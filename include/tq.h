@@ -288,9 +288,11 @@ tq_status tq_causal_attention(const tq_ctx* ctx, const void* q, tq_dtype dtype, 
  * 16 = a kernel's shared-memory layout did not fit (it did no work). */
 tq_status tq_check_device_status(const tq_ctx* ctx, uint32_t* flags);
 
-/* Counters of near-boundary decisions the quantize kernels re-took in fp64
- * since creation (or the last reset): out[0] codes, out[1] key vectors whose
- * signs were re-taken.  Synchronises the device. */
+/* Counters of the decisions the quantize kernels took again exactly (fp64 or
+ * double-float) because their fast arithmetic found them inside its guard,
+ * since creation (or the last reset): out[0] codes near a boundary, out[1]
+ * sign bits near zero (the CUDA-core fp32-input kernel counts key vectors
+ * with any such sign).  Synchronises the device. */
 tq_status tq_refine_counters(const tq_ctx* ctx, unsigned long long out[2], int reset);
 
 const char* tq_status_string(tq_status status);

@@ -6,7 +6,7 @@
 // Lloyd-Max codebook is only looked up), §4.3 (residual r = x - Q^-1(Q(x)) and
 // the 1-bit sign sketch of a random projection of r), §3.1 (paged blocks).
 //
-// One persistent CTA per SM, 17 warps, tiles of 128 vectors (K tiles first,
+// One persistent CTA per SM, 18 warps, tiles of 128 vectors (K tiles first,
 // then V tiles).  Roles:
 //   warp 16, one lane: the TMA of x tiles (bf16 rows, two 64-channel boxes
 //       with the 128-byte swizzle) into a two-stage ring, and every MMA:
@@ -17,7 +17,11 @@
 //   warps 0-15: the epilogue, two groups of eight (group s takes the tiles of
 //       slot s = local tile index % 2); a row (vector) has two threads, one
 //       per 64-channel half: warp w reads tensor-memory lanes 32 (w % 4)..,
-//       half (w / 4) % 2.
+//       half (w / 4) % 2;
+//   warp 17: the fixer.  A row whose fast path met a decision it cannot take
+//       for certain (below) is handed to it through a shared-memory ring, and
+//       it quantizes that vector again from x, every decision made exactly,
+//       and rewrites the whole record.
 // Tensor memory: slot s = columns [256 s, 256 s + 256): y, then z, in the first
 // 128; in the second 128, first x (fp16, 64 columns), then r' (fp16 hi and
 // lo, 64 columns each).  While one group works on tile j, the other group's
@@ -26,21 +30,23 @@
 // Epilogue of a tile, per thread (64 channels):
 //   1. from the bf16 x tile in shared memory: the sum of squares of its half
 //      (exact squares, fp32 sums), the halves added through shared memory, the
-//      fp32 norm and the exactly rounded fp16 norm (recomputed in double-float
-//      when the fp32 norm lies within 4e-6 of an fp16 rounding midpoint); then
-//      x * 2^(14 - e), e the norm's binary exponent, to fp16 (exact for bf16
-//      values above 2^-28 of the norm) into tensor memory for the y MMA.
+//      fp32 norm and its fp16 rounding; then x * 2^(14 - e), e the norm's
+//      binary exponent, to fp16 (exact for bf16 values above 2^-28 of the
+//      norm) into tensor memory for the y MMA.
 //   2. per 32-channel chunk: fg = 8 u + 32, u = sqrt(d) y / ||x||; the cell
 //      floor(fg) of a 128-entry table (cells of 1/8 over u in [-4, 12), the
 //      unsigned conversion clamps the low end) gives the one boundary that can
 //      matter there (in the same units) and the code below it; codes as
 //      nibbles, then the stored words; for keys r' = y sqrt(d)/fp16(||x||) -
-//      c[code] as fp16 hi + lo pairs stored to tensor memory.  A u within
-//      4.5e-6 of its boundary is decided again by the warp from a double-float
-//      y and norm.
-//   3. keys: the sign bits of z; |z| below 2e-5 ||r'|| is decided again by the
-//      warp in double-float ((S Pi)_p x - fp16(||x||)/sqrt(d) S_p c^).
-//      fp16(||r||) from the two halves' sums.
+//      c[code] as fp16 hi + lo pairs stored to tensor memory.
+//   3. keys: the sign bits of z; fp16(||r||) from the two halves' sums.
+// The fast path writes every record.  A row goes to the fixer when its fp32
+// norm lies within 4e-6 of an fp16 rounding midpoint, a u within 4.5e-6 of
+// its boundary, or a |z| below 2e-5 ||r'||: after the group's next barrier
+// (both halves have stored the row by then) its thread puts it in the ring.
+// The fixer's own pass: the norm in double-float, y and z in fp32 with
+// four partial sums, and every u within 1e-4 of a boundary or |z| within
+// 2e-4 ||r|| of zero decided again in double-float.
 // Every wait is bounded: a wait that gives up sets the error word and every
 // later wait of that thread returns at once, so the CTA still reaches its end
 // (every named barrier is still met).
@@ -61,8 +67,11 @@ namespace {
 constexpr int kRows = 128;
 constexpr int kEpiWarps = 16;
 constexpr int kCtlWarp = 16;                 // TMA + MMA issue
-constexpr int kThreadsP = (kEpiWarps + 1) * 32;
+constexpr int kFixWarp = 17;                 // exact re-quantization of flagged rows
+constexpr int kThreadsP = (kEpiWarps + 2) * 32;
+constexpr int kQueue = 64;                   // fixer ring entries (tile * 128 + row)
 constexpr int kWaitLimitP = 1 << 22;
+constexpr int kFixIdleLimit = 1 << 26;       // the fixer's polls of an empty ring (about 128 ns apart)
 constexpr int kCells = 128;                  // cells of width 1/8 over u in [-4, 12)
 constexpr float kSqrtD = 11.313708498984761f;
 constexpr double kSqrtD64 = 11.313708498984760390;
@@ -73,7 +82,12 @@ constexpr float kInvSqrtDLo = 1.512702185735293e-09f;
 // rounding of fg and of the tabled 8t + 32 (2.4e-7 each).
 constexpr float kGuardFg = 8.0f * 4.5e-6f;
 constexpr float kGuardSign = 2e-5f;          // |z| < 2e-5 ||r'||: decide in double-float
-constexpr float kNormTol = 4e-6f;            // fp32 norm this close to an fp16 midpoint: exact norm
+// fp32 norm this close (relative) to an fp16 rounding midpoint: exact norm.  The
+// sum of the (exact) squares rounds at most 8 times along any path, so its
+// relative error is below 8 * 2^-24, the norm's below 3e-7.
+constexpr float kNormTol = 5e-7f;
+constexpr float kFixGuardU = 1e-4f;          // the fixer's fp32 u this close to a boundary: double-float
+constexpr float kFixGuardZ = 2e-4f;          // the fixer's fp32 |z| below this times ||r||: double-float
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffPIH = 0;                   // 16 Pi rounded to fp16, 128 x 128, 128-byte swizzle, K-major
@@ -95,7 +109,11 @@ constexpr int kTabBar = 9280;                // mbarriers
 constexpr int kBarTab = 0, kBarXFull = 1, kBarXFree = 3, kBarXTmem = 5, kBarYFull = 7, kBarRFull = 9, kBarZFull = 11,
               kNumBars = 13;
 constexpr int kTabTmem = kTabBar + 8 * kNumBars;
-constexpr int kTabBytes = kTabTmem + 16;
+constexpr int kTabT32 = kTabTmem + 16;       // [4][16] float boundaries (the fixer)
+constexpr int kTabQ = kTabT32 + 256;         // the fixer's ring (32-bit words, below)
+constexpr int kQTail = 0, kQHead = 1, kQDone = 2, kQProg = 4, kQVal = 8, kQSeq = 8 + 2 * kQueue;
+constexpr int kQWords = kQSeq + kQueue;
+constexpr int kTabBytes = kTabQ + 4 * kQWords;
 constexpr int kSmemP = kOffTab + kTabBytes + 1024;
 static_assert(kSmemP <= 232448, "shared memory per block");
 
@@ -489,6 +507,278 @@ __device__ __noinline__ uint32_t exact_sign(const __nv_bfloat16* xrow, const flo
   return (z.h > 0.0f || (z.h == 0.0f && z.l >= 0.0f)) ? 1u : 0u;
 }
 
+// Exact sign bit of projection p (warp together) from the lane's own four
+// channels (4 lane .. 4 lane + 3): x and the centroid-table indices of their
+// codes; the same double-float sum as exact_sign.
+__device__ __noinline__ uint32_t exact_sign_regs(const float (&xv)[4], const float* adf_row, const float* sdf_row,
+                                                 const int (&cidx)[4], const float* cents, const float* centl,
+                                                 float n16f, int lane) {
+  const float4* ar = reinterpret_cast<const float4*>(adf_row) + 2 * lane;
+  const float4* sr = reinterpret_cast<const float4*>(sdf_row) + 2 * lane;
+  const float4 a0 = __ldg(ar), a1 = __ldg(ar + 1), s0 = __ldg(sr), s1 = __ldg(sr + 1);
+  const float ah[4] = {a0.x, a0.z, a1.x, a1.z}, al[4] = {a0.y, a0.w, a1.y, a1.w};
+  const float sh[4] = {s0.x, s0.z, s1.x, s1.z}, sl[4] = {s0.y, s0.w, s1.y, s1.w};
+  DF d1{0.f, 0.f}, d2{0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    d1 = df_fma_acc(d1, ah[k], al[k], xv[k]);
+    d2 = df_add(d2, df_mul(DF{sh[k], sl[k]}, DF{cents[cidx[k]], centl[cidx[k]]}));
+  }
+  d1 = warp_df_sum(d1);
+  d2 = warp_df_sum(d2);
+  const DF f = df_mul(DF{n16f, 0.f}, DF{kInvSqrtDHi, kInvSqrtDLo});
+  const DF fz = df_mul(f, d2);
+  const DF z = df_add(d1, DF{-fz.h, -fz.l});
+  return (z.h > 0.0f || (z.h == 0.0f && z.l >= 0.0f)) ? 1u : 0u;
+}
+
+// Record of vector gv (null when its position or page is out of range; the
+// epilogue flags those).
+__device__ __forceinline__ unsigned char* locate(const QuantizeArgs& a, long long gv, long long nvec, int& slot,
+                                                 bool flag) {
+  int hh, t, b;
+  if (nvec < (1LL << 31)) {
+    const uint32_t g32 = static_cast<uint32_t>(gv), H32 = static_cast<uint32_t>(a.H);
+    const uint32_t bt = g32 / H32;
+    hh = static_cast<int>(g32 - bt * H32);
+    b = static_cast<int>(bt / static_cast<uint32_t>(a.n_new));
+    t = static_cast<int>(bt - static_cast<uint32_t>(b) * static_cast<uint32_t>(a.n_new));
+  } else {
+    const long long bt = gv / a.H;
+    hh = static_cast<int>(gv % a.H);
+    t = static_cast<int>(bt % a.n_new);
+    b = static_cast<int>(bt / a.n_new);
+  }
+  const int pos = a.start_pos[b] + t;
+  const int blk = pos >> 4;
+  if (pos < 0 || blk >= a.maxp) {
+    if (flag) atomicOr(a.tab.err, kErrBlock);
+    return nullptr;
+  }
+  const int page = a.block_table[static_cast<long long>(b) * a.maxp + blk];
+  if (page < 0 || page >= a.num_pages) {
+    if (flag) atomicOr(a.tab.err, kErrPage);
+    return nullptr;
+  }
+  slot = pos & 15;
+  return a.cache + static_cast<long long>(page) * a.page_bytes + static_cast<long long>(hh) * a.lay.block_bytes;
+}
+
+__device__ __forceinline__ uint32_t ld_vol(const uint32_t* p) {
+  return *reinterpret_cast<const volatile uint32_t*>(p);
+}
+__device__ __forceinline__ void st_vol(uint32_t* p, uint32_t v) { *reinterpret_cast<volatile uint32_t*>(p) = v; }
+
+// The fixer's ring (one producer thread at a time per call): reserve n
+// consecutive entries if there is room (false: decide here instead), then
+// write each entry and publish it by its sequence number.  An entry is two
+// words: local tile index << 7 | row, and kind << 16 | channel or projection.
+__device__ bool ring_reserve(uint32_t* q, uint32_t n, uint32_t& base) {
+  for (int it = 0; it < 64; ++it) {
+    const uint32_t t = ld_vol(q + kQTail);
+    if (t + n - ld_vol(q + kQHead) > static_cast<uint32_t>(kQueue)) return false;
+    if (atomicCAS(q + kQTail, t, t + n) == t) {
+      base = t;
+      return true;
+    }
+  }
+  return false;
+}
+__device__ __forceinline__ void ring_publish(uint32_t* q, uint32_t idx, uint32_t v0, uint32_t v1) {
+  st_vol(q + kQVal + 2 * (idx % kQueue), v0);
+  st_vol(q + kQVal + 2 * (idx % kQueue) + 1, v1);
+  __threadfence_block();
+  st_vol(q + kQSeq + idx % kQueue, idx + 1);
+}
+constexpr uint32_t kEntryCode = 0u, kEntrySign = 1u;
+
+// 8 bits to bits 0, 4, ..., 28.
+__device__ __forceinline__ uint32_t spread4(uint32_t x) {
+  x = (x | (x << 12)) & 0x000F000Fu;
+  x = (x | (x << 6)) & 0x03030303u;
+  return (x | (x << 3)) & 0x11111111u;
+}
+
+// The fixer: quantize vector gv again (the whole warp; lane l owns channels
+// and projections 4l .. 4l + 3) with every decision exact, and rewrite its
+// record: fp16 norm from a double-float norm; y = Pi x in fp32 (four partial
+// sums of 32 terms); codes, the ones within kFixGuardU of a boundary decided
+// in double-float; keys: r = y - fp16(||x||)/sqrt(d) c[code], z = S r in fp32,
+// the |z| below kFixGuardZ ||r|| decided in double-float; fp16(||r||).
+__device__ __forceinline__ void fix_vector(const QuantizeArgs& a, bool key, bool qjl, long long gv, long long nvec,
+                                           const unsigned char* tab, int bits0, int bits1, int split, int lane) {
+  int slot = 0;
+  unsigned char* rec = locate(a, gv, nvec, slot, false);
+  if (!rec) return;                                         // warp-uniform
+  const __nv_bfloat16* xrow = static_cast<const __nv_bfloat16*>(a.x) + gv * kD;
+  const int gofs = key ? 0 : 2;
+  float xv[4];
+  lane_x(xrow, lane, xv);
+  DF n2{0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) n2 = df_add(n2, df_sq(xv[k]));
+  n2 = warp_df_sum(n2);
+  float nf = 0.0f;
+  __half n16h = __float2half_rn(0.0f);
+  if (n2.h > 0.0f) {
+    const float rr = sqrtf(n2.h);
+    const float rl = (fmaf(-rr, rr, n2.h) + n2.l) / (2.0f * rr);
+    nf = rr + rl;
+    n16h = df_to_half(nf, rl - (nf - rr));
+  }
+  const float n16f = __half2float(n16h);
+
+  // y = Pi x: x_k from lane k / 4, row k of Pi^T (fp32) as one float4 per lane
+  float y[4];
+  {
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[c][i] = 0.0f;
+    const float4* pt = reinterpret_cast<const float4*>(a.tab.pit) + lane;
+#pragma unroll 2
+    for (int k = 0; k < kD; k += 4) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float xk = __shfl_sync(0xffffffffu, xv[c], k >> 2);
+        const float4 p4 = __ldg(pt + (k + c) * (kD / 4));
+        acc[c][0] = fmaf(p4.x, xk, acc[c][0]);
+        acc[c][1] = fmaf(p4.y, xk, acc[c][1]);
+        acc[c][2] = fmaf(p4.z, xk, acc[c][2]);
+        acc[c][3] = fmaf(p4.w, xk, acc[c][3]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y[i] = (acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i]);
+  }
+
+  // codes
+  const float* t32 = reinterpret_cast<const float*>(tab + kTabT32);
+  const double* t64 = reinterpret_cast<const double*>(tab + kTabT64);
+  const float ku = nf > 0.0f ? kSqrtD / nf : 0.0f;
+  int code[4];
+  uint32_t pend = 0u;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int j = 4 * lane + i, grp = j < split ? 0 : 1, nb = (1 << (grp ? bits1 : bits0)) - 1;
+    const float u = y[i] * ku;
+    const float* tb = t32 + (gofs + grp) * 16;
+    int c = 0;
+    bool near = false;
+    for (int k = 0; k < nb; ++k) {
+      c += u >= tb[k] ? 1 : 0;
+      near = near || fabsf(u - tb[k]) < kFixGuardU;
+    }
+    code[i] = c;
+    pend |= (near ? 1u : 0u) << i;
+  }
+  for (int it = 0; it < 128; ++it) {                         // at most 4 per lane: 128 rounds
+    const uint32_t who = __ballot_sync(0xffffffffu, pend != 0u);
+    if (!who) break;
+    const int src = __ffs(who) - 1;
+    const int i = __shfl_sync(0xffffffffu, __ffs(pend) - 1, src);
+    if (lane == src) pend &= pend - 1u;
+    const int j = 4 * src + i, grp = j < split ? 0 : 1, nb = (1 << (grp ? bits1 : bits0)) - 1;
+    const int c = exact_code(xrow, a.tab.pi_df + j * kD * 2, t64 + (gofs + grp) * 16, nb, lane);
+    if (lane == src) code[i] = c;
+  }
+
+  // stored code words: channels 8w .. 8w + 7 as nibbles come from lanes 2w, 2w + 1
+  uint32_t* cw = reinterpret_cast<uint32_t*>(rec + slot * a.lay.code_bytes);
+  {
+    const uint32_t nib = static_cast<uint32_t>(code[0] | (code[1] << 4) | (code[2] << 8) | (code[3] << 12));
+    const uint32_t pairw = nib | (__shfl_down_sync(0xffffffffu, nib, 1) << 16);
+    uint32_t cp[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cp[i] = __shfl_sync(0xffffffffu, pairw, (lane & ~7) + 2 * i);
+    if ((lane & 7) == 0) {
+      const int ch0 = 4 * lane, grp = ch0 < split ? 0 : 1, b = grp ? bits1 : bits0;
+      uint32_t w[4];
+      pack_dispatch(b, cp, w);
+      uint32_t* dst = cw + ((grp ? split * bits0 : 0) + (ch0 - grp * split) * b) / 32;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (k < b) dst[k] = w[k];
+    }
+  }
+  if (lane == 0) *(reinterpret_cast<unsigned short*>(rec + a.lay.off_norm) + slot) = __half_as_ushort(n16h);
+  if (!(key && qjl)) return;
+
+  // residual, its norm, z = S r
+  const float* cents = reinterpret_cast<const float*>(tab + kTabCent);
+  const float* centl = reinterpret_cast<const float*>(tab + kTabCentLo);
+  const float cs = n16f * kInvSqrtDHi;
+  float r[4];
+  int cidx[4];
+  float rho2 = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int j = 4 * lane + i;
+    cidx[i] = (j < split ? 0 : 16) + code[i];
+    r[i] = n16f > 0.0f ? fmaf(-cs, cents[cidx[i]], y[i]) : y[i];
+    rho2 = fmaf(r[i], r[i], rho2);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) rho2 += __shfl_xor_sync(0xffffffffu, rho2, o);
+  const float rho = sqrtf(rho2);
+  const int m = a.m;
+  const bool own = 4 * lane < m;
+  float z[4];
+  {
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[c][i] = 0.0f;
+    const float4* st4 = reinterpret_cast<const float4*>(a.tab.st) + (own ? lane : 0);
+#pragma unroll 2
+    for (int j = 0; j < kD; j += 4) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float rj = __shfl_sync(0xffffffffu, r[c], j >> 2);
+        const float4 s4 = __ldg(st4 + (j + c) * (m / 4));
+        acc[c][0] = fmaf(s4.x, rj, acc[c][0]);
+        acc[c][1] = fmaf(s4.y, rj, acc[c][1]);
+        acc[c][2] = fmaf(s4.z, rj, acc[c][2]);
+        acc[c][3] = fmaf(s4.w, rj, acc[c][3]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) z[i] = (acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i]);
+  }
+  uint32_t sb = 0u;
+  pend = 0u;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    sb |= (z[i] >= 0.0f ? 1u : 0u) << i;
+    pend |= (own && fabsf(z[i]) < kFixGuardZ * rho ? 1u : 0u) << i;
+  }
+  for (int it = 0; it < 128; ++it) {
+    const uint32_t who = __ballot_sync(0xffffffffu, pend != 0u);
+    if (!who) break;
+    const int src = __ffs(who) - 1;
+    const int i = __shfl_sync(0xffffffffu, __ffs(pend) - 1, src);
+    if (lane == src) pend &= pend - 1u;
+    const int p = 4 * src + i;
+    const uint32_t bit = exact_sign_regs(xv, a.tab.a_df + static_cast<long long>(p) * kD * 2,
+                                         a.tab.s_df + static_cast<long long>(p) * kD * 2, cidx, cents, centl, n16f, lane);
+    if (lane == src) sb = (sb & ~(1u << i)) | (bit << i);
+  }
+  // sign word w: bit 4 (l - 8w) + i is projection 4l + i
+  uint32_t bl[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) bl[i] = __ballot_sync(0xffffffffu, (sb >> i) & 1u);
+  if (lane < m / 32) {
+    uint32_t word = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) word |= spread4((bl[i] >> (8 * lane)) & 0xFFu) << i;
+    reinterpret_cast<uint32_t*>(rec + a.lay.off_signs + slot * (m / 8))[lane] = word;
+  }
+  if (lane == 0)
+    *(reinterpret_cast<unsigned short*>(rec + a.lay.off_rnorm) + slot) = __half_as_ushort(__float2half_rn(rho));
+}
+
 // Cell table of one group: cell g covers u in [-4 + g/8, -4 + (g+1)/8) (cell 0
 // reaches down to -inf, cell 127 up to +inf); it keeps the boundary inside it,
 // else the nearest one (as 8t + 32), and the number of boundaries below that
@@ -519,7 +809,8 @@ struct PipeParams {
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreadsP, 1)
+// 18 warps need <= 96 registers a thread: five warps share one SM sub-partition.
+__global__ void __maxnreg__(96)
     quantize_pipe_kernel(QuantizeArgs ka, QuantizeArgs va, const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv, PipeParams pp) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -546,8 +837,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     reinterpret_cast<float*>(tab + kTabCent)[tid] = k < (1 << gb.bits) ? gb.c[k] : 0.0f;
     reinterpret_cast<float*>(tab + kTabCentLo)[tid] = k < (1 << gb.bits) ? gb.c_lo[k] : 0.0f;
     reinterpret_cast<double*>(tab + kTabT64)[tid] = gb.t64[k];
+    reinterpret_cast<float*>(tab + kTabT32)[tid] = k < gb.nb ? gb.t[k] : 0.0f;
     if (tid < 16) reinterpret_cast<float*>(tab + kTabZero)[tid] = 0.0f;
   }
+  for (int i = tid; i < kQWords; i += kThreadsP) reinterpret_cast<uint32_t*>(tab + kTabQ)[i] = 0u;
   if (warp == kCtlWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tabs + kTabTmem),
                  "r"(512)
@@ -660,6 +953,97 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         (void)mbar_wait(bar(kBarZFull + ((nz - 1) & 1)), ((nz - 1) >> 1) & 1, f2);
     }
     __syncwarp();
+  } else if (warp == kFixWarp) {
+    // ---- fixer: decisions from the ring until both epilogue groups are done ---------
+    // A code entry: the exact code, compared with the stored one; when they differ
+    // (the fast path was wrong, not just close) the row is quantized again as a
+    // whole, once the group is past it.  A sign entry: the exact sign bit, patched
+    // into the stored word.
+    uint32_t* q = reinterpret_cast<uint32_t*>(tab + kTabQ);
+    const float* cents_k = reinterpret_cast<const float*>(tab + kTabCent);
+    const float* centl_k = reinterpret_cast<const float*>(tab + kTabCentLo);
+    uint32_t h = 0;
+    int idle = 0;
+    for (;;) {
+      uint32_t v0 = 0u, v1 = 0u, have = 0u;
+      if (lane == 0 && ld_vol(q + kQSeq + h % kQueue) == h + 1) {
+        __threadfence_block();
+        v0 = ld_vol(q + kQVal + 2 * (h % kQueue));
+        v1 = ld_vol(q + kQVal + 2 * (h % kQueue) + 1);
+        have = 1u;
+      }
+      have = __shfl_sync(0xffffffffu, have, 0);
+      if (have) {
+        v0 = __shfl_sync(0xffffffffu, v0, 0);
+        v1 = __shfl_sync(0xffffffffu, v1, 0);
+        ++h;
+        if (lane == 0) st_vol(q + kQHead, h);                 // the entry is free again
+        idle = 0;
+        const int jl = static_cast<int>(v0 >> 7), row = static_cast<int>(v0 & 127u);
+        const int tile = tile_of(jl);
+        const bool key = tile < pp.nk;
+        const QuantizeArgs& a = key ? ka : va;
+        const long long nvec = static_cast<long long>(a.batch) * a.n_new * a.H;
+        const long long gv = static_cast<long long>(key ? tile : tile - pp.nk) * kRows + row;
+        const int bits0 = key ? pp.kbits[0] : pp.vbits[0], bits1 = key ? pp.kbits[1] : pp.vbits[1];
+        const int split = key ? pp.ksplit : pp.vsplit;
+        int slot = 0;
+        unsigned char* rec = locate(a, gv, nvec, slot, false);
+        if (!rec) continue;
+        const __nv_bfloat16* sx = static_cast<const __nv_bfloat16*>(a.x) + gv * kD;
+        const uint32_t* cw = reinterpret_cast<const uint32_t*>(rec + slot * a.lay.code_bytes);
+        const int idx = static_cast<int>(v1 & 0xFFFFu);
+        if ((v1 >> 16) == kEntryCode) {
+          const int grp = idx < split ? 0 : 1;
+          const int code = exact_code(sx, a.tab.pi_df + idx * kD * 2,
+                                      reinterpret_cast<const double*>(tab + kTabT64) + ((key ? 0 : 2) + grp) * 16,
+                                      (1 << (grp ? bits1 : bits0)) - 1, lane);
+          if (lane == 0) atomicAdd(&a.tab.counters[0], 1ULL);
+          if (code != record_code(cw, bits0, bits1, split, idx)) {
+            // the rest of the row depends on this code: wait until the group
+            // is past the row's tile, then quantize the vector again
+            bool ok = false;
+            for (int it = 0; it < kWaitLimitP && !ok; ++it) {
+              ok = static_cast<int>(ld_vol(q + kQProg + (jl & 1))) > jl;
+              if (!ok) __nanosleep(64);
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1u : 0u, 0) != 0u;
+            if (!ok) {
+              failed = true;
+              break;
+            }
+            __threadfence();
+            fix_vector(a, key, kqjl, gv, nvec, tab, bits0, bits1, split, lane);
+          }
+        } else {
+          const float n16f = __half2float(__ushort_as_half(
+              __ldcg(reinterpret_cast<const unsigned short*>(rec + a.lay.off_norm) + slot)));
+          const uint32_t bit = exact_sign(sx, a.tab.a_df + static_cast<long long>(idx) * kD * 2,
+                                          a.tab.s_df + static_cast<long long>(idx) * kD * 2, cw, bits0, bits1, split,
+                                          cents_k, centl_k, n16f, lane);
+          if (lane == 0) {
+            atomicAdd(&a.tab.counters[1], 1ULL);
+            uint32_t* sw = reinterpret_cast<uint32_t*>(rec + a.lay.off_signs + slot * (a.m / 8)) + idx / 32;
+            const uint32_t w = __ldcg(sw), nw = (w & ~(1u << (idx & 31))) | (bit << (idx & 31));
+            if (nw != w) *sw = nw;
+          }
+        }
+        __syncwarp();
+        continue;
+      }
+      uint32_t done = 0u;
+      if (lane == 0 && ld_vol(q + kQDone) == 2u) {
+        __threadfence_block();
+        done = ld_vol(q + kQTail) == h ? 1u : 0u;
+      }
+      if (__shfl_sync(0xffffffffu, done, 0)) break;
+      if (++idle > kFixIdleLimit) {
+        failed = true;
+        break;
+      }
+      __nanosleep(128);
+    }
+    if (failed && lane == 0) atomicOr(ka.tab.err, kErrTimeout);
   } else {
     // ---- epilogue ---------------------------------------------------------------
     const int q = warp & 3, h = (warp >> 2) & 1, s = warp >> 3;
@@ -670,6 +1054,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     float* rho_part = reinterpret_cast<float*>(tab + kTabRho) + s * 256;
     const float* cents_k = reinterpret_cast<const float*>(tab + kTabCent);
     const float* centl_k = reinterpret_cast<const float*>(tab + kTabCentLo);
+    uint32_t* qring = reinterpret_cast<uint32_t*>(tab + kTabQ);
     for (int j = s; j < local_tiles; j += 2) {
       const int tile = tile_of(j);
       const bool key = tile < pp.nk;
@@ -705,6 +1090,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         ss_part[h * 128 + row] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       }
       named_sync(gbar, 256);
+      // the group is past its previous tile (the fixer may rewrite those rows)
+      if (q == 0 && h == 0 && lane == 0) st_vol(qring + kQProg + s, static_cast<uint32_t>(j));
       const float ss = ss_part[row] + ss_part[128 + row];
       float nf = ss > 0.0f ? sqrtf(ss) : 0.0f;
       // x * 2^(14 - e) with nf < 2^e: every |x_k| <= ||x|| stays below 2^14
@@ -818,6 +1205,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         const int b = grp ? bits1 : bits0;
         const uint32_t ctab = tabs + kTabCellT + (gofs + grp) * kCells * 4;
         uint32_t cp[4];
+        uint32_t dpend[2] = {0u, 0u}, dbase[2] = {0u, 0u};   // codes handed to the fixer
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {               // 16 channels at a time
           const int cb = ch0 + 16 * hh;
@@ -827,16 +1215,22 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           float dmin = INFINITY;
           codes_pass(v, ctab, k8, cpa, cpb, dmin);
           if (!valid || nf == 0.0f || !cw) dmin = INFINITY;
-          if (__any_sync(0xffffffffu, dmin < kGuardFg)) {
-            // rare: the warp decides the near codes exactly and patches their nibbles
-            uint32_t pend = 0;
-            if (dmin < kGuardFg) {
+          // rare: codes within the guard of their boundary go to the fixer (published
+          // once this chunk's words are stored); when its ring has no room, the warp
+          // decides them here and patches their nibbles
+          uint32_t pend = 0u;
+          if (dmin < kGuardFg) {
 #pragma unroll
-              for (int cc = 0; cc < 16; ++cc) {
-                const float fg = fmaf(v[cc], k8, 32.0f);
-                pend |= (fabsf(fg - lds_f(ctab + cell_off(fg))) < kGuardFg ? 1u : 0u) << cc;
-              }
+            for (int cc = 0; cc < 16; ++cc) {
+              const float fg = fmaf(v[cc], k8, 32.0f);
+              pend |= (fabsf(fg - lds_f(ctab + cell_off(fg))) < kGuardFg ? 1u : 0u) << cc;
             }
+            if (ring_reserve(qring, __popc(pend), dbase[hh])) {
+              dpend[hh] = pend;
+              pend = 0u;
+            }
+          }
+          if (__any_sync(0xffffffffu, pend != 0u)) {
             for (;;) {
               const uint32_t who = __ballot_sync(0xffffffffu, pend != 0);
               if (!who) break;
@@ -875,6 +1269,19 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           for (int k = 0; k < 4; ++k)
             if (k < b) dst[k] = w[k];
         }
+        if (dpend[0] | dpend[1]) {
+          __threadfence();                               // the words are stored before the fixer reads them
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t pm = dpend[hh], idx = dbase[hh];
+            while (pm) {
+              const int cc = __ffs(pm) - 1;
+              pm &= pm - 1u;
+              ring_publish(qring, idx++, (static_cast<uint32_t>(j) << 7) | static_cast<uint32_t>(row),
+                           (kEntryCode << 16) | static_cast<uint32_t>(ch0 + 16 * hh + cc));
+            }
+          }
+        }
       }
       if (h == 0 && rec) *(reinterpret_cast<unsigned short*>(rec + a.lay.off_norm) + slot) = __half_as_ushort(n16h);
       if (sk) {
@@ -903,12 +1310,18 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           }
           uint32_t word = ~neg;
           if (!sgn) amin = INFINITY;
-          if (__any_sync(0xffffffffu, amin <= guard)) {
-            uint32_t pend = 0;
-            if (amin <= guard) {
+          // rare: signs of |z| within the guard go to the fixer after the word is
+          // stored, or (no room in its ring) are decided here by the warp
+          uint32_t pend = 0u, dp = 0u, db = 0u;
+          if (amin <= guard) {
 #pragma unroll
-              for (int k = 0; k < 32; ++k) pend |= (fabsf(v[k]) <= guard ? 1u : 0u) << k;
+            for (int k = 0; k < 32; ++k) pend |= (fabsf(v[k]) <= guard ? 1u : 0u) << k;
+            if (ring_reserve(qring, __popc(pend), db)) {
+              dp = pend;
+              pend = 0u;
             }
+          }
+          if (__any_sync(0xffffffffu, pend != 0u)) {
             for (;;) {
               const uint32_t who = __ballot_sync(0xffffffffu, pend != 0);
               if (!who) break;
@@ -928,12 +1341,28 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             }
           }
           if (sgn) sgn[c] = word;
+          if (dp) {
+            __threadfence();
+            while (dp) {
+              const int kk = __ffs(dp) - 1;
+              dp &= dp - 1u;
+              ring_publish(qring, db++, (static_cast<uint32_t>(j) << 7) | static_cast<uint32_t>(row),
+                           (kEntrySign << 16) | static_cast<uint32_t>(32 * c + kk));
+            }
+          }
         }
         if (h == 0 && rec)
           *(reinterpret_cast<unsigned short*>(rec + a.lay.off_rnorm) + slot) =
               __half_as_ushort(__float2half_rn(rho * n16f * kInvSqrtDHi));
       }
       tc_fence_before();
+    }
+    // every row of this group is stored and every entry published: tell the fixer
+    named_sync(gbar, 256);
+    if (q == 0 && h == 0 && lane == 0) {
+      st_vol(qring + kQProg + s, 0x7FFFFFFFu);
+      __threadfence_block();
+      atomicAdd(qring + kQDone, 1u);
     }
     if (failed) atomicOr(ka.tab.err, kErrTimeout);
   }
@@ -1016,6 +1445,7 @@ bool launch_quantize_pipe(const QuantizeArgs& k, const QuantizeArgs& v, cudaStre
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int cap = any.max_ctas > 0 && any.max_ctas < sms ? any.max_ctas : sms;
   const int grid = static_cast<int>(tiles < cap ? tiles : cap);
+  if ((tiles + grid - 1) / grid >= (1LL << 24)) return false;   // ring entries hold a CTA's tile index in 25 bits
   const QuantizeArgs& kk = k.x ? k : v;
   const QuantizeArgs& vv = v.x ? v : k;
   quantize_pipe_kernel<<<grid, kThreadsP, kSmemP, s>>>(kk, vv, mk, mv, pp);

@@ -142,6 +142,63 @@ def test_zero_and_boundary_vectors():
             assert res["signs_mismatch"] == 0, res
 
 
+def _near_decision_vectors(p, n_code, n_sign, seed):
+    """bf16-valued vectors whose exact quantization has a code within 3e-6 of a boundary (u units) or a sign bit
+    with |z| < 1.5e-5 ||r|| -- decisions the fast tensor-core arithmetic cannot take for certain -- found by
+    searching seeded N(0,1) draws with the oracle."""
+    rng = np.random.default_rng(seed)
+    near_code, near_sign = [], []
+    for _ in range(200):
+        if len(near_code) >= n_code and len(near_sign) >= n_sign:
+            break
+        X = wl.bf16_round(rng.standard_normal((8192, 128)).astype(np.float32)).astype(np.float64)
+        q = oracle.quantize_vectors(p, X, "k")
+        t = p.books[3].boundaries
+        dist = np.min(np.abs(q["u"][:, :, None] - t[None, None, :]), axis=(1, 2))
+        zmin = np.min(np.abs(q["z"]), axis=1) / q["rho"]
+        near_code += list(X[dist < 3e-6])
+        near_sign += list(X[(zmin < 1.5e-5) & (dist >= 3e-6)])
+    assert len(near_code) >= n_code and len(near_sign) >= n_sign
+    return np.array(near_code[:n_code]), np.array(near_sign[:n_sign])
+
+
+def test_bf16_decisions_near_boundaries_are_exact():
+    """The bf16 tensor-core path hands every decision inside its guard (code near a boundary, sign near zero) to
+    exact double-float arithmetic.  Two tiles of vectors with a code near a boundary and two with a sign near
+    zero give hundreds of such decisions at once -- more than the kernel's queue for them holds, so some are
+    taken where they arise -- and every record still equals the oracle's, inside the 1e-6 bands too."""
+    w = wl.Workload("t", "quantize", 1, 1, 1, 1024, k_bits=(3, 3), v_bits=(3, 3), seed=5)
+    p = th.params_for(w)
+    near_code, near_sign = _near_decision_vectors(p, 256, 256, seed=17)
+    rest = wl.bf16_round(np.random.default_rng(18).standard_normal((512, 128)).astype(np.float32))
+    X = np.concatenate([near_code, near_sign, rest]).astype(np.float32)
+    T = X.shape[0]
+    K = X.reshape(1, T, 1, 128)
+    bt = np.arange(T // 16, dtype=np.int32)[None, :]
+    ctx = ctx_for(w)
+    try:
+        tq.tq_refine_counters(ctx, reset=True)
+        kc, vc = alloc_caches(ctx, 1, T // 16)
+        gpu_quantize(ctx, K, K, "bf16", [0], bt, T // 16, kc, vc)
+        assert tq.tq_check_device_status(ctx) == 0
+        refined = tq.tq_refine_counters(ctx)
+        got = {"k": kc.cpu().numpy(), "v": vc.cpu().numpy()}
+    finally:
+        tq.tq_destroy(ctx)
+    assert refined[0] >= 2 * 256 and refined[1] >= 256, refined
+    pages, slots, heads = seq_locations(bt, 0, np.arange(T), 1)
+    for kind in ("k", "v"):
+        q = oracle.quantize_vectors(p, X.astype(np.float64), kind)
+        ex = oracle.quantize_exclusions(p, q, kind)
+        res = th.compare_records(p, kind, got[kind], q, ex, pages, slots, heads, 1)
+        assert res["codes_mismatch"] == 0 and res["codes_mismatch_excluded"] == 0 and res["norm_mismatch"] == 0, res
+        if kind == "k":
+            raw = oracle.read_paged(p, "k", got["k"], pages, slots, heads, 1)
+            rec = oracle.unpack_k_records(p, raw)
+            assert np.array_equal(rec["signs"], q["signs"])            # every sign bit, inside the band too
+            assert res["rnorm_ulp_max"] <= 1, res
+
+
 def test_out_of_range_pages_are_skipped_and_flagged():
     w = wl.Workload("t", "quantize", 2, 1, 1, 20, seed=3)
     rng = np.random.default_rng(3)
