@@ -523,7 +523,7 @@ def search_measure(torch, tq, stream, steps, warmup, peak, peak_kind):
     del X
     q_h = torch.randn(SEARCH_NQ, 128, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).pin_memory()
     q = q_h.to(dev)
-    ws_n = tq.tq_search_workspace_size(ctx, SEARCH_NQ, SEARCH_N)
+    ws_n = tq.tq_search_workspace_size(ctx, SEARCH_NQ, SEARCH_N, SEARCH_K)
     ws = torch.empty(ws_n, dtype=torch.uint8, device=dev)
     ts = torch.empty(SEARCH_NQ, SEARCH_K, device=dev)
     ti = torch.empty(SEARCH_NQ, SEARCH_K, dtype=torch.int32, device=dev)
@@ -549,13 +549,15 @@ def search_measure(torch, tq, stream, steps, warmup, peak, peak_kind):
     return {
         "metric": "inner-product search: quantized database GB/s per query batch",
         "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms, 4), "steps": steps, "warmup": warmup,
-        "higher_is_better": True, "dtype": "packed 3-bit codes + QJL signs, fp32 scores",
+        "higher_is_better": True,
+        "dtype": "packed 3-bit codes + QJL signs; fp16 tensor-core products (tcgen05), fp32 accumulation",
         "data": "synthetic (seeded N(0,1), channels 0-3 x10)",
         "config": {"workload": f"search: {SEARCH_N} database vectors (one KV head, K 3-bit + QJL m=128), "
                                f"{SEARCH_NQ} bf16 queries, top {SEARCH_K}",
                    "database_bytes": db_bytes, "scores_per_s": round(SEARCH_NQ * SEARCH_N / (ms * 1e-3), 1),
                    "l2": l2_note},
-        "roofline": {"kernel": "tq_search (qprep, CUDA-core scores, top k)", "bound": "hbm",
+        "roofline": {"kernel": "tq_search: qprep, search_tc_kernel (scores + per-thread top 16), merge; "
+                               "timed as the whole call", "bound": "hbm",
                      "achieved": round(value, 2), "peak": peak, "unit": "GB/s", "frac": round(value / peak, 5),
                      "peak_source": peak_kind, "algorithmic_bytes_per_launch": db_bytes, "traffic": None},
         "e2e": {"value": round(db_bytes / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",

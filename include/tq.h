@@ -313,18 +313,35 @@ const char* tq_last_cuda_error(void);
  * block_table[t / 16], slot t % 16 (device int32 [ceil(n_db/16)]); num_pages
  * bounds the page ids (an id outside [0, num_pages) is skipped, its score is
  * -inf and the device error word is set).  q: device [nq][d] in `dtype`.
- * top_scores (fp32) and top_index (int32): device [nq][k_top].  Requires
- * 1 <= k_top <= min(n_db, 1024); workspace (device, 16-byte aligned) of
- * tq_search_workspace_size bytes holds the q~/u rows and the [nq][n_db]
- * scores (fp32, in the workspace after them).  Stream-ordered; no allocation.
- * Errors: null pointers, k_top out of range, n_db > 16 num_pages, misaligned
- * buffers -> TQ_ERR_INVALID_ARG; a small workspace -> TQ_ERR_WORKSPACE;
- * nq > 524280 (65535 x 8) -> TQ_ERR_UNSUPPORTED.  All checked before any launch. */
-tq_status tq_search_workspace_size(const tq_ctx* ctx, int nq, int n_db, size_t* bytes);
+ * top_scores (fp32) and top_index (int32): device [nq][k_top].
+ *
+ * Two paths, chosen from the configuration and k_top:
+ *  - tensor cores (d = m = 128, channel split 64, key groups of 2-4 bits,
+ *    k_top <= 16): 64 queries at a time, a tile of 128 vectors' codes turned
+ *    into fp16 centroids and sign operands in shared memory and multiplied on
+ *    tcgen05 (the decode's fp16 operands: scores within about 1e-3 of the
+ *    query's largest |score|), the best 16 per query kept per CTA thread and
+ *    merged; no score array is written;
+ *  - CUDA cores (every other case, k_top <= 1024): fp32 scores into the
+ *    workspace, then a radix-select top k.
+ * Workspace (device, 16-byte aligned): tq_search_workspace_size(ctx, nq,
+ * n_db, k_top) bytes (k_top = 0: the size tq_search_scores needs).  Stream-
+ * ordered; no allocation.  Errors: null pointers, k_top out of range,
+ * n_db > 16 num_pages, misaligned buffers -> TQ_ERR_INVALID_ARG; a small
+ * workspace -> TQ_ERR_WORKSPACE; d != 128 or nq > 524280 ->
+ * TQ_ERR_UNSUPPORTED.  All checked before any launch. */
+tq_status tq_search_workspace_size(const tq_ctx* ctx, int nq, int n_db, int k_top, size_t* bytes);
 tq_status tq_search(const tq_ctx* ctx, const void* q, tq_dtype dtype, int nq, const void* k_cache,
                     const int32_t* block_table, int num_pages, int n_db, int k_top,
                     float* top_scores, int32_t* top_index, void* workspace, size_t workspace_bytes,
                     void* stream);
+/* Every score of the same search, scores: device fp32 [nq][n_db], by the
+ * arithmetic of the path tq_search takes with this k_top (so tq_search's
+ * result is the stable ranking of these scores).  Workspace: the size
+ * tq_search_workspace_size gives for k_top = 0.  Same errors as tq_search. */
+tq_status tq_search_scores(const tq_ctx* ctx, const void* q, tq_dtype dtype, int nq, const void* k_cache,
+                           const int32_t* block_table, int num_pages, int n_db, int k_top, float* scores,
+                           void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -797,25 +797,18 @@ extern "C" const char* tq_status_string(tq_status s) {
 // ---------------------------------------------------------------------------
 // inner-product search
 // ---------------------------------------------------------------------------
-extern "C" tq_status tq_search_workspace_size(const tq_ctx* ctx, int nq, int n_db, size_t* bytes) {
-  if (!ctx || !bytes || nq < 1 || n_db < 1) return TQ_ERR_INVALID_ARG;
-  *bytes = search_ws_bytes(nq, n_db, ctx->cfg.m);
-  return TQ_OK;
+namespace {
+// Workspace of a search: the q~/u rows, then the tensor-core path's candidate
+// lists, or the CUDA-core path's [nq][n_db] scores (k_top > 0); the rows alone
+// for tq_search_scores (k_top = 0).
+size_t search_bytes(const tq_ctx* ctx, int nq, int n_db, int k_top) {
+  const size_t rows = search_qrows_bytes(nq, ctx->cfg.m);
+  if (k_top == 0) return rows + 256;
+  if (search_tc_supported(ctx->kl, ctx->cfg.m, k_top)) return rows + search_tc_cand_bytes() + 256;
+  return rows + sizeof(float) * static_cast<size_t>(nq) * n_db + 256;
 }
 
-extern "C" tq_status tq_search(const tq_ctx* ctx, const void* q, tq_dtype dtype, int nq, const void* k_cache,
-                               const int32_t* block_table, int num_pages, int n_db, int k_top,
-                               float* top_scores, int32_t* top_index, void* workspace, size_t workspace_bytes,
-                               void* stream) {
-  if (!ctx || !q || !k_cache || !block_table || !top_scores || !top_index || !workspace) return TQ_ERR_INVALID_ARG;
-  if (dtype != TQ_BF16 && dtype != TQ_F32) return TQ_ERR_INVALID_ARG;
-  if (nq < 1 || n_db < 1 || num_pages < 1 || k_top < 1 || k_top > n_db || k_top > search_max_k())
-    return TQ_ERR_INVALID_ARG;
-  if (static_cast<long long>(num_pages) * kPage < n_db) return TQ_ERR_INVALID_ARG;
-  if (nq > search_max_queries() || ctx->cfg.d != kD) return TQ_ERR_UNSUPPORTED;   // checked before any launch
-  if ((reinterpret_cast<uintptr_t>(workspace) & 15) || (reinterpret_cast<uintptr_t>(k_cache) & 15))
-    return TQ_ERR_INVALID_ARG;
-  if (workspace_bytes < search_ws_bytes(nq, n_db, ctx->cfg.m)) return TQ_ERR_WORKSPACE;
+DecodeArgs search_args(const tq_ctx* ctx, const void* q, tq_dtype dtype, int nq, void* workspace) {
   DecodeArgs a{};
   a.q = q;
   a.f32 = dtype == TQ_F32 ? 1 : 0;
@@ -830,6 +823,60 @@ extern "C" tq_status tq_search(const tq_ctx* ctx, const void* q, tq_dtype dtype,
   a.qprep = static_cast<float*>(workspace);
   a.qfrag = nullptr;
   a.sched = nullptr;
-  return cuda_status(launch_search(a, static_cast<const uint8_t*>(k_cache), block_table, num_pages, n_db, k_top,
-                                   top_scores, top_index, static_cast<cudaStream_t>(stream)));
+  return a;
+}
+
+// Checks shared by tq_search and tq_search_scores, before any launch.
+tq_status search_check(const tq_ctx* ctx, const void* q, tq_dtype dtype, int nq, const void* k_cache,
+                       const int32_t* block_table, int num_pages, int n_db, const void* workspace) {
+  if (!ctx || !q || !k_cache || !block_table || !workspace) return TQ_ERR_INVALID_ARG;
+  if (dtype != TQ_BF16 && dtype != TQ_F32) return TQ_ERR_INVALID_ARG;
+  if (nq < 1 || n_db < 1 || num_pages < 1) return TQ_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_pages) * kPage < n_db) return TQ_ERR_INVALID_ARG;
+  if (nq > search_max_queries() || ctx->cfg.d != kD) return TQ_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 15) || (reinterpret_cast<uintptr_t>(k_cache) & 15))
+    return TQ_ERR_INVALID_ARG;
+  return TQ_OK;
+}
+}  // namespace
+
+extern "C" tq_status tq_search_workspace_size(const tq_ctx* ctx, int nq, int n_db, int k_top, size_t* bytes) {
+  if (!ctx || !bytes || nq < 1 || n_db < 1 || k_top < 0) return TQ_ERR_INVALID_ARG;
+  *bytes = search_bytes(ctx, nq, n_db, k_top);
+  return TQ_OK;
+}
+
+extern "C" tq_status tq_search(const tq_ctx* ctx, const void* q, tq_dtype dtype, int nq, const void* k_cache,
+                               const int32_t* block_table, int num_pages, int n_db, int k_top,
+                               float* top_scores, int32_t* top_index, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  if (!top_scores || !top_index) return TQ_ERR_INVALID_ARG;
+  if (k_top < 1 || k_top > n_db || k_top > search_max_k()) return TQ_ERR_INVALID_ARG;
+  tq_status st = search_check(ctx, q, dtype, nq, k_cache, block_table, num_pages, n_db, workspace);
+  if (st != TQ_OK) return st;
+  if (workspace_bytes < search_bytes(ctx, nq, n_db, k_top)) return TQ_ERR_WORKSPACE;
+  DecodeArgs a = search_args(ctx, q, dtype, nq, workspace);
+  char* extra = static_cast<char*>(workspace) + search_qrows_bytes(nq, ctx->cfg.m);
+  const auto* kc = static_cast<const uint8_t*>(k_cache);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (search_tc_supported(ctx->kl, ctx->cfg.m, k_top))
+    return cuda_status(launch_search_tc(a, kc, block_table, num_pages, n_db, k_top, top_scores, top_index, nullptr,
+                                        extra, s));
+  return cuda_status(launch_search(a, kc, block_table, num_pages, n_db, k_top, top_scores, top_index,
+                                   reinterpret_cast<float*>(extra), s));
+}
+
+extern "C" tq_status tq_search_scores(const tq_ctx* ctx, const void* q, tq_dtype dtype, int nq, const void* k_cache,
+                                      const int32_t* block_table, int num_pages, int n_db, int k_top, float* scores,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (!scores || k_top < 1 || k_top > n_db || k_top > search_max_k()) return TQ_ERR_INVALID_ARG;
+  tq_status st = search_check(ctx, q, dtype, nq, k_cache, block_table, num_pages, n_db, workspace);
+  if (st != TQ_OK) return st;
+  if (workspace_bytes < search_bytes(ctx, nq, n_db, 0)) return TQ_ERR_WORKSPACE;
+  DecodeArgs a = search_args(ctx, q, dtype, nq, workspace);
+  const auto* kc = static_cast<const uint8_t*>(k_cache);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (search_tc_supported(ctx->kl, ctx->cfg.m, k_top))
+    return cuda_status(launch_search_tc(a, kc, block_table, num_pages, n_db, 1, nullptr, nullptr, scores, nullptr, s));
+  return cuda_status(launch_search(a, kc, block_table, num_pages, n_db, 1, nullptr, nullptr, scores, s));
 }

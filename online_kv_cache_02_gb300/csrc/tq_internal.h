@@ -200,14 +200,22 @@ cudaError_t launch_decode_generic(const DecodeArgs& a, int d, int stages, cudaSt
 int lut_decode_ctas(const KindLayout& kl, const KindLayout& vl, int m, int G);
 long long lut_cost(long long items, int ctas, int warps, long long chunk_cost);
 int lut_warps_for(long long items, int ctas);
-// Inner-product search (tq_search.cu): workspace bytes (q~/u rows, then the
-// [nq][n_db] scores), the launches (qprep of qa, scores, top k) and the
-// largest k supported.
-size_t search_ws_bytes(int nq, int n_db, int m);
+// Inner-product search on CUDA cores (tq_search.cu): bytes of the q~/u rows;
+// the launches (qprep of qa, scores into `scores`, then the top k unless
+// top_s is null) and the largest k supported.
+size_t search_qrows_bytes(int nq, int m);
 cudaError_t launch_search(const DecodeArgs& qa, const uint8_t* kc, const int32_t* bt, int num_pages, int n_db,
-                          int k, float* top_s, int32_t* top_i, cudaStream_t st);
+                          int k, float* top_s, int32_t* top_i, float* scores, cudaStream_t st);
 int search_max_k();
 int search_max_queries();
+// Inner-product search on the tensor cores (tq_search_tc.cu): whether the
+// configuration and k take that path, the bytes of its per-CTA candidate
+// lists, and the launches (qprep of qa, the scoring kernel per 64 queries,
+// then the merge into the top k; with `scores` set, every score instead).
+bool search_tc_supported(const KindLayout& kl, int m, int k_top);
+size_t search_tc_cand_bytes();
+cudaError_t launch_search_tc(const DecodeArgs& qa, const uint8_t* kc, const int32_t* bt, int num_pages, int n_db,
+                             int k, float* top_s, int32_t* top_i, float* scores, void* cand, cudaStream_t st);
 bool launch_partials_lut(const DecodeArgs& a, cudaStream_t s, cudaError_t* err);
 
 }  // namespace tq

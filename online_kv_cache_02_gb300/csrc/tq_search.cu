@@ -256,13 +256,12 @@ __global__ void __launch_bounds__(kTThreads) search_topk_kernel(const float* sco
 
 }  // namespace
 
-size_t search_ws_bytes(int nq, int n_db, int m) {
-  const size_t a = (sizeof(float) * static_cast<size_t>(nq) * (kD + m) + 255) & ~static_cast<size_t>(255);
-  return a + sizeof(float) * static_cast<size_t>(nq) * n_db + 256;
+size_t search_qrows_bytes(int nq, int m) {
+  return (sizeof(float) * static_cast<size_t>(nq) * (kD + m) + 255) & ~static_cast<size_t>(255);
 }
 
 cudaError_t launch_search(const DecodeArgs& qa, const uint8_t* kc, const int32_t* bt, int num_pages, int n_db,
-                          int k, float* top_s, int32_t* top_i, cudaStream_t st) {
+                          int k, float* top_s, int32_t* top_i, float* scores, cudaStream_t st) {
   cudaError_t e = launch_decode(qa, TQ_STAGE_QPREP, st);
   if (e != cudaSuccess) return e;
   SearchArgs s;
@@ -275,13 +274,11 @@ cudaError_t launch_search(const DecodeArgs& qa, const uint8_t* kc, const int32_t
   s.bt = bt;
   s.kl = qa.kl;
   s.err = qa.tab.err;
-  s.scores = reinterpret_cast<float*>(reinterpret_cast<char*>(qa.qprep) +
-                                      ((sizeof(float) * static_cast<size_t>(s.nq) * (kD + s.m) + 255) &
-                                       ~static_cast<size_t>(255)));
+  s.scores = scores;
   const dim3 grid(static_cast<unsigned>((n_db + kSChunk - 1) / kSChunk), static_cast<unsigned>((s.nq + kSG - 1) / kSG));
   search_score_kernel<<<grid, kSThreads, 0, st>>>(s);
   e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || !top_s) return e;
   search_topk_kernel<<<s.nq, kTThreads, 0, st>>>(s.scores, n_db, k, top_s, top_i);
   return cudaGetLastError();
 }

@@ -64,8 +64,9 @@ EXPORTS = {
     "tq_host_qjl": ([_I, _I, _U64, _P], _S),
     "tq_host_codebook": ([_I, _P, _P], _S),
     "tq_host_codebook_ex": ([_I, _I, _I, _P, _P], _S),
-    "tq_search_workspace_size": ([_P, _I, _I, ctypes.POINTER(ctypes.c_size_t)], _S),
+    "tq_search_workspace_size": ([_P, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)], _S),
     "tq_search": ([_P, _P, _I, _I, _P, _P, _I, _I, _I, _P, _P, _P, ctypes.c_size_t, _P], _S),
+    "tq_search_scores": ([_P, _P, _I, _I, _P, _P, _I, _I, _I, _P, _P, ctypes.c_size_t, _P], _S),
     "tq_quantize": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P], _S),
     "tq_workspace_size": ([_P, _I, _I, _I, _I, ctypes.POINTER(_SZ)], _S),
     "tq_decode_chunk": ([_P, _I, _I, _I, ctypes.c_longlong, _I, _I, ctypes.POINTER(_I)], _S),
@@ -297,9 +298,10 @@ def tq_causal_attention(ctx, q, dtype, batch, n_new, num_q_heads, num_kv_heads, 
         ctypes.c_float(softmax_scale), _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
-def tq_search_workspace_size(ctx, nq, n_db):
+def tq_search_workspace_size(ctx, nq, n_db, k_top):
+    """Workspace bytes of tq_search with this k_top (0: of tq_search_scores)."""
     n = ctypes.c_size_t()
-    _check("tq_search_workspace_size", _lib.tq_search_workspace_size(ctx, nq, n_db, ctypes.byref(n)))
+    _check("tq_search_workspace_size", _lib.tq_search_workspace_size(ctx, nq, n_db, k_top, ctypes.byref(n)))
     return n.value
 
 
@@ -309,3 +311,11 @@ def tq_search(ctx, q, dtype, nq, k_cache, block_table, num_pages, n_db, k_top, t
     _check("tq_search", _lib.tq_search(ctx, _ptr(q), dtype, nq, _ptr(k_cache), _ptr(block_table), num_pages, n_db,
                                        k_top, _ptr(top_scores), _ptr(top_index), _ptr(workspace), workspace_bytes,
                                        _stream(stream)))
+
+
+def tq_search_scores(ctx, q, dtype, nq, k_cache, block_table, num_pages, n_db, k_top, scores, workspace,
+                     workspace_bytes, stream=None):
+    """Every score [nq][n_db] of the search, by the arithmetic tq_search uses for this k_top (see tq.h)."""
+    _check("tq_search_scores", _lib.tq_search_scores(ctx, _ptr(q), dtype, nq, _ptr(k_cache), _ptr(block_table),
+                                                     num_pages, n_db, k_top, _ptr(scores), _ptr(workspace),
+                                                     workspace_bytes, _stream(stream)))

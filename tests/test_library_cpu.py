@@ -113,7 +113,8 @@ def test_null_context_is_rejected(tq):
     assert st("tq_cache_layout", None, 8, ctypes.byref(n), None) == tq.TQ_ERR_INVALID_ARG
     c = ctypes.c_int()
     assert st("tq_decode_chunk", None, 16, 32, 8, 16 * 1000, 1000, 0, ctypes.byref(c)) == tq.TQ_ERR_INVALID_ARG
-    assert st("tq_search_workspace_size", None, 4, 100, ctypes.byref(n)) == tq.TQ_ERR_INVALID_ARG
+    assert st("tq_search_workspace_size", None, 4, 100, 10, ctypes.byref(n)) == tq.TQ_ERR_INVALID_ARG
+    assert st("tq_search_scores", None, 1, 0, 4, 1, 1, 8, 100, 10, 1, 1, 1 << 20, None) == tq.TQ_ERR_INVALID_ARG
     assert st("tq_search", None, 1, 0, 4, 1, 1, 8, 100, 10, 1, 1, 1, 1 << 20, None) == tq.TQ_ERR_INVALID_ARG
 
 
