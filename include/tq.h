@@ -170,6 +170,11 @@ tq_status tq_decode_chunk(const tq_ctx* ctx, int batch, int num_q_heads, int num
  * out = Pi^T sum_t w_t (vnorm_t/sqrt(d)) c_v[code_t], fp32.  The context is
  * split into chunks of chunk_tokens (a multiple of 16; 0 picks one) merged
  * with a log-sum-exp reduction.  A sequence of length 0 yields zeros.
+ * Accuracy: max_j |out_j - exact_j| / max_j |exact_j| <= 2e-3 against the
+ * same scores in fp64.  With d = 128 and |softmax_scale| <= 1/sqrt(d) the
+ * tensor-core kernels run (fp16 q~, u and centroids, fp32 accumulation: their
+ * logit error grows with the scale); a larger |softmax_scale| runs the fp32
+ * CUDA-core kernels (slower), which keep the bound at any scale.
  * workspace (device) of at least tq_workspace_size() bytes. */
 tq_status tq_decode_attention(const tq_ctx* ctx, const void* q, tq_dtype dtype,
                               int batch, int num_q_heads, int num_kv_heads,
@@ -268,8 +273,9 @@ tq_status tq_append_decode_ex(const tq_ctx* ctx, const void* k_new, const void* 
  * fp32): [batch][n_new][Hq][d].  start_pos[b] + n_new <= max_seq_len.  The
  * context is split into chunks of chunk_tokens (0 picks one) merged per query.
  * Runs the bit-width combinations of the persistent decode kernel (d = 128,
- * m = 128, split 64; K/V bits 3/3, 4-3/4-3, 3-2/3-2, 4/4, 2/2, 4/2), else
- * TQ_ERR_UNSUPPORTED; query heads per KV head <= 8.  workspace (device) of
+ * m = 128, split 64; K/V bits 3/3, 4-3/4-3, 3-2/3-2, 4/4, 2/2, 4/2) with
+ * |softmax_scale| <= 1/sqrt(d) (the 2e-3 bar of tq_decode_attention; its
+ * query is fp16 hi + lo), else TQ_ERR_UNSUPPORTED; query heads per KV head <= 8.  workspace (device) of
  * tq_causal_workspace_size bytes; stream-ordered, no allocation.  Errors as
  * tq_decode_attention. */
 tq_status tq_causal_workspace_size(const tq_ctx* ctx, int batch, int n_new, int num_q_heads, int max_seq_len,

@@ -535,6 +535,13 @@ struct FusedStep {
   cudaEvent_t partials_begin, partials_end;
 };
 
+// The tensor-core decode multiplies fp16 operands (q~, u, centroids): its logit
+// error grows with |softmax_scale|, and the 2e-3 output bar holds up to
+// 1/sqrt(d).  Larger scales run the fp32 CUDA-core kernels.
+bool precise_scale(const tq_ctx* ctx, float softmax_scale) {
+  return std::fabs(static_cast<double>(softmax_scale)) > (1.0 + 1e-6) / std::sqrt(static_cast<double>(ctx->cfg.d));
+}
+
 tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batch, int Hq, int H,
                       const int32_t* seq_lens, int len_add, int max_seq_len, const int32_t* block_table, int maxp,
                       int num_pages, const void* k_cache, const void* v_cache, int chunk_tokens,
@@ -550,7 +557,8 @@ tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batc
   if (batch == 0) return TQ_OK;
   if (!q || !seq_lens || !block_table || !k_cache || !v_cache || !out || !workspace)
     return TQ_ERR_INVALID_ARG;
-  int lut_ctas = ctx->cfg.d == kD ? lut_decode_ctas(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H) : 0;
+  const bool generic = ctx->cfg.d != kD || precise_scale(ctx, softmax_scale);
+  int lut_ctas = generic ? 0 : lut_decode_ctas(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H);
   if (fused && lut_ctas > 0) lut_ctas -= fused->reserve;
   int chunk = chunk_tokens              ? chunk_tokens
               : lut_ctas > 0            ? pick_chunk_warps(batch * H, max_seq_len, lut_ctas)
@@ -593,7 +601,7 @@ tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batc
   a.sched = reinterpret_cast<int*>(w + o_frag + align256(sizeof(uint32_t) * static_cast<size_t>(batch) * Hq * kQFragWords));
   a.out = out;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (d != kD) return cuda_status(launch_decode_generic(a, d, stages, st));
+  if (generic) return cuda_status(launch_decode_generic(a, d, stages, st));
   if (!fused) return cuda_status(launch_decode(a, stages, st));
   a.new_token = 1;                       // len_add is 0 here: the partials cover [0, seq_lens[b])
   a.max_ctas = sm_count() - fused->reserve;
@@ -646,7 +654,7 @@ extern "C" tq_status tq_append_decode_ex(const tq_ctx* ctx, const void* k_new, c
   if (!k_cache || !v_cache || maxp < 1 || num_pages < 1) return TQ_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15) return TQ_ERR_INVALID_ARG;
   if (static_cast<long long>(batch) * H > (1LL << 31) - 1) return TQ_ERR_INVALID_ARG;
-  if (ctx->cfg.d != kD) {                 // other head dimensions: append, then decode over L + 1
+  if (ctx->cfg.d != kD || precise_scale(ctx, softmax_scale)) {   // CUDA-core decode: append, then decode L + 1
     st = quantize_impl(ctx, k_new, v_new, dtype, batch, 1, H, seq_lens, block_table, maxp, num_pages, k_cache, v_cache,
                        stream, 0);
     if (st != TQ_OK) return st;
@@ -706,7 +714,7 @@ extern "C" tq_status tq_causal_attention(const tq_ctx* ctx, const void* q, tq_dt
     return TQ_ERR_INVALID_ARG;
   if (dtype != TQ_BF16 && dtype != TQ_F32) return TQ_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return TQ_ERR_INVALID_ARG;
-  if (Hq / H > kMaxGroup || ctx->cfg.d != kD) return TQ_ERR_UNSUPPORTED;
+  if (Hq / H > kMaxGroup || ctx->cfg.d != kD || precise_scale(ctx, softmax_scale)) return TQ_ERR_UNSUPPORTED;
   const int lut_ctas = lut_decode_ctas(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H);
   if (lut_ctas <= 0) return TQ_ERR_UNSUPPORTED;        // the bit widths the persistent kernel takes
   if (batch == 0) return TQ_OK;

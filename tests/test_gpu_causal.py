@@ -92,6 +92,20 @@ def test_causal_one_token_equals_decode():
     assert th.rel_err(got[:, 0].reshape(-1, 128), dec.reshape(-1, 128)).max() <= th.ATT_TOL
 
 
+def test_causal_rejects_scales_above_the_bar():
+    """Causal attention runs on the tensor cores only: |softmax_scale| above 1/sqrt(d) is rejected before any
+    launch (the pointers below are never read)."""
+    w = wl.Workload("t", "decode", 1, 4, 1, 0, k_bits=(3, 3), v_bits=(3, 3), seed=1)
+    ctx = ctx_for(w)
+    try:
+        for scale in (0.3, -0.1):
+            st = tq.raw_status("tq_causal_attention", ctx, 16, tq.TQ_BF16, 1, 4, 4, 1, 16, 64, 16, 4, 4, 16, 16, 0,
+                               scale, 16, 16, 1 << 30, None)
+            assert st == tq.TQ_ERR_UNSUPPORTED
+    finally:
+        tq.tq_destroy(ctx)
+
+
 def test_causal_unsupported_widths_are_rejected():
     w = wl.Workload("t", "decode", 1, 4, 1, 0, k_bits=(1, 1), v_bits=(1, 1), seed=1)
     ctx = ctx_for(w)

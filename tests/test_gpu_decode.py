@@ -63,11 +63,10 @@ def _check(w, lens, Hq, H, chunk=0, scale=None, seed=0, qdtype=None, kv=None, Q=
     ref = oracle.decode_attention(p, Q.astype(np.float64), lens, bt, kc, vc, H, scale=scale)
     err = th.rel_err(got, ref)
     assert np.all(np.isfinite(got))
-    # The bar is 2e-3 at the standard scale 1/sqrt(d).  The tensor-core path rounds q~ and the
-    # centroids to fp16 (relative 2^-12 each), so its logit error grows with the scale: above
-    # 1/sqrt(d) the bar is 2e-3 * scale * sqrt(d).
+    # The bar is 2e-3 at every scale: above 1/sqrt(d) the library runs its fp32 kernels (the
+    # tensor-core path's fp16 operands would carry a logit error that grows with the scale).
     if tol is None:
-        tol = th.ATT_TOL * max(1.0, scale * np.sqrt(128))
+        tol = th.ATT_TOL
     assert err.max() <= tol, (err.max(), np.unravel_index(err.argmax(), err.shape))
     return err.max()
 
@@ -154,6 +153,13 @@ def test_decode_fp32_queries_and_scale():
     _check(w, [257, 90], Hq=4, H=2, chunk=32, scale=0.0, seed=5)    # uniform weights
 
 
+@pytest.mark.parametrize("scale", [1.0, -0.25, 0.09])
+def test_decode_large_scales_keep_the_bar(scale):
+    """|scale| above 1/sqrt(d) (0.0884) runs the fp32 kernels: the attention bar holds for sharp softmaxes too,
+    for both bit layouts the tensor-core path would take."""
+    _check(BASE.scaled(dtype="bf16", k_bits=(4, 3), v_bits=(4, 3)), [300, 17], Hq=8, H=2, scale=scale, seed=6)
+
+
 def test_decode_config_c1():
     """Single head, N=1024 fp32 keys (channels 0-3 x10) and values, 8 fp32 queries, 3-bit + QJL."""
     w = wl.WORKLOADS["c1"]
@@ -208,9 +214,12 @@ def test_workspace_too_small_is_rejected():
         tq.tq_destroy(ctx)
 
 
-def test_append_decode_equals_separate_calls():
+@pytest.mark.parametrize("scale", [None, 0.5])
+def test_append_decode_equals_separate_calls(scale):
+    """The fused step equals quantize + decode over L + 1 (scale 0.5: both on the fp32 kernels)."""
     import torch
     from .gpu_common import gpu_quantize
+    scale = th.scale_for() if scale is None else scale
     w = BASE.scaled(k_bits=(4, 3), v_bits=(4, 3), dtype="bf16")
     rng = np.random.default_rng(21)
     B, H, Hq = 3, 2, 8
@@ -239,11 +248,11 @@ def test_append_decode_equals_separate_calls():
             if fused:
                 tq.tq_append_decode(ctx, to_dev(kn).to(torch.bfloat16), to_dev(vn).to(torch.bfloat16), qd, tq.TQ_BF16,
                                     B, Hq, H, to_dev(lens), max_len, to_dev(bt), pps, num_pages, kc, vc, 16,
-                                    th.scale_for(), out, ws, n)
+                                    scale, out, ws, n)
             else:
                 gpu_quantize(ctx, kn, vn, "bf16", lens, bt, num_pages, kc, vc)
                 tq.tq_decode_attention(ctx, qd, tq.TQ_BF16, B, Hq, H, to_dev(lens + 1), max_len, to_dev(bt), pps,
-                                       num_pages, kc, vc, 16, th.scale_for(), out, ws, n)
+                                       num_pages, kc, vc, 16, scale, out, ws, n)
             torch.cuda.synchronize()
             outs.append(out.cpu().numpy())
             caches.append((kc.cpu().numpy(), vc.cpu().numpy()))
