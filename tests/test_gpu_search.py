@@ -166,6 +166,32 @@ def test_search_bad_page_and_arguments():
         tq.tq_destroy(ctx)
 
 
+@pytest.mark.parametrize("k,bad_pages", [(8, (0, 2)), (40, (0, 2)), (16, (0, 1, 2))])
+def test_search_bad_pages_and_too_few_finite_scores(k, bad_pages):
+    """Out-of-range page ids in a 50-vector database: their vectors score -inf and the device error word is
+    set.  When fewer than k scores are finite (k = 40 with 18 finite on the CUDA-core path, k = 16 with 2
+    finite on the tensor-core path) the rest of the answer is the -inf vectors in index order."""
+    w = wl.Workload("s", "search", 1, 1, 1, 0, k_bits=(3, 3), seed=8)
+    p, X, row, num_pages, cache = _database(w, 50, 6)
+    row = row.copy()
+    for j, pg in enumerate(bad_pages):
+        row[pg] = num_pages + 1 + j if j % 2 == 0 else -3
+    Q = wl.bf16_round(np.random.default_rng(7).standard_normal((3, 128)).astype(np.float32))
+    ctx = ctx_for(w)
+    try:
+        ts, ti, scores = _search(ctx, Q, "bf16", row, num_pages, cache, 50, k)
+        assert tq.tq_check_device_status(ctx) & 1
+    finally:
+        tq.tq_destroy(ctx)
+    bad = np.concatenate([np.arange(16 * pg, 16 * pg + 16) for pg in bad_pages])
+    finite = 50 - bad.size
+    assert np.all(np.isneginf(scores[:, bad])) and np.all(np.isfinite(np.delete(scores, bad, axis=1)))
+    assert np.array_equal(ti, np.argsort(-scores, axis=1, kind="stable")[:, :k])
+    assert np.array_equal(ts, np.take_along_axis(scores, ti, axis=1))
+    if k > finite:
+        assert np.array_equal(ti[:, finite:], np.tile(bad[:k - finite], (3, 1)))
+
+
 def test_query_count_beyond_the_grid_is_rejected_before_launch():
     """nq above 65535 x 8 queries returns TQ_ERR_UNSUPPORTED before anything runs (the pointers are never read)."""
     ctx = ctx_for(wl.WORKLOADS["c2"])
