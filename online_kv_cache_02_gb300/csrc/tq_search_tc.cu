@@ -126,6 +126,30 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
+// Explicit shared-space accesses (32-bit addresses) for the hot loops.
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float ldsf(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void stsf(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -259,7 +283,10 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
       }
       *reinterpret_cast<uint32_t*>(sm + G::LUT + e * 256 + g * 128 + l * 4) = v;
     }
-    // q~ and u rows of this launch as fp16 (zero rows past the last query)
+    // q~ and u rows of this launch as fp16 (zero rows past the last query); the
+    // query prep (the kernel before this one) wrote them: wait for it here, after
+    // the tables above were built
+    pdl_wait();
     for (int i = tid; i < kQB * 32; i += kThrS) {        // (query, 8-channel chunk) of q~ and of u
       const int qr = i >> 5, c = i & 31, which = c >> 4, ch = c & 15;
       uint32_t w[4] = {0u, 0u, 0u, 0u};
@@ -403,12 +430,12 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
       const bool valid = (mask >> (v >> 4) & 1u) && t < a.n_db;
       float fa = __int_as_float(0x7FC00000), fb = 0.0f;   // NaN factor: no score for this row
       if (valid) {
-        const unsigned char* blk = sm + L::REC + s * G::STAGE + (v >> 4) * G::KBB;   // stage s = i % S
+        const uint32_t blk = sb + L::REC + s * G::STAGE + (v >> 4) * G::KBB;   // stage s = i % S
         const int slot = v & 15;
         uint32_t w[17];
 #pragma unroll
         for (int k = 0; k < G::CBK / 8; ++k) {
-          const uint2 x = *reinterpret_cast<const uint2*>(blk + slot * G::CBK + 8 * k);
+          const uint2 x = lds64(blk + slot * G::CBK + 8 * k);
           w[2 * k] = x.x;
           w[2 * k + 1] = x.y;
         }
@@ -428,7 +455,7 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
         }
         if (QJL) {
           // sign tile row: byte c of the sign bits -> projections 8c .. 8c + 7 as (1 + c b) pairs
-          const uint4 sw = *reinterpret_cast<const uint4*>(blk + G::K_SIGNS + slot * 16);
+          const uint4 sw = lds128(blk + G::K_SIGNS + slot * 16);
           const uint32_t sws[4] = {sw.x, sw.y, sw.z, sw.w};
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
@@ -440,13 +467,14 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
             sts128(sb + L::AS + chunk_off(v, c, kTV), prmt(zl, 0x3C3C3C3Cu, 0x4948u), prmt(zl, 0x3C3C3C3Cu, 0x4B4Au),
                    prmt(zh, 0x3C3C3C3Cu, 0x4948u), prmt(zh, 0x3C3C3C3Cu, 0x4B4Au));
           }
-          fb = __half2float(reinterpret_cast<const __half*>(blk + G::K_RNORM)[slot]) * (kSqrtHalfPiS / m);
+          fb = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(blk + G::K_RNORM + 2 * slot)))) *
+               (kSqrtHalfPiS / m);
         }
-        fa = __half2float(reinterpret_cast<const __half*>(blk + G::K_NORM)[slot]) * kInvSqrtDS;
+        fa = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(blk + G::K_NORM + 2 * slot)))) * kInvSqrtDS;
       }
-      float* fac = reinterpret_cast<float*>(sm + L::FAC) + (i & 3) * 256;
-      fac[v] = fa;
-      fac[128 + v] = fb;
+      const uint32_t fac = sb + L::FAC + (i & 3) * 1024;
+      stsf(fac + 4 * v, fa);
+      stsf(fac + 512 + 4 * v, fb);
       fence_async_smem();                      // the operand rows, for the tensor cores
       __syncwarp();
       if (lane == 0) {
@@ -460,8 +488,8 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
     const int wq = warp & 3, v = 32 * wq + lane;       // tensor-memory lanes 32 wq .. : vector v
     const int tl = tid - 192;                            // 0 .. 127
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * wq) << 16);
-    float* sc = reinterpret_cast<float*>(sm + L::SC);
-    const float* su = reinterpret_cast<const float*>(sm + L::SU);
+    const uint32_t sc = sb + L::SC;
+    const uint32_t su = sb + L::SU;
     float best[kTop];
     int bidx[kTop];
 #pragma unroll
@@ -474,10 +502,12 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
       // a wait that gives up leaves this tile's results undefined (the error word
       // says so) but the loop goes on, so the named barriers below are still met
       // the shared bar of this thread's scan query, read early (an L2 round trip)
-      const unsigned gkey = a.scores ? 0u : __ldcg(a.thr + sq);
+      unsigned gkey = 0u;
+      if (!a.scores)   // volatile: issued here, not sunk to its first use
+        asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(gkey) : "l"(a.thr + sq) : "memory");
       bool ok = bar_wait(barx(L::kFacFull + (i & 3)), (i >> 2) & 1, failed);
-      const float* fac = reinterpret_cast<const float*>(sm + L::FAC) + (i & 3) * 256;
-      const float fa = fac[v], fb = fac[128 + v];
+      const uint32_t fac = sb + L::FAC + (i & 3) * 1024;
+      const float fa = ldsf(fac + 4 * v), fb = ldsf(fac + 512 + 4 * v);
       ok = bar_wait(barx(L::kTFull + slot), (i >> 1) & 1, failed) && ok;
       if (!__all_sync(0xffffffffu, ok)) failed = true;
       tc_after();
@@ -491,7 +521,7 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           const int qq = 32 * h + k;
-          const float q2 = QJL ? fmaf(2.0f / kSignC, s2[k], su[qq]) : 0.0f;
+          const float q2 = QJL ? fmaf(2.0f / kSignC, s2[k], ldsf(su + 4 * qq)) : 0.0f;
           s1[k] = has ? fmaf(fa, s1[k], fb * q2) : -INFINITY;
         }
         if (a.scores) {
@@ -503,7 +533,7 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
           }
         } else {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) sc[(32 * h + k) * kScoreRow + v + (v >= 64 ? 4 : 0)] = s1[k];
+          for (int k = 0; k < 32; ++k) stsf(sc + 4 * ((32 * h + k) * kScoreRow + v + (v >= 64 ? 4 : 0)), s1[k]);
         }
       }
       tc_before();
@@ -511,7 +541,7 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
       if (lane == 0) bar_arrive(barx(L::kTEmpty + slot));
       if (!a.scores) {
         nsync(1, 128);                                   // the tile's scores are in
-        const float* row = sc + sq * kScoreRow + 68 * sh;
+        const uint32_t row = sc + 4 * (sq * kScoreRow + 68 * sh);
         const int tb = t0 + 64 * sh;
         // a score below the largest published k-th score of this query cannot be in
         // the answer (that list's k best are candidates); equal ones still can
@@ -519,12 +549,11 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
         // pass 1 (every lane, no branches): the elements over the bar, as a bit mask
         const bool use_gt = gt > kth;
         uint32_t mlo = 0u, mhi = 0u;
-        float gmax[16];
 #pragma unroll
         for (int j = 0; j < 64; j += 4) {
-          const float4 x = *reinterpret_cast<const float4*>(row + j);
-          const float xv[4] = {x.x, x.y, x.z, x.w};
-          gmax[j >> 2] = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+          const uint4 xu = lds128(row + 4 * j);
+          const float xv[4] = {__uint_as_float(xu.x), __uint_as_float(xu.y), __uint_as_float(xu.z),
+                               __uint_as_float(xu.w)};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const uint32_t bit = (use_gt ? xv[e] >= gt : xv[e] > kth) ? 1u : 0u;
@@ -536,7 +565,14 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
         // maxima is at most this tile's k-th best (k distinct elements reach it),
         // so an element below it cannot be among the list's final k
         float bar0 = -INFINITY;
-        if (kth == -INFINITY) {
+        if (kth == -INFINITY) {                          // (rare: the first tiles) the tile again
+          float gmax[16];
+#pragma unroll
+          for (int j = 0; j < 64; j += 4) {
+            const uint4 xu = lds128(row + 4 * j);
+            gmax[j >> 2] = fmaxf(fmaxf(__uint_as_float(xu.x), __uint_as_float(xu.y)),
+                                 fmaxf(__uint_as_float(xu.z), __uint_as_float(xu.w)));
+          }
 #pragma unroll
           for (int g = 0; g < 16; ++g) {
             int ge = 0;
@@ -551,7 +587,7 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
           const int e = mlo ? __ffs(mlo) - 1 : 31 + __ffs(mhi);
           if (mlo) mlo &= mlo - 1u;
           else mhi &= mhi - 1u;
-          const float cs = row[e];
+          const float cs = ldsf(row + 4 * e);
           if (!(cs > kth && cs >= gt && cs >= bar0)) continue;   // the bar rose since pass 1
           const int ci = tb + e;
           // insert at position p = #entries >= cs (equal scores keep the earlier, lower
@@ -583,6 +619,7 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
     }
   }
   if (failed) atomicOr(a.err, kErrTimeout);
+  pdl_trigger();                                         // the merge may be launched (it waits for this grid)
   tc_before();
   __syncthreads();
   tc_after();
@@ -614,6 +651,7 @@ __global__ void __launch_bounds__(kMergeThreads) search_merge_kernel(const float
     return cand + (static_cast<long long>(l >> 1) * kTV + 2 * ql + (l & 1)) * kTop;
   };
   if (tid == 0) nbuf = 0;
+  pdl_wait();                                            // the scoring kernel's lists
   float tau = -INFINITY;
 #pragma unroll 4
   for (int l = tid; l < nl; l += kMergeThreads) {
@@ -724,13 +762,16 @@ cudaError_t launch_tc(const TcSearchArgs& base, int grid, int k, float* top_s, i
     TcSearchArgs a = base;
     a.q0 = q0;
     a.k = k;
-    if (!a.scores && (e = cudaMemsetAsync(a.thr, 0, kQB * sizeof(unsigned), st)) != cudaSuccess) return e;
-    search_tc_kernel<BH, BL, QJL><<<grid, kThrS, G::SMEM, st>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (q0 > 0 && !a.scores && (e = cudaMemsetAsync(a.thr, 0, kQB * sizeof(unsigned), st)) != cudaSuccess)
+      return e;   // (the first block's bars are cleared before the query prep)
+    if ((e = launch_pdl(search_tc_kernel<BH, BL, QJL>, dim3(grid), dim3(kThrS), static_cast<size_t>(G::SMEM), st, a)) !=
+        cudaSuccess)
+      return e;
     if (!a.scores) {
       const int nql = base.nq - q0 < kQB ? base.nq - q0 : kQB;
-      search_merge_kernel<<<nql, kMergeThreads, 0, st>>>(a.cand, grid, q0, a.n_db, k, top_s, top_i);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      if ((e = launch_pdl(search_merge_kernel, dim3(nql), dim3(kMergeThreads), size_t{0}, st,
+                          static_cast<const float2*>(a.cand), grid, q0, a.n_db, k, top_s, top_i)) != cudaSuccess)
+        return e;
     }
   }
   return cudaSuccess;
@@ -765,7 +806,12 @@ size_t search_tc_cand_bytes() {
 
 cudaError_t launch_search_tc(const DecodeArgs& qa, const uint8_t* kc, const int32_t* bt, int num_pages, int n_db,
                              int k, float* top_s, int32_t* top_i, float* scores, void* cand, cudaStream_t st) {
-  cudaError_t e = launch_decode(qa, TQ_STAGE_QPREP, st);
+  cudaError_t e = cudaSuccess;
+  if (!scores) {   // the shared per-query bars of the first 64 queries start at "none"
+    e = cudaMemsetAsync(static_cast<char*>(cand) + search_tc_cand_bytes() - 256, 0, kQB * sizeof(unsigned), st);
+    if (e != cudaSuccess) return e;
+  }
+  e = launch_decode(qa, TQ_STAGE_QPREP, st);
   if (e != cudaSuccess) return e;
   TcSearchArgs a{};
   a.qprep = qa.qprep;
