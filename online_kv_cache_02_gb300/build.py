@@ -13,7 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libtq.so")
-SOURCES = ["tq_api.cu", "tq_quantize.cu", "tq_quantize_tc.cu", "tq_quantize_pipe.cu", "tq_decode.cu", "tq_decode_lut.cu", "tq_noalloc.cu", "tq_search.cu", "tq_search_tc.cu",
+SOURCES = ["tq_api.cu", "tq_quantize.cu", "tq_quantize_tc.cu", "tq_quantize_pipe.cu", "tq_decode.cu", "tq_decode_lut.cu", "tq_noalloc.cu", "tq_search.cu", "tq_search_tc.cu", "tq_causal_tc.cu",
            "tq_generic.cu",
            "tq_host.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

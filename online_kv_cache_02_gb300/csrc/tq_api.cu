@@ -689,10 +689,6 @@ extern "C" tq_status tq_append_decode_ex(const tq_ctx* ctx, const void* k_new, c
 // ---------------------------------------------------------------------------
 // multi-query causal attention (many new tokens per sequence)
 // ---------------------------------------------------------------------------
-namespace {
-int causal_qblocks(int T, int G) { return (T * G + 7) / 8; }
-}  // namespace
-
 extern "C" tq_status tq_causal_workspace_size(const tq_ctx* ctx, int batch, int n_new, int Hq, int max_seq_len,
                                               int chunk_tokens, size_t* bytes) {
   if (!ctx || !bytes || batch < 0 || n_new < 1 || Hq < 1 || max_seq_len < n_new || chunk_tokens < 0 ||
@@ -722,11 +718,21 @@ extern "C" tq_status tq_causal_attention(const tq_ctx* ctx, const void* q, tq_dt
   if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15) return TQ_ERR_INVALID_ARG;
   const long long rows = static_cast<long long>(batch) * n_new;
   if (rows * Hq > (1LL << 31) - 1 || rows > 65535LL * 65535LL) return TQ_ERR_UNSUPPORTED;
-  const int G = Hq / H, nqb = causal_qblocks(n_new, G);
-  const int chunk = chunk_tokens ? chunk_tokens
-                                 : pick_chunk_warps(static_cast<int>(std::min<long long>(
-                                                        static_cast<long long>(batch) * H * nqb, 1 << 30)),
-                                                    max_seq_len, lut_ctas);
+  const int G = Hq / H;
+  // tensor cores: blocks of 128 query rows, chunks of at most 1024 tokens;
+  // else the lookup-table partials kernel's causal instances (8 rows a block)
+  const bool tc = causal_tc_supported(ctx->kl, ctx->vl, ctx->cfg.m) && chunk_tokens <= causal_tc_max_chunk();
+  const int rows_blk = tc ? causal_tc_block_rows() : 8;
+  const int nqb = static_cast<int>((static_cast<long long>(n_new) * G + rows_blk - 1) / rows_blk);
+  int chunk = chunk_tokens;
+  if (!chunk && tc) {                 // the largest chunk that still gives three items per SM
+    const long long bhq = static_cast<long long>(batch) * H * nqb;
+    chunk = causal_tc_max_chunk();
+    while (chunk > 256 && bhq * nchunks_for(max_seq_len, chunk) < 3LL * sm_count()) chunk /= 2;
+  } else if (!chunk) {
+    chunk = pick_chunk_warps(static_cast<int>(std::min<long long>(static_cast<long long>(batch) * H * nqb, 1 << 30)),
+                             max_seq_len, lut_ctas);
+  }
   const int nch = nchunks_for(max_seq_len, chunk);
   const int d = ctx->cfg.d, m = ctx->cfg.m;
   if (workspace_bytes < ws_bytes(static_cast<int>(rows), Hq, d, m, nch)) return TQ_ERR_WORKSPACE;
@@ -765,7 +771,13 @@ extern "C" tq_status tq_causal_attention(const tq_ctx* ctx, const void* q, tq_dt
   a.qfrag = reinterpret_cast<uint32_t*>(w + o_frag);
   a.sched = reinterpret_cast<int*>(w + o_frag + align256(sizeof(uint32_t) * static_cast<size_t>(rows) * Hq * kQFragWords));
   a.out = out;
-  return cuda_status(launch_decode(a, TQ_STAGE_ALL, static_cast<cudaStream_t>(stream)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!tc) return cuda_status(launch_decode(a, TQ_STAGE_ALL, st));
+  a.qfrag = nullptr;                  // the tensor-core kernel reads the fp32 q~/u rows
+  cudaError_t e = launch_decode(a, TQ_STAGE_QPREP, st);
+  if (e == cudaSuccess) e = launch_causal_tc(a, nqb, st);
+  if (e == cudaSuccess) e = launch_decode(a, TQ_STAGE_MERGE, st);
+  return cuda_status(e);
 }
 
 extern "C" tq_status tq_check_device_status(const tq_ctx* ctx, uint32_t* flags) {

@@ -1,0 +1,852 @@
+// Multi-query causal attention over the compressed cache on the tensor cores
+// (tcgen05): a block of 128 query rows against 64-token tiles of the cache,
+// flash-style, with the cache dequantized once per block instead of once per
+// eight rows.
+//
+// [P4] riverfrot.github.io "TurboQuant란 무엇이며…", §2.3 (every new token's
+// K/V join the cache; new token t's query attends over its prefix), §4.3 (the
+// score: stage-1 reconstruction plus the QJL correction; softmax(score·scale)),
+// §4.2 (the codebook is only looked up); [P2] "생각정리 209 (TurboQuant)", stage 2.
+//
+// An item is (sequence b, KV head h, block of 128 query rows r = t·G + g,
+// chunk of key positions).  Per 64-token tile:
+//   S  = Q~ K^T   (Q~ = hi + lo fp16 in tensor memory, K^ the keys' centroids
+//                  as fp16 in shared memory: M = 128 rows, N = 64 tokens)
+//   S2 = U A^T    (A = 1 + c·b from the sign bits, c = 255/1024, so that
+//                  <u, 2b − 1> = (2/c)(S2 − (1 + c/2) Σu))
+//   logit = fa_t·S + fb_t·(S2 − (1 + c/2)·Σu) + bias_t with fa_t =
+//           scale·n_t/sqrt(d), fb_t = scale·(2/c)·sqrt(pi/2)/m·rho_t, bias_t =
+//           −∞ for a token that is not there (past the tile or on a skipped
+//           page); −∞ too past the row's causal end;
+//   online softmax per row in base 2 (the running max moves only when a
+//   logit passes it by more than 3, so p ≤ 8 fits fp16);
+//   [O | l] += P [V'^ | 1]  (P = p as fp16 in tensor memory; V'^ = n_v/sqrt(d)
+//                times the values' centroids, transposed in shared memory, with
+//                a row of ones under it so that column 128 of the product
+//                accumulates the softmax sum: M = 128, N = 144, K = 64 tokens).
+// Each item ends with the chunk partial (max, sum, O) of its 128 rows; the
+// decode's merge kernel combines the chunks and rotates back.
+//
+// One persistent CTA per SM, 18 warps:
+//   warp 0: items from a global counter; a tile's four K and V page blocks by
+//       bulk copy into a three-stage ring (page ids of the item loaded once);
+//   warp 1: tensor memory (496 of 512 columns) and, one lane, the MMAs, each
+//       issued as soon as its inputs are ready (the barriers are polled);
+//   warps 2-9: the tile's operands in shared memory (two buffers): warps 2-5
+//       the K^ rows, the sign rows and the per-token factors, warps 6-9 V'^
+//       transposed (a table lookup per pair of consecutive tokens of one
+//       channel) and the ones row;
+//   warps 10-17: the softmax.  Warps w and w + 4 share tensor-memory lanes
+//       32 (w % 4) .. + 31, thread = query row; the first takes tokens 0-31
+//       of a tile, the second 32-63, and they agree on the row max through
+//       shared memory.
+// Every wait is bounded; a wait that gives up sets the device error word and
+// the CTA still reaches its end.
+
+#include "tq_internal.h"
+#include "tq_tc.cuh"
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <type_traits>
+#include <utility>
+
+namespace tq {
+namespace {
+
+using namespace tcx;
+
+constexpr int kCR = 128;                  // query rows per item (MMA M)
+constexpr int kCT = 64;                   // tokens per tile
+constexpr int kCMaxChunk = 1024;          // an item's page ids: two per lane of a warp
+constexpr int kCOpWarps = 8, kCEpWarps = 8;
+constexpr int kCThreadsTC = 32 * (2 + kCOpWarps + kCEpWarps);
+constexpr int kCStages = 3;
+constexpr int kCVN = 144;                 // V'^ rows: 128 channels, the ones row, 15 zero rows
+constexpr long long kCPollLimit = 1LL << 26;
+constexpr float kInvSqrtDC = 0.08838834764831845f;
+constexpr float kSqrtHalfPiC = 1.2533141373155003f;
+constexpr float kSignCC = 255.0f / 1024.0f;
+constexpr float kLazyC = 3.0f;
+constexpr float kNegBigC = -1.0e30f;
+// tensor-memory columns
+constexpr uint32_t kTQH = 0, kTQL = 64, kTU = 128, kTS = 192, kTS2 = 256, kTO = 320, kTP = 480;
+static_assert(kTO + kCVN <= kTP && kTP + 32 <= 512, "tensor memory columns");
+
+// Lookup table of the fp16 centroid pair of a byte of two codes, per bit width
+// (replicated per lane: entry e at 128 e + 4 lane), at these offsets.
+__host__ __device__ constexpr int lut_entries_c(int b) { return b == 4 ? 256 : b == 3 ? 120 : 16; }
+constexpr int kLut2 = 0, kLut3 = 16 * 128, kLut4 = kLut3 + 120 * 128, kLutBytes = kLut4 + 256 * 128;
+__host__ __device__ constexpr int lut_off(int b) { return b == 4 ? kLut4 : b == 3 ? kLut3 : kLut2; }
+__device__ __forceinline__ int stored_code_c(int b, int f) { return b == 4 ? (f < 8 ? f + 8 : 15 - f) : f; }
+
+struct CDesc {                 // one tile of the stream
+  int item;                    // -1: end
+  int tile, last, first;
+  int p0, npos;                // first position, positions in the tile (<= 64)
+  unsigned mask;               // valid pages (4 bits)
+  int pad;
+};
+
+template <int KBH, int KBL, int VBH, int VBL, bool QJL>
+struct CGeo {
+  static constexpr int CBK = 8 * (KBH + KBL);
+  static constexpr int CBV = 8 * (VBH + VBL);
+  static constexpr int KBB = 16 * (CBK + (QJL ? 16 + 2 : 0) + 2);
+  static constexpr int VBB = 16 * (CBV + 2);
+  static constexpr int K_SIGNS = 16 * CBK;
+  static constexpr int K_NORM = K_SIGNS + (QJL ? 16 * 16 : 0);
+  static constexpr int K_RNORM = K_NORM + 32;
+  static constexpr int V_NORM = 16 * CBV;
+  static constexpr int PAGE = KBB + VBB;           // a page: K block, then V block
+  static constexpr int STAGE = 4 * PAGE;           // a tile
+  // shared memory (offsets from a 1024-aligned base)
+  static constexpr int KH = 0, AS = 16384, VT = 32768;   // in an operand buffer: K^, A [64][128], V'^ [144][64]
+  static constexpr int OPS_BYTES = VT + kCVN * 128;
+  static constexpr int OPS = 0;
+  static constexpr int LUT = OPS + 2 * OPS_BYTES;
+  static constexpr int REC = LUT + kLutBytes;
+  static constexpr int FAC = (REC + kCStages * STAGE + 1023) & ~1023;   // [2][fa | fb | bias][64] floats
+  static constexpr int XMAX = FAC + 2 * 3 * 64 * 4;                     // [2][2][128] partial row maxima
+  static constexpr int DESC = XMAX + 2 * 2 * 128 * 4;                   // [4] CDesc + [kCStages] CDesc
+  static constexpr int BAR = DESC + (4 + kCStages) * 32;
+  static constexpr int kRecFull = 0, kRecEmpty = 3, kOpsFull = 6, kKFree = 8, kVFree = 10, kDescFull = 12,
+                       kSFull = 16, kSEmpty = 17, kPFull = 18, kODone = 19, kQReady = 20, kDrain = 21,
+                       kXch = 22, kNumBar = 30;           // kXch + 2 q + parity: the row-max exchange of pair q
+  static constexpr int TMEMA = BAR + 8 * kNumBar;
+  static constexpr int SMEM = TMEMA + 16 + 1024;
+  static_assert(KBB % 16 == 0 && VBB % 16 == 0, "bulk copy unit");
+  static_assert(OPS_BYTES % 1024 == 0, "operand tiles on 1024-byte boundaries");
+  static_assert(SMEM <= 232448, "shared memory per block");
+};
+
+__device__ __forceinline__ uint32_t octet_nibbles_c(uint32_t v) {
+  return (v & 0x00777777u) | (((v & 0x00888888u) * 0x00204080u) & 0x77000000u);
+}
+__device__ __forceinline__ uint32_t stream_bits_c(const uint32_t (&w)[17], int off) {
+  return (off & 31) ? __funnelshift_r(w[off >> 5], w[(off >> 5) + 1], off & 31) : w[off >> 5];
+}
+// Lookup indices of chunk cc (8 channels) of a group of B-bit codes at stream
+// bit `base`: byte i = the index of channels (2i, 2i + 1).
+template <int B>
+__device__ __forceinline__ uint32_t chunk_bytes_c(const uint32_t (&w)[17], int base, int cc) {
+  if (B == 4) return w[(base >> 5) + cc];
+  if (B == 3) return octet_nibbles_c(stream_bits_c(w, base + 24 * cc));
+  const uint32_t x = stream_bits_c(w, base + 16 * cc) & 0xFFFFu;
+  return (x & 0xFu) | ((x & 0xF0u) << 4) | ((x & 0xF00u) << 8) | ((x & 0xF000u) << 12);
+}
+// Pair index of channel c (0..7) of an 8-channel chunk from two tokens' code
+// words xa (token 2i) and xb (2i + 1), each holding channel c in nibble c (B =
+// 3, 4: code in the low bits) or in bits 2c .. 2c + 1 (B = 2): token a's code
+// in the low bits of the index.
+template <int B>
+__device__ __forceinline__ uint32_t v_pair_c(uint32_t xa, uint32_t xb, int c) {
+  if (B == 2) {
+    const uint32_t ca = (xa >> (2 * c)) & 3u, cb = (xb >> (2 * c)) & 3u;
+    return ca | (cb << 2);
+  }
+  return ((xa >> (4 * c)) & 15u) | (((xb >> (4 * c)) & 15u) << 4);
+}
+
+// K^ rows of one 64-channel half (B-bit codes at `src`) for token row t: the
+// fp16 centroid of every channel, zero for an invalid token.
+template <int B>
+__device__ __forceinline__ void k_half_rows(uint32_t tile, uint32_t src, int t, int hf, bool tv, uint32_t tb) {
+  uint32_t w[17];
+#pragma unroll
+  for (int k = 0; k < 17; ++k) w[k] = 0u;
+  if (tv) {
+#pragma unroll
+    for (int k = 0; k < B; ++k) {
+      const uint2 x = lds64(src + 8 * k);
+      w[2 * k] = x.x;
+      w[2 * k + 1] = x.y;
+    }
+  }
+#pragma unroll
+  for (int cc = 0; cc < 8; ++cc) {
+    uint32_t p[4] = {0u, 0u, 0u, 0u};
+    if (tv) {
+      const uint32_t x = chunk_bytes_c<B>(w, 0, cc);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) p[i] = lds32(tb + ((x >> (8 * i)) & 0xFFu) * 128u);
+    }
+    sts128(tile + chunk_off(t, 8 * hf + cc, kCT), p[0], p[1], p[2], p[3]);
+  }
+}
+
+// V'^ for channels 8 cg .. 8 cg + 7 (B-bit codes of the group starting at
+// stream bit `base`) and tokens 8 tg .. 8 tg + 7 of the tile: one table lookup
+// per (channel, pair of tokens), times the pair's n_v/sqrt(d); zero for a
+// token that is not there.
+template <int B>
+__device__ __forceinline__ void v_cols(uint32_t vt, uint32_t rec, const CDesc& d, int cg, int tg, int base, int cbv,
+                                       int kbb, int v_norm, int page, uint32_t tb) {
+  const int off = base + B * 8 * (cg & 7), wi = off >> 5, sh = off & 31;
+  const bool two = sh != 0 && 4 * (wi + 1) < cbv;
+  uint32_t rows[8][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t xw[2];
+    float fv[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int t = 8 * tg + 2 * i + e, pg = t >> 4, slot = t & 15;
+      uint32_t x = 0u;
+      fv[e] = 0.0f;
+      if (t < d.npos && ((d.mask >> pg) & 1u)) {
+        const uint32_t vb = rec + pg * page + kbb;
+        const uint32_t src = vb + slot * cbv + 4 * wi;
+        const uint32_t lo = lds32(src);
+        const uint32_t hi = two ? lds32(src + 4) : 0u;
+        x = sh ? __funnelshift_r(lo, hi, sh) : lo;
+        if (B == 3) x = octet_nibbles_c(x);
+        if (B == 2) x &= 0xFFFFu;
+        fv[e] = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(vb + v_norm + 2 * slot)))) * kInvSqrtDC;
+      }
+      xw[e] = x;
+    }
+    const __half2 f2 = __floats2half2_rn(fv[0], fv[1]);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t e8 = lds32(tb + v_pair_c<B>(xw[0], xw[1], c) * 128u);
+      const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&e8), f2);
+      rows[c][i] = *reinterpret_cast<const uint32_t*>(&r);
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) sts128(vt + chunk_off(8 * cg + c, tg, kCVN), rows[c][0], rows[c][1], rows[c][2], rows[c][3]);
+}
+
+template <int KBH, int KBL, int VBH, int VBL, bool QJL>
+__global__ void __launch_bounds__(kCThreadsTC, 1)
+    causal_tc_kernel(const __grid_constant__ DecodeArgs a, int total_items, int nqb) {
+  using G = CGeo<KBH, KBL, VBH, VBL, QJL>;
+  extern __shared__ __align__(1024) unsigned char sm_raw[];
+  unsigned char* sm = sm_raw + ((0u - su32(sm_raw)) & 1023u);
+  const uint32_t sb = su32(sm);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto barx = [&](int i) { return sb + G::BAR + 8u * static_cast<uint32_t>(i); };
+  const int nch = a.nchunks, C = a.chunk, rows_all = a.T * a.G;
+  auto seq_len = [&](int b) {
+    int L = a.seq_lens[b] + a.len_add;
+    if (L < 0 || L > a.max_seq_len || L > a.maxp * kPage) {
+      atomicOr(a.tab.err, kErrSeqLen);
+      L = L < 0 ? 0 : L;
+      L = L > a.max_seq_len ? a.max_seq_len : L;
+      L = L > a.maxp * kPage ? a.maxp * kPage : L;
+    }
+    return L;
+  };
+  // item -> (b, h, query block, chunk) and its key range [c0, c1): the chunk
+  // cut at the causal end of the block's last row
+  auto item_range = [&](int it, int& b, int& h, int& qb, int& chunk, int& c0, int& c1) {
+    chunk = it % nch;
+    const int rest = it / nch;
+    qb = rest % nqb;
+    const int bh = rest / nqb;
+    h = bh % a.H;
+    b = bh / a.H;
+    const int last_row = min(rows_all, kCR * (qb + 1)) - 1;
+    const int Lq = min(seq_len(b), a.seq_lens[b] + last_row / a.G + 1);
+    c0 = chunk * C;
+    c1 = min(c0 + C, Lq);
+  };
+
+  // ---- setup: lookup tables, the constant rows of V'^, barriers, tensor memory ------
+  {
+    for (int i = tid; i < kLutBytes / 4; i += kCThreadsTC) {
+      const int off = 4 * i;
+      const int b = off >= kLut4 ? 4 : off >= kLut3 ? 3 : 2;
+      const int e = (off - lut_off(b)) >> 7;
+      const int w = b == 2 ? 2 : 4, mask = b == 4 ? 15 : b == 3 ? 7 : 3;
+      const int ilo = stored_code_c(b, e & mask), ihi = stored_code_c(b, (e >> w) & mask);
+      // one codebook per bit width (the host checks that the groups agree)
+      float clo = 0.0f, chi = 0.0f;
+      bool has = true;
+      if (a.kl.g[0].bits == b) {
+        clo = a.kl.g[0].c[ilo];
+        chi = a.kl.g[0].c[ihi];
+      } else if (a.kl.g[1].bits == b) {
+        clo = a.kl.g[1].c[ilo];
+        chi = a.kl.g[1].c[ihi];
+      } else if (a.vl.g[0].bits == b) {
+        clo = a.vl.g[0].c[ilo];
+        chi = a.vl.g[0].c[ihi];
+      } else if (a.vl.g[1].bits == b) {
+        clo = a.vl.g[1].c[ilo];
+        chi = a.vl.g[1].c[ihi];
+      } else {
+        has = false;
+      }
+      uint32_t v = 0u;
+      if (has && e < lut_entries_c(b))
+        v = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(clo))) |
+            (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(chi))) << 16);
+      *reinterpret_cast<uint32_t*>(sm + G::LUT + off) = v;
+    }
+    // rows 129 .. 143 of V'^ stay zero (row 128, the ones, is written per tile)
+    for (int i = tid; i < 2 * (kCVN - 129) * 8; i += kCThreadsTC) {
+      const int buf = i / ((kCVN - 129) * 8), rc = i % ((kCVN - 129) * 8);
+      sts128(sb + G::OPS + buf * G::OPS_BYTES + G::VT + chunk_off(129 + rc / 8, rc % 8, kCVN), 0u, 0u, 0u, 0u);
+    }
+    if (tid == 0) {
+      for (int s = 0; s < kCStages; ++s) {
+        bar_init(barx(G::kRecFull + s), 1);
+        bar_init(barx(G::kRecEmpty + s), kCOpWarps);
+      }
+      for (int s = 0; s < 2; ++s) {
+        bar_init(barx(G::kOpsFull + s), kCOpWarps);
+        bar_init(barx(G::kKFree + s), 1);
+        bar_init(barx(G::kVFree + s), 1);
+      }
+      for (int s = 0; s < 4; ++s) bar_init(barx(G::kDescFull + s), kCOpWarps);
+      bar_init(barx(G::kSFull), 1);
+      bar_init(barx(G::kSEmpty), kCEpWarps);
+      bar_init(barx(G::kPFull), kCEpWarps);
+      bar_init(barx(G::kODone), 1);
+      bar_init(barx(G::kQReady), kCEpWarps);
+      bar_init(barx(G::kDrain), 1);
+      for (int q = 0; q < 8; ++q) bar_init(barx(G::kXch + q), 2);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sb + G::TMEMA), "r"(512)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    pdl_wait();                        // the query prep before this kernel zeroed the counter and wrote q~/u
+    fence_async_smem();
+    tc_before();
+    __syncthreads();
+    tc_after();
+  }
+  const uint32_t tmem = *reinterpret_cast<const uint32_t*>(sm + G::TMEMA);
+  bool failed = false;
+  CDesc* desc = reinterpret_cast<CDesc*>(sm + G::DESC);                // per tile of the stream (4)
+  CDesc* rec_desc = reinterpret_cast<CDesc*>(sm + G::DESC + 4 * 32);   // per record stage
+
+  if (warp == 0) {
+    // ---- producer: items, page ids, the tile's page blocks ----------------------------
+    int seq = 0, item = -1, ntile = 0, tile = 0, b = 0, h = 0, c0 = 0, c1 = 0;
+    int pid0 = -1, pid1 = -1;            // page ids 2 lane, 2 lane + 1 of the item (from page c0 / 16)
+    for (;; ++seq) {
+      const int s = seq % kCStages;
+      bool ok = true;
+      if (lane == 0 && seq >= kCStages)
+        ok = bar_wait(barx(G::kRecEmpty + s), (seq / kCStages - 1) & 1, failed);
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+        failed = true;
+        break;
+      }
+      while (item != -2 && tile >= ntile) {          // the next item with work
+        int it = 0;
+        if (lane == 0) it = atomicAdd(a.sched, 1);
+        it = __shfl_sync(0xffffffffu, it, 0);
+        if (it >= total_items) {
+          item = -2;
+          break;
+        }
+        int qb, chunk;
+        item_range(it, b, h, qb, chunk, c0, c1);
+        if (c1 <= c0) continue;
+        item = it;
+        tile = 0;
+        ntile = (c1 - c0 + kCT - 1) / kCT;
+        const int pg0 = c0 >> 4, npg = (c1 - 1) / 16 - pg0 + 1;
+        const int* row = a.block_table + static_cast<long long>(b) * a.maxp + pg0;
+        pid0 = 2 * lane < npg ? __ldg(row + 2 * lane) : -1;
+        pid1 = 2 * lane + 1 < npg ? __ldg(row + 2 * lane + 1) : -1;
+      }
+      CDesc d{};
+      d.item = -1;
+      if (item >= 0) {
+        d.item = item;
+        d.tile = tile;
+        d.first = tile == 0;
+        d.last = tile == ntile - 1;
+        d.p0 = c0 + kCT * tile;
+        d.npos = min(kCT, c1 - d.p0);
+      }
+      // the tile's pages: lane j < 4 takes page j of the tile
+      const int pg = (d.item >= 0 ? (d.p0 - c0) >> 4 : 0) + (lane & 3);
+      const int v0 = __shfl_sync(0xffffffffu, pid0, (pg >> 1) & 31), v1 = __shfl_sync(0xffffffffu, pid1, (pg >> 1) & 31);
+      const int pid = (pg & 1) ? v1 : v0;
+      const bool in_range = d.item >= 0 && lane < 4 && 16 * lane < d.npos;
+      const bool valid = in_range && pid >= 0 && pid < a.num_pages;
+      if (in_range && !valid) atomicOr(a.tab.err, kErrPage);
+      const uint32_t mask = __ballot_sync(0xffffffffu, valid);
+      d.mask = mask;
+      if (lane == 0) {
+        rec_desc[s] = d;
+        if (mask) bar_arrive_tx(barx(G::kRecFull + s), static_cast<uint32_t>(__popc(mask) * G::PAGE));
+        else bar_arrive(barx(G::kRecFull + s));
+      }
+      __syncwarp();
+      if (valid) {
+        fence_async_smem();
+        const uint32_t dst = sb + G::REC + s * G::STAGE + lane * G::PAGE;
+        g2s(dst, a.kc + static_cast<long long>(pid) * a.k_page_bytes + static_cast<long long>(h) * G::KBB, G::KBB,
+            barx(G::kRecFull + s));
+        g2s(dst + G::KBB, a.vc + static_cast<long long>(pid) * a.v_page_bytes + static_cast<long long>(h) * G::VBB,
+            G::VBB, barx(G::kRecFull + s));
+      }
+      if (d.item < 0) break;
+      ++tile;
+    }
+    if (lane == 0) {                                 // copies still in flight land before the CTA ends
+      bool f2 = false;
+      for (int j = seq >= kCStages ? seq - kCStages + 1 : 0; j <= seq; ++j)
+        (void)bar_wait(barx(G::kRecFull + j % kCStages), (j / kCStages) & 1, f2);
+    }
+  } else if (warp == 1) {
+    // ---- MMA issue: S(k) once its operands are in and S(k - 1) was read (and, for
+    // an item's first tile, its queries are in); O(k) once P(k) is in --------------------
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_f16(kCT), id_o = idesc_f16(kCVN);
+      int ns = 0, no = 0, end = 1 << 30, items = 0;
+      uint32_t firsts = 0u;                            // bit k % 32: tile k opens its item
+      long long idle = 0;
+      while (no < end) {
+        bool did = false;
+        if (ns < end && ns <= no + 2 && bar_poll(barx(G::kOpsFull + (ns & 1)), (ns >> 1) & 1)) {
+          const CDesc dn = desc[ns & 3];
+          if (dn.item < 0) {
+            end = ns;
+            did = true;
+          } else if ((ns == 0 || bar_poll(barx(G::kSEmpty), (ns - 1) & 1)) &&
+                     (!dn.first || bar_poll(barx(G::kQReady), items & 1))) {
+            items += dn.first ? 1 : 0;
+            tc_after();
+            const uint32_t kh = sb + G::OPS + (ns & 1) * G::OPS_BYTES + G::KH, as = kh - G::KH + G::AS;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_ts(tmem + kTS, tmem + kTQH + 8u * k, kdesc(kh, kCT, k), id_s, k > 0 ? 1u : 0u);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mma_ts(tmem + kTS, tmem + kTQL + 8u * k, kdesc(kh, kCT, k), id_s, 1u);
+            if (QJL) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                mma_ts(tmem + kTS2, tmem + kTU + 8u * k, kdesc(as, kCT, k), id_s, k > 0 ? 1u : 0u);
+            }
+            mma_commit(barx(G::kSFull));
+            mma_commit(barx(G::kKFree + (ns & 1)));
+            firsts = dn.first ? (firsts | (1u << (ns & 31))) : (firsts & ~(1u << (ns & 31)));
+            ++ns;
+            did = true;
+          }
+        }
+        if (no < ns && bar_poll(barx(G::kPFull), no & 1)) {
+          tc_after();
+          const uint32_t vt = sb + G::OPS + (no & 1) * G::OPS_BYTES + G::VT;
+          const bool first = (firsts >> (no & 31)) & 1u;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ts(tmem + kTO, tmem + kTP + 8u * k, kdesc(vt, kCVN, k), id_o, (first && k == 0) ? 0u : 1u);
+          mma_commit(barx(G::kODone));
+          mma_commit(barx(G::kVFree + (no & 1)));
+          ++no;
+          did = true;
+        }
+        if (did) {
+          idle = 0;
+        } else if (++idle > kCPollLimit) {
+          failed = true;
+          break;
+        }
+      }
+      mma_commit(barx(G::kDrain));                     // every MMA issued completes before the CTA ends
+      bool f2 = false;
+      (void)bar_wait(barx(G::kDrain), 0, f2);
+    }
+    __syncwarp();
+  } else if (warp < 2 + kCOpWarps) {
+    // ---- operands --------------------------------------------------------------------------
+    const int u = tid - 64;                            // 0 .. 255
+    const bool vside = u >= 128;                       // warps 6-9: V'^ and the ones row
+    const int t = u & 63, hf = (u >> 6) & 1;           // K side: token row, channel half (warp-uniform)
+    const uint32_t lane_off = static_cast<uint32_t>(lane) * 4u;
+    for (int seq = 0;; ++seq) {
+      const int s = seq % kCStages, buf = seq & 1;
+      bool ok = bar_wait(barx(G::kRecFull + s), (seq / kCStages) & 1, failed);
+      if (seq >= 2) {                                  // the MMAs of two tiles back have read this buffer
+        ok = bar_wait(barx(G::kKFree + buf), ((seq - 2) >> 1) & 1, failed) && ok;
+        ok = bar_wait(barx(G::kVFree + buf), ((seq - 2) >> 1) & 1, failed) && ok;
+      }
+      if (!__all_sync(0xffffffffu, ok)) {
+        failed = true;
+        break;
+      }
+      const CDesc d = rec_desc[s];
+      if (d.item >= 0) {
+        const uint32_t rec = sb + G::REC + s * G::STAGE;
+        const uint32_t ob = sb + G::OPS + buf * G::OPS_BYTES;
+        if (!vside) {
+          const int pg = t >> 4, slot = t & 15;
+          const bool tv = t < d.npos && ((d.mask >> pg) & 1u);
+          const uint32_t kb = rec + pg * G::PAGE;
+          if (hf == 0)
+            k_half_rows<KBH>(ob + G::KH, kb + slot * G::CBK, t, 0, tv, sb + G::LUT + lut_off(KBH) + lane_off);
+          else
+            k_half_rows<KBL>(ob + G::KH, kb + slot * G::CBK + 8 * KBH, t, 1, tv, sb + G::LUT + lut_off(KBL) + lane_off);
+          if (QJL) {                                   // A = 1 + c b for the 64 projections of this half
+            uint2 sw = make_uint2(0u, 0u);
+            if (tv) sw = lds64(kb + G::K_SIGNS + slot * 16 + 8 * hf);
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+              const uint32_t byte = ((cc < 4 ? sw.x : sw.y) >> (8 * (cc & 3))) & 0xFFu;
+              const uint32_t zl = ((byte & 0xFu) * 0x10204080u) & 0x80808080u;
+              const uint32_t zh = ((byte >> 4) * 0x10204080u) & 0x80808080u;
+              const uint32_t dst = ob + G::AS + chunk_off(t, 8 * hf + cc, kCT);
+              if (tv)
+                sts128(dst, prmt(zl, 0x3C3C3C3Cu, 0x4948u), prmt(zl, 0x3C3C3C3Cu, 0x4B4Au),
+                       prmt(zh, 0x3C3C3C3Cu, 0x4948u), prmt(zh, 0x3C3C3C3Cu, 0x4B4Au));
+              else
+                sts128(dst, 0u, 0u, 0u, 0u);
+            }
+          }
+          // per-token factors (base-2 logits): half 0 fa and the bias, half 1 fb
+          const uint32_t fac = sb + G::FAC + buf * 768;
+          if (hf == 0) {
+            float fa = 0.0f;
+            if (tv)
+              fa = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(kb + G::K_NORM + 2 * slot)))) *
+                   kInvSqrtDC * a.scale_log2;
+            stsf(fac + 4 * t, fa);
+            stsf(fac + 512 + 4 * t, tv ? 0.0f : -INFINITY);
+          } else {
+            float fb = 0.0f;
+            if (QJL && tv)
+              fb = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(kb + G::K_RNORM + 2 * slot)))) *
+                   (kSqrtHalfPiC / 128.0f * (2.0f / kSignCC)) * a.scale_log2;
+            stsf(fac + 256 + 4 * t, fb);
+          }
+        } else {
+          const int v = u - 128;                       // channel block v / 8 (group v / 64), token block v % 8
+          if (v < 64)
+            v_cols<VBH>(ob + G::VT, rec, d, v >> 3, v & 7, 0, G::CBV, G::KBB, G::V_NORM, G::PAGE,
+                        sb + G::LUT + lut_off(VBH) + lane_off);
+          else
+            v_cols<VBL>(ob + G::VT, rec, d, v >> 3, v & 7, 64 * VBH, G::CBV, G::KBB, G::V_NORM, G::PAGE,
+                        sb + G::LUT + lut_off(VBL) + lane_off);
+          if (v < 8) {                                 // the ones row: 1 for a token that is there
+            uint32_t w4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int ta = 8 * v + 2 * i, tb2 = ta + 1;
+              const bool va = ta < d.npos && ((d.mask >> (ta >> 4)) & 1u);
+              const bool vb2 = tb2 < d.npos && ((d.mask >> (tb2 >> 4)) & 1u);
+              w4[i] = (va ? 0x3C00u : 0u) | (vb2 ? 0x3C000000u : 0u);
+            }
+            sts128(ob + G::VT + chunk_off(128, v, kCVN), w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+      }
+      if (u == 0) desc[seq & 3] = d;
+      fence_async_smem();                               // the operand tiles, for the tensor cores
+      __syncwarp();
+      if (lane == 0) {
+        bar_arrive(barx(G::kOpsFull + buf));
+        bar_arrive(barx(G::kDescFull + (seq & 3)));
+        if (d.item >= 0) bar_arrive(barx(G::kRecEmpty + s));
+      }
+      if (d.item < 0) break;
+    }
+  } else {
+    // ---- softmax (thread = query row of the item, tensor-memory lane r) --------------------
+    const int e = warp - 2 - kCOpWarps;                // 0 .. 7
+    const int wq = warp & 3, hh = e >> 2, r = 32 * wq + lane;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(32 * wq) << 16);
+    const int qstride = kD + a.m;
+    const float kappa = 1.0f + 0.5f * kSignCC;
+    float m_run = kNegBigC, ksu = 0.0f;
+    int row_end = 0;                                   // exclusive causal end of this row
+    long long qrow = -1;
+    int chunk = 0, wmin_end = 0;
+    for (int seq = 0;; ++seq) {
+      bool ok = bar_wait(barx(G::kDescFull + (seq & 3)), (seq >> 2) & 1, failed);
+      if (!__all_sync(0xffffffffu, ok)) {
+        failed = true;
+        break;
+      }
+      const CDesc d = desc[seq & 3];
+      if (d.item < 0) break;
+      if (d.first) {
+        int b, h, qb, c0, c1;
+        item_range(d.item, b, h, qb, chunk, c0, c1);
+        const int rr = kCR * qb + r;                   // row t G + g among the sequence's new tokens
+        qrow = rr < rows_all ? (static_cast<long long>(b) * a.T + rr / a.G) * a.Hq + h * a.G + rr % a.G : -1;
+        row_end = rr < rows_all ? a.seq_lens[b] + rr / a.G + 1 : 0;
+        int me = rr < rows_all ? row_end : 0x7FFFFFFF;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) me = min(me, __shfl_xor_sync(0xffffffffu, me, o));
+        wmin_end = me;
+        // q~ (fp16 hi + lo; first warp of the pair) and u (fp16; second) into this row's lane
+        const float* src = qrow >= 0 ? a.qprep + qrow * qstride : nullptr;
+        float su = 0.0f;
+        if (QJL) {
+#pragma unroll
+          for (int hv = 0; hv < 4; ++hv) {
+            uint32_t uh[16];
+#pragma unroll
+            for (int k4 = 0; k4 < 8; ++k4) {
+              const float4 x = src ? *reinterpret_cast<const float4*>(src + kD + 32 * hv + 4 * k4)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+              const __half2 h0 = __floats2half2_rn(x.x, x.y), h1 = __floats2half2_rn(x.z, x.w);
+              const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+              su += (f0.x + f0.y) + (f1.x + f1.y);
+              uh[2 * k4] = *reinterpret_cast<const uint32_t*>(&h0);
+              uh[2 * k4 + 1] = *reinterpret_cast<const uint32_t*>(&h1);
+            }
+            if (hh == 1) tst16(trow + kTU + 16u * hv, uh);
+          }
+        }
+        ksu = kappa * su;
+        if (hh == 0) {
+#pragma unroll
+          for (int hv = 0; hv < 4; ++hv) {
+            uint32_t qh[16], ql[16];
+#pragma unroll
+            for (int k4 = 0; k4 < 8; ++k4) {
+              const float4 x = src ? *reinterpret_cast<const float4*>(src + 32 * hv + 4 * k4)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+              const __half2 h0 = __floats2half2_rn(x.x, x.y), h1 = __floats2half2_rn(x.z, x.w);
+              const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+              const __half2 l0 = __floats2half2_rn(x.x - f0.x, x.y - f0.y);
+              const __half2 l1 = __floats2half2_rn(x.z - f1.x, x.w - f1.y);
+              qh[2 * k4] = *reinterpret_cast<const uint32_t*>(&h0);
+              qh[2 * k4 + 1] = *reinterpret_cast<const uint32_t*>(&h1);
+              ql[2 * k4] = *reinterpret_cast<const uint32_t*>(&l0);
+              ql[2 * k4 + 1] = *reinterpret_cast<const uint32_t*>(&l1);
+            }
+            tst16(trow + kTQH + 16u * hv, qh);
+            tst16(trow + kTQL + 16u * hv, ql);
+          }
+        }
+        tst_wait();
+        tc_before();
+        __syncwarp();
+        if (lane == 0) bar_arrive(barx(G::kQReady));
+        m_run = kNegBigC;
+      }
+      // this tile's scores (tokens 32 hh .. 32 hh + 31): read, release, logits
+      ok = bar_wait(barx(G::kSFull), seq & 1, failed);
+      if (!__all_sync(0xffffffffu, ok)) {
+        failed = true;
+        break;
+      }
+      tc_after();
+      float x[32];
+      const uint32_t fac = sb + G::FAC + (seq & 1) * 768 + 128u * hh;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {                    // 16 tokens at a time
+        float s1[16], s2[16];
+        tld16(trow + kTS + 32u * hh + 16u * q, s1);
+        if (QJL) tld16(trow + kTS2 + 32u * hh + 16u * q, s2);
+        if (q == 1) {
+          tc_before();
+          __syncwarp();
+          if (lane == 0) bar_arrive(barx(G::kSEmpty));
+        }
+#pragma unroll
+        for (int j4 = 0; j4 < 4; ++j4) {
+          const int j = 16 * q + 4 * j4;
+          const uint4 fa4 = lds128(fac + 4 * j), bi4 = lds128(fac + 512 + 4 * j);
+          const float fa[4] = {__uint_as_float(fa4.x), __uint_as_float(fa4.y), __uint_as_float(fa4.z),
+                               __uint_as_float(fa4.w)};
+          const float bi[4] = {__uint_as_float(bi4.x), __uint_as_float(bi4.y), __uint_as_float(bi4.z),
+                               __uint_as_float(bi4.w)};
+          if (QJL) {
+            const uint4 fb4 = lds128(fac + 256 + 4 * j);
+            const float fb[4] = {__uint_as_float(fb4.x), __uint_as_float(fb4.y), __uint_as_float(fb4.z),
+                                 __uint_as_float(fb4.w)};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) x[j + i] = fmaf(fa[i], s1[4 * j4 + i], fmaf(fb[i], s2[4 * j4 + i] - ksu, bi[i]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) x[j + i] = fmaf(fa[i], s1[4 * j4 + i], bi[i]);
+          }
+        }
+      }
+      const int pbase = d.p0 + 32 * hh;
+      if (pbase + 32 > wmin_end) {                     // the causal end falls inside (or before) these tokens
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = pbase + j < row_end ? x[j] : -INFINITY;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int j = 1; j < 32; ++j) mx = fmaxf(mx, x[j]);
+      // the pair's row max: through shared memory, double-buffered by tile parity
+      {
+        float* xm = reinterpret_cast<float*>(sm + G::XMAX) + (seq & 1) * 256;
+        xm[hh * 128 + r] = mx;
+        __syncwarp();
+        if (lane == 0) bar_arrive(barx(G::kXch + 2 * wq + (seq & 1)));
+        ok = bar_wait(barx(G::kXch + 2 * wq + (seq & 1)), (seq >> 1) & 1, failed);
+        if (!__all_sync(0xffffffffu, ok)) {
+          failed = true;
+          break;
+        }
+        mx = fmaxf(mx, xm[(1 - hh) * 128 + r]);
+      }
+      // the previous tile's O MMA has read P and updated O before either changes
+      if (!d.first) {
+        ok = bar_wait(barx(G::kODone), (seq - 1) & 1, failed);
+        if (!__all_sync(0xffffffffu, ok)) {
+          failed = true;
+          break;
+        }
+        tc_after();
+      }
+      const bool moved = mx > m_run + kLazyC;         // the running max moves: rescale this row of O and l
+      float alpha = 1.0f;
+      if (moved) {
+        alpha = exp2f(m_run - mx);
+        m_run = mx;
+      }
+      if (!d.first && __any_sync(0xffffffffu, moved)) {   // warp-wide: the tensor-memory accesses are collective
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float o[16];
+          uint32_t ou[16];
+          const uint32_t col = kTO + 64u * hh + 16u * q4;
+          tld16(trow + col, o);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) ou[k] = __float_as_uint(o[k] * alpha);
+          tst16(trow + col, ou);
+        }
+        if (hh == 0) tst1(trow + kTO + 128u, __float_as_uint(__uint_as_float(tld1(trow + kTO + 128u)) * alpha));
+        tst_wait();
+      }
+      uint32_t pp[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const __half2 h2 = __floats2half2_rn(exp2f(x[2 * k] - m_run), exp2f(x[2 * k + 1] - m_run));
+        pp[k] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      tst16(trow + kTP + 16u * hh, pp);
+      tst_wait();
+      tc_before();
+      __syncwarp();
+      if (lane == 0) bar_arrive(barx(G::kPFull));
+      if (d.last) {                                    // the item's partial (max, sum, O) for this row
+        ok = bar_wait(barx(G::kODone), seq & 1, failed);
+        if (!__all_sync(0xffffffffu, ok)) {
+          failed = true;
+          break;
+        }
+        tc_after();
+        float* dst = qrow >= 0 ? a.part + (qrow * nch + chunk) * (kD + 2) : nullptr;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float o[16];
+          tld16(trow + kTO + 64u * hh + 16u * q4, o);
+          if (dst) {
+#pragma unroll
+            for (int k = 0; k < 16; k += 2)
+              *reinterpret_cast<float2*>(dst + 2 + 64 * hh + 16 * q4 + k) = make_float2(o[k], o[k + 1]);
+          }
+        }
+        if (hh == 0) {
+          const float l = __uint_as_float(tld1(trow + kTO + 128u));
+          if (dst) *reinterpret_cast<float2*>(dst) = make_float2(m_run, l);
+        }
+        tc_before();
+      }
+    }
+  }
+  if (failed) atomicOr(a.tab.err, kErrTimeout);
+  tc_before();
+  __syncthreads();
+  tc_after();
+  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
+}
+
+template <int A, int B, int C, int D, typename F>
+bool launch_widths(std::integer_sequence<int, A, B, C, D>, F&& f) {
+  return f(std::integral_constant<int, A>{}, std::integral_constant<int, B>{}, std::integral_constant<int, C>{},
+           std::integral_constant<int, D>{});
+}
+
+template <int KBH, int KBL, int VBH, int VBL, bool QJL>
+bool layout_matches(const KindLayout& kl, const KindLayout& vl) {
+  using G = CGeo<KBH, KBL, VBH, VBL, QJL>;
+  return kl.block_bytes == G::KBB && vl.block_bytes == G::VBB && kl.code_bytes == G::CBK && vl.code_bytes == G::CBV &&
+         kl.off_norm == G::K_NORM && (!QJL || (kl.off_signs == G::K_SIGNS && kl.off_rnorm == G::K_RNORM)) &&
+         vl.off_norm == G::V_NORM;
+}
+
+template <int KBH, int KBL, int VBH, int VBL, bool QJL>
+cudaError_t launch_causal_tc_t(const DecodeArgs& a, int items, int nqb, int grid, cudaStream_t s) {
+  using G = CGeo<KBH, KBL, VBH, VBL, QJL>;
+  static std::atomic<unsigned long long> configured{0};
+  const cudaError_t e = smem_attr_once(causal_tc_kernel<KBH, KBL, VBH, VBL, QJL>, G::SMEM, configured);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(causal_tc_kernel<KBH, KBL, VBH, VBL, QJL>, dim3(grid), dim3(kCThreadsTC),
+                    static_cast<size_t>(G::SMEM), s, a, items, nqb);
+}
+
+// The bit widths (K high, K low, V high, V low) with a compiled instance.
+template <typename F>
+bool with_widths(const KindLayout& kl, const KindLayout& vl, F&& f) {
+  switch (kl.g[0].bits * 1000 + kl.g[1].bits * 100 + vl.g[0].bits * 10 + vl.g[1].bits) {
+    case 3333: return f(std::integer_sequence<int, 3, 3, 3, 3>{});
+    case 4343: return f(std::integer_sequence<int, 4, 3, 4, 3>{});
+    case 3232: return f(std::integer_sequence<int, 3, 2, 3, 2>{});
+    case 4444: return f(std::integer_sequence<int, 4, 4, 4, 4>{});
+    case 2222: return f(std::integer_sequence<int, 2, 2, 2, 2>{});
+    case 4422: return f(std::integer_sequence<int, 4, 4, 2, 2>{});
+    default: return false;
+  }
+}
+
+}  // namespace
+
+int causal_tc_block_rows() { return kCR; }
+int causal_tc_max_chunk() { return kCMaxChunk; }
+
+bool causal_tc_supported(const KindLayout& kl, const KindLayout& vl, int m) {
+  if (m != 128 || kl.split != 64 || vl.split != 64) return false;
+  // one lookup table per bit width: every group of that width has the same centroids
+  const GroupBook* gs[4] = {&kl.g[0], &kl.g[1], &vl.g[0], &vl.g[1]};
+  for (int i = 0; i < 4; ++i)
+    for (int j = i + 1; j < 4; ++j)
+      if (gs[i]->bits == gs[j]->bits)
+        for (int k = 0; k < (1 << gs[i]->bits); ++k)
+          if (gs[i]->c[k] != gs[j]->c[k]) return false;
+  return with_widths(kl, vl, [&](auto w) {
+    return launch_widths(w, [&](auto kbh, auto kbl, auto vbh, auto vbl) {
+      constexpr int KH = decltype(kbh)::value, KL = decltype(kbl)::value, VH = decltype(vbh)::value,
+                    VL = decltype(vbl)::value;
+      return kl.qjl ? layout_matches<KH, KL, VH, VL, true>(kl, vl) : layout_matches<KH, KL, VH, VL, false>(kl, vl);
+    });
+  });
+}
+
+cudaError_t launch_causal_tc(const DecodeArgs& a, int nqb, cudaStream_t s) {
+  const long long items = static_cast<long long>(a.B) * a.H * nqb * a.nchunks;
+  if (items < 1 || items > (1LL << 30) || a.chunk < kPage || a.chunk > kCMaxChunk || a.chunk % kPage)
+    return cudaErrorInvalidValue;
+  int dev = 0, sms = 152;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int grid = static_cast<int>(items < sms ? items : sms);
+  const int n = static_cast<int>(items);
+  e = cudaErrorInvalidValue;
+  with_widths(a.kl, a.vl, [&](auto w) {
+    return launch_widths(w, [&](auto kbh, auto kbl, auto vbh, auto vbl) {
+      constexpr int KH = decltype(kbh)::value, KL = decltype(kbl)::value, VH = decltype(vbh)::value,
+                    VL = decltype(vbl)::value;
+      e = a.kl.qjl ? launch_causal_tc_t<KH, KL, VH, VL, true>(a, n, nqb, grid, s)
+                   : launch_causal_tc_t<KH, KL, VH, VL, false>(a, n, nqb, grid, s);
+      return true;
+    });
+  });
+  return e;
+}
+
+}  // namespace tq

@@ -217,6 +217,14 @@ size_t search_tc_cand_bytes();
 cudaError_t launch_search_tc(const DecodeArgs& qa, const uint8_t* kc, const int32_t* bt, int num_pages, int n_db,
                              int k, float* top_s, int32_t* top_i, float* scores, void* cand, cudaStream_t st);
 bool launch_partials_lut(const DecodeArgs& a, cudaStream_t s, cudaError_t* err);
+// Causal attention on the tensor cores (tq_causal_tc.cu): query rows per
+// block (the MMA's M), the largest chunk, whether the configuration takes
+// that path, and the partials launch over B x H x query blocks x chunks items
+// (qprep before it, the merge after it, as for the decode).
+int causal_tc_block_rows();
+int causal_tc_max_chunk();
+bool causal_tc_supported(const KindLayout& kl, const KindLayout& vl, int m);
+cudaError_t launch_causal_tc(const DecodeArgs& a, int nqb, cudaStream_t s);
 
 }  // namespace tq
 

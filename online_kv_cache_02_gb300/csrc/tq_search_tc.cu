@@ -35,6 +35,7 @@
 // the CTA drains its copies and MMAs before it ends.
 
 #include "tq_internal.h"
+#include "tq_tc.cuh"
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -44,134 +45,17 @@
 namespace tq {
 namespace {
 
+using namespace tcx;
+
 constexpr int kQB = 64;                 // queries per launch (MMA N)
 constexpr int kTV = 128;                // database vectors per tile (MMA M)
 constexpr int kTop = 16;                // list length per epilogue thread
 constexpr int kWarpsS = 10;
 constexpr int kThrS = 32 * kWarpsS;
-constexpr int kWaitS = 1 << 22;
 constexpr float kInvSqrtDS = 0.08838834764831845f;
 constexpr float kSqrtHalfPiS = 1.2533141373155003f;
 constexpr float kSignC = 255.0f / 1024.0f;
 constexpr int kScoreRow = 136;          // floats per query row of the score tile (bank skew)
-
-// ---- PTX wrappers ------------------------------------------------------------
-__device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
-__device__ __forceinline__ void bar_init(uint32_t b, uint32_t n) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(b), "r"(n) : "memory");
-}
-__device__ __forceinline__ void bar_arrive(uint32_t b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(b) : "memory");
-}
-__device__ __forceinline__ void bar_arrive_tx(uint32_t b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool bar_test(uint32_t b, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(done)
-      : "r"(b), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-// Bounded wait; once `failed` is set every later wait returns false at once.
-__device__ __forceinline__ bool bar_wait(uint32_t b, uint32_t parity, bool& failed) {
-  if (failed) return false;
-  for (int i = 0; i < kWaitS; ++i)
-    if (bar_test(b, parity)) return true;
-  failed = true;
-  return false;
-}
-__device__ __forceinline__ void g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t b) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(b)
-               : "memory");
-}
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void nsync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint32_t b) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(b) : "memory");
-}
-__device__ __forceinline__ void tld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(s));
-  return d;
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-// Explicit shared-space accesses (32-bit addresses) for the hot loops.
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ float ldsf(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
-  unsigned short v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ void stsf(uint32_t addr, float v) {
-  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
-// Shared-memory matrix descriptor (K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart) and k-step s (16 channels) of a 128-channel operand of
-// `rows` rows stored as two 64-channel halves of [rows][128 B].
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
-  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) |
-         (2ull << 61);
-}
-__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int rows, int s) {
-  return sdesc(tile + (s >> 2) * rows * 128 + (s & 3) * 32);
-}
-// Byte offset of 16-byte chunk c (channels 8c .. 8c + 7) of row r in such an operand.
-__device__ __forceinline__ uint32_t chunk_off(int r, int c, int rows) {
-  return static_cast<uint32_t>((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
-// kind::f16, fp32 accumulate, fp16 A and B, K-major, M = 128, N = n.
-__host__ __device__ constexpr uint32_t idesc_f16(int n) {
-  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
-}
 
 // ---- codes ------------------------------------------------------------------
 __host__ __device__ constexpr int lut_entries_s(int b) { return b == 4 ? 256 : b == 3 ? 120 : 16; }

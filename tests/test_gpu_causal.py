@@ -115,3 +115,17 @@ def test_causal_unsupported_widths_are_rejected():
         assert st == tq.TQ_ERR_UNSUPPORTED
     finally:
         tq.tq_destroy(ctx)
+
+
+def test_causal_large_chunks_take_the_lookup_table_kernel():
+    """Chunks above 1024 tokens run on the lookup-table kernel's causal instances (blocks of 8 query rows)
+    instead of the tensor-core kernel; the same bar holds."""
+    w = wl.Workload("t", "decode", 2, 8, 2, 0, k_bits=(3, 3), v_bits=(3, 3), seed=8)
+    _causal(w, starts=[1500, 40], T=9, Hq=8, H=2, seed=4, chunk=2048)
+
+
+def test_causal_many_query_blocks():
+    """More than 128 query rows per (sequence, KV head): several row blocks of the tensor-core kernel, the last
+    one ragged, with chunks that cut the prefix into several items."""
+    w = wl.Workload("t", "decode", 2, 8, 2, 0, k_bits=(4, 3), v_bits=(4, 3), seed=9)
+    _causal(w, starts=[700, 5], T=70, Hq=8, H=2, seed=6, chunk=256)
