@@ -9,34 +9,37 @@
 // §4.2 (the codebook is only looked up); [P2] "생각정리 209 (TurboQuant)", stage 2.
 //
 // An item is (sequence b, KV head h, block of 128 query rows r = t·G + g,
-// chunk of key positions).  Per 64-token tile:
-//   S  = Q~ K^T   (Q~ = hi + lo fp16 in tensor memory, K^ the keys' centroids
-//                  as fp16 in shared memory: M = 128 rows, N = 64 tokens)
-//   S2 = U A^T    (A = 1 + c·b from the sign bits, c = 255/1024, so that
-//                  <u, 2b − 1> = (2/c)(S2 − (1 + c/2) Σu))
-//   logit = fa_t·S + fb_t·(S2 − (1 + c/2)·Σu) + bias_t with fa_t =
-//           scale·n_t/sqrt(d), fb_t = scale·(2/c)·sqrt(pi/2)/m·rho_t, bias_t =
-//           −∞ for a token that is not there (past the tile or on a skipped
-//           page); −∞ too past the row's causal end;
-//   online softmax per row in base 2 (the running max moves only when a
-//   logit passes it by more than 3, so p ≤ 8 fits fp16);
+// chunk of key positions).  Per 64-token tile, with base-2 logits:
+//   S = Q~ K^T + U A'^T   (one accumulator: M = 128 rows, N = 64 tokens)
+//       Q~ = hi + lo fp16 and U = S·Pi q in fp16 sit in tensor memory;
+//       K^ = the key's centroids and A' = (fb_t/fa_t)(2 b − 1) from the sign
+//       bits, fp16 in shared memory, with fa_t = n_t/sqrt(d) and fb_t =
+//       sqrt(pi/2)/m·rho_t;
+//   logit = scale·log2(e)·fa_t·S + bias_t, bias_t = −∞ for a token that is
+//       not there (past the tile or on a skipped page), −∞ too past the row's
+//       causal end;
+//   online softmax per row (the running max moves only when a logit passes it
+//   by more than 3, so p ≤ 8 fits fp16);
 //   [O | l] += P [V'^ | 1]  (P = p as fp16 in tensor memory; V'^ = n_v/sqrt(d)
-//                times the values' centroids, transposed in shared memory, with
-//                a row of ones under it so that column 128 of the product
-//                accumulates the softmax sum: M = 128, N = 144, K = 64 tokens).
+//       times the values' centroids, transposed in shared memory, with a row of
+//       ones under it so that column 128 accumulates the softmax sum: M = 128,
+//       N = 144, K = 64 tokens).
 // Each item ends with the chunk partial (max, sum, O) of its 128 rows; the
 // decode's merge kernel combines the chunks and rotates back.
 //
 // One persistent CTA per SM, 18 warps:
 //   warp 0: items from a global counter; a tile's four K and V page blocks by
 //       bulk copy into a three-stage ring (page ids of the item loaded once);
-//   warp 1: tensor memory (496 of 512 columns) and, one lane, the MMAs, each
-//       issued as soon as its inputs are ready (the barriers are polled);
-//   warps 2-9: the tile's operands in shared memory (two buffers): warps 2-5
-//       the K^ rows, the sign rows and the per-token factors, warps 6-9 V'^
-//       transposed (a table lookup per pair of consecutive tokens of one
-//       channel) and the ones row;
-//   warps 10-17: the softmax.  Warps w and w + 4 share tensor-memory lanes
+//   warp 1: tensor memory (496 of 512 columns) and, one lane, the MMAs;
+//   warps 4, 5, 16, 17: K^ and A' rows and the token factors (two buffers,
+//       free again once the tile's S MMAs have run);
+//   warps 2, 3, 6, 7: V'^ transposed (a table lookup per pair of consecutive
+//       tokens of one channel) and the ones row (two buffers, free again once
+//       the tile's O MMAs have run);
+//   (a warp runs on SMSP warp % 4: each SMSP holds two softmax warps and one
+//   side of the operand work, so that fewer code paths share its instruction
+//   cache)
+//   warps 8-15: the softmax.  Warps w and w + 4 share tensor-memory lanes
 //       32 (w % 4) .. + 31, thread = query row; the first takes tokens 0-31
 //       of a tile, the second 32-63, and they agree on the row max through
 //       shared memory.
@@ -65,14 +68,12 @@ constexpr int kCOpWarps = 8, kCEpWarps = 8;
 constexpr int kCThreadsTC = 32 * (2 + kCOpWarps + kCEpWarps);
 constexpr int kCStages = 3;
 constexpr int kCVN = 144;                 // V'^ rows: 128 channels, the ones row, 15 zero rows
-constexpr long long kCPollLimit = 1LL << 26;
 constexpr float kInvSqrtDC = 0.08838834764831845f;
 constexpr float kSqrtHalfPiC = 1.2533141373155003f;
-constexpr float kSignCC = 255.0f / 1024.0f;
 constexpr float kLazyC = 3.0f;
 constexpr float kNegBigC = -1.0e30f;
 // tensor-memory columns
-constexpr uint32_t kTQH = 0, kTQL = 64, kTU = 128, kTS = 192, kTS2 = 256, kTO = 320, kTP = 480;
+constexpr uint32_t kTQH = 0, kTQL = 64, kTU = 128, kTS = 192, kTO = 320, kTP = 480;
 static_assert(kTO + kCVN <= kTP && kTP + 32 <= 512, "tensor memory columns");
 
 // Lookup table of the fp16 centroid pair of a byte of two codes, per bit width
@@ -103,18 +104,18 @@ struct CGeo {
   static constexpr int PAGE = KBB + VBB;           // a page: K block, then V block
   static constexpr int STAGE = 4 * PAGE;           // a tile
   // shared memory (offsets from a 1024-aligned base)
-  static constexpr int KH = 0, AS = 16384, VT = 32768;   // in an operand buffer: K^, A [64][128], V'^ [144][64]
+  static constexpr int KH = 0, AS = 16384, VT = 32768;   // in an operand buffer: K^, A' [64][128], V'^ [144][64]
   static constexpr int OPS_BYTES = VT + kCVN * 128;
   static constexpr int OPS = 0;
   static constexpr int LUT = OPS + 2 * OPS_BYTES;
   static constexpr int REC = LUT + kLutBytes;
-  static constexpr int FAC = (REC + kCStages * STAGE + 1023) & ~1023;   // [2][fa | fb | bias][64] floats
-  static constexpr int XMAX = FAC + 2 * 3 * 64 * 4;                     // [2][2][128] partial row maxima
+  static constexpr int FAC = (REC + kCStages * STAGE + 1023) & ~1023;   // [4][fa | bias][64] floats
+  static constexpr int XMAX = FAC + 4 * 2 * 64 * 4;                     // [2][2][128] partial row maxima
   static constexpr int DESC = XMAX + 2 * 2 * 128 * 4;                   // [4] CDesc + [kCStages] CDesc
   static constexpr int BAR = DESC + (4 + kCStages) * 32;
-  static constexpr int kRecFull = 0, kRecEmpty = 3, kOpsFull = 6, kKFree = 8, kVFree = 10, kDescFull = 12,
-                       kSFull = 16, kSEmpty = 17, kPFull = 18, kODone = 19, kQReady = 20, kDrain = 21,
-                       kXch = 22, kNumBar = 30;           // kXch + 2 q + parity: the row-max exchange of pair q
+  static constexpr int kRecFull = 0, kRecEmpty = 3, kKOps = 6, kVOps = 8, kKFree = 10, kVFree = 12,
+                       kDescFull = 14, kSFull = 18, kSEmpty = 19, kPFull = 20, kODone = 21, kQReady = 22,
+                       kDrain = 23, kXch = 24, kNumBar = 32;  // kXch + 2 q + parity: the row-max exchange of pair q
   static constexpr int TMEMA = BAR + 8 * kNumBar;
   static constexpr int SMEM = TMEMA + 16 + 1024;
   static_assert(KBB % 16 == 0 && VBB % 16 == 0, "bulk copy unit");
@@ -150,26 +151,28 @@ __device__ __forceinline__ uint32_t v_pair_c(uint32_t xa, uint32_t xb, int c) {
   return ((xa >> (4 * c)) & 15u) | (((xb >> (4 * c)) & 15u) << 4);
 }
 
-// K^ rows of one 64-channel half (B-bit codes at `src`) for token row t: the
-// fp16 centroid of every channel, zero for an invalid token.
+// K^ rows of one 64-channel half (B-bit codes at `src`, 8 B bytes) for token
+// row t: the fp16 centroid of every channel, zero for an invalid token.  The
+// chunk loop stays rolled: the kernel's roles share each SM's instruction
+// cache.
 template <int B>
 __device__ __forceinline__ void k_half_rows(uint32_t tile, uint32_t src, int t, int hf, bool tv, uint32_t tb) {
-  uint32_t w[17];
-#pragma unroll
-  for (int k = 0; k < 17; ++k) w[k] = 0u;
-  if (tv) {
-#pragma unroll
-    for (int k = 0; k < B; ++k) {
-      const uint2 x = lds64(src + 8 * k);
-      w[2 * k] = x.x;
-      w[2 * k + 1] = x.y;
-    }
-  }
-#pragma unroll
+#pragma unroll 1
   for (int cc = 0; cc < 8; ++cc) {
     uint32_t p[4] = {0u, 0u, 0u, 0u};
     if (tv) {
-      const uint32_t x = chunk_bytes_c<B>(w, 0, cc);
+      const int off = B * 8 * cc, wi = off >> 5, sh = off & 31;
+      const uint32_t lo = lds32(src + 4 * wi);
+      uint32_t x;
+      if (B == 4) {
+        x = lo;
+      } else if (B == 3) {
+        const uint32_t hi = sh > 8 ? lds32(src + 4 * wi + 4) : 0u;
+        x = octet_nibbles_c(sh ? __funnelshift_r(lo, hi, sh) : lo);
+      } else {
+        const uint32_t y = (lo >> sh) & 0xFFFFu;
+        x = (y & 0xFu) | ((y & 0xF0u) << 4) | ((y & 0xF00u) << 8) | ((y & 0xF000u) << 12);
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i) p[i] = lds32(tb + ((x >> (8 * i)) & 0xFFu) * 128u);
     }
@@ -180,16 +183,16 @@ __device__ __forceinline__ void k_half_rows(uint32_t tile, uint32_t src, int t, 
 // V'^ for channels 8 cg .. 8 cg + 7 (B-bit codes of the group starting at
 // stream bit `base`) and tokens 8 tg .. 8 tg + 7 of the tile: one table lookup
 // per (channel, pair of tokens), times the pair's n_v/sqrt(d); zero for a
-// token that is not there.
+// token that is not there.  The channel loop stays rolled (instruction cache).
 template <int B>
 __device__ __forceinline__ void v_cols(uint32_t vt, uint32_t rec, const CDesc& d, int cg, int tg, int base, int cbv,
                                        int kbb, int v_norm, int page, uint32_t tb) {
   const int off = base + B * 8 * (cg & 7), wi = off >> 5, sh = off & 31;
   const bool two = sh != 0 && 4 * (wi + 1) < cbv;
-  uint32_t rows[8][4];
+  uint32_t xw[8];
+  __half2 f2[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint32_t xw[2];
     float fv[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
@@ -206,18 +209,21 @@ __device__ __forceinline__ void v_cols(uint32_t vt, uint32_t rec, const CDesc& d
         if (B == 2) x &= 0xFFFFu;
         fv[e] = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(vb + v_norm + 2 * slot)))) * kInvSqrtDC;
       }
-      xw[e] = x;
+      xw[2 * i + e] = x;
     }
-    const __half2 f2 = __floats2half2_rn(fv[0], fv[1]);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint32_t e8 = lds32(tb + v_pair_c<B>(xw[0], xw[1], c) * 128u);
-      const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&e8), f2);
-      rows[c][i] = *reinterpret_cast<const uint32_t*>(&r);
-    }
+    f2[i] = __floats2half2_rn(fv[0], fv[1]);
   }
+#pragma unroll 1
+  for (int c = 0; c < 8; ++c) {
+    uint32_t w4[4];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) sts128(vt + chunk_off(8 * cg + c, tg, kCVN), rows[c][0], rows[c][1], rows[c][2], rows[c][3]);
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t e8 = lds32(tb + v_pair_c<B>(xw[2 * i], xw[2 * i + 1], c) * 128u);
+      const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&e8), f2[i]);
+      w4[i] = *reinterpret_cast<const uint32_t*>(&r);
+    }
+    sts128(vt + chunk_off(8 * cg + c, tg, kCVN), w4[0], w4[1], w4[2], w4[3]);
+  }
 }
 
 template <int KBH, int KBL, int VBH, int VBL, bool QJL>
@@ -298,11 +304,12 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
         bar_init(barx(G::kRecEmpty + s), kCOpWarps);
       }
       for (int s = 0; s < 2; ++s) {
-        bar_init(barx(G::kOpsFull + s), kCOpWarps);
+        bar_init(barx(G::kKOps + s), kCOpWarps / 2);
+        bar_init(barx(G::kVOps + s), kCOpWarps / 2);
         bar_init(barx(G::kKFree + s), 1);
         bar_init(barx(G::kVFree + s), 1);
       }
-      for (int s = 0; s < 4; ++s) bar_init(barx(G::kDescFull + s), kCOpWarps);
+      for (int s = 0; s < 4; ++s) bar_init(barx(G::kDescFull + s), kCOpWarps / 2);
       bar_init(barx(G::kSFull), 1);
       bar_init(barx(G::kSEmpty), kCEpWarps);
       bar_init(barx(G::kPFull), kCEpWarps);
@@ -402,166 +409,170 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
         (void)bar_wait(barx(G::kRecFull + j % kCStages), (j / kCStages) & 1, f2);
     }
   } else if (warp == 1) {
-    // ---- MMA issue: S(k) once its operands are in and S(k - 1) was read (and, for
-    // an item's first tile, its queries are in); O(k) once P(k) is in --------------------
+    // ---- MMA issue, one lane, in stream order: S(k + 1) goes ahead of O(k) (its
+    // operands and the release of S(k) come early in tile k), except that an item's
+    // first S waits for its queries, which follow O(k) of the item before --------------
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_f16(kCT), id_o = idesc_f16(kCVN);
-      int ns = 0, no = 0, end = 1 << 30, items = 0;
-      uint32_t firsts = 0u;                            // bit k % 32: tile k opens its item
-      long long idle = 0;
-      while (no < end) {
-        bool did = false;
-        if (ns < end && ns <= no + 2 && bar_poll(barx(G::kOpsFull + (ns & 1)), (ns >> 1) & 1)) {
-          const CDesc dn = desc[ns & 3];
-          if (dn.item < 0) {
-            end = ns;
-            did = true;
-          } else if ((ns == 0 || bar_poll(barx(G::kSEmpty), (ns - 1) & 1)) &&
-                     (!dn.first || bar_poll(barx(G::kQReady), items & 1))) {
-            items += dn.first ? 1 : 0;
-            tc_after();
-            const uint32_t kh = sb + G::OPS + (ns & 1) * G::OPS_BYTES + G::KH, as = kh - G::KH + G::AS;
+      auto issue_s = [&](int k) {
+        const uint32_t kh = sb + G::OPS + (k & 1) * G::OPS_BYTES + G::KH, as = kh - G::KH + G::AS;
+        tc_after();
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              mma_ts(tmem + kTS, tmem + kTQH + 8u * k, kdesc(kh, kCT, k), id_s, k > 0 ? 1u : 0u);
+        for (int j = 0; j < 8; ++j) mma_ts(tmem + kTS, tmem + kTQH + 8u * j, kdesc(kh, kCT, j), id_s, j > 0 ? 1u : 0u);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) mma_ts(tmem + kTS, tmem + kTQL + 8u * k, kdesc(kh, kCT, k), id_s, 1u);
-            if (QJL) {
+        for (int j = 0; j < 8; ++j) mma_ts(tmem + kTS, tmem + kTQL + 8u * j, kdesc(kh, kCT, j), id_s, 1u);
+        if (QJL) {
 #pragma unroll
-              for (int k = 0; k < 8; ++k)
-                mma_ts(tmem + kTS2, tmem + kTU + 8u * k, kdesc(as, kCT, k), id_s, k > 0 ? 1u : 0u);
-            }
-            mma_commit(barx(G::kSFull));
-            mma_commit(barx(G::kKFree + (ns & 1)));
-            firsts = dn.first ? (firsts | (1u << (ns & 31))) : (firsts & ~(1u << (ns & 31)));
-            ++ns;
-            did = true;
-          }
+          for (int j = 0; j < 8; ++j) mma_ts(tmem + kTS, tmem + kTU + 8u * j, kdesc(as, kCT, j), id_s, 1u);
         }
-        if (no < ns && bar_poll(barx(G::kPFull), no & 1)) {
-          tc_after();
-          const uint32_t vt = sb + G::OPS + (no & 1) * G::OPS_BYTES + G::VT;
-          const bool first = (firsts >> (no & 31)) & 1u;
+        mma_commit(barx(G::kSFull));
+        mma_commit(barx(G::kKFree + (k & 1)));
+      };
+      auto issue_o = [&](int k, bool first) {
+        const uint32_t vt = sb + G::OPS + (k & 1) * G::OPS_BYTES + G::VT;
+        tc_after();
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + kTO, tmem + kTP + 8u * k, kdesc(vt, kCVN, k), id_o, (first && k == 0) ? 0u : 1u);
-          mma_commit(barx(G::kODone));
-          mma_commit(barx(G::kVFree + (no & 1)));
-          ++no;
-          did = true;
+        for (int j = 0; j < 4; ++j)
+          mma_ts(tmem + kTO, tmem + kTP + 8u * j, kdesc(vt, kCVN, j), id_o, (first && j == 0) ? 0u : 1u);
+        mma_commit(barx(G::kODone));
+        mma_commit(barx(G::kVFree + (k & 1)));
+      };
+      int items = 0;
+      CDesc d{};
+      bool run = bar_wait(barx(G::kKOps), 0, failed);
+      if (run) {
+        d = desc[0];
+        run = d.item >= 0 && bar_wait(barx(G::kQReady), items++ & 1, failed);
+      }
+      if (run) issue_s(0);
+      for (int k = 0; run; ++k) {
+        if (!bar_wait(barx(G::kKOps + ((k + 1) & 1)), ((k + 1) >> 1) & 1, failed)) break;
+        const CDesc dn = desc[(k + 1) & 3];
+        const bool more = dn.item >= 0;
+        if (more && !dn.first) {
+          if (!bar_wait(barx(G::kSEmpty), k & 1, failed)) break;
+          issue_s(k + 1);
         }
-        if (did) {
-          idle = 0;
-        } else if (++idle > kCPollLimit) {
-          failed = true;
-          break;
+        if (!bar_wait(barx(G::kVOps + (k & 1)), (k >> 1) & 1, failed)) break;
+        if (!bar_wait(barx(G::kPFull), k & 1, failed)) break;
+        issue_o(k, d.first != 0);
+        if (more && dn.first) {
+          if (!bar_wait(barx(G::kQReady), items++ & 1, failed)) break;
+          if (!bar_wait(barx(G::kSEmpty), k & 1, failed)) break;
+          issue_s(k + 1);
         }
+        if (!more) break;
+        d = dn;
       }
       mma_commit(barx(G::kDrain));                     // every MMA issued completes before the CTA ends
       bool f2 = false;
       (void)bar_wait(barx(G::kDrain), 0, f2);
     }
     __syncwarp();
-  } else if (warp < 2 + kCOpWarps) {
-    // ---- operands --------------------------------------------------------------------------
-    const int u = tid - 64;                            // 0 .. 255
-    const bool vside = u >= 128;                       // warps 6-9: V'^ and the ones row
+  } else if (warp < 8 || warp >= 16) {
+    // ---- operands: K side on warps 4, 5, 16, 17 (the first two SMSPs), V side on warps 2, 3,
+    // 6, 7 (the other two), each its own pipeline ---------------------------------------------
+    const bool vside = warp < 4 || (warp >= 6 && warp < 8);
+    const int ridx = vside ? (warp < 4 ? warp - 2 : warp - 4) : (warp < 8 ? warp - 4 : warp - 14);
+    const int u = 32 * ridx + lane + (vside ? 128 : 0);   // K side 0 .. 127, V side 128 .. 255
     const int t = u & 63, hf = (u >> 6) & 1;           // K side: token row, channel half (warp-uniform)
     const uint32_t lane_off = static_cast<uint32_t>(lane) * 4u;
     for (int seq = 0;; ++seq) {
       const int s = seq % kCStages, buf = seq & 1;
       bool ok = bar_wait(barx(G::kRecFull + s), (seq / kCStages) & 1, failed);
-      if (seq >= 2) {                                  // the MMAs of two tiles back have read this buffer
-        ok = bar_wait(barx(G::kKFree + buf), ((seq - 2) >> 1) & 1, failed) && ok;
-        ok = bar_wait(barx(G::kVFree + buf), ((seq - 2) >> 1) & 1, failed) && ok;
-      }
+      if (seq >= 2)                                    // this side's MMAs of two tiles back have read the buffer
+        ok = bar_wait(barx((vside ? G::kVFree : G::kKFree) + buf), ((seq - 2) >> 1) & 1, failed) && ok;
       if (!__all_sync(0xffffffffu, ok)) {
         failed = true;
         break;
       }
       const CDesc d = rec_desc[s];
-      if (d.item >= 0) {
-        const uint32_t rec = sb + G::REC + s * G::STAGE;
-        const uint32_t ob = sb + G::OPS + buf * G::OPS_BYTES;
-        if (!vside) {
+      const uint32_t rec = sb + G::REC + s * G::STAGE;
+      const uint32_t ob = sb + G::OPS + buf * G::OPS_BYTES;
+      if (!vside) {
+        if (d.item >= 0) {
           const int pg = t >> 4, slot = t & 15;
           const bool tv = t < d.npos && ((d.mask >> pg) & 1u);
           const uint32_t kb = rec + pg * G::PAGE;
+          float fa = 0.0f, fb = 0.0f;
+          if (tv) {
+            fa = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(kb + G::K_NORM + 2 * slot)))) *
+                 kInvSqrtDC;
+            if (QJL)
+              fb = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(kb + G::K_RNORM + 2 * slot)))) *
+                   (kSqrtHalfPiC / 128.0f);
+          }
           if (hf == 0)
             k_half_rows<KBH>(ob + G::KH, kb + slot * G::CBK, t, 0, tv, sb + G::LUT + lut_off(KBH) + lane_off);
           else
             k_half_rows<KBL>(ob + G::KH, kb + slot * G::CBK + 8 * KBH, t, 1, tv, sb + G::LUT + lut_off(KBL) + lane_off);
-          if (QJL) {                                   // A = 1 + c b for the 64 projections of this half
+          if (QJL) {                                   // A' = (fb / fa)(2 b - 1) for the 64 projections of this half
             uint2 sw = make_uint2(0u, 0u);
             if (tv) sw = lds64(kb + G::K_SIGNS + slot * 16 + 8 * hf);
-#pragma unroll
+            const __half2 fb2 = __float2half2_rn(fa > 0.0f ? fb / fa : 0.0f);
+            const uint32_t fbs = *reinterpret_cast<const uint32_t*>(&fb2) | 0x80008000u;   // -fb in both halves
+#pragma unroll 1
             for (int cc = 0; cc < 8; ++cc) {
               const uint32_t byte = ((cc < 4 ? sw.x : sw.y) >> (8 * (cc & 3))) & 0xFFu;
-              const uint32_t zl = ((byte & 0xFu) * 0x10204080u) & 0x80808080u;
+              const uint32_t zl = ((byte & 0xFu) * 0x10204080u) & 0x80808080u;   // sign bit j <- bit j
               const uint32_t zh = ((byte >> 4) * 0x10204080u) & 0x80808080u;
               const uint32_t dst = ob + G::AS + chunk_off(t, 8 * hf + cc, kCT);
-              if (tv)
-                sts128(dst, prmt(zl, 0x3C3C3C3Cu, 0x4948u), prmt(zl, 0x3C3C3C3Cu, 0x4B4Au),
-                       prmt(zh, 0x3C3C3C3Cu, 0x4948u), prmt(zh, 0x3C3C3C3Cu, 0x4B4Au));
-              else
-                sts128(dst, 0u, 0u, 0u, 0u);
+              // a set bit clears the half's sign: +fb; a clear bit leaves -fb
+              sts128(dst, tv ? fbs ^ (prmt(zl, 0u, 0x9080u) & 0x80008000u) : 0u,
+                     tv ? fbs ^ (prmt(zl, 0u, 0xB0A0u) & 0x80008000u) : 0u,
+                     tv ? fbs ^ (prmt(zh, 0u, 0x9080u) & 0x80008000u) : 0u,
+                     tv ? fbs ^ (prmt(zh, 0u, 0xB0A0u) & 0x80008000u) : 0u);
             }
           }
-          // per-token factors (base-2 logits): half 0 fa and the bias, half 1 fb
-          const uint32_t fac = sb + G::FAC + buf * 768;
           if (hf == 0) {
-            float fa = 0.0f;
-            if (tv)
-              fa = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(kb + G::K_NORM + 2 * slot)))) *
-                   kInvSqrtDC * a.scale_log2;
-            stsf(fac + 4 * t, fa);
-            stsf(fac + 512 + 4 * t, tv ? 0.0f : -INFINITY);
-          } else {
-            float fb = 0.0f;
-            if (QJL && tv)
-              fb = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(kb + G::K_RNORM + 2 * slot)))) *
-                   (kSqrtHalfPiC / 128.0f * (2.0f / kSignCC)) * a.scale_log2;
-            stsf(fac + 256 + 4 * t, fb);
-          }
-        } else {
-          const int v = u - 128;                       // channel block v / 8 (group v / 64), token block v % 8
-          if (v < 64)
-            v_cols<VBH>(ob + G::VT, rec, d, v >> 3, v & 7, 0, G::CBV, G::KBB, G::V_NORM, G::PAGE,
-                        sb + G::LUT + lut_off(VBH) + lane_off);
-          else
-            v_cols<VBL>(ob + G::VT, rec, d, v >> 3, v & 7, 64 * VBH, G::CBV, G::KBB, G::V_NORM, G::PAGE,
-                        sb + G::LUT + lut_off(VBL) + lane_off);
-          if (v < 8) {                                 // the ones row: 1 for a token that is there
-            uint32_t w4[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int ta = 8 * v + 2 * i, tb2 = ta + 1;
-              const bool va = ta < d.npos && ((d.mask >> (ta >> 4)) & 1u);
-              const bool vb2 = tb2 < d.npos && ((d.mask >> (tb2 >> 4)) & 1u);
-              w4[i] = (va ? 0x3C00u : 0u) | (vb2 ? 0x3C000000u : 0u);
-            }
-            sts128(ob + G::VT + chunk_off(128, v, kCVN), w4[0], w4[1], w4[2], w4[3]);
+            const uint32_t fac = sb + G::FAC + (seq & 3) * 512;
+            stsf(fac + 4 * t, fa * a.scale_log2);
+            stsf(fac + 256 + 4 * t, tv ? 0.0f : -INFINITY);
           }
         }
-      }
-      if (u == 0) desc[seq & 3] = d;
-      fence_async_smem();                               // the operand tiles, for the tensor cores
-      __syncwarp();
-      if (lane == 0) {
-        bar_arrive(barx(G::kOpsFull + buf));
-        bar_arrive(barx(G::kDescFull + (seq & 3)));
-        if (d.item >= 0) bar_arrive(barx(G::kRecEmpty + s));
+        if (u == 0) desc[seq & 3] = d;
+        fence_async_smem();                             // the operand tiles, for the tensor cores
+        __syncwarp();
+        if (lane == 0) {
+          bar_arrive(barx(G::kKOps + buf));
+          bar_arrive(barx(G::kDescFull + (seq & 3)));
+          if (d.item >= 0) bar_arrive(barx(G::kRecEmpty + s));
+        }
+      } else if (d.item >= 0) {
+        const int v = u - 128;                         // channel block v / 8 (group v / 64), token block v % 8
+        if (v < 64)
+          v_cols<VBH>(ob + G::VT, rec, d, v >> 3, v & 7, 0, G::CBV, G::KBB, G::V_NORM, G::PAGE,
+                      sb + G::LUT + lut_off(VBH) + lane_off);
+        else
+          v_cols<VBL>(ob + G::VT, rec, d, v >> 3, v & 7, 64 * VBH, G::CBV, G::KBB, G::V_NORM, G::PAGE,
+                      sb + G::LUT + lut_off(VBL) + lane_off);
+        if (v < 8) {                                   // the ones row: 1 for a token that is there
+          uint32_t w4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int ta = 8 * v + 2 * i, tb2 = ta + 1;
+            const bool va = ta < d.npos && ((d.mask >> (ta >> 4)) & 1u);
+            const bool vb2 = tb2 < d.npos && ((d.mask >> (tb2 >> 4)) & 1u);
+            w4[i] = (va ? 0x3C00u : 0u) | (vb2 ? 0x3C000000u : 0u);
+          }
+          sts128(ob + G::VT + chunk_off(128, v, kCVN), w4[0], w4[1], w4[2], w4[3]);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          bar_arrive(barx(G::kVOps + buf));
+          bar_arrive(barx(G::kRecEmpty + s));
+        }
       }
       if (d.item < 0) break;
     }
   } else {
     // ---- softmax (thread = query row of the item, tensor-memory lane r) --------------------
-    const int e = warp - 2 - kCOpWarps;                // 0 .. 7
+    const int e = warp - 8;                            // 0 .. 7
     const int wq = warp & 3, hh = e >> 2, r = 32 * wq + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * wq) << 16);
     const int qstride = kD + a.m;
-    const float kappa = 1.0f + 0.5f * kSignCC;
-    float m_run = kNegBigC, ksu = 0.0f;
+    float m_run = kNegBigC;
     int row_end = 0;                                   // exclusive causal end of this row
     long long qrow = -1;
     int chunk = 0, wmin_end = 0;
@@ -585,9 +596,8 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
         wmin_end = me;
         // q~ (fp16 hi + lo; first warp of the pair) and u (fp16; second) into this row's lane
         const float* src = qrow >= 0 ? a.qprep + qrow * qstride : nullptr;
-        float su = 0.0f;
-        if (QJL) {
-#pragma unroll
+        if (QJL && hh == 1) {
+#pragma unroll 1
           for (int hv = 0; hv < 4; ++hv) {
             uint32_t uh[16];
 #pragma unroll
@@ -595,17 +605,14 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
               const float4 x = src ? *reinterpret_cast<const float4*>(src + kD + 32 * hv + 4 * k4)
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
               const __half2 h0 = __floats2half2_rn(x.x, x.y), h1 = __floats2half2_rn(x.z, x.w);
-              const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
-              su += (f0.x + f0.y) + (f1.x + f1.y);
               uh[2 * k4] = *reinterpret_cast<const uint32_t*>(&h0);
               uh[2 * k4 + 1] = *reinterpret_cast<const uint32_t*>(&h1);
             }
-            if (hh == 1) tst16(trow + kTU + 16u * hv, uh);
+            tst16(trow + kTU + 16u * hv, uh);
           }
         }
-        ksu = kappa * su;
         if (hh == 0) {
-#pragma unroll
+#pragma unroll 1
           for (int hv = 0; hv < 4; ++hv) {
             uint32_t qh[16], ql[16];
 #pragma unroll
@@ -639,35 +646,19 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
       }
       tc_after();
       float x[32];
-      const uint32_t fac = sb + G::FAC + (seq & 1) * 768 + 128u * hh;
+      tld32(trow + kTS + 32u * hh, x);
+      tc_before();
+      __syncwarp();
+      if (lane == 0) bar_arrive(barx(G::kSEmpty));
+      {
+        const uint32_t fac = sb + G::FAC + (seq & 3) * 512 + 128u * hh;
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {                    // 16 tokens at a time
-        float s1[16], s2[16];
-        tld16(trow + kTS + 32u * hh + 16u * q, s1);
-        if (QJL) tld16(trow + kTS2 + 32u * hh + 16u * q, s2);
-        if (q == 1) {
-          tc_before();
-          __syncwarp();
-          if (lane == 0) bar_arrive(barx(G::kSEmpty));
-        }
-#pragma unroll
-        for (int j4 = 0; j4 < 4; ++j4) {
-          const int j = 16 * q + 4 * j4;
-          const uint4 fa4 = lds128(fac + 4 * j), bi4 = lds128(fac + 512 + 4 * j);
-          const float fa[4] = {__uint_as_float(fa4.x), __uint_as_float(fa4.y), __uint_as_float(fa4.z),
-                               __uint_as_float(fa4.w)};
-          const float bi[4] = {__uint_as_float(bi4.x), __uint_as_float(bi4.y), __uint_as_float(bi4.z),
-                               __uint_as_float(bi4.w)};
-          if (QJL) {
-            const uint4 fb4 = lds128(fac + 256 + 4 * j);
-            const float fb[4] = {__uint_as_float(fb4.x), __uint_as_float(fb4.y), __uint_as_float(fb4.z),
-                                 __uint_as_float(fb4.w)};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) x[j + i] = fmaf(fa[i], s1[4 * j4 + i], fmaf(fb[i], s2[4 * j4 + i] - ksu, bi[i]));
-          } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) x[j + i] = fmaf(fa[i], s1[4 * j4 + i], bi[i]);
-          }
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const uint4 fa = lds128(fac + 16 * j4), bi = lds128(fac + 256 + 16 * j4);
+          x[4 * j4] = fmaf(__uint_as_float(fa.x), x[4 * j4], __uint_as_float(bi.x));
+          x[4 * j4 + 1] = fmaf(__uint_as_float(fa.y), x[4 * j4 + 1], __uint_as_float(bi.y));
+          x[4 * j4 + 2] = fmaf(__uint_as_float(fa.z), x[4 * j4 + 2], __uint_as_float(bi.z));
+          x[4 * j4 + 3] = fmaf(__uint_as_float(fa.w), x[4 * j4 + 3], __uint_as_float(bi.w));
         }
       }
       const int pbase = d.p0 + 32 * hh;
@@ -707,7 +698,7 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
         m_run = mx;
       }
       if (!d.first && __any_sync(0xffffffffu, moved)) {   // warp-wide: the tensor-memory accesses are collective
-#pragma unroll
+#pragma unroll 1
         for (int q4 = 0; q4 < 4; ++q4) {
           float o[16];
           uint32_t ou[16];
@@ -739,7 +730,7 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
         }
         tc_after();
         float* dst = qrow >= 0 ? a.part + (qrow * nch + chunk) * (kD + 2) : nullptr;
-#pragma unroll
+#pragma unroll 1
         for (int q4 = 0; q4 < 4; ++q4) {
           float o[16];
           tld16(trow + kTO + 64u * hh + 16u * q4, o);

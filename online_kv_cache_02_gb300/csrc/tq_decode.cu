@@ -147,6 +147,99 @@ __global__ void __launch_bounds__(kQThreads) qprep_kernel(DecodeArgs a) {
   }
 }
 
+// [q~; u] = W q for many query rows (causal attention, no fragment output): a
+// block takes 64 rows x 128 outputs with the whole K = 128 staged in shared
+// memory (q transposed, the W^T slice); a thread holds 8 rows x 4 outputs, so
+// three 16-byte shared loads feed 32 FMAs.  Each output is summed over k in
+// order, as in qprep_kernel.
+constexpr int kQRRows = 64, kQROut = 128, kQRThreads = 256, kQRPad = kD + 4;
+constexpr int kQRSmem = (kQRRows * kQRPad + kD * kQROut) * 4;
+
+__global__ void __launch_bounds__(kQRThreads) qprep_rows_kernel(DecodeArgs a, long long nq) {
+  extern __shared__ __align__(16) float qsm[];
+  float(*qs)[kQRPad] = reinterpret_cast<float(*)[kQRPad]>(qsm);
+  float(*ws)[kQROut] = reinterpret_cast<float(*)[kQROut]>(qsm + kQRRows * kQRPad);
+  const int nout = kD + a.m;
+  const long long r0 = static_cast<long long>(blockIdx.x) * kQRRows;
+  const int c0 = blockIdx.y * kQROut;
+  const int tid = threadIdx.x;
+  pdl_trigger();
+  if (blockIdx.x == 0 && blockIdx.y == 0 && tid < 2 && a.sched) a.sched[tid] = 0;   // partials work counters
+  // every load of the block's W^T slice and q rows issued before the first store
+  {
+    float4 wv[kD * kQROut / 4 / kQRThreads];
+#pragma unroll
+    for (int it = 0; it < kD * kQROut / 4 / kQRThreads; ++it) {
+      const int v = tid + it * kQRThreads, k = v / (kQROut / 4), c = 4 * (v % (kQROut / 4));
+      wv[it] = c0 + c < nout ? *reinterpret_cast<const float4*>(a.tab.wt + static_cast<long long>(k) * nout + c0 + c)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float qv[kQRRows * kD / kQRThreads];                 // 32 values: row tid / 4, channels 32 (tid % 4) ..
+    const int qr = tid >> 2, qc = 32 * (tid & 3);
+    const bool in = r0 + qr < nq;
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+      if (a.f32) {
+        const float4 x0 = in ? *reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + (r0 + qr) * kD + qc + j)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 x1 = in ? *reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + (r0 + qr) * kD + qc + j + 4)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        qv[j] = x0.x; qv[j + 1] = x0.y; qv[j + 2] = x0.z; qv[j + 3] = x0.w;
+        qv[j + 4] = x1.x; qv[j + 5] = x1.y; qv[j + 6] = x1.z; qv[j + 7] = x1.w;
+      } else {
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (in) x = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + (r0 + qr) * kD + qc + j);
+        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          qv[j + 2 * e] = __uint_as_float(xs[e] << 16);
+          qv[j + 2 * e + 1] = __uint_as_float(xs[e] & 0xFFFF0000u);
+        }
+      }
+    }
+#pragma unroll
+    for (int it = 0; it < kD * kQROut / 4 / kQRThreads; ++it) {
+      const int v = tid + it * kQRThreads, k = v / (kQROut / 4), c = 4 * (v % (kQROut / 4));
+      *reinterpret_cast<float4*>(&ws[k][c]) = wv[it];
+    }
+#pragma unroll
+    for (int j = 0; j < 32; j += 4)
+      *reinterpret_cast<float4*>(&qs[qr][qc + j]) = make_float4(qv[j], qv[j + 1], qv[j + 2], qv[j + 3]);
+  }
+  __syncthreads();
+  const int tr = tid >> 5, to = tid & 31;          // rows 8 tr .. 8 tr + 7, outputs 4 to .. 4 to + 3
+  float acc[8][4];
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.0f;
+#pragma unroll 1
+  for (int k0 = 0; k0 < kD; k0 += 4) {
+    float4 w[4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) w[kk] = *reinterpret_cast<const float4*>(&ws[k0 + kk][4 * to]);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const float4 q4 = *reinterpret_cast<const float4*>(&qs[8 * tr + r][k0]);
+      const float qk[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        acc[r][0] = fmaf(w[kk].x, qk[kk], acc[r][0]);
+        acc[r][1] = fmaf(w[kk].y, qk[kk], acc[r][1]);
+        acc[r][2] = fmaf(w[kk].z, qk[kk], acc[r][2]);
+        acc[r][3] = fmaf(w[kk].w, qk[kk], acc[r][3]);
+      }
+    }
+  }
+  if (c0 + 4 * to < nout) {
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (r0 + 8 * tr + r < nq)
+        *reinterpret_cast<float4*>(a.qprep + (r0 + 8 * tr + r) * nout + c0 + 4 * to) =
+            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+  }
+}
+
 // Code of channel j from a vector's code words (the stored format of tq.h).
 __device__ __forceinline__ int code_at(const unsigned* rec, int bh, int bl, int split, int j) {
   const int grp = j < split ? 0 : 1;
@@ -485,6 +578,126 @@ __global__ void __launch_bounds__(kMThreads) merge_kernel(DecodeArgs a) {
   if (grp == 0) a.out[row * kD + j] = (part[0][j] + part[1][j]) + (part[2][j] + part[3][j]);
 }
 
+// Merge for many query rows (causal attention: B T Hq rows): a block takes 32
+// rows.  Each warp combines the chunk partials of four rows (log-sum-exp of
+// the chunk maxima, then the weighted sums; a lane holds four channels) into
+// o~ = acc / l in shared memory; then the block rotates its 32 rows back at
+// once, o = Pi^T o~, reading Pi once per 32 rows instead of once per row.
+constexpr int kMRRows = 32;
+constexpr int kMRThreads = 256;
+
+__global__ void __launch_bounds__(kMRThreads) merge_rows_kernel(DecodeArgs a, long long rows) {
+  pdl_wait();                          // the partials kernel before it has completed
+  __shared__ __align__(16) float os[kMRRows][kD + 4];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long r0 = static_cast<long long>(blockIdx.x) * kMRRows;
+  // a warp's four rows together, so that their loads are in flight at once;
+  // lane c holds chunk c's weight (chunks c, c + 32, ... in turn)
+  constexpr int R = kMRRows / (kMRThreads / 32);
+  const float* P[R];
+  int nc[R];
+  float M[R], l[R], acc[R][4];
+  int ncmax = 0;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const long long row = r0 + warp * R + i;
+    nc[i] = 0;
+    P[i] = a.part;
+    if (row < rows) {
+      // row (b, t, h) attends positions [0, seq_lens[b] + t]
+      int L = a.seq_lens[row / a.Hq / a.T] + static_cast<int>((row / a.Hq) % a.T) + 1;
+      L = L < 0 ? 0 : L;
+      L = L > a.max_seq_len ? a.max_seq_len : L;
+      L = L > a.maxp * kPage ? a.maxp * kPage : L;
+      nc[i] = min(a.nchunks, (L + a.chunk - 1) / a.chunk);
+      P[i] = a.part + row * a.nchunks * (kD + 2);
+    }
+    ncmax = max(ncmax, nc[i]);
+    M[i] = -INFINITY;
+    l[i] = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[i][c] = 0.0f;
+  }
+  for (int cb = 0; cb < ncmax; cb += 32) {
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      if (cb + lane < nc[i]) M[i] = fmaxf(M[i], P[i][static_cast<long long>(cb + lane) * (kD + 2)]);
+  }
+#pragma unroll
+  for (int i = 0; i < R; ++i) M[i] = warp_max(M[i]);
+  for (int cb = 0; cb < ncmax; cb += 32) {
+    float w[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      w[i] = 0.0f;
+      if (cb + lane < nc[i]) {
+        const float2 ml = *reinterpret_cast<const float2*>(P[i] + static_cast<long long>(cb + lane) * (kD + 2));
+        w[i] = exp2f(ml.x - M[i]);
+        l[i] = fmaf(w[i], ml.y, l[i]);
+      }
+    }
+    const int n = min(32, ncmax - cb);
+    for (int j0 = 0; j0 < n; j0 += 2) {
+      float2 x[R][2][2];
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+          const int c = cb + j0 + jj;
+          x[i][jj][0] = x[i][jj][1] = make_float2(0.f, 0.f);
+          if (j0 + jj < n && c < nc[i]) {
+            const float* pc = P[i] + static_cast<long long>(c) * (kD + 2) + 2 + 4 * lane;
+            x[i][jj][0] = *reinterpret_cast<const float2*>(pc);
+            x[i][jj][1] = *reinterpret_cast<const float2*>(pc + 2);
+          }
+        }
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+          const float wj = __shfl_sync(0xffffffffu, w[i], (j0 + jj) & 31);
+          acc[i][0] = fmaf(wj, x[i][jj][0].x, acc[i][0]);
+          acc[i][1] = fmaf(wj, x[i][jj][0].y, acc[i][1]);
+          acc[i][2] = fmaf(wj, x[i][jj][1].x, acc[i][2]);
+          acc[i][3] = fmaf(wj, x[i][jj][1].y, acc[i][3]);
+        }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const float lt = warp_sum(l[i]);
+    const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+    *reinterpret_cast<float4*>(&os[warp * R + i][4 * lane]) =
+        make_float4(acc[i][0] * inv, acc[i][1] * inv, acc[i][2] * inv, acc[i][3] * inv);
+  }
+  __syncthreads();
+  // thread: rows 4 rg .. 4 rg + 3, output channels 4 cg .. 4 cg + 3
+  const int rg = tid >> 5, cg = tid & 31;
+  float o[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) o[r][c] = 0.0f;
+#pragma unroll 4
+  for (int i = 0; i < kD; ++i) {
+    const float4 p = __ldg(reinterpret_cast<const float4*>(a.tab.pi + i * kD + 4 * cg));
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float x = os[4 * rg + r][i];
+      o[r][0] = fmaf(p.x, x, o[r][0]);
+      o[r][1] = fmaf(p.y, x, o[r][1]);
+      o[r][2] = fmaf(p.z, x, o[r][2]);
+      o[r][3] = fmaf(p.w, x, o[r][3]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const long long row = r0 + 4 * rg + r;
+    if (row < rows)
+      *reinterpret_cast<float4*>(a.out + row * kD + 4 * cg) = make_float4(o[r][0], o[r][1], o[r][2], o[r][3]);
+  }
+}
+
 template <int G>
 cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
   dim3 grid(a.nchunks, a.H, a.B);
@@ -496,7 +709,16 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
 
 cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
-  if (stages & TQ_STAGE_QPREP) {
+  if ((stages & TQ_STAGE_QPREP) && !a.qfrag && a.T > 0 && (reinterpret_cast<uintptr_t>(a.q) & 15) == 0) {
+    const long long nq = static_cast<long long>(a.B) * a.T * a.Hq;
+    const dim3 grid(static_cast<unsigned>((nq + kQRRows - 1) / kQRRows), static_cast<unsigned>((kD + a.m + kQROut - 1) / kQROut));
+    static std::atomic<unsigned long long> configured{0};   // q rows and the W^T slice take 99 KB
+    e = smem_attr_once(qprep_rows_kernel, kQRSmem, configured);
+    if (e != cudaSuccess) return e;
+    qprep_rows_kernel<<<grid, kQRThreads, kQRSmem, s>>>(a, nq);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  } else if (stages & TQ_STAGE_QPREP) {
     const dim3 grid(static_cast<unsigned>((static_cast<long long>(a.B) * (a.T > 0 ? a.T : 1) * a.Hq + kQP - 1) / kQP),
                     static_cast<unsigned>((kD + a.m + kQO - 1) / kQO));
     static std::atomic<unsigned long long> configured{0};   // the W slice and q rows take 49 KB
@@ -526,8 +748,14 @@ cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
     }
   }
   if (stages & TQ_STAGE_MERGE) {
-    e = launch_pdl(merge_kernel, dim3(static_cast<unsigned>(static_cast<long long>(a.B) * (a.T > 0 ? a.T : 1) * a.Hq)),
-                   dim3(kMThreads), 0, s, a);
+    if (a.T > 0) {
+      const long long rows = static_cast<long long>(a.B) * a.T * a.Hq;
+      e = launch_pdl(merge_rows_kernel, dim3(static_cast<unsigned>((rows + kMRRows - 1) / kMRRows)), dim3(kMRThreads),
+                     0, s, a, rows);
+    } else {
+      e = launch_pdl(merge_kernel, dim3(static_cast<unsigned>(static_cast<long long>(a.B) * a.Hq)), dim3(kMThreads), 0,
+                     s, a);
+    }
   }
   return e;
 }
