@@ -20,10 +20,10 @@
 //       causal end;
 //   online softmax per row (the running max moves only when a logit passes it
 //   by more than 3, so p ≤ 8 fits fp16);
-//   [O | l] += P [V'^ | 1]  (P = p as fp16 in tensor memory; V'^ = n_v/sqrt(d)
-//       times the values' centroids, transposed in shared memory, with a row of
-//       ones under it so that column 128 accumulates the softmax sum: M = 128,
-//       N = 144, K = 64 tokens).
+//   [O | l] += P [V' | 1]  (P = p as fp16 in tensor memory; V' = n_v/sqrt(d)
+//       times the values' centroids, token rows in shared memory read MN-major,
+//       with a column of ones beside it so that column 128 accumulates the
+//       softmax sum: M = 128, N = 144, K = 64 tokens).
 // Each item ends with the chunk partial (max, sum, O) of its 128 rows; the
 // decode's merge kernel combines the chunks and rotates back.
 //
@@ -33,9 +33,8 @@
 //   warp 1: tensor memory (496 of 512 columns) and, one lane, the MMAs;
 //   warps 4, 5, 16, 17: K^ and A' rows and the token factors (two buffers,
 //       free again once the tile's S MMAs have run);
-//   warps 2, 3, 6, 7: V'^ transposed (a table lookup per pair of consecutive
-//       tokens of one channel) and the ones row (two buffers, free again once
-//       the tile's O MMAs have run);
+//   warps 2, 3, 6, 7: V' rows and the ones column (two buffers, free again
+//       once the tile's O MMAs have run);
 //   (a warp runs on SMSP warp % 4: each SMSP holds two softmax warps and one
 //   side of the operand work, so that fewer code paths share its instruction
 //   cache)
@@ -67,7 +66,7 @@ constexpr int kCMaxChunk = 1024;          // an item's page ids: two per lane of
 constexpr int kCOpWarps = 8, kCEpWarps = 8;
 constexpr int kCThreadsTC = 32 * (2 + kCOpWarps + kCEpWarps);
 constexpr int kCStages = 3;
-constexpr int kCVN = 144;                 // V'^ rows: 128 channels, the ones row, 15 zero rows
+constexpr int kCVN = 144;                 // V' columns: 128 channels, the ones column, 15 zero columns
 constexpr float kInvSqrtDC = 0.08838834764831845f;
 constexpr float kSqrtHalfPiC = 1.2533141373155003f;
 constexpr float kLazyC = 3.0f;
@@ -104,8 +103,10 @@ struct CGeo {
   static constexpr int PAGE = KBB + VBB;           // a page: K block, then V block
   static constexpr int STAGE = 4 * PAGE;           // a tile
   // shared memory (offsets from a 1024-aligned base)
-  static constexpr int KH = 0, AS = 16384, VT = 32768;   // in an operand buffer: K^, A' [64][128], V'^ [144][64]
-  static constexpr int OPS_BYTES = VT + kCVN * 128;
+  // in an operand buffer: K^ and A' [64 tokens][128] K-major, V' [64 tokens][192] MN-major (three
+  // 64-channel blocks of [64][128 B]; the third holds the ones column and zeros)
+  static constexpr int KH = 0, AS = 16384, VT = 32768;
+  static constexpr int OPS_BYTES = VT + 3 * 64 * 128;
   static constexpr int OPS = 0;
   static constexpr int LUT = OPS + 2 * OPS_BYTES;
   static constexpr int REC = LUT + kLutBytes;
@@ -138,19 +139,6 @@ __device__ __forceinline__ uint32_t chunk_bytes_c(const uint32_t (&w)[17], int b
   const uint32_t x = stream_bits_c(w, base + 16 * cc) & 0xFFFFu;
   return (x & 0xFu) | ((x & 0xF0u) << 4) | ((x & 0xF00u) << 8) | ((x & 0xF000u) << 12);
 }
-// Pair index of channel c (0..7) of an 8-channel chunk from two tokens' code
-// words xa (token 2i) and xb (2i + 1), each holding channel c in nibble c (B =
-// 3, 4: code in the low bits) or in bits 2c .. 2c + 1 (B = 2): token a's code
-// in the low bits of the index.
-template <int B>
-__device__ __forceinline__ uint32_t v_pair_c(uint32_t xa, uint32_t xb, int c) {
-  if (B == 2) {
-    const uint32_t ca = (xa >> (2 * c)) & 3u, cb = (xb >> (2 * c)) & 3u;
-    return ca | (cb << 2);
-  }
-  return ((xa >> (4 * c)) & 15u) | (((xb >> (4 * c)) & 15u) << 4);
-}
-
 // K^ rows of one 64-channel half (B-bit codes at `src`, 8 B bytes) for token
 // row t: the fp16 centroid of every channel, zero for an invalid token.  The
 // chunk loop stays rolled: the kernel's roles share each SM's instruction
@@ -180,50 +168,45 @@ __device__ __forceinline__ void k_half_rows(uint32_t tile, uint32_t src, int t, 
   }
 }
 
-// V'^ for channels 8 cg .. 8 cg + 7 (B-bit codes of the group starting at
-// stream bit `base`) and tokens 8 tg .. 8 tg + 7 of the tile: one table lookup
-// per (channel, pair of tokens), times the pair's n_v/sqrt(d); zero for a
-// token that is not there.  The channel loop stays rolled (instruction cache).
+// V' rows of one 64-channel half (B-bit codes at `src`) for token row t: the
+// fp16 centroid of every channel times the token's n_v/sqrt(d) (f2), zero for
+// an invalid token.  As the K^ rows; the O MMA reads this operand MN-major.
 template <int B>
-__device__ __forceinline__ void v_cols(uint32_t vt, uint32_t rec, const CDesc& d, int cg, int tg, int base, int cbv,
-                                       int kbb, int v_norm, int page, uint32_t tb) {
-  const int off = base + B * 8 * (cg & 7), wi = off >> 5, sh = off & 31;
-  const bool two = sh != 0 && 4 * (wi + 1) < cbv;
-  uint32_t xw[8];
-  __half2 f2[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float fv[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int t = 8 * tg + 2 * i + e, pg = t >> 4, slot = t & 15;
-      uint32_t x = 0u;
-      fv[e] = 0.0f;
-      if (t < d.npos && ((d.mask >> pg) & 1u)) {
-        const uint32_t vb = rec + pg * page + kbb;
-        const uint32_t src = vb + slot * cbv + 4 * wi;
-        const uint32_t lo = lds32(src);
-        const uint32_t hi = two ? lds32(src + 4) : 0u;
-        x = sh ? __funnelshift_r(lo, hi, sh) : lo;
-        if (B == 3) x = octet_nibbles_c(x);
-        if (B == 2) x &= 0xFFFFu;
-        fv[e] = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(vb + v_norm + 2 * slot)))) * kInvSqrtDC;
-      }
-      xw[2 * i + e] = x;
-    }
-    f2[i] = __floats2half2_rn(fv[0], fv[1]);
-  }
+__device__ __forceinline__ void v_half_rows(uint32_t tile, uint32_t src, int t, int hf, bool tv, uint32_t tb,
+                                            __half2 f2) {
 #pragma unroll 1
-  for (int c = 0; c < 8; ++c) {
-    uint32_t w4[4];
+  for (int cc = 0; cc < 8; ++cc) {
+    uint32_t p[4] = {0u, 0u, 0u, 0u};
+    if (tv) {
+      const int off = B * 8 * cc, wi = off >> 5, sh = off & 31;
+      const uint32_t lo = lds32(src + 4 * wi);
+      uint32_t x;
+      if (B == 4) {
+        x = lo;
+      } else if (B == 3) {
+        const uint32_t hi = sh > 8 ? lds32(src + 4 * wi + 4) : 0u;
+        x = octet_nibbles_c(sh ? __funnelshift_r(lo, hi, sh) : lo);
+      } else {
+        const uint32_t y = (lo >> sh) & 0xFFFFu;
+        x = (y & 0xFu) | ((y & 0xF0u) << 4) | ((y & 0xF00u) << 8) | ((y & 0xF000u) << 12);
+      }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t e8 = lds32(tb + v_pair_c<B>(xw[2 * i], xw[2 * i + 1], c) * 128u);
-      const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&e8), f2[i]);
-      w4[i] = *reinterpret_cast<const uint32_t*>(&r);
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t e = lds32(tb + ((x >> (8 * i)) & 0xFFu) * 128u);
+        const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&e), f2);
+        p[i] = *reinterpret_cast<const uint32_t*>(&r);
+      }
     }
-    sts128(vt + chunk_off(8 * cg + c, tg, kCVN), w4[0], w4[1], w4[2], w4[3]);
+    sts128(tile + chunk_off(t, 8 * hf + cc, kCT), p[0], p[1], p[2], p[3]);
   }
+}
+
+// Shared-memory descriptor of an MN-major operand with 128-byte swizzle: rows
+// of 64 MN elements (128 B) along K, 8-row groups 1024 B apart, 64-element MN
+// blocks 8192 B apart.
+__device__ __forceinline__ uint64_t sdesc_mn(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(8192 >> 4) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
 template <int KBH, int KBL, int VBH, int VBL, bool QJL>
@@ -292,11 +275,6 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
         v = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(clo))) |
             (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(chi))) << 16);
       *reinterpret_cast<uint32_t*>(sm + G::LUT + off) = v;
-    }
-    // rows 129 .. 143 of V'^ stay zero (row 128, the ones, is written per tile)
-    for (int i = tid; i < 2 * (kCVN - 129) * 8; i += kCThreadsTC) {
-      const int buf = i / ((kCVN - 129) * 8), rc = i % ((kCVN - 129) * 8);
-      sts128(sb + G::OPS + buf * G::OPS_BYTES + G::VT + chunk_off(129 + rc / 8, rc % 8, kCVN), 0u, 0u, 0u, 0u);
     }
     if (tid == 0) {
       for (int s = 0; s < kCStages; ++s) {
@@ -413,7 +391,7 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
     // operands and the release of S(k) come early in tile k), except that an item's
     // first S waits for its queries, which follow O(k) of the item before --------------
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_f16(kCT), id_o = idesc_f16(kCVN);
+      constexpr uint32_t id_s = idesc_f16(kCT), id_o = idesc_f16(kCVN) | (1u << 16);   // O: B MN-major
       auto issue_s = [&](int k) {
         const uint32_t kh = sb + G::OPS + (k & 1) * G::OPS_BYTES + G::KH, as = kh - G::KH + G::AS;
         tc_after();
@@ -433,7 +411,7 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
         tc_after();
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          mma_ts(tmem + kTO, tmem + kTP + 8u * j, kdesc(vt, kCVN, j), id_o, (first && j == 0) ? 0u : 1u);
+          mma_ts(tmem + kTO, tmem + kTP + 8u * j, sdesc_mn(vt + 2048u * j), id_o, (first && j == 0) ? 0u : 1u);
         mma_commit(barx(G::kODone));
         mma_commit(barx(G::kVFree + (k & 1)));
       };
@@ -539,23 +517,21 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
           if (d.item >= 0) bar_arrive(barx(G::kRecEmpty + s));
         }
       } else if (d.item >= 0) {
-        const int v = u - 128;                         // channel block v / 8 (group v / 64), token block v % 8
-        if (v < 64)
-          v_cols<VBH>(ob + G::VT, rec, d, v >> 3, v & 7, 0, G::CBV, G::KBB, G::V_NORM, G::PAGE,
-                      sb + G::LUT + lut_off(VBH) + lane_off);
-        else
-          v_cols<VBL>(ob + G::VT, rec, d, v >> 3, v & 7, 64 * VBH, G::CBV, G::KBB, G::V_NORM, G::PAGE,
-                      sb + G::LUT + lut_off(VBL) + lane_off);
-        if (v < 8) {                                   // the ones row: 1 for a token that is there
-          uint32_t w4[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int ta = 8 * v + 2 * i, tb2 = ta + 1;
-            const bool va = ta < d.npos && ((d.mask >> (ta >> 4)) & 1u);
-            const bool vb2 = tb2 < d.npos && ((d.mask >> (tb2 >> 4)) & 1u);
-            w4[i] = (va ? 0x3C00u : 0u) | (vb2 ? 0x3C000000u : 0u);
-          }
-          sts128(ob + G::VT + chunk_off(128, v, kCVN), w4[0], w4[1], w4[2], w4[3]);
+        const int pg = t >> 4, slot = t & 15;
+        const bool tv = t < d.npos && ((d.mask >> pg) & 1u);
+        const uint32_t vb = rec + pg * G::PAGE + G::KBB;
+        float fv = 0.0f;
+        if (tv)
+          fv = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(vb + G::V_NORM + 2 * slot)))) * kInvSqrtDC;
+        const __half2 fv2 = __float2half2_rn(fv);
+        if (hf == 0) {
+          v_half_rows<VBH>(ob + G::VT, vb + slot * G::CBV, t, 0, tv, sb + G::LUT + lut_off(VBH) + lane_off, fv2);
+          // channels 128 .. 143: 1 in channel 128 for a token that is there, else 0
+          sts128(ob + G::VT + chunk_off(t, 16, kCT), tv ? 0x3C00u : 0u, 0u, 0u, 0u);
+          sts128(ob + G::VT + chunk_off(t, 17, kCT), 0u, 0u, 0u, 0u);
+        } else {
+          v_half_rows<VBL>(ob + G::VT, vb + slot * G::CBV + 8 * VBH, t, 1, tv, sb + G::LUT + lut_off(VBL) + lane_off,
+                           fv2);
         }
         fence_async_smem();
         __syncwarp();
