@@ -773,7 +773,8 @@ extern "C" tq_status tq_causal_attention(const tq_ctx* ctx, const void* q, tq_dt
   a.out = out;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (!tc) return cuda_status(launch_decode(a, TQ_STAGE_ALL, st));
-  a.qfrag = nullptr;                  // the tensor-core kernel reads the fp32 q~/u rows
+  a.qfrag = nullptr;
+  a.qhalf = 1;                        // the tensor-core kernel reads q~/u as fp16 words in column order
   cudaError_t e = launch_decode(a, TQ_STAGE_QPREP, st);
   if (e == cudaSuccess) e = launch_causal_tc(a, nqb, st);
   if (e == cudaSuccess) e = launch_decode(a, TQ_STAGE_MERGE, st);

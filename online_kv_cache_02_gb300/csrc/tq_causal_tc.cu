@@ -87,8 +87,11 @@ struct CDesc {                 // one tile of the stream
   int tile, last, first;
   int p0, npos;                // first position, positions in the tile (<= 64)
   unsigned mask;               // valid pages (4 bits)
-  int pad;
+  int b, h, qb, chunk;         // the item: sequence, KV head, query block, chunk
+  int start;                   // the sequence's first new position
+  int pad[4];
 };
+static_assert(sizeof(CDesc) == 64, "descriptor size");
 
 template <int KBH, int KBL, int VBH, int VBL, bool QJL>
 struct CGeo {
@@ -113,7 +116,7 @@ struct CGeo {
   static constexpr int FAC = (REC + kCStages * STAGE + 1023) & ~1023;   // [4][fa | bias][64] floats
   static constexpr int XMAX = FAC + 4 * 2 * 64 * 4;                     // [2][2][128] partial row maxima
   static constexpr int DESC = XMAX + 2 * 2 * 128 * 4;                   // [4] CDesc + [kCStages] CDesc
-  static constexpr int BAR = DESC + (4 + kCStages) * 32;
+  static constexpr int BAR = DESC + (4 + kCStages) * 64;
   static constexpr int kRecFull = 0, kRecEmpty = 3, kKOps = 6, kVOps = 8, kKFree = 10, kVFree = 12,
                        kDescFull = 14, kSFull = 18, kSEmpty = 19, kPFull = 20, kODone = 21, kQReady = 22,
                        kDrain = 23, kXch = 24, kNumBar = 32;  // kXch + 2 q + parity: the row-max exchange of pair q
@@ -199,6 +202,13 @@ __device__ __forceinline__ void v_half_rows(uint32_t tile, uint32_t src, int t, 
     }
     sts128(tile + chunk_off(t, 8 * hf + cc, kCT), p[0], p[1], p[2], p[3]);
   }
+}
+
+// 2^x by the SFU (ex2.approx.ftz: relative error about 2^-22; -inf gives 0).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Shared-memory descriptor of an MN-major operand with 128-byte swizzle: rows
@@ -311,11 +321,11 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
   const uint32_t tmem = *reinterpret_cast<const uint32_t*>(sm + G::TMEMA);
   bool failed = false;
   CDesc* desc = reinterpret_cast<CDesc*>(sm + G::DESC);                // per tile of the stream (4)
-  CDesc* rec_desc = reinterpret_cast<CDesc*>(sm + G::DESC + 4 * 32);   // per record stage
+  CDesc* rec_desc = reinterpret_cast<CDesc*>(sm + G::DESC + 4 * 64);   // per record stage
 
   if (warp == 0) {
     // ---- producer: items, page ids, the tile's page blocks ----------------------------
-    int seq = 0, item = -1, ntile = 0, tile = 0, b = 0, h = 0, c0 = 0, c1 = 0;
+    int seq = 0, item = -1, ntile = 0, tile = 0, b = 0, h = 0, qb = 0, chunk = 0, c0 = 0, c1 = 0;
     int pid0 = -1, pid1 = -1;            // page ids 2 lane, 2 lane + 1 of the item (from page c0 / 16)
     for (;; ++seq) {
       const int s = seq % kCStages;
@@ -334,7 +344,6 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
           item = -2;
           break;
         }
-        int qb, chunk;
         item_range(it, b, h, qb, chunk, c0, c1);
         if (c1 <= c0) continue;
         item = it;
@@ -354,6 +363,11 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
         d.last = tile == ntile - 1;
         d.p0 = c0 + kCT * tile;
         d.npos = min(kCT, c1 - d.p0);
+        d.b = b;
+        d.h = h;
+        d.qb = qb;
+        d.chunk = chunk;
+        d.start = a.seq_lens[b];
       }
       // the tile's pages: lane j < 4 takes page j of the tile
       const int pg = (d.item >= 0 ? (d.p0 - c0) >> 4 : 0) + (lane & 3);
@@ -561,51 +575,56 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
       const CDesc d = desc[seq & 3];
       if (d.item < 0) break;
       if (d.first) {
-        int b, h, qb, c0, c1;
-        item_range(d.item, b, h, qb, chunk, c0, c1);
-        const int rr = kCR * qb + r;                   // row t G + g among the sequence's new tokens
-        qrow = rr < rows_all ? (static_cast<long long>(b) * a.T + rr / a.G) * a.Hq + h * a.G + rr % a.G : -1;
-        row_end = rr < rows_all ? a.seq_lens[b] + rr / a.G + 1 : 0;
+        chunk = d.chunk;
+        const int rr = kCR * d.qb + r;                 // row t G + g among the sequence's new tokens
+        qrow = rr < rows_all ? (static_cast<long long>(d.b) * a.T + rr / a.G) * a.Hq + d.h * a.G + rr % a.G : -1;
+        row_end = rr < rows_all ? d.start + rr / a.G + 1 : 0;
         int me = rr < rows_all ? row_end : 0x7FFFFFFF;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) me = min(me, __shfl_xor_sync(0xffffffffu, me, o));
         wmin_end = me;
-        // q~ (fp16 hi + lo; first warp of the pair) and u (fp16; second) into this row's lane
-        const float* src = qrow >= 0 ? a.qprep + qrow * qstride : nullptr;
-        if (QJL && hh == 1) {
-#pragma unroll 1
-          for (int hv = 0; hv < 4; ++hv) {
-            uint32_t uh[16];
+        // this row's q~ hi/lo and u words (written by the query prep in column order), half
+        // hh of each: columns 32 hh .. 32 hh + 31 of the three blocks
+        const uint4* src = qrow >= 0 ? reinterpret_cast<const uint4*>(a.qprep + qrow * qstride) : nullptr;
+        {
+          uint4 x[16];
 #pragma unroll
-            for (int k4 = 0; k4 < 8; ++k4) {
-              const float4 x = src ? *reinterpret_cast<const float4*>(src + kD + 32 * hv + 4 * k4)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-              const __half2 h0 = __floats2half2_rn(x.x, x.y), h1 = __floats2half2_rn(x.z, x.w);
-              uh[2 * k4] = *reinterpret_cast<const uint32_t*>(&h0);
-              uh[2 * k4 + 1] = *reinterpret_cast<const uint32_t*>(&h1);
-            }
-            tst16(trow + kTU + 16u * hv, uh);
+          for (int i = 0; i < 8; ++i) {
+            x[i] = src ? src[8 * hh + i] : make_uint4(0u, 0u, 0u, 0u);
+            x[8 + i] = src ? src[16 + 8 * hh + i] : make_uint4(0u, 0u, 0u, 0u);
           }
-        }
-        if (hh == 0) {
-#pragma unroll 1
-          for (int hv = 0; hv < 4; ++hv) {
-            uint32_t qh[16], ql[16];
 #pragma unroll
-            for (int k4 = 0; k4 < 8; ++k4) {
-              const float4 x = src ? *reinterpret_cast<const float4*>(src + 32 * hv + 4 * k4)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-              const __half2 h0 = __floats2half2_rn(x.x, x.y), h1 = __floats2half2_rn(x.z, x.w);
-              const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
-              const __half2 l0 = __floats2half2_rn(x.x - f0.x, x.y - f0.y);
-              const __half2 l1 = __floats2half2_rn(x.z - f1.x, x.w - f1.y);
-              qh[2 * k4] = *reinterpret_cast<const uint32_t*>(&h0);
-              qh[2 * k4 + 1] = *reinterpret_cast<const uint32_t*>(&h1);
-              ql[2 * k4] = *reinterpret_cast<const uint32_t*>(&l0);
-              ql[2 * k4 + 1] = *reinterpret_cast<const uint32_t*>(&l1);
+          for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+            for (int h16 = 0; h16 < 2; ++h16) {
+              uint32_t w[16];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint4 v = x[8 * blk + 4 * h16 + i];
+                w[4 * i] = v.x;
+                w[4 * i + 1] = v.y;
+                w[4 * i + 2] = v.z;
+                w[4 * i + 3] = v.w;
+              }
+              tst16(trow + (blk ? kTQL : kTQH) + 32u * hh + 16u * h16, w);
             }
-            tst16(trow + kTQH + 16u * hv, qh);
-            tst16(trow + kTQL + 16u * hv, ql);
+        }
+        if (QJL) {
+          uint4 x[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[i] = src ? src[32 + 8 * hh + i] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int h16 = 0; h16 < 2; ++h16) {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint4 v = x[4 * h16 + i];
+              w[4 * i] = v.x;
+              w[4 * i + 1] = v.y;
+              w[4 * i + 2] = v.z;
+              w[4 * i + 3] = v.w;
+            }
+            tst16(trow + kTU + 32u * hh + 16u * h16, w);
           }
         }
         tst_wait();
@@ -690,7 +709,7 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
       uint32_t pp[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
-        const __half2 h2 = __floats2half2_rn(exp2f(x[2 * k] - m_run), exp2f(x[2 * k + 1] - m_run));
+        const __half2 h2 = __floats2half2_rn(ex2_ftz(x[2 * k] - m_run), ex2_ftz(x[2 * k + 1] - m_run));
         pp[k] = *reinterpret_cast<const uint32_t*>(&h2);
       }
       tst16(trow + kTP + 16u * hh, pp);

@@ -177,9 +177,13 @@ __global__ void __launch_bounds__(kQRThreads) qprep_rows_kernel(DecodeArgs a, lo
     float qv[kQRRows * kD / kQRThreads];                 // 32 values: row tid / 4, channels 32 (tid % 4) ..
     const int qr = tid >> 2, qc = 32 * (tid & 3);
     const bool in = r0 + qr < nq;
+    const bool vec = (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
 #pragma unroll
     for (int j = 0; j < 32; j += 8) {
-      if (a.f32) {
+      if (!vec) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qv[j + e] = in ? load_q(a.q, a.f32, (r0 + qr) * kD + qc + j + e) : 0.0f;
+      } else if (a.f32) {
         const float4 x0 = in ? *reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + (r0 + qr) * kD + qc + j)
                              : make_float4(0.f, 0.f, 0.f, 0.f);
         const float4 x1 = in ? *reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + (r0 + qr) * kD + qc + j + 4)
@@ -231,12 +235,29 @@ __global__ void __launch_bounds__(kQRThreads) qprep_rows_kernel(DecodeArgs a, lo
       }
     }
   }
-  if (c0 + 4 * to < nout) {
+  if (c0 + 4 * to >= nout) return;
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
-      if (r0 + 8 * tr + r < nq)
-        *reinterpret_cast<float4*>(a.qprep + (r0 + 8 * tr + r) * nout + c0 + 4 * to) =
-            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+  for (int r = 0; r < 8; ++r) {
+    if (r0 + 8 * tr + r >= nq) continue;
+    float* row = a.qprep + (r0 + 8 * tr + r) * nout;
+    if (!a.qhalf) {
+      *reinterpret_cast<float4*>(row + c0 + 4 * to) = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      continue;
+    }
+    // fp16 words in tensor-memory column order: q~ hi pairs at 0, q~ lo pairs at 64, u pairs at 128
+    uint32_t* w = reinterpret_cast<uint32_t*>(row);
+    const __half2 h0 = __floats2half2_rn(acc[r][0], acc[r][1]), h1 = __floats2half2_rn(acc[r][2], acc[r][3]);
+    const int pw = (c0 + 4 * to) / 2;
+    if (c0 + 4 * to < kD) {
+      const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+      const __half2 l0 = __floats2half2_rn(acc[r][0] - f0.x, acc[r][1] - f0.y);
+      const __half2 l1 = __floats2half2_rn(acc[r][2] - f1.x, acc[r][3] - f1.y);
+      *reinterpret_cast<uint2*>(w + pw) = make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+      *reinterpret_cast<uint2*>(w + 64 + pw) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&l0), *reinterpret_cast<const uint32_t*>(&l1));
+    } else {
+      *reinterpret_cast<uint2*>(w + 64 + pw) = make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+    }
   }
 }
 
@@ -709,7 +730,7 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
 
 cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
-  if ((stages & TQ_STAGE_QPREP) && !a.qfrag && a.T > 0 && (reinterpret_cast<uintptr_t>(a.q) & 15) == 0) {
+  if ((stages & TQ_STAGE_QPREP) && a.qhalf) {
     const long long nq = static_cast<long long>(a.B) * a.T * a.Hq;
     const dim3 grid(static_cast<unsigned>((nq + kQRRows - 1) / kQRRows), static_cast<unsigned>((kD + a.m + kQROut - 1) / kQROut));
     static std::atomic<unsigned long long> configured{0};   // q rows and the W^T slice take 99 KB

@@ -134,6 +134,10 @@ struct DecodeArgs {
   // kernel takes query rows eight at a time (nqb blocks per sequence and KV head)
   int T;
   int nqb;
+  // 1: qprep writes each row as fp16 words in tensor-memory column order
+  // (64 of q~ hi pairs, 64 of q~ lo pairs, 64 of u pairs) for the tensor-core
+  // causal kernel, instead of the fp32 [q~; u]
+  int qhalf;
 };
 
 // Opt kernel `fn` into `bytes` of dynamic shared memory on the current device,
