@@ -461,6 +461,13 @@ tq_status quantize_impl(const tq_ctx* ctx, const void* k, const void* v, tq_dtyp
 namespace {
 int nchunks_for(int max_seq_len, int chunk) { return max_seq_len <= 0 ? 1 : (max_seq_len + chunk - 1) / chunk; }
 
+// Causal attention on the tensor cores: fp16 query words (48 x 16 B per block
+// row), partials (130 floats per block row and chunk), the work counters.
+size_t causal_tc_ws_bytes(long long nblk, int nch) {
+  return align256(static_cast<size_t>(nblk) * 128 * 48 * 16) +
+         align256(static_cast<size_t>(nblk) * nch * (kD + 2) * 128 * sizeof(float)) + 256;
+}
+
 size_t ws_bytes(int B, int Hq, int d, int m, int nch) {
   return align256(sizeof(float) * static_cast<size_t>(B) * Hq * (d + m)) +
          align256(sizeof(float) * static_cast<size_t>(B) * Hq * nch * (d + 2)) +
@@ -694,6 +701,12 @@ extern "C" tq_status tq_causal_workspace_size(const tq_ctx* ctx, int batch, int 
   if (!ctx || !bytes || batch < 0 || n_new < 1 || Hq < 1 || max_seq_len < n_new || chunk_tokens < 0 ||
       chunk_tokens % kPage)
     return TQ_ERR_INVALID_ARG;
+  if (causal_tc_supported(ctx->kl, ctx->vl, ctx->cfg.m) && chunk_tokens <= causal_tc_max_chunk()) {
+    // tensor-core path: at most Hq ceil(n_new / 128) query blocks per sequence, chunks of at least 256
+    const long long nblk = static_cast<long long>(batch) * Hq * ((n_new + 127) / 128);
+    *bytes = causal_tc_ws_bytes(nblk, nchunks_for(max_seq_len, chunk_tokens ? chunk_tokens : 256));
+    return TQ_OK;
+  }
   const int chunk = chunk_tokens ? chunk_tokens : 64;   // the smallest automatic chunk
   *bytes = ws_bytes(static_cast<int>(static_cast<long long>(batch) * n_new), Hq, ctx->cfg.d, ctx->cfg.m,
                     nchunks_for(max_seq_len, chunk));
@@ -735,7 +748,9 @@ extern "C" tq_status tq_causal_attention(const tq_ctx* ctx, const void* q, tq_dt
   }
   const int nch = nchunks_for(max_seq_len, chunk);
   const int d = ctx->cfg.d, m = ctx->cfg.m;
-  if (workspace_bytes < ws_bytes(static_cast<int>(rows), Hq, d, m, nch)) return TQ_ERR_WORKSPACE;
+  const long long nblk = static_cast<long long>(batch) * H * nqb;
+  if (workspace_bytes < (tc ? causal_tc_ws_bytes(nblk, nch) : ws_bytes(static_cast<int>(rows), Hq, d, m, nch)))
+    return TQ_ERR_WORKSPACE;
   if (static_cast<long long>(batch) * H * nqb * nch > (1LL << 30) || nch > 65535) return TQ_ERR_UNSUPPORTED;
   DecodeArgs a{};
   a.q = q;
@@ -774,7 +789,11 @@ extern "C" tq_status tq_causal_attention(const tq_ctx* ctx, const void* q, tq_dt
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (!tc) return cuda_status(launch_decode(a, TQ_STAGE_ALL, st));
   a.qfrag = nullptr;
-  a.qhalf = 1;                        // the tensor-core kernel reads q~/u as fp16 words in column order
+  a.qhalf = 1;                        // fp16 query words and partials stored by query block
+  a.qprep = reinterpret_cast<float*>(w);
+  a.part = reinterpret_cast<float*>(w + align256(static_cast<size_t>(nblk) * 128 * 48 * 16));
+  a.sched = reinterpret_cast<int*>(reinterpret_cast<char*>(a.part) +
+                                   align256(static_cast<size_t>(nblk) * nch * (kD + 2) * 128 * sizeof(float)));
   cudaError_t e = launch_decode(a, TQ_STAGE_QPREP, st);
   if (e == cudaSuccess) e = launch_causal_tc(a, nqb, st);
   if (e == cudaSuccess) e = launch_decode(a, TQ_STAGE_MERGE, st);

@@ -561,10 +561,9 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
     const int e = warp - 8;                            // 0 .. 7
     const int wq = warp & 3, hh = e >> 2, r = 32 * wq + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * wq) << 16);
-    const int qstride = kD + a.m;
     float m_run = kNegBigC;
     int row_end = 0;                                   // exclusive causal end of this row
-    long long qrow = -1;
+    long long blk = 0;                                 // the item's query block (b H + h) nqb + qb
     int chunk = 0, wmin_end = 0;
     for (int seq = 0;; ++seq) {
       bool ok = bar_wait(barx(G::kDescFull + (seq & 3)), (seq >> 2) & 1, failed);
@@ -577,7 +576,6 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
       if (d.first) {
         chunk = d.chunk;
         const int rr = kCR * d.qb + r;                 // row t G + g among the sequence's new tokens
-        qrow = rr < rows_all ? (static_cast<long long>(d.b) * a.T + rr / a.G) * a.Hq + d.h * a.G + rr % a.G : -1;
         row_end = rr < rows_all ? d.start + rr / a.G + 1 : 0;
         int me = rr < rows_all ? row_end : 0x7FFFFFFF;
 #pragma unroll
@@ -585,34 +583,35 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
         wmin_end = me;
         // this row's q~ hi/lo and u words (written by the query prep in column order), half
         // hh of each: columns 32 hh .. 32 hh + 31 of the three blocks
-        const uint4* src = qrow >= 0 ? reinterpret_cast<const uint4*>(a.qprep + qrow * qstride) : nullptr;
+        blk = (static_cast<long long>(d.b) * a.H + d.h) * nqb + d.qb;
+        const uint4* src = rr < rows_all ? reinterpret_cast<const uint4*>(a.qprep) + blk * 48 * 128 + r : nullptr;
         {
           uint4 x[16];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            x[i] = src ? src[8 * hh + i] : make_uint4(0u, 0u, 0u, 0u);
-            x[8 + i] = src ? src[16 + 8 * hh + i] : make_uint4(0u, 0u, 0u, 0u);
+            x[i] = src ? src[(8 * hh + i) * 128] : make_uint4(0u, 0u, 0u, 0u);
+            x[8 + i] = src ? src[(16 + 8 * hh + i) * 128] : make_uint4(0u, 0u, 0u, 0u);
           }
 #pragma unroll
-          for (int blk = 0; blk < 2; ++blk)
+          for (int bk = 0; bk < 2; ++bk)
 #pragma unroll
             for (int h16 = 0; h16 < 2; ++h16) {
               uint32_t w[16];
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                const uint4 v = x[8 * blk + 4 * h16 + i];
+                const uint4 v = x[8 * bk + 4 * h16 + i];
                 w[4 * i] = v.x;
                 w[4 * i + 1] = v.y;
                 w[4 * i + 2] = v.z;
                 w[4 * i + 3] = v.w;
               }
-              tst16(trow + (blk ? kTQL : kTQH) + 32u * hh + 16u * h16, w);
+              tst16(trow + (bk ? kTQL : kTQH) + 32u * hh + 16u * h16, w);
             }
         }
         if (QJL) {
           uint4 x[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) x[i] = src ? src[32 + 8 * hh + i] : make_uint4(0u, 0u, 0u, 0u);
+          for (int i = 0; i < 8; ++i) x[i] = src ? src[(32 + 8 * hh + i) * 128] : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
           for (int h16 = 0; h16 < 2; ++h16) {
             uint32_t w[16];
@@ -724,20 +723,19 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
           break;
         }
         tc_after();
-        float* dst = qrow >= 0 ? a.part + (qrow * nch + chunk) * (kD + 2) : nullptr;
+        // stored by query block, row-minor: a warp's stores are 128 contiguous bytes
+        float* dst = a.part + ((blk * nch + chunk) * (kD + 2)) * 128 + r;
 #pragma unroll 1
         for (int q4 = 0; q4 < 4; ++q4) {
           float o[16];
           tld16(trow + kTO + 64u * hh + 16u * q4, o);
-          if (dst) {
 #pragma unroll
-            for (int k = 0; k < 16; k += 2)
-              *reinterpret_cast<float2*>(dst + 2 + 64 * hh + 16 * q4 + k) = make_float2(o[k], o[k + 1]);
-          }
+          for (int k = 0; k < 16; ++k) dst[(2 + 64 * hh + 16 * q4 + k) * 128] = o[k];
         }
         if (hh == 0) {
           const float l = __uint_as_float(tld1(trow + kTO + 128u));
-          if (dst) *reinterpret_cast<float2*>(dst) = make_float2(m_run, l);
+          dst[0] = m_run;
+          dst[128] = l;
         }
         tc_before();
       }

@@ -147,25 +147,34 @@ __global__ void __launch_bounds__(kQThreads) qprep_kernel(DecodeArgs a) {
   }
 }
 
-// [q~; u] = W q for many query rows (causal attention, no fragment output): a
-// block takes 64 rows x 128 outputs with the whole K = 128 staged in shared
-// memory (q transposed, the W^T slice); a thread holds 8 rows x 4 outputs, so
-// three 16-byte shared loads feed 32 FMAs.  Each output is summed over k in
-// order, as in qprep_kernel.
+// [q~; u] = W q for the tensor-core causal kernel, by query block: a CTA
+// takes 64 rows r of one block (block rows r = t G + g of one sequence and KV
+// head) x 128 outputs (q~, or u), with the whole K = 128 staged in shared
+// memory; a thread holds 8 rows x 4 outputs, so three 16-byte shared loads feed
+// 32 FMAs, each output summed over k in order as in qprep_kernel.  The outputs
+// leave as fp16 words in tensor-memory column order (q~ hi pairs 0..63, q~ lo
+// pairs 64..127, u pairs 128..191), word w of block row r at uint4
+// (blk 48 + w / 4) 128 + r: restaged in shared memory so that the stores, like
+// the causal kernel's loads (lane = block row), are 512 contiguous bytes.
 constexpr int kQRRows = 64, kQROut = 128, kQRThreads = 256, kQRPad = kD + 4;
 constexpr int kQRSmem = (kQRRows * kQRPad + kD * kQROut) * 4;
 
-__global__ void __launch_bounds__(kQRThreads) qprep_rows_kernel(DecodeArgs a, long long nq) {
+__global__ void __launch_bounds__(kQRThreads) qprep_rows_kernel(DecodeArgs a) {
   extern __shared__ __align__(16) float qsm[];
   float(*qs)[kQRPad] = reinterpret_cast<float(*)[kQRPad]>(qsm);
   float(*ws)[kQROut] = reinterpret_cast<float(*)[kQROut]>(qsm + kQRRows * kQRPad);
   const int nout = kD + a.m;
-  const long long r0 = static_cast<long long>(blockIdx.x) * kQRRows;
-  const int c0 = blockIdx.y * kQROut;
+  const long long blk = blockIdx.x >> 1;
+  const int xh = blockIdx.x & 1, c0 = blockIdx.y * kQROut;
+  const int qb = static_cast<int>(blk % a.nqb);
+  const long long bh = blk / a.nqb;
+  const int h = static_cast<int>(bh % a.H);
+  const long long b = bh / a.H;
+  const int rows_all = a.T * a.G, rb = 128 * qb + 64 * xh;   // the CTA's first block row (as t G + g)
   const int tid = threadIdx.x;
   pdl_trigger();
   if (blockIdx.x == 0 && blockIdx.y == 0 && tid < 2 && a.sched) a.sched[tid] = 0;   // partials work counters
-  // every load of the block's W^T slice and q rows issued before the first store
+  // every load of the W^T slice and the q rows issued before the first store
   {
     float4 wv[kD * kQROut / 4 / kQRThreads];
 #pragma unroll
@@ -174,25 +183,25 @@ __global__ void __launch_bounds__(kQRThreads) qprep_rows_kernel(DecodeArgs a, lo
       wv[it] = c0 + c < nout ? *reinterpret_cast<const float4*>(a.tab.wt + static_cast<long long>(k) * nout + c0 + c)
                              : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    float qv[kQRRows * kD / kQRThreads];                 // 32 values: row tid / 4, channels 32 (tid % 4) ..
-    const int qr = tid >> 2, qc = 32 * (tid & 3);
-    const bool in = r0 + qr < nq;
+    float qv[32];                                      // row tid / 4, channels 32 (tid % 4) ..
+    const int qr = tid >> 2, qc = 32 * (tid & 3), rr = rb + qr;
+    const bool in = rr < rows_all;
+    const long long R = in ? (b * a.T + rr / a.G) * a.Hq + h * a.G + rr % a.G : 0;
     const bool vec = (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
 #pragma unroll
     for (int j = 0; j < 32; j += 8) {
       if (!vec) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) qv[j + e] = in ? load_q(a.q, a.f32, (r0 + qr) * kD + qc + j + e) : 0.0f;
+        for (int e = 0; e < 8; ++e) qv[j + e] = in ? load_q(a.q, a.f32, R * kD + qc + j + e) : 0.0f;
       } else if (a.f32) {
-        const float4 x0 = in ? *reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + (r0 + qr) * kD + qc + j)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 x1 = in ? *reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + (r0 + qr) * kD + qc + j + 4)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* src = static_cast<const float*>(a.q) + R * kD + qc + j;
+        const float4 x0 = in ? *reinterpret_cast<const float4*>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 x1 = in ? *reinterpret_cast<const float4*>(src + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
         qv[j] = x0.x; qv[j + 1] = x0.y; qv[j + 2] = x0.z; qv[j + 3] = x0.w;
         qv[j + 4] = x1.x; qv[j + 5] = x1.y; qv[j + 6] = x1.z; qv[j + 7] = x1.w;
       } else {
         uint4 x = make_uint4(0u, 0u, 0u, 0u);
-        if (in) x = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + (r0 + qr) * kD + qc + j);
+        if (in) x = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + R * kD + qc + j);
         const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -235,30 +244,29 @@ __global__ void __launch_bounds__(kQRThreads) qprep_rows_kernel(DecodeArgs a, lo
       }
     }
   }
-  if (c0 + 4 * to >= nout) return;
+  __syncthreads();                                 // the W^T slice is read: its space restages the words
+  // staging: [group g (q~: hi 0..15, lo 16..31; u: 0..15)][row 64] x 16 bytes
+  uint2* stg = reinterpret_cast<uint2*>(ws);
+  const bool qt = c0 < kD;
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
-    if (r0 + 8 * tr + r >= nq) continue;
-    float* row = a.qprep + (r0 + 8 * tr + r) * nout;
-    if (!a.qhalf) {
-      *reinterpret_cast<float4*>(row + c0 + 4 * to) = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-      continue;
-    }
-    // fp16 words in tensor-memory column order: q~ hi pairs at 0, q~ lo pairs at 64, u pairs at 128
-    uint32_t* w = reinterpret_cast<uint32_t*>(row);
+    const int rl = 8 * tr + r;
     const __half2 h0 = __floats2half2_rn(acc[r][0], acc[r][1]), h1 = __floats2half2_rn(acc[r][2], acc[r][3]);
-    const int pw = (c0 + 4 * to) / 2;
-    if (c0 + 4 * to < kD) {
+    stg[((to >> 1) * 64 + rl) * 2 + (to & 1)] =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+    if (qt) {
       const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
       const __half2 l0 = __floats2half2_rn(acc[r][0] - f0.x, acc[r][1] - f0.y);
       const __half2 l1 = __floats2half2_rn(acc[r][2] - f1.x, acc[r][3] - f1.y);
-      *reinterpret_cast<uint2*>(w + pw) = make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
-      *reinterpret_cast<uint2*>(w + 64 + pw) =
+      stg[((16 + (to >> 1)) * 64 + rl) * 2 + (to & 1)] =
           make_uint2(*reinterpret_cast<const uint32_t*>(&l0), *reinterpret_cast<const uint32_t*>(&l1));
-    } else {
-      *reinterpret_cast<uint2*>(w + 64 + pw) = make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
     }
   }
+  __syncthreads();
+  const int ng = qt ? 32 : 16, g0 = qt ? 0 : 32;   // groups of 4 words: this CTA's, and its first in the row
+  uint4* dst = reinterpret_cast<uint4*>(a.qprep) + blk * 48 * 128 + 64 * xh;
+  const uint4* src = reinterpret_cast<const uint4*>(ws);
+  for (int i = tid; i < ng * 64; i += kQRThreads) dst[(g0 + i / 64) * 128 + i % 64] = src[i];
 }
 
 // Code of channel j from a vector's code words (the stored format of tq.h).
@@ -719,6 +727,102 @@ __global__ void __launch_bounds__(kMRThreads) merge_rows_kernel(DecodeArgs a, lo
   }
 }
 
+// Merge for the tensor-core causal kernel, whose partials are stored by query
+// block: (max, sum, acc[128]) of block row r for chunk c at float
+// ((blk nchunks + c) 130 + f) 128 + r.  A block takes 32 rows of a query
+// block: lane = row, warp w the channels 16 w .. 16 w + 15, so that every load
+// of a warp is 128 contiguous bytes; then o = Pi^T o~ for the 32 rows.
+constexpr int kMBThreads = 512;
+
+__global__ void __launch_bounds__(kMBThreads) merge_blk_kernel(DecodeArgs a) {
+  pdl_wait();                          // the partials kernel before it has completed
+  __shared__ __align__(16) float os[32][kD + 4];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long blk = blockIdx.x >> 2;
+  const int sub = blockIdx.x & 3;
+  const int qb = static_cast<int>(blk % a.nqb);
+  const long long bh = blk / a.nqb;
+  const int h = static_cast<int>(bh % a.H);
+  const long long b = bh / a.H;
+  const int rows_all = a.T * a.G;
+  {
+    const int rr = 128 * qb + 32 * sub + lane;
+    int nc = 0;
+    if (rr < rows_all) {
+      int L = a.seq_lens[b] + rr / a.G + 1;          // row t G + g attends positions [0, start + t]
+      L = L < 0 ? 0 : L;
+      L = L > a.max_seq_len ? a.max_seq_len : L;
+      L = L > a.maxp * kPage ? a.maxp * kPage : L;
+      nc = min(a.nchunks, (L + a.chunk - 1) / a.chunk);
+    }
+    const float* pb = a.part + blk * a.nchunks * (kD + 2) * 128 + 32 * sub + lane;
+    constexpr long long kCS = (kD + 2) * 128;          // floats between a row's chunks
+    int ncw = nc;                                      // the warp's largest chunk count
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ncw = max(ncw, __shfl_xor_sync(0xffffffffu, ncw, o));
+    // loads in batches of eight chunks (maxima) and four chunks (sums and this warp's channels)
+    float M = -INFINITY;
+    for (int c0 = 0; c0 < ncw; c0 += 8) {
+      float mv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mv[j] = c0 + j < nc ? pb[(c0 + j) * kCS] : -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) M = fmaxf(M, mv[j]);
+    }
+    float l = 0.0f, acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
+    for (int c0 = 0; c0 < ncw; c0 += 4) {
+      float mv[4], lv[4], xv[4][8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool in = c0 + j < nc;
+        const float* pc = pb + (c0 + j) * kCS;
+        mv[j] = in ? pc[0] : -INFINITY;
+        lv[j] = in ? pc[128] : 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) xv[j][k] = in ? pc[(2 + 8 * warp + k) * 128] : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float w = c0 + j < nc ? exp2f(mv[j] - M) : 0.0f;
+        l = fmaf(w, lv[j], l);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] = fmaf(w, xv[j][k], acc[k]);
+      }
+    }
+    const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+    *reinterpret_cast<float4*>(&os[lane][8 * warp]) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<float4*>(&os[lane][8 * warp + 4]) = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+  }
+  __syncthreads();
+  const int rg = tid >> 5, cg = tid & 31;            // rows 2 rg, 2 rg + 1, output channels 4 cg .. 4 cg + 3
+  float o[2][4];
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) o[r][c] = 0.0f;
+#pragma unroll 4
+  for (int i = 0; i < kD; ++i) {
+    const float4 p = __ldg(reinterpret_cast<const float4*>(a.tab.pi + i * kD + 4 * cg));
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const float x = os[2 * rg + r][i];
+      o[r][0] = fmaf(p.x, x, o[r][0]);
+      o[r][1] = fmaf(p.y, x, o[r][1]);
+      o[r][2] = fmaf(p.z, x, o[r][2]);
+      o[r][3] = fmaf(p.w, x, o[r][3]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int rr = 128 * qb + 32 * sub + 2 * rg + r;
+    if (rr >= rows_all) continue;
+    const long long row = (b * a.T + rr / a.G) * a.Hq + h * a.G + rr % a.G;
+    *reinterpret_cast<float4*>(a.out + row * kD + 4 * cg) = make_float4(o[r][0], o[r][1], o[r][2], o[r][3]);
+  }
+}
+
 template <int G>
 cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
   dim3 grid(a.nchunks, a.H, a.B);
@@ -731,12 +835,12 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
 cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
   if ((stages & TQ_STAGE_QPREP) && a.qhalf) {
-    const long long nq = static_cast<long long>(a.B) * a.T * a.Hq;
-    const dim3 grid(static_cast<unsigned>((nq + kQRRows - 1) / kQRRows), static_cast<unsigned>((kD + a.m + kQROut - 1) / kQROut));
+    const long long nblk = static_cast<long long>(a.B) * a.H * a.nqb;
+    const dim3 grid(static_cast<unsigned>(2 * nblk), static_cast<unsigned>((kD + a.m + kQROut - 1) / kQROut));
     static std::atomic<unsigned long long> configured{0};   // q rows and the W^T slice take 99 KB
     e = smem_attr_once(qprep_rows_kernel, kQRSmem, configured);
     if (e != cudaSuccess) return e;
-    qprep_rows_kernel<<<grid, kQRThreads, kQRSmem, s>>>(a, nq);
+    qprep_rows_kernel<<<grid, kQRThreads, kQRSmem, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   } else if (stages & TQ_STAGE_QPREP) {
@@ -769,7 +873,10 @@ cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
     }
   }
   if (stages & TQ_STAGE_MERGE) {
-    if (a.T > 0) {
+    if (a.T > 0 && a.qhalf) {
+      const long long nblk = static_cast<long long>(a.B) * a.H * a.nqb;
+      e = launch_pdl(merge_blk_kernel, dim3(static_cast<unsigned>(4 * nblk)), dim3(kMBThreads), 0, s, a);
+    } else if (a.T > 0) {
       const long long rows = static_cast<long long>(a.B) * a.T * a.Hq;
       e = launch_pdl(merge_rows_kernel, dim3(static_cast<unsigned>((rows + kMRRows - 1) / kMRRows)), dim3(kMRThreads),
                      0, s, a, rows);
