@@ -112,7 +112,8 @@ struct CGeo {
   static constexpr int OPS_BYTES = VT + 3 * 64 * 128;
   static constexpr int OPS = 0;
   static constexpr int LUT = OPS + 2 * OPS_BYTES;
-  static constexpr int REC = LUT + kLutBytes;
+  static constexpr int SGN = LUT + kLutBytes;      // sign masks of a nibble: [16][32 lanes] x 8 bytes
+  static constexpr int REC = SGN + 16 * 32 * 8;
   static constexpr int FAC = (REC + kCStages * STAGE + 1023) & ~1023;   // [4][fa | bias][64] floats
   static constexpr int XMAX = FAC + 4 * 2 * 64 * 4;                     // [2][2][128] partial row maxima
   static constexpr int DESC = XMAX + 2 * 2 * 128 * 4;                   // [4] CDesc + [kCStages] CDesc
@@ -142,65 +143,55 @@ __device__ __forceinline__ uint32_t chunk_bytes_c(const uint32_t (&w)[17], int b
   const uint32_t x = stream_bits_c(w, base + 16 * cc) & 0xFFFFu;
   return (x & 0xFu) | ((x & 0xF0u) << 4) | ((x & 0xF00u) << 8) | ((x & 0xF000u) << 12);
 }
-// K^ rows of one 64-channel half (B-bit codes at `src`, 8 B bytes) for token
-// row t: the fp16 centroid of every channel, zero for an invalid token.  The
-// chunk loop stays rolled: the kernel's roles share each SM's instruction
-// cache.
+// Lookup indices of chunk cc (8 channels) of a 64-channel group of B-bit codes
+// at `src` (8 B bytes): byte i = the index of channels (2i, 2i + 1).  The words
+// are loaded first (chunk_words) so that two chunks' loads are in flight
+// together, then unpacked (chunk_index).
 template <int B>
-__device__ __forceinline__ void k_half_rows(uint32_t tile, uint32_t src, int t, int hf, bool tv, uint32_t tb) {
-#pragma unroll 1
-  for (int cc = 0; cc < 8; ++cc) {
-    uint32_t p[4] = {0u, 0u, 0u, 0u};
-    if (tv) {
-      const int off = B * 8 * cc, wi = off >> 5, sh = off & 31;
-      const uint32_t lo = lds32(src + 4 * wi);
-      uint32_t x;
-      if (B == 4) {
-        x = lo;
-      } else if (B == 3) {
-        const uint32_t hi = sh > 8 ? lds32(src + 4 * wi + 4) : 0u;
-        x = octet_nibbles_c(sh ? __funnelshift_r(lo, hi, sh) : lo);
-      } else {
-        const uint32_t y = (lo >> sh) & 0xFFFFu;
-        x = (y & 0xFu) | ((y & 0xF0u) << 4) | ((y & 0xF00u) << 8) | ((y & 0xF000u) << 12);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) p[i] = lds32(tb + ((x >> (8 * i)) & 0xFFu) * 128u);
-    }
-    sts128(tile + chunk_off(t, 8 * hf + cc, kCT), p[0], p[1], p[2], p[3]);
-  }
+__device__ __forceinline__ uint2 chunk_words(uint32_t src, int cc) {
+  const int off = B * 8 * cc, wi = off >> 5, sh = off & 31;
+  return make_uint2(lds32(src + 4 * wi), (B == 3 && sh > 8) ? lds32(src + 4 * wi + 4) : 0u);
+}
+template <int B>
+__device__ __forceinline__ uint32_t chunk_index(uint2 w, int cc) {
+  const int sh = (B * 8 * cc) & 31;
+  if (B == 4) return w.x;
+  if (B == 3) return octet_nibbles_c(sh ? __funnelshift_r(w.x, w.y, sh) : w.x);
+  const uint32_t y = (w.x >> sh) & 0xFFFFu;
+  return (y & 0xFu) | ((y & 0xF0u) << 4) | ((y & 0xF00u) << 8) | ((y & 0xF000u) << 12);
 }
 
-// V' rows of one 64-channel half (B-bit codes at `src`) for token row t: the
-// fp16 centroid of every channel times the token's n_v/sqrt(d) (f2), zero for
-// an invalid token.  As the K^ rows; the O MMA reads this operand MN-major.
-template <int B>
-__device__ __forceinline__ void v_half_rows(uint32_t tile, uint32_t src, int t, int hf, bool tv, uint32_t tb,
-                                            __half2 f2) {
+// Rows of one 64-channel half for token row t (B-bit codes at `src`): the fp16
+// centroid pair of every channel pair, times f2 when SCALE (V'), zero for an
+// invalid token.  Two chunks per step with their loads ahead of their stores
+// (the shared-memory accesses keep program order); the step loop stays rolled
+// because the kernel's roles share each SM's instruction cache.
+template <int B, bool SCALE>
+__device__ __forceinline__ void half_rows(uint32_t tile, uint32_t src, int t, int hf, bool tv, uint32_t tb,
+                                          __half2 f2) {
 #pragma unroll 1
-  for (int cc = 0; cc < 8; ++cc) {
-    uint32_t p[4] = {0u, 0u, 0u, 0u};
+  for (int cc = 0; cc < 8; cc += 2) {
+    uint32_t p[2][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};
     if (tv) {
-      const int off = B * 8 * cc, wi = off >> 5, sh = off & 31;
-      const uint32_t lo = lds32(src + 4 * wi);
-      uint32_t x;
-      if (B == 4) {
-        x = lo;
-      } else if (B == 3) {
-        const uint32_t hi = sh > 8 ? lds32(src + 4 * wi + 4) : 0u;
-        x = octet_nibbles_c(sh ? __funnelshift_r(lo, hi, sh) : lo);
-      } else {
-        const uint32_t y = (lo >> sh) & 0xFFFFu;
-        x = (y & 0xFu) | ((y & 0xF0u) << 4) | ((y & 0xF00u) << 8) | ((y & 0xF000u) << 12);
-      }
+      const uint2 w0 = chunk_words<B>(src, cc), w1 = chunk_words<B>(src, cc + 1);
+      const uint32_t x0 = chunk_index<B>(w0, cc), x1 = chunk_index<B>(w1, cc + 1);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint32_t e = lds32(tb + ((x >> (8 * i)) & 0xFFu) * 128u);
-        const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&e), f2);
-        p[i] = *reinterpret_cast<const uint32_t*>(&r);
+        p[0][i] = lds32(tb + __byte_perm(x0, 0u, 0x4440u + i) * 128u);
+        p[1][i] = lds32(tb + __byte_perm(x1, 0u, 0x4440u + i) * 128u);
+      }
+      if (SCALE) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&p[j][i]), f2);
+            p[j][i] = *reinterpret_cast<const uint32_t*>(&r);
+          }
       }
     }
-    sts128(tile + chunk_off(t, 8 * hf + cc, kCT), p[0], p[1], p[2], p[3]);
+    sts128(tile + chunk_off(t, 8 * hf + cc, kCT), p[0][0], p[0][1], p[0][2], p[0][3]);
+    sts128(tile + chunk_off(t, 8 * hf + cc + 1, kCT), p[1][0], p[1][1], p[1][2], p[1][3]);
   }
 }
 
@@ -285,6 +276,14 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
         v = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(clo))) |
             (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(chi))) << 16);
       *reinterpret_cast<uint32_t*>(sm + G::LUT + off) = v;
+    }
+    // nibble n of sign bits (projections 4j .. 4j + 3) -> two words of fp16 sign masks: the sign
+    // of a half is set where the bit is clear (2 b - 1 = -1)
+    for (int i = tid; i < 16 * 32; i += kCThreadsTC) {
+      const int n = i >> 5;
+      const uint32_t w0 = ((n & 1) ? 0u : 0x8000u) | ((n & 2) ? 0u : 0x80000000u);
+      const uint32_t w1 = ((n & 4) ? 0u : 0x8000u) | ((n & 8) ? 0u : 0x80000000u);
+      *reinterpret_cast<uint2*>(sm + G::SGN + 8 * i) = make_uint2(w0, w1);
     }
     if (tid == 0) {
       for (int s = 0; s < kCStages; ++s) {
@@ -495,25 +494,27 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
                    (kSqrtHalfPiC / 128.0f);
           }
           if (hf == 0)
-            k_half_rows<KBH>(ob + G::KH, kb + slot * G::CBK, t, 0, tv, sb + G::LUT + lut_off(KBH) + lane_off);
+            half_rows<KBH, false>(ob + G::KH, kb + slot * G::CBK, t, 0, tv, sb + G::LUT + lut_off(KBH) + lane_off, __half2());
           else
-            k_half_rows<KBL>(ob + G::KH, kb + slot * G::CBK + 8 * KBH, t, 1, tv, sb + G::LUT + lut_off(KBL) + lane_off);
+            half_rows<KBL, false>(ob + G::KH, kb + slot * G::CBK + 8 * KBH, t, 1, tv, sb + G::LUT + lut_off(KBL) + lane_off,
+                                  __half2());
           if (QJL) {                                   // A' = (fb / fa)(2 b - 1) for the 64 projections of this half
             uint2 sw = make_uint2(0u, 0u);
             if (tv) sw = lds64(kb + G::K_SIGNS + slot * 16 + 8 * hf);
             const __half2 fb2 = __float2half2_rn(fa > 0.0f ? fb / fa : 0.0f);
-            const uint32_t fbs = *reinterpret_cast<const uint32_t*>(&fb2) | 0x80008000u;   // -fb in both halves
+            const uint32_t fbv = tv ? *reinterpret_cast<const uint32_t*>(&fb2) : 0u;   // |A'| in both halves
+            const uint32_t vm = tv ? 0xFFFFFFFFu : 0u;
+            const uint32_t st = sb + G::SGN + lane_off * 2;
 #pragma unroll 1
-            for (int cc = 0; cc < 8; ++cc) {
-              const uint32_t byte = ((cc < 4 ? sw.x : sw.y) >> (8 * (cc & 3))) & 0xFFu;
-              const uint32_t zl = ((byte & 0xFu) * 0x10204080u) & 0x80808080u;   // sign bit j <- bit j
-              const uint32_t zh = ((byte >> 4) * 0x10204080u) & 0x80808080u;
-              const uint32_t dst = ob + G::AS + chunk_off(t, 8 * hf + cc, kCT);
-              // a set bit clears the half's sign: +fb; a clear bit leaves -fb
-              sts128(dst, tv ? fbs ^ (prmt(zl, 0u, 0x9080u) & 0x80008000u) : 0u,
-                     tv ? fbs ^ (prmt(zl, 0u, 0xB0A0u) & 0x80008000u) : 0u,
-                     tv ? fbs ^ (prmt(zh, 0u, 0x9080u) & 0x80008000u) : 0u,
-                     tv ? fbs ^ (prmt(zh, 0u, 0xB0A0u) & 0x80008000u) : 0u);
+            for (int cc = 0; cc < 8; cc += 2) {           // two chunks per step, loads first
+              const uint32_t w = cc < 4 ? sw.x : sw.y;
+              const uint32_t b0 = __byte_perm(w, 0u, 0x4440u + (cc & 3)), b1 = __byte_perm(w, 0u, 0x4441u + (cc & 3));
+              const uint2 l0 = lds64(st + (b0 & 0xFu) * 256u), h0 = lds64(st + (b0 >> 4) * 256u);
+              const uint2 l1 = lds64(st + (b1 & 0xFu) * 256u), h1 = lds64(st + (b1 >> 4) * 256u);
+              sts128(ob + G::AS + chunk_off(t, 8 * hf + cc, kCT), fbv | (l0.x & vm), fbv | (l0.y & vm), fbv | (h0.x & vm),
+                     fbv | (h0.y & vm));
+              sts128(ob + G::AS + chunk_off(t, 8 * hf + cc + 1, kCT), fbv | (l1.x & vm), fbv | (l1.y & vm),
+                     fbv | (h1.x & vm), fbv | (h1.y & vm));
             }
           }
           if (hf == 0) {
@@ -539,13 +540,13 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
           fv = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(vb + G::V_NORM + 2 * slot)))) * kInvSqrtDC;
         const __half2 fv2 = __float2half2_rn(fv);
         if (hf == 0) {
-          v_half_rows<VBH>(ob + G::VT, vb + slot * G::CBV, t, 0, tv, sb + G::LUT + lut_off(VBH) + lane_off, fv2);
+          half_rows<VBH, true>(ob + G::VT, vb + slot * G::CBV, t, 0, tv, sb + G::LUT + lut_off(VBH) + lane_off, fv2);
           // channels 128 .. 143: 1 in channel 128 for a token that is there, else 0
           sts128(ob + G::VT + chunk_off(t, 16, kCT), tv ? 0x3C00u : 0u, 0u, 0u, 0u);
           sts128(ob + G::VT + chunk_off(t, 17, kCT), 0u, 0u, 0u, 0u);
         } else {
-          v_half_rows<VBL>(ob + G::VT, vb + slot * G::CBV + 8 * VBH, t, 1, tv, sb + G::LUT + lut_off(VBL) + lane_off,
-                           fv2);
+          half_rows<VBL, true>(ob + G::VT, vb + slot * G::CBV + 8 * VBH, t, 1, tv, sb + G::LUT + lut_off(VBL) + lane_off,
+                               fv2);
         }
         fence_async_smem();
         __syncwarp();
