@@ -65,6 +65,16 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def tensor_peak():
+    """Dense fp16 tensor peak in TFLOP/s: the measured bf16 burst figure (fp16 and bf16 share one rate), else the
+    fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (bf16 burst; fp16 runs at the same rate)"
+    return 1900.0, "fallback"
+
+
 # ---------------------------------------------------------------------------
 # clocks (NVML through ctypes; read-only queries)
 # ---------------------------------------------------------------------------
@@ -452,12 +462,22 @@ def causal_measure(torch, tq, stream, steps, warmup, dist, peak, peak_kind, worl
         tq.tq_causal_attention(ctx, q, tq.TQ_BF16, B, T, Hq, H, start, L + T, bt, pps, B * pps, kc, vc, 0,
                                1.0 / math.sqrt(128), out, ws, ws_n, stream)
 
+    def attend(i=None):
+        tq.tq_causal_attention(ctx, q, tq.TQ_BF16, B, T, Hq, H, start, L + T, bt, pps, B * pps, kc, vc, 0,
+                               1.0 / math.sqrt(128), out, ws, ws_n, stream)
+
     step()
     torch.cuda.synchronize()
     sampler = ClockSampler(torch)
     with sampler:
         ms = timed(torch, stream, step, steps, warmup, dist) / steps
+        ms_att = timed(torch, stream, attend, steps, warmup, dist) / steps
     bytes_step = B * H * (L + T) * wl.packed_bytes_per_token_head(w)     # every token up to the last new one
+    # algorithmic flops: every attended (query row, token) pair costs <q~, k^> + <u, signs> + p v, 2 (d + m + d)
+    pairs = B * Hq * sum(L + t + 1 for t in range(T))
+    flops = pairs * 2 * (128 + w.m + 128)
+    tpk, tpk_kind = tensor_peak()
+    tflops = flops * world / (ms_att * 1e-3) / 1e12
     flags = tq.tq_check_device_status(ctx)
     tq.tq_destroy(ctx)
     value = bytes_step * world / (ms * 1e-3) / 1e9
@@ -470,7 +490,12 @@ def causal_measure(torch, tq, stream, steps, warmup, dist, peak, peak_kind, worl
             "roofline": {"kernel": "whole step (quantize-append + qprep + causal partials + merge)", "bound": "hbm",
                          "achieved": round(value, 2), "peak": peak, "unit": "GB/s", "frac": round(value / peak, 4),
                          "peak_source": peak_kind, "algorithmic_bytes_per_launch": bytes_step, "traffic": None},
-            "gpu_launches": 4 * steps, "clocks": sampler.result(), "device_flags": flags}
+            "attention_only": {"ms": round(ms_att, 5), "launches": "qprep_rows + causal_tc + merge_blk",
+                               "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": tpk,
+                                            "unit": "TFLOP/s", "frac": round(tflops / tpk, 4), "peak_source": tpk_kind,
+                                            "algorithmic_flops_per_call": flops,
+                                            "note": "768 flops per attended (query row, token) pair"}},
+            "gpu_launches": 7 * steps, "clocks": sampler.result(), "device_flags": flags}
 
 
 def quantize_measure(torch, tq, qw, stream, qsteps, warmup, dist, peak, peak_kind, world):
