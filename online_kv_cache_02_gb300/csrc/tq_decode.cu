@@ -74,9 +74,40 @@ __global__ void __launch_bounds__(kQThreads) qprep_kernel(DecodeArgs a) {
     if (c0 + c < nout) x = *reinterpret_cast<const float4*>(a.tab.wt + static_cast<long long>(k) * nout + c0 + c);
     *reinterpret_cast<float4*>(&ws[k][c]) = x;
   }
-  for (int idx = tid; idx < kQP * kD; idx += kQThreads) {
-    const int r = idx / kD, c = idx % kD;
-    qs[r][c] = r0 + r < nq ? load_q(a.q, a.f32, (r0 + r) * kD + c) : 0.0f;
+  {
+    // row tid / 4, channels 32 (tid % 4) .. + 31: every load issued before the first store
+    const int qr = tid >> 2, qc = 32 * (tid & 3);
+    const bool in = r0 + qr < nq;
+    float qv[32];
+    if ((reinterpret_cast<uintptr_t>(a.q) & 15) == 0 && !a.f32) {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + (r0 + qr) * kD + qc);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 x = in ? src[j] : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          qv[8 * j + 2 * e] = __uint_as_float(xs[e] << 16);
+          qv[8 * j + 2 * e + 1] = __uint_as_float(xs[e] & 0xFFFF0000u);
+        }
+      }
+    } else if ((reinterpret_cast<uintptr_t>(a.q) & 15) == 0) {
+      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + (r0 + qr) * kD + qc);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 x = in ? src[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+        qv[4 * j] = x.x;
+        qv[4 * j + 1] = x.y;
+        qv[4 * j + 2] = x.z;
+        qv[4 * j + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) qv[j] = in ? load_q(a.q, a.f32, (r0 + qr) * kD + qc + j) : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < 32; j += 4)
+      *reinterpret_cast<float4*>(&qs[qr][qc + j]) = make_float4(qv[j], qv[j + 1], qv[j + 2], qv[j + 3]);
   }
   __syncthreads();
   float acc[4][4];
@@ -607,6 +638,161 @@ __global__ void __launch_bounds__(kMThreads) merge_kernel(DecodeArgs a) {
   if (grp == 0) a.out[row * kD + j] = (part[0][j] + part[1][j]) + (part[2][j] + part[3][j]);
 }
 
+// Decode merge, a warp per query row (eight rows per block): the chunk maxima
+// and weights live on the lanes (chunk c on lane c % 32), the weighted partials
+// are read eight chunks at a time with a lane holding four channels (the first
+// eight issued with the maxima), the fused step's new token is scored by the
+// same warp from its stored record, and the warp rotates its row back
+// (o = Pi^T o~) from a copy of Pi the block staged in shared memory before its
+// grid dependency wait.  No block-wide reductions; few rounds of dependent loads.
+constexpr int kMDRows = 8;
+
+// The token at position seq_lens[b] of a fused decode step for query row `row`
+// (its KV head's stored record: the quantize-append ran on another stream):
+// the logit in log2 units, and in vn the value's channels 4 lane .. 4 lane + 3
+// times n_v/sqrt(d).  -inf when there is no such token (a bad length or page
+// id, flagged once per sequence).
+__device__ float new_token_logit_warp(const DecodeArgs& a, long long row, int lane, float (&vn)[4]) {
+  const int b = static_cast<int>(row / a.Hq), hq = static_cast<int>(row % a.Hq), hkv = hq / a.G;
+  const int L0 = a.seq_lens[b];
+  if (L0 < 0 || L0 >= a.maxp * kPage || L0 + 1 > a.max_seq_len) {
+    if (lane == 0 && hq == 0) atomicOr(a.tab.err, kErrSeqLen);
+    return -INFINITY;
+  }
+  const int page = a.block_table[static_cast<long long>(b) * a.maxp + (L0 >> 4)], slot = L0 & 15;
+  if (page < 0 || page >= a.num_pages) {
+    if (lane == 0 && hq == 0) atomicOr(a.tab.err, kErrPage);
+    return -INFINITY;
+  }
+  const uint8_t* krec = a.kc + static_cast<long long>(page) * a.k_page_bytes + static_cast<long long>(hkv) * a.kl.block_bytes;
+  const uint8_t* vrec = a.vc + static_cast<long long>(page) * a.v_page_bytes + static_cast<long long>(hkv) * a.vl.block_bytes;
+  const float* qr = a.qprep + row * (kD + a.m);
+  const float4 q4 = *reinterpret_cast<const float4*>(qr + 4 * lane);
+  const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+  const unsigned* kw = reinterpret_cast<const unsigned*>(krec + slot * a.kl.code_bytes);
+  const unsigned* vw = reinterpret_cast<const unsigned*>(vrec + slot * a.vl.code_bytes);
+  const float nv = __half2float(reinterpret_cast<const __half*>(vrec + a.vl.off_norm)[slot]) * kInvSqrtD;
+  float s1 = 0.0f, s2 = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int j = 4 * lane + i;
+    const int kc = code_at(kw, a.kl.g[0].bits, a.kl.g[1].bits, a.kl.split, j);
+    s1 = fmaf(qv[i], a.kl.g[j < a.kl.split ? 0 : 1].c[kc], s1);
+    const int vc = code_at(vw, a.vl.g[0].bits, a.vl.g[1].bits, a.vl.split, j);
+    vn[i] = nv * a.vl.g[j < a.vl.split ? 0 : 1].c[vc];
+    if (a.kl.qjl && j < a.m) {                       // <u, +-1 signs>
+      const uint8_t sbyte = krec[a.kl.off_signs + slot * (a.m / 8) + (j >> 3)];
+      const float u = qr[kD + j];
+      s2 += ((sbyte >> (j & 7)) & 1u) ? u : -u;
+    }
+  }
+  s1 = warp_sum(s1);
+  s2 = warp_sum(s2);
+  const float nk = __half2float(reinterpret_cast<const __half*>(krec + a.kl.off_norm)[slot]);
+  float lg = nk * kInvSqrtD * s1;
+  if (a.kl.qjl) {
+    const float rk = __half2float(reinterpret_cast<const __half*>(krec + a.kl.off_rnorm)[slot]);
+    lg = fmaf(kSqrtHalfPi / static_cast<float>(a.m) * rk, s2, lg);
+  }
+  return lg * a.scale_log2;
+}
+
+constexpr int kMDSmem = (kD * kD + kMDRows * kD) * 4;   // Pi, then the rows' o~
+
+__global__ void __launch_bounds__(32 * kMDRows) merge_dec_kernel(DecodeArgs a, long long rows) {
+  extern __shared__ __align__(16) float mds[];
+  float(*pis)[kD] = reinterpret_cast<float(*)[kD]>(mds);
+  float(*os)[kD] = reinterpret_cast<float(*)[kD]>(mds + kD * kD);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Pi does not depend on the partials kernel: staged before the grid dependency wait
+#pragma unroll
+  for (int k = 0; k < kD * kD / 4 / (32 * kMDRows); ++k) {
+    const int v = tid + k * 32 * kMDRows;
+    *reinterpret_cast<float4*>(&pis[0][0] + 4 * v) = __ldg(reinterpret_cast<const float4*>(a.tab.pi) + v);
+  }
+  pdl_wait();                          // the partials kernel before it has completed
+  const long long row = static_cast<long long>(blockIdx.x) * kMDRows + warp;
+  const bool live = row < rows;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f}, l = 0.0f;
+  if (live) {
+    int L = a.seq_lens[row / a.Hq] + a.len_add;
+    L = L < 0 ? 0 : L;
+    L = L > a.max_seq_len ? a.max_seq_len : L;
+    L = L > a.maxp * kPage ? a.maxp * kPage : L;
+    const int nc = min(a.nchunks, (L + a.chunk - 1) / a.chunk);
+    const float* P = a.part + row * a.nchunks * (kD + 2);
+    // the first 32 chunks' (max, sum) on the lanes and their first eight partial vectors, all issued
+    // before anything waits on them
+    float2 ml = make_float2(-INFINITY, 0.0f);
+    if (lane < nc) ml = *reinterpret_cast<const float2*>(P + static_cast<long long>(lane) * (kD + 2));
+    float2 x[8][2];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      x[j][0] = x[j][1] = make_float2(0.f, 0.f);
+      if (j < nc) {
+        const float* pc = P + static_cast<long long>(j) * (kD + 2) + 2 + 4 * lane;
+        x[j][0] = *reinterpret_cast<const float2*>(pc);
+        x[j][1] = *reinterpret_cast<const float2*>(pc + 2);
+      }
+    }
+    float vn[4] = {0.f, 0.f, 0.f, 0.f};
+    const float lg_new = a.new_token ? new_token_logit_warp(a, row, lane, vn) : -INFINITY;
+    float M = ml.x;
+    for (int c = lane + 32; c < nc; c += 32) M = fmaxf(M, P[static_cast<long long>(c) * (kD + 2)]);
+    M = fmaxf(warp_max(M), lg_new);
+    for (int cb = 0; cb < nc; cb += 32) {
+      if (cb > 0) ml = cb + lane < nc ? *reinterpret_cast<const float2*>(P + static_cast<long long>(cb + lane) * (kD + 2))
+                                      : make_float2(-INFINITY, 0.0f);
+      const float w = cb + lane < nc ? exp2f(ml.x - M) : 0.0f;
+      l = fmaf(w, ml.y, l);
+      const int n = min(32, nc - cb);
+      for (int j0 = 0; j0 < n; j0 += 8) {
+        if (cb + j0 > 0) {                           // the next eight chunks (the first eight are loaded)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            x[j][0] = x[j][1] = make_float2(0.f, 0.f);
+            if (j0 + j < n) {
+              const float* pc = P + static_cast<long long>(cb + j0 + j) * (kD + 2) + 2 + 4 * lane;
+              x[j][0] = *reinterpret_cast<const float2*>(pc);
+              x[j][1] = *reinterpret_cast<const float2*>(pc + 2);
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float wj = __shfl_sync(0xffffffffu, w, (j0 + j) & 31);
+          acc[0] = fmaf(wj, x[j][0].x, acc[0]);
+          acc[1] = fmaf(wj, x[j][0].y, acc[1]);
+          acc[2] = fmaf(wj, x[j][1].x, acc[2]);
+          acc[3] = fmaf(wj, x[j][1].y, acc[3]);
+        }
+      }
+    }
+    l = warp_sum(l);
+    if (lg_new > -INFINITY) {
+      const float wn = exp2f(lg_new - M);
+      l += wn;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] = fmaf(wn, vn[i], acc[i]);
+    }
+  }
+  const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+  *reinterpret_cast<float4*>(&os[warp][4 * lane]) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+  __syncthreads();                     // Pi staged by every thread
+  if (!live) return;
+  float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+  for (int i = 0; i < kD; ++i) {
+    const float4 p = *reinterpret_cast<const float4*>(&pis[i][4 * lane]);
+    const float xo = os[warp][i];
+    o[0] = fmaf(p.x, xo, o[0]);
+    o[1] = fmaf(p.y, xo, o[1]);
+    o[2] = fmaf(p.z, xo, o[2]);
+    o[3] = fmaf(p.w, xo, o[3]);
+  }
+  *reinterpret_cast<float4*>(a.out + row * kD + 4 * lane) = make_float4(o[0], o[1], o[2], o[3]);
+}
+
 // Merge for many query rows (causal attention: B T Hq rows): a block takes 32
 // rows.  Each warp combines the chunk partials of four rows (log-sum-exp of
 // the chunk maxima, then the weighted sums; a lane holds four channels) into
@@ -880,9 +1066,17 @@ cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
       const long long rows = static_cast<long long>(a.B) * a.T * a.Hq;
       e = launch_pdl(merge_rows_kernel, dim3(static_cast<unsigned>((rows + kMRRows - 1) / kMRRows)), dim3(kMRThreads),
                      0, s, a, rows);
-    } else {
+    } else if (static_cast<long long>(a.B) * a.Hq < 1024) {
+      // few rows: a block per row has more loads in flight per row than a warp
       e = launch_pdl(merge_kernel, dim3(static_cast<unsigned>(static_cast<long long>(a.B) * a.Hq)), dim3(kMThreads), 0,
                      s, a);
+    } else {
+      const long long rows = static_cast<long long>(a.B) * a.Hq;
+      static std::atomic<unsigned long long> configured{0};   // Pi and the rows take 68 KB
+      e = smem_attr_once(merge_dec_kernel, kMDSmem, configured);
+      if (e != cudaSuccess) return e;
+      e = launch_pdl(merge_dec_kernel, dim3(static_cast<unsigned>((rows + kMDRows - 1) / kMDRows)), dim3(32 * kMDRows),
+                     static_cast<size_t>(kMDSmem), s, a, rows);
     }
   }
   return e;
