@@ -583,11 +583,9 @@ __global__ void __launch_bounds__(kMThreads) merge_kernel(DecodeArgs a) {
   __shared__ float os[kD];
   __shared__ float vnew[kD];
   __shared__ float red[kMThreads / 32];
-  const long long row = blockIdx.x;                 // b * Hq + query head (causal: (b T + t) Hq + query head)
+  const long long row = blockIdx.x;                 // b * Hq + query head (decode; causal rows use the row merges)
   const int tid = threadIdx.x, j = tid & (kD - 1), grp = tid >> 7;
-  // causal: row (b, t, h) attends positions [0, seq_lens[b] + t]
-  int L = a.T > 0 ? a.seq_lens[row / a.Hq / a.T] + static_cast<int>((row / a.Hq) % a.T) + 1
-                  : a.seq_lens[row / a.Hq] + a.len_add;
+  int L = a.seq_lens[row / a.Hq] + a.len_add;
   L = L < 0 ? 0 : L;
   L = L > a.max_seq_len ? a.max_seq_len : L;
   L = L > a.maxp * kPage ? a.maxp * kPage : L;
