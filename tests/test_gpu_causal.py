@@ -129,3 +129,66 @@ def test_causal_many_query_blocks():
     one ragged, with chunks that cut the prefix into several items."""
     w = wl.Workload("t", "decode", 2, 8, 2, 0, k_bits=(4, 3), v_bits=(4, 3), seed=9)
     _causal(w, starts=[700, 5], T=70, Hq=8, H=2, seed=6, chunk=256)
+
+
+def test_causal_unaligned_queries():
+    """A query tensor 2 bytes off a 16-byte boundary: the tensor-core path's query prep falls back to scalar
+    loads (same results as from an aligned copy)."""
+    import torch
+    w = wl.Workload("t", "decode", 2, 8, 2, 0, k_bits=(3, 3), v_bits=(3, 3), seed=6)
+    starts = np.array([20, 3], np.int32)
+    T, Hq, H = 5, 8, 2
+    lens = starts + T
+    p, bt, num_pages, kc, vc = _oracle_setup(w, lens, H, 2)
+    Q = wl.bf16_round(np.random.default_rng(8).standard_normal((2, T, Hq, 128)).astype(np.float32))
+    ctx = ctx_for(w)
+    try:
+        big = torch.empty(Q.size + 1, dtype=torch.bfloat16, device=DEV)
+        qt = big[1:].view(2, T, Hq, 128)
+        qt.copy_(torch.from_numpy(Q).to(DEV).to(torch.bfloat16))
+        assert qt.data_ptr() % 16 != 0
+        n = tq.tq_causal_workspace_size(ctx, 2, T, Hq, int(lens.max()), 0)
+        ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+        out = torch.full((2, T, Hq, 128), float("nan"), dtype=torch.float32, device=DEV)
+        scale = th.scale_for()
+        tq.tq_causal_attention(ctx, qt, tq.TQ_BF16, 2, T, Hq, H, to_dev(starts), int(lens.max()), to_dev(bt),
+                               bt.shape[1], num_pages, to_dev(kc), to_dev(vc), 0, scale, out, ws, n)
+        torch.cuda.synchronize()
+        assert tq.tq_check_device_status(ctx) == 0
+        got = out.cpu().numpy()
+    finally:
+        tq.tq_destroy(ctx)
+    want = oracle.causal_attention(p, Q.astype(np.float64), starts, bt, kc, vc, H, scale=scale)
+    assert th.rel_err(got.reshape(-1, 128), want.reshape(-1, 128)).max() <= th.ATT_TOL
+
+
+def test_causal_bad_page_is_skipped_and_flagged():
+    """A block-table entry outside [0, num_pages) in sequence 0's prefix: the kernel skips that page's tokens,
+    flags the page bit, and sequence 1 (untouched) still matches the oracle."""
+    import torch
+    w = wl.Workload("t", "decode", 2, 8, 2, 0, k_bits=(4, 3), v_bits=(4, 3), seed=7)
+    starts = np.array([90, 60], np.int32)
+    T, Hq, H = 6, 8, 2
+    lens = starts + T
+    p, bt, num_pages, kc, vc = _oracle_setup(w, lens, H, 3)
+    Q = wl.bf16_round(np.random.default_rng(11).standard_normal((2, T, Hq, 128)).astype(np.float32))
+    bad = bt.copy()
+    bad[0, 2] = num_pages + 7                            # positions 32..47 of sequence 0
+    ctx = ctx_for(w)
+    try:
+        qt, code = input_tensor(Q, "bf16")
+        n = tq.tq_causal_workspace_size(ctx, 2, T, Hq, int(lens.max()), 0)
+        ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+        out = torch.full((2, T, Hq, 128), float("nan"), dtype=torch.float32, device=DEV)
+        scale = th.scale_for()
+        tq.tq_causal_attention(ctx, qt, code, 2, T, Hq, H, to_dev(starts), int(lens.max()), to_dev(bad),
+                               bad.shape[1], num_pages, to_dev(kc), to_dev(vc), 0, scale, out, ws, n)
+        torch.cuda.synchronize()
+        flags = tq.tq_check_device_status(ctx)
+        got = out.cpu().numpy()
+    finally:
+        tq.tq_destroy(ctx)
+    assert flags & 1                                     # the page-id bit
+    assert np.all(np.isfinite(got))
+    want = oracle.causal_attention(p, Q.astype(np.float64), starts, bt, kc, vc, H, scale=scale)
+    assert th.rel_err(got[1].reshape(-1, 128), want[1].reshape(-1, 128)).max() <= th.ATT_TOL

@@ -282,3 +282,60 @@ def test_decode_chunk_choice():
             tq.tq_decode_chunk(ctx, 16, 32, 8, 16 * 32769 + 1, 32769)
     finally:
         tq.tq_destroy(ctx)
+
+
+def test_decode_many_rows_use_the_warp_merge():
+    """1,280 query rows (B = 40, 32/8 heads): the merge runs a warp per row with Pi staged in shared memory
+    (batches of 1,024 rows and more); lengths 0..47, chunks of 16 so that rows merge several chunks."""
+    rng = np.random.default_rng(31)
+    lens = rng.integers(0, 48, size=40)
+    lens[3] = 0
+    w = BASE.scaled(k_bits=(4, 3), v_bits=(4, 3), dtype="bf16")
+    _check(w, lens, 32, 8, chunk=16, seed=5)
+
+
+def test_append_decode_many_rows_against_the_oracle():
+    """The fused step at 1,024 query rows (B = 64, 16/4 heads): the warp-per-row merge scores the new token from
+    its stored record.  The oracle quantizes the cached tokens; the library appends the new one; the oracle then
+    decodes over all L + 1 from the bytes the library holds."""
+    import torch
+    w = BASE.scaled(k_bits=(3, 3), v_bits=(3, 3), dtype="bf16")
+    rng = np.random.default_rng(41)
+    B, H, Hq = 64, 4, 16
+    lens = rng.integers(8, 60, size=B).astype(np.int32)            # cached tokens; the new one goes at lens[b]
+    p, bt, num_pages, kc, vc = _oracle_setup(w, lens + 1, H, 9)
+    pos = lens.astype(np.int64)
+    kn = np.zeros((B, 1, H, 128), np.float32)
+    vn = np.zeros((B, 1, H, 128), np.float32)
+    # the new token's bf16 K/V: re-drawn here and written by the oracle at position lens[b], over what the setup put
+    r2 = np.random.default_rng(43)
+    for b in range(B):
+        K = wl.bf16_round(r2.standard_normal((1, H, 128)).astype(np.float32))
+        V = wl.bf16_round(r2.standard_normal((1, H, 128)).astype(np.float32))
+        kn[b, 0], vn[b, 0] = K[0], V[0]
+        pages, slots, heads = seq_locations(bt, b, [int(pos[b])], H)
+        th.oracle_quantize_into(p, "k", kc, K.reshape(-1, 128), pages, slots, heads, H)
+        th.oracle_quantize_into(p, "v", vc, V.reshape(-1, 128), pages, slots, heads, H)
+    Q = wl.bf16_round(rng.standard_normal((B, Hq, 128)).astype(np.float32))
+    scale = th.scale_for()
+    ctx = ctx_for(w)
+    try:
+        kcd, vcd = to_dev(kc), to_dev(vc)
+        max_len = int(lens.max()) + 1
+        n = tq.tq_workspace_size(ctx, B, Hq, max_len, 16)
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, device="cuda")
+        tq.tq_append_decode(ctx, to_dev(kn).to(torch.bfloat16), to_dev(vn).to(torch.bfloat16),
+                            to_dev(Q).to(torch.bfloat16), tq.TQ_BF16, B, Hq, H, to_dev(lens), max_len, to_dev(bt),
+                            bt.shape[1], num_pages, kcd, vcd, 16, scale, out, ws, n)
+        torch.cuda.synchronize()
+        assert tq.tq_check_device_status(ctx) == 0
+        got = out.cpu().numpy()
+        kc_gpu, vc_gpu = kcd.cpu().numpy(), vcd.cpu().numpy()
+    finally:
+        tq.tq_destroy(ctx)
+    # the oracle decodes the bytes the library holds (quantize exactness has its own tests; a value within the
+    # 1e-6 band of a boundary may take the other code)
+    ref = oracle.decode_attention(p, Q.astype(np.float64), lens + 1, bt, kc_gpu, vc_gpu, H, scale=scale)
+    assert np.all(np.isfinite(got))
+    assert th.rel_err(got, ref).max() <= th.ATT_TOL
