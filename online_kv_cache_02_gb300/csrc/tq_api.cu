@@ -164,7 +164,7 @@ int pick_chunk_total(int batch, int H, long long total_tokens, int max_seq_len, 
     long long chunk = (max_seq_len + nch - 1) / nch;
     chunk = ((chunk + kPage - 1) / kPage) * kPage;
     if (chunk < kPage) chunk = kPage;
-    if (chunk < 256 && nch > 1) break;
+    if (chunk < 64 && nch > 1) break;
     const long long full = static_cast<long long>(batch) * ((max_seq_len + chunk - 1) / chunk);
     const long long est = (total_tokens + chunk - 1) / chunk + batch / 2;
     const long long items = static_cast<long long>(H) * (est < full ? est : full);
@@ -187,7 +187,7 @@ int pick_chunk_warps(int units, int max_seq_len, int ctas) {
     long long chunk = (max_seq_len + nch - 1) / nch;
     chunk = ((chunk + kPage - 1) / kPage) * kPage;
     if (chunk < kPage) chunk = kPage;
-    if (chunk < 256 && nch > 1) break;
+    if (chunk < 64 && nch > 1) break;
     const long long real = (max_seq_len + chunk - 1) / chunk;
     const long long items = real * units;
     const long long cost = std::min(lut_cost(items, ctas, 12, chunk + 64), lut_cost(items, ctas, 16, chunk + 64));
