@@ -31,10 +31,11 @@
 //   warp 0: items from a global counter; a tile's four K and V page blocks by
 //       bulk copy into a three-stage ring (page ids of the item loaded once);
 //   warp 1: tensor memory (496 of 512 columns) and, one lane, the MMAs;
-//   warps 4, 5, 16, 17: K^ and A' rows and the token factors (two buffers,
-//       free again once the tile's S MMAs have run);
-//   warps 2, 3, 6, 7: V' rows and the ones column (two buffers, free again
-//       once the tile's O MMAs have run);
+//   warps 4, 5, 16, 17: K^ rows and the token factors (two buffers, free again
+//       once the tile's S MMAs have run);
+//   warps 2, 3, 6, 7: the sign rows A' (in the K buffers, as soon as S of two
+//       tiles back has run), then V' rows and the ones column (two buffers,
+//       free again once the tile's O MMAs have run);
 //   (a warp runs on SMSP warp % 4: each SMSP holds two softmax warps and one
 //   side of the operand work, so that fewer code paths share its instruction
 //   cache)
@@ -66,6 +67,7 @@ constexpr int kCMaxChunk = 1024;          // an item's page ids: two per lane of
 constexpr int kCOpWarps = 8, kCEpWarps = 8;
 constexpr int kCThreadsTC = 32 * (2 + kCOpWarps + kCEpWarps);
 constexpr int kCStages = 3;
+constexpr long long kCPollLimit = 1LL << 26;   // idle polls of the MMA lane before it gives up
 constexpr int kCVN = 144;                 // V' columns: 128 channels, the ones column, 15 zero columns
 constexpr float kInvSqrtDC = 0.08838834764831845f;
 constexpr float kSqrtHalfPiC = 1.2533141373155003f;
@@ -291,7 +293,7 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
         bar_init(barx(G::kRecEmpty + s), kCOpWarps);
       }
       for (int s = 0; s < 2; ++s) {
-        bar_init(barx(G::kKOps + s), kCOpWarps / 2);
+        bar_init(barx(G::kKOps + s), kCOpWarps);      // K^ rows (K side) and A' rows (V side)
         bar_init(barx(G::kVOps + s), kCOpWarps / 2);
         bar_init(barx(G::kKFree + s), 1);
         bar_init(barx(G::kVFree + s), 1);
@@ -400,9 +402,7 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
         (void)bar_wait(barx(G::kRecFull + j % kCStages), (j / kCStages) & 1, f2);
     }
   } else if (warp == 1) {
-    // ---- MMA issue, one lane, in stream order: S(k + 1) goes ahead of O(k) (its
-    // operands and the release of S(k) come early in tile k), except that an item's
-    // first S waits for its queries, which follow O(k) of the item before --------------
+    // ---- MMA issue, one lane ------------------------------------------------------------
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_f16(kCT), id_o = idesc_f16(kCVN) | (1u << 16);   // O: B MN-major
       auto issue_s = [&](int k) {
@@ -428,32 +428,42 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
         mma_commit(barx(G::kODone));
         mma_commit(barx(G::kVFree + (k & 1)));
       };
-      int items = 0;
-      CDesc d{};
-      bool run = bar_wait(barx(G::kKOps), 0, failed);
-      if (run) {
-        d = desc[0];
-        run = d.item >= 0 && bar_wait(barx(G::kQReady), items++ & 1, failed);
-      }
-      if (run) issue_s(0);
-      for (int k = 0; run; ++k) {
-        if (!bar_wait(barx(G::kKOps + ((k + 1) & 1)), ((k + 1) >> 1) & 1, failed)) break;
-        const CDesc dn = desc[(k + 1) & 3];
-        const bool more = dn.item >= 0;
-        if (more && !dn.first) {
-          if (!bar_wait(barx(G::kSEmpty), k & 1, failed)) break;
-          issue_s(k + 1);
+      // event-driven: S(k) once its K operands are in (both sides), S(k - 1) was read and, for an
+      // item's first tile, its queries are in; O(k) once its V' and P(k) are in.  Nothing ready:
+      // a short sleep, so that the poll does not take issue slots from the SMSP's other warps.
+      int ns = 0, no = 0, end = 1 << 30, items = 0;
+      uint32_t firsts = 0u;                            // bit k % 32: tile k opens its item
+      long long idle = 0;
+      while (no < end) {
+        bool did = false;
+        if (ns < end && ns <= no + 2 && bar_poll(barx(G::kKOps + (ns & 1)), (ns >> 1) & 1)) {
+          const CDesc dn = desc[ns & 3];
+          if (dn.item < 0) {
+            end = ns;
+            did = true;
+          } else if ((ns == 0 || bar_poll(barx(G::kSEmpty), (ns - 1) & 1)) &&
+                     (!dn.first || bar_poll(barx(G::kQReady), items & 1))) {
+            items += dn.first ? 1 : 0;
+            issue_s(ns);
+            firsts = dn.first ? (firsts | (1u << (ns & 31))) : (firsts & ~(1u << (ns & 31)));
+            ++ns;
+            did = true;
+          }
         }
-        if (!bar_wait(barx(G::kVOps + (k & 1)), (k >> 1) & 1, failed)) break;
-        if (!bar_wait(barx(G::kPFull), k & 1, failed)) break;
-        issue_o(k, d.first != 0);
-        if (more && dn.first) {
-          if (!bar_wait(barx(G::kQReady), items++ & 1, failed)) break;
-          if (!bar_wait(barx(G::kSEmpty), k & 1, failed)) break;
-          issue_s(k + 1);
+        if (no < ns && bar_poll(barx(G::kVOps + (no & 1)), (no >> 1) & 1) && bar_poll(barx(G::kPFull), no & 1)) {
+          issue_o(no, (firsts >> (no & 31)) & 1u);
+          ++no;
+          did = true;
         }
-        if (!more) break;
-        d = dn;
+        if (did) {
+          idle = 0;
+        } else {
+          if (++idle > kCPollLimit) {
+            failed = true;
+            break;
+          }
+          __nanosleep(32);
+        }
       }
       mma_commit(barx(G::kDrain));                     // every MMA issued completes before the CTA ends
       bool f2 = false;
@@ -461,18 +471,20 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
     }
     __syncwarp();
   } else if (warp < 8 || warp >= 16) {
-    // ---- operands: K side on warps 4, 5, 16, 17 (the first two SMSPs), V side on warps 2, 3,
-    // 6, 7 (the other two), each its own pipeline ---------------------------------------------
+    // ---- operands: K side on warps 4, 5, 16, 17 (the first two SMSPs): K^ rows and the
+    // token factors; V side on warps 2, 3, 6, 7 (the other two): the sign rows A', then
+    // V' and the ones column.  A tile's S MMAs wait for both sides' K-operand arrivals;
+    // the V side builds A'(k) as soon as S(k - 2) has run, ahead of V'(k) --------------------
     const bool vside = warp < 4 || (warp >= 6 && warp < 8);
     const int ridx = vside ? (warp < 4 ? warp - 2 : warp - 4) : (warp < 8 ? warp - 4 : warp - 14);
     const int u = 32 * ridx + lane + (vside ? 128 : 0);   // K side 0 .. 127, V side 128 .. 255
-    const int t = u & 63, hf = (u >> 6) & 1;           // K side: token row, channel half (warp-uniform)
+    const int t = u & 63, hf = (u >> 6) & 1;           // token row, channel (projection) half (warp-uniform)
     const uint32_t lane_off = static_cast<uint32_t>(lane) * 4u;
     for (int seq = 0;; ++seq) {
       const int s = seq % kCStages, buf = seq & 1;
       bool ok = bar_wait(barx(G::kRecFull + s), (seq / kCStages) & 1, failed);
-      if (seq >= 2)                                    // this side's MMAs of two tiles back have read the buffer
-        ok = bar_wait(barx((vside ? G::kVFree : G::kKFree) + buf), ((seq - 2) >> 1) & 1, failed) && ok;
+      if (seq >= 2)                                    // the S MMAs of two tiles back have read K^ and A'
+        ok = bar_wait(barx(G::kKFree + buf), ((seq - 2) >> 1) & 1, failed) && ok;
       if (!__all_sync(0xffffffffu, ok)) {
         failed = true;
         break;
@@ -480,43 +492,20 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
       const CDesc d = rec_desc[s];
       const uint32_t rec = sb + G::REC + s * G::STAGE;
       const uint32_t ob = sb + G::OPS + buf * G::OPS_BYTES;
+      const int pg = t >> 4, slot = t & 15;
+      const bool tv = d.item >= 0 && t < d.npos && ((d.mask >> pg) & 1u);
+      const uint32_t kb = rec + pg * G::PAGE;
       if (!vside) {
         if (d.item >= 0) {
-          const int pg = t >> 4, slot = t & 15;
-          const bool tv = t < d.npos && ((d.mask >> pg) & 1u);
-          const uint32_t kb = rec + pg * G::PAGE;
-          float fa = 0.0f, fb = 0.0f;
-          if (tv) {
+          float fa = 0.0f;
+          if (tv)
             fa = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(kb + G::K_NORM + 2 * slot)))) *
                  kInvSqrtDC;
-            if (QJL)
-              fb = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(kb + G::K_RNORM + 2 * slot)))) *
-                   (kSqrtHalfPiC / 128.0f);
-          }
           if (hf == 0)
             half_rows<KBH, false>(ob + G::KH, kb + slot * G::CBK, t, 0, tv, sb + G::LUT + lut_off(KBH) + lane_off, __half2());
           else
             half_rows<KBL, false>(ob + G::KH, kb + slot * G::CBK + 8 * KBH, t, 1, tv, sb + G::LUT + lut_off(KBL) + lane_off,
                                   __half2());
-          if (QJL) {                                   // A' = (fb / fa)(2 b - 1) for the 64 projections of this half
-            uint2 sw = make_uint2(0u, 0u);
-            if (tv) sw = lds64(kb + G::K_SIGNS + slot * 16 + 8 * hf);
-            const __half2 fb2 = __float2half2_rn(fa > 0.0f ? fb / fa : 0.0f);
-            const uint32_t fbv = tv ? *reinterpret_cast<const uint32_t*>(&fb2) : 0u;   // |A'| in both halves
-            const uint32_t vm = tv ? 0xFFFFFFFFu : 0u;
-            const uint32_t st = sb + G::SGN + lane_off * 2;
-#pragma unroll 1
-            for (int cc = 0; cc < 8; cc += 2) {           // two chunks per step, loads first
-              const uint32_t w = cc < 4 ? sw.x : sw.y;
-              const uint32_t b0 = __byte_perm(w, 0u, 0x4440u + (cc & 3)), b1 = __byte_perm(w, 0u, 0x4441u + (cc & 3));
-              const uint2 l0 = lds64(st + (b0 & 0xFu) * 256u), h0 = lds64(st + (b0 >> 4) * 256u);
-              const uint2 l1 = lds64(st + (b1 & 0xFu) * 256u), h1 = lds64(st + (b1 >> 4) * 256u);
-              sts128(ob + G::AS + chunk_off(t, 8 * hf + cc, kCT), fbv | (l0.x & vm), fbv | (l0.y & vm), fbv | (h0.x & vm),
-                     fbv | (h0.y & vm));
-              sts128(ob + G::AS + chunk_off(t, 8 * hf + cc + 1, kCT), fbv | (l1.x & vm), fbv | (l1.y & vm),
-                     fbv | (h1.x & vm), fbv | (h1.y & vm));
-            }
-          }
           if (hf == 0) {
             const uint32_t fac = sb + G::FAC + (seq & 3) * 512;
             stsf(fac + 4 * t, fa * a.scale_log2);
@@ -531,10 +520,48 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
           bar_arrive(barx(G::kDescFull + (seq & 3)));
           if (d.item >= 0) bar_arrive(barx(G::kRecEmpty + s));
         }
-      } else if (d.item >= 0) {
-        const int pg = t >> 4, slot = t & 15;
-        const bool tv = t < d.npos && ((d.mask >> pg) & 1u);
-        const uint32_t vb = rec + pg * G::PAGE + G::KBB;
+        if (d.item < 0) break;
+        continue;
+      }
+      // V side: A' = (fb / fa)(2 b - 1) for the 64 projections of this half (zero for a missing token)
+      if (QJL && d.item >= 0) {
+        float ratio = 0.0f;
+        uint2 sw = make_uint2(0u, 0u);
+        if (tv) {
+          const float nk = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(kb + G::K_NORM + 2 * slot))));
+          const float rk = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(kb + G::K_RNORM + 2 * slot))));
+          sw = lds64(kb + G::K_SIGNS + slot * 16 + 8 * hf);
+          const float fa = nk * kInvSqrtDC, fb = rk * (kSqrtHalfPiC / 128.0f);
+          ratio = fa > 0.0f ? fb / fa : 0.0f;
+        }
+        const __half2 fb2 = __float2half2_rn(ratio);
+        const uint32_t fbv = tv ? *reinterpret_cast<const uint32_t*>(&fb2) : 0u;   // |A'| in both halves
+        const uint32_t vm = tv ? 0xFFFFFFFFu : 0u;
+        const uint32_t st = sb + G::SGN + lane_off * 2;
+#pragma unroll 1
+        for (int cc = 0; cc < 8; cc += 2) {               // two chunks per step, loads first
+          const uint32_t w = cc < 4 ? sw.x : sw.y;
+          const uint32_t b0 = __byte_perm(w, 0u, 0x4440u + (cc & 3)), b1 = __byte_perm(w, 0u, 0x4441u + (cc & 3));
+          const uint2 l0 = lds64(st + (b0 & 0xFu) * 256u), h0 = lds64(st + (b0 >> 4) * 256u);
+          const uint2 l1 = lds64(st + (b1 & 0xFu) * 256u), h1 = lds64(st + (b1 >> 4) * 256u);
+          sts128(ob + G::AS + chunk_off(t, 8 * hf + cc, kCT), fbv | (l0.x & vm), fbv | (l0.y & vm), fbv | (h0.x & vm),
+                 fbv | (h0.y & vm));
+          sts128(ob + G::AS + chunk_off(t, 8 * hf + cc + 1, kCT), fbv | (l1.x & vm), fbv | (l1.y & vm),
+                 fbv | (h1.x & vm), fbv | (h1.y & vm));
+        }
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) bar_arrive(barx(G::kKOps + buf));
+      if (d.item < 0) break;
+      // V' rows, once the O MMAs of two tiles back have read the buffer
+      ok = seq < 2 || bar_wait(barx(G::kVFree + buf), ((seq - 2) >> 1) & 1, failed);
+      if (!__all_sync(0xffffffffu, ok)) {
+        failed = true;
+        break;
+      }
+      {
+        const uint32_t vb = kb + G::KBB;
         float fv = 0.0f;
         if (tv)
           fv = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(vb + G::V_NORM + 2 * slot)))) * kInvSqrtDC;
@@ -548,14 +575,13 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
           half_rows<VBL, true>(ob + G::VT, vb + slot * G::CBV + 8 * VBH, t, 1, tv, sb + G::LUT + lut_off(VBL) + lane_off,
                                fv2);
         }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          bar_arrive(barx(G::kVOps + buf));
-          bar_arrive(barx(G::kRecEmpty + s));
-        }
       }
-      if (d.item < 0) break;
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        bar_arrive(barx(G::kVOps + buf));
+        bar_arrive(barx(G::kRecEmpty + s));
+      }
     }
   } else {
     // ---- softmax (thread = query row of the item, tensor-memory lane r) --------------------
