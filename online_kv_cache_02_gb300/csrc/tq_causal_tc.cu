@@ -402,73 +402,75 @@ __global__ void __launch_bounds__(kCThreadsTC, 1)
         (void)bar_wait(barx(G::kRecFull + j % kCStages), (j / kCStages) & 1, f2);
     }
   } else if (warp == 1) {
-    // ---- MMA issue, one lane ------------------------------------------------------------
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_f16(kCT), id_o = idesc_f16(kCVN) | (1u << 16);   // O: B MN-major
-      auto issue_s = [&](int k) {
-        const uint32_t kh = sb + G::OPS + (k & 1) * G::OPS_BYTES + G::KH, as = kh - G::KH + G::AS;
-        tc_after();
+    // ---- MMA issue: the whole warp runs the loop converged (branch conditions are warp
+    // votes) and one elected lane issues each MMA and commit, so that the operands stay in
+    // uniform registers --------------------------------------------------------------------
+    constexpr uint32_t id_s = idesc_f16(kCT), id_o = idesc_f16(kCVN) | (1u << 16);   // O: B MN-major
+    auto uni = [](bool x) { return __all_sync(0xffffffffu, x); };
+    auto issue_s = [&](int k) {
+      const uint32_t kh = sb + G::OPS + (k & 1) * G::OPS_BYTES + G::KH, as = kh - G::KH + G::AS;
+      tc_after();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) mma_ts(tmem + kTS, tmem + kTQH + 8u * j, kdesc(kh, kCT, j), id_s, j > 0 ? 1u : 0u);
+      for (int j = 0; j < 8; ++j) mma_ts_warp(tmem + kTS, tmem + kTQH + 8u * j, kdesc(kh, kCT, j), id_s, j > 0 ? 1u : 0u);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) mma_ts(tmem + kTS, tmem + kTQL + 8u * j, kdesc(kh, kCT, j), id_s, 1u);
-        if (QJL) {
+      for (int j = 0; j < 8; ++j) mma_ts_warp(tmem + kTS, tmem + kTQL + 8u * j, kdesc(kh, kCT, j), id_s, 1u);
+      if (QJL) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) mma_ts(tmem + kTS, tmem + kTU + 8u * j, kdesc(as, kCT, j), id_s, 1u);
-        }
-        mma_commit(barx(G::kSFull));
-        mma_commit(barx(G::kKFree + (k & 1)));
-      };
-      auto issue_o = [&](int k, bool first) {
-        const uint32_t vt = sb + G::OPS + (k & 1) * G::OPS_BYTES + G::VT;
-        tc_after();
+        for (int j = 0; j < 8; ++j) mma_ts_warp(tmem + kTS, tmem + kTU + 8u * j, kdesc(as, kCT, j), id_s, 1u);
+      }
+      mma_commit_warp(barx(G::kSFull));
+      mma_commit_warp(barx(G::kKFree + (k & 1)));
+    };
+    auto issue_o = [&](int k, bool first) {
+      const uint32_t vt = sb + G::OPS + (k & 1) * G::OPS_BYTES + G::VT;
+      tc_after();
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          mma_ts(tmem + kTO, tmem + kTP + 8u * j, sdesc_mn(vt + 2048u * j), id_o, (first && j == 0) ? 0u : 1u);
-        mma_commit(barx(G::kODone));
-        mma_commit(barx(G::kVFree + (k & 1)));
-      };
-      // event-driven: S(k) once its K operands are in (both sides), S(k - 1) was read and, for an
-      // item's first tile, its queries are in; O(k) once its V' and P(k) are in.  Nothing ready:
-      // a short sleep, so that the poll does not take issue slots from the SMSP's other warps.
-      int ns = 0, no = 0, end = 1 << 30, items = 0;
-      uint32_t firsts = 0u;                            // bit k % 32: tile k opens its item
-      long long idle = 0;
-      while (no < end) {
-        bool did = false;
-        if (ns < end && ns <= no + 2 && bar_poll(barx(G::kKOps + (ns & 1)), (ns >> 1) & 1)) {
-          const CDesc dn = desc[ns & 3];
-          if (dn.item < 0) {
-            end = ns;
-            did = true;
-          } else if ((ns == 0 || bar_poll(barx(G::kSEmpty), (ns - 1) & 1)) &&
-                     (!dn.first || bar_poll(barx(G::kQReady), items & 1))) {
-            items += dn.first ? 1 : 0;
-            issue_s(ns);
-            firsts = dn.first ? (firsts | (1u << (ns & 31))) : (firsts & ~(1u << (ns & 31)));
-            ++ns;
-            did = true;
-          }
-        }
-        if (no < ns && bar_poll(barx(G::kVOps + (no & 1)), (no >> 1) & 1) && bar_poll(barx(G::kPFull), no & 1)) {
-          issue_o(no, (firsts >> (no & 31)) & 1u);
-          ++no;
+      for (int j = 0; j < 4; ++j)
+        mma_ts_warp(tmem + kTO, tmem + kTP + 8u * j, sdesc_mn(vt + 2048u * j), id_o, (first && j == 0) ? 0u : 1u);
+      mma_commit_warp(barx(G::kODone));
+      mma_commit_warp(barx(G::kVFree + (k & 1)));
+    };
+    // event-driven: S(k) once its K operands are in (both sides), S(k - 1) was read and, for an
+    // item's first tile, its queries are in; O(k) once its V' and P(k) are in.  Nothing ready:
+    // a short sleep, so that the poll does not take issue slots from the SMSP's other warps.
+    int ns = 0, no = 0, end = 1 << 30, items = 0;
+    uint32_t firsts = 0u;                              // bit k % 32: tile k opens its item
+    long long idle = 0;
+    while (no < end) {
+      bool did = false;
+      if (ns < end && ns <= no + 2 && uni(bar_poll(barx(G::kKOps + (ns & 1)), (ns >> 1) & 1))) {
+        const CDesc dn = desc[ns & 3];
+        const bool fin = uni(dn.item < 0), first = uni(dn.first != 0);
+        if (fin) {
+          end = ns;
+          did = true;
+        } else if ((ns == 0 || uni(bar_poll(barx(G::kSEmpty), (ns - 1) & 1))) &&
+                   (!first || uni(bar_poll(barx(G::kQReady), items & 1)))) {
+          items += first ? 1 : 0;
+          issue_s(ns);
+          firsts = first ? (firsts | (1u << (ns & 31))) : (firsts & ~(1u << (ns & 31)));
+          ++ns;
           did = true;
         }
-        if (did) {
-          idle = 0;
-        } else {
-          if (++idle > kCPollLimit) {
-            failed = true;
-            break;
-          }
-          __nanosleep(32);
-        }
       }
-      mma_commit(barx(G::kDrain));                     // every MMA issued completes before the CTA ends
-      bool f2 = false;
-      (void)bar_wait(barx(G::kDrain), 0, f2);
+      if (no < ns && uni(bar_poll(barx(G::kVOps + (no & 1)), (no >> 1) & 1)) && uni(bar_poll(barx(G::kPFull), no & 1))) {
+        issue_o(no, (firsts >> (no & 31)) & 1u);
+        ++no;
+        did = true;
+      }
+      if (did) {
+        idle = 0;
+      } else {
+        if (++idle > kCPollLimit) {
+          failed = true;
+          break;
+        }
+        __nanosleep(32);
+      }
     }
+    mma_commit_warp(barx(G::kDrain));                  // every MMA issued completes before the CTA ends
+    bool f2 = false;
+    (void)bar_wait(barx(G::kDrain), 0, f2);
     __syncwarp();
   } else if (warp < 8 || warp >= 16) {
     // ---- operands: K side on warps 4, 5, 16, 17 (the first two SMSPs): K^ rows and the

@@ -159,6 +159,23 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, 
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
+// The same MMA and commit issued by the whole (converged) warp, one elected
+// lane executing them: in converged code the compiler keeps the operands in
+// uniform registers, where a single-lane branch would move them there per MMA.
+// The elected lane is the lowest active one, so commits track the same lane's MMAs.
+__device__ __forceinline__ void mma_ts_warp(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_warp(uint32_t b) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(b)
+      : "memory");
+}
 // Store 32 columns of this thread's lane (32x32b shape), then wait for the stores.
 __device__ __forceinline__ void tst32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
