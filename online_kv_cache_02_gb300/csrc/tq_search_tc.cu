@@ -273,24 +273,26 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
         (void)bar_wait(barx(L::kRecFull + j % S), (j / S) & 1, f2);
     }
   } else if (warp == 1) {
-    // ---- MMA issue --------------------------------------------------------------
-    if (lane == 0) {
+    // ---- MMA issue: the whole warp converged (conditions are warp votes), an elected lane
+    // issuing each MMA and commit, so the operands stay in uniform registers ------------------
+    {
       constexpr uint32_t id = idesc_f16(kQB);
+      auto uni = [](bool x) { return __all_sync(0xffffffffu, x); };
       int done = 0;
       for (int i = 0; i < local; ++i) {
         const int slot = i & 1;
-        if (!bar_wait(barx(L::kAFull), i & 1, failed)) break;
-        if (i >= 2 && !bar_wait(barx(L::kTEmpty + slot), ((i - 2) >> 1) & 1, failed)) break;
+        if (!uni(bar_wait(barx(L::kAFull), i & 1, failed))) break;
+        if (i >= 2 && !uni(bar_wait(barx(L::kTEmpty + slot), ((i - 2) >> 1) & 1, failed))) break;
         tc_after();
         const uint32_t d1 = tmem + 128u * slot, d2 = d1 + 64u;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mma_ss(d1, kdesc(sb + L::AK, kTV, k), kdesc(sb + L::QH, kQB, k), id, k > 0);
+        for (int k = 0; k < 8; ++k) mma_ss_warp(d1, kdesc(sb + L::AK, kTV, k), kdesc(sb + L::QH, kQB, k), id, k > 0);
         if (QJL) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) mma_ss(d2, kdesc(sb + L::AS, kTV, k), kdesc(sb + L::UH, kQB, k), id, k > 0);
+          for (int k = 0; k < 8; ++k) mma_ss_warp(d2, kdesc(sb + L::AS, kTV, k), kdesc(sb + L::UH, kQB, k), id, k > 0);
         }
-        mma_commit(barx(L::kAEmpty));
-        mma_commit(barx(L::kTFull + slot));
+        mma_commit_warp(barx(L::kAEmpty));
+        mma_commit_warp(barx(L::kTFull + slot));
         done = i + 1;
       }
       bool f2 = false;
