@@ -271,13 +271,17 @@ tq_status tq_append_decode_ex(const tq_ctx* ctx, const void* k_new, const void* 
  * first).  Query t of sequence b attends over positions 0 .. start_pos[b] + t
  * with the scores, softmax and value sums of tq_decode_attention; out (device,
  * fp32): [batch][n_new][Hq][d].  start_pos[b] + n_new <= max_seq_len.  The
- * context is split into chunks of chunk_tokens (0 picks one) merged per query.
- * Runs the bit-width combinations of the persistent decode kernel (d = 128,
- * m = 128, split 64; K/V bits 3/3, 4-3/4-3, 3-2/3-2, 4/4, 2/2, 4/2) with
- * |softmax_scale| <= 1/sqrt(d) (the 2e-3 bar of tq_decode_attention; its
- * query is fp16 hi + lo), else TQ_ERR_UNSUPPORTED; query heads per KV head <= 8.  workspace (device) of
- * tq_causal_workspace_size bytes; stream-ordered, no allocation.  Errors as
- * tq_decode_attention. */
+ * context is split into chunks of chunk_tokens (0 picks one, 256 to 1024 tokens)
+ * merged per query.  Runs the bit-width combinations of the persistent decode
+ * kernel (d = 128, m = 128, split 64; K/V bits 3/3, 4-3/4-3, 3-2/3-2, 4/4, 2/2,
+ * 4/2) with |softmax_scale| <= 1/sqrt(d) (the 2e-3 bar of tq_decode_attention;
+ * its query is fp16 hi + lo), else TQ_ERR_UNSUPPORTED; query heads per KV head
+ * <= 8.  Chunks of at most 1024 tokens run on the tensor cores (blocks of 128
+ * query rows t * G + g of one sequence and KV head against 64-token tiles);
+ * longer chunks on the lookup-table kernel (blocks of 8 rows).  q needs no
+ * particular alignment (16-byte aligned rows load faster).  workspace (device)
+ * of tq_causal_workspace_size bytes for the same chunk_tokens; stream-ordered,
+ * no allocation.  Errors as tq_decode_attention. */
 tq_status tq_causal_workspace_size(const tq_ctx* ctx, int batch, int n_new, int num_q_heads, int max_seq_len,
                                    int chunk_tokens, size_t* bytes);
 tq_status tq_causal_attention(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batch, int n_new,
