@@ -230,11 +230,8 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
   const int d = cfg->d, m = cfg->m;
   tq_ctx* ctx = new (std::nothrow) tq_ctx();
   if (!ctx) return TQ_ERR_OOM;
-  ctx->fused_mu = new (std::nothrow) std::mutex();
-  if (!ctx->fused_mu) { delete ctx; return TQ_ERR_OOM; }
   ctx->cfg = *cfg;
   if (cudaGetDevice(&ctx->device) != cudaSuccess) {
-    delete static_cast<std::mutex*>(ctx->fused_mu);
     delete ctx;
     return TQ_ERR_CUDA;
   }
@@ -310,7 +307,6 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
   size_t total = align256(o_cnt + 2 * sizeof(unsigned long long));
   void* blk = nullptr;
   if (cudaMalloc(&blk, total) != cudaSuccess) {
-    delete static_cast<std::mutex*>(ctx->fused_mu);
     delete ctx;
     cudaGetLastError();
     return TQ_ERR_OOM;
@@ -346,34 +342,13 @@ extern "C" tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out) {
             cudaMemcpy(ctx->tab.s_df, sdf.data(), sizeof(float) * d * m * 2, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemcpy(ctx->tab.wt, wt.data(), sizeof(float) * d * (d + m), cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemset(b + o_err, 0, total - o_err) == cudaSuccess;
-  if (!ok) { cudaFree(blk); delete static_cast<std::mutex*>(ctx->fused_mu); delete ctx; cudaGetLastError(); return TQ_ERR_CUDA; }
-  // the fused decode step's second stream and its fork/join events: made here,
-  // so tq_append_decode creates nothing
-  if (cudaStreamCreateWithFlags(&ctx->aux_stream, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaEventCreateWithFlags(&ctx->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&ctx->ev_join, cudaEventDisableTiming) != cudaSuccess) {
-    cudaGetLastError();
-    if (ctx->aux_stream) cudaStreamDestroy(ctx->aux_stream);
-    if (ctx->ev_fork) cudaEventDestroy(ctx->ev_fork);
-    if (ctx->ev_join) cudaEventDestroy(ctx->ev_join);
-    cudaFree(blk);
-    delete static_cast<std::mutex*>(ctx->fused_mu);
-    delete ctx;
-    return TQ_ERR_CUDA;
-  }
+  if (!ok) { cudaFree(blk); delete ctx; cudaGetLastError(); return TQ_ERR_CUDA; }
   *out = ctx;
   return TQ_OK;
 }
 
 extern "C" tq_status tq_destroy(tq_ctx* ctx) {
   if (!ctx) return TQ_ERR_INVALID_ARG;
-  if (ctx->aux_stream) {
-    cudaStreamSynchronize(ctx->aux_stream);
-    cudaStreamDestroy(ctx->aux_stream);
-    cudaEventDestroy(ctx->ev_fork);
-    cudaEventDestroy(ctx->ev_join);
-  }
-  delete static_cast<std::mutex*>(ctx->fused_mu);
   cudaError_t e = cudaFree(ctx->dev_block);
   delete ctx;
   return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
@@ -497,13 +472,6 @@ int sm_count() {
   return sms;
 }
 
-// SMs left to the one-token append of a fused step: one per 128-vector tile of
-// K and of V (the append's CTAs), at most 8.
-int append_reserve(int batch, int H) {
-  const long long tiles = 2 * ((static_cast<long long>(batch) * H + 127) / 128);
-  return static_cast<int>(tiles < 8 ? tiles : 8);
-}
-
 }  // namespace
 
 extern "C" tq_status tq_decode_chunk(const tq_ctx* ctx, int batch, int Hq, int H, long long total_tokens,
@@ -511,8 +479,8 @@ extern "C" tq_status tq_decode_chunk(const tq_ctx* ctx, int batch, int Hq, int H
   if (!ctx || !chunk_tokens || batch < 1 || Hq < 1 || H < 1 || Hq % H || max_seq_len < 0 || total_tokens < 0 ||
       total_tokens > static_cast<long long>(batch) * max_seq_len)
     return TQ_ERR_INVALID_ARG;
-  int ctas = ctx->cfg.d == kD ? lut_decode_ctas(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H) : 0;
-  if (fused_append && ctas > 0) ctas -= append_reserve(batch, H);
+  (void)fused_append;   // the fused step's partials kernel has every SM (the append runs before it)
+  const int ctas = ctx->cfg.d == kD ? lut_decode_ctas(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H) : 0;
   if (ctas > 0)
     *chunk_tokens = pick_chunk_total(batch, H, total_tokens, max_seq_len, ctas);
   else
@@ -532,13 +500,11 @@ extern "C" tq_status tq_decode_attention(const tq_ctx* ctx, const void* q, tq_dt
 }
 
 namespace {
-// The fused decode step (tq_append_decode): the partials kernel covers the
-// cached tokens and leaves `reserve` SMs to the new token's quantize-append on
-// the context's second stream; the merge waits for it (join) and adds the new
-// token itself.  Optional events bracket the partials launch.
+// The fused decode step (tq_append_decode): the append kernel, then qprep as
+// its dependent launch (overlapping it, finishing after it), the partials
+// kernel over the L + 1 tokens and the merge.  Optional events bracket the
+// partials launch.
 struct FusedStep {
-  int reserve;
-  cudaEvent_t join;
   cudaEvent_t partials_begin, partials_end;
 };
 
@@ -566,7 +532,6 @@ tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batc
     return TQ_ERR_INVALID_ARG;
   const bool generic = ctx->cfg.d != kD || precise_scale(ctx, softmax_scale);
   int lut_ctas = generic ? 0 : lut_decode_ctas(ctx->kl, ctx->vl, ctx->cfg.m, Hq / H);
-  if (fused && lut_ctas > 0) lut_ctas -= fused->reserve;
   int chunk = chunk_tokens              ? chunk_tokens
               : lut_ctas > 0            ? pick_chunk_warps(batch * H, max_seq_len, lut_ctas)
                                         : pick_chunk(batch * H, max_seq_len);
@@ -610,13 +575,11 @@ tq_status decode_impl(const tq_ctx* ctx, const void* q, tq_dtype dtype, int batc
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (generic) return cuda_status(launch_decode_generic(a, d, stages, st));
   if (!fused) return cuda_status(launch_decode(a, stages, st));
-  a.new_token = 1;                       // len_add is 0 here: the partials cover [0, seq_lens[b])
-  a.max_ctas = sm_count() - fused->reserve;
+  a.chained = 1;
   bool ok = launch_decode(a, TQ_STAGE_QPREP, st) == cudaSuccess;
   if (ok && fused->partials_begin) ok = cudaEventRecord(fused->partials_begin, st) == cudaSuccess;
   ok = ok && launch_decode(a, TQ_STAGE_PARTIALS, st) == cudaSuccess;
   if (ok && fused->partials_end) ok = cudaEventRecord(fused->partials_end, st) == cudaSuccess;
-  ok = ok && cudaStreamWaitEvent(st, fused->join, 0) == cudaSuccess;
   ok = ok && launch_decode(a, TQ_STAGE_MERGE, st) == cudaSuccess;
   return ok ? TQ_OK : cuda_fail(cudaGetLastError());
 }
@@ -674,22 +637,37 @@ extern "C" tq_status tq_append_decode_ex(const tq_ctx* ctx, const void* k_new, c
       return cuda_fail(cudaGetLastError());
     return st;
   }
-  tq_ctx* c = const_cast<tq_ctx*>(ctx);
-  // the fork/join events are shared by every call on this context: one host
-  // thread at a time records and waits on them
-  std::lock_guard<std::mutex> lock(*static_cast<std::mutex*>(c->fused_mu));
+  // one stream: the append kernel (a warp per new vector), then the decode
+  // over L + 1 tokens with qprep launched dependent on the append
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  FusedStep f{append_reserve(batch, H), c->ev_join, static_cast<cudaEvent_t>(partials_begin),
-              static_cast<cudaEvent_t>(partials_end)};
-  // fork: the quantize-append of the new token runs on the second stream
-  if (cudaEventRecord(c->ev_fork, s) != cudaSuccess || cudaStreamWaitEvent(c->aux_stream, c->ev_fork, 0) != cudaSuccess)
-    return TQ_ERR_CUDA;
-  st = quantize_impl(ctx, k_new, v_new, dtype, batch, 1, H, seq_lens, block_table, maxp, num_pages, k_cache, v_cache,
-                     c->aux_stream, f.reserve);
-  if (st != TQ_OK) return st;
-  if (cudaEventRecord(c->ev_join, c->aux_stream) != cudaSuccess) return TQ_ERR_CUDA;
-  // qprep and the partials over the cached tokens, then (joined) the merge
-  return decode_impl(ctx, q, dtype, batch, Hq, H, seq_lens, 0, max_seq_len, block_table, maxp, num_pages, k_cache,
+  QuantizeArgs qa[2]{};
+  for (int kind = 0; kind < 2; ++kind) {
+    QuantizeArgs& x = qa[kind];
+    x.x = kind == 0 ? k_new : v_new;
+    x.f32 = dtype == TQ_F32;
+    x.batch = batch;
+    x.n_new = 1;
+    x.H = H;
+    x.start_pos = seq_lens;
+    x.block_table = block_table;
+    x.maxp = maxp;
+    x.num_pages = num_pages;
+    x.cache = static_cast<uint8_t*>(kind == 0 ? k_cache : v_cache);
+    x.lay = kind == 0 ? ctx->kl : ctx->vl;
+    x.page_bytes = static_cast<long long>(x.lay.block_bytes) * H;
+    x.m = ctx->cfg.m;
+    x.tab = ctx->tab;
+  }
+  cudaError_t e = cudaSuccess;
+  if (!launch_append(qa[0], qa[1], s, &e)) {
+    st = quantize_impl(ctx, k_new, v_new, dtype, batch, 1, H, seq_lens, block_table, maxp, num_pages, k_cache,
+                       v_cache, stream, 0);
+    if (st != TQ_OK) return st;
+  } else if (e != cudaSuccess) {
+    return cuda_fail(e);
+  }
+  FusedStep f{static_cast<cudaEvent_t>(partials_begin), static_cast<cudaEvent_t>(partials_end)};
+  return decode_impl(ctx, q, dtype, batch, Hq, H, seq_lens, 1, max_seq_len, block_table, maxp, num_pages, k_cache,
                      v_cache, chunk_tokens, softmax_scale, out, workspace, workspace_bytes, TQ_STAGE_ALL, stream, &f);
 }
 

@@ -47,24 +47,27 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // [q~; u] = W q with W = [Pi; S Pi] (fp32, built once at create time): a
 // block takes 32 query heads x 64 outputs; its 32 KB slice of W^T arrives in
-// one round of independent 16-byte loads (dynamic shared memory), then each
-// of the 128 threads computes a 4 heads x 4 outputs tile (one 16-byte W load
-// and four broadcast q loads per 16 FMAs), every output summed over k in order.
+// one round of independent 16-byte loads (dynamic shared memory), then four
+// groups of 128 threads take a quarter of k each, a thread a 4 heads x 4
+// outputs tile (one 16-byte W load and four broadcast q loads per 16 FMAs);
+// the four partial tiles are summed through shared memory.
 constexpr int kQP = 32;
 constexpr int kQO = 64;
-constexpr int kQThreads = 128;
+constexpr int kQThreads = 512;
+constexpr int kQK = kD / (kQThreads / 128);      // k per group
 constexpr int kQPad = kD + 4;                   // q rows, padded
-constexpr int kQprepSmem = (kD * kQO + kQP * kQPad) * 4;
+constexpr int kQprepSmem = (kD * kQO + kQP * kQPad + (kQThreads / 128) * kQP * kQO) * 4;
 
 __global__ void __launch_bounds__(kQThreads) qprep_kernel(DecodeArgs a) {
   extern __shared__ __align__(16) float qsm[];
   float(*ws)[kQO] = reinterpret_cast<float(*)[kQO]>(qsm);
   float(*qs)[kQPad] = reinterpret_cast<float(*)[kQPad]>(qsm + kD * kQO);
+  float(*ps)[kQP][kQO] = reinterpret_cast<float(*)[kQP][kQO]>(qsm + kD * kQO + kQP * kQPad);   // partial tiles
   const int nout = kD + a.m;
   const long long r0 = static_cast<long long>(blockIdx.x) * kQP;
   const int c0 = blockIdx.y * kQO;
   const long long nq = static_cast<long long>(a.B) * (a.T > 0 ? a.T : 1) * a.Hq;   // query rows
-  const int tid = threadIdx.x, oq = 4 * (tid & 15), h0 = 4 * (tid >> 4);
+  const int tid = threadIdx.x, kg = tid >> 7, oq = 4 * (tid & 15), h0 = 4 * ((tid & 127) >> 4);
   pdl_trigger();                       // the partials kernel may launch now (it waits for this grid's results)
   if (blockIdx.x == 0 && blockIdx.y == 0 && tid < 2 && a.sched) a.sched[tid] = 0;   // partials work counters
 #pragma unroll
@@ -75,26 +78,23 @@ __global__ void __launch_bounds__(kQThreads) qprep_kernel(DecodeArgs a) {
     *reinterpret_cast<float4*>(&ws[k][c]) = x;
   }
   {
-    // row tid / 4, channels 32 (tid % 4) .. + 31: every load issued before the first store
-    const int qr = tid >> 2, qc = 32 * (tid & 3);
+    // row tid / 16, channels 8 (tid % 16) .. + 7: every load issued before the first store
+    const int qr = tid >> 4, qc = 8 * (tid & 15);
     const bool in = r0 + qr < nq;
-    float qv[32];
+    float qv[8];
     if ((reinterpret_cast<uintptr_t>(a.q) & 15) == 0 && !a.f32) {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + (r0 + qr) * kD + qc);
+      const uint4 x = in ? *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + (r0 + qr) * kD + qc)
+                         : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 x = in ? src[j] : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          qv[8 * j + 2 * e] = __uint_as_float(xs[e] << 16);
-          qv[8 * j + 2 * e + 1] = __uint_as_float(xs[e] & 0xFFFF0000u);
-        }
+      for (int e = 0; e < 4; ++e) {
+        qv[2 * e] = __uint_as_float(xs[e] << 16);
+        qv[2 * e + 1] = __uint_as_float(xs[e] & 0xFFFF0000u);
       }
     } else if ((reinterpret_cast<uintptr_t>(a.q) & 15) == 0) {
       const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + (r0 + qr) * kD + qc);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 2; ++j) {
         const float4 x = in ? src[j] : make_float4(0.f, 0.f, 0.f, 0.f);
         qv[4 * j] = x.x;
         qv[4 * j + 1] = x.y;
@@ -103,37 +103,56 @@ __global__ void __launch_bounds__(kQThreads) qprep_kernel(DecodeArgs a) {
       }
     } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) qv[j] = in ? load_q(a.q, a.f32, (r0 + qr) * kD + qc + j) : 0.0f;
+      for (int j = 0; j < 8; ++j) qv[j] = in ? load_q(a.q, a.f32, (r0 + qr) * kD + qc + j) : 0.0f;
     }
 #pragma unroll
-    for (int j = 0; j < 32; j += 4)
+    for (int j = 0; j < 8; j += 4)
       *reinterpret_cast<float4*>(&qs[qr][qc + j]) = make_float4(qv[j], qv[j + 1], qv[j + 2], qv[j + 3]);
   }
   __syncthreads();
-  float acc[4][4];
-#pragma unroll
-  for (int r = 0; r < 4; ++r)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) acc[r][c] = 0.0f;
-#pragma unroll 4
-  for (int k = 0; k < kD; ++k) {
-    const float4 w = *reinterpret_cast<const float4*>(&ws[k][oq]);
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const float qv = qs[h0 + r][k];
-      acc[r][0] = fmaf(w.x, qv, acc[r][0]);
-      acc[r][1] = fmaf(w.y, qv, acc[r][1]);
-      acc[r][2] = fmaf(w.z, qv, acc[r][2]);
-      acc[r][3] = fmaf(w.w, qv, acc[r][3]);
-    }
-  }
-  if (c0 + oq < nout) {
+  {
+    float acc[4][4];
 #pragma unroll
     for (int r = 0; r < 4; ++r)
-      if (r0 + h0 + r < nq)
-        *reinterpret_cast<float4*>(a.qprep + (r0 + h0 + r) * nout + c0 + oq) =
-            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[r][c] = 0.0f;
+#pragma unroll 4
+    for (int k = kg * kQK; k < kg * kQK + kQK; ++k) {
+      const float4 w = *reinterpret_cast<const float4*>(&ws[k][oq]);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float qv = qs[h0 + r][k];
+        acc[r][0] = fmaf(w.x, qv, acc[r][0]);
+        acc[r][1] = fmaf(w.y, qv, acc[r][1]);
+        acc[r][2] = fmaf(w.z, qv, acc[r][2]);
+        acc[r][3] = fmaf(w.w, qv, acc[r][3]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+      *reinterpret_cast<float4*>(&ps[kg][h0 + r][oq]) = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
   }
+  __syncthreads();
+  // thread tid: head tid / 16, outputs 4 (tid % 16) .. + 3, the quarters summed in order
+  const int hr = tid >> 4, oc = 4 * (tid & 15);
+  float acc[4];
+  {
+    float4 x = *reinterpret_cast<const float4*>(&ps[0][hr][oc]);
+#pragma unroll
+    for (int g = 1; g < kQThreads / 128; ++g) {
+      const float4 y = *reinterpret_cast<const float4*>(&ps[g][hr][oc]);
+      x.x += y.x;
+      x.y += y.y;
+      x.z += y.z;
+      x.w += y.w;
+    }
+    acc[0] = x.x, acc[1] = x.y, acc[2] = x.z, acc[3] = x.w;
+  }
+  if (c0 + oc < nout && r0 + hr < nq)
+    *reinterpret_cast<float4*>(a.qprep + (r0 + hr) * nout + c0 + oc) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  // fused step: this grid ends only after the append kernel before it (the
+  // partials kernel, which waits for this grid, then sees the new token)
+  if (a.chained) pdl_wait();
   if (!a.qfrag || a.m != kD) return;
   // fp16 fragments of the persistent partials kernel: this block's 64 outputs
   // hold, per head, 32 of its 128 words (slice 0/1: key pairs of channel group
@@ -141,13 +160,11 @@ __global__ void __launch_bounds__(kQThreads) qprep_kernel(DecodeArgs a) {
   __shared__ __half hs[kQP][kQO];
   __shared__ __half hl[kQP][kQO];          // fp16 of the rounding remainder (q~ low parts)
 #pragma unroll
-  for (int r = 0; r < 4; ++r)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const __half h = __float2half_rn(acc[r][c]);
-      hs[h0 + r][oq + c] = h;
-      hl[h0 + r][oq + c] = __float2half_rn(acc[r][c] - __half2float(h));
-    }
+  for (int c = 0; c < 4; ++c) {
+    const __half h = __float2half_rn(acc[c]);
+    hs[hr][oc + c] = h;
+    hl[hr][oc + c] = __float2half_rn(acc[c] - __half2float(h));
+  }
   __syncthreads();
   const int y = blockIdx.y;
   for (int idx = tid; idx < kQP * 32; idx += kQThreads) {
@@ -499,296 +516,131 @@ __global__ void __launch_bounds__(kThreads) chunk_kernel(DecodeArgs a) {
   }
 }
 
-// Log-sum-exp merge of the chunk partials and o = Pi^T (acc / l): one block
-// per (sequence, KV head) for its G query heads, Pi read once per block.
-// One block per query head: log-sum-exp merge of its chunk partials, then
-// o = Pi^T (acc / sum).  Four groups of 128 threads split the chunks (two
-// accumulation chains each) and then the rows of Pi.  Chunks that start at or
-// past the sequence end hold no partial and are skipped.
-template <int NT>
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
-  v = is_max ? warp_max(v) : warp_sum(v);
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) red[w] = v;
-  __syncthreads();
-  float r = red[0];
-#pragma unroll
-  for (int k = 1; k < NT / 32; ++k) r = is_max ? fmaxf(r, red[k]) : r + red[k];
-  return r;
-}
+// Decode merge (one query per row): log-sum-exp of the chunk partials, then
+// o = Pi^T (acc / l).
+// A block of eight warps takes 8 / WR rows, WR warps per row; warp k of a row
+// reads chunks k, k + WR, ... (a lane holds four channels), every load of a
+// batch of eight issued before the first use.  Each warp forms its row's
+// maximum and weight sum itself (lane c holds chunks c, c + 32, ...), so only
+// the channel sums cross warps.  What does not depend on the partials kernel
+// is read before the grid dependency wait: Pi (staged in shared memory) and
+// the rows' lengths.  The row's WR warps then rotate it back, warp k taking
+// rows 128 k / WR .. of Pi.
+constexpr int kMDWarps = 8;
+constexpr int kMDBatch = 8;                           // chunks in flight per warp
+constexpr int kMDSmem = (kD * kD + 2 * kMDWarps * kD) * 4;   // Pi, the warps' channel sums, their rotated parts
 
-constexpr int kMGroups = 4;
-constexpr int kMThreads = kMGroups * kD;
-
-// The token at position seq_lens[b] of a fused decode step, scored here from its
-// stored record (the quantize-append ran on another stream, next to the
-// partials kernel, which covered positions [0, seq_lens[b])): logit (log2
-// units) and, in vnew, its dequantized value scaled by n_v/sqrt(d).
-// Returns -inf when there is no such token (flags a bad page id or length).
-__device__ float new_token_logit(const DecodeArgs& a, long long row, float* vnew, float* red) {
-  const int tid = threadIdx.x, j = tid & (kD - 1), grp = tid >> 7;
-  const int b = static_cast<int>(row / a.Hq), hkv = static_cast<int>(row % a.Hq) / a.G;
-  const int L0 = a.seq_lens[b];
-  if (L0 < 0 || L0 >= a.maxp * kPage || L0 + 1 > a.max_seq_len) {
-    if (tid == 0 && (row % a.Hq) == 0) atomicOr(a.tab.err, kErrSeqLen);
-    return -INFINITY;
-  }
-  const int page = a.block_table[static_cast<long long>(b) * a.maxp + (L0 >> 4)], slot = L0 & 15;
-  if (page < 0 || page >= a.num_pages) {
-    if (tid == 0 && (row % a.Hq) == 0) atomicOr(a.tab.err, kErrPage);
-    return -INFINITY;
-  }
-  const uint8_t* krec = a.kc + static_cast<long long>(page) * a.k_page_bytes + static_cast<long long>(hkv) * a.kl.block_bytes;
-  const uint8_t* vrec = a.vc + static_cast<long long>(page) * a.v_page_bytes + static_cast<long long>(hkv) * a.vl.block_bytes;
-  const float* qr = a.qprep + row * (kD + a.m);
-  float part = 0.0f;
-  if (grp == 0) {                      // <q~, c_K[code]>
-    const unsigned* kw = reinterpret_cast<const unsigned*>(krec + slot * a.kl.code_bytes);
-    const int code = code_at(kw, a.kl.g[0].bits, a.kl.g[1].bits, a.kl.split, j);
-    part = qr[j] * a.kl.g[j < a.kl.split ? 0 : 1].c[code];
-  } else if (grp == 1 && a.kl.qjl && j < a.m) {   // <u, +-1 signs>
-    const uint8_t sb = krec[a.kl.off_signs + slot * (a.m / 8) + (j >> 3)];
-    part = ((sb >> (j & 7)) & 1u) ? qr[kD + j] : -qr[kD + j];
-  } else if (grp == 2) {               // value
-    const unsigned* vw = reinterpret_cast<const unsigned*>(vrec + slot * a.vl.code_bytes);
-    const int code = code_at(vw, a.vl.g[0].bits, a.vl.g[1].bits, a.vl.split, j);
-    const float nv = __half2float(reinterpret_cast<const __half*>(vrec + a.vl.off_norm)[slot]);
-    vnew[j] = nv * kInvSqrtD * a.vl.g[j < a.vl.split ? 0 : 1].c[code];
-  }
-  part = warp_sum(part);
-  __syncthreads();
-  if ((tid & 31) == 0) red[tid >> 5] = part;
-  __syncthreads();
-  float s1 = 0.f, s2 = 0.f;
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    s1 += red[w];
-    s2 += red[4 + w];
-  }
-  const float nk = __half2float(reinterpret_cast<const __half*>(krec + a.kl.off_norm)[slot]);
-  float lg = nk * kInvSqrtD * s1;
-  if (a.kl.qjl) {
-    const float rk = __half2float(reinterpret_cast<const __half*>(krec + a.kl.off_rnorm)[slot]);
-    lg = fmaf(kSqrtHalfPi / static_cast<float>(a.m) * rk, s2, lg);
-  }
-  __syncthreads();                     // red is reused by the caller
-  return lg * a.scale_log2;
-}
-
-__global__ void __launch_bounds__(kMThreads) merge_kernel(DecodeArgs a) {
-  pdl_wait();                          // the partials kernel before it has completed
-  __shared__ float wsh[kMThreads];
-  __shared__ float part[kMGroups][kD];
-  __shared__ float os[kD];
-  __shared__ float vnew[kD];
-  __shared__ float red[kMThreads / 32];
-  const long long row = blockIdx.x;                 // b * Hq + query head (decode; causal rows use the row merges)
-  const int tid = threadIdx.x, j = tid & (kD - 1), grp = tid >> 7;
-  int L = a.seq_lens[row / a.Hq] + a.len_add;
-  L = L < 0 ? 0 : L;
-  L = L > a.max_seq_len ? a.max_seq_len : L;
-  L = L > a.maxp * kPage ? a.maxp * kPage : L;
-  const int nc = min(a.nchunks, (L + a.chunk - 1) / a.chunk);
-  const float* P = a.part + row * a.nchunks * (kD + 2);
-  // the chunk maxima are requested before the new token is scored
-  float M = -INFINITY;
-  for (int c = tid; c < nc; c += kMThreads) M = fmaxf(M, P[static_cast<long long>(c) * (kD + 2)]);
-  const float lg_new = a.new_token ? new_token_logit(a, row, vnew, red) : -INFINITY;
-  M = fmaxf(block_reduce<kMThreads>(M, true, red), lg_new);
-  const float w_new = lg_new > -INFINITY ? exp2f(lg_new - M) : 0.0f;
-  float lpart = 0.0f, A0 = 0.0f, A1 = 0.0f;
-  for (int c0 = 0; c0 < nc; c0 += kMThreads) {
-    const int c = c0 + tid;
-    float w = 0.0f;
-    if (c < nc) {
-      const float* pc = P + static_cast<long long>(c) * (kD + 2);
-      w = exp2f(pc[0] - M);
-      lpart = fmaf(w, pc[1], lpart);
-    }
-    __syncthreads();
-    wsh[tid] = w;
-    __syncthreads();
-    const int n = min(kMThreads, nc - c0);
-    int cc = grp;
-    for (; cc + kMGroups < n; cc += 2 * kMGroups) {
-      A0 = fmaf(wsh[cc], P[static_cast<long long>(c0 + cc) * (kD + 2) + 2 + j], A0);
-      A1 = fmaf(wsh[cc + kMGroups], P[static_cast<long long>(c0 + cc + kMGroups) * (kD + 2) + 2 + j], A1);
-    }
-    if (cc < n) A0 = fmaf(wsh[cc], P[static_cast<long long>(c0 + cc) * (kD + 2) + 2 + j], A0);
-  }
-  if (tid == 0) lpart += w_new;
-  if (grp == 0 && w_new > 0.0f) A0 = fmaf(w_new, vnew[j], A0);
-  const float l = block_reduce<kMThreads>(lpart, false, red);
-  part[grp][j] = A0 + A1;
-  __syncthreads();
-  if (grp == 0) os[j] = l > 0.0f ? ((part[0][j] + part[1][j]) + (part[2][j] + part[3][j])) / l : 0.0f;
-  __syncthreads();
-  float o0 = 0.f, o1 = 0.f;                         // rows grp*32 .. grp*32+31 of Pi
-  const int i0 = grp * (kD / kMGroups);
-#pragma unroll 8
-  for (int i = 0; i < kD / kMGroups; i += 2) {
-    o0 = fmaf(a.tab.pi[(i0 + i) * kD + j], os[i0 + i], o0);
-    o1 = fmaf(a.tab.pi[(i0 + i + 1) * kD + j], os[i0 + i + 1], o1);
-  }
-  part[grp][j] = o0 + o1;
-  __syncthreads();
-  if (grp == 0) a.out[row * kD + j] = (part[0][j] + part[1][j]) + (part[2][j] + part[3][j]);
-}
-
-// Decode merge, a warp per query row (eight rows per block): the chunk maxima
-// and weights live on the lanes (chunk c on lane c % 32), the weighted partials
-// are read eight chunks at a time with a lane holding four channels (the first
-// eight issued with the maxima), the fused step's new token is scored by the
-// same warp from its stored record, and the warp rotates its row back
-// (o = Pi^T o~) from a copy of Pi the block staged in shared memory before its
-// grid dependency wait.  No block-wide reductions; few rounds of dependent loads.
-constexpr int kMDRows = 8;
-
-// The token at position seq_lens[b] of a fused decode step for query row `row`
-// (its KV head's stored record: the quantize-append ran on another stream):
-// the logit in log2 units, and in vn the value's channels 4 lane .. 4 lane + 3
-// times n_v/sqrt(d).  -inf when there is no such token (a bad length or page
-// id, flagged once per sequence).
-__device__ float new_token_logit_warp(const DecodeArgs& a, long long row, int lane, float (&vn)[4]) {
-  const int b = static_cast<int>(row / a.Hq), hq = static_cast<int>(row % a.Hq), hkv = hq / a.G;
-  const int L0 = a.seq_lens[b];
-  if (L0 < 0 || L0 >= a.maxp * kPage || L0 + 1 > a.max_seq_len) {
-    if (lane == 0 && hq == 0) atomicOr(a.tab.err, kErrSeqLen);
-    return -INFINITY;
-  }
-  const int page = a.block_table[static_cast<long long>(b) * a.maxp + (L0 >> 4)], slot = L0 & 15;
-  if (page < 0 || page >= a.num_pages) {
-    if (lane == 0 && hq == 0) atomicOr(a.tab.err, kErrPage);
-    return -INFINITY;
-  }
-  const uint8_t* krec = a.kc + static_cast<long long>(page) * a.k_page_bytes + static_cast<long long>(hkv) * a.kl.block_bytes;
-  const uint8_t* vrec = a.vc + static_cast<long long>(page) * a.v_page_bytes + static_cast<long long>(hkv) * a.vl.block_bytes;
-  const float* qr = a.qprep + row * (kD + a.m);
-  const float4 q4 = *reinterpret_cast<const float4*>(qr + 4 * lane);
-  const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
-  const unsigned* kw = reinterpret_cast<const unsigned*>(krec + slot * a.kl.code_bytes);
-  const unsigned* vw = reinterpret_cast<const unsigned*>(vrec + slot * a.vl.code_bytes);
-  const float nv = __half2float(reinterpret_cast<const __half*>(vrec + a.vl.off_norm)[slot]) * kInvSqrtD;
-  float s1 = 0.0f, s2 = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int j = 4 * lane + i;
-    const int kc = code_at(kw, a.kl.g[0].bits, a.kl.g[1].bits, a.kl.split, j);
-    s1 = fmaf(qv[i], a.kl.g[j < a.kl.split ? 0 : 1].c[kc], s1);
-    const int vc = code_at(vw, a.vl.g[0].bits, a.vl.g[1].bits, a.vl.split, j);
-    vn[i] = nv * a.vl.g[j < a.vl.split ? 0 : 1].c[vc];
-    if (a.kl.qjl && j < a.m) {                       // <u, +-1 signs>
-      const uint8_t sbyte = krec[a.kl.off_signs + slot * (a.m / 8) + (j >> 3)];
-      const float u = qr[kD + j];
-      s2 += ((sbyte >> (j & 7)) & 1u) ? u : -u;
-    }
-  }
-  s1 = warp_sum(s1);
-  s2 = warp_sum(s2);
-  const float nk = __half2float(reinterpret_cast<const __half*>(krec + a.kl.off_norm)[slot]);
-  float lg = nk * kInvSqrtD * s1;
-  if (a.kl.qjl) {
-    const float rk = __half2float(reinterpret_cast<const __half*>(krec + a.kl.off_rnorm)[slot]);
-    lg = fmaf(kSqrtHalfPi / static_cast<float>(a.m) * rk, s2, lg);
-  }
-  return lg * a.scale_log2;
-}
-
-constexpr int kMDSmem = (kD * kD + kMDRows * kD) * 4;   // Pi, then the rows' o~
-
-__global__ void __launch_bounds__(32 * kMDRows) merge_dec_kernel(DecodeArgs a, long long rows) {
+template <int WR>
+__global__ void __launch_bounds__(32 * kMDWarps) merge_dec_kernel(DecodeArgs a, long long rows) {
   extern __shared__ __align__(16) float mds[];
   float(*pis)[kD] = reinterpret_cast<float(*)[kD]>(mds);
-  float(*os)[kD] = reinterpret_cast<float(*)[kD]>(mds + kD * kD);
+  float(*cs)[kD] = reinterpret_cast<float(*)[kD]>(mds + kD * kD);                  // channel sums, per warp
+  float(*rs)[kD] = reinterpret_cast<float(*)[kD]>(mds + kD * kD + kMDWarps * kD);  // rotated parts, per warp
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Pi does not depend on the partials kernel: staged before the grid dependency wait
+  const int k = warp % WR, w0 = warp - k;              // this warp's share of its row, the row's first warp
+  const long long row = static_cast<long long>(blockIdx.x) * (kMDWarps / WR) + warp / WR;
+  const bool live = row < rows;
 #pragma unroll
-  for (int k = 0; k < kD * kD / 4 / (32 * kMDRows); ++k) {
-    const int v = tid + k * 32 * kMDRows;
+  for (int v4 = 0; v4 < kD * kD / 4 / (32 * kMDWarps); ++v4) {
+    const int v = tid + v4 * 32 * kMDWarps;
     *reinterpret_cast<float4*>(&pis[0][0] + 4 * v) = __ldg(reinterpret_cast<const float4*>(a.tab.pi) + v);
   }
-  pdl_wait();                          // the partials kernel before it has completed
-  const long long row = static_cast<long long>(blockIdx.x) * kMDRows + warp;
-  const bool live = row < rows;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f}, l = 0.0f;
+  int nc = 0;
   if (live) {
     int L = a.seq_lens[row / a.Hq] + a.len_add;
     L = L < 0 ? 0 : L;
     L = L > a.max_seq_len ? a.max_seq_len : L;
     L = L > a.maxp * kPage ? a.maxp * kPage : L;
-    const int nc = min(a.nchunks, (L + a.chunk - 1) / a.chunk);
+    nc = min(a.nchunks, (L + a.chunk - 1) / a.chunk);
+  }
+  pdl_wait();                          // the partials kernel before it has completed
+  float acc[4] = {0.f, 0.f, 0.f, 0.f}, l = 0.0f;
+  if (live) {
     const float* P = a.part + row * a.nchunks * (kD + 2);
-    // the first 32 chunks' (max, sum) on the lanes and their first eight partial vectors, all issued
-    // before anything waits on them
+    // this warp's first batch of chunks and the row's (max, sum) pairs, all issued before any use
+    float2 x[kMDBatch][2];
+    float mx[kMDBatch];
+#pragma unroll
+    for (int j = 0; j < kMDBatch; ++j) {
+      const int c = k + WR * j;
+      x[j][0] = x[j][1] = make_float2(0.f, 0.f);
+      mx[j] = -INFINITY;
+      if (c < nc) {
+        const float* pc = P + static_cast<long long>(c) * (kD + 2);
+        mx[j] = pc[0];
+        x[j][0] = *reinterpret_cast<const float2*>(pc + 2 + 4 * lane);
+        x[j][1] = *reinterpret_cast<const float2*>(pc + 4 + 4 * lane);
+      }
+    }
     float2 ml = make_float2(-INFINITY, 0.0f);
     if (lane < nc) ml = *reinterpret_cast<const float2*>(P + static_cast<long long>(lane) * (kD + 2));
-    float2 x[8][2];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      x[j][0] = x[j][1] = make_float2(0.f, 0.f);
-      if (j < nc) {
-        const float* pc = P + static_cast<long long>(j) * (kD + 2) + 2 + 4 * lane;
-        x[j][0] = *reinterpret_cast<const float2*>(pc);
-        x[j][1] = *reinterpret_cast<const float2*>(pc + 2);
-      }
-    }
-    float vn[4] = {0.f, 0.f, 0.f, 0.f};
-    const float lg_new = a.new_token ? new_token_logit_warp(a, row, lane, vn) : -INFINITY;
     float M = ml.x;
     for (int c = lane + 32; c < nc; c += 32) M = fmaxf(M, P[static_cast<long long>(c) * (kD + 2)]);
-    M = fmaxf(warp_max(M), lg_new);
-    for (int cb = 0; cb < nc; cb += 32) {
-      if (cb > 0) ml = cb + lane < nc ? *reinterpret_cast<const float2*>(P + static_cast<long long>(cb + lane) * (kD + 2))
-                                      : make_float2(-INFINITY, 0.0f);
-      const float w = cb + lane < nc ? exp2f(ml.x - M) : 0.0f;
-      l = fmaf(w, ml.y, l);
-      const int n = min(32, nc - cb);
-      for (int j0 = 0; j0 < n; j0 += 8) {
-        if (cb + j0 > 0) {                           // the next eight chunks (the first eight are loaded)
+    M = warp_max(M);
+    if (M > -INFINITY) {
+      l = lane < nc ? exp2f(ml.x - M) * ml.y : 0.0f;
+      for (int c = lane + 32; c < nc; c += 32) {
+        const float2 m2 = *reinterpret_cast<const float2*>(P + static_cast<long long>(c) * (kD + 2));
+        l = fmaf(exp2f(m2.x - M), m2.y, l);
+      }
+      for (int cb = 0;; cb += kMDBatch) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            x[j][0] = x[j][1] = make_float2(0.f, 0.f);
-            if (j0 + j < n) {
-              const float* pc = P + static_cast<long long>(cb + j0 + j) * (kD + 2) + 2 + 4 * lane;
-              x[j][0] = *reinterpret_cast<const float2*>(pc);
-              x[j][1] = *reinterpret_cast<const float2*>(pc + 2);
-            }
+        for (int j = 0; j < kMDBatch; ++j) {
+          const float w = exp2f(mx[j] - M);          // 0 past the row's chunks (-inf)
+          acc[0] = fmaf(w, x[j][0].x, acc[0]);
+          acc[1] = fmaf(w, x[j][0].y, acc[1]);
+          acc[2] = fmaf(w, x[j][1].x, acc[2]);
+          acc[3] = fmaf(w, x[j][1].y, acc[3]);
+        }
+        if (k + WR * (cb + kMDBatch) >= nc) break;
+#pragma unroll
+        for (int j = 0; j < kMDBatch; ++j) {       // the next batch
+          const int c = k + WR * (cb + kMDBatch + j);
+          x[j][0] = x[j][1] = make_float2(0.f, 0.f);
+          mx[j] = -INFINITY;
+          if (c < nc) {
+            const float* pc = P + static_cast<long long>(c) * (kD + 2);
+            mx[j] = pc[0];
+            x[j][0] = *reinterpret_cast<const float2*>(pc + 2 + 4 * lane);
+            x[j][1] = *reinterpret_cast<const float2*>(pc + 4 + 4 * lane);
           }
         }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float wj = __shfl_sync(0xffffffffu, w, (j0 + j) & 31);
-          acc[0] = fmaf(wj, x[j][0].x, acc[0]);
-          acc[1] = fmaf(wj, x[j][0].y, acc[1]);
-          acc[2] = fmaf(wj, x[j][1].x, acc[2]);
-          acc[3] = fmaf(wj, x[j][1].y, acc[3]);
-        }
       }
-    }
-    l = warp_sum(l);
-    if (lg_new > -INFINITY) {
-      const float wn = exp2f(lg_new - M);
-      l += wn;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] = fmaf(wn, vn[i], acc[i]);
+      l = warp_sum(l);
     }
   }
   const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-  *reinterpret_cast<float4*>(&os[warp][4 * lane]) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-  __syncthreads();                     // Pi staged by every thread
-  if (!live) return;
+  *reinterpret_cast<float4*>(&cs[warp][4 * lane]) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+  __syncthreads();                     // Pi staged, every warp's channel sums written
+  // o = Pi^T o~ over rows i of Pi in [i0, i0 + 128 / WR): o~_i summed over the row's warps
+  constexpr int NI = kD / WR;
+  const int i0 = k * NI;
   float o[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
-  for (int i = 0; i < kD; ++i) {
+  for (int i = i0; i < i0 + NI; ++i) {
     const float4 p = *reinterpret_cast<const float4*>(&pis[i][4 * lane]);
-    const float xo = os[warp][i];
+    float xo = cs[w0][i];
+#pragma unroll
+    for (int r = 1; r < WR; ++r) xo += cs[w0 + r][i];
     o[0] = fmaf(p.x, xo, o[0]);
     o[1] = fmaf(p.y, xo, o[1]);
     o[2] = fmaf(p.z, xo, o[2]);
     o[3] = fmaf(p.w, xo, o[3]);
   }
-  *reinterpret_cast<float4*>(a.out + row * kD + 4 * lane) = make_float4(o[0], o[1], o[2], o[3]);
+  if (WR > 1) {
+    *reinterpret_cast<float4*>(&rs[warp][4 * lane]) = make_float4(o[0], o[1], o[2], o[3]);
+    __syncthreads();
+    if (k != 0) return;
+#pragma unroll
+    for (int r = 1; r < WR; ++r) {
+      const float4 q = *reinterpret_cast<const float4*>(&rs[w0 + r][4 * lane]);
+      o[0] += q.x;
+      o[1] += q.y;
+      o[2] += q.z;
+      o[3] += q.w;
+    }
+  }
+  if (live) *reinterpret_cast<float4*>(a.out + row * kD + 4 * lane) = make_float4(o[0], o[1], o[2], o[3]);
 }
 
 // Merge for many query rows (causal attention: B T Hq rows): a block takes 32
@@ -1030,11 +882,15 @@ cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
   } else if (stages & TQ_STAGE_QPREP) {
     const dim3 grid(static_cast<unsigned>((static_cast<long long>(a.B) * (a.T > 0 ? a.T : 1) * a.Hq + kQP - 1) / kQP),
                     static_cast<unsigned>((kD + a.m + kQO - 1) / kQO));
-    static std::atomic<unsigned long long> configured{0};   // the W slice and q rows take 49 KB
+    static std::atomic<unsigned long long> configured{0};   // the W slice, q rows and partial tiles take 81 KB
     e = smem_attr_once(qprep_kernel, kQprepSmem, configured);
     if (e != cudaSuccess) return e;
-    qprep_kernel<<<grid, kQThreads, kQprepSmem, s>>>(a);
-    e = cudaGetLastError();
+    if (a.chained) {
+      e = launch_pdl(qprep_kernel, grid, dim3(kQThreads), static_cast<size_t>(kQprepSmem), s, a);
+    } else {
+      qprep_kernel<<<grid, kQThreads, kQprepSmem, s>>>(a);
+      e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
   }
   if (stages & TQ_STAGE_PARTIALS) {
@@ -1064,17 +920,27 @@ cudaError_t launch_decode(const DecodeArgs& a, int stages, cudaStream_t s) {
       const long long rows = static_cast<long long>(a.B) * a.T * a.Hq;
       e = launch_pdl(merge_rows_kernel, dim3(static_cast<unsigned>((rows + kMRRows - 1) / kMRRows)), dim3(kMRThreads),
                      0, s, a, rows);
-    } else if (static_cast<long long>(a.B) * a.Hq < 1024) {
-      // few rows: a block per row has more loads in flight per row than a warp
-      e = launch_pdl(merge_kernel, dim3(static_cast<unsigned>(static_cast<long long>(a.B) * a.Hq)), dim3(kMThreads), 0,
-                     s, a);
     } else {
+      // warps per row: a batch of eight chunks per warp for up to 32 chunks, then
+      // as many warps as keep the batches (and the rows per block) few
       const long long rows = static_cast<long long>(a.B) * a.Hq;
-      static std::atomic<unsigned long long> configured{0};   // Pi and the rows take 68 KB
-      e = smem_attr_once(merge_dec_kernel, kMDSmem, configured);
+      const int wr = a.nchunks <= 8 ? 1 : a.nchunks <= 16 ? 2 : a.nchunks <= 32 ? 4 : 8;
+      const dim3 grid(static_cast<unsigned>((rows + kMDWarps / wr - 1) / (kMDWarps / wr)));
+      static std::atomic<unsigned long long> configured[4];   // Pi and the warps' sums take 72 KB
+      switch (wr) {
+        case 1: e = smem_attr_once(merge_dec_kernel<1>, kMDSmem, configured[0]); break;
+        case 2: e = smem_attr_once(merge_dec_kernel<2>, kMDSmem, configured[1]); break;
+        case 4: e = smem_attr_once(merge_dec_kernel<4>, kMDSmem, configured[2]); break;
+        default: e = smem_attr_once(merge_dec_kernel<8>, kMDSmem, configured[3]); break;
+      }
       if (e != cudaSuccess) return e;
-      e = launch_pdl(merge_dec_kernel, dim3(static_cast<unsigned>((rows + kMDRows - 1) / kMDRows)), dim3(32 * kMDRows),
-                     static_cast<size_t>(kMDSmem), s, a, rows);
+      const size_t sm = static_cast<size_t>(kMDSmem);
+      switch (wr) {
+        case 1: e = launch_pdl(merge_dec_kernel<1>, grid, dim3(32 * kMDWarps), sm, s, a, rows); break;
+        case 2: e = launch_pdl(merge_dec_kernel<2>, grid, dim3(32 * kMDWarps), sm, s, a, rows); break;
+        case 4: e = launch_pdl(merge_dec_kernel<4>, grid, dim3(32 * kMDWarps), sm, s, a, rows); break;
+        default: e = launch_pdl(merge_dec_kernel<8>, grid, dim3(32 * kMDWarps), sm, s, a, rows); break;
+      }
     }
   }
   return e;

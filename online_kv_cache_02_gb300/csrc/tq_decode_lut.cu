@@ -27,8 +27,8 @@
 //     prmt per pair, and <u, 2b - 1> = (2/c) S2 - (2/c + 1) sum(u);
 //   * logits = (n_k/sqrt(d) S1 + sqrt(pi/2)/m rho S2) * scale; online softmax
 //     on the accumulator fragments;
-//   * P' = p * n_v / sqrt(d) through a 256-byte shared tile into the B operand
-//     of O^T += V^^T P'^T (M = channels, K = tokens).
+//   * P' = p * n_v / sqrt(d), transposed in registers (movmatrix) into the B
+//     operand of O^T += V^^T P'^T (M = channels, K = tokens).
 // The channel order inside the fragments is a fixed permutation that makes each
 // thread's code bytes contiguous; Q~ and the output use the same permutation.
 //
@@ -117,6 +117,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 __device__ __forceinline__ uint32_t f16bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
+// (lo, hi) as an fp16 pair, each rounded to nearest even.
+__device__ __forceinline__ uint32_t pack_rn(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+// Transpose of an 8x8 fp16 matrix held as one pair per lane (lane 4r + c: row r,
+// columns 2c, 2c + 1), returned in the same layout.
+__device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
+  uint32_t y;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) { return f16bits(lo) | (f16bits(hi) << 16); }
 
 // ---------------------------------------------------------------------------
@@ -227,8 +239,8 @@ struct Geo {
   static constexpr int R0 = region_bytes(KBH, VBH);
   static constexpr int R1 = region_bytes(KBL, VBL);
   static constexpr int TABLES = R0 + R1;
-  // per warp: ring, then (in the extras block) S barriers, S slots, a 256-byte P tile
-  __host__ __device__ static constexpr int extras(int st) { return W * (st * 8 + st * 16 + 256); }
+  // per warp: ring, then (in the extras block) S barriers and S slots
+  __host__ __device__ static constexpr int extras(int st) { return W * (st * 8 + st * 16); }
   // the tables start at a 64 KiB-aligned shared address; the gap below them
   // takes whole warp rings, so at most one ring (or, when every ring fits in
   // the gap, the rest of the gap) is lost to the alignment
@@ -260,6 +272,9 @@ template <int W, int KBH, int KBL, int VBH, int VBL, bool QJL, bool CAUSAL = fal
 __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, int total_items) {
   using Gm = Geo<W, KBH, KBL, VBH, VBL, QJL>;
   constexpr int S = Gm::STAGES;
+  // the merge after this kernel may launch now: it stages what it can and then
+  // waits for this grid; persistent CTAs are all resident, so none is delayed
+  pdl_trigger();
   extern __shared__ __align__(1024) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -292,7 +307,6 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
   unsigned char* ring = at(warp < n_low ? base + warp * Gm::RINGW : tab + Gm::TABLES + (warp - n_low) * Gm::RINGW);
   unsigned long long* bars = reinterpret_cast<unsigned long long*>(at(ext)) + warp * S;
   Slot* slots = reinterpret_cast<Slot*>(at(ext + W * S * 8)) + warp * S;
-  __half(*ptile)[16] = reinterpret_cast<__half(*)[16]>(at(ext + W * S * 24 + warp * 256));
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(smem_u32(&bars[s]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -633,18 +647,17 @@ __global__ void __launch_bounds__(32 * W, 1) lut_partials_kernel(DecodeArgs a, i
         pr[c + 2] = fast_exp2(lg[c + 2] - m_run[c]);
         l_run[c] += pr[c] + pr[c + 2];
       }
-      // ---- P' = p * nv / sqrt(d) into the transposed shared tile -------------
+      // ---- P' = p * nv / sqrt(d), transposed in registers ----------------------
+      // the accumulator layout holds (token g | g + 8, heads 2t, 2t + 1); the B
+      // operand wants (tokens 2t, 2t + 1 | 2t + 8, 2t + 9, head g): one 8x8 fp16
+      // transpose per token half
+      uint32_t pb0, pb1;
       {
         const float wg = vg ? __half2float(nv[g]) * kInvSqrtD : 0.0f;
         const float wg8 = vg8 ? __half2float(nv[g + 8]) * kInvSqrtD : 0.0f;
-        ptile[2 * t][g] = __float2half_rn(pr[0] * wg);
-        ptile[2 * t + 1][g] = __float2half_rn(pr[1] * wg);
-        ptile[2 * t][g + 8] = __float2half_rn(pr[2] * wg8);
-        ptile[2 * t + 1][g + 8] = __float2half_rn(pr[3] * wg8);
+        pb0 = transpose8x8(pack_rn(pr[0] * wg, pr[1] * wg));
+        pb1 = transpose8x8(pack_rn(pr[2] * wg8, pr[3] * wg8));
       }
-      __syncwarp();
-      const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(&ptile[g][2 * t]);
-      const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(&ptile[g][2 * t + 8]);
       // ---- O^T += V^^T P'^T ---------------------------------------------------
       {
         const uint32_t* r0 = reinterpret_cast<const uint32_t*>(vb + (2 * t) * Gm::CBV);

@@ -123,7 +123,9 @@ struct DecodeArgs {
   float* part;           // [B][Hq][nchunks][d + 2]
   float* out;            // [B][Hq][d]
   int* sched;            // [2] work counter and finished-warp count of the persistent kernel (zeroed by qprep)
-  int new_token;         // 1: merge adds the token at position seq_lens[b] itself (fused decode step)
+  int chained;           // 1: qprep follows the fused step's append kernel (a dependent launch that
+                         // overlaps it and waits for it before finishing, so the partials kernel sees
+                         // the new token in the cache)
   int max_ctas;          // partials kernel: 0 = one CTA per SM, else at most this many
   uint32_t* qfrag;       // [B][Hq][kQFragWords] fp16 pairs in the persistent kernel's fragment order (m = 128
                          // only): words 32 t .. 32 t + 31 for lane t%4 of a KV-head warp (16 of q~ key pairs, 16
@@ -180,6 +182,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
+// One warp per vector (a decode step's new tokens): false if the shapes are not taken.
+bool launch_append(const QuantizeArgs& k, const QuantizeArgs& v, cudaStream_t s, cudaError_t* err);
 // Tensor-core quantize of K and V in one launch (bf16 inputs, supported
 // bit-width combinations); returns false when the configuration is not covered.
 bool launch_quantize_tc(const QuantizeArgs& k, const QuantizeArgs& v, cudaStream_t s, cudaError_t* err);
@@ -238,12 +242,6 @@ struct tq_ctx {
   tq::KindLayout kl, vl;
   tq::DeviceTables tab;
   void* dev_block;       // single allocation holding every device table
-  // fused decode step: the new token's quantize-append runs on this stream
-  // next to the partials kernel (stream and events made by tq_create_ex;
-  // fused_mu serialises the host-side enqueue that records the shared events)
-  void* fused_mu;        // std::mutex*
-  cudaStream_t aux_stream;
-  cudaEvent_t ev_fork, ev_join;
 };
 
 #endif  // TQ_INTERNAL_H_

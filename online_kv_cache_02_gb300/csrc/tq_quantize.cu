@@ -438,11 +438,295 @@ cudaError_t launch_kind(const QuantizeArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-}  // namespace
-
-cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s) {
+cudaError_t launch_quantize_impl(const QuantizeArgs& a, cudaStream_t s) {
   if (a.lay.qjl) return launch_kind<true>(a, s);
   return launch_kind<false>(a, s);
+}
+
+// ---------------------------------------------------------------------------
+// Latency-first append of a few vectors (a decode step's new token per
+// sequence and KV head): one warp per vector, four vectors per CTA (each warp
+// reads all of Pi^T from shared memory: few warps per SM keep that short), K
+// and V vectors in one launch (CTAs [0, nbk) keys, the rest values).  Pi^T
+// (and for keys S^T) are staged once per CTA by asynchronous 16-byte copies,
+// all in flight at once; the fast
+// path is the tile kernel's above, vector by vector: y = Pi x summed over k in
+// order (fp32), the same code and sign guards, the same packing.  A decision
+// inside a guard is retaken in fp64 by the whole warp, one decision at a time
+// (a lane takes four of the 128 terms, so each costs one round of loads):
+// a code from y_j = Pi_j x, a sign bit from z_p = (S Pi)_p x - fp16(||x||) /
+// sqrt(d) S_p c^ (the product S Pi as a double-float table, the codes as
+// decided).  The residual norm stays the fp32 one.  Lane l holds channels
+// (projections) 4 l .. 4 l + 3.
+constexpr int kAppWarps = 4;
+constexpr int kAppScratch = 128 * 4 + 128 * 4 + 128;   // x, r, codes per warp
+constexpr int kAppSmem = 2 * 128 * 128 * 4 + kAppWarps * kAppScratch;
+
+__device__ void append_vector(const QuantizeArgs& a, bool key, long long gv, const float* pit, const float* st,
+                              unsigned char* scratch, int lane) {
+  const KindLayout& L = a.lay;
+  float* xs = reinterpret_cast<float*>(scratch);
+  float* rs = xs + 128;
+  unsigned char* codes = reinterpret_cast<unsigned char*>(rs + 128);
+  const float inv_sqrt_d = 0.08838834764831845f;
+  const double inv_sqrt_d64 = 1.0 / sqrt(128.0);
+  const double sqrt_d64 = sqrt(128.0);
+  // 1. x and its double-float squared norm
+  float xv[4];
+  if (a.f32) {
+    const float4 x4 = reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + gv * kD)[lane];
+    xv[0] = x4.x, xv[1] = x4.y, xv[2] = x4.z, xv[3] = x4.w;
+  } else {
+    const uint2 x2 = reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(a.x) + gv * kD)[lane];
+    xv[0] = __uint_as_float(x2.x << 16), xv[1] = __uint_as_float(x2.x & 0xFFFF0000u);
+    xv[2] = __uint_as_float(x2.y << 16), xv[3] = __uint_as_float(x2.y & 0xFFFF0000u);
+  }
+  *reinterpret_cast<float4*>(xs + 4 * lane) = make_float4(xv[0], xv[1], xv[2], xv[3]);
+  float sh = 0.0f, sl = 0.0f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float p = xv[q] * xv[q];
+    const float e = fmaf(xv[q], xv[q], -p);
+    float s, t;
+    two_sum(sh, p, s, t);
+    sh = s;
+    sl += t + e;
+  }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float bh = __shfl_xor_sync(0xffffffffu, sh, o), bl = __shfl_xor_sync(0xffffffffu, sl, o);
+    df_add(sh, sl, bh, bl);
+  }
+  float nh = 0.0f, nl = 0.0f;
+  if (sh > 0.0f) {
+    const float r = sqrtf(sh);
+    const float res = fmaf(-r, r, sh) + sl;
+    fast_two_sum(r, res / (2.0f * r), nh, nl);
+  }
+  const float scale = nh > 0.0f ? 11.313708498984761f / nh : 0.0f;   // sqrt(128) / ||x||
+  const __half n16 = df_to_half(nh, nl);
+  const float n16f = __half2float(n16);
+  __syncwarp();
+  // 2. y = Pi x for outputs 4 lane .. 4 lane + 3
+  float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+  for (int k = 0; k < 128; ++k) {
+    const float4 p = *reinterpret_cast<const float4*>(pit + k * 128 + 4 * lane);
+    const float xk = xs[k];
+    y[0] = fmaf(p.x, xk, y[0]);
+    y[1] = fmaf(p.y, xk, y[1]);
+    y[2] = fmaf(p.z, xk, y[2]);
+    y[3] = fmaf(p.w, xk, y[3]);
+  }
+  // 3. codes (fp64 re-decision near a boundary); keys: the residual
+  float rpart = 0.0f;
+  unsigned cw = 0;
+  int code4[4];
+  unsigned guarded = 0;          // bit oi: channel 4 lane + oi within the code guard
+#pragma unroll
+  for (int oi = 0; oi < 4; ++oi) {
+    const int i = 4 * lane + oi;
+    const GroupBook& gb = L.g[i < L.split ? 0 : 1];
+    const float u = y[oi] * scale;
+    int code = 0;
+    float mind = INFINITY;
+    for (int k = 0; k < gb.nb; ++k) {
+      code += u >= gb.t[k];
+      mind = fminf(mind, fabsf(u - gb.t[k]));
+    }
+    code4[oi] = code;
+    if (mind < kCodeGuard) guarded |= 1u << oi;
+  }
+  // the guarded codes in fp64, the warp together on each
+  const double n64 = static_cast<double>(nh) + static_cast<double>(nl);
+#pragma unroll
+  for (int oi = 0; oi < 4; ++oi) {
+    unsigned todo = __ballot_sync(0xffffffffu, (guarded >> oi) & 1u);
+    while (todo) {
+      const int src = __ffs(todo) - 1;
+      todo &= todo - 1u;
+      const int i = 4 * src + oi;
+      const double2 p0 = *reinterpret_cast<const double2*>(a.tab.pi64 + i * 128 + 4 * lane);
+      const double2 p1 = *reinterpret_cast<const double2*>(a.tab.pi64 + i * 128 + 4 * lane + 2);
+      double y64 = fma(p0.x, static_cast<double>(xs[4 * lane]), fma(p0.y, static_cast<double>(xs[4 * lane + 1]),
+                   fma(p1.x, static_cast<double>(xs[4 * lane + 2]), p1.y * static_cast<double>(xs[4 * lane + 3]))));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) y64 += __shfl_xor_sync(0xffffffffu, y64, o);
+      if (lane == src) {
+        const GroupBook& gb = L.g[i < L.split ? 0 : 1];
+        const double u64 = n64 > 0.0 ? sqrt_d64 * y64 / n64 : 0.0;
+        int code = 0;
+        for (int k = 0; k < gb.nb; ++k) code += u64 >= gb.t64[k];
+        code4[oi] = code;
+        atomicAdd(&a.tab.counters[0], 1ULL);
+      }
+    }
+  }
+#pragma unroll
+  for (int oi = 0; oi < 4; ++oi) {
+    const int i = 4 * lane + oi;
+    const GroupBook& gb = L.g[i < L.split ? 0 : 1];
+    const int code = code4[oi];
+    cw |= static_cast<unsigned>(code) << (8 * oi);
+    if (key) {
+      const float r = fmaf(-n16f * inv_sqrt_d, gb.c[code], y[oi]);
+      rs[i] = r;
+      rpart = fmaf(r, r, rpart);
+    }
+  }
+  *reinterpret_cast<unsigned*>(codes + 4 * lane) = cw;
+  unsigned sword = 0;          // lanes 0 .. m/32 - 1: sign word `lane`
+  bool refine = false;
+  float rho2 = 0.0f;
+  if (key && L.qjl) {
+    rho2 = rpart;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) rho2 += __shfl_xor_sync(0xffffffffu, rho2, o);
+    __syncwarp();
+    // 4. z = S r for projections 4 lane .. 4 lane + 3
+    float z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int j = 0; j < 128; ++j) {
+      const float4 s4 = *reinterpret_cast<const float4*>(st + j * 128 + 4 * lane);
+      const float rj = rs[j];
+      z[0] = fmaf(s4.x, rj, z[0]);
+      z[1] = fmaf(s4.y, rj, z[1]);
+      z[2] = fmaf(s4.z, rj, z[2]);
+      z[3] = fmaf(s4.w, rj, z[3]);
+    }
+    const float guard = kSignGuard * sqrtf(rho2);
+    unsigned nib = 0, near = 0;
+#pragma unroll
+    for (int oi = 0; oi < 4; ++oi) {
+      nib |= (z[oi] >= 0.0f ? 1u : 0u) << oi;
+      if (4 * lane + oi < a.m && fabsf(z[oi]) < guard) near |= 1u << oi;
+    }
+    // word w = projections 32 w .. 32 w + 31 = the nibbles of lanes 8 w .. 8 w + 7
+#pragma unroll
+    for (int l = 0; l < 8; ++l) {
+      const unsigned n = __shfl_sync(0xffffffffu, nib, (8 * lane + l) & 31);
+      sword |= n << (4 * l);
+    }
+    // the guarded sign bits in fp64: z_p = (S Pi)_p x - n16 / sqrt(d) S_p c^, the warp together on each;
+    // lane l's terms are channels 4 l .. 4 l + 3 (their codes are this lane's)
+    const double ns = static_cast<double>(n16f) * inv_sqrt_d64;
+    double cx[4], xd[4];
+#pragma unroll
+    for (int oi = 0; oi < 4; ++oi) {
+      const int j = 4 * lane + oi;
+      cx[oi] = ns * L.g[j < L.split ? 0 : 1].c64[code4[oi]];
+      xd[oi] = static_cast<double>(xs[j]);
+    }
+#pragma unroll
+    for (int oi = 0; oi < 4; ++oi) {
+      unsigned todo = __ballot_sync(0xffffffffu, (near >> oi) & 1u);
+      if (todo) refine = true;
+      while (todo) {
+        const int src = __ffs(todo) - 1;
+        todo &= todo - 1u;
+        const int pj = 4 * src + oi;
+        const float4 a0 = *reinterpret_cast<const float4*>(a.tab.a_df + (pj * 128 + 4 * lane) * 2);
+        const float4 a1 = *reinterpret_cast<const float4*>(a.tab.a_df + (pj * 128 + 4 * lane) * 2 + 4);
+        const double2 s0 = *reinterpret_cast<const double2*>(a.tab.s64 + pj * 128 + 4 * lane);
+        const double2 s1 = *reinterpret_cast<const double2*>(a.tab.s64 + pj * 128 + 4 * lane + 2);
+        double zz = fma(static_cast<double>(a0.x) + static_cast<double>(a0.y), xd[0], -s0.x * cx[0]);
+        zz += fma(static_cast<double>(a0.z) + static_cast<double>(a0.w), xd[1], -s0.y * cx[1]);
+        zz += fma(static_cast<double>(a1.x) + static_cast<double>(a1.y), xd[2], -s1.x * cx[2]);
+        zz += fma(static_cast<double>(a1.z) + static_cast<double>(a1.w), xd[3], -s1.y * cx[3]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
+        if (lane == (pj >> 5)) sword = (sword & ~(1u << (pj & 31))) | ((zz >= 0.0 ? 1u : 0u) << (pj & 31));
+      }
+    }
+  }
+  unsigned short r16 = 0;
+  if (key && L.qjl) {
+    r16 = __half_as_ushort(__float2half_rn(sqrtf(rho2)));
+    if (refine && lane == 0) atomicAdd(&a.tab.counters[1], 1ULL);
+  }
+  __syncwarp();
+  // 5. store at (page, slot, head)
+  const int h = static_cast<int>(gv % a.H);
+  const long long bt = gv / a.H;
+  const int t = static_cast<int>(bt % a.n_new);
+  const int b = static_cast<int>(bt / a.n_new);
+  const int pos = a.start_pos[b] + t;
+  const int blk = pos >> 4;
+  if (pos < 0 || blk >= a.maxp) {
+    if (lane == 0) atomicOr(a.tab.err, kErrBlock);
+    return;
+  }
+  const int page = a.block_table[static_cast<long long>(b) * a.maxp + blk];
+  if (page < 0 || page >= a.num_pages) {
+    if (lane == 0) atomicOr(a.tab.err, kErrPage);
+    return;
+  }
+  const int slot = pos & 15;
+  unsigned char* base = a.cache + static_cast<long long>(page) * a.page_bytes + static_cast<long long>(h) * L.block_bytes;
+  for (int w = lane; w < L.code_bytes / 4; w += 32)
+    reinterpret_cast<unsigned*>(base + slot * L.code_bytes)[w] = pack_code_word(L, codes, w);
+  if (key && L.qjl) {
+    if (lane < a.m / 32) reinterpret_cast<unsigned*>(base + L.off_signs + slot * (a.m / 8))[lane] = sword;
+    if (lane == 0) reinterpret_cast<unsigned short*>(base + L.off_rnorm)[slot] = r16;
+  }
+  if (lane == 0) reinterpret_cast<unsigned short*>(base + L.off_norm)[slot] = __half_as_ushort(n16);
+}
+
+__global__ void __launch_bounds__(32 * kAppWarps, 1) append_kernel(QuantizeArgs ka, QuantizeArgs va, int nbk) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float* pit = reinterpret_cast<float*>(smem_raw);
+  float* st = pit + 128 * 128;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool key = static_cast<int>(blockIdx.x) < nbk;
+  const QuantizeArgs& a = key ? ka : va;
+  const bool qjl = key && a.lay.qjl;
+  pdl_trigger();                       // the query prep may start now (it waits for this grid before it ends)
+  // the matrices: every 16-byte copy of the CTA in flight at once
+  {
+    const uint32_t pit_s = static_cast<uint32_t>(__cvta_generic_to_shared(pit));
+    const uint32_t st_s = static_cast<uint32_t>(__cvta_generic_to_shared(st));
+    for (int v = tid; v < 128 * 128 / 4; v += 32 * kAppWarps)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(pit_s + 16 * v), "l"(a.tab.pit + 4 * v) : "memory");
+    if (qjl) {
+      // S^T with rows of m projections, as [128][128] (projections >= m zero-filled)
+      for (int v = tid; v < 128 * 128 / 4; v += 32 * kAppWarps) {
+        const int j = v >> 5, c = 4 * (v & 31);
+        const float* src = a.tab.st + j * a.m + (c < a.m ? c : 0);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(st_s + 16 * v), "l"(src),
+                     "r"(c < a.m ? 16 : 0) : "memory");
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  }
+  __syncthreads();
+  const long long nvec = static_cast<long long>(a.batch) * a.n_new * a.H;
+  const long long gv = static_cast<long long>(key ? blockIdx.x : blockIdx.x - nbk) * kAppWarps + warp;
+  if (gv < nvec)
+    append_vector(a, key, gv, pit, st, smem_raw + 2 * 128 * 128 * 4 + warp * kAppScratch, lane);
+}
+
+}  // namespace
+
+// Supported: d = 128, m a multiple of 32 (at most 128), 16-byte aligned inputs;
+// at most 2^16 CTAs.  False: the caller takes another quantize kernel.
+cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s) { return launch_quantize_impl(a, s); }
+
+bool launch_append(const QuantizeArgs& k, const QuantizeArgs& v, cudaStream_t s, cudaError_t* err) {
+  const QuantizeArgs& a0 = k.x ? k : v;
+  if (!k.x && !v.x) return false;
+  if (k.x && k.lay.qjl && (k.m % 32 || k.m > 128 || k.m < 32)) return false;
+  const long long nvec = static_cast<long long>(a0.batch) * a0.n_new * a0.H;
+  const long long nb = (nvec + kAppWarps - 1) / kAppWarps;
+  const long long nbk = k.x ? nb : 0, nbv = v.x ? nb : 0;
+  if (nbk + nbv > 65535) return false;
+  static std::atomic<unsigned long long> configured{0};
+  cudaError_t e = smem_attr_once(append_kernel, kAppSmem, configured);
+  if (e == cudaSuccess) {
+    append_kernel<<<static_cast<unsigned>(nbk + nbv), 32 * kAppWarps, kAppSmem, s>>>(k, v, static_cast<int>(nbk));
+    e = cudaGetLastError();
+  }
+  *err = e;
+  return true;
 }
 
 }  // namespace tq

@@ -260,9 +260,10 @@ def test_append_decode_equals_separate_calls(scale):
     finally:
         tq.tq_destroy(ctx)
     assert np.array_equal(caches[0][0], caches[1][0]) and np.array_equal(caches[0][1], caches[1][1])
-    # the fused step scores the new token in the merge (fp32) rather than in the partials kernel (fp16 operands)
+    # the same kernels over the same bytes and chunks: the fused step's chaining (the query prep ends only
+    # after the append) changes no result
     assert np.all(np.isfinite(outs[0]))
-    assert th.rel_err(outs[0], outs[1]).max() <= th.ATT_TOL
+    assert np.array_equal(outs[0], outs[1])
 
 
 def test_decode_chunk_choice():
@@ -285,8 +286,8 @@ def test_decode_chunk_choice():
 
 
 def test_decode_many_rows_use_the_warp_merge():
-    """1,280 query rows (B = 40, 32/8 heads): the merge runs a warp per row with Pi staged in shared memory
-    (batches of 1,024 rows and more); lengths 0..47, chunks of 16 so that rows merge several chunks."""
+    """1,280 query rows (B = 40, 32/8 heads); lengths 0..47 and chunks of 16, so that rows merge up to three
+    chunks (one warp per row in the merge, Pi staged in shared memory)."""
     rng = np.random.default_rng(31)
     lens = rng.integers(0, 48, size=40)
     lens[3] = 0
@@ -294,10 +295,17 @@ def test_decode_many_rows_use_the_warp_merge():
     _check(w, lens, 32, 8, chunk=16, seed=5)
 
 
+def test_decode_merge_many_chunks():
+    """Up to 69 chunks per row (lengths 1,100 / 700 / 5, chunks of 16): the merge gives a row eight warps, each
+    merging two batches of chunks, and the row maximum and weight sum run over chunks past the first 32."""
+    w = BASE.scaled(k_bits=(3, 3), v_bits=(3, 3), dtype="bf16")
+    _check(w, [1100, 700, 5], 8, 2, chunk=16, seed=12)
+
+
 def test_append_decode_many_rows_against_the_oracle():
-    """The fused step at 1,024 query rows (B = 64, 16/4 heads): the warp-per-row merge scores the new token from
-    its stored record.  The oracle quantizes the cached tokens; the library appends the new one; the oracle then
-    decodes over all L + 1 from the bytes the library holds."""
+    """The fused step at 1,024 query rows (B = 64, 16/4 heads): the append kernel writes the new token, the
+    partials kernel covers all L + 1 positions.  The oracle quantizes the cached tokens; the library appends the
+    new one; the oracle then decodes over all L + 1 from the bytes the library holds."""
     import torch
     w = BASE.scaled(k_bits=(3, 3), v_bits=(3, 3), dtype="bf16")
     rng = np.random.default_rng(41)
