@@ -20,6 +20,7 @@
 // ones exact arithmetic gives, except for values within ~1e-13 of a boundary.
 
 #include "tq_internal.h"
+#include "tq_tc.cuh"
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -448,29 +449,70 @@ cudaError_t launch_quantize_impl(const QuantizeArgs& a, cudaStream_t s) {
 // sequence and KV head): one warp per vector, four vectors per CTA (each warp
 // reads all of Pi^T from shared memory: few warps per SM keep that short), K
 // and V vectors in one launch (CTAs [0, nbk) keys, the rest values).  Pi^T
-// (and for keys S^T) are staged once per CTA by asynchronous 16-byte copies,
-// all in flight at once; the fast
-// path is the tile kernel's above, vector by vector: y = Pi x summed over k in
-// order (fp32), the same code and sign guards, the same packing.  A decision
-// inside a guard is retaken in fp64 by the whole warp, one decision at a time
-// (a lane takes four of the 128 terms, so each costs one round of loads):
-// a code from y_j = Pi_j x, a sign bit from z_p = (S Pi)_p x - fp16(||x||) /
-// sqrt(d) S_p c^ (the product S Pi as a double-float table, the codes as
-// decided).  The residual norm stays the fp32 one.  Lane l holds channels
-// (projections) 4 l .. 4 l + 3.
+// (and for keys S^T) are staged once per CTA by two bulk copies while the warps
+// load their vectors and norms.  The fast path is the tile kernel's above,
+// vector by vector: y = Pi x summed over k in order (fp32), the same code and
+// sign guards; the stored format of tq.h is built by OR-ing each code field
+// into its word in shared memory.  A decision inside a guard is retaken in
+// fp64 by the whole warp, one decision at a time (a lane takes four of the 128
+// terms, so each costs one round of loads): a code from y_j = Pi_j x, a sign
+// bit from z_p = (S Pi)_p x - fp16(||x||) / sqrt(d) S_p c^ (the product S Pi as
+// a double-float table, the codes as decided).  The residual norm stays the
+// fp32 one.  Lane l holds channels (projections) 4 l .. 4 l + 3.
 constexpr int kAppWarps = 4;
-constexpr int kAppScratch = 128 * 4 + 128 * 4 + 128;   // x, r, codes per warp
+constexpr int kAppScratch = 128 * 4 + 128 * 4 + 16 * 4;   // x, r, packed code words per warp
 constexpr int kAppSmem = 2 * 128 * 128 * 4 + kAppWarps * kAppScratch;
 
-__device__ void append_vector(const QuantizeArgs& a, bool key, long long gv, const float* pit, const float* st,
-                              unsigned char* scratch, int lane) {
+// The kind's two codebooks, copied to shared memory once per CTA (boundaries
+// past 2^b - 1 are +inf, as in GroupBook).
+struct AppBook {
+  float t[2][16];
+  float c[2][16];
+  double t64[2][16];
+  double c64[2][16];
+};
+
+// Bit position of channel j's code field in the vector's code stream, the
+// stored field value, and for 3-bit channels 6 and 7 of an octet the three
+// single bits (see the stored format): fields never straddle a 32-bit word.
+__device__ __forceinline__ void or_code(uint32_t* pw, const KindLayout& L, int bits0, int bits1, int j, int code) {
+  const int g = j < L.split ? 0 : 1;
+  const int b = g ? bits1 : bits0;
+  const int cj = g ? j - L.split : j;
+  const int base = g ? L.split * bits0 : 0;
+  if (b == 3) {
+    const int ob = base + 24 * (cj >> 3), i = cj & 7;
+    if (i < 6) {
+      const int pos = ob + 4 * i;
+      atomicOr(pw + (pos >> 5), static_cast<uint32_t>(code) << (pos & 31));
+    } else {
+      const int s0 = ob + (i == 6 ? 3 : 7);
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        const int pos = s0 + 8 * q;
+        atomicOr(pw + (pos >> 5), static_cast<uint32_t>((code >> q) & 1) << (pos & 31));
+      }
+    }
+  } else {
+    const uint32_t v = b == 4 ? stored4(static_cast<unsigned>(code)) : static_cast<uint32_t>(code);
+    const int pos = base + b * cj;
+    atomicOr(pw + (pos >> 5), v << (pos & 31));
+  }
+}
+
+// Returns false when a wait for the staged matrices gave up (nothing stored).
+__device__ bool append_vector(const QuantizeArgs& a, bool key, long long gv, uint32_t pit_s, uint32_t st_s,
+                              const AppBook& bk, unsigned char* scratch, int lane, uint32_t bar_pi, uint32_t bar_s) {
   const KindLayout& L = a.lay;
   float* xs = reinterpret_cast<float*>(scratch);
   float* rs = xs + 128;
-  unsigned char* codes = reinterpret_cast<unsigned char*>(rs + 128);
+  uint32_t* pw = reinterpret_cast<uint32_t*>(rs + 128);
+  const uint32_t xs_s = tcx::su32(xs), rs_s = tcx::su32(rs);
   const float inv_sqrt_d = 0.08838834764831845f;
   const double inv_sqrt_d64 = 1.0 / sqrt(128.0);
   const double sqrt_d64 = sqrt(128.0);
+  const int g = 4 * lane < L.split ? 0 : 1;     // the group of this lane's four channels (split % 8 == 0)
+  const int bits0 = L.g[0].bits, bits1 = L.g[1].bits;
   // 1. x and its double-float squared norm
   float xv[4];
   if (a.f32) {
@@ -482,6 +524,7 @@ __device__ void append_vector(const QuantizeArgs& a, bool key, long long gv, con
     xv[2] = __uint_as_float(x2.y << 16), xv[3] = __uint_as_float(x2.y & 0xFFFF0000u);
   }
   *reinterpret_cast<float4*>(xs + 4 * lane) = make_float4(xv[0], xv[1], xv[2], xv[3]);
+  if (lane < 16) pw[lane] = 0u;
   float sh = 0.0f, sl = 0.0f;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -507,37 +550,41 @@ __device__ void append_vector(const QuantizeArgs& a, bool key, long long gv, con
   const __half n16 = df_to_half(nh, nl);
   const float n16f = __half2float(n16);
   __syncwarp();
+  bool failed = false;
+  if (!__all_sync(0xffffffffu, tcx::bar_wait(bar_pi, 0, failed))) return false;   // Pi^T staged
   // 2. y = Pi x for outputs 4 lane .. 4 lane + 3
   float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
+#pragma unroll 16
   for (int k = 0; k < 128; ++k) {
-    const float4 p = *reinterpret_cast<const float4*>(pit + k * 128 + 4 * lane);
-    const float xk = xs[k];
-    y[0] = fmaf(p.x, xk, y[0]);
-    y[1] = fmaf(p.y, xk, y[1]);
-    y[2] = fmaf(p.z, xk, y[2]);
-    y[3] = fmaf(p.w, xk, y[3]);
+    const uint4 p = tcx::lds128(pit_s + 512 * k + 16 * lane);
+    const float xk = tcx::ldsf(xs_s + 4 * k);
+    y[0] = fmaf(__uint_as_float(p.x), xk, y[0]);
+    y[1] = fmaf(__uint_as_float(p.y), xk, y[1]);
+    y[2] = fmaf(__uint_as_float(p.z), xk, y[2]);
+    y[3] = fmaf(__uint_as_float(p.w), xk, y[3]);
   }
-  // 3. codes (fp64 re-decision near a boundary); keys: the residual
-  float rpart = 0.0f;
-  unsigned cw = 0;
-  int code4[4];
+  // 3. codes against the 15 boundary slots (+inf past 2^b - 1), the guarded ones
+  // re-decided in fp64 by the whole warp; keys: the residual
+  int code4[4] = {0, 0, 0, 0};
   unsigned guarded = 0;          // bit oi: channel 4 lane + oi within the code guard
+  {
+    float mind[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
+    float u[4];
 #pragma unroll
-  for (int oi = 0; oi < 4; ++oi) {
-    const int i = 4 * lane + oi;
-    const GroupBook& gb = L.g[i < L.split ? 0 : 1];
-    const float u = y[oi] * scale;
-    int code = 0;
-    float mind = INFINITY;
-    for (int k = 0; k < gb.nb; ++k) {
-      code += u >= gb.t[k];
-      mind = fminf(mind, fabsf(u - gb.t[k]));
+    for (int oi = 0; oi < 4; ++oi) u[oi] = y[oi] * scale;
+#pragma unroll
+    for (int k = 0; k < 15; ++k) {
+      const float t = bk.t[g][k];
+#pragma unroll
+      for (int oi = 0; oi < 4; ++oi) {
+        code4[oi] += u[oi] >= t;
+        mind[oi] = fminf(mind[oi], fabsf(u[oi] - t));
+      }
     }
-    code4[oi] = code;
-    if (mind < kCodeGuard) guarded |= 1u << oi;
+#pragma unroll
+    for (int oi = 0; oi < 4; ++oi)
+      if (mind[oi] < kCodeGuard) guarded |= 1u << oi;
   }
-  // the guarded codes in fp64, the warp together on each
   const double n64 = static_cast<double>(nh) + static_cast<double>(nl);
 #pragma unroll
   for (int oi = 0; oi < 4; ++oi) {
@@ -548,33 +595,30 @@ __device__ void append_vector(const QuantizeArgs& a, bool key, long long gv, con
       const int i = 4 * src + oi;
       const double2 p0 = *reinterpret_cast<const double2*>(a.tab.pi64 + i * 128 + 4 * lane);
       const double2 p1 = *reinterpret_cast<const double2*>(a.tab.pi64 + i * 128 + 4 * lane + 2);
-      double y64 = fma(p0.x, static_cast<double>(xs[4 * lane]), fma(p0.y, static_cast<double>(xs[4 * lane + 1]),
-                   fma(p1.x, static_cast<double>(xs[4 * lane + 2]), p1.y * static_cast<double>(xs[4 * lane + 3]))));
+      double y64 = fma(p0.x, static_cast<double>(xv[0]), fma(p0.y, static_cast<double>(xv[1]),
+                   fma(p1.x, static_cast<double>(xv[2]), p1.y * static_cast<double>(xv[3]))));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) y64 += __shfl_xor_sync(0xffffffffu, y64, o);
       if (lane == src) {
-        const GroupBook& gb = L.g[i < L.split ? 0 : 1];
         const double u64 = n64 > 0.0 ? sqrt_d64 * y64 / n64 : 0.0;
         int code = 0;
-        for (int k = 0; k < gb.nb; ++k) code += u64 >= gb.t64[k];
+#pragma unroll
+        for (int k = 0; k < 15; ++k) code += u64 >= bk.t64[g][k];
         code4[oi] = code;
         atomicAdd(&a.tab.counters[0], 1ULL);
       }
     }
   }
+  float rpart = 0.0f;
 #pragma unroll
   for (int oi = 0; oi < 4; ++oi) {
-    const int i = 4 * lane + oi;
-    const GroupBook& gb = L.g[i < L.split ? 0 : 1];
-    const int code = code4[oi];
-    cw |= static_cast<unsigned>(code) << (8 * oi);
+    or_code(pw, L, bits0, bits1, 4 * lane + oi, code4[oi]);
     if (key) {
-      const float r = fmaf(-n16f * inv_sqrt_d, gb.c[code], y[oi]);
-      rs[i] = r;
+      const float r = fmaf(-n16f * inv_sqrt_d, bk.c[g][code4[oi]], y[oi]);
+      rs[4 * lane + oi] = r;
       rpart = fmaf(r, r, rpart);
     }
   }
-  *reinterpret_cast<unsigned*>(codes + 4 * lane) = cw;
   unsigned sword = 0;          // lanes 0 .. m/32 - 1: sign word `lane`
   bool refine = false;
   float rho2 = 0.0f;
@@ -583,16 +627,18 @@ __device__ void append_vector(const QuantizeArgs& a, bool key, long long gv, con
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) rho2 += __shfl_xor_sync(0xffffffffu, rho2, o);
     __syncwarp();
-    // 4. z = S r for projections 4 lane .. 4 lane + 3
+    if (!__all_sync(0xffffffffu, tcx::bar_wait(bar_s, 0, failed))) return false;   // S^T staged
+    // 4. z = S r for projections 4 lane .. 4 lane + 3 (S^T rows of m; lanes past m idle)
     float z[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
+    const uint32_t sa = st_s + 16 * (4 * lane < a.m ? lane : 0);
+#pragma unroll 16
     for (int j = 0; j < 128; ++j) {
-      const float4 s4 = *reinterpret_cast<const float4*>(st + j * 128 + 4 * lane);
-      const float rj = rs[j];
-      z[0] = fmaf(s4.x, rj, z[0]);
-      z[1] = fmaf(s4.y, rj, z[1]);
-      z[2] = fmaf(s4.z, rj, z[2]);
-      z[3] = fmaf(s4.w, rj, z[3]);
+      const uint4 s4 = tcx::lds128(sa + 4 * a.m * j);
+      const float rj = tcx::ldsf(rs_s + 4 * j);
+      z[0] = fmaf(__uint_as_float(s4.x), rj, z[0]);
+      z[1] = fmaf(__uint_as_float(s4.y), rj, z[1]);
+      z[2] = fmaf(__uint_as_float(s4.z), rj, z[2]);
+      z[3] = fmaf(__uint_as_float(s4.w), rj, z[3]);
     }
     const float guard = kSignGuard * sqrtf(rho2);
     unsigned nib = 0, near = 0;
@@ -610,13 +656,9 @@ __device__ void append_vector(const QuantizeArgs& a, bool key, long long gv, con
     // the guarded sign bits in fp64: z_p = (S Pi)_p x - n16 / sqrt(d) S_p c^, the warp together on each;
     // lane l's terms are channels 4 l .. 4 l + 3 (their codes are this lane's)
     const double ns = static_cast<double>(n16f) * inv_sqrt_d64;
-    double cx[4], xd[4];
+    double cx[4];
 #pragma unroll
-    for (int oi = 0; oi < 4; ++oi) {
-      const int j = 4 * lane + oi;
-      cx[oi] = ns * L.g[j < L.split ? 0 : 1].c64[code4[oi]];
-      xd[oi] = static_cast<double>(xs[j]);
-    }
+    for (int oi = 0; oi < 4; ++oi) cx[oi] = ns * bk.c64[g][code4[oi]];
 #pragma unroll
     for (int oi = 0; oi < 4; ++oi) {
       unsigned todo = __ballot_sync(0xffffffffu, (near >> oi) & 1u);
@@ -629,10 +671,10 @@ __device__ void append_vector(const QuantizeArgs& a, bool key, long long gv, con
         const float4 a1 = *reinterpret_cast<const float4*>(a.tab.a_df + (pj * 128 + 4 * lane) * 2 + 4);
         const double2 s0 = *reinterpret_cast<const double2*>(a.tab.s64 + pj * 128 + 4 * lane);
         const double2 s1 = *reinterpret_cast<const double2*>(a.tab.s64 + pj * 128 + 4 * lane + 2);
-        double zz = fma(static_cast<double>(a0.x) + static_cast<double>(a0.y), xd[0], -s0.x * cx[0]);
-        zz += fma(static_cast<double>(a0.z) + static_cast<double>(a0.w), xd[1], -s0.y * cx[1]);
-        zz += fma(static_cast<double>(a1.x) + static_cast<double>(a1.y), xd[2], -s1.x * cx[2]);
-        zz += fma(static_cast<double>(a1.z) + static_cast<double>(a1.w), xd[3], -s1.y * cx[3]);
+        double zz = fma(static_cast<double>(a0.x) + static_cast<double>(a0.y), static_cast<double>(xv[0]), -s0.x * cx[0]);
+        zz += fma(static_cast<double>(a0.z) + static_cast<double>(a0.w), static_cast<double>(xv[1]), -s0.y * cx[1]);
+        zz += fma(static_cast<double>(a1.x) + static_cast<double>(a1.y), static_cast<double>(xv[2]), -s1.x * cx[2]);
+        zz += fma(static_cast<double>(a1.z) + static_cast<double>(a1.w), static_cast<double>(xv[3]), -s1.y * cx[3]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
         if (lane == (pj >> 5)) sword = (sword & ~(1u << (pj & 31))) | ((zz >= 0.0 ? 1u : 0u) << (pj & 31));
@@ -654,26 +696,27 @@ __device__ void append_vector(const QuantizeArgs& a, bool key, long long gv, con
   const int blk = pos >> 4;
   if (pos < 0 || blk >= a.maxp) {
     if (lane == 0) atomicOr(a.tab.err, kErrBlock);
-    return;
+    return true;
   }
   const int page = a.block_table[static_cast<long long>(b) * a.maxp + blk];
   if (page < 0 || page >= a.num_pages) {
     if (lane == 0) atomicOr(a.tab.err, kErrPage);
-    return;
+    return true;
   }
   const int slot = pos & 15;
   unsigned char* base = a.cache + static_cast<long long>(page) * a.page_bytes + static_cast<long long>(h) * L.block_bytes;
-  for (int w = lane; w < L.code_bytes / 4; w += 32)
-    reinterpret_cast<unsigned*>(base + slot * L.code_bytes)[w] = pack_code_word(L, codes, w);
+  if (lane < L.code_bytes / 4) reinterpret_cast<unsigned*>(base + slot * L.code_bytes)[lane] = pw[lane];
   if (key && L.qjl) {
     if (lane < a.m / 32) reinterpret_cast<unsigned*>(base + L.off_signs + slot * (a.m / 8))[lane] = sword;
     if (lane == 0) reinterpret_cast<unsigned short*>(base + L.off_rnorm)[slot] = r16;
   }
   if (lane == 0) reinterpret_cast<unsigned short*>(base + L.off_norm)[slot] = __half_as_ushort(n16);
+  return true;
 }
 
 __global__ void __launch_bounds__(32 * kAppWarps, 1) append_kernel(QuantizeArgs ka, QuantizeArgs va, int nbk) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ AppBook bk;
   float* pit = reinterpret_cast<float*>(smem_raw);
   float* st = pit + 128 * 128;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -681,40 +724,60 @@ __global__ void __launch_bounds__(32 * kAppWarps, 1) append_kernel(QuantizeArgs 
   const QuantizeArgs& a = key ? ka : va;
   const bool qjl = key && a.lay.qjl;
   pdl_trigger();                       // the query prep may start now (it waits for this grid before it ends)
-  // the matrices: every 16-byte copy of the CTA in flight at once
-  {
-    const uint32_t pit_s = static_cast<uint32_t>(__cvta_generic_to_shared(pit));
-    const uint32_t st_s = static_cast<uint32_t>(__cvta_generic_to_shared(st));
-    for (int v = tid; v < 128 * 128 / 4; v += 32 * kAppWarps)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(pit_s + 16 * v), "l"(a.tab.pit + 4 * v) : "memory");
+  // the matrices, two bulk copies (Pi^T, and S^T for keys with QJL) on their own
+  // barriers: each warp takes x and its norm meanwhile, and waits for S^T only
+  // when it gets to z
+  __shared__ __align__(8) unsigned long long bars[2];
+  const uint32_t bar_pi = tcx::su32(&bars[0]), bar_s = tcx::su32(&bars[1]);
+  if (tid == 0) {
+    tcx::bar_init(bar_pi, 1);
+    tcx::bar_init(bar_s, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tcx::bar_arrive_tx(bar_pi, 128 * 128 * 4);
+    tcx::g2s(tcx::su32(pit), a.tab.pit, 128 * 128 * 4, bar_pi);
     if (qjl) {
-      // S^T with rows of m projections, as [128][128] (projections >= m zero-filled)
-      for (int v = tid; v < 128 * 128 / 4; v += 32 * kAppWarps) {
-        const int j = v >> 5, c = 4 * (v & 31);
-        const float* src = a.tab.st + j * a.m + (c < a.m ? c : 0);
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(st_s + 16 * v), "l"(src),
-                     "r"(c < a.m ? 16 : 0) : "memory");
-      }
+      tcx::bar_arrive_tx(bar_s, 128 * a.m * 4);
+      tcx::g2s(tcx::su32(st), a.tab.st, 128 * a.m * 4, bar_s);
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
+  }
+  // the codebooks (boundaries past 2^b - 1 are +inf)
+  for (int i = tid; i < 2 * 16; i += 32 * kAppWarps) {
+    const int gi = i >> 4, k = i & 15;
+    const GroupBook& gb = a.lay.g[gi];
+    bk.t[gi][k] = k < gb.nb ? gb.t[k] : INFINITY;
+    bk.t64[gi][k] = k < gb.nb ? gb.t64[k] : static_cast<double>(INFINITY);
+    bk.c[gi][k] = gb.c[k];
+    bk.c64[gi][k] = gb.c64[k];
   }
   __syncthreads();
   const long long nvec = static_cast<long long>(a.batch) * a.n_new * a.H;
   const long long gv = static_cast<long long>(key ? blockIdx.x : blockIdx.x - nbk) * kAppWarps + warp;
+  bool ok = true;
   if (gv < nvec)
-    append_vector(a, key, gv, pit, st, smem_raw + 2 * 128 * 128 * 4 + warp * kAppScratch, lane);
+    ok = append_vector(a, key, gv, tcx::su32(pit), tcx::su32(st), bk, smem_raw + 2 * 128 * 128 * 4 + warp * kAppScratch,
+                       lane, bar_pi, bar_s);
+  if (!ok && lane == 0) atomicOr(a.tab.err, kErrTimeout);
+  // the CTA ends only after its copies have landed (warps without a vector, or
+  // a wait that gave up, may not have seen them)
+  __syncthreads();
+  if (tid == 0) {
+    bool f = false;
+    (void)tcx::bar_wait(bar_pi, 0, f);
+    if (qjl) (void)tcx::bar_wait(bar_s, 0, f);
+  }
 }
 
 }  // namespace
 
-// Supported: d = 128, m a multiple of 32 (at most 128), 16-byte aligned inputs;
-// at most 2^16 CTAs.  False: the caller takes another quantize kernel.
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s) { return launch_quantize_impl(a, s); }
 
+// Supported: d = 128, m a multiple of 32 (at most 128), 16-byte aligned inputs;
+// at most 2^16 CTAs.  False: the caller takes another quantize kernel.
 bool launch_append(const QuantizeArgs& k, const QuantizeArgs& v, cudaStream_t s, cudaError_t* err) {
   const QuantizeArgs& a0 = k.x ? k : v;
   if (!k.x && !v.x) return false;
   if (k.x && k.lay.qjl && (k.m % 32 || k.m > 128 || k.m < 32)) return false;
+  if ((k.x && k.lay.split % 8) || (v.x && v.lay.split % 8)) return false;   // a lane's channels in one group
   const long long nvec = static_cast<long long>(a0.batch) * a0.n_new * a0.H;
   const long long nb = (nvec + kAppWarps - 1) / kAppWarps;
   const long long nbk = k.x ? nb : 0, nbv = v.x ? nb : 0;
