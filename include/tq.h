@@ -104,8 +104,7 @@ tq_status tq_config_init(tq_config* cfg, int d, int b, int m, uint64_t seed);
  * streams 1 and 2 of `seed`, and the Lloyd-Max codebooks for cfg->codebook's
  * density (tq_create: Gaussian).  The only call
  * that allocates device memory (about 0.5 MB) and the only one that copies
- * host to device; it also creates the second stream and the two events of the
- * fused decode step (tq_append_decode), so no later call creates anything.
+ * host to device; no later call creates anything (streams, events, memory).
  * `*out` receives the context; free it with tq_destroy. */
 tq_status tq_create(int d, int b, int m, uint64_t seed, tq_ctx** out);
 tq_status tq_create_ex(const tq_config* cfg, tq_ctx** out);
@@ -154,8 +153,8 @@ tq_status tq_workspace_size(const tq_ctx* ctx, int batch, int num_q_heads,
  * sequences are shorter) that balances the work of the partials kernel over
  * the GPU.  Passing 0 as chunk_tokens to the decode calls assumes every
  * sequence has max_seq_len tokens; with very unequal lengths this call gives
- * a better split.  fused_append = 1 sizes it for tq_append_decode, whose
- * partials kernel leaves a few SMs to the new token's quantize-append.  No
+ * a better split.  fused_append is accepted for compatibility and changes
+ * nothing (tq_append_decode's partials kernel has the whole GPU).  No
  * counterpart in the pages (an implementation detail of the split-K decode).
  * Host only, no CUDA work. */
 tq_status tq_decode_chunk(const tq_ctx* ctx, int batch, int num_q_heads, int num_kv_heads,
@@ -246,14 +245,14 @@ tq_status tq_append_decode(const tq_ctx* ctx, const void* k_new, const void* v_n
 
 /* tq_append_decode with two optional CUDA events (cudaEvent_t, may be NULL)
  * recorded on `stream` just before and just after the split-K partials kernel,
- * for timing it inside the fused step.  Execution: the new token's
- * quantize-append runs on a second stream that tq_create made with the
- * context (joined with events; calls sharing a context serialise their
- * host-side enqueue) next to the query prep and the partials kernel, which covers the
- * seq_lens[b] cached tokens and leaves a few SMs to the append; the merge then
- * scores the new token from its stored record and adds it to the log-sum-exp
- * merge.  Results equal tq_quantize + tq_decode_attention over L+1 tokens up
- * to fp32 rounding of the new token's term. */
+ * for timing it inside the fused step (an event between two launches keeps the
+ * second from starting early, so a step with events takes a little longer).
+ * Execution, all on `stream`: the append (a warp per new K/V vector; d = 128
+ * with the channel split a multiple of 8, else the tile quantize kernels),
+ * the query prep launched dependent on it (it overlaps the append and ends
+ * after it), the partials kernel over all seq_lens[b] + 1 positions and the
+ * merge, each launched dependent on the one before.  Results equal
+ * tq_quantize + tq_decode_attention over L+1 tokens bit for bit. */
 tq_status tq_append_decode_ex(const tq_ctx* ctx, const void* k_new, const void* v_new, const void* q,
                               tq_dtype dtype, int batch, int num_q_heads, int num_kv_heads,
                               const int32_t* seq_lens, int max_seq_len,
