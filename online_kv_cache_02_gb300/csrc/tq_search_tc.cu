@@ -15,7 +15,7 @@
 //   score = n16/sqrt(d) S1 + sqrt(pi/2)/m rho16 <u, 2b - 1>,
 // the same fp16 operands the decode's partials kernel multiplies.
 //
-// One persistent CTA per SM, 10 warps:
+// One persistent CTA per SM, 14 warps (10 for 4-bit keys):
 //   warp 0 (one lane): bulk copies of a tile's eight 16-vector key blocks into
 //       a two-stage ring (page ids from the block table; an id out of range is
 //       flagged and its vectors score -inf);
@@ -23,11 +23,15 @@
 //       the MMAs of a tile once its operands are in shared memory;
 //   warps 2-5: thread v builds row v of the two A tiles (fp16, 128-byte
 //       swizzled K-major) from vector v's record, and its two score factors;
-//   warps 6-9: thread v reads row v (its vector) of S1 and S2, writes the 64
-//       scores to a shared tile; then thread 2q + h scans query q's scores of
-//       vectors [64h, 64h + 64) and keeps its 16 best (descending; vectors
-//       arrive in increasing index, so equal scores keep the lower index).
-// search_merge_kernel then takes, per query, the k best of every CTA's lists
+//   warps 6-13: two groups of four, group g taking the tiles of tensor-memory
+//       slot g (every other tile), so one group's scan overlaps the other's
+//       scores (4-bit keys: one group, warps 6-9; its lookup table leaves no
+//       room for a second score tile); in a group, thread v reads row v (its vector) of S1 and S2,
+//       writes the 64 scores to the group's shared tile; then thread 2q + h
+//       scans query q's scores of vectors [64h, 64h + 64) and keeps its 16 best
+//       (descending; a group sees its vectors in increasing index, so equal
+//       scores keep the lower index).
+// search_merge_kernel then takes, per query, the k best of every group's lists
 // (equal scores: lower index), and fills with -inf vectors in index order when
 // fewer than k scores are finite.  With `scores` set the epilogue writes every
 // score instead (the same arithmetic) and keeps no lists.
@@ -50,12 +54,13 @@ using namespace tcx;
 constexpr int kQB = 64;                 // queries per launch (MMA N)
 constexpr int kTV = 128;                // database vectors per tile (MMA M)
 constexpr int kTop = 16;                // list length per epilogue thread
-constexpr int kWarpsS = 10;
-constexpr int kThrS = 32 * kWarpsS;
+constexpr int kWarpsFixed = 6;          // producer, MMA, four operand warps; then 4 or 8 epilogue warps
 constexpr float kInvSqrtDS = 0.08838834764831845f;
 constexpr float kSqrtHalfPiS = 1.2533141373155003f;
 constexpr float kSignC = 255.0f / 1024.0f;
 constexpr int kScoreRow = 136;          // floats per query row of the score tile (bank skew)
+constexpr int kThrStride = 32;          // words between two queries' shared bars
+constexpr int kThrBytes = kQB * kThrStride * 4;
 
 // ---- codes ------------------------------------------------------------------
 __host__ __device__ constexpr int lut_entries_s(int b) { return b == 4 ? 256 : b == 3 ? 120 : 16; }
@@ -88,7 +93,9 @@ struct TcSearchArgs {
   uint32_t* err;
   float2* cand;              // top-k lists of this launch: [gridDim.x][128][kTop] (score, index bits)
   float* scores;             // every score [nq][n_db] instead of lists (null: lists)
-  unsigned* thr;             // [64] per query of this launch: the largest k-th score any list has
+  unsigned* thr;             // [64][kThrStride] per query of this launch (one 128-byte line each, so the
+                             // CTAs' atomics on different queries meet in different L2 slices): the
+                             // largest k-th score any list has
                              // published, as an order-preserving key (0: none yet)
   int k;
 };
@@ -103,14 +110,16 @@ __device__ __forceinline__ float funkey(unsigned u) {
   return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
 }
 
-// Shared memory (offsets from a 1024-aligned base).
+// Shared memory (offsets from a 1024-aligned base); EG epilogue groups, a
+// score tile each.
+template <int EG>
 struct SLayout {
   static constexpr int QH = 0;                       // q~ fp16 [64][128], swizzled
   static constexpr int UH = QH + kQB * 256;          // u fp16 [64][128]
   static constexpr int AK = UH + kQB * 256;          // K^ fp16 [128][128]
   static constexpr int AS = AK + kTV * 256;          // 1 + c b fp16 [128][128]
-  static constexpr int SC = AS + kTV * 256;          // score tile [64][kScoreRow] fp32
-  static constexpr int FAC = SC + kQB * kScoreRow * 4;   // [4][256] fp32 score factors (ring)
+  static constexpr int SC = AS + kTV * 256;          // score tiles [2 groups][64][kScoreRow] fp32
+  static constexpr int FAC = SC + EG * kQB * kScoreRow * 4;   // [4][256] fp32 score factors (ring)
   static constexpr int SU = FAC + 4 * 256 * 4;       // [64] -(2/c + 1) sum(u) per query
   static constexpr int PV = SU + kQB * 4;            // [4] page-valid masks
   static constexpr int BAR = PV + 16;                // mbarriers
@@ -130,19 +139,26 @@ struct SGeo {
   static constexpr int K_RNORM = K_NORM + 32;
   static constexpr int STAGE = 8 * KBB;
   static constexpr int E = lut_entries_s(BH) > lut_entries_s(BL) ? lut_entries_s(BH) : lut_entries_s(BL);
-  // the deepest record ring (4, 3 or 2 stages) that fits; + 1024 alignment slack
-  static constexpr int need(int st) { return ((SLayout::REC + st * STAGE + 1023) & ~1023) + 256 * E + 1024; }
-  static constexpr int S = need(4) <= kSmemCapS ? 4 : need(3) <= kSmemCapS ? 3 : 2;
-  static constexpr int LUT = (SLayout::REC + S * STAGE + 1023) & ~1023;
+  // two epilogue groups when their second score tile fits next to a ring of at
+  // least two record stages (the 4-bit lookup table is too large for it), then
+  // the deepest ring (4, 3 or 2 stages) that fits; + 1024 alignment slack
+  template <int eg>
+  static constexpr int need(int st) { return ((SLayout<eg>::REC + st * STAGE + 1023) & ~1023) + 256 * E + 1024; }
+  static constexpr int EG = need<2>(2) <= kSmemCapS ? 2 : 1;
+  using L = SLayout<EG>;
+  static constexpr int S = need<EG>(4) <= kSmemCapS ? 4 : need<EG>(3) <= kSmemCapS ? 3 : 2;
+  static constexpr int NT = 32 * (kWarpsFixed + 4 * EG);   // threads per CTA
+  static constexpr int LUT = (L::REC + S * STAGE + 1023) & ~1023;
   static constexpr int SMEM = LUT + 256 * E + 1024;
   static_assert(KBB % 16 == 0, "bulk copy unit");
   static_assert(SMEM <= kSmemCapS, "shared memory per block");
 };
 
 template <int BH, int BL, bool QJL>
-__global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
+__global__ void __launch_bounds__(SGeo<BH, BL, QJL>::NT, 1) search_tc_kernel(TcSearchArgs a) {
   using G = SGeo<BH, BL, QJL>;
-  using L = SLayout;
+  using L = typename G::L;
+  constexpr int kThrS = G::NT;
   extern __shared__ __align__(1024) unsigned char sm_raw[];
   unsigned char* sm = sm_raw + ((0u - su32(sm_raw)) & 1023u);
   const uint32_t sb = su32(sm);
@@ -371,10 +387,13 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
     }
   } else {
     // ---- epilogue ---------------------------------------------------------------
+    // G::EG groups of four warps, group eg taking the tiles i = eg, eg + EG, ...
+    // (with two groups, group eg has tensor-memory slot eg)
+    const int eg = (warp - 6) >> 2;
     const int wq = warp & 3, v = 32 * wq + lane;       // tensor-memory lanes 32 wq .. : vector v
-    const int tl = tid - 192;                            // 0 .. 127
+    const int tl = (tid - 192) & 127;                    // 0 .. 127 within the group
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * wq) << 16);
-    const uint32_t sc = sb + L::SC;
+    const uint32_t sc = sb + L::SC + eg * (kQB * kScoreRow * 4);
     const uint32_t su = sb + L::SU;
     float best[kTop];
     int bidx[kTop];
@@ -383,14 +402,14 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
     const int sq = tl >> 1, sh = tl & 1;                 // scan: query sq, vectors [64 sh, 64 sh + 64)
     float kth = -INFINITY;                               // this list's k-th best (its insertion bar)
     unsigned published = 0u;
-    for (int i = 0; i < local; ++i) {
+    for (int i = eg; i < local; i += G::EG) {
       const int slot = i & 1;
       // a wait that gives up leaves this tile's results undefined (the error word
       // says so) but the loop goes on, so the named barriers below are still met
       // the shared bar of this thread's scan query, read early (an L2 round trip)
       unsigned gkey = 0u;
       if (!a.scores)   // volatile: issued here, not sunk to its first use
-        asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(gkey) : "l"(a.thr + sq) : "memory");
+        asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(gkey) : "l"(a.thr + kThrStride * sq) : "memory");
       bool ok = bar_wait(barx(L::kFacFull + (i & 3)), (i >> 2) & 1, failed);
       const uint32_t fac = sb + L::FAC + (i & 3) * 1024;
       const float fa = ldsf(fac + 4 * v), fb = ldsf(fac + 512 + 4 * v);
@@ -426,32 +445,18 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
       __syncwarp();
       if (lane == 0) bar_arrive(barx(L::kTEmpty + slot));
       if (!a.scores) {
-        nsync(1, 128);                                   // the tile's scores are in
+        nsync(1 + eg, 128);                              // the tile's scores are in
         const uint32_t row = sc + 4 * (sq * kScoreRow + 68 * sh);
         const int tb = t0 + 64 * sh;
         // a score below the largest published k-th score of this query cannot be in
         // the answer (that list's k best are candidates); equal ones still can
         const float gt = funkey(gkey);
-        // pass 1 (every lane, no branches): the elements over the bar, as a bit mask
-        const bool use_gt = gt > kth;
-        uint32_t mlo = 0u, mhi = 0u;
-#pragma unroll
-        for (int j = 0; j < 64; j += 4) {
-          const uint4 xu = lds128(row + 4 * j);
-          const float xv[4] = {__uint_as_float(xu.x), __uint_as_float(xu.y), __uint_as_float(xu.z),
-                               __uint_as_float(xu.w)};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t bit = (use_gt ? xv[e] >= gt : xv[e] > kth) ? 1u : 0u;
-            if (j + e < 32) mlo |= bit << (j + e);
-            else mhi |= bit << (j + e - 32);
-          }
-        }
         // while the list is short of k entries: the k-th largest of the 16 group
         // maxima is at most this tile's k-th best (k distinct elements reach it),
-        // so an element below it cannot be among the list's final k
+        // so an element below it cannot be among the list's final k (taken first,
+        // so that pass 1 marks only the elements over it)
         float bar0 = -INFINITY;
-        if (kth == -INFINITY) {                          // (rare: the first tiles) the tile again
+        if (kth == -INFINITY) {                          // (rare: the first tiles) the tile twice
           float gmax[16];
 #pragma unroll
           for (int j = 0; j < 64; j += 4) {
@@ -465,6 +470,39 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
 #pragma unroll
             for (int h = 0; h < 16; ++h) ge += gmax[h] >= gmax[g] ? 1 : 0;
             if (ge >= a.k) bar0 = fmaxf(bar0, gmax[g]);
+          }
+        }
+        // pass 1 (every lane, no branches): the elements over the bar, as a bit mask;
+        // while the list is short, the bar is bar0 (the list's own is -inf then)
+        const bool use_gt = gt > kth;
+        const float bar = use_gt ? gt : kth;
+        uint32_t mlo = 0u, mhi = 0u;
+        if (bar0 > -INFINITY) {
+          const float b0 = fmaxf(bar0, gt);
+#pragma unroll
+          for (int j = 0; j < 64; j += 4) {
+            const uint4 xu = lds128(row + 4 * j);
+            const float xv[4] = {__uint_as_float(xu.x), __uint_as_float(xu.y), __uint_as_float(xu.z),
+                                 __uint_as_float(xu.w)};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t bit = xv[e] >= b0 ? 1u : 0u;
+              if (j + e < 32) mlo |= bit << (j + e);
+              else mhi |= bit << (j + e - 32);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 64; j += 4) {
+            const uint4 xu = lds128(row + 4 * j);
+            const float xv[4] = {__uint_as_float(xu.x), __uint_as_float(xu.y), __uint_as_float(xu.z),
+                                 __uint_as_float(xu.w)};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t bit = (use_gt ? xv[e] >= bar : xv[e] > bar) ? 1u : 0u;
+              if (j + e < 32) mlo |= bit << (j + e);
+              else mhi |= bit << (j + e - 32);
+            }
           }
         }
         // pass 2: the (few) marked elements in index order; the warp loops only as
@@ -493,13 +531,13 @@ __global__ void __launch_bounds__(kThrS, 1) search_tc_kernel(TcSearchArgs a) {
         }
         if (kth > -INFINITY && fkey(kth) > published) {  // share this list's k-th best
           published = fkey(kth);
-          atomicMax(a.thr + sq, published);
+          atomicMax(a.thr + kThrStride * sq, published);
         }
-        nsync(1, 128);                                   // before the next tile's scores
+        nsync(1 + eg, 128);                              // before the next tile's scores
       }
     }
     if (!a.scores) {
-      float2* out = a.cand + (static_cast<long long>(blockIdx.x) * kTV + tl) * kTop;
+      float2* out = a.cand + ((G::EG * static_cast<long long>(blockIdx.x) + eg) * kTV + tl) * kTop;
 #pragma unroll
       for (int j = 0; j < kTop; ++j) out[j] = make_float2(best[j], __int_as_float(bidx[j]));
     }
@@ -517,7 +555,9 @@ __device__ __forceinline__ bool better(float s, int i, float s2, int i2) {
   return s > s2 || (s == s2 && static_cast<unsigned>(i) < static_cast<unsigned>(i2));
 }
 
-constexpr int kMergeBuf = 5120;     // 2 lists x 160 CTAs x 16: every entry, when all tie
+// The merge's buffer holds every entry of every list (when all tie): 2 lists of
+// 16 per query in each of the 2 x grid epilogue groups.
+size_t merge_smem_bytes(int groups) { return sizeof(float2) * 2 * static_cast<size_t>(groups) * kTop; }
 
 // Launched after the scoring kernel of queries q0 .. q0 + gridDim.x - 1, one
 // block of four warps per query.  tau, the largest k-th score over the lists,
@@ -528,11 +568,12 @@ constexpr int kMergeBuf = 5120;     // 2 lists x 160 CTAs x 16: every entry, whe
 constexpr int kMergeThreads = 128;
 __global__ void __launch_bounds__(kMergeThreads) search_merge_kernel(const float2* cand, int grid, int q0, int n_db,
                                                                     int k, float* top_s, int32_t* top_i) {
-  __shared__ float2 buf[kMergeBuf];
+  extern __shared__ float2 buf[];                        // 2 grid kTop entries (grid: epilogue groups)
+  const int kMergeBuf = 2 * grid * kTop;
   __shared__ float wmax[kMergeThreads / 32];
   __shared__ int nbuf;
   const int ql = blockIdx.x, q = q0 + ql, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nl = 2 * grid;                               // list l: thread 2 ql + (l & 1) of CTA l / 2
+  const int nl = 2 * grid;                               // list l: thread 2 ql + (l & 1) of group l / 2
   auto list = [&](int l) {
     return cand + (static_cast<long long>(l >> 1) * kTV + 2 * ql + (l & 1)) * kTop;
   };
@@ -637,6 +678,16 @@ __global__ void __launch_bounds__(kMergeThreads) search_merge_kernel(const float
   }
 }
 
+// The merge kernel's shared memory, set once per device for the largest case
+// (two groups per CTA, one CTA per SM), whichever configuration comes first.
+cudaError_t merge_attr(int grid) {
+  static std::atomic<unsigned long long> configured{0};
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (grid > sms) return cudaErrorInvalidValue;
+  return smem_attr_once(search_merge_kernel, static_cast<int>(merge_smem_bytes(2 * sms)), configured);
+}
+
 // Per 64 queries: the scoring kernel, then (lists) the merge of its lists.
 template <int BH, int BL, bool QJL>
 cudaError_t launch_tc(const TcSearchArgs& base, int grid, int k, float* top_s, int32_t* top_i, cudaStream_t st) {
@@ -644,19 +695,20 @@ cudaError_t launch_tc(const TcSearchArgs& base, int grid, int k, float* top_s, i
   static std::atomic<unsigned long long> configured{0};
   cudaError_t e = smem_attr_once(search_tc_kernel<BH, BL, QJL>, G::SMEM, configured);
   if (e != cudaSuccess) return e;
+  if ((e = merge_attr(grid)) != cudaSuccess) return e;
   for (int q0 = 0; q0 < base.nq; q0 += kQB) {
     TcSearchArgs a = base;
     a.q0 = q0;
     a.k = k;
-    if (q0 > 0 && !a.scores && (e = cudaMemsetAsync(a.thr, 0, kQB * sizeof(unsigned), st)) != cudaSuccess)
+    if (q0 > 0 && !a.scores && (e = cudaMemsetAsync(a.thr, 0, kThrBytes, st)) != cudaSuccess)
       return e;   // (the first block's bars are cleared before the query prep)
-    if ((e = launch_pdl(search_tc_kernel<BH, BL, QJL>, dim3(grid), dim3(kThrS), static_cast<size_t>(G::SMEM), st, a)) !=
+    if ((e = launch_pdl(search_tc_kernel<BH, BL, QJL>, dim3(grid), dim3(G::NT), static_cast<size_t>(G::SMEM), st, a)) !=
         cudaSuccess)
       return e;
     if (!a.scores) {
       const int nql = base.nq - q0 < kQB ? base.nq - q0 : kQB;
-      if ((e = launch_pdl(search_merge_kernel, dim3(nql), dim3(kMergeThreads), size_t{0}, st,
-                          static_cast<const float2*>(a.cand), grid, q0, a.n_db, k, top_s, top_i)) != cudaSuccess)
+      if ((e = launch_pdl(search_merge_kernel, dim3(nql), dim3(kMergeThreads), merge_smem_bytes(G::EG * grid), st,
+                          static_cast<const float2*>(a.cand), G::EG * grid, q0, a.n_db, k, top_s, top_i)) != cudaSuccess)
         return e;
     }
   }
@@ -687,14 +739,14 @@ bool search_tc_supported(const KindLayout& kl, int m, int k_top) {
 size_t search_tc_cand_bytes() {
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  return sizeof(float2) * static_cast<size_t>(sms) * kTV * kTop + 256;   // + the thresholds
+  return sizeof(float2) * 2 * static_cast<size_t>(sms) * kTV * kTop + kThrBytes;   // two groups' lists, the bars
 }
 
 cudaError_t launch_search_tc(const DecodeArgs& qa, const uint8_t* kc, const int32_t* bt, int num_pages, int n_db,
                              int k, float* top_s, int32_t* top_i, float* scores, void* cand, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
   if (!scores) {   // the shared per-query bars of the first 64 queries start at "none"
-    e = cudaMemsetAsync(static_cast<char*>(cand) + search_tc_cand_bytes() - 256, 0, kQB * sizeof(unsigned), st);
+    e = cudaMemsetAsync(static_cast<char*>(cand) + search_tc_cand_bytes() - kThrBytes, 0, kThrBytes, st);
     if (e != cudaSuccess) return e;
   }
   e = launch_decode(qa, TQ_STAGE_QPREP, st);
@@ -712,7 +764,7 @@ cudaError_t launch_search_tc(const DecodeArgs& qa, const uint8_t* kc, const int3
   a.err = qa.tab.err;
   a.cand = scores ? nullptr : static_cast<float2*>(cand);
   a.thr = scores ? nullptr
-                 : reinterpret_cast<unsigned*>(static_cast<char*>(cand) + search_tc_cand_bytes() - 256);
+                 : reinterpret_cast<unsigned*>(static_cast<char*>(cand) + search_tc_cand_bytes() - kThrBytes);
   a.scores = scores;
   const int grid = tc_grid(a.ntiles);
   switch (qa.kl.g[0].bits * 10 + qa.kl.g[1].bits) {
