@@ -31,7 +31,9 @@
 //       scans query q's scores of vectors [64h, 64h + 64) and keeps its 16 best
 //       (descending; a group sees its vectors in increasing index, so equal
 //       scores keep the lower index).
-// search_merge_kernel then takes, per query, the k best of every group's lists
+// With two groups, group 0 merges the pair of lists of each (query, half) at
+// the end.  search_merge_kernel then takes, per query, the k best of every
+// CTA's lists
 // (equal scores: lower index), and fills with -inf vectors in index order when
 // fewer than k scores are finite.  With `scores` set the epilogue writes every
 // score instead (the same arithmetic) and keeps no lists.
@@ -108,6 +110,12 @@ __device__ __forceinline__ unsigned fkey(float f) {
 __device__ __forceinline__ float funkey(unsigned u) {
   if (u == 0u) return -INFINITY;
   return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+
+// (score, index) ranks before (s2, i2): higher score, or equal score and lower
+// index (an empty entry, index -1, last).
+__device__ __forceinline__ bool better(float s, int i, float s2, int i2) {
+  return s > s2 || (s == s2 && static_cast<unsigned>(i) < static_cast<unsigned>(i2));
 }
 
 // Shared memory (offsets from a 1024-aligned base); EG epilogue groups, a
@@ -537,9 +545,31 @@ __global__ void __launch_bounds__(SGeo<BH, BL, QJL>::NT, 1) search_tc_kernel(TcS
       }
     }
     if (!a.scores) {
-      float2* out = a.cand + ((G::EG * static_cast<long long>(blockIdx.x) + eg) * kTV + tl) * kTop;
+      float2* out = a.cand + (static_cast<long long>(blockIdx.x) * kTV + tl) * kTop;
+      if (G::EG == 1) {
 #pragma unroll
-      for (int j = 0; j < kTop; ++j) out[j] = make_float2(best[j], __int_as_float(bidx[j]));
+        for (int j = 0; j < kTop; ++j) out[j] = make_float2(best[j], __int_as_float(bidx[j]));
+      } else {
+        // the two groups' lists of this (query, half) merged into one (the merge
+        // kernel then reads one list per (query, half) and CTA): each group puts
+        // its list in its own score tile, group 0 merges the pair
+        float2* mine = reinterpret_cast<float2*>(sm + L::SC + eg * (kQB * kScoreRow * 4)) + tl * kTop;
+#pragma unroll
+        for (int j = 0; j < kTop; ++j) mine[j] = make_float2(best[j], __int_as_float(bidx[j]));
+        nsync(3, 256);
+        if (eg == 0) {
+          const float2* other = reinterpret_cast<const float2*>(sm + L::SC + kQB * kScoreRow * 4) + tl * kTop;
+          int ia = 0, ib = 0;
+          for (int j = 0; j < kTop; ++j) {
+            const float2 x = mine[ia], y = other[ib];
+            const bool take_a = ib >= kTop ||
+                                (ia < kTop && !better(y.x, __float_as_int(y.y), x.x, __float_as_int(x.y)));
+            out[j] = take_a ? x : y;
+            ia += take_a ? 1 : 0;
+            ib += take_a ? 0 : 1;
+          }
+        }
+      }
     }
   }
   if (failed) atomicOr(a.err, kErrTimeout);
@@ -551,12 +581,9 @@ __global__ void __launch_bounds__(SGeo<BH, BL, QJL>::NT, 1) search_tc_kernel(TcS
 }
 
 // ---- merge: the k best of every CTA's lists, one warp per query ----------------
-__device__ __forceinline__ bool better(float s, int i, float s2, int i2) {
-  return s > s2 || (s == s2 && static_cast<unsigned>(i) < static_cast<unsigned>(i2));
-}
 
 // The merge's buffer holds every entry of every list (when all tie): 2 lists of
-// 16 per query in each of the 2 x grid epilogue groups.
+// 16 per query in each of the grid CTAs (a CTA's two epilogue groups merged).
 size_t merge_smem_bytes(int groups) { return sizeof(float2) * 2 * static_cast<size_t>(groups) * kTop; }
 
 // Launched after the scoring kernel of queries q0 .. q0 + gridDim.x - 1, one
@@ -568,12 +595,12 @@ size_t merge_smem_bytes(int groups) { return sizeof(float2) * 2 * static_cast<si
 constexpr int kMergeThreads = 128;
 __global__ void __launch_bounds__(kMergeThreads) search_merge_kernel(const float2* cand, int grid, int q0, int n_db,
                                                                     int k, float* top_s, int32_t* top_i) {
-  extern __shared__ float2 buf[];                        // 2 grid kTop entries (grid: epilogue groups)
+  extern __shared__ float2 buf[];                        // 2 grid kTop entries
   const int kMergeBuf = 2 * grid * kTop;
   __shared__ float wmax[kMergeThreads / 32];
   __shared__ int nbuf;
   const int ql = blockIdx.x, q = q0 + ql, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nl = 2 * grid;                               // list l: thread 2 ql + (l & 1) of group l / 2
+  const int nl = 2 * grid;                               // list l: thread 2 ql + (l & 1) of CTA l / 2
   auto list = [&](int l) {
     return cand + (static_cast<long long>(l >> 1) * kTV + 2 * ql + (l & 1)) * kTop;
   };
@@ -678,14 +705,14 @@ __global__ void __launch_bounds__(kMergeThreads) search_merge_kernel(const float
   }
 }
 
-// The merge kernel's shared memory, set once per device for the largest case
-// (two groups per CTA, one CTA per SM), whichever configuration comes first.
+// The merge kernel's shared memory, set once per device for the largest grid
+// (one CTA per SM).
 cudaError_t merge_attr(int grid) {
   static std::atomic<unsigned long long> configured{0};
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (grid > sms) return cudaErrorInvalidValue;
-  return smem_attr_once(search_merge_kernel, static_cast<int>(merge_smem_bytes(2 * sms)), configured);
+  return smem_attr_once(search_merge_kernel, static_cast<int>(merge_smem_bytes(sms)), configured);
 }
 
 // Per 64 queries: the scoring kernel, then (lists) the merge of its lists.
@@ -707,8 +734,8 @@ cudaError_t launch_tc(const TcSearchArgs& base, int grid, int k, float* top_s, i
       return e;
     if (!a.scores) {
       const int nql = base.nq - q0 < kQB ? base.nq - q0 : kQB;
-      if ((e = launch_pdl(search_merge_kernel, dim3(nql), dim3(kMergeThreads), merge_smem_bytes(G::EG * grid), st,
-                          static_cast<const float2*>(a.cand), G::EG * grid, q0, a.n_db, k, top_s, top_i)) != cudaSuccess)
+      if ((e = launch_pdl(search_merge_kernel, dim3(nql), dim3(kMergeThreads), merge_smem_bytes(grid), st,
+                          static_cast<const float2*>(a.cand), grid, q0, a.n_db, k, top_s, top_i)) != cudaSuccess)
         return e;
     }
   }
@@ -739,7 +766,7 @@ bool search_tc_supported(const KindLayout& kl, int m, int k_top) {
 size_t search_tc_cand_bytes() {
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  return sizeof(float2) * 2 * static_cast<size_t>(sms) * kTV * kTop + kThrBytes;   // two groups' lists, the bars
+  return sizeof(float2) * static_cast<size_t>(sms) * kTV * kTop + kThrBytes;   // the CTAs' lists, the bars
 }
 
 cudaError_t launch_search_tc(const DecodeArgs& qa, const uint8_t* kc, const int32_t* bt, int num_pages, int n_db,
