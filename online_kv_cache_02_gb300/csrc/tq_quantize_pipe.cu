@@ -1206,8 +1206,9 @@ __global__ void __maxnreg__(96)
         const uint32_t ctab = tabs + kTabCellT + (gofs + grp) * kCells * 4;
         uint32_t cp[4];
         uint32_t dpend[2] = {0u, 0u}, dbase[2] = {0u, 0u};   // codes handed to the fixer
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {               // 16 channels at a time
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {               // 16 channels at a time (rolled: a smaller loop body
+                                                        // for the instruction cache, 2% faster at c2)
           const int cb = ch0 + 16 * hh;
           float v[16];
           tmem_ld16(trow + cb, v);
