@@ -165,8 +165,9 @@ def traffic_for(kernel_file, kernel, workload):
 
 class DecodeBench:
     """One decode workload resident on the GPU.  A step with append (c3-c5) is one tq_append_decode_ex call:
-    quantize-append the new token at position L, decode over L+1; without append (c1) it is the three stages of
-    tq_decode_attention_ex over the cached tokens."""
+    quantize-append the new token at position L, decode over L+1; without append (c1) it is one
+    tq_decode_attention_ex call over the cached tokens (its three stages one by one in the pass that times the
+    partials kernel by events)."""
 
     def __init__(self, w, torch, tq):
         self.w, self.torch, self.tq = w, torch, tq
@@ -263,6 +264,11 @@ class DecodeBench:
                 raise self.tq.TQError("tq_append_decode_ex", st)
             return
         args, sp = self._args[1], self._args[2]
+        if ev is None:                   # the whole decode in one call, as a user makes it
+            st = lib.tq_decode_attention_ex(*args, self.tq.TQ_STAGE_ALL, sp)
+            if st != 0:
+                raise self.tq.TQError("tq_decode_attention_ex", st)
+            return
         for stage in (self.tq.TQ_STAGE_QPREP, self.tq.TQ_STAGE_PARTIALS, self.tq.TQ_STAGE_MERGE):
             if ev is not None and stage == self.tq.TQ_STAGE_PARTIALS:
                 ev[0].record(stream)
@@ -382,8 +388,8 @@ def l2_flusher(torch, bytes_step):
 
 
 def decode_measure(torch, tq, w, stream, steps, warmup, dist, peak, peak_kind, world, profile=False):
-    """One decode workload: `steps` timed steps after `warmup` (CUDA events on the launch stream), the partials
-    kernel timed by events recorded inside every step, then the same steps end to end from pinned host memory."""
+    """One decode workload: `steps` timed steps after `warmup` (CUDA events on the launch stream), the same steps
+    again with the partials kernel bracketed by events, then the same steps end to end from pinned host memory."""
     db = DecodeBench(w, torch, tq)
     ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(steps)]
     for pair in ev:                      # create the CUDA events (the library records them inside the step)
