@@ -426,8 +426,9 @@ __global__ void __launch_bounds__(SGeo<BH, BL, QJL>::NT, 1) search_tc_kernel(TcS
       tc_after();
       const int t0 = tile_of(i) * kTV;
       const bool has = !isnan(fa);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {                      // queries 32h .. 32h + 31
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {                      // queries 32h .. 32h + 31 (rolled, as below: smaller
+                                                         // epilogue code for the instruction cache)
         float s1[32], s2[32];
         tld32(trow + 128u * slot + 32u * h, s1);
         if (QJL) tld32(trow + 128u * slot + 64u + 32u * h, s2);
@@ -472,7 +473,7 @@ __global__ void __launch_bounds__(SGeo<BH, BL, QJL>::NT, 1) search_tc_kernel(TcS
             gmax[j >> 2] = fmaxf(fmaxf(__uint_as_float(xu.x), __uint_as_float(xu.y)),
                                  fmaxf(__uint_as_float(xu.z), __uint_as_float(xu.w)));
           }
-#pragma unroll
+#pragma unroll 1
           for (int g = 0; g < 16; ++g) {
             int ge = 0;
 #pragma unroll
