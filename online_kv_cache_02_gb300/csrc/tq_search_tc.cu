@@ -588,12 +588,12 @@ __global__ void __launch_bounds__(SGeo<BH, BL, QJL>::NT, 1) search_tc_kernel(TcS
 size_t merge_smem_bytes(int groups) { return sizeof(float2) * 2 * static_cast<size_t>(groups) * kTop; }
 
 // Launched after the scoring kernel of queries q0 .. q0 + gridDim.x - 1, one
-// block of four warps per query.  tau, the largest k-th score over the lists,
+// block of sixteen warps per query (a thread loads one whole list at once).  tau, the largest k-th score over the lists,
 // is at most the answer's k-th score (that list's k best are candidates), so
 // only entries >= tau can be in the answer; they are gathered (usually a little
 // over k), then sorted by (score descending, index ascending) -- by warp 0 in
 // registers when 32 or fewer, else by k rounds of selection.
-constexpr int kMergeThreads = 128;
+constexpr int kMergeThreads = 512;   // 16 warps: one or two lists per thread, loads in one round
 __global__ void __launch_bounds__(kMergeThreads) search_merge_kernel(const float2* cand, int grid, int q0, int n_db,
                                                                     int k, float* top_s, int32_t* top_i) {
   extern __shared__ float2 buf[];                        // 2 grid kTop entries
@@ -607,23 +607,7 @@ __global__ void __launch_bounds__(kMergeThreads) search_merge_kernel(const float
   };
   if (tid == 0) nbuf = 0;
   pdl_wait();                                            // the scoring kernel's lists
-  float tau = -INFINITY;
-#pragma unroll 4
-  for (int l = tid; l < nl; l += kMergeThreads) {
-    const float2 e = list(l)[k - 1];
-    if (__float_as_int(e.y) >= 0) tau = fmaxf(tau, e.x);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tau = fmaxf(tau, __shfl_xor_sync(0xffffffffu, tau, o));
-  if (lane == 0) wmax[warp] = tau;
-  __syncthreads();
-  tau = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
-#pragma unroll 2
-  for (int l = tid; l < nl; l += kMergeThreads) {
-    const float4* src = reinterpret_cast<const float4*>(list(l));
-    float4 x[kTop / 2];
-#pragma unroll
-    for (int j = 0; j < kTop / 2; ++j) x[j] = src[j];   // the whole list in one batch of loads
+  auto gather = [&](const float4 (&x)[kTop / 2], float tau) {
 #pragma unroll
     for (int j = 0; j < kTop / 2; ++j) {
       if (__float_as_int(x[j].y) >= 0 && x[j].x >= tau) {
@@ -634,6 +618,50 @@ __global__ void __launch_bounds__(kMergeThreads) search_merge_kernel(const float
         const int at = atomicAdd(&nbuf, 1);
         if (at < kMergeBuf) buf[at] = make_float2(x[j].z, x[j].w);
       }
+    }
+  };
+  auto block_max = [&](float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (lane == 0) wmax[warp] = v;
+    __syncthreads();
+    v = wmax[0];
+#pragma unroll
+    for (int w = 1; w < kMergeThreads / 32; ++w) v = fmaxf(v, wmax[w]);
+    return v;
+  };
+  if (nl <= kMergeThreads) {
+    // one list per thread at most: the whole list in one batch of loads, tau from
+    // the registers, then the entries >= tau
+    float4 x[kTop / 2];
+    float t = -INFINITY;
+    if (tid < nl) {
+      const float4* src = reinterpret_cast<const float4*>(list(tid));
+#pragma unroll
+      for (int j = 0; j < kTop / 2; ++j) x[j] = src[j];
+#pragma unroll
+      for (int j = 0; j < kTop / 2; ++j) {               // entry k - 1: x[(k-1)/2], half (k-1)&1
+        if (2 * j == k - 1 && __float_as_int(x[j].y) >= 0) t = x[j].x;
+        if (2 * j + 1 == k - 1 && __float_as_int(x[j].w) >= 0) t = x[j].z;
+      }
+    }
+    const float tau = block_max(t);
+    if (tid < nl) gather(x, tau);
+  } else {
+    float t = -INFINITY;
+#pragma unroll 4
+    for (int l = tid; l < nl; l += kMergeThreads) {
+      const float2 e = list(l)[k - 1];
+      if (__float_as_int(e.y) >= 0) t = fmaxf(t, e.x);
+    }
+    const float tau = block_max(t);
+#pragma unroll 2
+    for (int l = tid; l < nl; l += kMergeThreads) {
+      const float4* src = reinterpret_cast<const float4*>(list(l));
+      float4 x[kTop / 2];
+#pragma unroll
+      for (int j = 0; j < kTop / 2; ++j) x[j] = src[j];   // the whole list in one batch of loads
+      gather(x, tau);
     }
   }
   __syncthreads();
