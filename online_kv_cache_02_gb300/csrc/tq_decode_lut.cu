@@ -720,8 +720,8 @@ cudaError_t launch_lut_q(const DecodeArgs& a, int items, cudaStream_t s) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   // one CTA per SM (fewer when there are fewer chunks than SMs, or when the
-  // fused decode step leaves SMs to the new token's quantize-append): a warp
-  // without a chunk exits at once, and every SM's copy engines are in use
+  // caller caps the CTAs): a warp without a chunk exits at once, and every
+  // SM's copy engines are in use
   const int cap = a.max_ctas > 0 && a.max_ctas < sms ? a.max_ctas : sms;
   const int grid = items < cap ? (items > 0 ? items : 1) : cap;
   if (a.T > 0)                         // causal (many new tokens): 16 warps

@@ -99,7 +99,7 @@ struct QuantizeArgs {
   int m;
   KindLayout lay;
   DeviceTables tab;
-  int max_ctas;          // 0: up to one CTA per SM; else at most this many (fused decode step)
+  int max_ctas;          // 0: up to one CTA per SM; else at most this many
 };
 
 struct DecodeArgs {
