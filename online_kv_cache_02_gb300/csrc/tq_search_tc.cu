@@ -112,6 +112,14 @@ __device__ __forceinline__ float funkey(unsigned u) {
   return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
 }
 
+// c ? x : y, as a select instruction (opaque to the optimizer).
+__device__ __forceinline__ float select_f(bool c, float x, float y) {
+  float r;
+  asm("{\n .reg .pred p;\n setp.ne.u32 p, %1, 0;\n selp.f32 %0, %2, %3, p;\n}" : "=f"(r)
+      : "r"(static_cast<unsigned>(c)), "f"(x), "f"(y));
+  return r;
+}
+
 // (score, index) ranks before (s2, i2): higher score, or equal score and lower
 // index (an empty entry, index -1, last).
 __device__ __forceinline__ bool better(float s, int i, float s2, int i2) {
@@ -534,9 +542,10 @@ __global__ void __launch_bounds__(SGeo<BH, BL, QJL>::NT, 1) search_tc_kernel(TcS
             bidx[r] = r > p ? bidx[r - 1] : (r == p ? ci : bidx[r]);
           }
           if (p == 0) best[0] = cs, bidx[0] = ci;
+          // the k-th entry by selects the compiler cannot fold into an indexed load
+          // (an index would move the list to local memory)
 #pragma unroll
-          for (int r = 0; r < kTop; ++r)
-            if (r == a.k - 1) kth = best[r];
+          for (int r = 0; r < kTop; ++r) kth = select_f(r == a.k - 1, best[r], kth);
         }
         if (kth > -INFINITY && fkey(kth) > published) {  // share this list's k-th best
           published = fkey(kth);
