@@ -111,3 +111,47 @@ def test_append_decisions_near_boundaries_are_exact():
     got_k, got_v, _, refined = _append(w, kn, kn, lens, H, 4, bt, B)
     assert refined[0] >= 40 and refined[1] >= 40, refined
     _check_records(w, H, bt, lens, kn, kn, got_k, got_v, exact_bands=True)
+
+
+def test_append_bad_page_is_flagged_and_others_written():
+    """The new token of one sequence maps to a page id out of range: the append stores nothing for it and
+    sets the device error word; the other sequences' records are written as the oracle's."""
+    w = wl.WORKLOADS["c3"].scaled(k_bits=(3, 3), v_bits=(3, 3), qjl=True, dtype="bf16")
+    rng = np.random.default_rng(9)
+    B, H, Hq = 6, 2, 4
+    lens = np.array([3, 17, 31, 40, 8, 22], np.int32)
+    pps = 4
+    num_pages = B * pps
+    bt = rng.permutation(num_pages).astype(np.int32).reshape(B, pps)
+    bad = 2
+    bt[bad, lens[bad] // 16] = num_pages + 7           # the page of sequence 2's new token
+    kn = wl.bf16_round(rng.standard_normal((B, 1, H, 128)).astype(np.float32))
+    vn = wl.bf16_round(rng.standard_normal((B, 1, H, 128)).astype(np.float32))
+    Q = wl.bf16_round(rng.standard_normal((B, Hq, 128)).astype(np.float32))
+    ctx = ctx_for(w)
+    try:
+        kc, vc = alloc_caches(ctx, H, num_pages)
+        n = tq.tq_workspace_size(ctx, B, Hq, int(lens.max()) + 1, 0)
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, device="cuda")
+        tq.tq_append_decode(ctx, to_dev(kn).to(torch.bfloat16), to_dev(vn).to(torch.bfloat16),
+                            to_dev(Q).to(torch.bfloat16), tq.TQ_BF16, B, Hq, H, to_dev(lens), int(lens.max()) + 1,
+                            to_dev(bt), pps, num_pages, kc, vc, 0, th.scale_for(), out, ws, n)
+        torch.cuda.synchronize()
+        assert tq.tq_check_device_status(ctx) != 0
+        got_k, got_v = kc.cpu().numpy(), vc.cpu().numpy()
+    finally:
+        tq.tq_destroy(ctx)
+    good = [b for b in range(B) if b != bad]
+    p = th.params_for(w)
+    pages, slots, heads = [], [], []
+    for b in good:
+        pg, sl, hd = seq_locations(bt, b, [int(lens[b])], H)
+        pages.append(pg), slots.append(sl), heads.append(hd)
+    pages, slots, heads = np.concatenate(pages), np.concatenate(slots), np.concatenate(heads)
+    for kind, got, X in (("k", got_k, kn), ("v", got_v, vn)):
+        q = oracle.quantize_vectors(p, X[good].reshape(-1, 128).astype(np.float64), kind)
+        res = th.compare_records(p, kind, got, q, oracle.quantize_exclusions(p, q, kind), pages, slots, heads, H)
+        th.assert_records_ok(res)
+        touched = th.touched_mask(p, kind, got.size, pages, slots, heads, H)
+        assert np.all(got[~touched] == SENTINEL)       # nothing written for the bad page, nor anywhere else
