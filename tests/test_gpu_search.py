@@ -116,10 +116,12 @@ def test_search_tensor_core_bit_widths(kb, qjl):
     _check(w, 1500, 7, 16)
 
 
-def test_search_several_query_blocks():
+@pytest.mark.parametrize("kb", [(4, 3), (3, 3)])
+def test_search_several_query_blocks(kb):
     """130 queries: three blocks of up to 64 on the tensor-core path (the last one ragged), 3000 vectors
-    (24 tiles of 128, the last partial)."""
-    w = wl.Workload("s", "search", 1, 1, 1, 0, k_bits=(4, 3), seed=10)
+    (24 tiles of 128, the last partial); 4/3-bit keys run one epilogue group, 3-bit keys two (each block's
+    shared bars cleared before it)."""
+    w = wl.Workload("s", "search", 1, 1, 1, 0, k_bits=kb, seed=10)
     _check(w, 3000, 130, 16, seed=5)
 
 
